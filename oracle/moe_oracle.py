@@ -1,0 +1,387 @@
+"""fp64 CPU oracle of the quantised routed-MoE layer forward.
+
+TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` may import this module; the library's own path never does, and it
+shares no code with the CUDA sources.
+
+What it computes, step by step, in the pages' order (DeepSeek-V3-style router with
+noaux_tc, routed_scaling_factor and an always-on shared expert: "Show HN: Menjalankan
+GLM 5.2 di komputer lambat", section "Fitur utama yang diimplementasikan"; batch-union
+MoE: same page and section, and "16 Teknik Özellik ve Yazılım Çıkarımları" on the
+Turkish restatement; NVFP4 experts with FP8 scales per 16 elements: "NVIDIA stellt
+neues GLM-5.2 NVFP4 Modell vor", section "Technische Details und Quantisierungsansatz"):
+
+1. logits l = x W_r^T (fp64, on the exactly widened x and W_r);
+2. gate scores s = sigmoid(l);
+3. biased scores b = s + bias; the bias only selects (auxiliary-loss-free balancing);
+4. group score = sum of the two largest b of each contiguous group of E/n_group experts;
+5. keep the topk_group best groups; experts of other groups are excluded (-inf);
+6. ids = the top_k largest b among kept experts; ties go to the lower index, for
+   groups and for experts;
+7. w = s[ids] / sum(s[ids]) * routed_scaling_factor (unbiased s);
+8. batch-union grouping: per expert, the (token, slot) entries that chose it, in
+   ascending token order; entry = token * top_k + slot;
+9. per (token, expert): gu = W_gu x_t; h = SiLU(gu[:I]) * gu[I:]; y = W_d h, with the
+   weights dequantised exactly (int4 code * fp16 scale, or E2M1 code * E4M3 block scale
+   * fp32 tensor scale);
+10. out_t = sum_j w[t, j] y_{t, ids[t, j]} + y_{t, shared}; the shared expert has weight 1.
+
+NVFP4 layers also quantise the activations that feed the routed experts (x before the
+gate/up projection, h before the down projection) to NVFP4 with a per-call tensor scale;
+the codes are decided in fp32 (the precision the kernel decides them in), and the
+dequantised values are then used exactly. The router and a bf16 shared expert read the
+unquantised x.
+
+Readings where the pages are silent are stated at each function. Every function here is
+pinned by ``tests/test_oracle_pins.py`` to something other than itself (brute force,
+closed forms, hand-worked fixtures, format definitions, library routines).
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+# ------------------------------------------------------------------ storage decoders
+
+
+def decode_int4(codes: np.ndarray) -> np.ndarray:
+    """Packed two's-complement int4 -> int64, element 2j from the low nibble of byte j,
+    2j+1 from the high nibble (the packed int4 container of "Fitur utama yang
+    diimplementasikan")."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    lo = (codes & 0x0F).astype(np.int64)
+    hi = (codes >> 4).astype(np.int64)
+    v = np.stack([lo, hi], axis=-1).reshape(*codes.shape[:-1], codes.shape[-1] * 2)
+    return np.where(v >= 8, v - 16, v)
+
+
+def dequant_int4_g32(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """W[n, k] = code[n, k] * scale[n, k // 32], exact in fp64 (dequant-on-use of the
+    packed int4 weights; one fp16 scale per 32 input-dim elements)."""
+    c = decode_int4(codes).astype(np.float64)
+    n, k = c.shape
+    s = np.asarray(scales, dtype=np.float16).astype(np.float64)
+    assert s.shape == (n, k // 32)
+    return (c.reshape(n, k // 32, 32) * s[..., None]).reshape(n, k)
+
+
+def decode_e2m1(nibbles: np.ndarray) -> np.ndarray:
+    """FP4 E2M1 (1 sign, 2 exponent bits with bias 1, 1 mantissa bit; exponent field 0
+    is subnormal with step 0.5) -> fp64."""
+    n = np.asarray(nibbles, dtype=np.int64) & 0xF
+    sign = np.where(n & 8, -1.0, 1.0)
+    e = (n >> 1) & 3
+    m = n & 1
+    mag = np.where(e == 0, 0.5 * m, (1.0 + 0.5 * m) * np.exp2(e - 1.0))
+    return sign * mag
+
+
+def decode_e4m3(bits: np.ndarray) -> np.ndarray:
+    """FP8 E4M3 (bias 7, subnormal step 2^-9, no infinities, S.1111.111 is NaN) -> fp64."""
+    b = np.asarray(bits, dtype=np.int64) & 0xFF
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = b & 7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((b & 0x7F) == 0x7F, np.nan, mag)
+    return sign * mag
+
+
+def dequant_nvfp4(codes: np.ndarray, scales: np.ndarray, tensor_scale) -> np.ndarray:
+    """W[n, k] = e2m1(code[n, k]) * e4m3(scale[n, k // 16]) * tensor_scale, exact in fp64
+    (NVFP4: 4-bit elements, an FP8 scale per 16 elements, one fp32 scale per tensor)."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    nib = np.stack([codes & 0x0F, codes >> 4], axis=-1).reshape(codes.shape[0], -1)
+    c = decode_e2m1(nib)
+    n, k = c.shape
+    sb = decode_e4m3(scales)
+    assert sb.shape == (n, k // 16)
+    return (c.reshape(n, k // 16, 16) * sb[..., None]).reshape(n, k) * float(np.float32(tensor_scale))
+
+
+def widen_bf16(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> fp64 (exact)."""
+    u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+# ----------------------------------------------------- NVFP4 activation quantiser
+
+
+_E2M1_MAGS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _e4m3_mags() -> np.ndarray:
+    return np.array([decode_e4m3(np.array([c]))[0] for c in range(0x7F)])
+
+
+_E4M3_MAGS = _e4m3_mags()
+
+
+def _rne_code(mag: np.ndarray, table: np.ndarray) -> np.ndarray:
+    """Index into ``table`` (ascending magnitudes, index parity = mantissa parity) of the
+    value nearest to ``mag``; halfway cases take the even index; saturates at the top."""
+    mag = np.asarray(mag, dtype=np.float64)
+    j = np.clip(np.searchsorted(table, mag, side="right") - 1, 0, len(table) - 2)
+    below = mag - table[j]          # table[j] <= mag < table[j + 1] inside the range
+    above = table[j + 1] - mag
+    up = (above < below) | ((above == below) & (j % 2 == 1))
+    return np.where(mag >= table[-1], len(table) - 1, j + up).astype(np.int64)
+
+
+def quantize_nvfp4_activation(a: np.ndarray) -> np.ndarray:
+    """Quantise a [M, K] activation to NVFP4 and return the dequantised values (fp64).
+
+    Reading of the NVFP4 scheme for activations (the pages give only "FP8 scales per 16
+    elements"): one dynamic fp32 tensor scale per call, ts = amax(|a|) / (6 * 448); per
+    16-element block, scale = E4M3_rne_satfinite((amax16 / 6) / ts); element code =
+    E2M1_rne_satfinite(a / (scale * ts)). Every quotient and product that decides a code
+    is an fp32 operation, in this order, on the fp32 value of ``a``.
+    """
+    a32 = np.asarray(a, dtype=np.float32)
+    m, k = a32.shape
+    amax = np.float32(np.max(np.abs(a32))) if a32.size else np.float32(0)
+    ts = np.float32(amax / np.float32(2688.0))
+    if ts == 0:
+        return np.zeros((m, k))
+    blocks = a32.reshape(m, k // 16, 16)
+    bamax = np.max(np.abs(blocks), axis=2)
+    ratio = ((bamax / np.float32(6.0)).astype(np.float32) / ts).astype(np.float32)
+    sb = _E4M3_MAGS[_rne_code(ratio, _E4M3_MAGS)]
+    denom = (sb.astype(np.float32) * ts).astype(np.float32)
+    q = np.zeros(blocks.shape, np.float32)
+    np.divide(blocks, denom[..., None], out=q, where=denom[..., None] != 0)
+    mag = _E2M1_MAGS[_rne_code(np.abs(q), _E2M1_MAGS)]
+    code_val = np.sign(q) * mag
+    return (code_val * sb[..., None].astype(np.float64) * float(ts)).reshape(m, k)
+
+
+# ----------------------------------------------------------------------- router
+
+
+def router_logits(x: np.ndarray, router_w: np.ndarray) -> np.ndarray:
+    """l[t, e] = sum_h x[t, h] W_r[e, h] in fp64 (the router projection)."""
+    return np.asarray(x, np.float64) @ np.asarray(router_w, np.float64).T
+
+
+def sigmoid(z: np.ndarray) -> np.ndarray:
+    """Gate score of the sigmoid router: 1 / (1 + e^-z)."""
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+@dataclass
+class Selection:
+    ids: np.ndarray          # [T, top_k] int64, slot order = descending b, ties lower id
+    group_margin: np.ndarray  # [T] gap between the last kept and the first dropped group
+    expert_margin: np.ndarray  # [T] gap between the k-th and (k+1)-th kept expert
+
+    @property
+    def margin(self) -> np.ndarray:
+        return np.minimum(self.group_margin, self.expert_margin)
+
+
+def select_experts(scores: np.ndarray, bias: np.ndarray, n_group: int, topk_group: int,
+                   top_k: int) -> Selection:
+    """noaux_tc grouped top-k on the biased scores b = s + bias.
+
+    Group score = sum of the two largest b in each contiguous group; the topk_group
+    best groups are kept; the top_k largest b among kept experts are selected. Ties go
+    to the lower index at both levels (stable descending order). Experts outside kept
+    groups are excluded outright (-inf), not zeroed.
+    """
+    s = np.asarray(scores, np.float64)
+    t_count, n_exp = s.shape
+    g_size = n_exp // n_group
+    if g_size * n_group != n_exp or g_size < 2 or not 1 <= topk_group <= n_group \
+            or not 1 <= top_k <= topk_group * g_size:
+        raise ValueError("invalid routing shape")
+    b = s + np.asarray(bias, np.float64)[None, :]
+    ids = np.empty((t_count, top_k), np.int64)
+    gm = np.full(t_count, np.inf)
+    em = np.full(t_count, np.inf)
+    for t in range(t_count):
+        grp = b[t].reshape(n_group, g_size)
+        top2 = -np.sort(-grp, axis=1)[:, :2]
+        gscore = top2[:, 0] + top2[:, 1]
+        g_order = np.argsort(-gscore, kind="stable")
+        kept = g_order[:topk_group]
+        if topk_group < n_group:
+            gm[t] = gscore[g_order[topk_group - 1]] - gscore[g_order[topk_group]]
+        masked = np.full(n_exp, -np.inf)
+        for g in kept:
+            masked[g * g_size:(g + 1) * g_size] = b[t, g * g_size:(g + 1) * g_size]
+        e_order = np.argsort(-masked, kind="stable")
+        ids[t] = e_order[:top_k]
+        if top_k < topk_group * g_size:
+            em[t] = masked[e_order[top_k - 1]] - masked[e_order[top_k]]
+    return Selection(ids, gm, em)
+
+
+def routing_weights(scores: np.ndarray, ids: np.ndarray, rsf: float) -> np.ndarray:
+    """w[t, j] = s[t, ids[t, j]] / sum_j s[t, ids[t, j]] * routed_scaling_factor."""
+    sel = np.take_along_axis(np.asarray(scores, np.float64), ids, axis=1)
+    return sel / sel.sum(axis=1, keepdims=True) * float(np.float32(rsf))
+
+
+def group_tokens(ids: np.ndarray, n_experts: int):
+    """Batch-union grouping: counts[E], offsets[E+1] (exclusive scan) and the entry list
+    [T*k] holding token*top_k + slot, grouped by expert, ascending token in each group."""
+    t_count, k = ids.shape
+    counts = np.bincount(ids.ravel(), minlength=n_experts)[:n_experts]
+    offsets = np.zeros(n_experts + 1, np.int64)
+    offsets[1:] = np.cumsum(counts)
+    lst = np.empty(t_count * k, np.int64)
+    cursor = offsets[:-1].copy()
+    for t in range(t_count):
+        for j in range(k):
+            e = ids[t, j]
+            lst[cursor[e]] = t * k + j
+            cursor[e] += 1
+    return counts, offsets, lst
+
+
+# ------------------------------------------------------------------- expert FFN
+
+
+def silu(z: np.ndarray) -> np.ndarray:
+    """SiLU(z) = z * sigmoid(z)."""
+    return z / (1.0 + np.exp(-z))
+
+
+def swiglu_hidden(w_gu: np.ndarray, xr: np.ndarray) -> np.ndarray:
+    """h = SiLU(gate) * up with [gate; up] = W_gu x (rows 0..I-1 gate, I..2I-1 up)."""
+    gu = np.asarray(xr, np.float64) @ np.asarray(w_gu, np.float64).T
+    i = gu.shape[1] // 2
+    return silu(gu[:, :i]) * gu[:, i:]
+
+
+def down_proj(w_d: np.ndarray, h: np.ndarray) -> np.ndarray:
+    """y = W_d h."""
+    return np.asarray(h, np.float64) @ np.asarray(w_d, np.float64).T
+
+
+# ----------------------------------------------------------------- whole layer
+
+
+@dataclass
+class LayerRef:
+    """Oracle outputs of one forward."""
+
+    out: np.ndarray            # [T, H] fp64
+    ids: np.ndarray            # [T, k]
+    weights: np.ndarray        # [T, k]
+    scores: np.ndarray         # [T, E] unbiased sigmoid scores
+    margin: np.ndarray         # [T]
+    counts: np.ndarray
+    offsets: np.ndarray
+    entries: np.ndarray
+
+
+class Layer:
+    """Weights of one layer as the oracle sees them (dequantised lazily, per expert)."""
+
+    def __init__(self, arrays: dict, *, hidden, inter, n_experts, top_k, n_group, topk_group,
+                 rsf, weight_format, act_dtype, router_dtype, shared_format):
+        self.a = arrays
+        self.H, self.I, self.E = hidden, inter, n_experts
+        self.top_k, self.n_group, self.topk_group = top_k, n_group, topk_group
+        self.rsf = rsf
+        self.weight_format, self.act_dtype = weight_format, act_dtype
+        self.router_dtype, self.shared_format = router_dtype, shared_format
+
+    @classmethod
+    def from_spec(cls, spec, arrays: dict) -> "Layer":
+        return cls(arrays, hidden=spec.hidden, inter=spec.inter, n_experts=spec.n_experts,
+                   top_k=spec.top_k, n_group=spec.n_group, topk_group=spec.topk_group,
+                   rsf=spec.rsf, weight_format=spec.weight_format, act_dtype=spec.act_dtype,
+                   router_dtype=spec.router_dtype, shared_format=spec.shared_format)
+
+    # -- weights
+    def router_w(self) -> np.ndarray:
+        w = self.a["router_w"]
+        return widen_bf16(w) if self.router_dtype == "bf16" else np.asarray(w, np.float64)
+
+    def _expert(self, prefix: str, idx: int, fmt: str):
+        a = self.a
+        if fmt == "int4_g32":
+            return (dequant_int4_g32(a[prefix + "gu_codes"][idx], a[prefix + "gu_scales"][idx]),
+                    dequant_int4_g32(a[prefix + "d_codes"][idx], a[prefix + "d_scales"][idx]))
+        if fmt == "nvfp4":
+            return (dequant_nvfp4(a[prefix + "gu_codes"][idx], a[prefix + "gu_scales"][idx],
+                                  a[prefix + "gu_tscale"][idx]),
+                    dequant_nvfp4(a[prefix + "d_codes"][idx], a[prefix + "d_scales"][idx],
+                                  a[prefix + "d_tscale"][idx]))
+        if fmt == "bf16":
+            return widen_bf16(a[prefix + "gu_bf16"][idx]), widen_bf16(a[prefix + "d_bf16"][idx])
+        raise ValueError(fmt)
+
+    def routed_expert(self, e: int):
+        return self._expert("", e, self.weight_format)
+
+    def shared_expert(self):
+        return self._expert("sh_", 0, self.shared_format)
+
+    def widen_x(self, x: np.ndarray) -> np.ndarray:
+        return widen_bf16(x) if self.act_dtype == "bf16" else np.asarray(x, np.float64)
+
+    # -- forward
+    def route(self, x64: np.ndarray):
+        scores = sigmoid(router_logits(x64, self.router_w()))
+        sel = select_experts(scores, self.a["bias"], self.n_group, self.topk_group, self.top_k)
+        return scores, sel
+
+    def forward(self, x: np.ndarray, ids: np.ndarray | None = None,
+                tokens: np.ndarray | None = None) -> LayerRef:
+        """Whole-layer forward. ``ids`` overrides the selection (used to re-run the
+        oracle on a near-tie token with the selection another implementation made);
+        ``tokens`` restricts the expert FFNs and the output to those rows (the routing
+        and the NVFP4 activation scales still see every token)."""
+        x64 = self.widen_x(x)
+        t_count = x64.shape[0]
+        scores, sel = self.route(x64)
+        use_ids = sel.ids if ids is None else np.asarray(ids, np.int64)
+        w = routing_weights(scores, use_ids, self.rsf)
+        counts, offsets, entries = group_tokens(use_ids, self.E)
+        rows = np.arange(t_count) if tokens is None else np.asarray(tokens, np.int64)
+        want = np.zeros(t_count, bool)
+        want[rows] = True
+        out = np.zeros((t_count, self.H))
+
+        nvfp4 = self.weight_format == "nvfp4"
+        x_in = quantize_nvfp4_activation(x64.astype(np.float32)) if nvfp4 else x64
+
+        # routed experts, batch-union: each expert's weights applied to all its tokens
+        hs = {}      # e -> (entries, h rows)
+        for e in range(self.E):
+            ent = entries[offsets[e]:offsets[e + 1]]
+            if not nvfp4:    # an NVFP4 layer needs every routed h for the h tensor scale
+                ent = ent[want[ent // self.top_k]]
+            if ent.size == 0:
+                continue
+            w_gu, _ = self.routed_expert(e)
+            hs[e] = (ent, swiglu_hidden(w_gu, x_in[ent // self.top_k]))
+        if nvfp4 and hs:
+            order = sorted(hs)
+            h_q = quantize_nvfp4_activation(
+                np.concatenate([hs[e][1] for e in order]).astype(np.float32))
+            n0 = 0
+            for e in order:
+                n1 = n0 + len(hs[e][0])
+                hs[e] = (hs[e][0], h_q[n0:n1])
+                n0 = n1
+        for e, (ent, h) in hs.items():
+            keep = want[ent // self.top_k]
+            if not keep.any():
+                continue
+            _, w_d = self.routed_expert(e)
+            y = down_proj(w_d, h[keep])
+            for r, yy in zip(ent[keep], y):
+                t, j = divmod(int(r), self.top_k)
+                out[t] += w[t, j] * yy
+
+        sh_gu, sh_d = self.shared_expert()
+        xs = x64[rows] if self.shared_format == "bf16" else x_in[rows]
+        out[rows] += down_proj(sh_d, swiglu_hidden(sh_gu, xs))
+        return LayerRef(out, use_ids, w, scores, sel.margin, counts, offsets, entries)

@@ -1,0 +1,346 @@
+"""Pins of the fp64 oracle: each check ties an oracle function to something other than
+itself (a format definition, a library routine, brute force, a closed form, an
+invariant). Every pin reads the oracle through the module object it is given, so the
+mutation tests can hand it a deliberately broken oracle and watch a pin fail.
+"""
+
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ------------------------------------------------------------------------ helpers
+
+
+def pack_int4_rows(codes: np.ndarray) -> np.ndarray:
+    """Pack int codes in [-8, 7] row-wise, element 2j in the low nibble of byte j."""
+    c = np.asarray(codes, np.int64)
+    u = (c & 0xF).astype(np.uint8)
+    return (u[..., 0::2] | (u[..., 1::2] << 4)).astype(np.uint8)
+
+
+def sigmoid_scalar(z: float) -> float:
+    return 1.0 / (1.0 + math.exp(-z))
+
+
+def silu_scalar(z: float) -> float:
+    return z * sigmoid_scalar(z)
+
+
+def hand_layer(O, case: str):
+    """Build the hand-worked two-expert layer of tests/golden/hand_two_expert.json."""
+    with open(os.path.join(GOLDEN, "hand_two_expert.json")) as f:
+        g = json.load(f)
+    H, I, E = g["hidden"], g["inter"], g["n_experts"]
+    x = np.zeros((1, H), np.float32)
+    for k, v in g["x_nonzero"].items():
+        x[0, int(k)] = v
+    wr = np.zeros((E, H), np.float32)
+    for e, row in g["router_w"].items():
+        for h, v in row.items():
+            wr[int(e), int(h)] = v
+
+    def expert(spec):
+        gu = np.zeros((2 * I, H), np.int64)
+        gus = np.zeros((2 * I, H // 32), np.float16)
+        for r, d in spec["gu"].items():
+            gu[int(r), :4] = d["codes"]
+            gus[int(r), 0] = d["scale"]
+        dd = np.zeros((H, I), np.int64)
+        ds = np.zeros((H, I // 32), np.float16)
+        for r, d in spec["d"].items():
+            dd[int(r), 0] = d["code0"]
+            ds[int(r), 0] = d["scale"]
+        return pack_int4_rows(gu), gus, pack_int4_rows(dd), ds
+
+    ex = [expert(s) for s in g["experts"]]
+    sh = expert(g["shared"])
+    c = g["cases"][case]
+    arrays = {
+        "router_w": wr, "bias": np.array(c["bias"], np.float32),
+        "gu_codes": np.stack([e[0] for e in ex]), "gu_scales": np.stack([e[1] for e in ex]),
+        "d_codes": np.stack([e[2] for e in ex]), "d_scales": np.stack([e[3] for e in ex]),
+        "sh_gu_codes": sh[0][None], "sh_gu_scales": sh[1][None],
+        "sh_d_codes": sh[2][None], "sh_d_scales": sh[3][None],
+    }
+    layer = O.Layer(arrays, hidden=H, inter=I, n_experts=E, top_k=c["top_k"], n_group=1,
+                    topk_group=1, rsf=g["rsf"], weight_format="int4_g32", act_dtype="f32",
+                    router_dtype="f32", shared_format="int4_g32")
+    return layer, x
+
+
+def brute_force_select(b: np.ndarray, n_group: int, topk_group: int, top_k: int):
+    """Exhaustive noaux_tc selection for one token with distinct scores: the best group
+    subset by summed group score, then the best expert subset by summed score."""
+    E = b.size
+    G = E // n_group
+    gscore = []
+    for g in range(n_group):
+        vals = b[g * G:(g + 1) * G]
+        best2 = max(vals[i] + vals[j] for i, j in itertools.combinations(range(G), 2))
+        gscore.append(best2)
+    best_groups = max(itertools.combinations(range(n_group), topk_group),
+                      key=lambda gs: sum(gscore[g] for g in gs))
+    cand = [e for g in best_groups for e in range(g * G, (g + 1) * G)]
+    best = max(itertools.combinations(cand, top_k), key=lambda es: sum(b[e] for e in es))
+    return sorted(best)
+
+
+# --------------------------------------------------------------- storage decoders
+
+
+def pin_decode_int4(O):
+    # two's complement by the machine: shift the nibble to the top of an int8
+    b = np.arange(256, dtype=np.uint8)
+    lo = (b << 4).astype(np.uint8).view(np.int8) >> 4
+    hi = b.view(np.int8) >> 4
+    got = O.decode_int4(b[:, None])
+    assert np.array_equal(got[:, 0], lo.astype(np.int64))
+    assert np.array_equal(got[:, 1], hi.astype(np.int64))
+    # hand examples: 0x8F -> (-1, -8), 0x7A -> (-6, 7), 0x21 -> (1, 2)
+    assert O.decode_int4(np.array([[0x8F, 0x7A, 0x21]], np.uint8)).tolist() == [[-1, -8, -6, 7, 1, 2]]
+
+
+def pin_decode_e4m3(O):
+    # library routine: torch's float8_e4m3fn for every bit pattern
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.decode_e4m3(np.arange(256))
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    # format facts: 0x7E = 448 (largest finite), 0x08 = 2^-6, 0x01 = 2^-9, 0x38 = 1
+    assert got[0x7E] == 448.0 and got[0x08] == 2.0 ** -6 and got[0x01] == 2.0 ** -9 and got[0x38] == 1.0
+
+
+def pin_decode_e2m1(O):
+    # OCP MX FP4 E2M1 value set, by the sign/exponent/mantissa fields written out
+    expected = []
+    for code in range(16):
+        s, e, m = code >> 3, (code >> 1) & 3, code & 1
+        mag = (m / 2.0) * 2.0 ** (1 - 1) if e == 0 else (1.0 + m / 2.0) * 2.0 ** (e - 1)
+        expected.append(-mag if s else mag)
+    assert np.array_equal(O.decode_e2m1(np.arange(16)), np.array(expected))
+    assert list(O.decode_e2m1(np.arange(8))) == [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+
+
+def pin_dequant_int4_g32(O):
+    codes = np.zeros((2, 64), np.int64)
+    codes[0, 0], codes[0, 31], codes[0, 32], codes[1, 63] = 3, -8, 7, -1
+    scales = np.array([[0.5, 2.0], [1.0, 0.125]], np.float16)
+    w = O.dequant_int4_g32(pack_int4_rows(codes), scales)
+    expect = np.zeros((2, 64))
+    expect[0, 0], expect[0, 31], expect[0, 32], expect[1, 63] = 1.5, -4.0, 14.0, -0.125
+    assert np.array_equal(w, expect)
+
+
+def pin_dequant_nvfp4(O):
+    codes = np.zeros((1, 32), np.int64)
+    codes[0, 0], codes[0, 15], codes[0, 16], codes[0, 31] = 0x7, 0xF, 0x3, 0x9   # 6, -6, 1.5, -0.5
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    scales = np.array([[0x38, 0x40]], np.uint8)   # e4m3: 1.0 and 2.0
+    w = O.dequant_nvfp4(packed, scales, np.float32(0.25))
+    expect = np.zeros((1, 32))
+    expect[0, 0], expect[0, 15], expect[0, 16], expect[0, 31] = 1.5, -1.5, 0.75, -0.25
+    assert np.array_equal(w, expect)
+
+
+# ------------------------------------------------------------ activation quantiser
+
+
+def _brute_round(v: float, table) -> int:
+    d = [abs(v - t) for t in table]
+    best = min(d)
+    cands = [i for i, x in enumerate(d) if x == best]
+    even = [i for i in cands if i % 2 == 0]
+    return (even or cands)[0]
+
+
+def pin_nvfp4_rounding(O):
+    rng = np.random.default_rng(7)
+    # E4M3 rounding against torch's conversion (RNE) on in-range values and exact ties
+    grid = O.decode_e4m3(np.arange(0x7F))
+    mids = (grid[:-1] + grid[1:]) / 2
+    vals = np.concatenate([rng.uniform(0, 440, 2000), rng.uniform(0, 0.02, 2000), mids, grid])
+    vals = vals.astype(np.float32).astype(np.float64)
+    ref = torch.from_numpy(vals.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = O._rne_code(vals, O._E4M3_MAGS)
+    assert np.array_equal(got, ref.astype(np.int64))
+    # E2M1 rounding against brute-force nearest-even over the 8 magnitudes
+    table = [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    vals = np.concatenate([rng.uniform(0, 7, 500), [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0, 9.0]])
+    got = O._rne_code(vals, O._E2M1_MAGS)
+    want = [7 if v >= 6 else _brute_round(v, table) for v in vals]
+    assert got.tolist() == want
+
+
+def pin_nvfp4_activation(O):
+    rng = np.random.default_rng(3)
+    # exactly representable input comes back unchanged: with amax 12 the block scales
+    # come out as 224, 448 and 112 (exact E4M3 values) and every element sits on the
+    # E2M1 grid times its block unit
+    a = np.zeros((2, 32), np.float32)
+    a[0, :16] = [6, -3, 1.5, 0.5, 0, 4, -2, 1, 6, 0, 0, 0, 0, 0, 0, 0]
+    a[0, 16:] = [12, 8, -6, 3, 1, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0]   # block scale 2
+    a[1, :16] = [3, 1.5, 0.5, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0]  # block scale 0.5
+    deq = O.quantize_nvfp4_activation(a)
+    assert np.allclose(deq, a, rtol=1e-6, atol=0), (deq, a)
+    # error bound on random data: half an E2M1 step at the code's magnitude, relative
+    # to the block's scale; at most a quarter of the block scale near zero
+    x = rng.standard_normal((8, 64)).astype(np.float32)
+    deq = O.quantize_nvfp4_activation(x)
+    ts = np.float32(np.abs(x).max() / np.float32(2688.0))
+    blk = np.abs(x).reshape(8, 4, 16).max(axis=2, keepdims=True) / 6.0
+    err = np.abs(deq.reshape(8, 4, 16) - x.reshape(8, 4, 16).astype(np.float64))
+    # the step at magnitude m/scale <= 6 is at most 2 units of the scale; block scale
+    # rounding to E4M3 adds at most 2^-4 relative
+    assert np.all(err <= blk * (1 + 2 ** -3) * 1.0 + 1e-6)
+    assert float(ts) > 0
+
+
+# ---------------------------------------------------------------------- router
+
+
+def pin_select_brute_force(O):
+    rng = np.random.default_rng(11)
+    shapes = [(16, 4, 2, 4), (12, 3, 2, 3), (12, 4, 1, 2), (16, 2, 1, 5), (9, 3, 3, 4),
+              (20, 5, 3, 6), (8, 1, 1, 3)]
+    for E, ng, tg, k in shapes:
+        for _ in range(40):
+            s = O.sigmoid(rng.standard_normal((1, E)))
+            bias = rng.normal(0, 0.3, E)
+            sel = O.select_experts(s, bias, ng, tg, k)
+            want = brute_force_select((s + bias)[0], ng, tg, k)
+            assert sorted(sel.ids[0].tolist()) == want, (E, ng, tg, k)
+
+
+def pin_select_special_cases(O):
+    rng = np.random.default_rng(5)
+    # one group: plain top-k of b, as torch.topk finds it (distinct values)
+    s = O.sigmoid(rng.standard_normal((64, 24)))
+    bias = rng.normal(0, 0.05, 24)
+    sel = O.select_experts(s, bias, 1, 1, 6)
+    ref = torch.topk(torch.from_numpy(s + bias), 6, dim=1).indices.numpy()
+    assert np.array_equal(np.sort(sel.ids, 1), np.sort(ref, 1))
+    # zero bias, one group: top-k of the logits (sigmoid is monotone)
+    logits = rng.standard_normal((64, 24))
+    sel = O.select_experts(O.sigmoid(logits), np.zeros(24), 1, 1, 5)
+    ref = torch.topk(torch.from_numpy(logits), 5, dim=1).indices.numpy()
+    assert np.array_equal(np.sort(sel.ids, 1), np.sort(ref, 1))
+    # ties: equal scores go to the lower index, among groups and among experts
+    b = np.array([[0.5, 0.5, 0.5, 0.5, 0.5, 0.5, 0.5, 0.5]])
+    sel = O.select_experts(b, np.zeros(8), 4, 2, 3)
+    assert sel.ids[0].tolist() == [0, 1, 2]
+    b = np.array([[0.1, 0.9, 0.2, 0.8, 0.9, 0.1, 0.85, 0.85]])   # groups of 2: 1.0, 1.0, 1.0, 1.7
+    sel = O.select_experts(b, np.zeros(8), 4, 2, 2)
+    assert sorted(sel.ids[0].tolist()) == [1, 6]
+    # a group of only negative biased scores still outranks a group of lower ones,
+    # and excluded experts never come back (no zero fill)
+    b = np.array([[-0.9, -0.8, -0.1, -0.2, -0.95, -0.99]])
+    sel = O.select_experts(b, np.zeros(6), 3, 1, 2)
+    assert sorted(sel.ids[0].tolist()) == [2, 3]
+
+
+def pin_routing_weights(O):
+    rng = np.random.default_rng(2)
+    s = O.sigmoid(rng.standard_normal((50, 16)))
+    bias = rng.normal(0, 0.5, 16)
+    sel = O.select_experts(s, bias, 4, 2, 4)
+    w = O.routing_weights(s, sel.ids, 2.5)
+    assert np.allclose(w.sum(1), 2.5, rtol=0, atol=1e-14)
+    # weights are proportional to the unbiased scores of the chosen experts
+    chosen = np.take_along_axis(s, sel.ids, 1)
+    assert np.allclose(w / chosen, (w / chosen)[:, :1], rtol=1e-13)
+    # k = 1 gives exactly rsf
+    sel1 = O.select_experts(s, bias, 4, 2, 1)
+    assert np.all(O.routing_weights(s, sel1.ids, 2.5) == 2.5)
+
+
+def pin_group_tokens(O):
+    rng = np.random.default_rng(4)
+    T, k, E = 37, 4, 16
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)])
+    counts, offsets, lst = O.group_tokens(ids, E)
+    assert counts.sum() == T * k and offsets[-1] == T * k and offsets[0] == 0
+    assert np.array_equal(np.diff(offsets), counts)
+    for e in range(E):
+        ent = lst[offsets[e]:offsets[e + 1]]
+        toks, slots = ent // k, ent % k
+        assert np.all(np.diff(toks) > 0)
+        assert np.all(ids[toks, slots] == e)
+    assert sorted(lst.tolist()) == list(range(T * k))
+
+
+# ------------------------------------------------------------------- expert FFN
+
+
+def pin_expert_ffn_torch(O):
+    rng = np.random.default_rng(9)
+    w_gu = rng.normal(0, 0.3, (2 * 48, 64))
+    w_d = rng.normal(0, 0.3, (64, 48))
+    x = rng.standard_normal((5, 64))
+    h = O.swiglu_hidden(w_gu, x)
+    y = O.down_proj(w_d, h)
+    tx, tgu, td = (torch.from_numpy(a) for a in (x, w_gu, w_d))
+    gu = torch.nn.functional.linear(tx, tgu)
+    th = torch.nn.functional.silu(gu[:, :48]) * gu[:, 48:]
+    ty = torch.nn.functional.linear(th, td)
+    assert torch.allclose(torch.from_numpy(h), th, rtol=1e-13, atol=1e-15)
+    assert torch.allclose(torch.from_numpy(y), ty, rtol=1e-12, atol=1e-14)
+
+
+def pin_hand_two_expert(O):
+    s0, s1 = sigmoid_scalar(0.25), sigmoid_scalar(-1.0)
+    h_e0 = silu_scalar(0.75) * 0.625
+    h_e1 = silu_scalar(4.0) * 2.0
+    h_sh = silu_scalar(1.0) * 3.0
+    # k = 2: both experts, weights from the unbiased scores
+    layer, x = hand_layer(O, "k2")
+    ref = layer.forward(x)
+    w0, w1 = s0 / (s0 + s1) * 2.5, s1 / (s0 + s1) * 2.5
+    expect = np.zeros(32)
+    expect[0] = w0 * 2 * h_e0 + w1 * h_e1
+    expect[5] = w0 * -3 * h_e0
+    expect[7] = w1 * 0.875 * h_e1
+    expect[1] = -2 * h_sh
+    assert np.allclose(ref.out[0], expect, rtol=1e-12, atol=1e-14), (ref.out[0][:8], expect[:8])
+    # k = 1 with a bias that flips the choice to expert 1; its weight is exactly rsf
+    layer, x = hand_layer(O, "k1")
+    ref = layer.forward(x)
+    assert ref.ids.tolist() == [[1]]
+    expect = np.zeros(32)
+    expect[0] = 2.5 * h_e1
+    expect[7] = 2.5 * 0.875 * h_e1
+    expect[1] = -2 * h_sh
+    assert np.allclose(ref.out[0], expect, rtol=1e-12, atol=1e-14), (ref.out[0][:8], expect[:8])
+
+
+def pin_layer_invariants(O, spec, arrays, x):
+    """Token permutation commutes with the layer; the routing weights sum to rsf;
+    doubling every routed W_d scale doubles the routed part of the output."""
+    layer = O.Layer.from_spec(spec, arrays)
+    ref = layer.forward(x)
+    perm = np.random.default_rng(1).permutation(x.shape[0])
+    ref_p = layer.forward(x[perm])
+    assert np.allclose(ref_p.out, ref.out[perm], rtol=1e-12, atol=1e-15)
+    assert np.allclose(ref.weights.sum(1), spec.rsf, atol=1e-12)
+    a2 = dict(arrays)
+    a2["d_scales"] = (arrays["d_scales"].astype(np.float32) * 2).astype(arrays["d_scales"].dtype)
+    ref2 = O.Layer.from_spec(spec, a2).forward(x)
+    a0 = dict(arrays)
+    a0["d_scales"] = np.zeros_like(arrays["d_scales"])
+    shared_only = O.Layer.from_spec(spec, a0).forward(x).out
+    assert np.allclose(ref2.out - shared_only, 2 * (ref.out - shared_only), rtol=1e-11, atol=1e-14)
+
+
+ALL_PINS = [pin_decode_int4, pin_decode_e4m3, pin_decode_e2m1, pin_dequant_int4_g32,
+            pin_dequant_nvfp4, pin_nvfp4_rounding, pin_nvfp4_activation, pin_select_brute_force,
+            pin_select_special_cases, pin_routing_weights, pin_group_tokens,
+            pin_expert_ffn_torch, pin_hand_two_expert]

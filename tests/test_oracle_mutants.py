@@ -1,0 +1,177 @@
+"""Planted mistakes in the oracle must be caught by its pins.
+
+Each mutant replaces one oracle function with a plausible wrong variant (a dropped
+term, a wrong sign or index, a transposed operand, a wrong tie rule) for the duration
+of one test, on the CPU, and asserts that at least one pin fails.
+"""
+
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as O
+from tests import oracle_pins as P
+
+_orig = {name: getattr(O, name) for name in dir(O)}
+
+
+def _nibbles_swapped(codes):
+    v = _orig["decode_int4"](codes)
+    out = v.copy()
+    out[..., 0::2], out[..., 1::2] = v[..., 1::2], v[..., 0::2]
+    return out
+
+
+def _unsigned_int4(codes):
+    v = _orig["decode_int4"](codes)
+    return np.where(v < 0, v + 16, v)
+
+
+def _scale_group_shift(codes, scales):
+    return _orig["dequant_int4_g32"](codes, np.roll(np.asarray(scales), 1, axis=-1))
+
+
+def _e4m3_bias8(bits):
+    return _orig["decode_e4m3"](bits) / 2.0
+
+
+def _e2m1_subnormal(n):
+    v = _orig["decode_e2m1"](n)
+    return np.where(np.abs(v) == 0.5, v / 2, v)
+
+
+def _sigmoid_sign(z):
+    return 1.0 / (1.0 + np.exp(z))
+
+
+def _silu_sign(z):
+    return z / (1.0 + np.exp(z))
+
+
+def _swiglu_swapped(w_gu, xr):
+    gu = np.asarray(xr, np.float64) @ np.asarray(w_gu, np.float64).T
+    i = gu.shape[1] // 2
+    return O.silu(gu[:, i:]) * gu[:, :i]
+
+
+def _down_transposed(w_d, h):
+    return np.asarray(h, np.float64) @ np.asarray(w_d, np.float64)
+
+
+def _select_top1_group(scores, bias, n_group, topk_group, top_k):
+    # group score from the single largest b instead of the top-2 sum
+    s = np.asarray(scores, np.float64)
+    T, E = s.shape
+    G = E // n_group
+    b = s + np.asarray(bias)[None]
+    ids = np.empty((T, top_k), np.int64)
+    for t in range(T):
+        gs = b[t].reshape(n_group, G).max(1)
+        kept = np.argsort(-gs, kind="stable")[:topk_group]
+        m = np.full(E, -np.inf)
+        for g in kept:
+            m[g * G:(g + 1) * G] = b[t, g * G:(g + 1) * G]
+        ids[t] = np.argsort(-m, kind="stable")[:top_k]
+    return O.Selection(ids, np.full(T, np.inf), np.full(T, np.inf))
+
+
+def _select_zero_fill(scores, bias, n_group, topk_group, top_k):
+    s = np.asarray(scores, np.float64)
+    T, E = s.shape
+    G = E // n_group
+    b = s + np.asarray(bias)[None]
+    ids = np.empty((T, top_k), np.int64)
+    for t in range(T):
+        grp = b[t].reshape(n_group, G)
+        gs = np.sort(grp, 1)[:, -2:].sum(1)
+        kept = np.argsort(-gs, kind="stable")[:topk_group]
+        m = np.zeros(E)
+        for g in kept:
+            m[g * G:(g + 1) * G] = b[t, g * G:(g + 1) * G]
+        ids[t] = np.argsort(-m, kind="stable")[:top_k]
+    return O.Selection(ids, np.full(T, np.inf), np.full(T, np.inf))
+
+
+def _select_ties_high(scores, bias, n_group, topk_group, top_k):
+    # mirror the expert axis so equal scores resolve to the higher index
+    E = np.asarray(scores).shape[1]
+    sel = _orig["select_experts"](np.asarray(scores)[:, ::-1], np.asarray(bias)[::-1],
+                                  n_group, topk_group, top_k)
+    return O.Selection(E - 1 - sel.ids, sel.group_margin, sel.expert_margin)
+
+
+def _select_bias_ignored(scores, bias, n_group, topk_group, top_k):
+    return _orig["select_experts"](scores, np.zeros_like(np.asarray(bias)), n_group,
+                                   topk_group, top_k)
+
+
+def _weights_no_rsf(scores, ids, rsf):
+    return _orig["routing_weights"](scores, ids, 1.0)
+
+
+def _weights_unnormalised(scores, ids, rsf):
+    return np.take_along_axis(np.asarray(scores, np.float64), ids, axis=1) * rsf
+
+
+def _group_descending(ids, n_experts):
+    counts, offsets, lst = _orig["group_tokens"](ids, n_experts)
+    lst = lst.copy()
+    for e in range(n_experts):
+        lst[offsets[e]:offsets[e + 1]] = lst[offsets[e]:offsets[e + 1]][::-1]
+    return counts, offsets, lst
+
+
+def _act_scale_no6(a):
+    a32 = np.asarray(a, np.float32)
+    return _orig["quantize_nvfp4_activation"](a32 * np.float32(6.0)) / 6.0 * 1.0001
+
+
+MUTANTS = {
+    "decode_int4/nibbles_swapped": ("decode_int4", _nibbles_swapped),
+    "decode_int4/unsigned": ("decode_int4", _unsigned_int4),
+    "dequant_int4_g32/scale_group_shift": ("dequant_int4_g32", _scale_group_shift),
+    "decode_e4m3/bias8": ("decode_e4m3", _e4m3_bias8),
+    "decode_e2m1/subnormal": ("decode_e2m1", _e2m1_subnormal),
+    "sigmoid/sign": ("sigmoid", _sigmoid_sign),
+    "silu/sign": ("silu", _silu_sign),
+    "swiglu/gate_up_swapped": ("swiglu_hidden", _swiglu_swapped),
+    "down_proj/transposed": ("down_proj", _down_transposed),
+    "select/top1_group_score": ("select_experts", _select_top1_group),
+    "select/zero_fill": ("select_experts", _select_zero_fill),
+    "select/ties_high": ("select_experts", _select_ties_high),
+    "select/bias_ignored": ("select_experts", _select_bias_ignored),
+    "weights/no_rsf": ("routing_weights", _weights_no_rsf),
+    "weights/unnormalised": ("routing_weights", _weights_unnormalised),
+    "group/descending": ("group_tokens", _group_descending),
+    "nvfp4_act/scale": ("quantize_nvfp4_activation", _act_scale_no6),
+}
+
+
+def _some_pin_fails() -> bool:
+    for pin in P.ALL_PINS:
+        try:
+            pin(O)
+        except (AssertionError, ValueError, IndexError):
+            return True
+    return False
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, monkeypatch):
+    attr, fn = MUTANTS[name]
+    monkeypatch.setattr(O, attr, fn)
+    assert _some_pin_fails(), f"no pin caught the planted mistake {name}"
+
+
+def test_shared_weighted_by_rsf_is_caught(monkeypatch):
+    orig = O.Layer.shared_expert
+
+    def scaled(self):
+        gu, d = orig(self)
+        return gu, d * self.rsf
+
+    monkeypatch.setattr(O.Layer, "shared_expert", scaled)
+    assert _some_pin_fails()
+
+
+def test_unmutated_oracle_passes_every_pin():
+    assert not _some_pin_fails()
