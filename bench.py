@@ -1,0 +1,336 @@
+#!/usr/bin/env python
+"""Benchmark of the quantised routed-MoE layer forward on B300.
+
+Workload (default): the GLM-5.2-shaped layer (H=6144, I=2048, E=256 routed + 1 shared
+expert, top-8 of 8 groups keep 4, int4 with an fp16 scale per 32 elements) at decode
+batch T=1, one fresh seeded token per step. A step is one whole forward (router,
+selection, grouping, gate/up + SwiGLU, down + combine). The timed region is one CUDA
+graph replay of K steps; step s reads layer copy s mod C (C identical copies at distinct
+addresses, so every step streams its experts from HBM rather than L2) and its own x.
+
+Prints one JSON line (rank 0). ``--impl reference`` times the fp64 CPU oracle instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s; expert-weight HBM GB/s vs ~8 TB/s at batch 1/32/2048"
+UNIT = "tokens/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="glm52_decode_t1")
+    p.add_argument("--copies", type=int, default=4)
+    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle time")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+
+def dist_info():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+class ClockSampler:
+    """NVML sampling of SM clock and clock-event reasons on a background thread."""
+
+    REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+               "hw_power_brake_slowdown": 0x80, "sw_power_cap": 0x4}
+
+    def __init__(self, index: int, period_s: float = 0.002):
+        self.index, self.period = index, period_s
+        self.samples, self.reasons = [], set()
+        self._stop = threading.Event()
+        self.ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as exc:  # pragma: no cover
+            self.err = repr(exc)
+
+    def _run(self):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
+                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for name, bit in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self.ok:
+            self.t.join()
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples)}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+def expert_bytes(spec):
+    """Stored bytes of one expert: (gate/up, down)."""
+    H, I = spec.hidden, spec.inter
+    if spec.weight_format == "int4_g32":
+        per = lambda n, k: n * (k // 2 + k // 32 * 2)
+    else:
+        per = lambda n, k: n * (k // 2 + k // 16) + 4
+    return per(2 * I, H), per(H, I)
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+
+def oracle_tokens_per_s(spec, arrays, T, budget_s, step0=0):
+    """Time the fp64 oracle on successive steps of the workload until ``budget_s``
+    seconds have passed (at least one step). Returns (tokens/s, steps, threads)."""
+    from oracle.moe_oracle import Layer
+    from synth import make_x
+    layer = Layer.from_spec(spec, arrays)
+    t0 = time.perf_counter()
+    steps = 0
+    while True:
+        layer.forward(make_x(spec, T, step0 + steps))
+        steps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        threads = 1
+    return steps * T / dt, steps, threads, dt
+
+
+# --------------------------------------------------------------------- arms
+
+
+def run_reference(args):
+    rank, _, world = dist_info()
+    if rank != 0:
+        return
+    from synth import WORKLOADS, make_layer
+    wl = WORKLOADS[args.workload]
+    spec, T = wl.layer, wl.tokens
+    arrays = make_layer(spec)
+    budget = min(150.0, max(10.0, 0.15 * (args.steps + args.warmup)))
+    if args.warmup:
+        oracle_tokens_per_s(spec, arrays, T, 0.0, step0=10_000)
+    value, steps, threads, dt = oracle_tokens_per_s(spec, arrays, T, budget)
+    sample = (f"fp64 numpy oracle, first {steps} of the {args.steps} steps' tokens "
+              f"(T={T} each, {dt:.1f} s time-bounded)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * dt / steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": wl.name, "tokens_per_step": T},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import quantized_moe_noaux_b300 as moe
+    from synth import WORKLOADS, make_layer, make_x
+
+    def x_to_device(x, act_dtype):
+        if act_dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+    rank, local_rank, world = dist_info()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl")
+    wl = WORKLOADS[args.workload]
+    spec, T = wl.layer, wl.tokens
+    K, W, C = args.steps, args.warmup, max(1, args.copies)
+    arrays = make_layer(spec)
+    layers = [moe.MoeLayer.from_spec(spec, arrays, max_tokens=T) for _ in range(C)]
+    stream = torch.cuda.Stream()
+    dt = torch.bfloat16 if spec.act_dtype == "bf16" else torch.float32
+    H = spec.hidden
+    base = 1000 * rank * (K + W)          # distinct tokens per rank
+    X = torch.stack([x_to_device(make_x(spec, T, base + s), spec.act_dtype) for s in range(K + W)])
+    OUT = torch.empty((K + W, T, H), dtype=dt, device="cuda")
+
+    with torch.cuda.stream(stream):
+        # warm-up (eager), also the source of per-step unique-expert counts
+        uniq = []
+        for s in range(W):
+            layers[s % C].forward(X[s], OUT[s], stream)
+        for s in range(K):
+            layers[s % C].forward(X[W + s], OUT[W + s], stream)
+            off = layers[s % C].routing(T, stream)["offsets"]
+            uniq.append(int(np.count_nonzero(np.diff(off))))
+        torch.cuda.synchronize()
+        for L in layers:
+            assert L.status() == 0, "device status word set"
+
+        launches0 = sum(L.launch_count() for L in layers)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for s in range(K):
+                layers[s % C].forward(X[W + s], OUT[W + s], stream)
+        launches = sum(L.launch_count() for L in layers) - launches0
+        graph.replay()
+        torch.cuda.synchronize()
+
+        # timed region
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(local_rank) as clocks:
+            ev0.record(stream)
+            graph.replay()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        ms = ev0.elapsed_time(ev1)
+        ms_t = torch.tensor([ms], device="cuda")
+        if world > 1:
+            dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+        ms = float(ms_t.item())
+        value = world * K * T / (ms / 1000.0)
+
+        # per-stage durations over a replay of the same K steps (stage events recorded
+        # inside a second graph capture)
+        for L in layers:
+            L.enable_timing((K + C - 1) // C)
+        graph2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph2, stream=stream):
+            for s in range(K):
+                layers[s % C].forward(X[W + s], OUT[W + s], stream)
+        graph2.replay()
+        torch.cuda.synchronize()
+        stage_ms = {name: 0.0 for name in moe.STAGES}
+        nfw = 0
+        for L in layers:
+            st, n = L.stage_times()
+            nfw += n
+            for kk, v in st.items():
+                stage_ms[kk] += v
+            L.enable_timing(0)
+
+        # end-to-end through the public API with host buffers (pinned)
+        KE = min(args.e2e_steps, K)
+        xh = X[W:W + KE].cpu().pin_memory()
+        oh = torch.empty((KE, T, H), dtype=dt).pin_memory()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for s in range(KE):
+            layers[s % C].forward_host(xh[s], oh[s], stream)
+        e2e_s = time.perf_counter() - t0
+        e2e_t = torch.tensor([e2e_s], device="cuda")
+        if world > 1:
+            dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+        e2e_value = world * KE * T / float(e2e_t.item())
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    gu_b, d_b = expert_bytes(spec)
+    n_units = sum(u + 1 for u in uniq)                # routed unique + shared, over K steps
+    dom = max(("gate_up_swiglu", "down_combine"), key=lambda k: stage_ms[k])
+    dom_bytes = n_units * (gu_b if dom == "gate_up_swiglu" else d_b)
+    dom_s = stage_ms[dom] / 1000.0
+    peak, peak_kind = measured_peaks()
+    achieved = dom_bytes / dom_s / 1e9
+    step_bytes = n_units * (gu_b + d_b) / K
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                "bytes_per_launch": dom_bytes / K,
+                "step_expert_bytes": step_bytes,
+                "step_expert_gbs": step_bytes / (ms / K / 1000.0) / 1e9}
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, random-init weights)",
+            "config": {"workload": wl.name, "tokens_per_step": T, "layer": spec.name,
+                       "layer_copies": C, "l2": f"inputs larger than L2: {C} layer copies "
+                       "rotated per step, each step streams its experts from HBM",
+                       "unique_experts_mean": float(np.mean(uniq)),
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roofline,
+            "stage_ms_per_step": {k: v / max(nfw, 1) for k, v in stage_ms.items()},
+            "gpu_launches": launches,
+            "clocks": clocks.summary(),
+            "e2e": {"value": e2e_value, "unit": UNIT,
+                    "h2d_bytes_per_step": T * H * (2 if spec.act_dtype == "bf16" else 4),
+                    "d2h_bytes_per_step": T * H * (2 if spec.act_dtype == "bf16" else 4),
+                    "steps": KE}}
+    if world == 1 and not args.no_cpu_baseline:
+        v, steps, threads, dt_cpu = oracle_tokens_per_s(spec, arrays, T, args.cpu_budget)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": f"{steps} steps of T={T} ({dt_cpu:.1f} s), fp64 numpy"}
+    print(json.dumps(line), flush=True)
+    for L in layers:
+        L.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

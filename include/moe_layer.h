@@ -1,0 +1,187 @@
+/*
+ * moe_layer.h - C ABI of the B300 quantised routed-MoE layer forward.
+ *
+ * The layer is the one the colibri engine runs for GLM-5.2 ("Show HN: Menjalankan GLM 5.2
+ * di komputer lambat", section "Fitur utama yang diimplementasikan"): a DeepSeek-V3-style
+ * sigmoid router with noaux_tc bias-corrected grouped top-k, routed_scaling_factor and an
+ * always-on shared expert; batch-union grouping, so each selected expert's weights are
+ * read once per call and applied to every token routed to it (same section, and
+ * "16 Teknik Özellik ve Yazılım Çıkarımları" of "Show HN: GLM 5.2 Modelini Yavaş
+ * Bilgisayarımda Çalıştırmak"); weight-only quantised SwiGLU experts in packed int4
+ * (one fp16 scale per 32 input-dim elements) or NVFP4 (E2M1 codes, an E4M3 scale per
+ * 16 elements and an fp32 tensor scale: "NVIDIA stellt neues GLM-5.2 NVFP4 Modell vor",
+ * section "Technische Details und Quantisierungsansatz"); and the weighted combine.
+ *
+ * out[t] = sum_j w[t,j] * FFN_{ids[t,j]}(x[t]) + FFN_shared(x[t])
+ *   FFN_e(v) = W_d^e (SiLU(W_g^e v) * (W_u^e v))
+ *   s = sigmoid(x W_r^T);  b = s + bias (selection only)
+ *   group score = sum of the two largest b per group of E/n_group experts
+ *   keep the topk_group best groups; ids = top_k largest b among kept experts
+ *   w[t,j] = s[ids[t,j]] / sum_j s[ids[t,j]] * routed_scaling_factor
+ * For NVFP4 layers the activations feeding the routed experts (x, and h before the
+ * down projection) are themselves quantised to NVFP4 with a per-call fp32 tensor scale
+ * (amax / (6*448)); a bf16 shared expert and the router read the unquantised x.
+ *
+ * All entry points return a moe_status and never abort the process. Device pointers
+ * are CUDA device (or managed) addresses on the device that was current at create time;
+ * "host" pointers may be pageable or pinned host memory. Streams are cudaStream_t passed
+ * as void* (NULL = the legacy default stream).
+ */
+#ifndef MOE_LAYER_H
+#define MOE_LAYER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* a NULL/misaligned pointer, a size out of range */
+  MOE_ERR_UNSUPPORTED = 2,   /* a shape or format combination this build does not run */
+  MOE_ERR_OOM = 3,           /* device or pinned-host allocation failed */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime call failed (launch, copy, sync) */
+  MOE_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up */
+  MOE_ERR_DEVICE_CHECK = 6   /* a device-side consistency check failed */
+} moe_status;
+
+/* storage formats */
+enum { MOE_W_INT4_G32 = 0, MOE_W_NVFP4 = 1, MOE_W_BF16 = 2 };
+/* activation / router element types */
+enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 };
+/* forward-path selection (moe_layer_set_path) */
+enum { MOE_PATH_AUTO = 0, MOE_PATH_GEMV = 1, MOE_PATH_GROUPED = 2 };
+
+typedef struct {
+  int32_t hidden;              /* H: multiple of 256 */
+  int32_t inter;               /* I: per-expert intermediate size, multiple of 64 */
+  int32_t n_experts;           /* E routed experts (the shared expert is extra) */
+  int32_t top_k;               /* experts per token, 1..16 */
+  int32_t n_group;             /* groups of E/n_group experts (>= 2 experts each) */
+  int32_t topk_group;          /* groups kept per token */
+  int32_t max_tokens;          /* largest T forward will be called with */
+  float routed_scaling_factor; /* rsf */
+  int32_t weight_format;       /* routed experts: MOE_W_INT4_G32 | MOE_W_NVFP4 */
+  int32_t shared_format;       /* shared expert: MOE_W_INT4_G32 | MOE_W_NVFP4 | MOE_W_BF16 */
+  int32_t act_dtype;           /* x and out: MOE_DT_F32 | MOE_DT_BF16 */
+  int32_t router_dtype;        /* W_r: MOE_DT_F32 | MOE_DT_BF16 */
+} moe_config;
+
+/*
+ * Layer weights, read once by moe_layer_create (host or device memory, contiguous,
+ * row-major). Routed arrays are stacked over the E experts:
+ *   router_w  [E, H]           fp32 or bf16 (router_dtype)
+ *   bias      [E]              fp32 e_score_correction_bias
+ *   gu_codes  [E, 2I, H/2]     uint8; rows 0..I-1 gate, I..2I-1 up; element 2j in the
+ *                              low nibble of byte j (int4: two's complement; NVFP4: E2M1)
+ *   gu_scales [E, 2I, H/32]    fp16 (int4_g32)  |  [E, 2I, H/16] uint8 E4M3 (NVFP4)
+ *   gu_tscale [E]              fp32 tensor scale (NVFP4 only, else NULL)
+ *   d_codes   [E, H, I/2], d_scales [E, H, I/32 | I/16], d_tscale [E]  (down projection)
+ * The shared expert uses the sh_* fields with the same layouts and no leading E
+ * dimension; for MOE_W_BF16, sh_gu is [2I, H] bf16, sh_d is [H, I] bf16 and the scale
+ * fields are NULL.
+ */
+typedef struct {
+  const void* router_w;
+  const float* bias;
+  const uint8_t* gu_codes;
+  const void* gu_scales;
+  const float* gu_tscale;
+  const uint8_t* d_codes;
+  const void* d_scales;
+  const float* d_tscale;
+  const void* sh_gu;
+  const void* sh_gu_scales;
+  const float* sh_gu_tscale;
+  const void* sh_d;
+  const void* sh_d_scales;
+  const float* sh_d_tscale;
+} moe_weights;
+
+typedef struct moe_layer moe_layer;
+
+/*
+ * Create a layer on the current CUDA device. Copies (and repacks) the weights into
+ * library-owned device memory and allocates the workspace for cfg->max_tokens tokens;
+ * the caller may free its weight buffers when this returns. Work is enqueued on
+ * `stream` and completed before return.
+ * Errors: MOE_ERR_INVALID_ARG (NULL pointer, bad sizes), MOE_ERR_UNSUPPORTED (shape or
+ * format outside the limits documented in moe_config), MOE_ERR_OOM, MOE_ERR_CUDA.
+ * On error *out is set to NULL and nothing is leaked.
+ */
+moe_status moe_layer_create(const moe_config* cfg, const moe_weights* w, void* stream,
+                            moe_layer** out);
+
+/*
+ * out[T, H] = layer(x[T, H]); x and out are device pointers in act_dtype, row-major,
+ * 16-byte aligned, not overlapping. 0 <= T <= max_tokens (T = 0 is a no-op).
+ * Asynchronous on `stream`: no host synchronisation, no allocation, capturable in a
+ * CUDA graph. Not thread-safe per layer (the workspace is shared by calls).
+ * Routing results stay on the device; moe_layer_get_routing copies them out.
+ * Errors: MOE_ERR_INVALID_ARG synchronously; device-side check failures are reported by
+ * moe_layer_status.
+ */
+moe_status moe_layer_forward(moe_layer* layer, const void* x, int32_t T, void* out, void* stream);
+
+/*
+ * Same computation with HOST buffers: copies x_host (T*H elements of act_dtype) to the
+ * device, runs the forward and copies the result into out_host, then synchronises
+ * `stream`. Uses the layer's own device staging buffers (allocated at create).
+ */
+moe_status moe_layer_forward_host(moe_layer* layer, const void* x_host, int32_t T,
+                                  void* out_host, void* stream);
+
+/*
+ * Copy the routing of the last forward (called with the same T) to host memory and
+ * synchronise `stream`. Any output pointer may be NULL to skip it.
+ *   ids     [T, top_k] int32 selected experts (slot order: descending biased score)
+ *   weights [T, top_k] fp32 combine weights
+ *   offsets [E + 1]    int32 exclusive scan of per-expert counts
+ *   entries [T * top_k] int32 token*top_k + slot, grouped by expert, ascending token
+ */
+moe_status moe_layer_get_routing(moe_layer* layer, int32_t T, int32_t* ids, float* weights,
+                                 int32_t* offsets, int32_t* entries, void* stream);
+
+/* Force the expert path (MOE_PATH_*) for later forwards; AUTO picks by T. */
+moe_status moe_layer_set_path(moe_layer* layer, int32_t path);
+
+/*
+ * Synchronise the device and report the sticky device-side status word (MOE_OK,
+ * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK) plus any pending CUDA error.
+ */
+moe_status moe_layer_status(moe_layer* layer);
+
+/*
+ * Stage timing (for measurement): with enable = N > 0 the layer creates N x 7 CUDA
+ * events and each of the next N forwards records 7 events on its stream at the stage
+ * boundaries: start | routing (router logits, selection, grouping) | activation quantise
+ * (NVFP4) | gate/up + SwiGLU | h quantise (NVFP4) | down + combine | output conversion |.
+ * Events recorded while the stream is being captured become graph nodes and are timed
+ * on replay. enable = 0 releases the events.
+ */
+moe_status moe_layer_enable_timing(moe_layer* layer, int32_t enable);
+
+/*
+ * Synchronise the device, then write into ms[0..5] the summed durations (milliseconds)
+ * of the 6 stages over the forwards recorded since timing was enabled (or last read),
+ * and their number into *n_forwards; resets the record count. An empty stage reads 0.
+ */
+moe_status moe_layer_stage_times(moe_layer* layer, float* ms, int32_t* n_forwards);
+
+/* Cumulative number of kernel launches this layer has issued (host-side count; a forward
+ * captured into a CUDA graph counts once at capture). */
+moe_status moe_layer_launch_count(moe_layer* layer, int64_t* count);
+
+/* Free everything the layer owns. NULL is a no-op. */
+void moe_layer_destroy(moe_layer* layer);
+
+/* Static string naming a status code. */
+const char* moe_status_string(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LAYER_H */

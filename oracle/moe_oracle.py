@@ -46,25 +46,42 @@ import numpy as np
 # ------------------------------------------------------------------ storage decoders
 
 
+def _int4_pair_table() -> np.ndarray:
+    """[256, 2] int64: the (low, high) two's-complement nibble values of every byte."""
+    b = np.arange(256)
+    lo, hi = b & 0x0F, b >> 4
+    return np.stack([np.where(lo >= 8, lo - 16, lo), np.where(hi >= 8, hi - 16, hi)], axis=1)
+
+
+_INT4_PAIRS = _int4_pair_table()
+
+
 def decode_int4(codes: np.ndarray) -> np.ndarray:
     """Packed two's-complement int4 -> int64, element 2j from the low nibble of byte j,
     2j+1 from the high nibble (the packed int4 container of "Fitur utama yang
     diimplementasikan")."""
     codes = np.asarray(codes, dtype=np.uint8)
-    lo = (codes & 0x0F).astype(np.int64)
-    hi = (codes >> 4).astype(np.int64)
-    v = np.stack([lo, hi], axis=-1).reshape(*codes.shape[:-1], codes.shape[-1] * 2)
-    return np.where(v >= 8, v - 16, v)
+    return _INT4_PAIRS[codes].reshape(*codes.shape[:-1], codes.shape[-1] * 2)
+
+
+_INT4_LO = _INT4_PAIRS[:, 0].astype(np.float64)
+_INT4_HI = _INT4_PAIRS[:, 1].astype(np.float64)
 
 
 def dequant_int4_g32(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     """W[n, k] = code[n, k] * scale[n, k // 32], exact in fp64 (dequant-on-use of the
     packed int4 weights; one fp16 scale per 32 input-dim elements)."""
-    c = decode_int4(codes).astype(np.float64)
-    n, k = c.shape
+    codes = np.asarray(codes, dtype=np.uint8)
+    n, kb = codes.shape
+    k = 2 * kb
+    c = np.empty((n, k))
+    np.take(_INT4_LO, codes, out=c[:, 0::2])
+    np.take(_INT4_HI, codes, out=c[:, 1::2])
     s = np.asarray(scales, dtype=np.float16).astype(np.float64)
     assert s.shape == (n, k // 32)
-    return (c.reshape(n, k // 32, 32) * s[..., None]).reshape(n, k)
+    c = c.reshape(n, k // 32, 32)
+    c *= s[..., None]
+    return c.reshape(n, k)
 
 
 def decode_e2m1(nibbles: np.ndarray) -> np.ndarray:

@@ -1,0 +1,230 @@
+"""B300-native quantised routed-MoE layer forward.
+
+A thin ctypes binding of ``libmoe.so`` (see ``include/moe_layer.h``): argument
+marshalling only. Every step of the layer runs in the library's CUDA kernels; there is
+no CPU or PyTorch fallback. The library is loaded on first use (``lib``), and that use
+fails loudly when it has not been built (``python -m quantized_moe_noaux_b300.build``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+__all__ = ["MoeLayer", "MoeError", "lib", "LIB_PATH", "SYMBOLS", "STAGES", "W_INT4_G32", "W_NVFP4",
+           "W_BF16", "DT_F32", "DT_BF16", "PATH_AUTO", "PATH_GEMV", "PATH_GROUPED"]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
+
+W_INT4_G32, W_NVFP4, W_BF16 = 0, 1, 2
+DT_F32, DT_BF16 = 0, 1
+PATH_AUTO, PATH_GEMV, PATH_GROUPED = 0, 1, 2
+
+_FMT = {"int4_g32": W_INT4_G32, "nvfp4": W_NVFP4, "bf16": W_BF16}
+_DT = {"f32": DT_F32, "bf16": DT_BF16}
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_OOM",
+          4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_DEVICE_CHECK"}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, call: str, code: int):
+        super().__init__(f"{call} failed: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32),
+                ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("n_group", ctypes.c_int32), ("topk_group", ctypes.c_int32),
+                ("max_tokens", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
+                ("weight_format", ctypes.c_int32), ("shared_format", ctypes.c_int32),
+                ("act_dtype", ctypes.c_int32), ("router_dtype", ctypes.c_int32)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_void_p) for name in (
+        "router_w", "bias", "gu_codes", "gu_scales", "gu_tscale", "d_codes", "d_scales",
+        "d_tscale", "sh_gu", "sh_gu_scales", "sh_gu_tscale", "sh_d", "sh_d_scales", "sh_d_tscale")]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+
+# name -> (restype, argtypes): every entry point the header declares
+SYMBOLS = {
+    "moe_layer_create": (_I, [ctypes.POINTER(Config), ctypes.POINTER(Weights), _P,
+                              ctypes.POINTER(_P)]),
+    "moe_layer_forward": (_I, [_P, _P, _I, _P, _P]),
+    "moe_layer_forward_host": (_I, [_P, _P, _I, _P, _P]),
+    "moe_layer_get_routing": (_I, [_P, _I, _P, _P, _P, _P, _P]),
+    "moe_layer_set_path": (_I, [_P, _I]),
+    "moe_layer_status": (_I, [_P]),
+    "moe_layer_destroy": (None, [_P]),
+    "moe_layer_enable_timing": (_I, [_P, _I]),
+    "moe_layer_stage_times": (_I, [_P, _P, _P]),
+    "moe_layer_launch_count": (_I, [_P, _P]),
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+}
+
+STAGES = ("routing", "act_quant", "gate_up_swiglu", "h_quant", "down_combine", "output")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -m quantized_moe_noaux_b300.build` (no fallback exists)")
+    handle = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SYMBOLS.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
+
+
+_lib = None
+
+
+def __getattr__(name):
+    if name == "lib":
+        return _get_lib()
+    raise AttributeError(name)
+
+
+def _get_lib():
+    global _lib
+    if _lib is None:
+        _lib = _load()
+    return _lib
+
+
+def _check(call: str, code: int):
+    if code != 0:
+        raise MoeError(call, code)
+
+
+def _ptr(a) -> int | None:
+    """Address of a contiguous numpy array or torch tensor (host or device)."""
+    if a is None:
+        return None
+    if isinstance(a, np.ndarray):
+        if not a.flags.c_contiguous:
+            raise ValueError("arrays must be C-contiguous")
+        return a.ctypes.data
+    if hasattr(a, "data_ptr"):
+        if not a.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        return a.data_ptr()
+    raise TypeError(type(a))
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if hasattr(stream, "cuda_stream"):
+        return stream.cuda_stream
+    return int(stream)
+
+
+class MoeLayer:
+    """One layer: ``MoeLayer(arrays, hidden=..., ..., max_tokens=...)``.
+
+    ``arrays`` maps the weight names of ``include/moe_layer.h`` (``router_w``, ``bias``,
+    ``gu_codes``, ``gu_scales``, ``gu_tscale``, ``d_codes``, ``d_scales``, ``d_tscale``,
+    and for the shared expert ``sh_gu_codes``/``sh_gu_bf16``, ``sh_gu_scales``, ...) to
+    contiguous numpy arrays or torch tensors (host or device). The library copies them.
+    """
+
+    def __init__(self, arrays: dict, *, hidden: int, inter: int, n_experts: int, top_k: int,
+                 n_group: int, topk_group: int, rsf: float, weight_format: str,
+                 shared_format: str, act_dtype: str, router_dtype: str, max_tokens: int,
+                 stream=None):
+        self.cfg = Config(hidden, inter, n_experts, top_k, n_group, topk_group, max_tokens,
+                          rsf, _FMT[weight_format], _FMT[shared_format], _DT[act_dtype],
+                          _DT[router_dtype])
+        self.hidden, self.top_k, self.n_experts, self.max_tokens = hidden, top_k, n_experts, max_tokens
+        self.act_dtype = act_dtype
+        a = arrays
+        sh_gu = a.get("sh_gu_bf16") if shared_format == "bf16" else a.get("sh_gu_codes")
+        sh_d = a.get("sh_d_bf16") if shared_format == "bf16" else a.get("sh_d_codes")
+        w = Weights(_ptr(a["router_w"]), _ptr(a["bias"]), _ptr(a["gu_codes"]),
+                    _ptr(a.get("gu_scales")), _ptr(a.get("gu_tscale")), _ptr(a["d_codes"]),
+                    _ptr(a.get("d_scales")), _ptr(a.get("d_tscale")), _ptr(sh_gu),
+                    _ptr(a.get("sh_gu_scales")), _ptr(a.get("sh_gu_tscale")), _ptr(sh_d),
+                    _ptr(a.get("sh_d_scales")), _ptr(a.get("sh_d_tscale")))
+        handle = _P()
+        _check("moe_layer_create", _get_lib().moe_layer_create(ctypes.byref(self.cfg), ctypes.byref(w),
+                                                         _stream(stream), ctypes.byref(handle)))
+        self._h = handle
+
+    @classmethod
+    def from_spec(cls, spec, arrays: dict, max_tokens: int, stream=None) -> "MoeLayer":
+        """Build from any object with the ``synth.LayerSpec`` attribute names."""
+        return cls(arrays, hidden=spec.hidden, inter=spec.inter, n_experts=spec.n_experts,
+                   top_k=spec.top_k, n_group=spec.n_group, topk_group=spec.topk_group,
+                   rsf=spec.rsf, weight_format=spec.weight_format,
+                   shared_format=spec.shared_format, act_dtype=spec.act_dtype,
+                   router_dtype=spec.router_dtype, max_tokens=max_tokens, stream=stream)
+
+    @property
+    def handle(self) -> int:
+        return self._h.value
+
+    def forward(self, x, out, stream=None):
+        """out[T, H] = layer(x[T, H]) on device tensors, asynchronous on ``stream``."""
+        T = int(x.shape[0])
+        _check("moe_layer_forward", _get_lib().moe_layer_forward(self._h, _ptr(x), T, _ptr(out),
+                                                           _stream(stream)))
+        return out
+
+    def forward_host(self, x_host, out_host, stream=None):
+        """Same with host buffers (copies in, forward, copies out, synchronises)."""
+        T = int(x_host.shape[0])
+        _check("moe_layer_forward_host", _get_lib().moe_layer_forward_host(
+            self._h, _ptr(x_host), T, _ptr(out_host), _stream(stream)))
+        return out_host
+
+    def routing(self, T: int, stream=None) -> dict:
+        """Routing of the last forward with T tokens, as host numpy arrays."""
+        k, E = self.top_k, self.n_experts
+        r = {"ids": np.empty((T, k), np.int32), "weights": np.empty((T, k), np.float32),
+             "offsets": np.empty(E + 1, np.int32), "entries": np.empty(T * k, np.int32)}
+        _check("moe_layer_get_routing", _get_lib().moe_layer_get_routing(
+            self._h, T, _ptr(r["ids"]), _ptr(r["weights"]), _ptr(r["offsets"]),
+            _ptr(r["entries"]), _stream(stream)))
+        return r
+
+    def set_path(self, path: int):
+        _check("moe_layer_set_path", _get_lib().moe_layer_set_path(self._h, path))
+
+    def enable_timing(self, n_forwards: int):
+        """Record stage events for the next ``n_forwards`` forwards (0 disables)."""
+        _check("moe_layer_enable_timing", _get_lib().moe_layer_enable_timing(self._h, n_forwards))
+
+    def stage_times(self) -> tuple[dict, int]:
+        """Summed stage durations (ms) over the recorded forwards, and their count."""
+        ms = (ctypes.c_float * 6)()
+        n = ctypes.c_int32()
+        _check("moe_layer_stage_times", _get_lib().moe_layer_stage_times(self._h, ms, ctypes.byref(n)))
+        return dict(zip(STAGES, list(ms))), n.value
+
+    def launch_count(self) -> int:
+        c = ctypes.c_int64()
+        _check("moe_layer_launch_count", _get_lib().moe_layer_launch_count(self._h, ctypes.byref(c)))
+        return c.value
+
+    def status(self) -> int:
+        return _get_lib().moe_layer_status(self._h)
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _get_lib().moe_layer_destroy(self._h)
+        self._h = _P()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,147 @@
+// Shared device helpers of the MoE layer kernels: storage decoders, element loads,
+// the device status word and the per-forward parameter block.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_layer.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ status word
+// Sticky device-side status: the first failing check wins (atomicCAS from MOE_OK).
+__device__ __forceinline__ void raise_status(int* status, int code) {
+  if (status) atomicCAS(status, MOE_OK, code);
+}
+
+// ------------------------------------------------------------- element decoders
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
+// int4 two's-complement nibble -> float
+__device__ __forceinline__ float int4_to_float(uint32_t nib) {
+  return (float)((int)(nib ^ 8u) - 8);
+}
+
+// FP4 E2M1 nibble -> float: 1 sign, 2 exponent bits (bias 1), 1 mantissa bit,
+// exponent field 0 is subnormal with step 0.5.
+__device__ __forceinline__ float e2m1_to_float(uint32_t nib) {
+  uint32_t e = (nib >> 1) & 3u, m = nib & 1u;
+  uint32_t mag = e ? (((e + 126u) << 23) | (m << 22)) : (m ? 0x3F000000u : 0u);
+  return __uint_as_float(mag | ((nib & 8u) << 28));
+}
+
+// FP8 E4M3 byte -> float (bias 7, subnormal step 2^-9). Scale bytes are non-negative
+// finite in this layer; the NaN pattern is not special-cased.
+__device__ __forceinline__ float e4m3_to_float(uint32_t b) {
+  uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  float mag = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;
+  return (b & 0x80u) ? -mag : mag;
+}
+
+// Load element i of an activation row stored as fp32 or bf16.
+template <int DT>
+__device__ __forceinline__ float load_act(const void* base, size_t i) {
+  if constexpr (DT == MOE_DT_F32) {
+    return __ldg(reinterpret_cast<const float*>(base) + i);
+  } else {
+    return bf16_bits_to_float(__ldg(reinterpret_cast<const unsigned short*>(base) + i));
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void store_act(void* base, size_t i, float v) {
+  if constexpr (DT == MOE_DT_F32) {
+    reinterpret_cast<float*>(base)[i] = v;
+  } else {
+    reinterpret_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
+  }
+}
+
+__device__ __forceinline__ float sigmoidf_acc(float z) { return 1.0f / (1.0f + expf(-z)); }
+__device__ __forceinline__ float siluf_acc(float z) { return z / (1.0f + expf(-z)); }
+
+// ------------------------------------------------------------ weight formats
+// A weight row is read in 16-byte chunks. Per chunk:
+//   int4_g32: 32 elements, one fp16 scale (the chunk is exactly one g32 group)
+//   nvfp4:    32 elements, two E4M3 scales (two 16-element blocks), tensor scale
+//   bf16:      8 elements, no scale
+template <int FMT>
+struct WFmt;
+
+template <>
+struct WFmt<MOE_W_INT4_G32> {
+  static constexpr int EPC = 32;             // elements per 16-byte chunk
+  static constexpr int SCALE_BYTES_PER_CHUNK = 2;
+  __device__ __forceinline__ static void decode(uint4 d, const uint8_t* srow, int chunk,
+                                                float /*tscale*/, float (&w)[EPC]) {
+    float s = __half2float(__ldg(reinterpret_cast<const __half*>(srow) + chunk));
+    uint32_t words[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[q * 8 + i] = int4_to_float((words[q] >> (4 * i)) & 15u) * s;
+  }
+};
+
+template <>
+struct WFmt<MOE_W_NVFP4> {
+  static constexpr int EPC = 32;
+  static constexpr int SCALE_BYTES_PER_CHUNK = 2;
+  __device__ __forceinline__ static void decode(uint4 d, const uint8_t* srow, int chunk,
+                                                float tscale, float (&w)[EPC]) {
+    float s0 = e4m3_to_float(__ldg(srow + 2 * chunk)) * tscale;
+    float s1 = e4m3_to_float(__ldg(srow + 2 * chunk + 1)) * tscale;
+    uint32_t words[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        w[q * 8 + i] = e2m1_to_float((words[q] >> (4 * i)) & 15u) * (q < 2 ? s0 : s1);
+  }
+};
+
+template <>
+struct WFmt<MOE_W_BF16> {
+  static constexpr int EPC = 8;
+  static constexpr int SCALE_BYTES_PER_CHUNK = 0;
+  __device__ __forceinline__ static void decode(uint4 d, const uint8_t*, int, float,
+                                                float (&w)[EPC]) {
+    uint32_t words[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      w[2 * q] = __uint_as_float(words[q] << 16);
+      w[2 * q + 1] = __uint_as_float(words[q] & 0xFFFF0000u);
+    }
+  }
+};
+
+// Bytes of one stored weight row of K input elements (codes) and of its scales.
+__host__ __device__ inline size_t row_code_bytes(int fmt, int K) {
+  return fmt == MOE_W_BF16 ? (size_t)K * 2 : (size_t)K / 2;
+}
+__host__ __device__ inline size_t row_scale_bytes(int fmt, int K) {
+  return fmt == MOE_W_INT4_G32 ? (size_t)K / 32 * 2 : fmt == MOE_W_NVFP4 ? (size_t)K / 16 : 0;
+}
+
+// ----------------------------------------------------------- work decomposition
+// Token chunk processed by one generic expert CTA.
+constexpr int kTokChunk = 4;
+// Work item: expert index (E = shared) in the high half, token chunk in the low half.
+__host__ __device__ inline int pack_item(int e, int chunk) { return (e << 16) | chunk; }
+
+// Device view of the expert weights (one format).
+struct ExpertWeights {
+  const uint8_t* gu_codes;   // [n, 2I, row_code_bytes(H)]
+  const uint8_t* gu_scales;  // [n, 2I, row_scale_bytes(H)]
+  const float* gu_tscale;    // [n] (NVFP4)
+  const uint8_t* d_codes;    // [n, H, row_code_bytes(I)]
+  const uint8_t* d_scales;
+  const float* d_tscale;
+};
+
+}  // namespace moe

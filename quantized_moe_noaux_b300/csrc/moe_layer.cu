@@ -1,0 +1,471 @@
+// C ABI of the MoE layer (include/moe_layer.h): layer creation (weight upload and
+// workspace sizing), the forward pipeline, routing read-back and status reporting.
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "kernels.h"
+
+using namespace moe;
+
+struct moe_layer {
+  moe_config cfg{};
+  int device = 0;
+  bool shared_inline = false;   // shared expert stored at index E of the routed arrays
+  int path = MOE_PATH_AUTO;
+  // weights (device)
+  void* router_w = nullptr;
+  float* bias = nullptr;
+  ExpertWeights w{};     // routed experts (+ shared when inline)
+  ExpertWeights ws{};    // separately stored shared expert
+  // workspace (device)
+  float* logits = nullptr;
+  int32_t* ids = nullptr;
+  float* weights = nullptr;
+  int32_t* counts = nullptr;
+  int32_t* offsets = nullptr;
+  int32_t* entries = nullptr;
+  int32_t* items = nullptr;
+  int32_t* meta = nullptr;
+  float* h = nullptr;
+  float* out_acc = nullptr;
+  float* xq = nullptr;
+  unsigned int* amax = nullptr;
+  int* status = nullptr;
+  void* x_stage = nullptr;
+  void* out_stage = nullptr;
+  std::vector<void*> allocs;
+  // measurement
+  std::vector<cudaEvent_t> events;   // kStageEvents per recorded forward
+  int timing_cap = 0;
+  int timing_used = 0;
+  int64_t launches = 0;
+};
+
+static constexpr int kStageEvents = 7;
+
+namespace {
+
+size_t act_bytes(int dt) { return dt == MOE_DT_F32 ? 4 : 2; }
+
+int max_items_for(const moe_config& c, int T) {
+  const long tk = (long)T * c.top_k;
+  long n = tk / kTokChunk + (tk < c.n_experts ? tk : c.n_experts) + (T + kTokChunk - 1) / kTokChunk + 1;
+  return (int)n;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+moe_status validate_config(const moe_config* c) {
+  if (c->hidden <= 0 || c->inter <= 0 || c->n_experts <= 0 || c->top_k <= 0 || c->n_group <= 0 ||
+      c->topk_group <= 0 || c->max_tokens <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (!(c->routed_scaling_factor > 0.f)) return MOE_ERR_INVALID_ARG;
+  if (c->weight_format != MOE_W_INT4_G32 && c->weight_format != MOE_W_NVFP4) return MOE_ERR_UNSUPPORTED;
+  if (c->shared_format != MOE_W_INT4_G32 && c->shared_format != MOE_W_NVFP4 &&
+      c->shared_format != MOE_W_BF16)
+    return MOE_ERR_UNSUPPORTED;
+  if (c->act_dtype != MOE_DT_F32 && c->act_dtype != MOE_DT_BF16) return MOE_ERR_UNSUPPORTED;
+  if (c->router_dtype != MOE_DT_F32 && c->router_dtype != MOE_DT_BF16) return MOE_ERR_UNSUPPORTED;
+  if (c->hidden % 256 || c->inter % 64) return MOE_ERR_UNSUPPORTED;
+  if ((size_t)kTokChunk * c->hidden * 4 > (size_t)kMaxDynSmem) return MOE_ERR_UNSUPPORTED;
+  if (c->n_experts > 1024 || c->n_experts % c->n_group || c->n_group > 32) return MOE_ERR_UNSUPPORTED;
+  const int G = c->n_experts / c->n_group;
+  if (G < 2 || c->topk_group > c->n_group || c->top_k > c->topk_group * G || c->top_k > 32)
+    return MOE_ERR_UNSUPPORTED;
+  // work items index grid.y (<= 65535) and carry a 16-bit token-chunk field
+  if (c->max_tokens > 16384 || max_items_for(*c, c->max_tokens) > 65535) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status dev_alloc(moe_layer* L, void** p, size_t bytes) {
+  *p = nullptr;
+  if (bytes == 0) return MOE_OK;
+  if (cudaMalloc(p, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    *p = nullptr;
+    return MOE_ERR_OOM;
+  }
+  L->allocs.push_back(*p);
+  return MOE_OK;
+}
+
+template <typename T>
+moe_status dev_alloc_t(moe_layer* L, T** p, size_t bytes) {
+  void* v = nullptr;
+  moe_status s = dev_alloc(L, &v, bytes);
+  *p = static_cast<T*>(v);
+  return s;
+}
+
+void free_all(moe_layer* L) {
+  for (void* p : L->allocs) cudaFree(p);
+  L->allocs.clear();
+}
+
+// Upload one expert matrix family (codes, scales, tensor scales) of n experts into slots
+// [first, first + n) of a store holding `cap` experts.
+moe_status upload_family(const void* codes, const void* scales, const float* tscale, int fmt,
+                         int rows, int K, int first, int n, uint8_t* dcodes, uint8_t* dscales,
+                         float* dtscale, cudaStream_t s) {
+  if (!codes) return MOE_ERR_INVALID_ARG;
+  const size_t cb = (size_t)rows * row_code_bytes(fmt, K), sb = (size_t)rows * row_scale_bytes(fmt, K);
+  if (cudaMemcpyAsync(dcodes + first * cb, codes, n * cb, cudaMemcpyDefault, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (sb) {
+    if (!scales) return MOE_ERR_INVALID_ARG;
+    if (cudaMemcpyAsync(dscales + first * sb, scales, n * sb, cudaMemcpyDefault, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  if (fmt == MOE_W_NVFP4) {
+    if (!tscale) return MOE_ERR_INVALID_ARG;
+    if (cudaMemcpyAsync(dtscale + first, tscale, n * sizeof(float), cudaMemcpyDefault, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status alloc_family(moe_layer* L, ExpertWeights& w, int fmt, int n, int H, int I) {
+  moe_status st;
+  const size_t gcb = (size_t)2 * I * row_code_bytes(fmt, H), gsb = (size_t)2 * I * row_scale_bytes(fmt, H);
+  const size_t dcb = (size_t)H * row_code_bytes(fmt, I), dsb = (size_t)H * row_scale_bytes(fmt, I);
+  uint8_t *gc, *gs, *dc, *ds;
+  float *gt = nullptr, *dt = nullptr;
+  if ((st = dev_alloc_t(L, &gc, n * gcb)) || (st = dev_alloc_t(L, &gs, n * gsb)) ||
+      (st = dev_alloc_t(L, &dc, n * dcb)) || (st = dev_alloc_t(L, &ds, n * dsb)))
+    return st;
+  if (fmt == MOE_W_NVFP4 &&
+      ((st = dev_alloc_t(L, &gt, n * sizeof(float))) || (st = dev_alloc_t(L, &dt, n * sizeof(float)))))
+    return st;
+  w = ExpertWeights{gc, gs, gt, dc, ds, dt};
+  return MOE_OK;
+}
+
+moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt, cudaStream_t s) {
+  moe_status st;
+  const int H = c->hidden, I = c->inter, E = c->n_experts, k = c->top_k, Tm = c->max_tokens;
+  if (!wt->router_w || !wt->bias || !wt->gu_codes || !wt->d_codes || !wt->sh_gu || !wt->sh_d)
+    return MOE_ERR_INVALID_ARG;
+  if (expert_kernels_init() != cudaSuccess) return MOE_ERR_CUDA;
+  L->shared_inline = c->shared_format == c->weight_format;
+  const int n_store = E + (L->shared_inline ? 1 : 0);
+
+  const size_t rw_bytes = (size_t)E * H * (c->router_dtype == MOE_DT_F32 ? 4 : 2);
+  if ((st = dev_alloc(L, &L->router_w, rw_bytes)) || (st = dev_alloc_t(L, &L->bias, E * sizeof(float))))
+    return st;
+  if (cudaMemcpyAsync(L->router_w, wt->router_w, rw_bytes, cudaMemcpyDefault, s) ||
+      cudaMemcpyAsync(L->bias, wt->bias, E * sizeof(float), cudaMemcpyDefault, s))
+    return MOE_ERR_CUDA;
+
+  if ((st = alloc_family(L, L->w, c->weight_format, n_store, H, I))) return st;
+  ExpertWeights& w = L->w;
+  if ((st = upload_family(wt->gu_codes, wt->gu_scales, wt->gu_tscale, c->weight_format, 2 * I, H, 0, E,
+                          const_cast<uint8_t*>(w.gu_codes), const_cast<uint8_t*>(w.gu_scales),
+                          const_cast<float*>(w.gu_tscale), s)) ||
+      (st = upload_family(wt->d_codes, wt->d_scales, wt->d_tscale, c->weight_format, H, I, 0, E,
+                          const_cast<uint8_t*>(w.d_codes), const_cast<uint8_t*>(w.d_scales),
+                          const_cast<float*>(w.d_tscale), s)))
+    return st;
+  ExpertWeights* sw = &L->w;
+  int slot = E;
+  if (!L->shared_inline) {
+    if ((st = alloc_family(L, L->ws, c->shared_format, 1, H, I))) return st;
+    sw = &L->ws;
+    slot = 0;
+  }
+  if ((st = upload_family(wt->sh_gu, wt->sh_gu_scales, wt->sh_gu_tscale, c->shared_format, 2 * I, H, slot,
+                          1, const_cast<uint8_t*>(sw->gu_codes), const_cast<uint8_t*>(sw->gu_scales),
+                          const_cast<float*>(sw->gu_tscale), s)) ||
+      (st = upload_family(wt->sh_d, wt->sh_d_scales, wt->sh_d_tscale, c->shared_format, H, I, slot, 1,
+                          const_cast<uint8_t*>(sw->d_codes), const_cast<uint8_t*>(sw->d_scales),
+                          const_cast<float*>(sw->d_tscale), s)))
+    return st;
+
+  const size_t ab = act_bytes(c->act_dtype);
+  if ((st = dev_alloc_t(L, &L->logits, (size_t)Tm * E * 4)) ||
+      (st = dev_alloc_t(L, &L->ids, (size_t)Tm * k * 4)) ||
+      (st = dev_alloc_t(L, &L->weights, (size_t)Tm * k * 4)) ||
+      (st = dev_alloc_t(L, &L->counts, (size_t)(E + 1) * 4)) ||
+      (st = dev_alloc_t(L, &L->offsets, (size_t)(E + 2) * 4)) ||
+      (st = dev_alloc_t(L, &L->entries, (size_t)Tm * k * 4)) ||
+      (st = dev_alloc_t(L, &L->items, (size_t)max_items_for(*c, Tm) * 4)) ||
+      (st = dev_alloc_t(L, &L->meta, 16 * 4)) ||
+      (st = dev_alloc_t(L, &L->h, (size_t)Tm * (k + 1) * I * 4)) ||
+      (st = dev_alloc_t(L, &L->out_acc, (size_t)Tm * H * 4)) ||
+      (st = dev_alloc_t(L, &L->amax, 4 * sizeof(unsigned int))) ||
+      (st = dev_alloc_t(L, &L->status, sizeof(int))) ||
+      (st = dev_alloc(L, &L->x_stage, (size_t)Tm * H * ab)) ||
+      (st = dev_alloc(L, &L->out_stage, (size_t)Tm * H * ab)))
+    return st;
+  if (c->weight_format == MOE_W_NVFP4 && (st = dev_alloc_t(L, &L->xq, (size_t)Tm * H * 4))) return st;
+  if (cudaMemsetAsync(L->status, 0, sizeof(int), s) || cudaMemsetAsync(L->meta, 0, 16 * 4, s))
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+#define MOE_CK(call)                       \
+  do {                                     \
+    if ((call) != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+// Kernel launch: counted, error-checked.
+#define MOE_LAUNCH(call)   \
+  do {                     \
+    ++L->launches;         \
+    MOE_CK(call);          \
+  } while (0)
+
+struct StageMarks {
+  cudaEvent_t* ev = nullptr;
+  cudaStream_t s;
+  // External records become event nodes when the stream is being captured into a graph.
+  cudaError_t mark(int i) {
+    return ev ? cudaEventRecordWithFlags(ev[i], s, cudaEventRecordExternal) : cudaSuccess;
+  }
+};
+
+void release_events(moe_layer* L) {
+  for (cudaEvent_t e : L->events) cudaEventDestroy(e);
+  L->events.clear();
+  L->timing_cap = L->timing_used = 0;
+}
+
+moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStream_t s) {
+  const moe_config& c = L->cfg;
+  const int H = c.hidden, I = c.inter, E = c.n_experts, k = c.top_k;
+  const bool nvfp4 = c.weight_format == MOE_W_NVFP4;
+  StageMarks m;
+  m.s = s;
+  if (L->timing_used < L->timing_cap) m.ev = &L->events[(size_t)kStageEvents * L->timing_used++];
+  MOE_CK(m.mark(0));
+  MOE_CK(cudaMemsetAsync(L->counts, 0, (E + 1) * sizeof(int32_t), s));
+  MOE_CK(cudaMemsetAsync(L->amax, 0, 4 * sizeof(unsigned int), s));
+  MOE_CK(cudaMemsetAsync(L->out_acc, 0, (size_t)T * H * sizeof(float), s));
+  MOE_LAUNCH(launch_router_logits(x, c.act_dtype, L->router_w, c.router_dtype, L->logits, T, E, H, s));
+  MOE_LAUNCH(launch_select(L->logits, L->bias, T, E, c.n_group, c.topk_group, k, c.routed_scaling_factor,
+                           L->ids, L->weights, L->counts, L->status, s));
+  MOE_LAUNCH(launch_group(L->ids, L->counts, T, k, E, L->shared_inline, L->offsets, L->entries,
+                          L->items, L->meta, s));
+  MOE_CK(m.mark(1));
+  const void* x_in = x;
+  int x_dt = c.act_dtype;
+  if (nvfp4) {
+    MOE_LAUNCH(launch_amax(x, c.act_dtype, (size_t)T * H, L->amax, s));
+    MOE_LAUNCH(launch_nvfp4_quant(x, c.act_dtype, L->xq, (size_t)T * H, L->amax, s));
+    x_in = L->xq;
+    x_dt = MOE_DT_F32;
+  }
+  MOE_CK(m.mark(2));
+  ExpertGemvArgs a{};
+  a.w = L->w;
+  a.fmt = c.weight_format;
+  a.H = H;
+  a.I = I;
+  a.E = E;
+  a.top_k = k;
+  a.T = T;
+  a.x = x_in;
+  a.x_dtype = x_dt;
+  a.offsets = L->offsets;
+  a.entries = L->entries;
+  a.items = L->items;
+  a.meta = L->meta;
+  a.expert_base = E;
+  a.h = L->h;
+  a.h_amax = nvfp4 ? L->amax + 1 : nullptr;
+  a.weights = L->weights;
+  a.out_acc = L->out_acc;
+  a.max_items = max_items_for(c, T);
+  ExpertGemvArgs sh = a;
+  if (!L->shared_inline) {
+    sh.w = L->ws;
+    sh.fmt = c.shared_format;
+    sh.items = nullptr;
+    sh.meta = nullptr;
+    sh.expert_base = 0;
+    sh.h_amax = nullptr;
+    sh.max_items = (T + kTokChunk - 1) / kTokChunk;
+    if (c.shared_format != MOE_W_NVFP4) {
+      sh.x = x;
+      sh.x_dtype = c.act_dtype;
+    }
+  }
+  MOE_LAUNCH(launch_expert_up(a, s));
+  if (!L->shared_inline) MOE_LAUNCH(launch_expert_up(sh, s));
+  MOE_CK(m.mark(3));
+  if (nvfp4) MOE_LAUNCH(launch_nvfp4_quant(L->h, MOE_DT_F32, L->h, (size_t)T * k * I, L->amax + 1, s));
+  MOE_CK(m.mark(4));
+  MOE_LAUNCH(launch_expert_down(a, s));
+  if (!L->shared_inline) MOE_LAUNCH(launch_expert_down(sh, s));
+  MOE_CK(m.mark(5));
+  MOE_LAUNCH(launch_finalize(L->out_acc, out, c.act_dtype, (size_t)T * H, s));
+  MOE_CK(m.mark(6));
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_layer_create(const moe_config* cfg, const moe_weights* w, void* stream,
+                            moe_layer** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || !w) return MOE_ERR_INVALID_ARG;
+  moe_status st = validate_config(cfg);
+  if (st) return st;
+  moe_layer* L = new (std::nothrow) moe_layer();
+  if (!L) return MOE_ERR_OOM;
+  L->cfg = *cfg;
+  if (cudaGetDevice(&L->device) != cudaSuccess) {
+    delete L;
+    return MOE_ERR_CUDA;
+  }
+  st = create_impl(L, cfg, w, static_cast<cudaStream_t>(stream));
+  if (st) {
+    cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    cudaGetLastError();
+    free_all(L);
+    delete L;
+    return st;
+  }
+  *out = L;
+  return MOE_OK;
+}
+
+moe_status moe_layer_forward(moe_layer* L, const void* x, int32_t T, void* out, void* stream) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > L->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !out || !aligned16(x) || !aligned16(out) || x == out) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(L->device);
+  return forward_impl(L, x, T, out, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_layer_forward_host(moe_layer* L, const void* x_host, int32_t T, void* out_host,
+                                  void* stream) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > L->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x_host || !out_host) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(L->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)T * L->cfg.hidden * act_bytes(L->cfg.act_dtype);
+  if (cudaMemcpyAsync(L->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  moe_status st = forward_impl(L, L->x_stage, T, L->out_stage, s);
+  if (st) return st;
+  if (cudaMemcpyAsync(out_host, L->out_stage, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_layer_get_routing(moe_layer* L, int32_t T, int32_t* ids, float* weights,
+                                 int32_t* offsets, int32_t* entries, void* stream) {
+  if (!L || T < 0 || T > L->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(L->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t tk = (size_t)T * L->cfg.top_k;
+  if ((ids && cudaMemcpyAsync(ids, L->ids, tk * 4, cudaMemcpyDeviceToHost, s)) ||
+      (weights && cudaMemcpyAsync(weights, L->weights, tk * 4, cudaMemcpyDeviceToHost, s)) ||
+      (offsets && cudaMemcpyAsync(offsets, L->offsets, (L->cfg.n_experts + 1) * 4, cudaMemcpyDeviceToHost, s)) ||
+      (entries && cudaMemcpyAsync(entries, L->entries, tk * 4, cudaMemcpyDeviceToHost, s)))
+    return MOE_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_layer_set_path(moe_layer* L, int32_t path) {
+  if (!L || path < MOE_PATH_AUTO || path > MOE_PATH_GROUPED) return MOE_ERR_INVALID_ARG;
+  L->path = path;
+  return MOE_OK;
+}
+
+moe_status moe_layer_status(moe_layer* L) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(L->device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  int code = 0;
+  if (cudaMemcpy(&code, L->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  return static_cast<moe_status>(code);
+}
+
+moe_status moe_layer_enable_timing(moe_layer* L, int32_t enable) {
+  if (!L || enable < 0) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(L->device);
+  release_events(L);
+  for (long i = 0; i < (long)enable * kStageEvents; ++i) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      release_events(L);
+      return MOE_ERR_CUDA;
+    }
+    L->events.push_back(e);
+  }
+  L->timing_cap = enable;
+  return MOE_OK;
+}
+
+moe_status moe_layer_stage_times(moe_layer* L, float* ms, int32_t* n_forwards) {
+  if (!L || !ms) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(L->device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  for (int j = 0; j < kStageEvents - 1; ++j) ms[j] = 0.f;
+  for (int i = 0; i < L->timing_used; ++i) {
+    cudaEvent_t* ev = &L->events[(size_t)kStageEvents * i];
+    for (int j = 0; j < kStageEvents - 1; ++j) {
+      float t = 0.f;
+      if (cudaEventElapsedTime(&t, ev[j], ev[j + 1]) != cudaSuccess) return MOE_ERR_CUDA;
+      ms[j] += t;
+    }
+  }
+  if (n_forwards) *n_forwards = L->timing_used;
+  L->timing_used = 0;
+  return MOE_OK;
+}
+
+moe_status moe_layer_launch_count(moe_layer* L, int64_t* count) {
+  if (!L || !count) return MOE_ERR_INVALID_ARG;
+  *count = L->launches;
+  return MOE_OK;
+}
+
+void moe_layer_destroy(moe_layer* L) {
+  if (!L) return;
+  {
+    DeviceGuard g(L->device);
+    cudaDeviceSynchronize();
+    release_events(L);
+    free_all(L);
+  }
+  delete L;
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_OOM: return "MOE_ERR_OOM";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+}  // extern "C"

@@ -6,6 +6,8 @@ from .layer import (  # noqa: F401
     LAYERS,
     WORKLOADS,
     make_layer,
+    make_router,
+    with_bias_of,
     make_x,
     f32_to_bf16_bits,
     bf16_bits_to_f32,

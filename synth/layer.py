@@ -41,7 +41,7 @@ from dataclasses import dataclass, replace
 import numpy as np
 
 __all__ = [
-    "LayerSpec", "Workload", "LAYERS", "WORKLOADS", "make_layer", "make_x",
+    "LayerSpec", "Workload", "LAYERS", "WORKLOADS", "make_layer", "make_router", "make_x",
     "f32_to_bf16_bits", "bf16_bits_to_f32", "quantize_int4_g32", "quantize_nvfp4_weight",
 ]
 
@@ -263,6 +263,18 @@ def _default_workers(n_items: int, hidden: int) -> int:
     return max(1, min(os.cpu_count() or 1, 64, n_items))
 
 
+def make_router(spec: LayerSpec):
+    """The router matrix and the selection bias of ``spec`` (the same arrays
+    ``make_layer`` returns; both come from streams independent of the experts)."""
+    H, E = spec.hidden, spec.n_experts
+    rng_r = np.random.default_rng(np.random.SeedSequence([spec.seed, 0]))
+    wr = rng_r.standard_normal((E, H), dtype=np.float32) * np.float32(1.0 / np.sqrt(H))
+    wr = f32_to_bf16_bits(wr) if spec.router_dtype == "bf16" else wr
+    rng_b = np.random.default_rng(np.random.SeedSequence([spec.seed, 1]))
+    bias = rng_b.standard_normal(E, dtype=np.float32) * np.float32(spec.bias_std)
+    return wr, bias
+
+
 @functools.lru_cache(maxsize=2)
 def make_layer(spec: LayerSpec, workers: int | None = None) -> dict:
     """Draw one layer. Returns read-only numpy arrays:
@@ -277,11 +289,7 @@ def make_layer(spec: LayerSpec, workers: int | None = None) -> dict:
     H, I, E = spec.hidden, spec.inter, spec.n_experts
     assert H % 32 == 0 and I % 32 == 0 and E % spec.n_group == 0
     out: dict = {}
-    rng_r = np.random.default_rng(np.random.SeedSequence([spec.seed, 0]))
-    wr = rng_r.standard_normal((E, H), dtype=np.float32) * np.float32(1.0 / np.sqrt(H))
-    out["router_w"] = f32_to_bf16_bits(wr) if spec.router_dtype == "bf16" else wr
-    rng_b = np.random.default_rng(np.random.SeedSequence([spec.seed, 1]))
-    out["bias"] = rng_b.standard_normal(E, dtype=np.float32) * np.float32(spec.bias_std)
+    out["router_w"], out["bias"] = make_router(spec)
 
     out.update(_alloc_expert_arrays(E, H, I, spec.weight_format, ""))
     out.update(_alloc_expert_arrays(1, H, I, spec.shared_format, "sh_"))
@@ -303,6 +311,15 @@ def make_layer(spec: LayerSpec, workers: int | None = None) -> dict:
                 _store(job[1], res)
     for val in out.values():
         val.flags.writeable = False
+    return out
+
+
+def with_bias_of(arrays: dict, spec: LayerSpec) -> dict:
+    """``arrays`` (a layer drawn for a spec that differs from ``spec`` only in bias_std)
+    with the bias of ``spec``: equal to ``make_layer(spec)`` without redrawing experts."""
+    out = dict(arrays)
+    out["bias"] = make_router(spec)[1]
+    out["bias"].flags.writeable = False
     return out
 
 

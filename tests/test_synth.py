@@ -78,3 +78,14 @@ def test_workload_table():
     assert WORKLOADS["glm52_decode_t32"].layer.bias_std == 0.0
     nv = WORKLOADS["glm52_nvfp4_t4096"].layer
     assert (nv.weight_format, nv.router_dtype, nv.shared_format) == ("nvfp4", "bf16", "bf16")
+
+
+def test_bias_swap_equals_fresh_draw():
+    from dataclasses import replace
+    from synth import with_bias_of
+    base = LAYERS["tiny"]
+    other = replace(base, name="tiny_bias0.5", bias_std=0.5)
+    a = with_bias_of(make_layer(base), other)
+    b = make_layer(other)
+    for k in b:
+        assert np.array_equal(a[k], b[k]), k
