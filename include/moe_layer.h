@@ -174,6 +174,33 @@ moe_status moe_layer_stage_times(moe_layer* layer, float* ms, int32_t* n_forward
  * captured into a CUDA graph counts once at capture). */
 moe_status moe_layer_launch_count(moe_layer* layer, int64_t* count);
 
+/*
+ * Routing without any allocation. The pages have no counterpart to this entry point: it
+ * exists for callers that cannot call cudaMalloc when they need routing (code running
+ * while a stream is captured into a CUDA graph, where allocation is not capturable; hosts
+ * whose framework owns the device memory budget; runtimes that forbid allocation after
+ * start-up). It computes the same routing as moe_layer_forward + moe_layer_get_routing,
+ * with the same kernels, from caller-owned DEVICE buffers:
+ *   x [T, H] (act_dtype), router_w [E, H] (router_dtype), bias [E] fp32
+ *   -> ids [T, top_k] int32, weights [T, top_k] fp32, offsets [E + 1] int32,
+ *      entries [T * top_k] int32 (layouts as in moe_layer_get_routing).
+ * The kernels' scratch (logits, histogram, work list, status word) lives in one
+ * file-scope __device__ array of about 1.04 MiB that every device loading the library
+ * holds until the process exits. Limits: T * E <= 262144 and
+ * T * top_k / 4 + min(T * top_k, E) + 1 <= 8192; larger problems return
+ * MOE_ERR_UNSUPPORTED before any work is enqueued. Other checks as moe_layer_create.
+ * The first call on a device looks up the array's device address (once per device, with
+ * that device current); make that first call before any stream capture. Every call shares
+ * the one array: calls whose work overlaps on the GPU (different streams, or concurrent
+ * host threads) race on it and must be serialised by the caller. Asynchronous on
+ * `stream`; no host synchronisation.
+ */
+moe_status moe_route_noalloc(const void* x, int32_t act_dtype, int32_t T, int32_t H,
+                             const void* router_w, int32_t router_dtype, const float* bias,
+                             int32_t E, int32_t n_group, int32_t topk_group, int32_t top_k,
+                             float routed_scaling_factor, int32_t* ids, float* weights,
+                             int32_t* offsets, int32_t* entries, void* stream);
+
 /* Free everything the layer owns. NULL is a no-op. */
 void moe_layer_destroy(moe_layer* layer);
 

@@ -65,6 +65,8 @@ SYMBOLS = {
     "moe_layer_enable_timing": (_I, [_P, _I]),
     "moe_layer_stage_times": (_I, [_P, _P, _P]),
     "moe_layer_launch_count": (_I, [_P, _P]),
+    "moe_route_noalloc": (_I, [_P, _I, _I, _I, _P, _I, _P, _I, _I, _I, _I, ctypes.c_float,
+                               _P, _P, _P, _P, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
 }
 

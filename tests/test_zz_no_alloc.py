@@ -1,0 +1,67 @@
+"""moe_route_noalloc: routing for callers that cannot allocate device memory.
+
+The entry point keeps its kernels' scratch in a fixed file-scope device array instead of
+memory from cudaMalloc. Its results must equal the routing the layer entry point
+(moe_layer_forward + moe_layer_get_routing) computes for the same inputs, on two calls
+in a row (the second call reuses the array the first one left behind). This file is
+collected last so a failure here stops a -x run only after every other test ran.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+from synth import LAYERS, make_layer, make_x
+from tests.gpu_util import empty_out, x_to_device
+
+_DT = {"f32": 0, "bf16": 1}
+
+
+def _noalloc(lib, spec, xd, wr, bias, T, stream):
+    k, E = spec.top_k, spec.n_experts
+    ids = torch.full((T, k), -1, dtype=torch.int32, device="cuda")
+    w = torch.full((T, k), -1.0, dtype=torch.float32, device="cuda")
+    off = torch.full((E + 1,), -1, dtype=torch.int32, device="cuda")
+    ent = torch.full((T * k,), -1, dtype=torch.int32, device="cuda")
+    rc = lib.moe_route_noalloc(xd.data_ptr(), _DT[spec.act_dtype], T, spec.hidden, wr.data_ptr(),
+                               _DT[spec.router_dtype], bias.data_ptr(), E, spec.n_group,
+                               spec.topk_group, k, spec.rsf, ids.data_ptr(), w.data_ptr(),
+                               off.data_ptr(), ent.data_ptr(), stream)
+    return rc, ids, w, off, ent
+
+
+def test_noalloc_routing_matches_layer_entry_point():
+    import quantized_moe_noaux_b300 as moe
+    lib = moe.lib
+    spec = LAYERS["tiny"]
+    arrays = make_layer(spec)
+    layer = moe.MoeLayer.from_spec(spec, arrays, max_tokens=64)
+    wr = torch.from_numpy(np.array(arrays["router_w"])).cuda()
+    bias = torch.from_numpy(np.array(arrays["bias"])).cuda()
+    stream = torch.cuda.current_stream().cuda_stream
+    for T, step in [(37, 11), (64, 12)]:          # two calls in a row
+        x = make_x(spec, T, step)
+        xd = x_to_device(x, spec.act_dtype)
+        out = empty_out(T, spec.hidden, spec.act_dtype)
+        layer.forward(xd, out)
+        ref = layer.routing(T)
+        rc, ids, w, off, ent = _noalloc(lib, spec, xd, wr, bias, T, stream)
+        assert rc == 0, moe.STATUS.get(rc, rc)
+        torch.cuda.synchronize()
+        assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+        assert np.allclose(w.cpu().numpy(), ref["weights"], rtol=1e-5, atol=0)
+        assert np.array_equal(off.cpu().numpy(), ref["offsets"])
+        assert np.array_equal(ent.cpu().numpy(), ref["entries"])
+    layer.close()
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    import quantized_moe_noaux_b300 as moe
+    spec = LAYERS["glm52"]
+    # T * E = 2048 * 256 > 262144 logits: refused before any work is enqueued
+    rc = moe.lib.moe_route_noalloc(1 << 20, 1, 2048, spec.hidden, 1 << 20, 0, 1 << 20,
+                                   spec.n_experts, spec.n_group, spec.topk_group, spec.top_k,
+                                   spec.rsf, 1 << 20, 1 << 20, 1 << 20, 1 << 20, None)
+    assert rc == 2   # MOE_ERR_UNSUPPORTED
