@@ -70,7 +70,9 @@ SYMBOLS = {
     "moe_status_string": (ctypes.c_char_p, [_I]),
 }
 
-STAGES = ("routing", "act_quant", "gate_up_swiglu", "h_quant", "down_combine", "output")
+# Stage slots of moe_layer_stage_times. The fused decode kernel (routing + gate/up + down +
+# combine in one launch) is recorded in the third slot.
+STAGES = ("routing", "act_quant", "gate_up_or_fused", "h_quant", "down_combine", "output")
 
 
 def _load():

@@ -1,0 +1,899 @@
+// Fused decode-path kernel of the MoE layer (T <= 8 tokens per call), plus the weight repack
+// it reads.
+//
+// One persistent cooperative grid (one CTA per SM) runs the whole layer forward of a decode
+// step: router logits, noaux_tc selection and batch-union grouping (by the last CTA to finish
+// its router rows), the SwiGLU gate/up projection of the shared and the selected experts, and
+// the down projection fused with the weighted combine ("Show HN: Menjalankan GLM 5.2 di
+// komputer lambat", section "Fitur utama yang diimplementasikan": DeepSeek-V3-style router
+// with noaux_tc, routed_scaling_factor and a shared expert; packed int4 with dequant-on-use;
+// batch-union MoE). Every selected expert's weights are streamed from HBM exactly once.
+//
+// Weights are repacked at layer creation into 16-row tiles in the register-fragment order of
+// the m16n8k16 fp16 MMA. One 32-bit word holds the 8 int4 codes a lane needs for one MMA;
+// a shift and four LOP3s turn it into the four fp16 A registers: (code + 8) is placed in the
+// mantissa of 1024.0 (rows 0-7: value 1032 + c) or at mantissa bit 4 (rows 8-15: value
+// 1152 + 16c). The MMA accumulates in fp32; the per-row bias (1032 or 1152 times the group's
+// activation sum) is removed and the fp16 group scale applied once per 32-element group (or
+// once per 8 groups when the single token's groups occupy the MMA's 8 columns).
+//
+// Work per CTA, in order, each item a 16-row x 2048-column panel (18 KB) brought in by a
+// producer warp with TMA bulk copies into a 4-slot ring:
+//   A  shared-expert gate/up tiles           (no dependency)
+//   C1 shared-expert down tiles              (waits until every shared gate/up tile is done)
+//   B  selected experts' gate/up tiles       (waits for the routing flag)
+//   C2 selected experts' down tiles          (waits until that expert's gate/up tiles are done)
+// Down tiles add w * y into an fp32 accumulator with atomics; after a grid-wide count every
+// CTA converts its slice to the output type. Gate/up completion is published per expert with
+// one release-add per run of tiles. All inter-CTA waits are bounded; on time-out the kernel
+// records MOE_ERR_TIMEOUT, drains its own copies in flight and returns.
+#include "kernels.h"
+#include "ptx.cuh"
+#include "route_dev.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kDecThreads = 288;      // 8 consumer warps + 1 producer warp
+constexpr int kConsumers = 256;
+constexpr int kSlots = 4;
+constexpr int kPanelK = 2048;          // columns per item
+constexpr int kCodeBytes = 16384;      // 16 rows x 2048 int4
+constexpr int kScaleBytes = 2048;      // 16 rows x 64 groups fp16
+constexpr int kItemBytes = kCodeBytes + kScaleBytes;
+constexpr int kMaxH = 6144;
+constexpr int kMaxI = 2048;
+constexpr int kMaxE = 256;
+constexpr int kMaxActive = 64;         // T * top_k <= 64 on this path
+constexpr int kMaxPairs = kMaxActive + 8;
+constexpr uint32_t kMbarSpin = 1u << 22;
+
+struct Smem {
+  uint8_t slots[kSlots][kItemBytes];
+  uint2 xpanel[kMaxH / 16 * 32];       // B fragments of x: 8 bytes per lane per MMA
+  union {
+    uint2 hpanel[kMaxI / 16 * 32];     // B fragments of h (down tiles)
+    struct {
+      float b[8][kMaxE];               // selection scratch (biased scores)
+      float s[8][kMaxE];               // selection scratch (sigmoid scores)
+    } sel;
+  } u;
+  float xsums[kMaxH / 32 * 8];         // per-group activation sums [group][column]
+  float hsums[kMaxI / 32 * 8];
+  float red[8][32][4];                 // cross-warp reduction
+  uint64_t full[kSlots];
+  uint64_t empty[kSlots];
+  uint64_t route_bar;
+  int sid[kMaxPairs];
+  int cnt[kMaxE];
+  int soff[kMaxE + 1];
+  int aslot[kMaxE];                    // expert -> active slot (selection CTA)
+  int active[kMaxE];
+  int meta_pair[kMaxActive][8];        // per active expert: h row of token n (-1: not routed)
+  float meta_w[kMaxActive][8];         // per active expert: combine weight of token n
+  int colpair[8];
+  float colw[8];
+  int n_active;
+  int flag;          // broadcast word
+  int abort;
+  int issued;
+  int consumed;
+};
+
+static_assert(sizeof(Smem) <= 227 * 1024, "decode kernel shared memory over the per-CTA limit");
+
+// ------------------------------------------------------------------ helpers
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float2 half2_to_float2(uint32_t u) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&u));
+}
+
+// One word of codes -> the four fp16 A registers of an m16n8k16 MMA (see file comment).
+__device__ __forceinline__ void decode_word(uint32_t w, uint32_t (&a)[4]) {
+  const uint32_t w2 = w >> 8;
+  a[0] = (w & 0x000F000Fu) ^ 0x64086408u;
+  a[1] = (w & 0x00F000F0u) ^ 0x64806480u;
+  a[2] = (w2 & 0x000F000Fu) ^ 0x64086408u;
+  a[3] = (w2 & 0x00F000F0u) ^ 0x64806480u;
+}
+
+// Bounded wait for *p >= target (one thread). Returns false on time-out.
+__device__ __forceinline__ bool wait_geq(const uint32_t* p, uint32_t target, uint32_t spin_max) {
+  for (uint32_t i = 0; i < spin_max; ++i) {
+    if (ptx::ld_acquire(p) >= target) return true;
+    __nanosleep(64);
+  }
+  return false;
+}
+
+struct Geo {
+  int T, H, I, E, k;
+  int NTu, Pu, NTd, Pd;   // tiles and panels per tile: up (gate/up) and down
+  int G, c;
+};
+
+// Item ranges of this CTA (balanced contiguous split of each segment over the grid).
+__device__ __forceinline__ void seg_range(int n, int G, int c, int& b, int& e) {
+  b = (int)(((long)n * c) / G);
+  e = (int)(((long)n * (c + 1)) / G);
+}
+
+// ----------------------------------------------------- consumer: B panels
+
+// Group sums of a B panel: per group j (MMAs 2j, 2j+1) and column n, the sum of the 32
+// fp16 values column n holds (exactly the values the MMA multiplies).
+template <int MODE>
+__device__ void panel_sums(const uint2* panel, float* sums, int ngroups, int ncols) {
+  for (int idx = threadIdx.x; idx < ngroups * 8; idx += kConsumers) {
+    const int j = idx >> 3, n = idx & 7;
+    float s = 0.f;
+    if ((MODE == 1 && n == 0) || (MODE == 0 && n < ncols)) {
+      const int gg = (MODE == 1) ? (j & 7) : n;   // lane group holding this column
+#pragma unroll
+      for (int mm = 0; mm < 2; ++mm)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const uint2 v = panel[(2 * j + mm) * 32 + gg * 4 + t];
+          const float2 f0 = half2_to_float2(v.x), f1 = half2_to_float2(v.y);
+          s += (f0.x + f0.y) + (f1.x + f1.y);
+        }
+    }
+    if (MODE == 1) {
+      if (n == 0) sums[j] = s;
+    } else {
+      sums[idx] = s;
+    }
+  }
+}
+
+template <int XDT>
+__device__ __forceinline__ uint32_t x_pair_half2(const void* x, size_t i) {
+  if constexpr (XDT == MOE_DT_F32) {
+    const float2 f = __ldg(reinterpret_cast<const float2*>(static_cast<const float*>(x) + i));
+    return pack_half2(f.x, f.y);
+  } else {
+    const uint32_t u = __ldg(reinterpret_cast<const unsigned int*>(static_cast<const unsigned short*>(x) + i));
+    return pack_half2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+  }
+}
+
+// x panel: MODE 1 (one token): column n of MMA m holds group (m/2) mod 8 only, so the 8
+// groups of a 256-column k-block land in 8 different accumulator columns. MODE 0: column n
+// holds token n (zero for n >= T).
+template <int MODE, int XDT>
+__device__ void build_x_panel(Smem& S, const void* x, const Geo& g) {
+  const int nm = g.H / 16;
+  for (int idx = threadIdx.x; idx < nm * 32; idx += kConsumers) {
+    const int m = idx >> 5, ln = idx & 31, gg = ln >> 2, t = ln & 3;
+    int tok = -1;
+    if (MODE == 1) {
+      if (gg == ((m >> 1) & 7)) tok = 0;
+    } else if (gg < g.T) {
+      tok = gg;
+    }
+    uint2 v = make_uint2(0u, 0u);
+    if (tok >= 0) {
+      const size_t base = (size_t)tok * g.H + 16 * m + 2 * t;
+      v.x = x_pair_half2<XDT>(x, base);
+      v.y = x_pair_half2<XDT>(x, base + 8);
+    }
+    S.xpanel[idx] = v;
+  }
+  ptx::bar_sync(1, kConsumers);
+  panel_sums<MODE>(S.xpanel, S.xsums, g.H / 32, g.T);
+}
+
+// h panel of the current expert (rows S.colpair), read through L2: the h rows were written
+// by other CTAs of this grid.
+template <int MODE>
+__device__ void build_h_panel(Smem& S, const __half* h16, const Geo& g) {
+  const int nm = g.I / 16;
+  for (int idx = threadIdx.x; idx < nm * 32; idx += kConsumers) {
+    const int m = idx >> 5, ln = idx & 31, gg = ln >> 2, t = ln & 3;
+    int row = -1;
+    if (MODE == 1) {
+      if (gg == ((m >> 1) & 7)) row = S.colpair[0];
+    } else {
+      row = S.colpair[gg];
+    }
+    uint2 v = make_uint2(0u, 0u);
+    if (row >= 0) {
+      const unsigned int* src = reinterpret_cast<const unsigned int*>(h16 + (size_t)row * g.I + 16 * m + 2 * t);
+      v.x = __ldcg(src);
+      v.y = __ldcg(src + 4);
+    }
+    S.u.hpanel[idx] = v;
+  }
+  ptx::bar_sync(1, kConsumers);
+  panel_sums<MODE>(S.u.hpanel, S.hsums, g.I / 32, 8);
+}
+
+// ------------------------------------------------------- consumer: compute
+
+// One item (16 rows x 2048 columns): warp `w` handles k-block w (256 columns = 16 MMAs).
+// m_base = global MMA index of the panel start (p * 128). kb = global k-block index.
+template <int MODE>
+__device__ __forceinline__ void compute_item(const uint2* panel, const float* sums, const uint8_t* slot,
+                                             int m_base, int kb, float (&acc)[4]) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int gq = lane >> 2, t = lane & 3;
+  const uint8_t* codes = slot + ((size_t)(4 * w) * 32 + lane) * 16;
+  const uint8_t* scl = slot + kCodeBytes + (w * 8 + gq) * 32;
+  const uint2* bp = panel + (size_t)(m_base + 16 * w) * 32 + lane;
+  if (MODE == 1) {
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      const uint4 q = *reinterpret_cast<const uint4*>(codes + cc * 32 * 16);
+      const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t a[4];
+        decode_word(words[i], a);
+        const uint2 b = bp[(4 * cc + i) * 32];
+        ptx::mma_16816(d, a, b.x, b.y, d);
+      }
+    }
+    const uint2 sraw = *reinterpret_cast<const uint2*>(scl + t * 8);
+    const float2 sg = half2_to_float2(sraw.x);   // s[g][j0], s[g][j0+1]
+    const float2 su = half2_to_float2(sraw.y);   // s[g+8][j0], s[g+8][j0+1]
+    const float2 X = *reinterpret_cast<const float2*>(sums + 8 * kb + 2 * t);
+    acc[0] = fmaf(sg.x, fmaf(-1032.f, X.x, d[0]), acc[0]);
+    acc[0] = fmaf(sg.y, fmaf(-1032.f, X.y, d[1]), acc[0]);
+    acc[1] = fmaf(su.x, fmaf(-1152.f, X.x, d[2]), acc[1]);
+    acc[1] = fmaf(su.y, fmaf(-1152.f, X.y, d[3]), acc[1]);
+  } else {
+    const uint4 s0 = *reinterpret_cast<const uint4*>(scl);
+    const uint4 s1 = *reinterpret_cast<const uint4*>(scl + 16);
+    const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      const uint4 q = *reinterpret_cast<const uint4*>(codes + cc * 32 * 16);
+      const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int gi = 0; gi < 2; ++gi) {
+        const int jl = 2 * cc + gi;   // group within the k-block
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          uint32_t a[4];
+          decode_word(words[2 * gi + i], a);
+          const uint2 b = bp[(4 * cc + 2 * gi + i) * 32];
+          ptx::mma_16816(d, a, b.x, b.y, d);
+        }
+        // scale words per (k-block, row g): [t'][s[g][2t'], s[g][2t'+1], s[g+8][2t'], s[g+8][2t'+1]]
+        const float2 sgp = half2_to_float2(sw[2 * (jl >> 1)]);
+        const float2 sup = half2_to_float2(sw[2 * (jl >> 1) + 1]);
+        const float sgate = (jl & 1) ? sgp.y : sgp.x;
+        const float sup1 = (jl & 1) ? sup.y : sup.x;
+        const float2 X = *reinterpret_cast<const float2*>(sums + (8 * kb + jl) * 8 + 2 * t);
+        acc[0] = fmaf(sgate, fmaf(-1032.f, X.x, d[0]), acc[0]);
+        acc[1] = fmaf(sgate, fmaf(-1032.f, X.y, d[1]), acc[1]);
+        acc[2] = fmaf(sup1, fmaf(-1152.f, X.x, d[2]), acc[2]);
+        acc[3] = fmaf(sup1, fmaf(-1152.f, X.y, d[3]), acc[3]);
+      }
+    }
+  }
+}
+
+// Cross-warp reduction of the tile accumulators into S.red (consumers, then named barrier).
+template <int MODE>
+__device__ __forceinline__ void stash_acc(Smem& S, float (&acc)[4]) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (MODE == 1) {
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
+      acc[1] += __shfl_xor_sync(0xffffffffu, acc[1], o);
+    }
+    if ((lane & 3) == 0) {
+      S.red[w][lane >> 2][0] = acc[0];
+      S.red[w][lane >> 2][1] = acc[1];
+    }
+  } else {
+    *reinterpret_cast<float4*>(&S.red[w][lane][0]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  }
+}
+
+// Value of MMA row r (0..15) for column n after the reduction (rows 8..15 carry a x16 unit).
+template <int MODE>
+__device__ __forceinline__ float reduced(const Smem& S, int r, int n) {
+  float v = 0.f;
+  if (MODE == 1) {
+#pragma unroll
+    for (int w = 0; w < 8; ++w) v += S.red[w][r & 7][r >> 3];
+  } else {
+    const int ln = (r & 7) * 4 + (n >> 1);
+    const int idx = (r >> 3) * 2 + (n & 1);
+#pragma unroll
+    for (int w = 0; w < 8; ++w) v += S.red[w][ln][idx];
+  }
+  return (r >= 8) ? v * 0.0625f : v;
+}
+
+}  // namespace
+
+struct DecodeArgs {
+  const void* x;
+  int T;
+  const void* router_w;
+  const float* bias;
+  int H, I, E, top_k, n_group, topk_group;
+  float rsf;
+  const uint8_t* up_store;     // [E+1][I/8 tiles][H/2048 panels][18432]
+  const uint8_t* down_store;   // [E+1][H/16 tiles][I/2048 panels][18432]
+  float* logits;               // [T, E]
+  int32_t* ids;
+  float* weights;
+  int32_t* offsets;
+  int32_t* entries;
+  int32_t* active_g;           // [E]
+  int32_t* meta_g;             // [64][16]: per active expert h row [8] and weight bits [8]
+  __half* h16;                 // [T*k + T, I]
+  float* out_acc;              // [T, H], zero between calls
+  void* out;
+  uint32_t* sync;              // see the kernel
+  int* status;
+  uint32_t spin_max;
+};
+
+namespace {
+
+template <int MODE, int XDT, int WDT>
+__global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  Geo g;
+  g.T = a.T;
+  g.H = a.H;
+  g.I = a.I;
+  g.E = a.E;
+  g.k = a.top_k;
+  g.NTu = a.I / 8;
+  g.Pu = a.H / kPanelK;
+  g.NTd = a.H / 16;
+  g.Pd = a.I / kPanelK;
+  g.G = gridDim.x;
+  g.c = blockIdx.x;
+  // sync words: [0] router rows done, [1] routing published, [2] CTAs exited,
+  // [3] active experts, [4] CTAs done with down tiles; [8..8+E] gate/up tiles done per expert
+  uint32_t* up_done = a.sync + 8;
+  const int shared_e = a.E;
+  const size_t up_tile_bytes = (size_t)g.Pu * kItemBytes;
+  const size_t dn_tile_bytes = (size_t)g.Pd * kItemBytes;
+
+  if (tid == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      ptx::mbar_init(&S.full[s], 1);
+      ptx::mbar_init(&S.empty[s], 8);
+    }
+    ptx::mbar_init(&S.route_bar, 1);
+    ptx::fence_mbar_init();
+    S.abort = 0;
+    S.issued = 0;
+    S.consumed = 0;
+    S.n_active = 0;
+  }
+  __syncthreads();
+
+  int a0, a1, c10, c11;
+  seg_range(g.NTu, g.G, g.c, a0, a1);    // shared gate/up tiles
+  seg_range(g.NTd, g.G, g.c, c10, c11);  // shared down tiles
+
+  if (warp == 8) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol = ptx::policy_evict_first();
+      int it = 0;
+      bool ok = true;
+      // Brings item `it` into slot it % kSlots once the consumers released its previous use.
+      auto issue = [&](const uint8_t* src) {
+        if (!ok) return;
+        const int slot = it % kSlots;
+        if (it >= kSlots && !ptx::mbar_wait(&S.empty[slot], ((it / kSlots) - 1) & 1, kMbarSpin)) ok = false;
+        if (ok && *(volatile int*)&S.abort) ok = false;
+        if (!ok) return;
+        ptx::mbar_arrive_expect_tx(&S.full[slot], kItemBytes);
+        ptx::bulk_g2s(S.slots[slot], src, kItemBytes, &S.full[slot], pol);
+        ++it;
+        *(volatile int*)&S.issued = it;
+      };
+      for (int tl = a0; tl < a1; ++tl)
+        for (int p = 0; p < g.Pu; ++p)
+          issue(a.up_store + ((size_t)shared_e * g.NTu + tl) * up_tile_bytes + (size_t)p * kItemBytes);
+      for (int tl = c10; tl < c11; ++tl)
+        for (int p = 0; p < g.Pd; ++p)
+          issue(a.down_store + ((size_t)shared_e * g.NTd + tl) * dn_tile_bytes + (size_t)p * kItemBytes);
+      // routing result of this call: active experts and their per-token metadata
+      if (wait_geq(a.sync + 1, 1, a.spin_max)) {
+        const int na = (int)__ldcg(a.sync + 3);
+        S.n_active = na;
+        for (int i = 0; i < na; ++i) {
+          S.active[i] = __ldcg(a.active_g + i);
+          for (int n = 0; n < 8; ++n) {
+            S.meta_pair[i][n] = __ldcg(a.meta_g + i * 16 + n);
+            S.meta_w[i][n] = __int_as_float(__ldcg(a.meta_g + i * 16 + 8 + n));
+          }
+        }
+      } else {
+        ok = false;
+        atomicExch(&S.abort, 1);
+        raise_status(a.status, MOE_ERR_TIMEOUT);
+      }
+      ptx::mbar_arrive(&S.route_bar);
+      const int na = S.n_active;
+      int b0, b1, c20, c21;
+      seg_range(na * g.NTu, g.G, g.c, b0, b1);
+      seg_range(na * g.NTd, g.G, g.c, c20, c21);
+      for (int r = b0; r < b1; ++r) {
+        const int e = S.active[r / g.NTu], tl = r % g.NTu;
+        for (int p = 0; p < g.Pu; ++p)
+          issue(a.up_store + ((size_t)e * g.NTu + tl) * up_tile_bytes + (size_t)p * kItemBytes);
+      }
+      for (int u = c20; u < c21; ++u) {
+        const int e = S.active[u / g.NTd], tl = u % g.NTd;
+        for (int p = 0; p < g.Pd; ++p)
+          issue(a.down_store + ((size_t)e * g.NTd + tl) * dn_tile_bytes + (size_t)p * kItemBytes);
+      }
+      if (!ok) {
+        atomicExch(&S.abort, 1);
+        raise_status(a.status, MOE_ERR_TIMEOUT);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- consumers
+    const int T = g.T, H = g.H, E = g.E, k = g.k;
+    build_x_panel<MODE, XDT>(S, a.x, g);
+
+    // router rows e = c, c + G, ... (same reduction order as the stand-alone router kernel)
+    for (int e = g.c; e < E; e += g.G) {
+      float racc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) racc[i] = 0.f;
+      for (int hh = tid; hh < H; hh += kConsumers) {
+        const float wv = load_act<WDT>(a.router_w, (size_t)e * H + hh);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i < T) racc[i] = fmaf(wv, load_act<XDT>(a.x, (size_t)i * H + hh), racc[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float v = racc[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) S.red[warp][i][0] = v;
+      }
+      ptx::bar_sync(1, kConsumers);
+      if (tid < T) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) v += S.red[w][tid][0];
+        a.logits[(size_t)tid * E + e] = v;
+      }
+      ptx::bar_sync(1, kConsumers);
+    }
+    if (tid == 0) {
+      __threadfence();
+      const uint32_t ticket = atomicAdd(a.sync + 0, 1u);
+      S.flag = (ticket == (uint32_t)g.G - 1) ? 1 : 0;
+    }
+    ptx::bar_sync(1, kConsumers);
+    if (S.flag) {
+      // ---- this CTA finished the router last: selection and grouping for all tokens
+      __threadfence();
+      if (warp < T) {
+        const int id = select_token(a.logits + (size_t)warp * E, a.bias, E, a.n_group, a.topk_group, k,
+                                    a.rsf, S.u.sel.b[warp], S.u.sel.s[warp], a.ids + (size_t)warp * k,
+                                    a.weights + (size_t)warp * k, a.status);
+        if (lane < k) S.sid[warp * k + lane] = id;
+      }
+      ptx::bar_sync(1, kConsumers);
+      if (warp == 0) {
+        const int n = T * k;
+        for (int e = lane; e < E; e += 32) S.cnt[e] = 0;
+        __syncwarp();
+        for (int f = lane; f < n; f += 32) atomicAdd(&S.cnt[S.sid[f]], 1);
+        __syncwarp();
+        // exclusive scans over experts (entry offsets, active-expert slots); lane owns
+        // E/32 consecutive experts
+        const int epl = E / 32;
+        int local = 0, nact = 0;
+        for (int i = 0; i < epl; ++i) {
+          const int cc = S.cnt[lane * epl + i];
+          local += cc;
+          nact += cc > 0;
+        }
+        int incl = local, inca = nact;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          const int va = __shfl_up_sync(0xffffffffu, inca, o);
+          if (lane >= o) {
+            incl += v;
+            inca += va;
+          }
+        }
+        int run = incl - local, apos = inca - nact;
+        for (int i = 0; i < epl; ++i) {
+          const int e = lane * epl + i;
+          S.soff[e] = run;
+          a.offsets[e] = run;
+          if (S.cnt[e] > 0) {
+            S.aslot[e] = apos;
+            a.active_g[apos++] = e;
+          }
+          run += S.cnt[e];
+        }
+        if (lane == 31) {
+          a.offsets[E] = run;
+          a.sync[3] = (uint32_t)inca;
+        }
+        const int na = __shfl_sync(0xffffffffu, inca, 31);
+        // per active expert: h row and combine weight of each token (-1 / 0 if not routed)
+        for (int i = lane; i < na * 8; i += 32) {
+          a.meta_g[(i >> 3) * 16 + (i & 7)] = -1;
+          a.meta_g[(i >> 3) * 16 + 8 + (i & 7)] = 0;
+        }
+        __syncwarp();
+        for (int f = lane; f < n; f += 32) {
+          const int e = S.sid[f];
+          int rank = 0;
+          for (int f2 = 0; f2 < f; ++f2) rank += (S.sid[f2] == e);
+          const int q = S.soff[e] + rank;
+          a.entries[q] = f;
+          const int sl = S.aslot[e], tok = f / k;
+          a.meta_g[sl * 16 + tok] = q;
+          a.meta_g[sl * 16 + 8 + tok] = __float_as_int(__ldcg(a.weights + f));
+        }
+      }
+      ptx::bar_sync(1, kConsumers);
+      if (tid == 0) {
+        __threadfence();
+        ptx::st_release(a.sync + 1, 1u);
+      }
+    }
+
+    float acc[4];
+    int it = 0;          // items consumed
+    int it_ok = 0;       // items whose copy this CTA saw complete (contiguous prefix)
+    // Wait for item `it`; on time-out or abort the item is skipped and not released, so
+    // its slot is never re-armed while a copy may still be in flight.
+    auto wait_item = [&](const uint8_t*& slot) -> bool {
+      const int s = it % kSlots;
+      slot = S.slots[s];
+      if (*(volatile int*)&S.abort) return false;
+      if (!ptx::mbar_wait(&S.full[s], (it / kSlots) & 1, kMbarSpin)) {
+        atomicExch(&S.abort, 1);
+        raise_status(a.status, MOE_ERR_TIMEOUT);
+        return false;
+      }
+      return true;
+    };
+    auto run_items = [&](int np, const uint2* panel, const float* sums) {
+      for (int p = 0; p < np; ++p) {
+        const uint8_t* slot;
+        const bool have = wait_item(slot);
+        if (have) compute_item<MODE>(panel, sums, slot, p * 128, p * 8 + warp, acc);
+        __syncwarp();
+        if (have) {
+          if (lane == 0) ptx::mbar_arrive(&S.empty[it % kSlots]);
+          if (it_ok == it) ++it_ok;
+        }
+        ++it;
+      }
+    };
+
+    // gate/up tiles are counted per expert and published with one release-add per run
+    int up_e = -1, up_n = 0;
+    auto flush_up = [&]() {
+      if (up_n > 0 && tid == 0) ptx::red_release_add(up_done + up_e, (uint32_t)up_n);
+      up_n = 0;
+    };
+
+    // gate/up tile `tl` of expert `e`; h rows of the routed tokens in S.colpair
+    auto up_tile = [&](int e, int tl) {
+      if (e != up_e) {
+        flush_up();
+        up_e = e;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+      run_items(g.Pu, S.xpanel, S.xsums);
+      stash_acc<MODE>(S, acc);
+      ptx::bar_sync(1, kConsumers);
+      const int nt = (MODE == 1) ? 8 : 64;
+      if (tid < nt) {
+        const int r = (MODE == 1) ? tid : (tid >> 3), n = (MODE == 1) ? 0 : (tid & 7);
+        const int pr = S.colpair[n];
+        if (pr >= 0) {
+          const float gate = reduced<MODE>(S, r, n), up = reduced<MODE>(S, r + 8, n);
+          a.h16[(size_t)pr * g.I + tl * 8 + r] = __float2half_rn(siluf_acc(gate) * up);
+        }
+      }
+      ptx::bar_sync(1, kConsumers);
+      ++up_n;
+    };
+
+    // down tile `tl` (16 output rows) of the current expert: out_acc += w * y
+    auto down_tile = [&](int tl) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+      run_items(g.Pd, S.u.hpanel, S.hsums);
+      stash_acc<MODE>(S, acc);
+      ptx::bar_sync(1, kConsumers);
+      const int nt = (MODE == 1) ? 16 : 128;
+      if (tid < nt) {
+        const int r = (MODE == 1) ? tid : (tid >> 3), n = (MODE == 1) ? 0 : (tid & 7);
+        const float wn = S.colw[n];
+        if (n < T && wn != 0.f) atomicAdd(a.out_acc + (size_t)n * H + tl * 16 + r, wn * reduced<MODE>(S, r, n));
+      }
+      ptx::bar_sync(1, kConsumers);
+    };
+
+    // one thread waits until every gate/up tile of expert e is done; uniform continuation
+    auto wait_up = [&](int e) {
+      if (tid == 0) {
+        const bool ok = !*(volatile int*)&S.abort && wait_geq(up_done + e, (uint32_t)g.NTu, a.spin_max);
+        if (!ok) {
+          atomicExch(&S.abort, 1);
+          raise_status(a.status, MOE_ERR_TIMEOUT);
+        }
+      }
+      ptx::bar_sync(1, kConsumers);
+    };
+
+    // colpair / colw for the shared expert (sl < 0) or active slot `sl`
+    auto set_meta = [&](int sl) {
+      ptx::bar_sync(1, kConsumers);
+      if (tid < 8) {
+        if (sl < 0) {
+          S.colpair[tid] = tid < T ? T * k + tid : -1;
+          S.colw[tid] = tid < T ? 1.f : 0.f;
+        } else {
+          S.colpair[tid] = S.meta_pair[sl][tid];
+          S.colw[tid] = S.meta_w[sl][tid];
+        }
+      }
+      ptx::bar_sync(1, kConsumers);
+    };
+
+    // ---- A: shared gate/up
+    set_meta(-1);
+    for (int tl = a0; tl < a1; ++tl) up_tile(shared_e, tl);
+    flush_up();
+    // ---- C1: shared down (needs every shared gate/up tile)
+    if (c11 > c10) {
+      wait_up(shared_e);
+      build_h_panel<MODE>(S, a.h16, g);   // colpair still describes the shared expert
+      ptx::bar_sync(1, kConsumers);
+      for (int tl = c10; tl < c11; ++tl) down_tile(tl);
+    }
+    // ---- routing known (the producer broadcasts it)
+    if (!ptx::mbar_wait(&S.route_bar, 0, kMbarSpin * 16) && tid == 0) {
+      atomicExch(&S.abort, 1);
+      raise_status(a.status, MOE_ERR_TIMEOUT);
+    }
+    ptx::bar_sync(1, kConsumers);
+    const int na = S.n_active;
+    int b0, b1, c20, c21;
+    seg_range(na * g.NTu, g.G, g.c, b0, b1);
+    seg_range(na * g.NTd, g.G, g.c, c20, c21);
+    // ---- B: selected experts' gate/up
+    int cur = -1;
+    for (int r = b0; r < b1; ++r) {
+      const int sl = r / g.NTu, tl = r % g.NTu;
+      if (sl != cur) {
+        set_meta(sl);
+        cur = sl;
+      }
+      up_tile(S.active[sl], tl);
+    }
+    flush_up();
+    // ---- C2: selected experts' down
+    cur = -1;
+    for (int u = c20; u < c21; ++u) {
+      const int sl = u / g.NTd, tl = u % g.NTd;
+      if (sl != cur) {
+        set_meta(sl);
+        wait_up(S.active[sl]);
+        build_h_panel<MODE>(S, a.h16, g);
+        ptx::bar_sync(1, kConsumers);
+        cur = sl;
+      }
+      down_tile(tl);
+    }
+    // ---- every CTA's down tiles are in out_acc: convert this CTA's slice of the output
+    ptx::bar_sync(1, kConsumers);
+    if (tid == 0) {
+      ptx::red_release_add(a.sync + 4, 1u);
+      if (!wait_geq(a.sync + 4, (uint32_t)g.G, a.spin_max)) raise_status(a.status, MOE_ERR_TIMEOUT);
+    }
+    ptx::bar_sync(1, kConsumers);
+    {
+      const size_t n = (size_t)T * H;
+      const size_t lo = n * g.c / g.G, hi = n * (g.c + 1) / g.G;
+      for (size_t i = lo + tid; i < hi; i += kConsumers) {
+        store_act<XDT>(a.out, i, __ldcg(a.out_acc + i));
+        a.out_acc[i] = 0.f;
+      }
+    }
+    if (tid == 0) S.consumed = it_ok;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // drain copies this CTA issued but did not see complete (only after an abort): the last
+    // issued item of each slot is the only one that can still be in flight
+    const int issued = S.issued;
+    for (int i = max(S.consumed, issued - kSlots); i < issued; ++i)
+      ptx::mbar_wait(&S.full[i % kSlots], (i / kSlots) & 1, kMbarSpin);
+    __threadfence();
+    const uint32_t old = atomicAdd(a.sync + 2, 1u);
+    if (old == (uint32_t)g.G - 1) {
+      // last CTA out: reset the counters for the next call
+      a.sync[0] = 0;
+      a.sync[1] = 0;
+      a.sync[3] = 0;
+      a.sync[4] = 0;
+      for (int i = 0; i <= g.E; ++i) up_done[i] = 0;
+      __threadfence();
+      a.sync[2] = 0;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ repack
+
+// Row-major int4-g32 matrix (codes [R][K/2], fp16 scales [R][K/32]) -> 16-row tiles of
+// 2048-column panels in MMA fragment order. `up` selects the gate/up row pairing
+// (MMA rows 0-7 = gate rows 8i.., rows 8-15 = up rows R/2 + 8i..).
+// Per panel: codes [32 chunks of 64 columns][32 lanes][4 words] (word q of lane (g, t) in
+// chunk c: the 8 nibbles (g, 2t) (g+8, 2t) (g, 2t+8) (g+8, 2t+8) (g, 2t+1) (g+8, 2t+1)
+// (g, 2t+9) (g+8, 2t+9) of MMA 4c+q, low nibble first), then scales [8 k-blocks][8 g][4 t]
+// x {s[g][j], s[g][j+1], s[g+8][j], s[g+8][j+1]} with j = 8 * kblock + 2t.
+__global__ void repack_kernel(const uint8_t* __restrict__ codes, const __half* __restrict__ scales,
+                              int R, int K, int up, uint8_t* __restrict__ dst) {
+  const int ntile = R / 16, np = K / kPanelK;
+  const size_t words_per_panel = kCodeBytes / 4;
+  const size_t total_words = (size_t)ntile * np * words_per_panel;
+  const size_t total_scl = (size_t)ntile * np * (kScaleBytes / 8);   // 8-byte scale quads
+  auto row_of = [&](int tile, int m) -> int {
+    if (!up) return tile * 16 + m;
+    const int half = R / 2;
+    return (m < 8) ? tile * 8 + m : half + tile * 8 + (m - 8);
+  };
+  auto nib = [&](int row, int kk) -> uint32_t {
+    const uint8_t b = codes[(size_t)row * (K / 2) + (kk >> 1)];
+    return (kk & 1) ? (b >> 4) : (b & 15u);
+  };
+  for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total_words + total_scl;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    if (idx < total_words) {
+      const size_t tp = idx / words_per_panel;          // tile * np + panel
+      const int wi = (int)(idx % words_per_panel);      // word within the panel
+      const int tile = (int)(tp / np), p = (int)(tp % np);
+      const int q = wi & 3, lane = (wi >> 2) & 31, c = wi >> 7;
+      const int gq = lane >> 2, t = lane & 3;
+      const int k0 = p * kPanelK + 64 * c + 16 * q;
+      const int rA = row_of(tile, gq), rB = row_of(tile, gq + 8);
+      const uint32_t w = nib(rA, k0 + 2 * t) | (nib(rB, k0 + 2 * t) << 4) | (nib(rA, k0 + 2 * t + 8) << 8) |
+                         (nib(rB, k0 + 2 * t + 8) << 12) | (nib(rA, k0 + 2 * t + 1) << 16) |
+                         (nib(rB, k0 + 2 * t + 1) << 20) | (nib(rA, k0 + 2 * t + 9) << 24) |
+                         (nib(rB, k0 + 2 * t + 9) << 28);
+      reinterpret_cast<uint32_t*>(dst + tp * kItemBytes)[wi] = w;
+    } else {
+      const size_t si = idx - total_words;
+      const size_t tp = si / (kScaleBytes / 8);
+      const int qi = (int)(si % (kScaleBytes / 8));     // (kb, g, t) quad
+      const int tile = (int)(tp / np), p = (int)(tp % np);
+      const int t = qi & 3, gq = (qi >> 2) & 7, kb = qi >> 5;
+      const int grp = (p * kPanelK) / 32 + 8 * kb + 2 * t;
+      const int rA = row_of(tile, gq), rB = row_of(tile, gq + 8);
+      __half* o = reinterpret_cast<__half*>(dst + tp * kItemBytes + kCodeBytes) + (size_t)qi * 4;
+      o[0] = scales[(size_t)rA * (K / 32) + grp];
+      o[1] = scales[(size_t)rA * (K / 32) + grp + 1];
+      o[2] = scales[(size_t)rB * (K / 32) + grp];
+      o[3] = scales[(size_t)rB * (K / 32) + grp + 1];
+    }
+  }
+}
+
+template <int MODE, int XDT, int WDT>
+cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = sizeof(Smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, moe_decode_kernel<MODE, XDT, WDT>, a);
+}
+
+template <int MODE, int XDT, int WDT>
+cudaError_t init_one() {
+  return cudaFuncSetAttribute(moe_decode_kernel<MODE, XDT, WDT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sizeof(Smem));
+}
+
+}  // namespace
+
+size_t decode_tile_bytes(int R, int K) { return (size_t)(R / 16) * (K / kPanelK) * kItemBytes; }
+
+bool decode_supported(int H, int I, int E, int top_k, int T) {
+  return H % kPanelK == 0 && I % kPanelK == 0 && H <= kMaxH && I <= kMaxI && E <= kMaxE && E % 32 == 0 &&
+         T >= 1 && T <= 8 && T * top_k <= kMaxActive && top_k <= 16;
+}
+
+size_t decode_smem_bytes() { return sizeof(Smem); }
+
+cudaError_t decode_occupancy(int* blocks_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, moe_decode_kernel<1, MOE_DT_BF16, MOE_DT_F32>,
+                                                       kDecThreads, sizeof(Smem));
+}
+
+cudaError_t launch_repack(const uint8_t* codes, const void* scales, int R, int K, bool up, uint8_t* dst,
+                          cudaStream_t s) {
+  repack_kernel<<<148 * 8, 256, 0, s>>>(codes, static_cast<const __half*>(scales), R, K, up ? 1 : 0, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t decode_kernels_init() {
+  cudaError_t e = cudaSuccess;
+  const cudaError_t r[] = {init_one<0, MOE_DT_F32, MOE_DT_F32>(), init_one<0, MOE_DT_BF16, MOE_DT_F32>(),
+                           init_one<0, MOE_DT_F32, MOE_DT_BF16>(), init_one<0, MOE_DT_BF16, MOE_DT_BF16>(),
+                           init_one<1, MOE_DT_F32, MOE_DT_F32>(), init_one<1, MOE_DT_BF16, MOE_DT_F32>(),
+                           init_one<1, MOE_DT_F32, MOE_DT_BF16>(), init_one<1, MOE_DT_BF16, MOE_DT_BF16>()};
+  for (cudaError_t x : r)
+    if (x != cudaSuccess) e = x;
+  return e;
+}
+
+cudaError_t launch_decode_fused(const DecodeLaunch& d, int act_dtype, int router_dtype, int grid,
+                                cudaStream_t s) {
+  DecodeArgs a;
+  a.x = d.x;
+  a.T = d.T;
+  a.router_w = d.router_w;
+  a.bias = d.bias;
+  a.H = d.H;
+  a.I = d.I;
+  a.E = d.E;
+  a.top_k = d.top_k;
+  a.n_group = d.n_group;
+  a.topk_group = d.topk_group;
+  a.rsf = d.rsf;
+  a.up_store = d.up_store;
+  a.down_store = d.down_store;
+  a.logits = d.logits;
+  a.ids = d.ids;
+  a.weights = d.weights;
+  a.offsets = d.offsets;
+  a.entries = d.entries;
+  a.active_g = d.active_g;
+  a.meta_g = d.meta_g;
+  a.h16 = static_cast<__half*>(d.h16);
+  a.out_acc = d.out_acc;
+  a.out = d.out;
+  a.sync = d.sync;
+  a.status = d.status;
+  a.spin_max = d.spin_max;
+  const bool xf = act_dtype == MOE_DT_F32, wf = router_dtype == MOE_DT_F32;
+  if (a.T == 1) {
+    if (xf) return wf ? launch_decode_t<1, MOE_DT_F32, MOE_DT_F32>(a, grid, s) : launch_decode_t<1, MOE_DT_F32, MOE_DT_BF16>(a, grid, s);
+    return wf ? launch_decode_t<1, MOE_DT_BF16, MOE_DT_F32>(a, grid, s) : launch_decode_t<1, MOE_DT_BF16, MOE_DT_BF16>(a, grid, s);
+  }
+  if (xf) return wf ? launch_decode_t<0, MOE_DT_F32, MOE_DT_F32>(a, grid, s) : launch_decode_t<0, MOE_DT_F32, MOE_DT_BF16>(a, grid, s);
+  return wf ? launch_decode_t<0, MOE_DT_BF16, MOE_DT_F32>(a, grid, s) : launch_decode_t<0, MOE_DT_BF16, MOE_DT_BF16>(a, grid, s);
+}
+
+}  // namespace moe

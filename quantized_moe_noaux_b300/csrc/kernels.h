@@ -57,6 +57,42 @@ cudaError_t launch_amax(const void* src, int src_dtype, size_t n, unsigned int* 
 cudaError_t launch_nvfp4_quant(const void* src, int src_dtype, float* dst, size_t n,
                                const unsigned int* amax_bits, cudaStream_t s);
 
+// ------------------------------------------------------------- fused decode path
+size_t decode_tile_bytes(int R, int K);
+bool decode_supported(int H, int I, int E, int top_k, int T);
+size_t decode_smem_bytes();
+cudaError_t decode_occupancy(int* blocks_per_sm);
+cudaError_t decode_kernels_init();
+// Repack a row-major int4-g32 matrix [R][K] into decode tiles (up = gate/up row pairing).
+cudaError_t launch_repack(const uint8_t* codes, const void* scales, int R, int K, bool up, uint8_t* dst,
+                          cudaStream_t s);
+
+struct DecodeLaunch {
+  const void* x;
+  int T;
+  const void* router_w;
+  const float* bias;
+  int H, I, E, top_k, n_group, topk_group;
+  float rsf;
+  const uint8_t* up_store;
+  const uint8_t* down_store;
+  float* logits;
+  int32_t* ids;
+  float* weights;
+  int32_t* offsets;
+  int32_t* entries;
+  int32_t* active_g;
+  int32_t* meta_g;
+  void* h16;
+  float* out_acc;
+  void* out;
+  uint32_t* sync;
+  int* status;
+  uint32_t spin_max;
+};
+cudaError_t launch_decode_fused(const DecodeLaunch& d, int act_dtype, int router_dtype, int grid,
+                                cudaStream_t s);
+
 // out[T, H] (act dtype) = out_acc
 cudaError_t launch_finalize(const float* out_acc, void* out, int act_dtype, size_t n,
                             cudaStream_t s);

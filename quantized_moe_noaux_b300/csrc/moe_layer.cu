@@ -35,6 +35,16 @@ struct moe_layer {
   int* status = nullptr;
   void* x_stage = nullptr;
   void* out_stage = nullptr;
+  // fused decode path (int4-g32 layers with an int4 shared expert)
+  bool decode_ok = false;
+  int n_sm = 0;
+  uint8_t* up_store = nullptr;
+  uint8_t* down_store = nullptr;
+  uint32_t* dsync = nullptr;
+  int32_t* active_g = nullptr;
+  int32_t* meta_g = nullptr;
+  void* h16 = nullptr;
+  float* dec_acc = nullptr;
   std::vector<void*> allocs;
   // measurement
   std::vector<cudaEvent_t> events;   // kStageEvents per recorded forward
@@ -209,6 +219,37 @@ moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt,
       (st = dev_alloc(L, &L->out_stage, (size_t)Tm * H * ab)))
     return st;
   if (c->weight_format == MOE_W_NVFP4 && (st = dev_alloc_t(L, &L->xq, (size_t)Tm * H * 4))) return st;
+
+  // fused decode path: repack the int4 experts into MMA-fragment tiles
+  int dev = 0;
+  if (cudaGetDevice(&dev) || cudaDeviceGetAttribute(&L->n_sm, cudaDevAttrMultiProcessorCount, dev))
+    return MOE_ERR_CUDA;
+  L->decode_ok = c->weight_format == MOE_W_INT4_G32 && L->shared_inline &&
+                 decode_supported(H, I, E, k, 1) && decode_kernels_init() == cudaSuccess;
+  int occ = 0;
+  if (L->decode_ok && (decode_occupancy(&occ) != cudaSuccess || occ < 1)) L->decode_ok = false;
+  if (L->decode_ok) {
+    const size_t ub = decode_tile_bytes(2 * I, H), db = decode_tile_bytes(H, I);
+    const int Td = Tm < 8 ? Tm : 8;
+    const size_t nsync = (size_t)8 + E + 1;
+    if ((st = dev_alloc_t(L, &L->up_store, (size_t)(E + 1) * ub)) ||
+        (st = dev_alloc_t(L, &L->down_store, (size_t)(E + 1) * db)) ||
+        (st = dev_alloc_t(L, &L->dsync, nsync * 4)) ||
+        (st = dev_alloc_t(L, &L->active_g, (size_t)E * 4)) ||
+        (st = dev_alloc_t(L, &L->meta_g, (size_t)64 * 16 * 4)) ||
+        (st = dev_alloc(L, &L->h16, (size_t)Td * (k + 1) * I * 2)) ||
+        (st = dev_alloc_t(L, &L->dec_acc, (size_t)Td * H * 4)))
+      return st;
+    const size_t gcb = (size_t)2 * I * (H / 2), gsb = (size_t)2 * I * (H / 32) * 2;
+    const size_t dcb = (size_t)H * (I / 2), dsb = (size_t)H * (I / 32) * 2;
+    for (int e = 0; e <= E; ++e) {
+      if (launch_repack(L->w.gu_codes + e * gcb, L->w.gu_scales + e * gsb, 2 * I, H, true, L->up_store + e * ub, s) ||
+          launch_repack(L->w.d_codes + e * dcb, L->w.d_scales + e * dsb, H, I, false, L->down_store + e * db, s))
+        return MOE_ERR_CUDA;
+    }
+    if (cudaMemsetAsync(L->dsync, 0, nsync * 4, s) || cudaMemsetAsync(L->dec_acc, 0, (size_t)Td * H * 4, s))
+      return MOE_ERR_CUDA;
+  }
   if (cudaMemsetAsync(L->status, 0, sizeof(int), s) || cudaMemsetAsync(L->meta, 0, 16 * 4, s))
     return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -249,6 +290,21 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
   StageMarks m;
   m.s = s;
   if (L->timing_used < L->timing_cap) m.ev = &L->events[(size_t)kStageEvents * L->timing_used++];
+  const bool decode = L->decode_ok && T <= 8 && (long)T * k <= 64 && L->path != MOE_PATH_GROUPED;
+  if (L->path == MOE_PATH_GEMV && !decode) return MOE_ERR_UNSUPPORTED;
+  if (decode) {
+    // one fused kernel: routing, gate/up, down + combine (recorded in the third stage slot)
+    MOE_CK(m.mark(0));
+    MOE_CK(m.mark(1));
+    MOE_CK(m.mark(2));
+    DecodeLaunch d{x, T, L->router_w, L->bias, H, I, E, k, c.n_group, c.topk_group,
+                   c.routed_scaling_factor, L->up_store, L->down_store, L->logits, L->ids,
+                   L->weights, L->offsets, L->entries, L->active_g, L->meta_g, L->h16, L->dec_acc,
+                   out, L->dsync, L->status, 1u << 22};
+    MOE_LAUNCH(launch_decode_fused(d, c.act_dtype, c.router_dtype, L->n_sm, s));
+    for (int i = 3; i < kStageEvents; ++i) MOE_CK(m.mark(i));
+    return MOE_OK;
+  }
   MOE_CK(m.mark(0));
   MOE_CK(cudaMemsetAsync(L->counts, 0, (E + 1) * sizeof(int32_t), s));
   MOE_CK(cudaMemsetAsync(L->amax, 0, 4 * sizeof(unsigned int), s));

@@ -5,6 +5,7 @@
 #include <math.h>
 
 #include "kernels.h"
+#include "route_dev.cuh"
 
 namespace moe {
 
@@ -47,19 +48,6 @@ router_logits_kernel(const void* __restrict__ x, const void* __restrict__ wr,
   }
 }
 
-// Warp-wide argmax of (value, index): larger value wins, equal values go to the lower index.
-__device__ __forceinline__ void warp_argmax(float& v, int& i) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-    if (ov > v || (ov == v && oi < i)) {
-      v = ov;
-      i = oi;
-    }
-  }
-}
-
 constexpr int kSelWarps = 4;
 constexpr int kMaxE = 1024;
 
@@ -73,73 +61,10 @@ select_kernel(const float* __restrict__ logits, const float* __restrict__ bias, 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kSelWarps + warp;
   if (t >= T) return;
-  float* b = sb[warp];
-  float* s = ss[warp];
-  for (int e = lane; e < E; e += 32) {
-    const float sc = sigmoidf_acc(logits[(size_t)t * E + e]);
-    s[e] = sc;
-    b[e] = sc + bias[e];
-  }
-  __syncwarp();
-  // group score: sum of the two largest biased scores of the group
-  const int G = E / n_group;
-  float gscore = -INFINITY;
-  if (lane < n_group) {
-    float m1 = -INFINITY, m2 = -INFINITY;
-    for (int i = 0; i < G; ++i) {
-      const float v = b[lane * G + i];
-      if (v > m1) {
-        m2 = m1;
-        m1 = v;
-      } else if (v > m2) {
-        m2 = v;
-      }
-    }
-    gscore = m1 + m2;
-  }
-  // keep the topk_group best groups (ties -> lower group index)
-  unsigned kept = 0;
-  for (int r = 0; r < topk_group; ++r) {
-    float v = gscore;
-    int gi = lane < n_group ? lane : 0x7fffffff;
-    warp_argmax(v, gi);
-    kept |= 1u << gi;
-    if (lane == gi) gscore = -INFINITY;
-  }
-  // top_k experts among kept groups (ties -> lower expert index)
-  float wsum = 0.f;
-  int my_id = -1;
-  float my_s = 0.f;
-  for (int j = 0; j < top_k; ++j) {
-    float v = -INFINITY;
-    int vi = 0x7fffffff;
-    for (int e = lane; e < E; e += 32) {
-      const float be = ((kept >> (e / G)) & 1u) ? b[e] : -INFINITY;
-      if (be > v) {
-        v = be;
-        vi = e;
-      }
-    }
-    warp_argmax(v, vi);
-    if (vi < 0 || vi >= E) {   // fewer candidates than top_k: host validation forbids it
-      raise_status(status, MOE_ERR_DEVICE_CHECK);
-      vi = 0;
-    }
-    const float sv = s[vi];
-    wsum += sv;
-    if (lane == j) {
-      my_id = vi;
-      my_s = sv;
-    }
-    __syncwarp();
-    if (lane == 0) b[vi] = -INFINITY;
-    __syncwarp();
-  }
-  if (lane < top_k) {
-    ids[(size_t)t * top_k + lane] = my_id;
-    weights[(size_t)t * top_k + lane] = my_s / wsum * rsf;
-    atomicAdd(&counts[my_id], 1);
-  }
+  const int id = select_token(logits + (size_t)t * E, bias, E, n_group, topk_group, top_k, rsf,
+                              sb[warp], ss[warp], ids + (size_t)t * top_k,
+                              weights + (size_t)t * top_k, status);
+  if (lane < top_k) atomicAdd(&counts[id], 1);
 }
 
 }  // namespace

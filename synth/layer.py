@@ -90,8 +90,14 @@ _GLM = LayerSpec("glm52_h6144_e256_int4g32", hidden=6144, inter=2048, n_experts=
                  n_group=8, topk_group=4, rsf=2.5, weight_format="int4_g32", act_dtype="bf16",
                  router_dtype="f32", shared_format="int4_g32", bias_std=0.01)
 
+_SMALL = LayerSpec("small_h2048_e32", hidden=2048, inter=2048, n_experts=32, top_k=4, n_group=4,
+                   topk_group=2, rsf=2.5, weight_format="int4_g32", act_dtype="bf16",
+                   router_dtype="f32", shared_format="int4_g32", bias_std=0.01)
+
 LAYERS = {
     "tiny": _TINY,
+    # smallest shape the fused decode kernel runs (2048-column panels, 32-expert groups)
+    "small": _SMALL,
     "glm52": _GLM,
     # decode at T=4 / T=32: the router is left unbiased so tokens share experts
     "glm52_unbiased": replace(_GLM, name="glm52_h6144_e256_int4g32_bias0", bias_std=0.0),
