@@ -51,8 +51,15 @@ typedef enum {
 enum { MOE_W_INT4_G32 = 0, MOE_W_NVFP4 = 1, MOE_W_BF16 = 2 };
 /* activation / router element types */
 enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 };
-/* forward-path selection (moe_layer_set_path) */
-enum { MOE_PATH_AUTO = 0, MOE_PATH_GEMV = 1, MOE_PATH_GROUPED = 2 };
+/*
+ * forward-path selection (moe_layer_set_path):
+ *   MOE_PATH_GEMV     fused decode kernel (int4 layers, T <= 8, T * top_k <= 64)
+ *   MOE_PATH_GROUPED  grouped tcgen05 tensor-core GEMMs (H, I multiples of 256)
+ *   MOE_PATH_GENERIC  CUDA-core batch-union kernels (any supported shape; slow, kept as a
+ *                     cross-check of the fast paths)
+ *   MOE_PATH_AUTO     GEMV when it applies, else GROUPED when it applies, else GENERIC
+ */
+enum { MOE_PATH_AUTO = 0, MOE_PATH_GEMV = 1, MOE_PATH_GROUPED = 2, MOE_PATH_GENERIC = 3 };
 
 typedef struct {
   int32_t hidden;              /* H: multiple of 256 */
@@ -144,7 +151,8 @@ moe_status moe_layer_forward_host(moe_layer* layer, const void* x_host, int32_t 
 moe_status moe_layer_get_routing(moe_layer* layer, int32_t T, int32_t* ids, float* weights,
                                  int32_t* offsets, int32_t* entries, void* stream);
 
-/* Force the expert path (MOE_PATH_*) for later forwards; AUTO picks by T. */
+/* Force the expert path (MOE_PATH_*) for later forwards; AUTO picks by T and shape. A
+ * forced path that does not apply to a forward makes it return MOE_ERR_UNSUPPORTED. */
 moe_status moe_layer_set_path(moe_layer* layer, int32_t path);
 
 /*
@@ -169,6 +177,18 @@ moe_status moe_layer_enable_timing(moe_layer* layer, int32_t enable);
  * and their number into *n_forwards; resets the record count. An empty stage reads 0.
  */
 moe_status moe_layer_stage_times(moe_layer* layer, float* ms, int32_t* n_forwards);
+
+/*
+ * Profiling hook: with a device buffer of n_ctas x 16 uint64 (n_ctas >= the device's SM
+ * count), each later fused-decode forward writes per-CTA %globaltimer stamps (ns) at its
+ * phase boundaries into buffer[cta * 16 + phase]: 0 start, 1 activation panel built,
+ * 2 router rows done, 3 routing published (selecting CTA only), 4 shared gate/up done,
+ * 5 shared gate/up of all CTAs seen, 6 shared down done, 7 routing seen, 8 routed gate/up
+ * done, 9 first routed expert's gate/up seen, 10 routed down done, 11 all CTAs' down
+ * seen, 12 output written, 13 producer done with shared tiles, 14 producer saw routing.
+ * buffer = NULL switches it off (the default). Other paths ignore it.
+ */
+moe_status moe_layer_set_trace(moe_layer* layer, void* buffer, int32_t n_ctas);
 
 /* Cumulative number of kernel launches this layer has issued (host-side count; a forward
  * captured into a CUDA graph counts once at capture). */

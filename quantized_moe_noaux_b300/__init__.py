@@ -14,13 +14,13 @@ import os
 import numpy as np
 
 __all__ = ["MoeLayer", "MoeError", "lib", "LIB_PATH", "SYMBOLS", "STAGES", "W_INT4_G32", "W_NVFP4",
-           "W_BF16", "DT_F32", "DT_BF16", "PATH_AUTO", "PATH_GEMV", "PATH_GROUPED"]
+           "W_BF16", "DT_F32", "DT_BF16", "PATH_AUTO", "PATH_GEMV", "PATH_GROUPED", "PATH_GENERIC"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
 
 W_INT4_G32, W_NVFP4, W_BF16 = 0, 1, 2
 DT_F32, DT_BF16 = 0, 1
-PATH_AUTO, PATH_GEMV, PATH_GROUPED = 0, 1, 2
+PATH_AUTO, PATH_GEMV, PATH_GROUPED, PATH_GENERIC = 0, 1, 2, 3
 
 _FMT = {"int4_g32": W_INT4_G32, "nvfp4": W_NVFP4, "bf16": W_BF16}
 _DT = {"f32": DT_F32, "bf16": DT_BF16}
@@ -65,6 +65,7 @@ SYMBOLS = {
     "moe_layer_enable_timing": (_I, [_P, _I]),
     "moe_layer_stage_times": (_I, [_P, _P, _P]),
     "moe_layer_launch_count": (_I, [_P, _P]),
+    "moe_layer_set_trace": (_I, [_P, _P, _I]),
     "moe_route_noalloc": (_I, [_P, _I, _I, _I, _P, _I, _P, _I, _I, _I, _I, ctypes.c_float,
                                _P, _P, _P, _P, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -213,6 +214,11 @@ class MoeLayer:
         n = ctypes.c_int32()
         _check("moe_layer_stage_times", _get_lib().moe_layer_stage_times(self._h, ms, ctypes.byref(n)))
         return dict(zip(STAGES, list(ms))), n.value
+
+    def set_trace(self, buffer, n_ctas: int):
+        """Profiling hook: per-CTA phase timestamps of the fused decode kernel into a
+        device buffer of n_ctas x 16 int64 (None switches it off)."""
+        _check("moe_layer_set_trace", _get_lib().moe_layer_set_trace(self._h, _ptr(buffer), n_ctas))
 
     def launch_count(self) -> int:
         c = ctypes.c_int64()

@@ -7,9 +7,6 @@
 // E4M3_rne_satfinite((amax16 / 6) / ts) and each element's code is
 // E2M1_rne_satfinite(v / (scale * ts)); every quotient and product that decides a code is a
 // correctly rounded fp32 operation in exactly that order (no contraction into FMAs).
-#include <cuda_fp4.h>
-#include <cuda_fp8.h>
-
 #include "kernels.h"
 
 namespace moe {
@@ -44,27 +41,13 @@ nvfp4_quant_kernel(const void* __restrict__ src, float* __restrict__ dst, size_t
   const float ts = __fdiv_rn(amax, 2688.0f);
   for (size_t b = (size_t)blockIdx.x * kThreads + threadIdx.x; b < nblocks;
        b += (size_t)gridDim.x * kThreads) {
-    float v[16];
-    float bmax = 0.f;
+    float v[16], c[16], sb;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = load_act<DT>(src, b * 16 + i);
+    nvfp4_block(v, ts, sb, c);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      v[i] = load_act<DT>(src, b * 16 + i);
-      bmax = fmaxf(bmax, fabsf(v[i]));
-    }
-    float sb = 0.f;
-    if (ts != 0.f) {
-      const float ratio = __fdiv_rn(__fdiv_rn(bmax, 6.0f), ts);
-      sb = e4m3_to_float(__nv_cvt_float_to_fp8(ratio, __NV_SATFINITE, __NV_E4M3));
-    }
-    const float denom = __fmul_rn(sb, ts);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float out = 0.f;
-      if (denom != 0.f) {
-        const float q = __fdiv_rn(v[i], denom);
-        const float c = e2m1_to_float(__nv_cvt_float_to_fp4(q, __NV_E2M1, cudaRoundNearest));
-        out = __fmul_rn(__fmul_rn(c, sb), ts);
-      }
+      const float out = __fmul_rn(__fmul_rn(c[i], sb), ts);
       dst[b * 16 + i] = out;
     }
   }

@@ -4,6 +4,8 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -64,6 +66,31 @@ __device__ __forceinline__ void store_act(void* base, size_t i, float v) {
 
 __device__ __forceinline__ float sigmoidf_acc(float z) { return 1.0f / (1.0f + expf(-z)); }
 __device__ __forceinline__ float siluf_acc(float z) { return z / (1.0f + expf(-z)); }
+
+// ------------------------------------------------------- NVFP4 activation blocks
+// One 16-element block of an NVFP4 activation with tensor scale ts ("NVIDIA stellt neues
+// GLM-5.2 NVFP4 Modell vor", section "Technische Details und Quantisierungsansatz": E2M1
+// elements with an FP8 E4M3 scale per 16 elements): block scale sb =
+// E4M3_rne_satfinite((amax16 / 6) / ts), element code c[i] = E2M1_rne_satfinite(v[i] /
+// (sb * ts)), each quotient and product a correctly rounded fp32 operation in that order.
+// The dequantised element is c[i] * sb * ts. ts = 0 gives sb = 0 and all-zero codes.
+__device__ __forceinline__ void nvfp4_block(const float (&v)[16], float ts, float& sb, float (&c)[16]) {
+  float bmax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+  sb = 0.f;
+  if (ts != 0.f) {
+    const float ratio = __fdiv_rn(__fdiv_rn(bmax, 6.0f), ts);
+    sb = e4m3_to_float(__nv_cvt_float_to_fp8(ratio, __NV_SATFINITE, __NV_E4M3));
+  }
+  const float denom = __fmul_rn(sb, ts);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    c[i] = 0.f;
+    if (denom != 0.f)
+      c[i] = e2m1_to_float(__nv_cvt_float_to_fp4(__fdiv_rn(v[i], denom), __NV_E2M1, cudaRoundNearest));
+  }
+}
 
 // ------------------------------------------------------------ weight formats
 // A weight row is read in 16-byte chunks. Per chunk:

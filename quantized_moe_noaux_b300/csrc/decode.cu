@@ -341,9 +341,22 @@ struct DecodeArgs {
   uint32_t* sync;              // see the kernel
   int* status;
   uint32_t spin_max;
+  unsigned long long* trace;   // optional [grid][16] phase timestamps (ns), or NULL
 };
 
 namespace {
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Phase timestamp of this CTA (profiling hook; one thread records).
+#define DEC_TRACE(i)                                                            \
+  do {                                                                          \
+    if (a.trace) a.trace[(size_t)blockIdx.x * 16 + (i)] = global_ns();          \
+  } while (0)
 
 template <int MODE, int XDT, int WDT>
 __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a) {
@@ -411,8 +424,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       for (int tl = c10; tl < c11; ++tl)
         for (int p = 0; p < g.Pd; ++p)
           issue(a.down_store + ((size_t)shared_e * g.NTd + tl) * dn_tile_bytes + (size_t)p * kItemBytes);
+      DEC_TRACE(13);
       // routing result of this call: active experts and their per-token metadata
       if (wait_geq(a.sync + 1, 1, a.spin_max)) {
+        DEC_TRACE(14);
         const int na = (int)__ldcg(a.sync + 3);
         S.n_active = na;
         for (int i = 0; i < na; ++i) {
@@ -450,7 +465,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
   } else {
     // ------------------------------------------------------------- consumers
     const int T = g.T, H = g.H, E = g.E, k = g.k;
+    if (tid == 0) DEC_TRACE(0);
     build_x_panel<MODE, XDT>(S, a.x, g);
+    if (tid == 0) DEC_TRACE(1);
 
     // router rows e = c, c + G, ... (same reduction order as the stand-alone router kernel)
     for (int e = g.c; e < E; e += g.G) {
@@ -485,6 +502,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       S.flag = (ticket == (uint32_t)g.G - 1) ? 1 : 0;
     }
     ptx::bar_sync(1, kConsumers);
+    if (tid == 0) DEC_TRACE(2);
     if (S.flag) {
       // ---- this CTA finished the router last: selection and grouping for all tokens
       __threadfence();
@@ -557,6 +575,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       if (tid == 0) {
         __threadfence();
         ptx::st_release(a.sync + 1, 1u);
+        DEC_TRACE(3);
       }
     }
 
@@ -668,13 +687,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     set_meta(-1);
     for (int tl = a0; tl < a1; ++tl) up_tile(shared_e, tl);
     flush_up();
+    if (tid == 0) DEC_TRACE(4);
     // ---- C1: shared down (needs every shared gate/up tile)
     if (c11 > c10) {
       wait_up(shared_e);
+      if (tid == 0) DEC_TRACE(5);
       build_h_panel<MODE>(S, a.h16, g);   // colpair still describes the shared expert
       ptx::bar_sync(1, kConsumers);
       for (int tl = c10; tl < c11; ++tl) down_tile(tl);
     }
+    if (tid == 0) DEC_TRACE(6);
     // ---- routing known (the producer broadcasts it)
     if (!ptx::mbar_wait(&S.route_bar, 0, kMbarSpin * 16) && tid == 0) {
       atomicExch(&S.abort, 1);
@@ -685,6 +707,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     int b0, b1, c20, c21;
     seg_range(na * g.NTu, g.G, g.c, b0, b1);
     seg_range(na * g.NTd, g.G, g.c, c20, c21);
+    if (tid == 0) DEC_TRACE(7);
     // ---- B: selected experts' gate/up
     int cur = -1;
     for (int r = b0; r < b1; ++r) {
@@ -696,6 +719,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       up_tile(S.active[sl], tl);
     }
     flush_up();
+    if (tid == 0) DEC_TRACE(8);
     // ---- C2: selected experts' down
     cur = -1;
     for (int u = c20; u < c21; ++u) {
@@ -703,17 +727,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       if (sl != cur) {
         set_meta(sl);
         wait_up(S.active[sl]);
+        if (tid == 0 && cur < 0) DEC_TRACE(9);
         build_h_panel<MODE>(S, a.h16, g);
         ptx::bar_sync(1, kConsumers);
         cur = sl;
       }
       down_tile(tl);
     }
+    if (tid == 0) DEC_TRACE(10);
     // ---- every CTA's down tiles are in out_acc: convert this CTA's slice of the output
     ptx::bar_sync(1, kConsumers);
     if (tid == 0) {
       ptx::red_release_add(a.sync + 4, 1u);
       if (!wait_geq(a.sync + 4, (uint32_t)g.G, a.spin_max)) raise_status(a.status, MOE_ERR_TIMEOUT);
+      DEC_TRACE(11);
     }
     ptx::bar_sync(1, kConsumers);
     {
@@ -724,7 +751,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
         a.out_acc[i] = 0.f;
       }
     }
-    if (tid == 0) S.consumed = it_ok;
+    if (tid == 0) {
+      S.consumed = it_ok;
+      DEC_TRACE(12);
+    }
   }
   __syncthreads();
   if (tid == 0) {
@@ -887,6 +917,7 @@ cudaError_t launch_decode_fused(const DecodeLaunch& d, int act_dtype, int router
   a.sync = d.sync;
   a.status = d.status;
   a.spin_max = d.spin_max;
+  a.trace = d.trace;
   const bool xf = act_dtype == MOE_DT_F32, wf = router_dtype == MOE_DT_F32;
   if (a.T == 1) {
     if (xf) return wf ? launch_decode_t<1, MOE_DT_F32, MOE_DT_F32>(a, grid, s) : launch_decode_t<1, MOE_DT_F32, MOE_DT_BF16>(a, grid, s);

@@ -1,0 +1,611 @@
+// Grouped expert GEMMs of the MoE layer on the tcgen05 tensor cores (the batch-union path
+// for more than a handful of tokens: "Batch-union MoE" in "Show HN: Menjalankan GLM 5.2 di
+// komputer lambat", section "Fitur utama yang diimplementasikan": each selected expert's
+// weights are read once per call and applied to every token routed to it).
+//
+// One CTA computes a 128 x N tile D = W[128 rows, K] . X[N tokens, K]^T of one expert:
+// weight rows on the MMA's M side, the expert's tokens (rows of an expert-sorted
+// activation matrix, N <= 256) on the N side, so a lightly loaded expert still fills the
+// tensor core's M dimension. The quantised weights stay quantised in HBM and are
+// dequantised on use (the packed int4 "dequant-on-use" of the same section; NVFP4 blocks
+// per "NVIDIA stellt neues GLM-5.2 NVFP4 Modell vor", section "Technische Details und
+// Quantisierungsansatz"):
+//   warp 6   TMA: 128 rows x 256 columns of packed codes (+ their scales) per weight stage
+//   warps 0-3 dequantise 64 columns per K stage into an fp16 tile in the 128-byte swizzle
+//            layout the MMA reads (int4 * fp16 scale rounded once to fp16; E2M1 * E4M3 is
+//            exact in fp16, the fp32 tensor scales are applied in the epilogue)
+//   warp 4   TMA: the N x 64 fp16 activation tile of the same K stage
+//   warp 5   issues tcgen05.mma kind::f16 (M=128, N, K=16) x 4 per stage into a TMEM
+//            accumulator and releases stages with tcgen05.commit
+//   warps 0-3 then read the accumulator (tcgen05.ld) and run the epilogue:
+//     gate/up: M rows pair 16 gate with 16 up rows per warp; h = SiLU(gate) * up is
+//              written to the expert-sorted h matrix (fp16, or fp32 for NVFP4 layers
+//              whose h is quantised next);
+//     down:    out_acc[token] += w[token, slot] * y (fp32 atomics; the weighted combine).
+// A separately stored bf16 shared expert (the NVFP4 layers keep it unquantised) is
+// converted to fp16 once at layer creation (exact for its range) and runs through the
+// same kernel with TMA-loaded weight tiles and no dequantisation (kWF16).
+// Every wait is bounded; a time-out sets MOE_ERR_TIMEOUT, the CTA stops issuing work,
+// lets copies in flight land, frees its TMEM and exits.
+#include <cuda.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kGThreads = 224;
+constexpr int kBM = 128;          // weight rows per tile (MMA M)
+constexpr int kBN = 256;          // max tokens per tile (MMA N)
+constexpr int kBK = 64;           // K per stage: one 128-byte swizzle atom of fp16
+constexpr int kSub = 4;           // K stages per weight stage (256 columns)
+constexpr int kABStages = 3;
+constexpr int kWStages = 3;
+constexpr int kAStage = kBM * kBK * 2;     // 16 KB fp16 weight tile
+constexpr int kBStage = kBN * kBK * 2;     // 32 KB fp16 activation tile
+constexpr int kWCodes = kBM * 128;         // 16 KB: 128 rows x 256 4-bit codes
+constexpr int kWScales = kBM * 16;         // 2 KB: 128 rows x 16 scale bytes
+constexpr int kBoxRows = 16;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kSpin = 1u << 22;
+
+struct GSmem {
+  uint8_t a[kABStages][kAStage];
+  uint8_t b[kABStages][kBStage];
+  uint8_t wc[kWStages][kWCodes];
+  uint8_t ws[kWStages][kWScales];
+  uint64_t full_ab[kABStages];
+  uint64_t empty_ab[kABStages];
+  uint64_t full_w[kWStages];
+  uint64_t empty_w[kWStages];
+  uint64_t tmem_full;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+  int col_tok[kBN];
+  float col_w[kBN];
+};
+
+constexpr size_t kGSmemBytes = sizeof(GSmem) + 1024;   // + alignment slack
+static_assert(kGSmemBytes <= 227 * 1024, "grouped GEMM shared memory over the per-CTA limit");
+
+// Bounded wait on an mbarrier phase with a short back-off; false on time-out.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpin; ++i) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (i >= 64) __nanosleep(32);
+  }
+  return false;
+}
+
+__device__ __forceinline__ void set_abort(GSmem& S, int* status) {
+  atomicExch(&S.abort, 1);
+  raise_status(status, MOE_ERR_TIMEOUT);
+}
+
+__device__ __forceinline__ bool aborted(const GSmem& S) { return *(volatile const int*)&S.abort != 0; }
+
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// 8 packed nibbles (element 2j in the low nibble of byte j) -> 4 words holding the nibble
+// pairs (e0,e1) (e2,e3) (e4,e5) (e6,e7) at bits 0-3 and 16-19.
+__device__ __forceinline__ void nibble_pairs(uint32_t w, uint32_t (&p)[4]) {
+  const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+  const uint32_t r0 = __byte_perm(lo, hi, 0x5410);   // e0 e2 e1 e3
+  const uint32_t r1 = __byte_perm(lo, hi, 0x7632);   // e4 e6 e5 e7
+  p[0] = r0 & 0x000F000Fu;
+  p[1] = (r0 >> 8) & 0x000F000Fu;
+  p[2] = r1 & 0x000F000Fu;
+  p[3] = (r1 >> 8) & 0x000F000Fu;
+}
+
+// int4 (two's complement) x 8 -> fp16 x 8 times the group scale: (nibble ^ 8) in the
+// mantissa of 1024 is 1032 + code exactly; subtracting 1032 is exact; the product with the
+// fp16 scale is rounded once.
+__device__ __forceinline__ uint4 dq_int4x8(uint32_t w, __half2 s2) {
+  uint32_t p[4];
+  nibble_pairs(w, p);
+  const __half2 k1032 = __float2half2_rn(1032.f);
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[i] = h2u(__hmul2(__hsub2(u2h(p[i] ^ 0x64086408u), k1032), s2));
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// E2M1 x 8 -> fp16 x 8 times the block scale. The nibble's exponent and mantissa bits placed
+// at fp16 bits 9-11 (sign at 15) give the E2M1 value times 2^-14 (its subnormal included);
+// both products are exact in fp16.
+__device__ __forceinline__ uint4 dq_e2m1x8(uint32_t w, __half2 s2) {
+  uint32_t p[4];
+  nibble_pairs(w, p);
+  const __half2 k2p14 = __float2half2_rn(16384.f);
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t bits = ((p[i] & 0x00070007u) << 9) | ((p[i] & 0x00080008u) << 12);
+    o[i] = h2u(__hmul2(__hmul2(u2h(bits), k2p14), s2));
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Non-negative E4M3 byte -> fp16 (exact): its 7 magnitude bits at fp16 bits 7-13 give the
+// value times 2^-8 (subnormals included).
+__device__ __forceinline__ __half e4m3_to_half(uint32_t b) {
+  const __half v = __ushort_as_half((unsigned short)((b & 0x7Fu) << 7));
+  return __hmul(v, __float2half(256.f));
+}
+
+template <int WFMT, int EPI>
+__device__ __forceinline__ int weight_row(const GemmParams& p, int e, int mt, int j) {
+  e -= p.e_sub;
+  if (EPI == 0) {   // box 2w: gate rows, box 2w+1: up rows 64 mt + 16 w ..
+    return e * p.rows_per_expert + ((j & 1) ? p.I : 0) + 64 * mt + 16 * (j >> 1);
+  }
+  return e * p.rows_per_expert + kBM * mt + kBoxRows * j;
+}
+
+template <int WFMT, int EPI>
+__global__ void __launch_bounds__(kGThreads, 1)
+moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
+                const __grid_constant__ CUtensorMap tm_b, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  GSmem& S = *reinterpret_cast<GSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if ((int)blockIdx.y >= __ldg(p.n_items)) return;
+  const int4 item = __ldg(p.items + blockIdx.y + (p.item_skip ? __ldg(p.item_skip) : 0));
+  const int e = item.x, row0 = item.y, n = item.z;
+  const int mt = blockIdx.x;
+  const int NK = p.K / kBK;
+  const int nbox = (n + kBoxRows - 1) / kBoxRows;
+  const int N = nbox * kBoxRows;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Tk = p.T * p.top_k;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kABStages; ++s) {
+      // B producer (+ tx) and the 4 dequant warps, or the two TMA producers (fp16 weights)
+      ptx::mbar_init(&S.full_ab[s], WFMT == kWF16 ? 2 : 5);
+      ptx::mbar_init(&S.empty_ab[s], 1);   // tcgen05.commit
+    }
+    for (int s = 0; s < kWStages; ++s) {
+      ptx::mbar_init(&S.full_w[s], 1);
+      ptx::mbar_init(&S.empty_w[s], 4);
+    }
+    ptx::mbar_init(&S.tmem_full, 1);
+    ptx::mbar_init(&S.mma_done, 1);
+    ptx::fence_mbar_init();
+    S.abort = 0;
+  }
+  if (warp == 5) {
+    ptx::tmem_alloc(&S.tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (EPI == 1) {
+    for (int c = threadIdx.x; c < n; c += kGThreads) {
+      const int q = row0 + c;
+      if (q < Tk) {
+        const int ent = __ldg(p.entries + q);
+        S.col_tok[c] = ent / p.top_k;
+        S.col_w[c] = __ldg(p.weights + ent);
+      } else {
+        S.col_tok[c] = q - Tk;
+        S.col_w[c] = 1.f;
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+
+  if (warp == 6 && WFMT == kWF16) {
+    // --------------------------------------------- fp16 weight tiles straight to A
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tm_codes);
+      for (int ks = 0; ks < NK; ++ks) {
+        const int s = ks % kABStages;
+        if (ks >= kABStages && !wait_bar(&S.empty_ab[s], ((ks / kABStages) - 1) & 1)) {
+          set_abort(S, p.status);
+          break;
+        }
+        if (aborted(S)) break;
+        ptx::mbar_arrive_expect_tx(&S.full_ab[s], kAStage);
+#pragma unroll 1
+        for (int j = 0; j < kBM / kBoxRows; ++j)
+          ptx::tma_load_2d(S.a[s] + j * kBoxRows * 128, &tm_codes, ks * kBK, weight_row<WFMT, EPI>(p, e, mt, j),
+                           &S.full_ab[s]);
+      }
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------ weight codes + scales producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tm_codes);
+      ptx::prefetch_tmap(&tm_scales);
+      const int NW = NK / kSub;
+      for (int w = 0; w < NW; ++w) {
+        const int s = w % kWStages;
+        if (w >= kWStages && !wait_bar(&S.empty_w[s], ((w / kWStages) - 1) & 1)) {
+          set_abort(S, p.status);
+          break;
+        }
+        if (aborted(S)) break;
+        ptx::mbar_arrive_expect_tx(&S.full_w[s], kWCodes + kWScales);
+#pragma unroll 1
+        for (int j = 0; j < kBM / kBoxRows; ++j) {
+          const int row = weight_row<WFMT, EPI>(p, e, mt, j);
+          ptx::tma_load_2d(S.wc[s] + j * kBoxRows * 128, &tm_codes, w * 128, row, &S.full_w[s]);
+          ptx::tma_load_2d(S.ws[s] + j * kBoxRows * 16, &tm_scales, w * 16, row, &S.full_w[s]);
+        }
+      }
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------------- activation producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tm_b);
+      for (int ks = 0; ks < NK; ++ks) {
+        const int s = ks % kABStages;
+        if (ks >= kABStages && !wait_bar(&S.empty_ab[s], ((ks / kABStages) - 1) & 1)) {
+          set_abort(S, p.status);
+          break;
+        }
+        if (aborted(S)) break;
+        ptx::mbar_arrive_expect_tx(&S.full_ab[s], (uint32_t)nbox * kBoxRows * 128);
+#pragma unroll 1
+        for (int j = 0; j < nbox; ++j)
+          ptx::tma_load_2d(S.b[s] + j * kBoxRows * 128, &tm_b, ks * kBK, row0 + kBoxRows * j, &S.full_ab[s]);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = ptx::f16_idesc(kBM, N, false);
+      for (int ks = 0; ks < NK; ++ks) {
+        const int s = ks % kABStages;
+        if (!wait_bar(&S.full_ab[s], (ks / kABStages) & 1)) {
+          set_abort(S, p.status);
+          break;
+        }
+        if (aborted(S)) break;
+        ptx::tc_fence_after();
+        const uint32_t a0 = ptx::smem_u32(S.a[s]), b0 = ptx::smem_u32(S.b[s]);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          ptx::tc_mma_f16(tmem, ptx::sw128_desc(a0 + 32 * kk), ptx::sw128_desc(b0 + 32 * kk), idesc,
+                          (ks | kk) != 0 ? 1u : 0u);
+        ptx::tc_commit(&S.empty_ab[s]);
+      }
+      ptx::tc_commit(&S.tmem_full);
+    }
+  } else {
+    // ------------------------------------------- dequantisers (warps 0-3), then epilogue
+    const int m = threadIdx.x;   // A row 0..127
+    uint4 sc = make_uint4(0u, 0u, 0u, 0u);
+    for (int ks = 0; ks < (WFMT == kWF16 ? 0 : NK); ++ks) {
+      const int w = ks / kSub, ws = w % kWStages, kq = ks % kSub;
+      if (kq == 0) {
+        if (!wait_bar(&S.full_w[ws], (w / kWStages) & 1)) set_abort(S, p.status);
+        sc = *reinterpret_cast<const uint4*>(S.ws[ws] + m * 16);
+      }
+      const int s = ks % kABStages;
+      if (ks >= kABStages && !wait_bar(&S.empty_ab[s], ((ks / kABStages) - 1) & 1)) set_abort(S, p.status);
+      if (__any_sync(0xffffffffu, aborted(S))) break;   // warp-uniform exit
+      const uint8_t* crow = S.wc[ws] + m * 128;
+      const uint4 q0 = *reinterpret_cast<const uint4*>(crow + (((2 * kq) ^ (m & 7)) << 4));
+      const uint4 q1 = *reinterpret_cast<const uint4*>(crow + (((2 * kq + 1) ^ (m & 7)) << 4));
+      const uint32_t sw = kq == 0 ? sc.x : kq == 1 ? sc.y : kq == 2 ? sc.z : sc.w;
+      uint4 o[8];
+      if (WFMT == MOE_W_INT4_G32) {
+        const __half2 s01 = u2h(sw);   // scales of groups 2kq (low) and 2kq + 1 (high)
+        const __half2 sa = __low2half2(s01), sb = __high2half2(s01);
+        o[0] = dq_int4x8(q0.x, sa);
+        o[1] = dq_int4x8(q0.y, sa);
+        o[2] = dq_int4x8(q0.z, sa);
+        o[3] = dq_int4x8(q0.w, sa);
+        o[4] = dq_int4x8(q1.x, sb);
+        o[5] = dq_int4x8(q1.y, sb);
+        o[6] = dq_int4x8(q1.z, sb);
+        o[7] = dq_int4x8(q1.w, sb);
+      } else {
+        const __half2 s0 = __half2half2(e4m3_to_half(sw & 0xFFu));
+        const __half2 s1 = __half2half2(e4m3_to_half((sw >> 8) & 0xFFu));
+        const __half2 s2 = __half2half2(e4m3_to_half((sw >> 16) & 0xFFu));
+        const __half2 s3 = __half2half2(e4m3_to_half(sw >> 24));
+        o[0] = dq_e2m1x8(q0.x, s0);
+        o[1] = dq_e2m1x8(q0.y, s0);
+        o[2] = dq_e2m1x8(q0.z, s1);
+        o[3] = dq_e2m1x8(q0.w, s1);
+        o[4] = dq_e2m1x8(q1.x, s2);
+        o[5] = dq_e2m1x8(q1.y, s2);
+        o[6] = dq_e2m1x8(q1.z, s3);
+        o[7] = dq_e2m1x8(q1.w, s3);
+      }
+      uint8_t* arow = S.a[s] + (m >> 3) * 1024 + (m & 7) * 128;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(arow + ((j ^ (m & 7)) << 4)) = o[j];
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(&S.full_ab[s]);
+        if (kq == kSub - 1) ptx::mbar_arrive(&S.empty_w[ws]);
+      }
+    }
+
+    // ------------------------------------------------------------------ epilogue
+    if (!wait_bar(&S.tmem_full, 0)) set_abort(S, p.status);
+    ptx::tc_fence_after();
+    if (!__any_sync(0xffffffffu, aborted(S))) {
+      float sc_out = 1.f;
+      if (WFMT == MOE_W_NVFP4) sc_out = __ldg(p.w_tscale + e) * __fdiv_rn(__uint_as_float(__ldg(p.act_amax)), 2688.0f);
+      const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+      for (int c0 = 0; c0 < N; c0 += 32) {
+        float v[32];
+        ptx::tmem_ld32(lane_addr + (uint32_t)c0, v);
+        if (EPI == 0) {
+          const bool upl = lane >= 16;
+          const int hcol = 64 * mt + 16 * warp + (lane & 15);
+          float hmax = 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float send = upl ? v[j] : v[16 + j];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+            const float g = (upl ? recv : v[j]) * sc_out;
+            const float u = (upl ? v[16 + j] : recv) * sc_out;
+            const int c = c0 + j + (upl ? 16 : 0);
+            if (c < n) {
+              const float hv = siluf_acc(g) * u;
+              const size_t idx = (size_t)(row0 + c) * p.I + hcol;
+              if (WFMT == MOE_W_NVFP4) {
+                p.h32[idx] = hv;
+                if (row0 + c < Tk) hmax = fmaxf(hmax, fabsf(hv));
+              } else {
+                p.h16[idx] = __float2half_rn(hv);
+              }
+            }
+          }
+          if (WFMT == MOE_W_NVFP4) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) hmax = fmaxf(hmax, __shfl_xor_sync(0xffffffffu, hmax, o));
+            if (lane == 0 && hmax > 0.f) atomicMax(p.h_amax, __float_as_uint(hmax));
+          }
+        } else {
+          const int hrow = kBM * mt + 32 * warp + lane;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int c = c0 + j;
+            if (c < n) atomicAdd(p.out_acc + (size_t)S.col_tok[c] * p.H + hrow, S.col_w[c] * (v[j] * sc_out));
+          }
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------------- teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (aborted(S) && threadIdx.x == 0) {
+    // copies and MMAs issued before the abort complete on their own; give them time to land
+    for (int i = 0; i < 2000; ++i) __nanosleep(1000);
+  }
+  if (warp == 5) {
+    if (aborted(S) && lane == 0) {
+      ptx::tc_commit(&S.mma_done);
+      wait_bar(&S.mma_done, 0);
+    }
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Items of the grouped GEMMs: chunks of <= kBN consecutive expert-sorted rows of one
+// expert: the routed experts in id order, then the shared expert (index E) over all T
+// tokens. n_items[0] = routed items, n_items[1] = shared items, n_items[2] = both.
+__global__ void gemm_items_kernel(const int32_t* __restrict__ offsets, int E, int T, int top_k,
+                                  int4* __restrict__ items, int32_t* __restrict__ n_items) {
+  if (threadIdx.x != 0) return;
+  int n = 0;
+  for (int e = 0; e < E; ++e) {
+    const int o = offsets[e], c = offsets[e + 1] - o;
+    for (int j = 0; j < c; j += kBN) items[n++] = make_int4(e, o + j, min(kBN, c - j), 0);
+  }
+  const int nr = n;
+  for (int j = 0; j < T; j += kBN) items[n++] = make_int4(E, T * top_k + j, min(kBN, T - j), 0);
+  n_items[0] = nr;
+  n_items[1] = n - nr;
+  n_items[2] = n;
+}
+
+__global__ void bf16_to_f16_kernel(const uint16_t* __restrict__ src, __half* __restrict__ dst, size_t n) {
+  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256)
+    dst[i] = __float2half_rn(__uint_as_float((uint32_t)src[i] << 16));
+}
+
+// Expert-sorted activation rows for the gate/up GEMM: row q < T*k is the token of entry q,
+// row T*k + t is token t (shared expert). x is converted to fp16, except that NVFP4 layers
+// quantise the routed rows (q < T*k) to NVFP4 with the per-call tensor scale
+// ts = amax / 2688: such a row holds code * block scale (exact in fp16) and ts is applied
+// in the GEMM epilogue. The shared expert always reads the unquantised x.
+template <int XDT, bool FP4>
+__global__ void __launch_bounds__(256)
+gather_act_kernel(const void* __restrict__ x, int H, const int32_t* __restrict__ entries, int Tk, int top_k,
+                  __half* __restrict__ dst, const unsigned int* __restrict__ amax_bits) {
+  const int q = blockIdx.x;
+  const int tok = q < Tk ? __ldg(entries + q) / top_k : q - Tk;
+  __half* drow = dst + (size_t)q * H;
+  if (!FP4 || q >= Tk) {
+    for (int i = threadIdx.x * 8; i < H; i += 256 * 8) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = load_act<XDT>(x, (size_t)tok * H + i + j);
+      uint4 o;
+      o.x = h2u(__floats2half2_rn(v[0], v[1]));
+      o.y = h2u(__floats2half2_rn(v[2], v[3]));
+      o.z = h2u(__floats2half2_rn(v[4], v[5]));
+      o.w = h2u(__floats2half2_rn(v[6], v[7]));
+      *reinterpret_cast<uint4*>(drow + i) = o;
+    }
+  } else {
+    const float ts = __fdiv_rn(__uint_as_float(__ldg(amax_bits)), 2688.0f);
+    for (int i = threadIdx.x * 16; i < H; i += 256 * 16) {
+      float v[16], c[16], sb;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = load_act<XDT>(x, (size_t)tok * H + i + j);
+      nvfp4_block(v, ts, sb, c);
+      uint32_t o[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o[j] = h2u(__floats2half2_rn(c[2 * j] * sb, c[2 * j + 1] * sb));
+      *reinterpret_cast<uint4*>(drow + i) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(drow + i + 8) = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+  }
+}
+
+// NVFP4 h: quantise the fp32 routed h rows with the per-call tensor scale (amax of all routed
+// h) into code * block scale in fp16.
+__global__ void __launch_bounds__(256)
+quant_h_kernel(const float* __restrict__ h, size_t nblocks, const unsigned int* __restrict__ amax_bits,
+               __half* __restrict__ dst) {
+  const float ts = __fdiv_rn(__uint_as_float(__ldg(amax_bits)), 2688.0f);
+  for (size_t b = (size_t)blockIdx.x * 256 + threadIdx.x; b < nblocks; b += (size_t)gridDim.x * 256) {
+    float v[16], c[16], sb;
+    const float4* src = reinterpret_cast<const float4*>(h + b * 16);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 f = src[j];
+      v[4 * j] = f.x;
+      v[4 * j + 1] = f.y;
+      v[4 * j + 2] = f.z;
+      v[4 * j + 3] = f.w;
+    }
+    nvfp4_block(v, ts, sb, c);
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = h2u(__floats2half2_rn(c[2 * j] * sb, c[2 * j + 1] * sb));
+    uint4* d = reinterpret_cast<uint4*>(dst + b * 16);
+    d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+// ----------------------------------------------------------------- tensor maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+template <int WFMT, int EPI>
+cudaError_t launch_gemm_t(const GemmMaps& m, const GemmParams& p, int mtiles, int max_items, cudaStream_t s) {
+  moe_gemm_kernel<WFMT, EPI><<<dim3(mtiles, max_items), kGThreads, kGSmemBytes, s>>>(
+      *reinterpret_cast<const CUtensorMap*>(&m.codes), *reinterpret_cast<const CUtensorMap*>(&m.scales),
+      *reinterpret_cast<const CUtensorMap*>(&m.act), p);
+  return cudaGetLastError();
+}
+
+template <int WFMT, int EPI>
+cudaError_t init_gemm_one() {
+  return cudaFuncSetAttribute(moe_gemm_kernel<WFMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kGSmemBytes);
+}
+
+}  // namespace
+
+static_assert(sizeof(CUtensorMap) == sizeof(TensorMapBytes), "tensor map storage size");
+
+bool make_tmap_2d(TensorMapBytes* out, const void* base, int elem_bytes, uint64_t inner, uint64_t rows,
+                  uint32_t box_inner, uint32_t box_rows, bool swizzle128) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  return fn(reinterpret_cast<CUtensorMap*>(out), dt, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool gemm_supported(int H, int I) { return H % 256 == 0 && I % 256 == 0 && H >= 256 && I >= 256; }
+
+int gemm_max_items(int T, int top_k, int E, bool routed, bool shared) {
+  const long tk = (long)T * top_k;
+  return (int)((routed ? tk / kBN + (tk < E ? tk : E) + 1 : 0) + (shared ? (T + kBN - 1) / kBN : 0));
+}
+
+cudaError_t gemm_kernels_init() {
+  cudaError_t e = cudaSuccess;
+  const cudaError_t r[] = {init_gemm_one<MOE_W_INT4_G32, 0>(), init_gemm_one<MOE_W_INT4_G32, 1>(),
+                           init_gemm_one<MOE_W_NVFP4, 0>(),    init_gemm_one<MOE_W_NVFP4, 1>(),
+                           init_gemm_one<kWF16, 0>(),          init_gemm_one<kWF16, 1>()};
+  for (cudaError_t x : r)
+    if (x != cudaSuccess) e = x;
+  return e;
+}
+
+cudaError_t launch_gemm_items(const int32_t* offsets, int E, int T, int top_k, int4* items, int32_t* n_items,
+                              cudaStream_t s) {
+  gemm_items_kernel<<<1, 32, 0, s>>>(offsets, E, T, top_k, items, n_items);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bf16_to_f16(const void* src, void* dst, size_t n, cudaStream_t s) {
+  size_t g = (n + 255) / 256;
+  if (g > 148 * 16) g = 148 * 16;
+  bf16_to_f16_kernel<<<(int)(g ? g : 1), 256, 0, s>>>(static_cast<const uint16_t*>(src), static_cast<__half*>(dst), n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_act(const void* x, int act_dtype, bool nvfp4, int H, const int32_t* entries, int Tk,
+                              int top_k, int rows, __half* dst, const unsigned int* amax_bits, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const bool xf = act_dtype == MOE_DT_F32;
+  if (nvfp4) {
+    if (xf) gather_act_kernel<MOE_DT_F32, true><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, dst, amax_bits);
+    else gather_act_kernel<MOE_DT_BF16, true><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, dst, amax_bits);
+  } else {
+    if (xf) gather_act_kernel<MOE_DT_F32, false><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, dst, amax_bits);
+    else gather_act_kernel<MOE_DT_BF16, false><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, dst, amax_bits);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_h(const float* h, size_t n, const unsigned int* amax_bits, __half* dst, cudaStream_t s) {
+  const size_t nb = n / 16;
+  if (nb == 0) return cudaSuccess;
+  size_t g = (nb + 255) / 256;
+  if (g > 148 * 16) g = 148 * 16;
+  quant_h_kernel<<<(int)g, 256, 0, s>>>(h, nb, amax_bits, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(int wfmt, int epi, const GemmMaps& m, const GemmParams& p, int mtiles, int max_items,
+                        cudaStream_t s) {
+  if (max_items <= 0) return cudaSuccess;
+  if (wfmt == MOE_W_INT4_G32)
+    return epi == 0 ? launch_gemm_t<MOE_W_INT4_G32, 0>(m, p, mtiles, max_items, s)
+                    : launch_gemm_t<MOE_W_INT4_G32, 1>(m, p, mtiles, max_items, s);
+  if (wfmt == MOE_W_NVFP4)
+    return epi == 0 ? launch_gemm_t<MOE_W_NVFP4, 0>(m, p, mtiles, max_items, s)
+                    : launch_gemm_t<MOE_W_NVFP4, 1>(m, p, mtiles, max_items, s);
+  if (wfmt == kWF16)
+    return epi == 0 ? launch_gemm_t<kWF16, 0>(m, p, mtiles, max_items, s)
+                    : launch_gemm_t<kWF16, 1>(m, p, mtiles, max_items, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -89,9 +89,56 @@ struct DecodeLaunch {
   uint32_t* sync;
   int* status;
   uint32_t spin_max;
+  unsigned long long* trace;   // optional per-CTA phase timestamps, or NULL
 };
 cudaError_t launch_decode_fused(const DecodeLaunch& d, int act_dtype, int router_dtype, int grid,
                                 cudaStream_t s);
+
+// ------------------------------------------------ grouped GEMM path (tcgen05)
+// Opaque storage of one CUtensorMap (128 bytes, 64-byte aligned).
+struct alignas(64) TensorMapBytes {
+  unsigned char b[128];
+};
+struct GemmMaps {
+  TensorMapBytes codes;    // packed weight codes [rows, K/2] bytes, 128 x 16 box, 128-byte swizzle
+  TensorMapBytes scales;   // weight scales [rows, K/16] bytes, 16 x 16 box
+  TensorMapBytes act;      // expert-sorted fp16 activations [rows, K], 64 x 16 box, 128-byte swizzle
+};
+// Weight storage of the grouped GEMM besides MOE_W_INT4_G32 / MOE_W_NVFP4: plain fp16
+// rows (a bf16 shared expert converted once at layer creation).
+constexpr int kWF16 = 3;
+
+struct GemmParams {
+  const int4* items;          // (expert, first sorted row, rows, 0)
+  const int32_t* n_items;     // device count of this launch's items
+  const int32_t* item_skip;   // device count of items to skip first, or NULL
+  int e_sub;                  // subtracted from the item's expert index to index the weights
+  int K;                      // reduction length (H for gate/up, I for down)
+  int rows_per_expert;        // 2I (gate/up) or H (down)
+  int H, I, T, top_k;
+  __half* h16;                // gate/up output [rows, I] (fp16)
+  float* h32;                 // gate/up output [rows, I] (fp32, NVFP4 layers)
+  unsigned int* h_amax;       // NVFP4: amax bits of the routed h
+  float* out_acc;             // down output [T, H] (fp32 accumulator)
+  const int32_t* entries;     // [T * top_k] token * top_k + slot, grouped by expert
+  const float* weights;       // [T * top_k]
+  const float* w_tscale;      // NVFP4 per-expert tensor scales of this matrix, or NULL
+  const unsigned int* act_amax;   // NVFP4: amax bits of the B activations, or NULL
+  int* status;
+};
+bool make_tmap_2d(TensorMapBytes* out, const void* base, int elem_bytes, uint64_t inner, uint64_t rows,
+                  uint32_t box_inner, uint32_t box_rows, bool swizzle128);
+bool gemm_supported(int H, int I);
+int gemm_max_items(int T, int top_k, int E, bool routed, bool shared);
+cudaError_t gemm_kernels_init();
+cudaError_t launch_gemm_items(const int32_t* offsets, int E, int T, int top_k, int4* items, int32_t* n_items,
+                              cudaStream_t s);
+cudaError_t launch_bf16_to_f16(const void* src, void* dst, size_t n, cudaStream_t s);
+cudaError_t launch_gather_act(const void* x, int act_dtype, bool nvfp4, int H, const int32_t* entries, int Tk,
+                              int top_k, int rows, __half* dst, const unsigned int* amax_bits, cudaStream_t s);
+cudaError_t launch_quant_h(const float* h, size_t n, const unsigned int* amax_bits, __half* dst, cudaStream_t s);
+cudaError_t launch_gemm(int wfmt, int epi, const GemmMaps& m, const GemmParams& p, int mtiles, int max_items,
+                        cudaStream_t s);
 
 // out[T, H] (act dtype) = out_acc
 cudaError_t launch_finalize(const float* out_acc, void* out, int act_dtype, size_t n,

@@ -45,12 +45,25 @@ struct moe_layer {
   int32_t* meta_g = nullptr;
   void* h16 = nullptr;
   float* dec_acc = nullptr;
+  // grouped tcgen05 GEMM path
+  bool gemm_ok = false;
+  int gemm_rows = 0;            // rows of the expert-sorted activation matrices
+  __half* x16s = nullptr;       // [gemm_rows, H] expert-sorted activations (fp16)
+  __half* h16s = nullptr;       // [gemm_rows, I] expert-sorted h (fp16)
+  float* h32 = nullptr;         // [T*k, I] routed h before NVFP4 quantisation
+  int4* gitems = nullptr;
+  int32_t* g_nitems = nullptr;
+  GemmMaps maps_up{}, maps_down{};
+  void* sh16_gu = nullptr;      // separately stored shared expert as fp16 [2I, H], [H, I]
+  void* sh16_d = nullptr;
+  GemmMaps maps_sh_up{}, maps_sh_down{};
   std::vector<void*> allocs;
   // measurement
   std::vector<cudaEvent_t> events;   // kStageEvents per recorded forward
   int timing_cap = 0;
   int timing_used = 0;
   int64_t launches = 0;
+  unsigned long long* trace = nullptr;   // decode-kernel phase timestamps (profiling)
 };
 
 static constexpr int kStageEvents = 7;
@@ -250,6 +263,38 @@ moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt,
     if (cudaMemsetAsync(L->dsync, 0, nsync * 4, s) || cudaMemsetAsync(L->dec_acc, 0, (size_t)Td * H * 4, s))
       return MOE_ERR_CUDA;
   }
+  // grouped GEMM path: expert-sorted activation buffers and the TMA descriptors; a
+  // separately stored (bf16) shared expert gets an fp16 copy for the same kernel
+  L->gemm_ok = gemm_supported(H, I) && gemm_kernels_init() == cudaSuccess &&
+               (L->shared_inline || c->shared_format == MOE_W_BF16);
+  if (L->gemm_ok) {
+    const int fmt = c->weight_format;
+    L->gemm_rows = Tm * k + Tm;
+    if ((st = dev_alloc(L, reinterpret_cast<void**>(&L->x16s), (size_t)L->gemm_rows * H * 2)) ||
+        (st = dev_alloc(L, reinterpret_cast<void**>(&L->h16s), (size_t)L->gemm_rows * I * 2)) ||
+        (st = dev_alloc_t(L, &L->gitems, (size_t)gemm_max_items(Tm, k, E, true, true) * sizeof(int4))) ||
+        (st = dev_alloc_t(L, &L->g_nitems, 4 * sizeof(int32_t))))
+      return st;
+    if (fmt == MOE_W_NVFP4 && (st = dev_alloc_t(L, &L->h32, (size_t)Tm * k * I * 4))) return st;
+    const uint64_t gu_rows = (uint64_t)n_store * 2 * I, d_rows = (uint64_t)n_store * H;
+    L->gemm_ok = make_tmap_2d(&L->maps_up.codes, L->w.gu_codes, 1, H / 2, gu_rows, 128, 16, true) &&
+                 make_tmap_2d(&L->maps_up.scales, L->w.gu_scales, 1, row_scale_bytes(fmt, H), gu_rows, 16, 16, false) &&
+                 make_tmap_2d(&L->maps_up.act, L->x16s, 2, H, L->gemm_rows, 64, 16, true) &&
+                 make_tmap_2d(&L->maps_down.codes, L->w.d_codes, 1, I / 2, d_rows, 128, 16, true) &&
+                 make_tmap_2d(&L->maps_down.scales, L->w.d_scales, 1, row_scale_bytes(fmt, I), d_rows, 16, 16, false) &&
+                 make_tmap_2d(&L->maps_down.act, L->h16s, 2, I, L->gemm_rows, 64, 16, true);
+    if (L->gemm_ok && !L->shared_inline) {
+      if ((st = dev_alloc(L, &L->sh16_gu, (size_t)2 * I * H * 2)) || (st = dev_alloc(L, &L->sh16_d, (size_t)H * I * 2)))
+        return st;
+      if (launch_bf16_to_f16(L->ws.gu_codes, L->sh16_gu, (size_t)2 * I * H, s) ||
+          launch_bf16_to_f16(L->ws.d_codes, L->sh16_d, (size_t)H * I, s))
+        return MOE_ERR_CUDA;
+      L->maps_sh_up = L->maps_up;
+      L->maps_sh_down = L->maps_down;
+      L->gemm_ok = make_tmap_2d(&L->maps_sh_up.codes, L->sh16_gu, 2, H, 2 * I, 64, 16, true) &&
+                   make_tmap_2d(&L->maps_sh_down.codes, L->sh16_d, 2, I, H, 64, 16, true);
+    }
+  }
   if (cudaMemsetAsync(L->status, 0, sizeof(int), s) || cudaMemsetAsync(L->meta, 0, 16 * 4, s))
     return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -283,6 +328,65 @@ void release_events(moe_layer* L) {
   L->timing_cap = L->timing_used = 0;
 }
 
+// Grouped tcgen05 path after routing: expert-sorted activations, gate/up GEMM with the
+// SwiGLU epilogue, down GEMM with the weighted-combine epilogue, output conversion.
+moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStream_t s, StageMarks& m) {
+  const moe_config& c = L->cfg;
+  const int H = c.hidden, I = c.inter, E = c.n_experts, k = c.top_k;
+  const bool nvfp4 = c.weight_format == MOE_W_NVFP4;
+  const int Tk = T * k;
+  const bool inl = L->shared_inline;
+  // inline shared expert: one launch covers routed and shared items (n_items[2]);
+  // otherwise the routed items (n_items[0]) and the fp16 shared expert (n_items[1], after
+  // the routed ones) are separate launches
+  const int routed_max = gemm_max_items(T, k, E, true, inl);
+  const int shared_max = gemm_max_items(T, k, E, false, true);
+  MOE_LAUNCH(launch_gemm_items(L->offsets, E, T, k, L->gitems, L->g_nitems, s));
+  if (nvfp4) MOE_LAUNCH(launch_amax(x, c.act_dtype, (size_t)T * H, L->amax, s));
+  MOE_LAUNCH(launch_gather_act(x, c.act_dtype, nvfp4, H, L->entries, Tk, k, Tk + T, L->x16s, L->amax, s));
+  MOE_CK(m.mark(2));
+  GemmParams p{};
+  p.items = L->gitems;
+  p.n_items = L->g_nitems + (inl ? 2 : 0);
+  p.H = H;
+  p.I = I;
+  p.T = T;
+  p.top_k = k;
+  p.h16 = L->h16s;
+  p.h32 = L->h32;
+  p.h_amax = L->amax + 1;
+  p.out_acc = L->out_acc;
+  p.entries = L->entries;
+  p.weights = L->weights;
+  p.status = L->status;
+  GemmParams ps = p;   // separately stored fp16 shared expert
+  ps.n_items = L->g_nitems + 1;
+  ps.item_skip = L->g_nitems;
+  ps.e_sub = E;
+  ps.w_tscale = nullptr;
+  ps.act_amax = nullptr;
+
+  p.K = ps.K = H;
+  p.rows_per_expert = ps.rows_per_expert = 2 * I;
+  p.w_tscale = L->w.gu_tscale;
+  p.act_amax = L->amax;
+  MOE_LAUNCH(launch_gemm(c.weight_format, 0, L->maps_up, p, 2 * I / 128, routed_max, s));
+  if (!inl) MOE_LAUNCH(launch_gemm(kWF16, 0, L->maps_sh_up, ps, 2 * I / 128, shared_max, s));
+  MOE_CK(m.mark(3));
+  if (nvfp4) MOE_LAUNCH(launch_quant_h(L->h32, (size_t)Tk * I, L->amax + 1, L->h16s, s));
+  MOE_CK(m.mark(4));
+  p.K = ps.K = I;
+  p.rows_per_expert = ps.rows_per_expert = H;
+  p.w_tscale = L->w.d_tscale;
+  p.act_amax = L->amax + 1;
+  MOE_LAUNCH(launch_gemm(c.weight_format, 1, L->maps_down, p, H / 128, routed_max, s));
+  if (!inl) MOE_LAUNCH(launch_gemm(kWF16, 1, L->maps_sh_down, ps, H / 128, shared_max, s));
+  MOE_CK(m.mark(5));
+  MOE_LAUNCH(launch_finalize(L->out_acc, out, c.act_dtype, (size_t)T * H, s));
+  MOE_CK(m.mark(6));
+  return MOE_OK;
+}
+
 moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStream_t s) {
   const moe_config& c = L->cfg;
   const int H = c.hidden, I = c.inter, E = c.n_experts, k = c.top_k;
@@ -290,8 +394,11 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
   StageMarks m;
   m.s = s;
   if (L->timing_used < L->timing_cap) m.ev = &L->events[(size_t)kStageEvents * L->timing_used++];
-  const bool decode = L->decode_ok && T <= 8 && (long)T * k <= 64 && L->path != MOE_PATH_GROUPED;
+  const bool decode = L->decode_ok && T <= 8 && (long)T * k <= 64 &&
+                     (L->path == MOE_PATH_AUTO || L->path == MOE_PATH_GEMV);
   if (L->path == MOE_PATH_GEMV && !decode) return MOE_ERR_UNSUPPORTED;
+  if (L->path == MOE_PATH_GROUPED && !L->gemm_ok) return MOE_ERR_UNSUPPORTED;
+  const bool gemm = !decode && L->gemm_ok && L->path != MOE_PATH_GENERIC;
   if (decode) {
     // one fused kernel: routing, gate/up, down + combine (recorded in the third stage slot)
     MOE_CK(m.mark(0));
@@ -300,7 +407,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
     DecodeLaunch d{x, T, L->router_w, L->bias, H, I, E, k, c.n_group, c.topk_group,
                    c.routed_scaling_factor, L->up_store, L->down_store, L->logits, L->ids,
                    L->weights, L->offsets, L->entries, L->active_g, L->meta_g, L->h16, L->dec_acc,
-                   out, L->dsync, L->status, 1u << 22};
+                   out, L->dsync, L->status, 1u << 22, L->trace};
     MOE_LAUNCH(launch_decode_fused(d, c.act_dtype, c.router_dtype, L->n_sm, s));
     for (int i = 3; i < kStageEvents; ++i) MOE_CK(m.mark(i));
     return MOE_OK;
@@ -315,6 +422,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
   MOE_LAUNCH(launch_group(L->ids, L->counts, T, k, E, L->shared_inline, L->offsets, L->entries,
                           L->items, L->meta, s));
   MOE_CK(m.mark(1));
+  if (gemm) return forward_gemm(L, x, T, out, s, m);
   const void* x_in = x;
   int x_dt = c.act_dtype;
   if (nvfp4) {
@@ -445,7 +553,7 @@ moe_status moe_layer_get_routing(moe_layer* L, int32_t T, int32_t* ids, float* w
 }
 
 moe_status moe_layer_set_path(moe_layer* L, int32_t path) {
-  if (!L || path < MOE_PATH_AUTO || path > MOE_PATH_GROUPED) return MOE_ERR_INVALID_ARG;
+  if (!L || path < MOE_PATH_AUTO || path > MOE_PATH_GENERIC) return MOE_ERR_INVALID_ARG;
   L->path = path;
   return MOE_OK;
 }
@@ -491,6 +599,12 @@ moe_status moe_layer_stage_times(moe_layer* L, float* ms, int32_t* n_forwards) {
   }
   if (n_forwards) *n_forwards = L->timing_used;
   L->timing_used = 0;
+  return MOE_OK;
+}
+
+moe_status moe_layer_set_trace(moe_layer* L, void* buffer, int32_t n_ctas) {
+  if (!L || n_ctas < 0 || (buffer && n_ctas < L->n_sm)) return MOE_ERR_INVALID_ARG;
+  L->trace = buffer ? static_cast<unsigned long long*>(buffer) : nullptr;
   return MOE_OK;
 }
 

@@ -1,0 +1,88 @@
+"""Run a few forwards of a seeded synthetic layer, for profilers (ncu) and phase traces.
+
+    python -m quantized_moe_noaux_b300.profile_run --layer glm52 --tokens 1 --iters 5
+    python -m quantized_moe_noaux_b300.profile_run --layer glm52_skewed --tokens 2048 --path grouped
+    python -m quantized_moe_noaux_b300.profile_run --layer glm52 --tokens 1 --trace trace.npy
+
+Each iteration is one ``moe_layer_forward`` on fresh seeded activations. ``--copies`` layer
+copies are used in turn so consecutive forwards read different weights (as in the
+benchmark). ``--trace`` records the fused decode kernel's per-CTA phase timestamps of the
+last iteration (``moe_layer_set_trace``) and saves them as a numpy array [CTAs, 16] in ns.
+No comparison against a reference is made here: the tests do that.
+"""
+
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import numpy as np
+
+PHASES = ["start", "activation panel", "router rows", "routing published", "shared gate/up",
+          "shared gate/up seen", "shared down", "routing seen", "routed gate/up",
+          "first routed gate/up seen", "routed down", "all down seen", "output written",
+          "producer: shared issued", "producer: routing seen"]
+
+_PATHS = {"auto": 0, "gemv": 1, "grouped": 2, "generic": 3}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--layer", default="glm52")
+    ap.add_argument("--tokens", type=int, default=1)
+    ap.add_argument("--iters", type=int, default=5)
+    ap.add_argument("--copies", type=int, default=1)
+    ap.add_argument("--path", default="auto", choices=sorted(_PATHS))
+    ap.add_argument("--trace", default=None, help="save decode phase timestamps here (.npy)")
+    args = ap.parse_args(argv)
+
+    import torch
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    import quantized_moe_noaux_b300 as moe
+    from synth import LAYERS, make_layer, make_x
+
+    spec = LAYERS[args.layer]
+    arrays = make_layer(spec)
+    T = args.tokens
+    layers = [moe.MoeLayer.from_spec(spec, arrays, max_tokens=T) for _ in range(max(1, args.copies))]
+    for L in layers:
+        L.set_path(_PATHS[args.path])
+    dt = torch.bfloat16 if spec.act_dtype == "bf16" else torch.float32
+
+    def dev(x):
+        if spec.act_dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+    xs = [dev(make_x(spec, T, s)) for s in range(args.iters)]
+    out = torch.empty((T, spec.hidden), dtype=dt, device="cuda")
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    buf = torch.zeros((nsm, 16), dtype=torch.int64, device="cuda") if args.trace else None
+    for s in range(args.iters):
+        L = layers[s % len(layers)]
+        if buf is not None and s == args.iters - 1:
+            torch.cuda.synchronize()
+            L.set_trace(buf, nsm)
+        L.forward(xs[s], out)
+    torch.cuda.synchronize()
+    for L in layers:
+        if L.status() != 0:
+            raise SystemExit("device status word set")
+    if buf is not None:
+        t = buf.cpu().numpy()
+        np.save(args.trace, t)
+        t0 = t[:, 0][t[:, 0] > 0].min() if (t[:, 0] > 0).any() else 0
+        for i, name in enumerate(PHASES):
+            v = t[:, i][t[:, i] > 0] - t0
+            if v.size:
+                print(f"{i:2d} {name:26s} CTAs={v.size:3d}  min {v.min() / 1e3:8.2f}  "
+                      f"median {np.median(v) / 1e3:8.2f}  max {v.max() / 1e3:8.2f} us")
+    print(f"ok: {args.iters} forwards of {spec.name} at T={T} (path {args.path})")
+
+
+if __name__ == "__main__":
+    main()

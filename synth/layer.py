@@ -98,6 +98,9 @@ LAYERS = {
     "tiny": _TINY,
     # smallest shape the fused decode kernel runs (2048-column panels, 32-expert groups)
     "small": _SMALL,
+    # the same shape with NVFP4 routed experts, bf16 router and bf16 shared expert
+    "small_nvfp4": replace(_SMALL, name="small_h2048_e32_nvfp4", weight_format="nvfp4",
+                           router_dtype="bf16", shared_format="bf16"),
     "glm52": _GLM,
     # decode at T=4 / T=32: the router is left unbiased so tokens share experts
     "glm52_unbiased": replace(_GLM, name="glm52_h6144_e256_int4g32_bias0", bias_std=0.0),
