@@ -140,6 +140,16 @@ def measured_peaks():
         return 6400.0, "fallback"
 
 
+def measured_tflops():
+    """Dense bf16 (= fp16 kind::f16 rate) tensor peak: the measured burst figure."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d["bf16_tflops"], "measured burst bf16 (kind::f16 runs fp16 at the same rate)"
+    except Exception:
+        return 1800.0, "fallback"
+
+
 def expert_bytes(spec):
     """Stored bytes of one expert: (gate/up, down)."""
     H, I = spec.hidden, spec.inter
@@ -153,16 +163,28 @@ def expert_bytes(spec):
 # ----------------------------------------------------------------- CPU oracle
 
 
-def oracle_tokens_per_s(spec, arrays, T, budget_s, step0=0):
+def oracle_tokens_per_s(spec, arrays, T, budget_s, step0=0, max_tokens=8):
     """Time the fp64 oracle on successive steps of the workload until ``budget_s``
-    seconds have passed (at least one step). Returns (tokens/s, steps, threads)."""
+    seconds have passed (at least one step). Each step routes all T tokens and runs the
+    expert FFNs and the combine for the first min(T, max_tokens) of them (the oracle's
+    ``tokens=`` restriction), so a step of a large batch stays a bounded sample (NVFP4
+    layers, whose h tensor scale depends on every routed token, run the first
+    min(T, max_tokens) tokens as a batch of their own instead). Returns
+    (tokens/s over the sampled tokens, steps, threads, seconds, sampled tokens per step)."""
     from oracle.moe_oracle import Layer
     from synth import make_x
     layer = Layer.from_spec(spec, arrays)
+    n = min(T, max_tokens)
+    toks = np.arange(n)
     t0 = time.perf_counter()
     steps = 0
     while True:
-        layer.forward(make_x(spec, T, step0 + steps))
+        x = make_x(spec, T, step0 + steps)
+        if spec.weight_format == "nvfp4":
+            # the h tensor scale needs every routed h of the batch: sample a T=n batch
+            layer.forward(x[:n])
+        else:
+            layer.forward(x, tokens=toks)
         steps += 1
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -172,7 +194,7 @@ def oracle_tokens_per_s(spec, arrays, T, budget_s, step0=0):
         threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
     except Exception:
         threads = 1
-    return steps * T / dt, steps, threads, dt
+    return steps * n / dt, steps, threads, dt, n
 
 
 # --------------------------------------------------------------------- arms
@@ -189,9 +211,9 @@ def run_reference(args):
     budget = min(150.0, max(10.0, 0.15 * (args.steps + args.warmup)))
     if args.warmup:
         oracle_tokens_per_s(spec, arrays, T, 0.0, step0=10_000)
-    value, steps, threads, dt = oracle_tokens_per_s(spec, arrays, T, budget)
-    sample = (f"fp64 numpy oracle, first {steps} of the {args.steps} steps' tokens "
-              f"(T={T} each, {dt:.1f} s time-bounded)")
+    value, steps, threads, dt, n = oracle_tokens_per_s(spec, arrays, T, budget)
+    sample = (f"fp64 numpy oracle, {steps} steps of the workload (T={T} routed, expert FFNs and "
+              f"combine for {n} tokens per step), {dt:.1f} s time-bounded")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * dt / steps, "higher_is_better": True, "scaling": "weak",
@@ -321,28 +343,53 @@ def run_ours(args):
     gu_b, d_b = expert_bytes(spec)
     n_units = sum(u + 1 for u in uniq)                # routed unique + shared, over K steps
     router_b = spec.n_experts * spec.hidden * (4 if spec.router_dtype == "f32" else 2)
+    if spec.shared_format == "bf16":                  # separately stored bf16 shared expert
+        sh_gu_b, sh_d_b = 2 * spec.inter * spec.hidden * 2, spec.hidden * spec.inter * 2
+        n_units -= K
+        unit_gu = n_units * gu_b + K * sh_gu_b
+        unit_all = n_units * (gu_b + d_b) + K * (sh_gu_b + sh_d_b)
+    else:
+        unit_gu = n_units * gu_b
+        unit_all = n_units * (gu_b + d_b)
     fused = launches == K                              # decode path: one kernel per step
+    peak_bw, peak_kind = measured_peaks()
+    peak_tf, tf_kind = measured_tflops()
+    step_s = ms / K / 1000.0
     if fused:
         dom = "gate_up_or_fused"
-        dom_bytes = n_units * (gu_b + d_b) + K * router_b
-        kernel_name = "moe_decode_kernel (router, selection, gate/up, down, combine)"
+        dom_bytes = unit_all + K * router_b
+        dom_s = stage_ms[dom] / 1000.0
+        achieved = dom_bytes / dom_s / 1e9
+        roofline = {"bound": "hbm", "kernel": "moe_decode_kernel (router, selection, gate/up, down, combine)",
+                    "achieved": achieved, "peak": peak_bw, "peak_kind": peak_kind, "unit": "GB/s",
+                    "frac": achieved / peak_bw, "traffic": None, "bytes_per_launch": dom_bytes / K}
     else:
-        dom = max(("gate_up_or_fused", "down_combine"), key=lambda k: stage_ms[k])
-        dom_bytes = n_units * (gu_b if dom == "gate_up_or_fused" else d_b)
-        kernel_name = "expert_up_kernel" if dom == "gate_up_or_fused" else "expert_down_kernel"
-    dom_s = stage_ms[dom] / 1000.0
-    peak, peak_kind = measured_peaks()
-    achieved = dom_bytes / dom_s / 1e9
-    step_bytes = n_units * (gu_b + d_b) / K
-    roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": achieved, "peak": peak,
-                "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
-                "bytes_per_launch": dom_bytes / K,
-                "step_expert_bytes": step_bytes,
-                "step_expert_gbs": step_bytes / (ms / K / 1000.0) / 1e9,
-                "frac_of_8tbs_nominal": step_bytes / (ms / K / 1000.0) / 8e12}
+        # dominant kernel: the gate/up GEMM (2/3 of the FLOPs and of the weight bytes)
+        dom = "gate_up_or_fused"
+        dom_s = stage_ms[dom] / 1000.0
+        rows = T * spec.top_k + T
+        flops = K * 2.0 * rows * 2 * spec.inter * spec.hidden
+        intensity = flops / unit_gu
+        if intensity > peak_tf * 1e12 / (peak_bw * 1e9):
+            achieved = flops / dom_s / 1e12
+            roofline = {"bound": "tensor", "kernel": "moe_gemm_kernel gate/up (tcgen05 kind::f16)",
+                        "achieved": achieved, "peak": peak_tf, "peak_kind": tf_kind, "unit": "TFLOP/s",
+                        "frac": achieved / peak_tf, "traffic": None, "flops_per_step": flops / K,
+                        "weight_bytes_per_step": unit_gu / K}
+        else:
+            achieved = unit_gu / dom_s / 1e9
+            roofline = {"bound": "hbm", "kernel": "moe_gemm_kernel gate/up (tcgen05 kind::f16)",
+                        "achieved": achieved, "peak": peak_bw, "peak_kind": peak_kind, "unit": "GB/s",
+                        "frac": achieved / peak_bw, "traffic": None, "bytes_per_launch": unit_gu / K,
+                        "flops_per_step": flops / K}
+        all_flops = K * 2.0 * rows * 3 * spec.inter * spec.hidden
+        roofline["layer_tflops"] = all_flops / (ms / 1000.0) / 1e12
+    roofline["step_expert_bytes"] = unit_all / K
+    roofline["step_expert_gbs"] = unit_all / K / step_s / 1e9
+    roofline["frac_of_8tbs_nominal"] = unit_all / K / step_s / 8e12
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, random-init weights)",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded, random-init weights)",
             "config": {"workload": wl.name, "tokens_per_step": T, "layer": spec.name,
                        "layer_copies": C, "l2": f"inputs larger than L2: {C} layer copies "
                        "rotated per step, each step streams its experts from HBM",
@@ -357,9 +404,10 @@ def run_ours(args):
                     "d2h_bytes_per_step": T * H * (2 if spec.act_dtype == "bf16" else 4),
                     "steps": KE}}
     if world == 1 and not args.no_cpu_baseline:
-        v, steps, threads, dt_cpu = oracle_tokens_per_s(spec, arrays, T, args.cpu_budget)
+        v, steps, threads, dt_cpu, n = oracle_tokens_per_s(spec, arrays, T, args.cpu_budget)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
-                                "sample": f"{steps} steps of T={T} ({dt_cpu:.1f} s), fp64 numpy"}
+                                "sample": f"{steps} steps of the workload, T={T} routed, {n} tokens "
+                                          f"through the experts per step ({dt_cpu:.1f} s), fp64 numpy"}
     print(json.dumps(line), flush=True)
     for L in layers:
         L.close()

@@ -106,6 +106,10 @@ LAYERS = {
     "glm52_unbiased": replace(_GLM, name="glm52_h6144_e256_int4g32_bias0", bias_std=0.0),
     # prefill: a wide bias skews the per-expert load
     "glm52_skewed": replace(_GLM, name="glm52_h6144_e256_int4g32_bias0.5", bias_std=0.5),
+    # GLM shapes with 64 routed experts and a wide bias: a 2.8 GB profiling stand-in for the
+    # skewed prefill layer (same per-expert matrices, a quarter of the experts)
+    "glm52_e64_skewed": replace(_GLM, name="glm52_h6144_e64_int4g32_bias0.5", n_experts=64,
+                                bias_std=0.5),
     # NVFP4 routed experts; router and shared expert stay bf16
     "glm52_nvfp4": replace(_GLM, name="glm52_h6144_e256_nvfp4", weight_format="nvfp4",
                            router_dtype="bf16", shared_format="bf16"),
