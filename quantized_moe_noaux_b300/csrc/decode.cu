@@ -2,31 +2,40 @@
 // it reads.
 //
 // One persistent cooperative grid (one CTA per SM) runs the whole layer forward of a decode
-// step: router logits, noaux_tc selection and batch-union grouping (by the last CTA to finish
-// its router rows), the SwiGLU gate/up projection of the shared and the selected experts, and
-// the down projection fused with the weighted combine ("Show HN: Menjalankan GLM 5.2 di
-// komputer lambat", section "Fitur utama yang diimplementasikan": DeepSeek-V3-style router
-// with noaux_tc, routed_scaling_factor and a shared expert; packed int4 with dequant-on-use;
-// batch-union MoE). Every selected expert's weights are streamed from HBM exactly once.
+// step: router logits, noaux_tc selection and batch-union grouping, the SwiGLU gate/up
+// projection of the shared and the selected experts, and the down projection fused with the
+// weighted combine ("Show HN: Menjalankan GLM 5.2 di komputer lambat", section "Fitur utama
+// yang diimplementasikan": DeepSeek-V3-style router with noaux_tc, routed_scaling_factor and
+// a shared expert; packed int4 with dequant-on-use; batch-union MoE). Every selected expert's
+// weights are streamed from HBM exactly once.
 //
 // Weights are repacked at layer creation into 16-row tiles in the register-fragment order of
 // the m16n8k16 fp16 MMA. One 32-bit word holds the 8 int4 codes a lane needs for one MMA;
 // a shift and four LOP3s turn it into the four fp16 A registers: (code + 8) is placed in the
 // mantissa of 1024.0 (rows 0-7: value 1032 + c) or at mantissa bit 4 (rows 8-15: value
 // 1152 + 16c). The MMA accumulates in fp32; the per-row bias (1032 or 1152 times the group's
-// activation sum) is removed and the fp16 group scale applied once per 32-element group (or
-// once per 8 groups when the single token's groups occupy the MMA's 8 columns).
+// activation sum) is removed and the fp16 group scale applied once per 32-element group.
+// Column layout of the MMA's B operand:
+//   MODE 1 (one token): column n of MMA m holds the token's values of group (m/2) mod 8, so the
+//     8 groups of a 256-column k-block land in 8 accumulator columns; the operand is built in
+//     registers from a compact fp16 copy of the activation (the other columns are zero);
+//   MODE 0 (2..8 tokens): column n holds token n, from a fragment-ordered activation panel.
 //
-// Work per CTA, in order, each item a 16-row x 2048-column panel (18 KB) brought in by a
-// producer warp with TMA bulk copies into a 4-slot ring:
+// Work per CTA, in order, each item a 16-row x 2048-column panel (18 KB) brought in by the
+// producer warp with TMA bulk copies into a ring of slots:
+//   consumers: activations staged; router rows e = cta, cta + grid (unrolled vector loads)
 //   A  shared-expert gate/up tiles           (no dependency)
 //   C1 shared-expert down tiles              (waits until every shared gate/up tile is done)
-//   B  selected experts' gate/up tiles       (waits for the routing flag)
+//   B  selected experts' gate/up tiles       (waits for the routing, in shared memory)
 //   C2 selected experts' down tiles          (waits until that expert's gate/up tiles are done)
+// The producer warp issues the shared-expert items, then waits until every CTA has written
+// its router rows and computes the selection and grouping itself (every CTA obtains the same
+// routing from the same logits; CTA 0 also writes it out), then issues the routed items.
 // Down tiles add w * y into an fp32 accumulator with atomics; after a grid-wide count every
-// CTA converts its slice to the output type. Gate/up completion is published per expert with
-// one release-add per run of tiles. All inter-CTA waits are bounded; on time-out the kernel
-// records MOE_ERR_TIMEOUT, drains its own copies in flight and returns.
+// CTA converts its slice to the output type. All inter-CTA waits are bounded; on time-out
+// the kernel records MOE_ERR_TIMEOUT, drains its own copies in flight and returns.
+#include <cstddef>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "route_dev.cuh"
@@ -37,7 +46,6 @@ namespace {
 
 constexpr int kDecThreads = 288;      // 8 consumer warps + 1 producer warp
 constexpr int kConsumers = 256;
-constexpr int kSlots = 4;
 constexpr int kPanelK = 2048;          // columns per item
 constexpr int kCodeBytes = 16384;      // 16 rows x 2048 int4
 constexpr int kScaleBytes = 2048;      // 16 rows x 64 groups fp16
@@ -45,43 +53,73 @@ constexpr int kItemBytes = kCodeBytes + kScaleBytes;
 constexpr int kMaxH = 6144;
 constexpr int kMaxI = 2048;
 constexpr int kMaxE = 256;
+constexpr int kMaxK = 16;
 constexpr int kMaxActive = 64;         // T * top_k <= 64 on this path
-constexpr int kMaxPairs = kMaxActive + 8;
 constexpr uint32_t kMbarSpin = 1u << 22;
 
-struct Smem {
-  uint8_t slots[kSlots][kItemBytes];
-  uint2 xpanel[kMaxH / 16 * 32];       // B fragments of x: 8 bytes per lane per MMA
-  union {
-    uint2 hpanel[kMaxI / 16 * 32];     // B fragments of h (down tiles)
-    struct {
-      float b[8][kMaxE];               // selection scratch (biased scores)
-      float s[8][kMaxE];               // selection scratch (sigmoid scores)
-    } sel;
-  } u;
-  float xsums[kMaxH / 32 * 8];         // per-group activation sums [group][column]
-  float hsums[kMaxI / 32 * 8];
+// Shared memory common to both modes (16-byte aligned: the reduction buffer takes float4
+// stores).
+struct alignas(16) DecCommon {
   float red[8][32][4];                 // cross-warp reduction
-  uint64_t full[kSlots];
-  uint64_t empty[kSlots];
-  uint64_t route_bar;
-  int sid[kMaxPairs];
+  float selb[kMaxE];                   // selection scratch (producer warp)
+  float sels[kMaxE];
+  int idsel[8][kMaxK];                 // per token: selected experts and weights
+  float wsel[8][kMaxK];
   int cnt[kMaxE];
-  int soff[kMaxE + 1];
-  int aslot[kMaxE];                    // expert -> active slot (selection CTA)
+  int soff[kMaxE];
+  int aslot[kMaxE];
   int active[kMaxE];
   int meta_pair[kMaxActive][8];        // per active expert: h row of token n (-1: not routed)
   float meta_w[kMaxActive][8];         // per active expert: combine weight of token n
   int colpair[8];
   float colw[8];
   int n_active;
-  int flag;          // broadcast word
+  int flag;
   int abort;
   int issued;
   int consumed;
 };
 
-static_assert(sizeof(Smem) <= 227 * 1024, "decode kernel shared memory over the per-CTA limit");
+template <int MODE>
+struct DecSmem;
+
+template <>
+struct DecSmem<1> {
+  static constexpr int kSlots = 8;
+  uint8_t slots[kSlots][kItemBytes];
+  uint32_t xs[kMaxH / 2];              // compact fp16 pairs of the token's activation
+  uint32_t hs[kMaxI / 2];              // compact fp16 pairs of the current h row
+  float xsums[kMaxH / 32];             // per 32-element group: sum of the fp16 values
+  float hsums[kMaxI / 32];
+  uint64_t full[kSlots];
+  uint64_t empty[kSlots];
+  uint64_t route_bar;
+  DecCommon c;
+};
+
+template <>
+struct DecSmem<0> {
+  static constexpr int kSlots = 3;
+  uint8_t slots[kSlots][kItemBytes];
+  uint2 xpanel[kMaxH / 16 * 32];       // B fragments of x: 8 bytes per lane per MMA
+  uint2 hpanel[kMaxI / 16 * 32];       // B fragments of h
+  float xsums[kMaxH / 32 * 8];         // per group and column: sum of the fp16 values
+  float hsums[kMaxI / 32 * 8];
+  uint64_t full[kSlots];
+  uint64_t empty[kSlots];
+  uint64_t route_bar;
+  DecCommon c;
+};
+
+static_assert(offsetof(DecSmem<1>, c) % 16 == 0 && offsetof(DecSmem<0>, c) % 16 == 0,
+              "vector stores into the common block need 16-byte alignment");
+static_assert(offsetof(DecSmem<1>, xs) % 16 == 0 && offsetof(DecSmem<1>, hs) % 16 == 0,
+              "vector accesses into the staged activations need 16-byte alignment");
+static_assert(offsetof(DecSmem<0>, xsums) % 8 == 0 && offsetof(DecSmem<1>, xsums) % 8 == 0 &&
+                  offsetof(DecSmem<0>, hsums) % 8 == 0 && offsetof(DecSmem<1>, hsums) % 8 == 0,
+              "float2 reads of the group sums need 8-byte alignment");
+static_assert(sizeof(DecSmem<1>) <= 227 * 1024, "decode kernel shared memory over the per-CTA limit");
+static_assert(sizeof(DecSmem<0>) <= 227 * 1024, "decode kernel shared memory over the per-CTA limit");
 
 // ------------------------------------------------------------------ helpers
 
@@ -124,167 +162,219 @@ __device__ __forceinline__ void seg_range(int n, int G, int c, int& b, int& e) {
   e = (int)(((long)n * (c + 1)) / G);
 }
 
-// ----------------------------------------------------- consumer: B panels
-
-// Group sums of a B panel: per group j (MMAs 2j, 2j+1) and column n, the sum of the 32
-// fp16 values column n holds (exactly the values the MMA multiplies).
-template <int MODE>
-__device__ void panel_sums(const uint2* panel, float* sums, int ngroups, int ncols) {
-  for (int idx = threadIdx.x; idx < ngroups * 8; idx += kConsumers) {
-    const int j = idx >> 3, n = idx & 7;
-    float s = 0.f;
-    if ((MODE == 1 && n == 0) || (MODE == 0 && n < ncols)) {
-      const int gg = (MODE == 1) ? (j & 7) : n;   // lane group holding this column
-#pragma unroll
-      for (int mm = 0; mm < 2; ++mm)
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const uint2 v = panel[(2 * j + mm) * 32 + gg * 4 + t];
-          const float2 f0 = half2_to_float2(v.x), f1 = half2_to_float2(v.y);
-          s += (f0.x + f0.y) + (f1.x + f1.y);
-        }
-    }
-    if (MODE == 1) {
-      if (n == 0) sums[j] = s;
-    } else {
-      sums[idx] = s;
-    }
-  }
-}
-
+// 8 consecutive activation elements at element index idx (bf16 or fp32 storage).
 template <int XDT>
-__device__ __forceinline__ uint32_t x_pair_half2(const void* x, size_t i) {
+__device__ __forceinline__ void load_act8(const void* x, size_t idx, float (&v)[8]) {
   if constexpr (XDT == MOE_DT_F32) {
-    const float2 f = __ldg(reinterpret_cast<const float2*>(static_cast<const float*>(x) + i));
-    return pack_half2(f.x, f.y);
+    const float4 a = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(x) + idx));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(x) + idx) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
   } else {
-    const uint32_t u = __ldg(reinterpret_cast<const unsigned int*>(static_cast<const unsigned short*>(x) + i));
-    return pack_half2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(x) + idx));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v[2 * q] = __uint_as_float(w[q] << 16);
+      v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+    }
   }
 }
 
-// x panel: MODE 1 (one token): column n of MMA m holds group (m/2) mod 8 only, so the 8
-// groups of a 256-column k-block land in 8 different accumulator columns. MODE 0: column n
-// holds token n (zero for n >= T).
-template <int MODE, int XDT>
-__device__ void build_x_panel(Smem& S, const void* x, const Geo& g) {
-  const int nm = g.H / 16;
-  for (int idx = threadIdx.x; idx < nm * 32; idx += kConsumers) {
-    const int m = idx >> 5, ln = idx & 31, gg = ln >> 2, t = ln & 3;
-    int tok = -1;
-    if (MODE == 1) {
-      if (gg == ((m >> 1) & 7)) tok = 0;
-    } else if (gg < g.T) {
-      tok = gg;
-    }
-    uint2 v = make_uint2(0u, 0u);
-    if (tok >= 0) {
-      const size_t base = (size_t)tok * g.H + 16 * m + 2 * t;
-      v.x = x_pair_half2<XDT>(x, base);
-      v.y = x_pair_half2<XDT>(x, base + 8);
-    }
-    S.xpanel[idx] = v;
+// Sum of the fp16 values held by 4 half2 words.
+__device__ __forceinline__ float sum4h2(const uint32_t (&p)[4]) {
+  float s = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 f = half2_to_float2(p[q]);
+    s += f.x + f.y;
   }
-  ptx::bar_sync(1, kConsumers);
-  panel_sums<MODE>(S.xpanel, S.xsums, g.H / 32, g.T);
+  return s;
 }
 
-// h panel of the current expert (rows S.colpair), read through L2: the h rows were written
-// by other CTAs of this grid.
-template <int MODE>
-__device__ void build_h_panel(Smem& S, const __half* h16, const Geo& g) {
-  const int nm = g.I / 16;
-  for (int idx = threadIdx.x; idx < nm * 32; idx += kConsumers) {
-    const int m = idx >> 5, ln = idx & 31, gg = ln >> 2, t = ln & 3;
-    int row = -1;
-    if (MODE == 1) {
-      if (gg == ((m >> 1) & 7)) row = S.colpair[0];
-    } else {
-      row = S.colpair[gg];
+// ------------------------------------------------------------- activation staging
+
+// MODE 1: compact fp16 pairs of token 0 and the per-group sums (thread per 32-element group).
+template <int XDT>
+__device__ void stage_x1(DecSmem<1>& S, const void* x, int H) {
+  for (int j = threadIdx.x; j < H / 32; j += kConsumers) {
+    float s = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float v[8];
+      load_act8<XDT>(x, (size_t)32 * j + 8 * q, v);
+      uint32_t p[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) p[i] = pack_half2(v[2 * i], v[2 * i + 1]);
+      s += sum4h2(p);
+      *reinterpret_cast<uint4*>(&S.xs[16 * j + 4 * q]) = make_uint4(p[0], p[1], p[2], p[3]);
     }
-    uint2 v = make_uint2(0u, 0u);
-    if (row >= 0) {
-      const unsigned int* src = reinterpret_cast<const unsigned int*>(h16 + (size_t)row * g.I + 16 * m + 2 * t);
-      v.x = __ldcg(src);
-      v.y = __ldcg(src + 4);
+    S.xsums[j] = s;
+  }
+}
+
+// MODE 0: fragment panel (column n = token n, zero for n >= T) and per-(group, token) sums.
+// Element pair (k, k+1), k = 16 m + r, goes to lane (token, (r mod 8) / 2), half r / 8.
+template <int XDT>
+__device__ void stage_x0(DecSmem<0>& S, const void* x, int T, int H) {
+  const int ng = H / 32;
+  for (int idx = threadIdx.x; idx < ng * 8; idx += kConsumers) {
+    const int j = idx >> 3, tok = idx & 7;
+    float s = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {   // 8 elements 32 j + 8 q ..: MMA m = 2 j + q / 2, half q & 1
+      uint32_t p[4] = {0u, 0u, 0u, 0u};
+      if (tok < T) {
+        float v[8];
+        load_act8<XDT>(x, (size_t)tok * H + 32 * j + 8 * q, v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) p[i] = pack_half2(v[2 * i], v[2 * i + 1]);
+        s += sum4h2(p);
+      }
+      const int m = 2 * j + (q >> 1);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t* e = reinterpret_cast<uint32_t*>(&S.xpanel[m * 32 + tok * 4 + i]);
+        e[q & 1] = p[i];
+      }
     }
-    S.u.hpanel[idx] = v;
+    S.xsums[idx] = s;   // [group j][column tok]
+  }
+}
+
+// h rows of the current expert (rows S.c.colpair, written by other CTAs: read through L2).
+__device__ void stage_h1(DecSmem<1>& S, const __half* h16, int I) {
+  const int row = S.c.colpair[0];
+  for (int i = threadIdx.x; i < I / 8; i += kConsumers) {
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (row >= 0) u = __ldcg(reinterpret_cast<const uint4*>(h16 + (size_t)row * I) + i);
+    *reinterpret_cast<uint4*>(&S.hs[4 * i]) = u;
   }
   ptx::bar_sync(1, kConsumers);
-  panel_sums<MODE>(S.u.hpanel, S.hsums, g.I / 32, 8);
+  for (int j = threadIdx.x; j < I / 32; j += kConsumers) {
+    float s = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = *reinterpret_cast<const uint4*>(&S.hs[16 * j + 4 * q]);
+      const uint32_t p[4] = {u.x, u.y, u.z, u.w};
+      s += sum4h2(p);
+    }
+    S.hsums[j] = s;
+  }
+}
+
+__device__ void stage_h0(DecSmem<0>& S, const __half* h16, int I) {
+  const int ng = I / 32;
+  for (int idx = threadIdx.x; idx < ng * 8; idx += kConsumers) {
+    const int j = idx >> 3, col = idx & 7;
+    const int row = S.c.colpair[col];
+    float s = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t p[4] = {0u, 0u, 0u, 0u};
+      if (row >= 0) {
+        const uint4 u = __ldcg(reinterpret_cast<const uint4*>(h16 + (size_t)row * I + 32 * j + 8 * q));
+        p[0] = u.x; p[1] = u.y; p[2] = u.z; p[3] = u.w;
+        s += sum4h2(p);
+      }
+      const int m = 2 * j + (q >> 1);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t* e = reinterpret_cast<uint32_t*>(&S.hpanel[m * 32 + col * 4 + i]);
+        e[q & 1] = p[i];
+      }
+    }
+    S.hsums[idx] = s;
+  }
 }
 
 // ------------------------------------------------------- consumer: compute
 
 // One item (16 rows x 2048 columns): warp `w` handles k-block w (256 columns = 16 MMAs).
 // m_base = global MMA index of the panel start (p * 128). kb = global k-block index.
-template <int MODE>
-__device__ __forceinline__ void compute_item(const uint2* panel, const float* sums, const uint8_t* slot,
-                                             int m_base, int kb, float (&acc)[4]) {
+// MODE 1: `act` = compact fp16 pairs; lane group g holds the operand of MMAs 2g, 2g+1 only.
+// Four independent accumulator chains keep the MMA pipe busy.
+__device__ __forceinline__ void compute_item1(const uint32_t* act, const float* sums, const uint8_t* slot,
+                                              int m_base, int kb, float (&acc)[4]) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const uint8_t* codes = slot + ((size_t)(4 * w) * 32 + lane) * 16;
+  const uint8_t* scl = slot + kCodeBytes + (w * 8 + g) * 32;
+  const uint32_t* xb = act + 8 * (m_base + 16 * w + 2 * g) + t;
+  const uint32_t b00 = xb[0], b01 = xb[4], b10 = xb[8], b11 = xb[12];
+  float d[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    const uint4 q = *reinterpret_cast<const uint4*>(codes + cc * 32 * 16);
+    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int mi = 4 * cc + i;           // MMA within the k-block; active lane group mi / 2
+      uint32_t a[4];
+      decode_word(words[i], a);
+      const bool on = (mi >> 1) == g;
+      const uint32_t bx = on ? ((mi & 1) ? b10 : b00) : 0u;
+      const uint32_t by = on ? ((mi & 1) ? b11 : b01) : 0u;
+      ptx::mma_16816(d[i], a, bx, by, d[i]);
+    }
+  }
+  float dd[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) dd[r] = (d[0][r] + d[1][r]) + (d[2][r] + d[3][r]);
+  const uint2 sraw = *reinterpret_cast<const uint2*>(scl + t * 8);
+  const float2 sg = half2_to_float2(sraw.x);   // s[g][j0], s[g][j0+1]
+  const float2 su = half2_to_float2(sraw.y);   // s[g+8][j0], s[g+8][j0+1]
+  const float2 X = *reinterpret_cast<const float2*>(sums + 8 * kb + 2 * t);
+  acc[0] = fmaf(sg.x, fmaf(-1032.f, X.x, dd[0]), acc[0]);
+  acc[0] = fmaf(sg.y, fmaf(-1032.f, X.y, dd[1]), acc[0]);
+  acc[1] = fmaf(su.x, fmaf(-1152.f, X.x, dd[2]), acc[1]);
+  acc[1] = fmaf(su.y, fmaf(-1152.f, X.y, dd[3]), acc[1]);
+}
+
+// MODE 0: B fragments from the panel; each group's two MMAs form an independent chain.
+__device__ __forceinline__ void compute_item0(const uint2* panel, const float* sums, const uint8_t* slot,
+                                              int m_base, int kb, float (&acc)[4]) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int gq = lane >> 2, t = lane & 3;
   const uint8_t* codes = slot + ((size_t)(4 * w) * 32 + lane) * 16;
   const uint8_t* scl = slot + kCodeBytes + (w * 8 + gq) * 32;
   const uint2* bp = panel + (size_t)(m_base + 16 * w) * 32 + lane;
-  if (MODE == 1) {
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint4 s0 = *reinterpret_cast<const uint4*>(scl);
+  const uint4 s1 = *reinterpret_cast<const uint4*>(scl + 16);
+  const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      const uint4 q = *reinterpret_cast<const uint4*>(codes + cc * 32 * 16);
-      const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+  for (int cc = 0; cc < 4; ++cc) {
+    const uint4 q = *reinterpret_cast<const uint4*>(codes + cc * 32 * 16);
+    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+    for (int gi = 0; gi < 2; ++gi) {
+      const int jl = 2 * cc + gi;   // group within the k-block
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
         uint32_t a[4];
-        decode_word(words[i], a);
-        const uint2 b = bp[(4 * cc + i) * 32];
+        decode_word(words[2 * gi + i], a);
+        const uint2 b = bp[(4 * cc + 2 * gi + i) * 32];
         ptx::mma_16816(d, a, b.x, b.y, d);
       }
-    }
-    const uint2 sraw = *reinterpret_cast<const uint2*>(scl + t * 8);
-    const float2 sg = half2_to_float2(sraw.x);   // s[g][j0], s[g][j0+1]
-    const float2 su = half2_to_float2(sraw.y);   // s[g+8][j0], s[g+8][j0+1]
-    const float2 X = *reinterpret_cast<const float2*>(sums + 8 * kb + 2 * t);
-    acc[0] = fmaf(sg.x, fmaf(-1032.f, X.x, d[0]), acc[0]);
-    acc[0] = fmaf(sg.y, fmaf(-1032.f, X.y, d[1]), acc[0]);
-    acc[1] = fmaf(su.x, fmaf(-1152.f, X.x, d[2]), acc[1]);
-    acc[1] = fmaf(su.y, fmaf(-1152.f, X.y, d[3]), acc[1]);
-  } else {
-    const uint4 s0 = *reinterpret_cast<const uint4*>(scl);
-    const uint4 s1 = *reinterpret_cast<const uint4*>(scl + 16);
-    const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      const uint4 q = *reinterpret_cast<const uint4*>(codes + cc * 32 * 16);
-      const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int gi = 0; gi < 2; ++gi) {
-        const int jl = 2 * cc + gi;   // group within the k-block
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          uint32_t a[4];
-          decode_word(words[2 * gi + i], a);
-          const uint2 b = bp[(4 * cc + 2 * gi + i) * 32];
-          ptx::mma_16816(d, a, b.x, b.y, d);
-        }
-        // scale words per (k-block, row g): [t'][s[g][2t'], s[g][2t'+1], s[g+8][2t'], s[g+8][2t'+1]]
-        const float2 sgp = half2_to_float2(sw[2 * (jl >> 1)]);
-        const float2 sup = half2_to_float2(sw[2 * (jl >> 1) + 1]);
-        const float sgate = (jl & 1) ? sgp.y : sgp.x;
-        const float sup1 = (jl & 1) ? sup.y : sup.x;
-        const float2 X = *reinterpret_cast<const float2*>(sums + (8 * kb + jl) * 8 + 2 * t);
-        acc[0] = fmaf(sgate, fmaf(-1032.f, X.x, d[0]), acc[0]);
-        acc[1] = fmaf(sgate, fmaf(-1032.f, X.y, d[1]), acc[1]);
-        acc[2] = fmaf(sup1, fmaf(-1152.f, X.x, d[2]), acc[2]);
-        acc[3] = fmaf(sup1, fmaf(-1152.f, X.y, d[3]), acc[3]);
-      }
+      // scale words per (k-block, row g): [t'][s[g][2t'], s[g][2t'+1], s[g+8][2t'], s[g+8][2t'+1]]
+      const float2 sgp = half2_to_float2(sw[2 * (jl >> 1)]);
+      const float2 sup = half2_to_float2(sw[2 * (jl >> 1) + 1]);
+      const float sgate = (jl & 1) ? sgp.y : sgp.x;
+      const float sup1 = (jl & 1) ? sup.y : sup.x;
+      const float2 X = *reinterpret_cast<const float2*>(sums + (8 * kb + jl) * 8 + 2 * t);
+      acc[0] = fmaf(sgate, fmaf(-1032.f, X.x, d[0]), acc[0]);
+      acc[1] = fmaf(sgate, fmaf(-1032.f, X.y, d[1]), acc[1]);
+      acc[2] = fmaf(sup1, fmaf(-1152.f, X.x, d[2]), acc[2]);
+      acc[3] = fmaf(sup1, fmaf(-1152.f, X.y, d[3]), acc[3]);
     }
   }
 }
 
-// Cross-warp reduction of the tile accumulators into S.red (consumers, then named barrier).
+// Cross-warp reduction of the tile accumulators into red (consumers, then named barrier).
 template <int MODE>
-__device__ __forceinline__ void stash_acc(Smem& S, float (&acc)[4]) {
+__device__ __forceinline__ void stash_acc(DecCommon& C, float (&acc)[4]) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   if (MODE == 1) {
 #pragma unroll
@@ -293,28 +383,117 @@ __device__ __forceinline__ void stash_acc(Smem& S, float (&acc)[4]) {
       acc[1] += __shfl_xor_sync(0xffffffffu, acc[1], o);
     }
     if ((lane & 3) == 0) {
-      S.red[w][lane >> 2][0] = acc[0];
-      S.red[w][lane >> 2][1] = acc[1];
+      C.red[w][lane >> 2][0] = acc[0];
+      C.red[w][lane >> 2][1] = acc[1];
     }
   } else {
-    *reinterpret_cast<float4*>(&S.red[w][lane][0]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(&C.red[w][lane][0]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
   }
 }
 
 // Value of MMA row r (0..15) for column n after the reduction (rows 8..15 carry a x16 unit).
 template <int MODE>
-__device__ __forceinline__ float reduced(const Smem& S, int r, int n) {
+__device__ __forceinline__ float reduced(const DecCommon& C, int r, int n) {
   float v = 0.f;
   if (MODE == 1) {
 #pragma unroll
-    for (int w = 0; w < 8; ++w) v += S.red[w][r & 7][r >> 3];
+    for (int w = 0; w < 8; ++w) v += C.red[w][r & 7][r >> 3];
   } else {
     const int ln = (r & 7) * 4 + (n >> 1);
     const int idx = (r >> 3) * 2 + (n & 1);
 #pragma unroll
-    for (int w = 0; w < 8; ++w) v += S.red[w][ln][idx];
+    for (int w = 0; w < 8; ++w) v += C.red[w][ln][idx];
   }
   return (r >= 8) ? v * 0.0625f : v;
+}
+
+// ------------------------------------------------------------------ selection
+
+// Whole warp: noaux_tc selection of one token from its fp32 logits (same rule and tie order
+// as select_token of the stand-alone path): writes ids/weights of the k slots to idsel/wsel.
+// Logits are read through L2 (written by other CTAs of this grid), all loads issued first.
+__device__ __forceinline__ void select_one(const float* logits_row, const float* bias, int E, int n_group,
+                                           int topk_group, int top_k, float rsf, float* b, float* s,
+                                           int* idsel, float* wsel, int* status) {
+  const int lane = threadIdx.x & 31;
+  float lg[kMaxE / 32], bs[kMaxE / 32];
+#pragma unroll
+  for (int i = 0; i < kMaxE / 32; ++i) {
+    const int e = lane + 32 * i;
+    lg[i] = e < E ? __ldcg(logits_row + e) : 0.f;
+    bs[i] = e < E ? __ldg(bias + e) : 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxE / 32; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const float sc = sigmoidf_acc(lg[i]);
+      s[e] = sc;
+      b[e] = sc + bs[i];
+    }
+  }
+  __syncwarp();
+  const int G = E / n_group;
+  float gscore = -INFINITY;
+  if (lane < n_group) {
+    float m1 = -INFINITY, m2 = -INFINITY;
+    for (int i = 0; i < G; ++i) {
+      const float v = b[lane * G + i];
+      if (v > m1) {
+        m2 = m1;
+        m1 = v;
+      } else if (v > m2) {
+        m2 = v;
+      }
+    }
+    gscore = m1 + m2;
+  }
+  unsigned kept = 0;
+  for (int r = 0; r < topk_group; ++r) {
+    float v = gscore;
+    int gi = lane < n_group ? lane : 0x7fffffff;
+    warp_argmax(v, gi);
+    kept |= 1u << gi;
+    if (lane == gi) gscore = -INFINITY;
+  }
+  // candidates: this lane's experts of kept groups
+  float cand[kMaxE / 32];
+#pragma unroll
+  for (int i = 0; i < kMaxE / 32; ++i) {
+    const int e = lane + 32 * i;
+    cand[i] = (e < E && ((kept >> (e / G)) & 1u)) ? b[e] : -INFINITY;
+  }
+  float wsum = 0.f, my_s = 0.f;
+  int my_id = -1;
+  for (int j = 0; j < top_k; ++j) {
+    float v = -INFINITY;
+    int vi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i)
+      if (cand[i] > v) {
+        v = cand[i];
+        vi = lane + 32 * i;
+      }
+    warp_argmax(v, vi);
+    if (vi < 0 || vi >= E) {   // fewer candidates than top_k: host validation forbids it
+      raise_status(status, MOE_ERR_DEVICE_CHECK);
+      vi = 0;
+    }
+    const float sv = s[vi];
+    wsum += sv;
+    if (lane == j) {
+      my_id = vi;
+      my_s = sv;
+    }
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i)
+      if (lane + 32 * i == vi) cand[i] = -INFINITY;
+  }
+  if (lane < top_k) {
+    idsel[lane] = my_id;
+    wsel[lane] = my_s / wsum * rsf;
+  }
+  __syncwarp();
 }
 
 }  // namespace
@@ -333,8 +512,6 @@ struct DecodeArgs {
   float* weights;
   int32_t* offsets;
   int32_t* entries;
-  int32_t* active_g;           // [E]
-  int32_t* meta_g;             // [64][16]: per active expert h row [8] and weight bits [8]
   __half* h16;                 // [T*k + T, I]
   float* out_acc;              // [T, H], zero between calls
   void* out;
@@ -358,10 +535,95 @@ __device__ __forceinline__ unsigned long long global_ns() {
     if (a.trace) a.trace[(size_t)blockIdx.x * 16 + (i)] = global_ns();          \
   } while (0)
 
+// Producer warp (all lanes): wait for every CTA's router rows, select every token, group
+// the entries per expert and publish the routing in shared memory (CTA 0 also to global).
+template <int MODE>
+__device__ void route_in_cta(DecSmem<MODE>& S, const DecodeArgs& a, const Geo& g) {
+  DecCommon& C = S.c;
+  const int lane = threadIdx.x & 31;
+  const int T = g.T, E = g.E, k = g.k;
+  bool ok = true;
+  if (lane == 0) ok = wait_geq(a.sync + 0, (uint32_t)g.G, a.spin_max);
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (!ok) {
+    if (lane == 0) {
+      atomicExch(&C.abort, 1);
+      raise_status(a.status, MOE_ERR_TIMEOUT);
+      C.n_active = 0;
+    }
+    __syncwarp();
+    return;
+  }
+  __threadfence();
+  for (int t = 0; t < T; ++t)
+    select_one(a.logits + (size_t)t * E, a.bias, E, a.n_group, a.topk_group, k, a.rsf, C.selb, C.sels, C.idsel[t],
+               C.wsel[t], a.status);
+  // grouping: counts, exclusive scans (entry offsets, active slots), entry lists
+  const int n = T * k;
+  for (int e = lane; e < E; e += 32) C.cnt[e] = 0;
+  __syncwarp();
+  for (int f = lane; f < n; f += 32) atomicAdd(&C.cnt[C.idsel[f / k][f % k]], 1);
+  __syncwarp();
+  const int epl = E / 32;   // lane owns experts lane*epl .. +epl-1
+  int local = 0, nact = 0;
+  for (int i = 0; i < epl; ++i) {
+    const int cc = C.cnt[lane * epl + i];
+    local += cc;
+    nact += cc > 0;
+  }
+  int incl = local, inca = nact;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    const int va = __shfl_up_sync(0xffffffffu, inca, o);
+    if (lane >= o) {
+      incl += v;
+      inca += va;
+    }
+  }
+  int run = incl - local, apos = inca - nact;
+  for (int i = 0; i < epl; ++i) {
+    const int e = lane * epl + i;
+    C.soff[e] = run;
+    if (g.c == 0) a.offsets[e] = run;
+    if (C.cnt[e] > 0) {
+      C.aslot[e] = apos;
+      C.active[apos++] = e;
+    }
+    run += C.cnt[e];
+  }
+  const int na = __shfl_sync(0xffffffffu, inca, 31);
+  if (lane == 31 && g.c == 0) a.offsets[E] = run;
+  for (int i = lane; i < na * 8; i += 32) {
+    C.meta_pair[i >> 3][i & 7] = -1;
+    C.meta_w[i >> 3][i & 7] = 0.f;
+  }
+  __syncwarp();
+  for (int f = lane; f < n; f += 32) {
+    const int tok = f / k, slot = f % k;
+    const int e = C.idsel[tok][slot];
+    int rank = 0;
+    for (int f2 = 0; f2 < f; ++f2) rank += (C.idsel[f2 / k][f2 % k] == e);
+    const int q = C.soff[e] + rank;
+    const int sl = C.aslot[e];
+    C.meta_pair[sl][tok] = q;
+    C.meta_w[sl][tok] = C.wsel[tok][slot];
+    if (g.c == 0) {
+      a.entries[q] = f;
+      a.ids[f] = e;
+      a.weights[f] = C.wsel[tok][slot];
+    }
+  }
+  if (lane == 0) C.n_active = na;
+  __syncwarp();
+}
+
 template <int MODE, int XDT, int WDT>
 __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  DecSmem<MODE>& S = *reinterpret_cast<DecSmem<MODE>*>(smem_raw);
+  DecCommon& C = S.c;
+  constexpr int kSlots = DecSmem<MODE>::kSlots;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   Geo g;
   g.T = a.T;
@@ -375,8 +637,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
   g.Pd = a.I / kPanelK;
   g.G = gridDim.x;
   g.c = blockIdx.x;
-  // sync words: [0] router rows done, [1] routing published, [2] CTAs exited,
-  // [3] active experts, [4] CTAs done with down tiles; [8..8+E] gate/up tiles done per expert
+  // sync words: [0] CTAs done with router rows, [2] CTAs exited, [4] CTAs done with down
+  // tiles; [8..8+E] gate/up tiles done per expert
   uint32_t* up_done = a.sync + 8;
   const int shared_e = a.E;
   const size_t up_tile_bytes = (size_t)g.Pu * kItemBytes;
@@ -389,10 +651,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     }
     ptx::mbar_init(&S.route_bar, 1);
     ptx::fence_mbar_init();
-    S.abort = 0;
-    S.issued = 0;
-    S.consumed = 0;
-    S.n_active = 0;
+    C.abort = 0;
+    C.issued = 0;
+    C.consumed = 0;
+    C.n_active = 0;
   }
   __syncthreads();
 
@@ -401,23 +663,23 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
   seg_range(g.NTd, g.G, g.c, c10, c11);  // shared down tiles
 
   if (warp == 8) {
-    // ------------------------------------------------------------- producer
+    // ------------------------------------------------------------- producer warp
+    const uint64_t pol = ptx::policy_evict_first();
+    int it = 0;
+    bool ok = true;
+    // Brings item `it` into slot it % kSlots once the consumers released its previous use.
+    auto issue = [&](const uint8_t* src) {
+      if (!ok) return;
+      const int slot = it % kSlots;
+      if (it >= kSlots && !ptx::mbar_wait(&S.empty[slot], ((it / kSlots) - 1) & 1, kMbarSpin)) ok = false;
+      if (ok && *(volatile int*)&C.abort) ok = false;
+      if (!ok) return;
+      ptx::mbar_arrive_expect_tx(&S.full[slot], kItemBytes);
+      ptx::bulk_g2s(S.slots[slot], src, kItemBytes, &S.full[slot], pol);
+      ++it;
+      *(volatile int*)&C.issued = it;
+    };
     if (lane == 0) {
-      const uint64_t pol = ptx::policy_evict_first();
-      int it = 0;
-      bool ok = true;
-      // Brings item `it` into slot it % kSlots once the consumers released its previous use.
-      auto issue = [&](const uint8_t* src) {
-        if (!ok) return;
-        const int slot = it % kSlots;
-        if (it >= kSlots && !ptx::mbar_wait(&S.empty[slot], ((it / kSlots) - 1) & 1, kMbarSpin)) ok = false;
-        if (ok && *(volatile int*)&S.abort) ok = false;
-        if (!ok) return;
-        ptx::mbar_arrive_expect_tx(&S.full[slot], kItemBytes);
-        ptx::bulk_g2s(S.slots[slot], src, kItemBytes, &S.full[slot], pol);
-        ++it;
-        *(volatile int*)&S.issued = it;
-      };
       for (int tl = a0; tl < a1; ++tl)
         for (int p = 0; p < g.Pu; ++p)
           issue(a.up_store + ((size_t)shared_e * g.NTu + tl) * up_tile_bytes + (size_t)p * kItemBytes);
@@ -425,158 +687,113 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
         for (int p = 0; p < g.Pd; ++p)
           issue(a.down_store + ((size_t)shared_e * g.NTd + tl) * dn_tile_bytes + (size_t)p * kItemBytes);
       DEC_TRACE(13);
-      // routing result of this call: active experts and their per-token metadata
-      if (wait_geq(a.sync + 1, 1, a.spin_max)) {
-        DEC_TRACE(14);
-        const int na = (int)__ldcg(a.sync + 3);
-        S.n_active = na;
-        for (int i = 0; i < na; ++i) {
-          S.active[i] = __ldcg(a.active_g + i);
-          for (int n = 0; n < 8; ++n) {
-            S.meta_pair[i][n] = __ldcg(a.meta_g + i * 16 + n);
-            S.meta_w[i][n] = __int_as_float(__ldcg(a.meta_g + i * 16 + 8 + n));
-          }
-        }
-      } else {
-        ok = false;
-        atomicExch(&S.abort, 1);
-        raise_status(a.status, MOE_ERR_TIMEOUT);
-      }
+    }
+    __syncwarp();
+    route_in_cta<MODE>(S, a, g);
+    if (lane == 0) {
+      DEC_TRACE(14);
       ptx::mbar_arrive(&S.route_bar);
-      const int na = S.n_active;
+      const int na = C.n_active;
       int b0, b1, c20, c21;
       seg_range(na * g.NTu, g.G, g.c, b0, b1);
       seg_range(na * g.NTd, g.G, g.c, c20, c21);
       for (int r = b0; r < b1; ++r) {
-        const int e = S.active[r / g.NTu], tl = r % g.NTu;
+        const int e = C.active[r / g.NTu], tl = r % g.NTu;
         for (int p = 0; p < g.Pu; ++p)
           issue(a.up_store + ((size_t)e * g.NTu + tl) * up_tile_bytes + (size_t)p * kItemBytes);
       }
       for (int u = c20; u < c21; ++u) {
-        const int e = S.active[u / g.NTd], tl = u % g.NTd;
+        const int e = C.active[u / g.NTd], tl = u % g.NTd;
         for (int p = 0; p < g.Pd; ++p)
           issue(a.down_store + ((size_t)e * g.NTd + tl) * dn_tile_bytes + (size_t)p * kItemBytes);
       }
       if (!ok) {
-        atomicExch(&S.abort, 1);
+        atomicExch(&C.abort, 1);
         raise_status(a.status, MOE_ERR_TIMEOUT);
       }
     }
   } else {
     // ------------------------------------------------------------- consumers
-    const int T = g.T, H = g.H, E = g.E, k = g.k;
+    const int T = g.T, H = g.H, E = g.E;
     if (tid == 0) DEC_TRACE(0);
-    build_x_panel<MODE, XDT>(S, a.x, g);
+    if constexpr (MODE == 1) {
+      stage_x1<XDT>(S, a.x, H);
+    } else {
+      stage_x0<XDT>(S, a.x, T, H);
+    }
+    ptx::bar_sync(1, kConsumers);
     if (tid == 0) DEC_TRACE(1);
 
-    // router rows e = c, c + G, ... (same reduction order as the stand-alone router kernel)
+    // router rows e = c, c + G, ...: each thread takes 4 consecutive columns per 1024 (all
+    // loads of a row issued together); fp32 FMA, then warp and CTA reductions
     for (int e = g.c; e < E; e += g.G) {
       float racc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) racc[i] = 0.f;
-      for (int hh = tid; hh < H; hh += kConsumers) {
-        const float wv = load_act<WDT>(a.router_w, (size_t)e * H + hh);
+      float4 wv[kMaxH / 1024];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (i < T) racc[i] = fmaf(wv, load_act<XDT>(a.x, (size_t)i * H + hh), racc[i]);
+      for (int q = 0; q < kMaxH / 1024; ++q) {
+        const int col = 1024 * q + 4 * tid;
+        wv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (col < H) {
+          if constexpr (WDT == MOE_DT_F32) {
+            wv[q] = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(a.router_w) + (size_t)e * H + col));
+          } else {
+            const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(a.router_w) +
+                                                                 (size_t)e * H + col));
+            wv[q] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                                __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kMaxH / 1024; ++q) {
+        const int col = 1024 * q + 4 * tid;
+        if (col < H) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (i < T) {
+              float xv[4];
+              if constexpr (XDT == MOE_DT_F32) {
+                const float4 f =
+                    __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + (size_t)i * H + col));
+                xv[0] = f.x; xv[1] = f.y; xv[2] = f.z; xv[3] = f.w;
+              } else {
+                const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(a.x) +
+                                                                     (size_t)i * H + col));
+                xv[0] = __uint_as_float(u.x << 16);
+                xv[1] = __uint_as_float(u.x & 0xFFFF0000u);
+                xv[2] = __uint_as_float(u.y << 16);
+                xv[3] = __uint_as_float(u.y & 0xFFFF0000u);
+              }
+              racc[i] = fmaf(wv[q].x, xv[0], racc[i]);
+              racc[i] = fmaf(wv[q].y, xv[1], racc[i]);
+              racc[i] = fmaf(wv[q].z, xv[2], racc[i]);
+              racc[i] = fmaf(wv[q].w, xv[3], racc[i]);
+            }
+          }
+        }
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         float v = racc[i];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) S.red[warp][i][0] = v;
+        if (lane == 0) C.red[warp][i][0] = v;
       }
       ptx::bar_sync(1, kConsumers);
       if (tid < T) {
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) v += S.red[w][tid][0];
+        for (int w = 0; w < 8; ++w) v += C.red[w][tid][0];
         a.logits[(size_t)tid * E + e] = v;
       }
       ptx::bar_sync(1, kConsumers);
     }
     if (tid == 0) {
       __threadfence();
-      const uint32_t ticket = atomicAdd(a.sync + 0, 1u);
-      S.flag = (ticket == (uint32_t)g.G - 1) ? 1 : 0;
-    }
-    ptx::bar_sync(1, kConsumers);
-    if (tid == 0) DEC_TRACE(2);
-    if (S.flag) {
-      // ---- this CTA finished the router last: selection and grouping for all tokens
-      __threadfence();
-      if (warp < T) {
-        const int id = select_token(a.logits + (size_t)warp * E, a.bias, E, a.n_group, a.topk_group, k,
-                                    a.rsf, S.u.sel.b[warp], S.u.sel.s[warp], a.ids + (size_t)warp * k,
-                                    a.weights + (size_t)warp * k, a.status);
-        if (lane < k) S.sid[warp * k + lane] = id;
-      }
-      ptx::bar_sync(1, kConsumers);
-      if (warp == 0) {
-        const int n = T * k;
-        for (int e = lane; e < E; e += 32) S.cnt[e] = 0;
-        __syncwarp();
-        for (int f = lane; f < n; f += 32) atomicAdd(&S.cnt[S.sid[f]], 1);
-        __syncwarp();
-        // exclusive scans over experts (entry offsets, active-expert slots); lane owns
-        // E/32 consecutive experts
-        const int epl = E / 32;
-        int local = 0, nact = 0;
-        for (int i = 0; i < epl; ++i) {
-          const int cc = S.cnt[lane * epl + i];
-          local += cc;
-          nact += cc > 0;
-        }
-        int incl = local, inca = nact;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, incl, o);
-          const int va = __shfl_up_sync(0xffffffffu, inca, o);
-          if (lane >= o) {
-            incl += v;
-            inca += va;
-          }
-        }
-        int run = incl - local, apos = inca - nact;
-        for (int i = 0; i < epl; ++i) {
-          const int e = lane * epl + i;
-          S.soff[e] = run;
-          a.offsets[e] = run;
-          if (S.cnt[e] > 0) {
-            S.aslot[e] = apos;
-            a.active_g[apos++] = e;
-          }
-          run += S.cnt[e];
-        }
-        if (lane == 31) {
-          a.offsets[E] = run;
-          a.sync[3] = (uint32_t)inca;
-        }
-        const int na = __shfl_sync(0xffffffffu, inca, 31);
-        // per active expert: h row and combine weight of each token (-1 / 0 if not routed)
-        for (int i = lane; i < na * 8; i += 32) {
-          a.meta_g[(i >> 3) * 16 + (i & 7)] = -1;
-          a.meta_g[(i >> 3) * 16 + 8 + (i & 7)] = 0;
-        }
-        __syncwarp();
-        for (int f = lane; f < n; f += 32) {
-          const int e = S.sid[f];
-          int rank = 0;
-          for (int f2 = 0; f2 < f; ++f2) rank += (S.sid[f2] == e);
-          const int q = S.soff[e] + rank;
-          a.entries[q] = f;
-          const int sl = S.aslot[e], tok = f / k;
-          a.meta_g[sl * 16 + tok] = q;
-          a.meta_g[sl * 16 + 8 + tok] = __float_as_int(__ldcg(a.weights + f));
-        }
-      }
-      ptx::bar_sync(1, kConsumers);
-      if (tid == 0) {
-        __threadfence();
-        ptx::st_release(a.sync + 1, 1u);
-        DEC_TRACE(3);
-      }
+      ptx::red_release_add(a.sync + 0, 1u);
+      DEC_TRACE(2);
     }
 
     float acc[4];
@@ -587,19 +804,25 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     auto wait_item = [&](const uint8_t*& slot) -> bool {
       const int s = it % kSlots;
       slot = S.slots[s];
-      if (*(volatile int*)&S.abort) return false;
+      if (*(volatile int*)&C.abort) return false;
       if (!ptx::mbar_wait(&S.full[s], (it / kSlots) & 1, kMbarSpin)) {
-        atomicExch(&S.abort, 1);
+        atomicExch(&C.abort, 1);
         raise_status(a.status, MOE_ERR_TIMEOUT);
         return false;
       }
       return true;
     };
-    auto run_items = [&](int np, const uint2* panel, const float* sums) {
+    auto run_items = [&](int np, bool up) {
       for (int p = 0; p < np; ++p) {
         const uint8_t* slot;
         const bool have = wait_item(slot);
-        if (have) compute_item<MODE>(panel, sums, slot, p * 128, p * 8 + warp, acc);
+        if (have) {
+          if constexpr (MODE == 1) {
+            compute_item1(up ? S.xs : S.hs, up ? S.xsums : S.hsums, slot, p * 128, p * 8 + warp, acc);
+          } else {
+            compute_item0(up ? S.xpanel : S.hpanel, up ? S.xsums : S.hsums, slot, p * 128, p * 8 + warp, acc);
+          }
+        }
         __syncwarp();
         if (have) {
           if (lane == 0) ptx::mbar_arrive(&S.empty[it % kSlots]);
@@ -616,7 +839,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       up_n = 0;
     };
 
-    // gate/up tile `tl` of expert `e`; h rows of the routed tokens in S.colpair
+    // gate/up tile `tl` of expert `e`; h rows of the routed tokens in C.colpair
     auto up_tile = [&](int e, int tl) {
       if (e != up_e) {
         flush_up();
@@ -624,15 +847,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[i] = 0.f;
-      run_items(g.Pu, S.xpanel, S.xsums);
-      stash_acc<MODE>(S, acc);
+      run_items(g.Pu, true);
+      stash_acc<MODE>(C, acc);
       ptx::bar_sync(1, kConsumers);
       const int nt = (MODE == 1) ? 8 : 64;
       if (tid < nt) {
         const int r = (MODE == 1) ? tid : (tid >> 3), n = (MODE == 1) ? 0 : (tid & 7);
-        const int pr = S.colpair[n];
+        const int pr = C.colpair[n];
         if (pr >= 0) {
-          const float gate = reduced<MODE>(S, r, n), up = reduced<MODE>(S, r + 8, n);
+          const float gate = reduced<MODE>(C, r, n), up = reduced<MODE>(C, r + 8, n);
           a.h16[(size_t)pr * g.I + tl * 8 + r] = __float2half_rn(siluf_acc(gate) * up);
         }
       }
@@ -644,14 +867,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     auto down_tile = [&](int tl) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[i] = 0.f;
-      run_items(g.Pd, S.u.hpanel, S.hsums);
-      stash_acc<MODE>(S, acc);
+      run_items(g.Pd, false);
+      stash_acc<MODE>(C, acc);
       ptx::bar_sync(1, kConsumers);
       const int nt = (MODE == 1) ? 16 : 128;
       if (tid < nt) {
         const int r = (MODE == 1) ? tid : (tid >> 3), n = (MODE == 1) ? 0 : (tid & 7);
-        const float wn = S.colw[n];
-        if (n < T && wn != 0.f) atomicAdd(a.out_acc + (size_t)n * H + tl * 16 + r, wn * reduced<MODE>(S, r, n));
+        const float wn = C.colw[n];
+        if (n < T && wn != 0.f) atomicAdd(a.out_acc + (size_t)n * H + tl * 16 + r, wn * reduced<MODE>(C, r, n));
       }
       ptx::bar_sync(1, kConsumers);
     };
@@ -659,9 +882,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     // one thread waits until every gate/up tile of expert e is done; uniform continuation
     auto wait_up = [&](int e) {
       if (tid == 0) {
-        const bool ok = !*(volatile int*)&S.abort && wait_geq(up_done + e, (uint32_t)g.NTu, a.spin_max);
+        const bool ok = !*(volatile int*)&C.abort && wait_geq(up_done + e, (uint32_t)g.NTu, a.spin_max);
         if (!ok) {
-          atomicExch(&S.abort, 1);
+          atomicExch(&C.abort, 1);
           raise_status(a.status, MOE_ERR_TIMEOUT);
         }
       }
@@ -673,12 +896,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       ptx::bar_sync(1, kConsumers);
       if (tid < 8) {
         if (sl < 0) {
-          S.colpair[tid] = tid < T ? T * k + tid : -1;
-          S.colw[tid] = tid < T ? 1.f : 0.f;
+          C.colpair[tid] = tid < T ? T * g.k + tid : -1;
+          C.colw[tid] = tid < T ? 1.f : 0.f;
         } else {
-          S.colpair[tid] = S.meta_pair[sl][tid];
-          S.colw[tid] = S.meta_w[sl][tid];
+          C.colpair[tid] = C.meta_pair[sl][tid];
+          C.colw[tid] = C.meta_w[sl][tid];
         }
+      }
+      ptx::bar_sync(1, kConsumers);
+    };
+
+    auto stage_h = [&]() {
+      if constexpr (MODE == 1) {
+        stage_h1(S, a.h16, g.I);
+      } else {
+        stage_h0(S, a.h16, g.I);
       }
       ptx::bar_sync(1, kConsumers);
     };
@@ -692,18 +924,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     if (c11 > c10) {
       wait_up(shared_e);
       if (tid == 0) DEC_TRACE(5);
-      build_h_panel<MODE>(S, a.h16, g);   // colpair still describes the shared expert
-      ptx::bar_sync(1, kConsumers);
+      stage_h();   // colpair still describes the shared expert
       for (int tl = c10; tl < c11; ++tl) down_tile(tl);
     }
     if (tid == 0) DEC_TRACE(6);
-    // ---- routing known (the producer broadcasts it)
+    // ---- routing known (the producer warp computed it)
     if (!ptx::mbar_wait(&S.route_bar, 0, kMbarSpin * 16) && tid == 0) {
-      atomicExch(&S.abort, 1);
+      atomicExch(&C.abort, 1);
       raise_status(a.status, MOE_ERR_TIMEOUT);
     }
     ptx::bar_sync(1, kConsumers);
-    const int na = S.n_active;
+    const int na = C.n_active;
     int b0, b1, c20, c21;
     seg_range(na * g.NTu, g.G, g.c, b0, b1);
     seg_range(na * g.NTd, g.G, g.c, c20, c21);
@@ -716,7 +947,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
         set_meta(sl);
         cur = sl;
       }
-      up_tile(S.active[sl], tl);
+      up_tile(C.active[sl], tl);
     }
     flush_up();
     if (tid == 0) DEC_TRACE(8);
@@ -726,10 +957,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       const int sl = u / g.NTd, tl = u % g.NTd;
       if (sl != cur) {
         set_meta(sl);
-        wait_up(S.active[sl]);
+        wait_up(C.active[sl]);
         if (tid == 0 && cur < 0) DEC_TRACE(9);
-        build_h_panel<MODE>(S, a.h16, g);
-        ptx::bar_sync(1, kConsumers);
+        stage_h();
         cur = sl;
       }
       down_tile(tl);
@@ -752,7 +982,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       }
     }
     if (tid == 0) {
-      S.consumed = it_ok;
+      C.consumed = it_ok;
       DEC_TRACE(12);
     }
   }
@@ -760,16 +990,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
   if (tid == 0) {
     // drain copies this CTA issued but did not see complete (only after an abort): the last
     // issued item of each slot is the only one that can still be in flight
-    const int issued = S.issued;
-    for (int i = max(S.consumed, issued - kSlots); i < issued; ++i)
+    const int issued = C.issued;
+    for (int i = max(C.consumed, issued - kSlots); i < issued; ++i)
       ptx::mbar_wait(&S.full[i % kSlots], (i / kSlots) & 1, kMbarSpin);
     __threadfence();
     const uint32_t old = atomicAdd(a.sync + 2, 1u);
     if (old == (uint32_t)g.G - 1) {
       // last CTA out: reset the counters for the next call
       a.sync[0] = 0;
-      a.sync[1] = 0;
-      a.sync[3] = 0;
       a.sync[4] = 0;
       for (int i = 0; i <= g.E; ++i) up_done[i] = 0;
       __threadfence();
@@ -839,7 +1067,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kDecThreads);
-  cfg.dynamicSmemBytes = sizeof(Smem);
+  cfg.dynamicSmemBytes = sizeof(DecSmem<MODE>);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -852,7 +1080,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t s) {
 template <int MODE, int XDT, int WDT>
 cudaError_t init_one() {
   return cudaFuncSetAttribute(moe_decode_kernel<MODE, XDT, WDT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)sizeof(Smem));
+                              (int)sizeof(DecSmem<MODE>));
 }
 
 }  // namespace
@@ -861,14 +1089,22 @@ size_t decode_tile_bytes(int R, int K) { return (size_t)(R / 16) * (K / kPanelK)
 
 bool decode_supported(int H, int I, int E, int top_k, int T) {
   return H % kPanelK == 0 && I % kPanelK == 0 && H <= kMaxH && I <= kMaxI && E <= kMaxE && E % 32 == 0 &&
-         T >= 1 && T <= 8 && T * top_k <= kMaxActive && top_k <= 16;
+         T >= 1 && T <= 8 && T * top_k <= kMaxActive && top_k <= kMaxK;
 }
 
-size_t decode_smem_bytes() { return sizeof(Smem); }
+size_t decode_smem_bytes() {
+  return sizeof(DecSmem<0>) > sizeof(DecSmem<1>) ? sizeof(DecSmem<0>) : sizeof(DecSmem<1>);
+}
 
 cudaError_t decode_occupancy(int* blocks_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, moe_decode_kernel<1, MOE_DT_BF16, MOE_DT_F32>,
-                                                       kDecThreads, sizeof(Smem));
+  int b0 = 0, b1 = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, moe_decode_kernel<0, MOE_DT_BF16, MOE_DT_F32>,
+                                                                kDecThreads, sizeof(DecSmem<0>));
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, moe_decode_kernel<1, MOE_DT_BF16, MOE_DT_F32>, kDecThreads,
+                                                      sizeof(DecSmem<1>));
+  *blocks_per_sm = b0 < b1 ? b0 : b1;
+  return e;
 }
 
 cudaError_t launch_repack(const uint8_t* codes, const void* scales, int R, int K, bool up, uint8_t* dst,
@@ -909,8 +1145,6 @@ cudaError_t launch_decode_fused(const DecodeLaunch& d, int act_dtype, int router
   a.weights = d.weights;
   a.offsets = d.offsets;
   a.entries = d.entries;
-  a.active_g = d.active_g;
-  a.meta_g = d.meta_g;
   a.h16 = static_cast<__half*>(d.h16);
   a.out_acc = d.out_acc;
   a.out = d.out;

@@ -81,8 +81,6 @@ struct DecodeLaunch {
   float* weights;
   int32_t* offsets;
   int32_t* entries;
-  int32_t* active_g;
-  int32_t* meta_g;
   void* h16;
   float* out_acc;
   void* out;
@@ -100,8 +98,7 @@ struct alignas(64) TensorMapBytes {
   unsigned char b[128];
 };
 struct GemmMaps {
-  TensorMapBytes codes;    // packed weight codes [rows, K/2] bytes, 128 x 16 box, 128-byte swizzle
-  TensorMapBytes scales;   // weight scales [rows, K/16] bytes, 16 x 16 box
+  TensorMapBytes codes;    // fp16 weights [rows, K], 64 x 16 box, 128-byte swizzle (kWF16 only)
   TensorMapBytes act;      // expert-sorted fp16 activations [rows, K], 64 x 16 box, 128-byte swizzle
 };
 // Weight storage of the grouped GEMM besides MOE_W_INT4_G32 / MOE_W_NVFP4: plain fp16
@@ -113,6 +110,8 @@ struct GemmParams {
   const int32_t* n_items;     // device count of this launch's items
   const int32_t* item_skip;   // device count of items to skip first, or NULL
   int e_sub;                  // subtracted from the item's expert index to index the weights
+  const uint8_t* wpack;       // packed weights (int4 / NVFP4), see gemm_pack_kernel
+  int mtiles;                 // 128-row tiles per expert
   int K;                      // reduction length (H for gate/up, I for down)
   int rows_per_expert;        // 2I (gate/up) or H (down)
   int H, I, T, top_k;
@@ -137,8 +136,12 @@ cudaError_t launch_bf16_to_f16(const void* src, void* dst, size_t n, cudaStream_
 cudaError_t launch_gather_act(const void* x, int act_dtype, bool nvfp4, int H, const int32_t* entries, int Tk,
                               int top_k, int rows, __half* dst, const unsigned int* amax_bits, cudaStream_t s);
 cudaError_t launch_quant_h(const float* h, size_t n, const unsigned int* amax_bits, __half* dst, cudaStream_t s);
-cudaError_t launch_gemm(int wfmt, int epi, const GemmMaps& m, const GemmParams& p, int mtiles, int max_items,
+// Persistent launch over n_items x mtiles tiles (max_tiles bounds them; grid <= n_sm).
+cudaError_t launch_gemm(int wfmt, int epi, const GemmMaps& m, const GemmParams& p, int max_tiles, int n_sm,
                         cudaStream_t s);
+size_t gemm_pack_bytes(int rows_per_expert, int K, int n_exp);
+cudaError_t launch_gemm_pack(const uint8_t* codes, const void* scales, int K, int n_exp, int rows_per_expert,
+                             int I, bool gate_up, uint8_t* dst, cudaStream_t s);
 
 // out[T, H] (act dtype) = out_acc
 cudaError_t launch_finalize(const float* out_acc, void* out, int act_dtype, size_t n,

@@ -41,8 +41,6 @@ struct moe_layer {
   uint8_t* up_store = nullptr;
   uint8_t* down_store = nullptr;
   uint32_t* dsync = nullptr;
-  int32_t* active_g = nullptr;
-  int32_t* meta_g = nullptr;
   void* h16 = nullptr;
   float* dec_acc = nullptr;
   // grouped tcgen05 GEMM path
@@ -54,6 +52,8 @@ struct moe_layer {
   int4* gitems = nullptr;
   int32_t* g_nitems = nullptr;
   GemmMaps maps_up{}, maps_down{};
+  uint8_t* gpack_up = nullptr;  // packed gate/up and down weights of the grouped GEMM
+  uint8_t* gpack_down = nullptr;
   void* sh16_gu = nullptr;      // separately stored shared expert as fp16 [2I, H], [H, I]
   void* sh16_d = nullptr;
   GemmMaps maps_sh_up{}, maps_sh_down{};
@@ -248,8 +248,6 @@ moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt,
     if ((st = dev_alloc_t(L, &L->up_store, (size_t)(E + 1) * ub)) ||
         (st = dev_alloc_t(L, &L->down_store, (size_t)(E + 1) * db)) ||
         (st = dev_alloc_t(L, &L->dsync, nsync * 4)) ||
-        (st = dev_alloc_t(L, &L->active_g, (size_t)E * 4)) ||
-        (st = dev_alloc_t(L, &L->meta_g, (size_t)64 * 16 * 4)) ||
         (st = dev_alloc(L, &L->h16, (size_t)Td * (k + 1) * I * 2)) ||
         (st = dev_alloc_t(L, &L->dec_acc, (size_t)Td * H * 4)))
       return st;
@@ -276,13 +274,16 @@ moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt,
         (st = dev_alloc_t(L, &L->g_nitems, 4 * sizeof(int32_t))))
       return st;
     if (fmt == MOE_W_NVFP4 && (st = dev_alloc_t(L, &L->h32, (size_t)Tm * k * I * 4))) return st;
-    const uint64_t gu_rows = (uint64_t)n_store * 2 * I, d_rows = (uint64_t)n_store * H;
-    L->gemm_ok = make_tmap_2d(&L->maps_up.codes, L->w.gu_codes, 1, H / 2, gu_rows, 128, 16, true) &&
-                 make_tmap_2d(&L->maps_up.scales, L->w.gu_scales, 1, row_scale_bytes(fmt, H), gu_rows, 16, 16, false) &&
-                 make_tmap_2d(&L->maps_up.act, L->x16s, 2, H, L->gemm_rows, 64, 16, true) &&
-                 make_tmap_2d(&L->maps_down.codes, L->w.d_codes, 1, I / 2, d_rows, 128, 16, true) &&
-                 make_tmap_2d(&L->maps_down.scales, L->w.d_scales, 1, row_scale_bytes(fmt, I), d_rows, 16, 16, false) &&
+    if ((st = dev_alloc_t(L, &L->gpack_up, gemm_pack_bytes(2 * I, H, n_store))) ||
+        (st = dev_alloc_t(L, &L->gpack_down, gemm_pack_bytes(H, I, n_store))))
+      return st;
+    if (launch_gemm_pack(L->w.gu_codes, L->w.gu_scales, H, n_store, 2 * I, I, true, L->gpack_up, s) ||
+        launch_gemm_pack(L->w.d_codes, L->w.d_scales, I, n_store, H, I, false, L->gpack_down, s))
+      return MOE_ERR_CUDA;
+    L->gemm_ok = make_tmap_2d(&L->maps_up.act, L->x16s, 2, H, L->gemm_rows, 64, 16, true) &&
                  make_tmap_2d(&L->maps_down.act, L->h16s, 2, I, L->gemm_rows, 64, 16, true);
+    L->maps_up.codes = L->maps_up.act;       // unused by the packed-weight kernels
+    L->maps_down.codes = L->maps_down.act;
     if (L->gemm_ok && !L->shared_inline) {
       if ((st = dev_alloc(L, &L->sh16_gu, (size_t)2 * I * H * 2)) || (st = dev_alloc(L, &L->sh16_d, (size_t)H * I * 2)))
         return st;
@@ -368,19 +369,23 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
 
   p.K = ps.K = H;
   p.rows_per_expert = ps.rows_per_expert = 2 * I;
+  p.mtiles = ps.mtiles = 2 * I / 128;
+  p.wpack = L->gpack_up;
   p.w_tscale = L->w.gu_tscale;
   p.act_amax = L->amax;
-  MOE_LAUNCH(launch_gemm(c.weight_format, 0, L->maps_up, p, 2 * I / 128, routed_max, s));
-  if (!inl) MOE_LAUNCH(launch_gemm(kWF16, 0, L->maps_sh_up, ps, 2 * I / 128, shared_max, s));
+  MOE_LAUNCH(launch_gemm(c.weight_format, 0, L->maps_up, p, routed_max * p.mtiles, L->n_sm, s));
+  if (!inl) MOE_LAUNCH(launch_gemm(kWF16, 0, L->maps_sh_up, ps, shared_max * ps.mtiles, L->n_sm, s));
   MOE_CK(m.mark(3));
   if (nvfp4) MOE_LAUNCH(launch_quant_h(L->h32, (size_t)Tk * I, L->amax + 1, L->h16s, s));
   MOE_CK(m.mark(4));
   p.K = ps.K = I;
   p.rows_per_expert = ps.rows_per_expert = H;
+  p.mtiles = ps.mtiles = H / 128;
+  p.wpack = L->gpack_down;
   p.w_tscale = L->w.d_tscale;
   p.act_amax = L->amax + 1;
-  MOE_LAUNCH(launch_gemm(c.weight_format, 1, L->maps_down, p, H / 128, routed_max, s));
-  if (!inl) MOE_LAUNCH(launch_gemm(kWF16, 1, L->maps_sh_down, ps, H / 128, shared_max, s));
+  MOE_LAUNCH(launch_gemm(c.weight_format, 1, L->maps_down, p, routed_max * p.mtiles, L->n_sm, s));
+  if (!inl) MOE_LAUNCH(launch_gemm(kWF16, 1, L->maps_sh_down, ps, shared_max * ps.mtiles, L->n_sm, s));
   MOE_CK(m.mark(5));
   MOE_LAUNCH(launch_finalize(L->out_acc, out, c.act_dtype, (size_t)T * H, s));
   MOE_CK(m.mark(6));
@@ -406,7 +411,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
     MOE_CK(m.mark(2));
     DecodeLaunch d{x, T, L->router_w, L->bias, H, I, E, k, c.n_group, c.topk_group,
                    c.routed_scaling_factor, L->up_store, L->down_store, L->logits, L->ids,
-                   L->weights, L->offsets, L->entries, L->active_g, L->meta_g, L->h16, L->dec_acc,
+                   L->weights, L->offsets, L->entries, L->h16, L->dec_acc,
                    out, L->dsync, L->status, 1u << 22, L->trace};
     MOE_LAUNCH(launch_decode_fused(d, c.act_dtype, c.router_dtype, L->n_sm, s));
     for (int i = 3; i < kStageEvents; ++i) MOE_CK(m.mark(i));

@@ -48,6 +48,87 @@ router_logits_kernel(const void* __restrict__ x, const void* __restrict__ wr,
   }
 }
 
+// Tiled router GEMM for larger batches: a CTA computes a 64-token x 64-expert block of
+// logits, staging 32-column slices of x and W_r in shared memory (fp32), so each router
+// row is read once per 64 tokens; 256 threads, 4 x 4 outputs each (rows ty + 16 i,
+// columns tx + 16 j), fp32 FMA in ascending column order.
+constexpr int kRgM = 64, kRgN = 64, kRgK = 32;
+
+template <int DT>
+__device__ __forceinline__ void load8(const void* base, size_t i, float (&v)[8]) {
+  if constexpr (DT == MOE_DT_F32) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + i));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + i) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(base) + i));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v[2 * q] = __uint_as_float(w[q] << 16);
+      v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+    }
+  }
+}
+
+template <int XDT, int WDT>
+__global__ void __launch_bounds__(256)
+router_gemm_kernel(const void* __restrict__ x, const void* __restrict__ wr, float* __restrict__ logits,
+                   int T, int E, int H) {
+  __shared__ float xs[kRgK][kRgM + 4];
+  __shared__ float ws[kRgK][kRgN + 4];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int t0 = blockIdx.y * kRgM, e0 = blockIdx.x * kRgN;
+  // loader: row lr (token or expert) of the tile, 8 consecutive columns at lk
+  const int lr = tid >> 2, lk = (tid & 3) * 8;
+  const bool xok = t0 + lr < T, wok = e0 + lr < E;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  float xv[8], wv[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) xv[q] = wv[q] = 0.f;
+  if (xok) load8<XDT>(x, (size_t)(t0 + lr) * H + lk, xv);
+  if (wok) load8<WDT>(wr, (size_t)(e0 + lr) * H + lk, wv);
+  for (int k0 = 0; k0 < H; k0 += kRgK) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      xs[lk + q][lr] = xv[q];
+      ws[lk + q][lr] = wv[q];
+    }
+    __syncthreads();
+    if (k0 + kRgK < H) {   // prefetch the next slice while this one is multiplied
+      if (xok) load8<XDT>(x, (size_t)(t0 + lr) * H + k0 + kRgK + lk, xv);
+      if (wok) load8<WDT>(wr, (size_t)(e0 + lr) * H + k0 + kRgK + lk, wv);
+    }
+#pragma unroll
+    for (int k = 0; k < kRgK; ++k) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = xs[k][ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = ws[k][tx + 16 * j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty + 16 * i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx + 16 * j;
+      if (e < E) logits[(size_t)t * E + e] = acc[i][j];
+    }
+  }
+}
+
 constexpr int kSelWarps = 4;
 constexpr int kMaxE = 1024;
 
@@ -72,6 +153,18 @@ select_kernel(const float* __restrict__ logits, const float* __restrict__ bias, 
 cudaError_t launch_router_logits(const void* x, int act_dtype, const void* router_w,
                                  int router_dtype, float* logits, int T, int E, int H,
                                  cudaStream_t s) {
+  if (T >= 128 && H % kRgK == 0) {
+    dim3 g((E + kRgN - 1) / kRgN, (T + kRgM - 1) / kRgM);
+    if (act_dtype == MOE_DT_F32 && router_dtype == MOE_DT_F32)
+      router_gemm_kernel<MOE_DT_F32, MOE_DT_F32><<<g, 256, 0, s>>>(x, router_w, logits, T, E, H);
+    else if (act_dtype == MOE_DT_BF16 && router_dtype == MOE_DT_F32)
+      router_gemm_kernel<MOE_DT_BF16, MOE_DT_F32><<<g, 256, 0, s>>>(x, router_w, logits, T, E, H);
+    else if (act_dtype == MOE_DT_F32 && router_dtype == MOE_DT_BF16)
+      router_gemm_kernel<MOE_DT_F32, MOE_DT_BF16><<<g, 256, 0, s>>>(x, router_w, logits, T, E, H);
+    else
+      router_gemm_kernel<MOE_DT_BF16, MOE_DT_BF16><<<g, 256, 0, s>>>(x, router_w, logits, T, E, H);
+    return cudaGetLastError();
+  }
   dim3 grid(E, (T + kRouterTokens - 1) / kRouterTokens);
   if (act_dtype == MOE_DT_F32 && router_dtype == MOE_DT_F32)
     router_logits_kernel<MOE_DT_F32, MOE_DT_F32><<<grid, kRouterThreads, 0, s>>>(x, router_w, logits, T, E, H);
