@@ -3,30 +3,33 @@
 // komputer lambat", section "Fitur utama yang diimplementasikan": each selected expert's
 // weights are read once per call and applied to every token routed to it).
 //
-// One CTA computes a 128 x N tile D = W[128 rows, K] . X[N tokens, K]^T of one expert:
-// weight rows on the MMA's M side, the expert's tokens (rows of an expert-sorted
-// activation matrix, N <= 256) on the N side, so a lightly loaded expert still fills the
-// tensor core's M dimension. The quantised weights stay quantised in HBM and are
-// dequantised on use (the packed int4 "dequant-on-use" of the same section; NVFP4 blocks
-// per "NVIDIA stellt neues GLM-5.2 NVFP4 Modell vor", section "Technische Details und
-// Quantisierungsansatz"):
-//   warp 6   TMA: 128 rows x 256 columns of packed codes (+ their scales) per weight stage
-//   warps 0-3 dequantise 64 columns per K stage into an fp16 tile in the 128-byte swizzle
-//            layout the MMA reads (int4 * fp16 scale rounded once to fp16; E2M1 * E4M3 is
-//            exact in fp16, the fp32 tensor scales are applied in the epilogue)
-//   warp 4   TMA: the N x 64 fp16 activation tile of the same K stage
-//   warp 5   issues tcgen05.mma kind::f16 (M=128, N, K=16) x 4 per stage into a TMEM
-//            accumulator and releases stages with tcgen05.commit
-//   warps 0-3 then read the accumulator (tcgen05.ld) and run the epilogue:
+// A tile is D = W[128 rows, K] . X[N tokens, K]^T of one expert: weight rows on the MMA's M
+// side, the expert's tokens (<= 256 rows of an expert-sorted activation matrix) on the N
+// side, so a lightly loaded expert still fills the tensor core's M dimension. The quantised
+// weights stay quantised in HBM and are dequantised on use (the packed int4
+// "dequant-on-use" of the same section; NVFP4 blocks per "NVIDIA stellt neues GLM-5.2 NVFP4
+// Modell vor", section "Technische Details und Quantisierungsansatz").
+//
+// Persistent CTAs (one per SM) walk the tiles (item, 128-row block) in a static round-robin
+// order; warp roles:
+//   warp 14    bulk copy of the packed weights: 128 rows x 256 columns of codes and their
+//              scales per copy (18 KB, laid out at layer creation for conflict-free reads)
+//   warps 4-11 dequantise 64 columns per K stage into an fp16 tile in the 128-byte swizzle
+//              layout the MMA reads (int4 * fp16 scale rounded once to fp16; E2M1 * E4M3 is
+//              exact in fp16, the fp32 tensor scales are applied in the epilogue)
+//   warp 12    TMA: the N x 64 fp16 activation tile of the same K stage
+//   warp 13    issues tcgen05.mma kind::f16 (M=128, N, K=16) x 4 per stage into one of two
+//              TMEM accumulators (256 columns each) and releases stages with tcgen05.commit
+//   warps 0-3  epilogue of the previous tile while the next one runs: tcgen05.ld, then
 //     gate/up: M rows pair 16 gate with 16 up rows per warp; h = SiLU(gate) * up is
 //              written to the expert-sorted h matrix (fp16, or fp32 for NVFP4 layers
 //              whose h is quantised next);
 //     down:    out_acc[token] += w[token, slot] * y (fp32 atomics; the weighted combine).
 // A separately stored bf16 shared expert (the NVFP4 layers keep it unquantised) is
-// converted to fp16 once at layer creation (exact for its range) and runs through the
-// same kernel with TMA-loaded weight tiles and no dequantisation (kWF16).
-// Every wait is bounded; a time-out sets MOE_ERR_TIMEOUT, the CTA stops issuing work,
-// lets copies in flight land, frees its TMEM and exits.
+// converted to fp16 once at layer creation (exact for its range) and runs through the same
+// kernel with its weight tiles loaded by TMA straight into the MMA's layout (kWF16).
+// Every wait is bounded; a time-out sets MOE_ERR_TIMEOUT, the CTA stops issuing work, lets
+// copies and MMAs in flight land, frees its TMEM and exits.
 #include <cuda.h>
 
 #include "kernels.h"
@@ -36,31 +39,38 @@ namespace moe {
 
 namespace {
 
-constexpr int kGThreads = 224;
+constexpr int kEpiWarps = 4;      // warps 0-3
+constexpr int kDqWarp0 = 4;       // warps 4-11
+constexpr int kDqWarps = 8;
+constexpr int kWarpB = 12;
+constexpr int kWarpMma = 13;
+constexpr int kWarpW = 14;
+constexpr int kGThreads = 15 * 32;
 constexpr int kBM = 128;          // weight rows per tile (MMA M)
 constexpr int kBN = 256;          // max tokens per tile (MMA N)
 constexpr int kBK = 64;           // K per stage: one 128-byte swizzle atom of fp16
-constexpr int kSub = 4;           // K stages per weight stage (256 columns)
+constexpr int kSub = 4;           // K stages per packed weight group (256 columns)
 constexpr int kABStages = 3;
 constexpr int kWStages = 3;
 constexpr int kAStage = kBM * kBK * 2;     // 16 KB fp16 weight tile
 constexpr int kBStage = kBN * kBK * 2;     // 32 KB fp16 activation tile
-constexpr int kWCodes = kBM * 128;         // 16 KB: 128 rows x 256 4-bit codes
-constexpr int kWScales = kBM * 16;         // 2 KB: 128 rows x 16 scale bytes
+constexpr int kGroupCodes = kBM * 128;     // 16 KB: 128 rows x 256 4-bit codes
+constexpr int kGroupBytes = kGroupCodes + kBM * 16;   // + 2 KB of scales
 constexpr int kBoxRows = 16;
-constexpr uint32_t kTmemCols = 256;
+constexpr int kAccCols = 256;
+constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr uint32_t kSpin = 1u << 22;
 
 struct GSmem {
   uint8_t a[kABStages][kAStage];
   uint8_t b[kABStages][kBStage];
-  uint8_t wc[kWStages][kWCodes];
-  uint8_t ws[kWStages][kWScales];
+  uint8_t w[kWStages][kGroupBytes];
   uint64_t full_ab[kABStages];
   uint64_t empty_ab[kABStages];
   uint64_t full_w[kWStages];
   uint64_t empty_w[kWStages];
-  uint64_t tmem_full;
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -90,28 +100,18 @@ __device__ __forceinline__ bool aborted(const GSmem& S) { return *(volatile cons
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
-// 8 packed nibbles (element 2j in the low nibble of byte j) -> 4 words holding the nibble
-// pairs (e0,e1) (e2,e3) (e4,e5) (e6,e7) at bits 0-3 and 16-19.
-__device__ __forceinline__ void nibble_pairs(uint32_t w, uint32_t (&p)[4]) {
-  const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
-  const uint32_t r0 = __byte_perm(lo, hi, 0x5410);   // e0 e2 e1 e3
-  const uint32_t r1 = __byte_perm(lo, hi, 0x7632);   // e4 e6 e5 e7
-  p[0] = r0 & 0x000F000Fu;
-  p[1] = (r0 >> 8) & 0x000F000Fu;
-  p[2] = r1 & 0x000F000Fu;
-  p[3] = (r1 >> 8) & 0x000F000Fu;
-}
-
-// int4 (two's complement) x 8 -> fp16 x 8 times the group scale: (nibble ^ 8) in the
-// mantissa of 1024 is 1032 + code exactly; subtracting 1032 is exact; the product with the
-// fp16 scale is rounded once.
+// Packed code word (see gemm_pack_kernel): element 2i at bits 4i..4i+3, element 2i+1 at bits
+// 16+4i..; pair i (elements 2i, 2i+1) is (w >> 4i) & 0x000F000F.
+// int4 (two's complement): (nibble ^ 8) in the mantissa of 1024 is 1032 + code exactly;
+// subtracting 1032 is exact; the product with the fp16 scale is rounded once.
 __device__ __forceinline__ uint4 dq_int4x8(uint32_t w, __half2 s2) {
-  uint32_t p[4];
-  nibble_pairs(w, p);
   const __half2 k1032 = __float2half2_rn(1032.f);
   uint32_t o[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) o[i] = h2u(__hmul2(__hsub2(u2h(p[i] ^ 0x64086408u), k1032), s2));
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t p = ((w >> (4 * i)) & 0x000F000Fu) ^ 0x64086408u;
+    o[i] = h2u(__hmul2(__hsub2(u2h(p), k1032), s2));
+  }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
@@ -119,13 +119,12 @@ __device__ __forceinline__ uint4 dq_int4x8(uint32_t w, __half2 s2) {
 // at fp16 bits 9-11 (sign at 15) give the E2M1 value times 2^-14 (its subnormal included);
 // both products are exact in fp16.
 __device__ __forceinline__ uint4 dq_e2m1x8(uint32_t w, __half2 s2) {
-  uint32_t p[4];
-  nibble_pairs(w, p);
   const __half2 k2p14 = __float2half2_rn(16384.f);
   uint32_t o[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t bits = ((p[i] & 0x00070007u) << 9) | ((p[i] & 0x00080008u) << 12);
+    const uint32_t p = (w >> (4 * i)) & 0x000F000Fu;
+    const uint32_t bits = ((p & 0x00070007u) << 9) | ((p & 0x00080008u) << 12);
     o[i] = h2u(__hmul2(__hmul2(u2h(bits), k2p14), s2));
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
@@ -138,207 +137,227 @@ __device__ __forceinline__ __half e4m3_to_half(uint32_t b) {
   return __hmul(v, __float2half(256.f));
 }
 
-template <int WFMT, int EPI>
+// Weight row of 16-row box j of tile mt (fp16 weights loaded by TMA): gate/up tiles pair
+// box 2w (gate rows 64 mt + 16 w ..) with box 2w+1 (the matching up rows).
+template <int EPI>
 __device__ __forceinline__ int weight_row(const GemmParams& p, int e, int mt, int j) {
   e -= p.e_sub;
-  if (EPI == 0) {   // box 2w: gate rows, box 2w+1: up rows 64 mt + 16 w ..
-    return e * p.rows_per_expert + ((j & 1) ? p.I : 0) + 64 * mt + 16 * (j >> 1);
-  }
+  if (EPI == 0) return e * p.rows_per_expert + ((j & 1) ? p.I : 0) + 64 * mt + 16 * (j >> 1);
   return e * p.rows_per_expert + kBM * mt + kBoxRows * j;
 }
 
 template <int WFMT, int EPI>
 __global__ void __launch_bounds__(kGThreads, 1)
-moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
-                const __grid_constant__ CUtensorMap tm_b, const GemmParams p) {
+moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
+                const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   GSmem& S = *reinterpret_cast<GSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  if ((int)blockIdx.y >= __ldg(p.n_items)) return;
-  const int4 item = __ldg(p.items + blockIdx.y + (p.item_skip ? __ldg(p.item_skip) : 0));
-  const int e = item.x, row0 = item.y, n = item.z;
-  const int mt = blockIdx.x;
+  const int MT = p.mtiles;
+  const int n_items = __ldg(p.n_items);
+  const int skip = p.item_skip ? __ldg(p.item_skip) : 0;
+  const int ntiles = n_items * MT;
+  if ((int)blockIdx.x >= ntiles) return;   // no tile for this CTA (uniform)
   const int NK = p.K / kBK;
-  const int nbox = (n + kBoxRows - 1) / kBoxRows;
-  const int N = nbox * kBoxRows;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Tk = p.T * p.top_k;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kABStages; ++s) {
-      // B producer (+ tx) and the 4 dequant warps, or the two TMA producers (fp16 weights)
-      ptx::mbar_init(&S.full_ab[s], WFMT == kWF16 ? 2 : 5);
+      // B producer (+ tx) and the dequant warps, or the two TMA producers (fp16 weights)
+      ptx::mbar_init(&S.full_ab[s], WFMT == kWF16 ? 2 : 1 + kDqWarps);
       ptx::mbar_init(&S.empty_ab[s], 1);   // tcgen05.commit
     }
     for (int s = 0; s < kWStages; ++s) {
       ptx::mbar_init(&S.full_w[s], 1);
-      ptx::mbar_init(&S.empty_w[s], 4);
+      ptx::mbar_init(&S.empty_w[s], kDqWarps);
     }
-    ptx::mbar_init(&S.tmem_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&S.tmem_full[b], 1);
+      ptx::mbar_init(&S.tmem_empty[b], kEpiWarps);
+    }
     ptx::mbar_init(&S.mma_done, 1);
     ptx::fence_mbar_init();
     S.abort = 0;
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     ptx::tmem_alloc(&S.tmem_base, kTmemCols);
     ptx::tmem_relinquish();
-  }
-  if (EPI == 1) {
-    for (int c = threadIdx.x; c < n; c += kGThreads) {
-      const int q = row0 + c;
-      if (q < Tk) {
-        const int ent = __ldg(p.entries + q);
-        S.col_tok[c] = ent / p.top_k;
-        S.col_w[c] = __ldg(p.weights + ent);
-      } else {
-        S.col_tok[c] = q - Tk;
-        S.col_w[c] = 1.f;
-      }
-    }
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = S.tmem_base;
 
-  if (warp == 6 && WFMT == kWF16) {
-    // --------------------------------------------- fp16 weight tiles straight to A
+  if (warp == kWarpW) {
+    // ------------------------------------------------------------ weight producer
     if (lane == 0) {
-      ptx::prefetch_tmap(&tm_codes);
-      for (int ks = 0; ks < NK; ++ks) {
-        const int s = ks % kABStages;
-        if (ks >= kABStages && !wait_bar(&S.empty_ab[s], ((ks / kABStages) - 1) & 1)) {
-          set_abort(S, p.status);
-          break;
-        }
-        if (aborted(S)) break;
-        ptx::mbar_arrive_expect_tx(&S.full_ab[s], kAStage);
+      if (WFMT == kWF16) ptx::prefetch_tmap(&tm_w);
+      int kg = 0, wg = 0;
+      for (int t = blockIdx.x; t < ntiles && !aborted(S); t += gridDim.x) {
+        const int4 it = __ldg(p.items + skip + t / MT);
+        const int e = it.x, mt = t % MT;
+        if (WFMT == kWF16) {
+          // fp16 weight tiles straight into the MMA's A stages
+          for (int ks = 0; ks < NK; ++ks, ++kg) {
+            const int s = kg % kABStages;
+            if (kg >= kABStages && !wait_bar(&S.empty_ab[s], ((kg / kABStages) - 1) & 1)) {
+              set_abort(S, p.status);
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(&S.full_ab[s], kAStage);
 #pragma unroll 1
-        for (int j = 0; j < kBM / kBoxRows; ++j)
-          ptx::tma_load_2d(S.a[s] + j * kBoxRows * 128, &tm_codes, ks * kBK, weight_row<WFMT, EPI>(p, e, mt, j),
-                           &S.full_ab[s]);
+            for (int j = 0; j < kBM / kBoxRows; ++j)
+              ptx::tma_load_2d(S.a[s] + j * kBoxRows * 128, &tm_w, ks * kBK, weight_row<EPI>(p, e, mt, j),
+                               &S.full_ab[s]);
+          }
+        } else {
+          const uint8_t* src =
+              p.wpack + ((size_t)(e - p.e_sub) * MT + mt) * (size_t)(NK / kSub) * kGroupBytes;
+          for (int g = 0; g < NK / kSub; ++g, ++wg) {
+            const int s = wg % kWStages;
+            if (wg >= kWStages && !wait_bar(&S.empty_w[s], ((wg / kWStages) - 1) & 1)) {
+              set_abort(S, p.status);
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(&S.full_w[s], kGroupBytes);
+            ptx::bulk_g2s(S.w[s], src + (size_t)g * kGroupBytes, kGroupBytes, &S.full_w[s],
+                          ptx::policy_evict_first());
+          }
+        }
       }
     }
-  } else if (warp == 6) {
-    // ------------------------------------------------ weight codes + scales producer
-    if (lane == 0) {
-      ptx::prefetch_tmap(&tm_codes);
-      ptx::prefetch_tmap(&tm_scales);
-      const int NW = NK / kSub;
-      for (int w = 0; w < NW; ++w) {
-        const int s = w % kWStages;
-        if (w >= kWStages && !wait_bar(&S.empty_w[s], ((w / kWStages) - 1) & 1)) {
-          set_abort(S, p.status);
-          break;
-        }
-        if (aborted(S)) break;
-        ptx::mbar_arrive_expect_tx(&S.full_w[s], kWCodes + kWScales);
-#pragma unroll 1
-        for (int j = 0; j < kBM / kBoxRows; ++j) {
-          const int row = weight_row<WFMT, EPI>(p, e, mt, j);
-          ptx::tma_load_2d(S.wc[s] + j * kBoxRows * 128, &tm_codes, w * 128, row, &S.full_w[s]);
-          ptx::tma_load_2d(S.ws[s] + j * kBoxRows * 16, &tm_scales, w * 16, row, &S.full_w[s]);
-        }
-      }
-    }
-  } else if (warp == 4) {
+  } else if (warp == kWarpB) {
     // ------------------------------------------------------- activation producer
     if (lane == 0) {
       ptx::prefetch_tmap(&tm_b);
-      for (int ks = 0; ks < NK; ++ks) {
-        const int s = ks % kABStages;
-        if (ks >= kABStages && !wait_bar(&S.empty_ab[s], ((ks / kABStages) - 1) & 1)) {
-          set_abort(S, p.status);
-          break;
-        }
-        if (aborted(S)) break;
-        ptx::mbar_arrive_expect_tx(&S.full_ab[s], (uint32_t)nbox * kBoxRows * 128);
+      int kg = 0;
+      for (int t = blockIdx.x; t < ntiles && !aborted(S); t += gridDim.x) {
+        const int4 it = __ldg(p.items + skip + t / MT);
+        const int row0 = it.y, nbox = (it.z + kBoxRows - 1) / kBoxRows;
+        for (int ks = 0; ks < NK; ++ks, ++kg) {
+          const int s = kg % kABStages;
+          if (kg >= kABStages && !wait_bar(&S.empty_ab[s], ((kg / kABStages) - 1) & 1)) {
+            set_abort(S, p.status);
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&S.full_ab[s], (uint32_t)nbox * kBoxRows * 128);
 #pragma unroll 1
-        for (int j = 0; j < nbox; ++j)
-          ptx::tma_load_2d(S.b[s] + j * kBoxRows * 128, &tm_b, ks * kBK, row0 + kBoxRows * j, &S.full_ab[s]);
+          for (int j = 0; j < nbox; ++j)
+            ptx::tma_load_2d(S.b[s] + j * kBoxRows * 128, &tm_b, ks * kBK, row0 + kBoxRows * j, &S.full_ab[s]);
+        }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = ptx::f16_idesc(kBM, N, false);
-      for (int ks = 0; ks < NK; ++ks) {
-        const int s = ks % kABStages;
-        if (!wait_bar(&S.full_ab[s], (ks / kABStages) & 1)) {
+      int kg = 0, tc = 0;
+      for (int t = blockIdx.x; t < ntiles && !aborted(S); t += gridDim.x, ++tc) {
+        const int4 it = __ldg(p.items + skip + t / MT);
+        const int N = ((it.z + kBoxRows - 1) / kBoxRows) * kBoxRows;
+        const uint32_t idesc = ptx::f16_idesc(kBM, N, false);
+        const int buf = tc & 1;
+        if (tc >= 2 && !wait_bar(&S.tmem_empty[buf], ((tc >> 1) - 1) & 1)) {
           set_abort(S, p.status);
           break;
         }
-        if (aborted(S)) break;
         ptx::tc_fence_after();
-        const uint32_t a0 = ptx::smem_u32(S.a[s]), b0 = ptx::smem_u32(S.b[s]);
+        const uint32_t d = tmem + (uint32_t)(buf * kAccCols);
+        for (int ks = 0; ks < NK; ++ks, ++kg) {
+          const int s = kg % kABStages;
+          if (!wait_bar(&S.full_ab[s], (kg / kABStages) & 1)) {
+            set_abort(S, p.status);
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a0 = ptx::smem_u32(S.a[s]), b0 = ptx::smem_u32(S.b[s]);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          ptx::tc_mma_f16(tmem, ptx::sw128_desc(a0 + 32 * kk), ptx::sw128_desc(b0 + 32 * kk), idesc,
-                          (ks | kk) != 0 ? 1u : 0u);
-        ptx::tc_commit(&S.empty_ab[s]);
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            ptx::tc_mma_f16(d, ptx::sw128_desc(a0 + 32 * kk), ptx::sw128_desc(b0 + 32 * kk), idesc,
+                            (ks | kk) != 0 ? 1u : 0u);
+          ptx::tc_commit(&S.empty_ab[s]);
+        }
+        ptx::tc_commit(&S.tmem_full[buf]);
       }
-      ptx::tc_commit(&S.tmem_full);
+    }
+  } else if (warp >= kDqWarp0) {
+    // ------------------------------------------------ dequantisers (warps 4-11)
+    if (WFMT != kWF16) {
+      const int dq = threadIdx.x - kDqWarp0 * 32;
+      const int r = dq & (kBM - 1), h = dq >> 7;   // A row, column half (32 of the stage's 64)
+      uint8_t* const arow_base = &S.a[0][0] + (r >> 3) * 1024 + (r & 7) * 128;
+      int kg = 0, wg = 0;
+      bool stop = false;
+      for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
+        for (int ks = 0; ks < NK; ++ks, ++kg) {
+          const int kq = ks % kSub, ws = wg % kWStages;
+          if (kq == 0 && !wait_bar(&S.full_w[ws], (wg / kWStages) & 1)) set_abort(S, p.status);
+          const int s = kg % kABStages;
+          if (kg >= kABStages && !wait_bar(&S.empty_ab[s], ((kg / kABStages) - 1) & 1)) set_abort(S, p.status);
+          if (__any_sync(0xffffffffu, aborted(S))) {   // warp-uniform exit
+            stop = true;
+            break;
+          }
+          const int slot = (kq * 2 + h) * kBM + r;
+          const uint4 q = *reinterpret_cast<const uint4*>(S.w[ws] + slot * 16);
+          const uint32_t sc = *reinterpret_cast<const unsigned short*>(S.w[ws] + kGroupCodes + slot * 2);
+          uint4 o[4];
+          if (WFMT == MOE_W_INT4_G32) {
+            const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)sc));
+            o[0] = dq_int4x8(q.x, s2);
+            o[1] = dq_int4x8(q.y, s2);
+            o[2] = dq_int4x8(q.z, s2);
+            o[3] = dq_int4x8(q.w, s2);
+          } else {
+            const __half2 s0 = __half2half2(e4m3_to_half(sc & 0xFFu));
+            const __half2 s1 = __half2half2(e4m3_to_half(sc >> 8));
+            o[0] = dq_e2m1x8(q.x, s0);
+            o[1] = dq_e2m1x8(q.y, s0);
+            o[2] = dq_e2m1x8(q.z, s1);
+            o[3] = dq_e2m1x8(q.w, s1);
+          }
+          uint8_t* arow = arow_base + s * kAStage;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(arow + (((4 * h + j) ^ (r & 7)) << 4)) = o[j];
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::mbar_arrive(&S.full_ab[s]);
+            if (kq == kSub - 1) ptx::mbar_arrive(&S.empty_w[ws]);
+          }
+          if (kq == kSub - 1) ++wg;
+        }
+      }
     }
   } else {
-    // ------------------------------------------- dequantisers (warps 0-3), then epilogue
-    const int m = threadIdx.x;   // A row 0..127
-    uint4 sc = make_uint4(0u, 0u, 0u, 0u);
-    for (int ks = 0; ks < (WFMT == kWF16 ? 0 : NK); ++ks) {
-      const int w = ks / kSub, ws = w % kWStages, kq = ks % kSub;
-      if (kq == 0) {
-        if (!wait_bar(&S.full_w[ws], (w / kWStages) & 1)) set_abort(S, p.status);
-        sc = *reinterpret_cast<const uint4*>(S.ws[ws] + m * 16);
+    // ------------------------------------------------------ epilogue (warps 0-3)
+    int tc = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tc) {
+      const int4 it = __ldg(p.items + skip + t / MT);
+      const int e = it.x, row0 = it.y, n = it.z, mt = t % MT;
+      const int N = ((n + kBoxRows - 1) / kBoxRows) * kBoxRows;
+      const int buf = tc & 1;
+      if (EPI == 1) {
+        ptx::bar_sync(2, kEpiWarps * 32);   // the previous tile's readers are done
+        for (int c = threadIdx.x; c < n; c += kEpiWarps * 32) {
+          const int q = row0 + c;
+          if (q < Tk) {
+            const int ent = __ldg(p.entries + q);
+            S.col_tok[c] = ent / p.top_k;
+            S.col_w[c] = __ldg(p.weights + ent);
+          } else {
+            S.col_tok[c] = q - Tk;
+            S.col_w[c] = 1.f;
+          }
+        }
+        ptx::bar_sync(2, kEpiWarps * 32);
       }
-      const int s = ks % kABStages;
-      if (ks >= kABStages && !wait_bar(&S.empty_ab[s], ((ks / kABStages) - 1) & 1)) set_abort(S, p.status);
-      if (__any_sync(0xffffffffu, aborted(S))) break;   // warp-uniform exit
-      const uint8_t* crow = S.wc[ws] + m * 128;
-      const uint4 q0 = *reinterpret_cast<const uint4*>(crow + (((2 * kq) ^ (m & 7)) << 4));
-      const uint4 q1 = *reinterpret_cast<const uint4*>(crow + (((2 * kq + 1) ^ (m & 7)) << 4));
-      const uint32_t sw = kq == 0 ? sc.x : kq == 1 ? sc.y : kq == 2 ? sc.z : sc.w;
-      uint4 o[8];
-      if (WFMT == MOE_W_INT4_G32) {
-        const __half2 s01 = u2h(sw);   // scales of groups 2kq (low) and 2kq + 1 (high)
-        const __half2 sa = __low2half2(s01), sb = __high2half2(s01);
-        o[0] = dq_int4x8(q0.x, sa);
-        o[1] = dq_int4x8(q0.y, sa);
-        o[2] = dq_int4x8(q0.z, sa);
-        o[3] = dq_int4x8(q0.w, sa);
-        o[4] = dq_int4x8(q1.x, sb);
-        o[5] = dq_int4x8(q1.y, sb);
-        o[6] = dq_int4x8(q1.z, sb);
-        o[7] = dq_int4x8(q1.w, sb);
-      } else {
-        const __half2 s0 = __half2half2(e4m3_to_half(sw & 0xFFu));
-        const __half2 s1 = __half2half2(e4m3_to_half((sw >> 8) & 0xFFu));
-        const __half2 s2 = __half2half2(e4m3_to_half((sw >> 16) & 0xFFu));
-        const __half2 s3 = __half2half2(e4m3_to_half(sw >> 24));
-        o[0] = dq_e2m1x8(q0.x, s0);
-        o[1] = dq_e2m1x8(q0.y, s0);
-        o[2] = dq_e2m1x8(q0.z, s1);
-        o[3] = dq_e2m1x8(q0.w, s1);
-        o[4] = dq_e2m1x8(q1.x, s2);
-        o[5] = dq_e2m1x8(q1.y, s2);
-        o[6] = dq_e2m1x8(q1.z, s3);
-        o[7] = dq_e2m1x8(q1.w, s3);
-      }
-      uint8_t* arow = S.a[s] + (m >> 3) * 1024 + (m & 7) * 128;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(arow + ((j ^ (m & 7)) << 4)) = o[j];
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        ptx::mbar_arrive(&S.full_ab[s]);
-        if (kq == kSub - 1) ptx::mbar_arrive(&S.empty_w[ws]);
-      }
-    }
-
-    // ------------------------------------------------------------------ epilogue
-    if (!wait_bar(&S.tmem_full, 0)) set_abort(S, p.status);
-    ptx::tc_fence_after();
-    if (!__any_sync(0xffffffffu, aborted(S))) {
+      if (!wait_bar(&S.tmem_full[buf], (tc >> 1) & 1)) set_abort(S, p.status);
+      if (__any_sync(0xffffffffu, aborted(S))) break;
+      ptx::tc_fence_after();
       float sc_out = 1.f;
-      if (WFMT == MOE_W_NVFP4) sc_out = __ldg(p.w_tscale + e) * __fdiv_rn(__uint_as_float(__ldg(p.act_amax)), 2688.0f);
-      const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+      if (WFMT == MOE_W_NVFP4)
+        sc_out = __ldg(p.w_tscale + e) * __fdiv_rn(__uint_as_float(__ldg(p.act_amax)), 2688.0f);
+      const uint32_t lane_addr = tmem + (uint32_t)(buf * kAccCols) + ((uint32_t)(32 * warp) << 16);
       for (int c0 = 0; c0 < N; c0 += 32) {
         float v[32];
         ptx::tmem_ld32(lane_addr + (uint32_t)c0, v);
@@ -378,6 +397,9 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_const
           }
         }
       }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&S.tmem_empty[buf]);
     }
   }
 
@@ -388,7 +410,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_const
     // copies and MMAs issued before the abort complete on their own; give them time to land
     for (int i = 0; i < 2000; ++i) __nanosleep(1000);
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     if (aborted(S) && lane == 0) {
       ptx::tc_commit(&S.mma_done);
       wait_bar(&S.mma_done, 0);
@@ -396,6 +418,58 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_const
     __syncwarp();
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Packed weights of the grouped GEMM, written once at layer creation from the row-major
+// store (codes [rows][K/2], scales [rows][K/16 bytes]). Per (expert, 128-row tile, 256-column
+// group), 18432 bytes: codes [k-stage 4][half 2][row 128][16 B] then scales
+// [k-stage 4][half 2][row 128][2 B], so the dequantising thread of (row, half) reads 16
+// consecutive bytes and its neighbours the next ones. The 16 bytes hold the 32 codes of
+// columns 64 kq + 32 h .. of the row; word j holds columns 8j..8j+7 with column 8j + 2i in
+// bits 4i..4i+3 and 8j + 2i + 1 in bits 16 + 4i... Scale bytes: int4 the fp16 scale of the
+// 32 columns; NVFP4 the two E4M3 scales of its 16-column blocks. Gate/up tiles take gate rows
+// 64 mt + 16 w + l and the matching up rows at tile rows 32 w + l and 32 w + 16 + l.
+__global__ void gemm_pack_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, int K,
+                                 int n_exp, int rows_per_expert, int I, int gate_up, int mtiles,
+                                 uint8_t* __restrict__ dst) {
+  const int ngroups = K / 256;
+  const size_t total = (size_t)n_exp * mtiles * ngroups * (kSub * 2 * kBM);   // (row, half, kq) entries
+  const size_t sbytes = (size_t)K / 16;                                        // scale bytes per row
+  for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+    const int slot = (int)(idx % (kSub * 2 * kBM));           // (kq * 2 + h) * 128 + r
+    const size_t grp = idx / (kSub * 2 * kBM);                // (e * mtiles + mt) * ngroups + g
+    const int g = (int)(grp % ngroups);
+    const int mt = (int)((grp / ngroups) % mtiles);
+    const int e = (int)(grp / ((size_t)ngroups * mtiles));
+    const int r = slot % kBM, h = (slot / kBM) & 1, kq = slot / (2 * kBM);
+    int row;
+    if (gate_up) {
+      const int w = r >> 5, l = r & 31;
+      row = (l < 16) ? 64 * mt + 16 * w + l : I + 64 * mt + 16 * w + (l - 16);
+    } else {
+      row = kBM * mt + r;
+    }
+    const size_t grow = (size_t)e * rows_per_expert + row;
+    const int col0 = 256 * g + 64 * kq + 32 * h;
+    const uint8_t* src = codes + grow * (K / 2) + col0 / 2;
+    uint32_t words[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t b = src[4 * j + i];   // columns 8j + 2i (low nibble), 8j + 2i + 1 (high)
+        w |= (b & 15u) << (4 * i);
+        w |= (b >> 4) << (16 + 4 * i);
+      }
+      words[j] = w;
+    }
+    uint8_t* out = dst + grp * kGroupBytes;
+    *reinterpret_cast<uint4*>(out + (size_t)slot * 16) = make_uint4(words[0], words[1], words[2], words[3]);
+    const uint8_t* ssrc = scales + grow * sbytes + col0 / 16;   // int4: fp16 of group col0/32
+    out[kGroupCodes + (size_t)slot * 2] = ssrc[0];
+    out[kGroupCodes + (size_t)slot * 2 + 1] = ssrc[1];
   }
 }
 
@@ -509,10 +583,9 @@ EncodeTiledFn encode_fn() {
 }
 
 template <int WFMT, int EPI>
-cudaError_t launch_gemm_t(const GemmMaps& m, const GemmParams& p, int mtiles, int max_items, cudaStream_t s) {
-  moe_gemm_kernel<WFMT, EPI><<<dim3(mtiles, max_items), kGThreads, kGSmemBytes, s>>>(
-      *reinterpret_cast<const CUtensorMap*>(&m.codes), *reinterpret_cast<const CUtensorMap*>(&m.scales),
-      *reinterpret_cast<const CUtensorMap*>(&m.act), p);
+cudaError_t launch_gemm_t(const GemmMaps& m, const GemmParams& p, int grid, cudaStream_t s) {
+  moe_gemm_kernel<WFMT, EPI><<<grid, kGThreads, kGSmemBytes, s>>>(
+      *reinterpret_cast<const CUtensorMap*>(&m.codes), *reinterpret_cast<const CUtensorMap*>(&m.act), p);
   return cudaGetLastError();
 }
 
@@ -593,19 +666,28 @@ cudaError_t launch_quant_h(const float* h, size_t n, const unsigned int* amax_bi
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(int wfmt, int epi, const GemmMaps& m, const GemmParams& p, int mtiles, int max_items,
+cudaError_t launch_gemm(int wfmt, int epi, const GemmMaps& m, const GemmParams& p, int max_tiles, int n_sm,
                         cudaStream_t s) {
-  if (max_items <= 0) return cudaSuccess;
+  if (max_tiles <= 0) return cudaSuccess;
+  const int grid = max_tiles < n_sm ? max_tiles : n_sm;
   if (wfmt == MOE_W_INT4_G32)
-    return epi == 0 ? launch_gemm_t<MOE_W_INT4_G32, 0>(m, p, mtiles, max_items, s)
-                    : launch_gemm_t<MOE_W_INT4_G32, 1>(m, p, mtiles, max_items, s);
+    return epi == 0 ? launch_gemm_t<MOE_W_INT4_G32, 0>(m, p, grid, s) : launch_gemm_t<MOE_W_INT4_G32, 1>(m, p, grid, s);
   if (wfmt == MOE_W_NVFP4)
-    return epi == 0 ? launch_gemm_t<MOE_W_NVFP4, 0>(m, p, mtiles, max_items, s)
-                    : launch_gemm_t<MOE_W_NVFP4, 1>(m, p, mtiles, max_items, s);
+    return epi == 0 ? launch_gemm_t<MOE_W_NVFP4, 0>(m, p, grid, s) : launch_gemm_t<MOE_W_NVFP4, 1>(m, p, grid, s);
   if (wfmt == kWF16)
-    return epi == 0 ? launch_gemm_t<kWF16, 0>(m, p, mtiles, max_items, s)
-                    : launch_gemm_t<kWF16, 1>(m, p, mtiles, max_items, s);
+    return epi == 0 ? launch_gemm_t<kWF16, 0>(m, p, grid, s) : launch_gemm_t<kWF16, 1>(m, p, grid, s);
   return cudaErrorInvalidValue;
+}
+
+size_t gemm_pack_bytes(int rows_per_expert, int K, int n_exp) {
+  return (size_t)n_exp * (rows_per_expert / kBM) * (K / 256) * kGroupBytes;
+}
+
+cudaError_t launch_gemm_pack(const uint8_t* codes, const void* scales, int K, int n_exp, int rows_per_expert,
+                             int I, bool gate_up, uint8_t* dst, cudaStream_t s) {
+  gemm_pack_kernel<<<148 * 8, 256, 0, s>>>(codes, static_cast<const uint8_t*>(scales), K, n_exp, rows_per_expert, I,
+                                          gate_up ? 1 : 0, rows_per_expert / kBM, dst);
+  return cudaGetLastError();
 }
 
 }  // namespace moe
