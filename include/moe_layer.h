@@ -179,14 +179,22 @@ moe_status moe_layer_enable_timing(moe_layer* layer, int32_t enable);
 moe_status moe_layer_stage_times(moe_layer* layer, float* ms, int32_t* n_forwards);
 
 /*
- * Profiling hook: with a device buffer of n_ctas x 16 uint64 (n_ctas >= the device's SM
- * count), each later fused-decode forward writes per-CTA %globaltimer stamps (ns) at its
- * phase boundaries into buffer[cta * 16 + phase]: 0 start, 1 activation panel built,
- * 2 router rows done, 3 routing published (selecting CTA only), 4 shared gate/up done,
- * 5 shared gate/up of all CTAs seen, 6 shared down done, 7 routing seen, 8 routed gate/up
- * done, 9 first routed expert's gate/up seen, 10 routed down done, 11 all CTAs' down
- * seen, 12 output written, 13 producer done with shared tiles, 14 producer saw routing.
- * buffer = NULL switches it off (the default). Other paths ignore it.
+ * Profiling hook. With a device buffer of n_ctas x 64 uint64 (n_ctas >= the device's SM
+ * count), later forwards write per-CTA records into buffer[cta * 64 + slot]:
+ *  - fused decode kernel, slots 0..14, %globaltimer stamps (ns) at its phase boundaries:
+ *    0 start, 1 activations staged, 2 router rows done, 4 shared gate/up done, 5 shared
+ *    gate/up of all CTAs seen, 6 shared down done, 7 routing seen, 8 routed gate/up done,
+ *    9 first routed expert's gate/up seen, 10 routed down done, 11 all CTAs' down seen,
+ *    12 output written, 13 producer done with shared items, 14 producer has the routing;
+ *    and in slots 16..22 clock cycles of consumer thread 0 waiting for item data,
+ *    computing items, reducing tiles, switching experts, the items it consumed, the
+ *    producer's cycles waiting for a free slot and the items it issued;
+ *  - grouped GEMMs, slots 16..26 (gate/up), 32..42 (down), 48..58 (separately stored
+ *    shared expert, gate/up), clock cycles: +0 kernel, +1 MMA waiting for operands, +2 MMA
+ *    waiting for an accumulator, +3 dequantiser waiting for weights, +4 dequantiser waiting
+ *    for a free stage, +5 activation producer waiting, +6 weight producer waiting, +7
+ *    epilogue waiting, +8 epilogue busy, +9 tiles, +10 dequantiser loop.
+ * buffer = NULL switches it off (the default).
  */
 moe_status moe_layer_set_trace(moe_layer* layer, void* buffer, int32_t n_ctas);
 

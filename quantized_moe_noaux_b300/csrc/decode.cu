@@ -60,7 +60,7 @@ constexpr uint32_t kMbarSpin = 1u << 22;
 // Shared memory common to both modes (16-byte aligned: the reduction buffer takes float4
 // stores).
 struct alignas(16) DecCommon {
-  float red[8][32][4];                 // cross-warp reduction
+  float red[2][8][32][4];              // cross-warp reduction (double-buffered per tile)
   float selb[kMaxE];                   // selection scratch (producer warp)
   float sels[kMaxE];
   int idsel[8][kMaxK];                 // per token: selected experts and weights
@@ -374,7 +374,7 @@ __device__ __forceinline__ void compute_item0(const uint2* panel, const float* s
 
 // Cross-warp reduction of the tile accumulators into red (consumers, then named barrier).
 template <int MODE>
-__device__ __forceinline__ void stash_acc(DecCommon& C, float (&acc)[4]) {
+__device__ __forceinline__ void stash_acc(DecCommon& C, int rb, float (&acc)[4]) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   if (MODE == 1) {
 #pragma unroll
@@ -383,26 +383,26 @@ __device__ __forceinline__ void stash_acc(DecCommon& C, float (&acc)[4]) {
       acc[1] += __shfl_xor_sync(0xffffffffu, acc[1], o);
     }
     if ((lane & 3) == 0) {
-      C.red[w][lane >> 2][0] = acc[0];
-      C.red[w][lane >> 2][1] = acc[1];
+      C.red[rb][w][lane >> 2][0] = acc[0];
+      C.red[rb][w][lane >> 2][1] = acc[1];
     }
   } else {
-    *reinterpret_cast<float4*>(&C.red[w][lane][0]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(&C.red[rb][w][lane][0]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
   }
 }
 
 // Value of MMA row r (0..15) for column n after the reduction (rows 8..15 carry a x16 unit).
 template <int MODE>
-__device__ __forceinline__ float reduced(const DecCommon& C, int r, int n) {
+__device__ __forceinline__ float reduced(const DecCommon& C, int rb, int r, int n) {
   float v = 0.f;
   if (MODE == 1) {
 #pragma unroll
-    for (int w = 0; w < 8; ++w) v += C.red[w][r & 7][r >> 3];
+    for (int w = 0; w < 8; ++w) v += C.red[rb][w][r & 7][r >> 3];
   } else {
     const int ln = (r & 7) * 4 + (n >> 1);
     const int idx = (r >> 3) * 2 + (n & 1);
 #pragma unroll
-    for (int w = 0; w < 8; ++w) v += C.red[w][ln][idx];
+    for (int w = 0; w < 8; ++w) v += C.red[rb][w][ln][idx];
   }
   return (r >= 8) ? v * 0.0625f : v;
 }
@@ -518,7 +518,7 @@ struct DecodeArgs {
   uint32_t* sync;              // see the kernel
   int* status;
   uint32_t spin_max;
-  unsigned long long* trace;   // optional [grid][16] phase timestamps (ns), or NULL
+  unsigned long long* trace;   // optional [grid][64] phase timestamps (ns, slots 0..15), or NULL
 };
 
 namespace {
@@ -532,7 +532,7 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // Phase timestamp of this CTA (profiling hook; one thread records).
 #define DEC_TRACE(i)                                                            \
   do {                                                                          \
-    if (a.trace) a.trace[(size_t)blockIdx.x * 16 + (i)] = global_ns();          \
+    if (a.trace) a.trace[(size_t)blockIdx.x * 64 + (i)] = global_ns();          \
   } while (0)
 
 // Producer warp (all lanes): wait for every CTA's router rows, select every token, group
@@ -667,11 +667,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     const uint64_t pol = ptx::policy_evict_first();
     int it = 0;
     bool ok = true;
+    unsigned long long p_wait = 0;   // cycles waiting for a free slot (profiling)
     // Brings item `it` into slot it % kSlots once the consumers released its previous use.
     auto issue = [&](const uint8_t* src) {
       if (!ok) return;
       const int slot = it % kSlots;
+      const unsigned long long t0 = clock64();
       if (it >= kSlots && !ptx::mbar_wait(&S.empty[slot], ((it / kSlots) - 1) & 1, kMbarSpin)) ok = false;
+      p_wait += clock64() - t0;
       if (ok && *(volatile int*)&C.abort) ok = false;
       if (!ok) return;
       ptx::mbar_arrive_expect_tx(&S.full[slot], kItemBytes);
@@ -710,6 +713,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       if (!ok) {
         atomicExch(&C.abort, 1);
         raise_status(a.status, MOE_ERR_TIMEOUT);
+      }
+      if (a.trace) {
+        a.trace[(size_t)blockIdx.x * 64 + 21] = p_wait;
+        a.trace[(size_t)blockIdx.x * 64 + 22] = (unsigned long long)it;
       }
     }
   } else {
@@ -779,13 +786,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
         float v = racc[i];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) C.red[warp][i][0] = v;
+        if (lane == 0) C.red[0][warp][i][0] = v;
       }
       ptx::bar_sync(1, kConsumers);
       if (tid < T) {
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) v += C.red[w][tid][0];
+        for (int w = 0; w < 8; ++w) v += C.red[0][w][tid][0];
         a.logits[(size_t)tid * E + e] = v;
       }
       ptx::bar_sync(1, kConsumers);
@@ -797,6 +804,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     }
 
     float acc[4];
+    // profiling counters (cycles, consumer thread 0): waiting for item data, computing items,
+    // tile reduction and epilogue, expert transitions
+    unsigned long long c_wait = 0, c_comp = 0, c_epi = 0, c_tr = 0;
     int it = 0;          // items consumed
     int it_ok = 0;       // items whose copy this CTA saw complete (contiguous prefix)
     // Wait for item `it`; on time-out or abort the item is skipped and not released, so
@@ -815,7 +825,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     auto run_items = [&](int np, bool up) {
       for (int p = 0; p < np; ++p) {
         const uint8_t* slot;
+        const unsigned long long t0 = clock64();
         const bool have = wait_item(slot);
+        const unsigned long long t1 = clock64();
+        c_wait += t1 - t0;
         if (have) {
           if constexpr (MODE == 1) {
             compute_item1(up ? S.xs : S.hs, up ? S.xsums : S.hsums, slot, p * 128, p * 8 + warp, acc);
@@ -824,6 +837,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
           }
         }
         __syncwarp();
+        c_comp += clock64() - t1;
         if (have) {
           if (lane == 0) ptx::mbar_arrive(&S.empty[it % kSlots]);
           if (it_ok == it) ++it_ok;
@@ -839,46 +853,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       up_n = 0;
     };
 
-    // gate/up tile `tl` of expert `e`; h rows of the routed tokens in C.colpair
-    auto up_tile = [&](int e, int tl) {
-      if (e != up_e) {
-        flush_up();
-        up_e = e;
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] = 0.f;
-      run_items(g.Pu, true);
-      stash_acc<MODE>(C, acc);
-      ptx::bar_sync(1, kConsumers);
-      const int nt = (MODE == 1) ? 8 : 64;
-      if (tid < nt) {
-        const int r = (MODE == 1) ? tid : (tid >> 3), n = (MODE == 1) ? 0 : (tid & 7);
-        const int pr = C.colpair[n];
-        if (pr >= 0) {
-          const float gate = reduced<MODE>(C, r, n), up = reduced<MODE>(C, r + 8, n);
-          a.h16[(size_t)pr * g.I + tl * 8 + r] = __float2half_rn(siluf_acc(gate) * up);
-        }
-      }
-      ptx::bar_sync(1, kConsumers);
-      ++up_n;
-    };
-
-    // down tile `tl` (16 output rows) of the current expert: out_acc += w * y
-    auto down_tile = [&](int tl) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] = 0.f;
-      run_items(g.Pd, false);
-      stash_acc<MODE>(C, acc);
-      ptx::bar_sync(1, kConsumers);
-      const int nt = (MODE == 1) ? 16 : 128;
-      if (tid < nt) {
-        const int r = (MODE == 1) ? tid : (tid >> 3), n = (MODE == 1) ? 0 : (tid & 7);
-        const float wn = C.colw[n];
-        if (n < T && wn != 0.f) atomicAdd(a.out_acc + (size_t)n * H + tl * 16 + r, wn * reduced<MODE>(C, r, n));
-      }
-      ptx::bar_sync(1, kConsumers);
-    };
-
     // one thread waits until every gate/up tile of expert e is done; uniform continuation
     auto wait_up = [&](int e) {
       if (tid == 0) {
@@ -891,80 +865,100 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       ptx::bar_sync(1, kConsumers);
     };
 
-    // colpair / colw for the shared expert (sl < 0) or active slot `sl`
-    auto set_meta = [&](int sl) {
-      ptx::bar_sync(1, kConsumers);
-      if (tid < 8) {
-        if (sl < 0) {
-          C.colpair[tid] = tid < T ? T * g.k + tid : -1;
-          C.colw[tid] = tid < T ? 1.f : 0.f;
-        } else {
-          C.colpair[tid] = C.meta_pair[sl][tid];
-          C.colw[tid] = C.meta_w[sl][tid];
+    // One loop over the four phases (A shared gate/up, C1 shared down, B routed gate/up,
+    // C2 routed down) so the unrolled item body exists once in the code: the consumer's
+    // instruction footprint stays small. Tile results are reduced through a double-buffered
+    // block, so one barrier per tile suffices.
+    int lo = a0, hi = a1, cur_sl = -2, cur_up = -1, rb = 0;
+#pragma unroll 1
+    for (int ph = 0; ph < 4; ++ph) {
+      if (ph == 1) {
+        lo = c10;
+        hi = c11;
+      } else if (ph == 2) {
+        if (tid == 0) DEC_TRACE(6);
+        // routing known (the producer warp computed it)
+        if (!ptx::mbar_wait(&S.route_bar, 0, kMbarSpin * 16) && tid == 0) {
+          atomicExch(&C.abort, 1);
+          raise_status(a.status, MOE_ERR_TIMEOUT);
         }
+        ptx::bar_sync(1, kConsumers);
+        if (tid == 0) DEC_TRACE(7);
+        seg_range(C.n_active * g.NTu, g.G, g.c, lo, hi);
+      } else if (ph == 3) {
+        seg_range(C.n_active * g.NTd, g.G, g.c, lo, hi);
       }
-      ptx::bar_sync(1, kConsumers);
-    };
-
-    auto stage_h = [&]() {
-      if constexpr (MODE == 1) {
-        stage_h1(S, a.h16, g.I);
-      } else {
-        stage_h0(S, a.h16, g.I);
+      const int up = (ph & 1) == 0;
+      const int ntl = up ? g.NTu : g.NTd;
+#pragma unroll 1
+      for (int u = lo; u < hi; ++u) {
+        const int sl = ph < 2 ? -1 : u / ntl;
+        const int tl = ph < 2 ? u : u % ntl;
+        const int e = sl < 0 ? shared_e : C.active[sl];
+        const unsigned long long tt0 = clock64();
+        if (sl != cur_sl || up != cur_up) {
+          // new expert or new direction: publish finished gate/up tiles, load the columns'
+          // h rows and weights, and for down tiles wait for that expert's h and stage it
+          flush_up();
+          up_e = e;
+          ptx::bar_sync(1, kConsumers);
+          if (tid < 8) {
+            if (sl < 0) {
+              C.colpair[tid] = tid < T ? T * g.k + tid : -1;
+              C.colw[tid] = tid < T ? 1.f : 0.f;
+            } else {
+              C.colpair[tid] = C.meta_pair[sl][tid];
+              C.colw[tid] = C.meta_w[sl][tid];
+            }
+          }
+          ptx::bar_sync(1, kConsumers);
+          if (!up) {
+            wait_up(e);
+            if (tid == 0 && ph == 1) DEC_TRACE(5);
+            if (tid == 0 && ph == 3) DEC_TRACE(9);
+            if constexpr (MODE == 1) {
+              stage_h1(S, a.h16, g.I);
+            } else {
+              stage_h0(S, a.h16, g.I);
+            }
+            ptx::bar_sync(1, kConsumers);
+          }
+          cur_sl = sl;
+          cur_up = up;
+        }
+        c_tr += clock64() - tt0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+        run_items(up ? g.Pu : g.Pd, up != 0);
+        const unsigned long long te0 = clock64();
+        stash_acc<MODE>(C, rb, acc);
+        ptx::bar_sync(1, kConsumers);
+        if (up) {
+          const int nt = (MODE == 1) ? 8 : 64;
+          if (tid < nt) {
+            const int r = (MODE == 1) ? tid : (tid >> 3), n = (MODE == 1) ? 0 : (tid & 7);
+            const int pr = C.colpair[n];
+            if (pr >= 0) {
+              const float gate = reduced<MODE>(C, rb, r, n), upv = reduced<MODE>(C, rb, r + 8, n);
+              a.h16[(size_t)pr * g.I + tl * 8 + r] = __float2half_rn(siluf_acc(gate) * upv);
+            }
+          }
+          ++up_n;
+        } else {
+          const int nt = (MODE == 1) ? 16 : 128;
+          if (tid < nt) {
+            const int r = (MODE == 1) ? tid : (tid >> 3), n = (MODE == 1) ? 0 : (tid & 7);
+            const float wn = C.colw[n];
+            if (n < T && wn != 0.f)
+              atomicAdd(a.out_acc + (size_t)n * H + tl * 16 + r, wn * reduced<MODE>(C, rb, r, n));
+          }
+        }
+        rb ^= 1;
+        c_epi += clock64() - te0;
       }
-      ptx::bar_sync(1, kConsumers);
-    };
-
-    // ---- A: shared gate/up
-    set_meta(-1);
-    for (int tl = a0; tl < a1; ++tl) up_tile(shared_e, tl);
-    flush_up();
-    if (tid == 0) DEC_TRACE(4);
-    // ---- C1: shared down (needs every shared gate/up tile)
-    if (c11 > c10) {
-      wait_up(shared_e);
-      if (tid == 0) DEC_TRACE(5);
-      stage_h();   // colpair still describes the shared expert
-      for (int tl = c10; tl < c11; ++tl) down_tile(tl);
+      if (up) flush_up();
+      if (tid == 0) DEC_TRACE(ph == 0 ? 4 : ph == 2 ? 8 : 10);
     }
-    if (tid == 0) DEC_TRACE(6);
-    // ---- routing known (the producer warp computed it)
-    if (!ptx::mbar_wait(&S.route_bar, 0, kMbarSpin * 16) && tid == 0) {
-      atomicExch(&C.abort, 1);
-      raise_status(a.status, MOE_ERR_TIMEOUT);
-    }
-    ptx::bar_sync(1, kConsumers);
-    const int na = C.n_active;
-    int b0, b1, c20, c21;
-    seg_range(na * g.NTu, g.G, g.c, b0, b1);
-    seg_range(na * g.NTd, g.G, g.c, c20, c21);
-    if (tid == 0) DEC_TRACE(7);
-    // ---- B: selected experts' gate/up
-    int cur = -1;
-    for (int r = b0; r < b1; ++r) {
-      const int sl = r / g.NTu, tl = r % g.NTu;
-      if (sl != cur) {
-        set_meta(sl);
-        cur = sl;
-      }
-      up_tile(C.active[sl], tl);
-    }
-    flush_up();
-    if (tid == 0) DEC_TRACE(8);
-    // ---- C2: selected experts' down
-    cur = -1;
-    for (int u = c20; u < c21; ++u) {
-      const int sl = u / g.NTd, tl = u % g.NTd;
-      if (sl != cur) {
-        set_meta(sl);
-        wait_up(C.active[sl]);
-        if (tid == 0 && cur < 0) DEC_TRACE(9);
-        stage_h();
-        cur = sl;
-      }
-      down_tile(tl);
-    }
-    if (tid == 0) DEC_TRACE(10);
     // ---- every CTA's down tiles are in out_acc: convert this CTA's slice of the output
     ptx::bar_sync(1, kConsumers);
     if (tid == 0) {
@@ -984,6 +978,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     if (tid == 0) {
       C.consumed = it_ok;
       DEC_TRACE(12);
+      if (a.trace) {
+        unsigned long long* tr = a.trace + (size_t)blockIdx.x * 64;
+        tr[16] = c_wait;
+        tr[17] = c_comp;
+        tr[18] = c_epi;
+        tr[19] = c_tr;
+        tr[20] = (unsigned long long)it;
+      }
     }
   }
   __syncthreads();

@@ -16,8 +16,10 @@
 //              scales per copy (18 KB, laid out at layer creation for conflict-free reads)
 //   warps 4-11 dequantise 64 columns per K stage into an fp16 tile in the 128-byte swizzle
 //              layout the MMA reads (int4 * fp16 scale rounded once to fp16; E2M1 * E4M3 is
-//              exact in fp16, the fp32 tensor scales are applied in the epilogue)
-//   warp 12    TMA: the N x 64 fp16 activation tile of the same K stage
+//              exact in fp16, the fp32 tensor scales are applied in the epilogue); two groups
+//              of 4 warps take alternate stages, a thread converts one row of its stage
+//   warp 12    TMA: the N x 64 fp16 activation tile of the same K stage (one box of 32, 64,
+//              128 or 256 rows)
 //   warp 13    issues tcgen05.mma kind::f16 (M=128, N, K=16) x 4 per stage into one of two
 //              TMEM accumulators (256 columns each) and releases stages with tcgen05.commit
 //   warps 0-3  epilogue of the previous tile while the next one runs: tcgen05.ld, then
@@ -26,8 +28,9 @@
 //              whose h is quantised next);
 //     down:    out_acc[token] += w[token, slot] * y (fp32 atomics; the weighted combine).
 // A separately stored bf16 shared expert (the NVFP4 layers keep it unquantised) is
-// converted to fp16 once at layer creation (exact for its range) and runs through the same
-// kernel with its weight tiles loaded by TMA straight into the MMA's layout (kWF16).
+// converted to fp16 once at layer creation (exact for its range, gate/up rows stored in tile
+// order) and runs through the same kernel with each stage's 128-row weight tile loaded by
+// one TMA box straight into the MMA's layout (kWF16).
 // Every wait is bounded; a time-out sets MOE_ERR_TIMEOUT, the CTA stops issuing work, lets
 // copies and MMAs in flight land, frees its TMEM and exits.
 #include <cuda.h>
@@ -90,6 +93,14 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity) {
   return false;
 }
 
+// Same, adding the cycles spent waiting to `acc` (profiling trace).
+__device__ __forceinline__ bool wait_bar_t(uint64_t* bar, uint32_t parity, unsigned long long& acc) {
+  const unsigned long long t0 = clock64();
+  const bool ok = wait_bar(bar, parity);
+  acc += clock64() - t0;
+  return ok;
+}
+
 __device__ __forceinline__ void set_abort(GSmem& S, int* status) {
   atomicExch(&S.abort, 1);
   raise_status(status, MOE_ERR_TIMEOUT);
@@ -137,19 +148,11 @@ __device__ __forceinline__ __half e4m3_to_half(uint32_t b) {
   return __hmul(v, __float2half(256.f));
 }
 
-// Weight row of 16-row box j of tile mt (fp16 weights loaded by TMA): gate/up tiles pair
-// box 2w (gate rows 64 mt + 16 w ..) with box 2w+1 (the matching up rows).
-template <int EPI>
-__device__ __forceinline__ int weight_row(const GemmParams& p, int e, int mt, int j) {
-  e -= p.e_sub;
-  if (EPI == 0) return e * p.rows_per_expert + ((j & 1) ? p.I : 0) + 64 * mt + 16 * (j >> 1);
-  return e * p.rows_per_expert + kBM * mt + kBoxRows * j;
-}
-
 template <int WFMT, int EPI>
 __global__ void __launch_bounds__(kGThreads, 1)
-moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
-                const GemmParams p) {
+moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b32,
+                const __grid_constant__ CUtensorMap tm_b64, const __grid_constant__ CUtensorMap tm_b128,
+                const __grid_constant__ CUtensorMap tm_b256, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   GSmem& S = *reinterpret_cast<GSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int MT = p.mtiles;
@@ -160,11 +163,19 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
   const int NK = p.K / kBK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Tk = p.T * p.top_k;
+  const unsigned long long t_start = clock64();
+  // optional per-CTA trace (cycles): [0] kernel, [1] MMA waiting operands, [2] MMA waiting
+  // an accumulator, [3] dequant waiting weights, [4] dequant waiting a free stage, [5]
+  // activation producer waiting, [6] weight producer waiting, [7] epilogue waiting, [8]
+  // epilogue busy, [9] tiles, [10] dequant loop
+  unsigned long long* tr = p.trace ? p.trace + (size_t)blockIdx.x * 64 + p.trace_base : nullptr;
+  unsigned long long w0 = 0, w1 = 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kABStages; ++s) {
-      // B producer (+ tx) and the dequant warps, or the two TMA producers (fp16 weights)
-      ptx::mbar_init(&S.full_ab[s], WFMT == kWF16 ? 2 : 1 + kDqWarps);
+      // B producer (+ tx) and one dequant group (4 warps), or the two TMA producers (fp16
+      // weights)
+      ptx::mbar_init(&S.full_ab[s], WFMT == kWF16 ? 2 : 1 + kDqWarps / 2);
       ptx::mbar_init(&S.empty_ab[s], 1);   // tcgen05.commit
     }
     for (int s = 0; s < kWStages; ++s) {
@@ -200,22 +211,19 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
           // fp16 weight tiles straight into the MMA's A stages
           for (int ks = 0; ks < NK; ++ks, ++kg) {
             const int s = kg % kABStages;
-            if (kg >= kABStages && !wait_bar(&S.empty_ab[s], ((kg / kABStages) - 1) & 1)) {
+            if (kg >= kABStages && !wait_bar_t(&S.empty_ab[s], ((kg / kABStages) - 1) & 1, w0)) {
               set_abort(S, p.status);
               break;
             }
             ptx::mbar_arrive_expect_tx(&S.full_ab[s], kAStage);
-#pragma unroll 1
-            for (int j = 0; j < kBM / kBoxRows; ++j)
-              ptx::tma_load_2d(S.a[s] + j * kBoxRows * 128, &tm_w, ks * kBK, weight_row<EPI>(p, e, mt, j),
-                               &S.full_ab[s]);
+            ptx::tma_load_2d(S.a[s], &tm_w, ks * kBK, (e - p.e_sub) * p.rows_per_expert + kBM * mt, &S.full_ab[s]);
           }
         } else {
           const uint8_t* src =
               p.wpack + ((size_t)(e - p.e_sub) * MT + mt) * (size_t)(NK / kSub) * kGroupBytes;
           for (int g = 0; g < NK / kSub; ++g, ++wg) {
             const int s = wg % kWStages;
-            if (wg >= kWStages && !wait_bar(&S.empty_w[s], ((wg / kWStages) - 1) & 1)) {
+            if (wg >= kWStages && !wait_bar_t(&S.empty_w[s], ((wg / kWStages) - 1) & 1, w0)) {
               set_abort(S, p.status);
               break;
             }
@@ -225,27 +233,34 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
           }
         }
       }
+      if (tr) tr[6] = w0;
     }
   } else if (warp == kWarpB) {
     // ------------------------------------------------------- activation producer
     if (lane == 0) {
-      ptx::prefetch_tmap(&tm_b);
+      ptx::prefetch_tmap(&tm_b32);
+      ptx::prefetch_tmap(&tm_b64);
+      ptx::prefetch_tmap(&tm_b128);
+      ptx::prefetch_tmap(&tm_b256);
       int kg = 0;
       for (int t = blockIdx.x; t < ntiles && !aborted(S); t += gridDim.x) {
         const int4 it = __ldg(p.items + skip + t / MT);
-        const int row0 = it.y, nbox = (it.z + kBoxRows - 1) / kBoxRows;
+        const int row0 = it.y, n = it.z;
+        // one TMA box per stage, the shortest of 32/64/128/256 rows that covers the tile
+        // (rows past the tile land in the stage buffer but the MMA's N stops short of them)
+        const CUtensorMap* tm = n <= 32 ? &tm_b32 : n <= 64 ? &tm_b64 : n <= 128 ? &tm_b128 : &tm_b256;
+        const uint32_t box_bytes = (n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : 256u) * 128u;
         for (int ks = 0; ks < NK; ++ks, ++kg) {
           const int s = kg % kABStages;
-          if (kg >= kABStages && !wait_bar(&S.empty_ab[s], ((kg / kABStages) - 1) & 1)) {
+          if (kg >= kABStages && !wait_bar_t(&S.empty_ab[s], ((kg / kABStages) - 1) & 1, w0)) {
             set_abort(S, p.status);
             break;
           }
-          ptx::mbar_arrive_expect_tx(&S.full_ab[s], (uint32_t)nbox * kBoxRows * 128);
-#pragma unroll 1
-          for (int j = 0; j < nbox; ++j)
-            ptx::tma_load_2d(S.b[s] + j * kBoxRows * 128, &tm_b, ks * kBK, row0 + kBoxRows * j, &S.full_ab[s]);
+          ptx::mbar_arrive_expect_tx(&S.full_ab[s], box_bytes);
+          ptx::tma_load_2d(S.b[s], tm, ks * kBK, row0, &S.full_ab[s]);
         }
       }
+      if (tr) tr[5] = w0;
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------- MMA issuer
@@ -256,7 +271,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
         const int N = ((it.z + kBoxRows - 1) / kBoxRows) * kBoxRows;
         const uint32_t idesc = ptx::f16_idesc(kBM, N, false);
         const int buf = tc & 1;
-        if (tc >= 2 && !wait_bar(&S.tmem_empty[buf], ((tc >> 1) - 1) & 1)) {
+        if (tc >= 2 && !wait_bar_t(&S.tmem_empty[buf], ((tc >> 1) - 1) & 1, w1)) {
           set_abort(S, p.status);
           break;
         }
@@ -264,7 +279,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
         const uint32_t d = tmem + (uint32_t)(buf * kAccCols);
         for (int ks = 0; ks < NK; ++ks, ++kg) {
           const int s = kg % kABStages;
-          if (!wait_bar(&S.full_ab[s], (kg / kABStages) & 1)) {
+          if (!wait_bar_t(&S.full_ab[s], (kg / kABStages) & 1, w0)) {
             set_abort(S, p.status);
             break;
           }
@@ -278,54 +293,74 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
         }
         ptx::tc_commit(&S.tmem_full[buf]);
       }
+      if (tr) {
+        tr[1] = w0;
+        tr[2] = w1;
+        tr[9] = tc;
+      }
     }
   } else if (warp >= kDqWarp0) {
     // ------------------------------------------------ dequantisers (warps 4-11)
+    // Two groups of 4 warps take alternate K stages (group 0 the even ones); a thread
+    // converts one whole 64-column row of its stage, then fences once for the tensor core.
     if (WFMT != kWF16) {
       const int dq = threadIdx.x - kDqWarp0 * 32;
-      const int r = dq & (kBM - 1), h = dq >> 7;   // A row, column half (32 of the stage's 64)
+      const int grp = dq >> 7, r = dq & (kBM - 1);
       uint8_t* const arow_base = &S.a[0][0] + (r >> 3) * 1024 + (r & 7) * 128;
+      unsigned long long w0d = 0, w1d = 0;
       int kg = 0, wg = 0;
       bool stop = false;
       for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
         for (int ks = 0; ks < NK; ++ks, ++kg) {
           const int kq = ks % kSub, ws = wg % kWStages;
-          if (kq == 0 && !wait_bar(&S.full_w[ws], (wg / kWStages) & 1)) set_abort(S, p.status);
-          const int s = kg % kABStages;
-          if (kg >= kABStages && !wait_bar(&S.empty_ab[s], ((kg / kABStages) - 1) & 1)) set_abort(S, p.status);
-          if (__any_sync(0xffffffffu, aborted(S))) {   // warp-uniform exit
-            stop = true;
-            break;
-          }
-          const int slot = (kq * 2 + h) * kBM + r;
-          const uint4 q = *reinterpret_cast<const uint4*>(S.w[ws] + slot * 16);
-          const uint32_t sc = *reinterpret_cast<const unsigned short*>(S.w[ws] + kGroupCodes + slot * 2);
-          uint4 o[4];
-          if (WFMT == MOE_W_INT4_G32) {
-            const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)sc));
-            o[0] = dq_int4x8(q.x, s2);
-            o[1] = dq_int4x8(q.y, s2);
-            o[2] = dq_int4x8(q.z, s2);
-            o[3] = dq_int4x8(q.w, s2);
-          } else {
-            const __half2 s0 = __half2half2(e4m3_to_half(sc & 0xFFu));
-            const __half2 s1 = __half2half2(e4m3_to_half(sc >> 8));
-            o[0] = dq_e2m1x8(q.x, s0);
-            o[1] = dq_e2m1x8(q.y, s0);
-            o[2] = dq_e2m1x8(q.z, s1);
-            o[3] = dq_e2m1x8(q.w, s1);
-          }
-          uint8_t* arow = arow_base + s * kAStage;
+          if ((kq & 1) == grp) {
+            if (kq == grp && !wait_bar_t(&S.full_w[ws], (wg / kWStages) & 1, w0d)) set_abort(S, p.status);
+            const int s = kg % kABStages;
+            if (kg >= kABStages && !wait_bar_t(&S.empty_ab[s], ((kg / kABStages) - 1) & 1, w1d))
+              set_abort(S, p.status);
+            if (__any_sync(0xffffffffu, aborted(S))) {   // warp-uniform exit
+              stop = true;
+              break;
+            }
+            uint8_t* arow = arow_base + s * kAStage;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(arow + (((4 * h + j) ^ (r & 7)) << 4)) = o[j];
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::mbar_arrive(&S.full_ab[s]);
-            if (kq == kSub - 1) ptx::mbar_arrive(&S.empty_w[ws]);
+            for (int h = 0; h < 2; ++h) {
+              const int slot = (kq * 2 + h) * kBM + r;
+              const uint4 q = *reinterpret_cast<const uint4*>(S.w[ws] + slot * 16);
+              const uint32_t sc = *reinterpret_cast<const unsigned short*>(S.w[ws] + kGroupCodes + slot * 2);
+              uint4 o[4];
+              if (WFMT == MOE_W_INT4_G32) {
+                const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)sc));
+                o[0] = dq_int4x8(q.x, s2);
+                o[1] = dq_int4x8(q.y, s2);
+                o[2] = dq_int4x8(q.z, s2);
+                o[3] = dq_int4x8(q.w, s2);
+              } else {
+                const __half2 s0 = __half2half2(e4m3_to_half(sc & 0xFFu));
+                const __half2 s1 = __half2half2(e4m3_to_half(sc >> 8));
+                o[0] = dq_e2m1x8(q.x, s0);
+                o[1] = dq_e2m1x8(q.y, s0);
+                o[2] = dq_e2m1x8(q.z, s1);
+                o[3] = dq_e2m1x8(q.w, s1);
+              }
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4*>(arow + (((4 * h + j) ^ (r & 7)) << 4)) = o[j];
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::mbar_arrive(&S.full_ab[s]);
+              if (kq >= kSub - 2) ptx::mbar_arrive(&S.empty_w[ws]);   // this group's last stage
+            }
           }
           if (kq == kSub - 1) ++wg;
         }
+      }
+      if (tr && threadIdx.x == kDqWarp0 * 32) {
+        tr[3] = w0d;
+        tr[4] = w1d;
+        tr[10] = clock64() - t_start;
       }
     }
   } else {
@@ -351,8 +386,9 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
         }
         ptx::bar_sync(2, kEpiWarps * 32);
       }
-      if (!wait_bar(&S.tmem_full[buf], (tc >> 1) & 1)) set_abort(S, p.status);
+      if (!wait_bar_t(&S.tmem_full[buf], (tc >> 1) & 1, w0)) set_abort(S, p.status);
       if (__any_sync(0xffffffffu, aborted(S))) break;
+      const unsigned long long t_busy = clock64();
       ptx::tc_fence_after();
       float sc_out = 1.f;
       if (WFMT == MOE_W_NVFP4)
@@ -400,12 +436,18 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&S.tmem_empty[buf]);
+      w1 += clock64() - t_busy;
+    }
+    if (tr && threadIdx.x == 0) {
+      tr[7] = w0;
+      tr[8] = w1;
     }
   }
 
   // ---------------------------------------------------------------------- teardown
   ptx::tc_fence_before();
   __syncthreads();
+  if (tr && threadIdx.x == 0) tr[0] = clock64() - t_start;
   if (aborted(S) && threadIdx.x == 0) {
     // copies and MMAs issued before the abort complete on their own; give them time to land
     for (int i = 0; i < 2000; ++i) __nanosleep(1000);
@@ -478,22 +520,49 @@ __global__ void gemm_pack_kernel(const uint8_t* __restrict__ codes, const uint8_
 // tokens. n_items[0] = routed items, n_items[1] = shared items, n_items[2] = both.
 __global__ void gemm_items_kernel(const int32_t* __restrict__ offsets, int E, int T, int top_k,
                                   int4* __restrict__ items, int32_t* __restrict__ n_items) {
-  if (threadIdx.x != 0) return;
-  int n = 0;
-  for (int e = 0; e < E; ++e) {
-    const int o = offsets[e], c = offsets[e + 1] - o;
-    for (int j = 0; j < c; j += kBN) items[n++] = make_int4(e, o + j, min(kBN, c - j), 0);
+  // one warp: lane owns a contiguous run of experts; a warp scan gives its first item slot
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x >= 32) return;
+  const int per = (E + 31) / 32;
+  const int x0 = min(E, lane * per), x1 = min(E, x0 + per);
+  int mine = 0;
+  for (int x = x0; x < x1; ++x) mine += (offsets[x + 1] - offsets[x] + kBN - 1) / kBN;
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
   }
-  const int nr = n;
-  for (int j = 0; j < T; j += kBN) items[n++] = make_int4(E, T * top_k + j, min(kBN, T - j), 0);
-  n_items[0] = nr;
-  n_items[1] = n - nr;
-  n_items[2] = n;
+  int pos = incl - mine;
+  for (int x = x0; x < x1; ++x) {
+    const int o = offsets[x], c = offsets[x + 1] - o;
+    for (int j = 0; j < c; j += kBN) items[pos++] = make_int4(x, o + j, min(kBN, c - j), 0);
+  }
+  const int nr = __shfl_sync(0xffffffffu, incl, 31);
+  const int nsh = (T + kBN - 1) / kBN;
+  for (int j = lane; j < nsh; j += 32) items[nr + j] = make_int4(E, T * top_k + kBN * j, min(kBN, T - kBN * j), 0);
+  if (lane == 0) {
+    n_items[0] = nr;
+    n_items[1] = nsh;
+    n_items[2] = nr + nsh;
+  }
 }
 
-__global__ void bf16_to_f16_kernel(const uint16_t* __restrict__ src, __half* __restrict__ dst, size_t n) {
-  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256)
-    dst[i] = __float2half_rn(__uint_as_float((uint32_t)src[i] << 16));
+// bf16 [rows][K] -> fp16. With gate_up, output row 128 mt + 32 w + l takes gate row
+// 64 mt + 16 w + l (l < 16) or up row I + 64 mt + 16 w + (l - 16), the row order of the
+// grouped GEMM's gate/up tiles, so one 128-row TMA box loads a whole tile.
+__global__ void bf16_to_f16_kernel(const uint16_t* __restrict__ src, __half* __restrict__ dst, size_t rows, int K,
+                                   int gate_up, int I) {
+  const size_t n = rows * (size_t)K;
+  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256) {
+    const size_t r = i / K, c = i % K;
+    size_t sr = r;
+    if (gate_up) {
+      const int mt = (int)(r / 128), w = (int)(r % 128) / 32, l = (int)(r % 32);
+      sr = l < 16 ? 64 * mt + 16 * w + l : I + 64 * mt + 16 * w + (l - 16);
+    }
+    dst[i] = __float2half_rn(__uint_as_float((uint32_t)src[sr * K + c] << 16));
+  }
 }
 
 // Expert-sorted activation rows for the gate/up GEMM: row q < T*k is the token of entry q,
@@ -585,7 +654,9 @@ EncodeTiledFn encode_fn() {
 template <int WFMT, int EPI>
 cudaError_t launch_gemm_t(const GemmMaps& m, const GemmParams& p, int grid, cudaStream_t s) {
   moe_gemm_kernel<WFMT, EPI><<<grid, kGThreads, kGSmemBytes, s>>>(
-      *reinterpret_cast<const CUtensorMap*>(&m.codes), *reinterpret_cast<const CUtensorMap*>(&m.act), p);
+      *reinterpret_cast<const CUtensorMap*>(&m.codes), *reinterpret_cast<const CUtensorMap*>(&m.act[0]),
+      *reinterpret_cast<const CUtensorMap*>(&m.act[1]), *reinterpret_cast<const CUtensorMap*>(&m.act[2]),
+      *reinterpret_cast<const CUtensorMap*>(&m.act[3]), p);
   return cudaGetLastError();
 }
 
@@ -636,10 +707,13 @@ cudaError_t launch_gemm_items(const int32_t* offsets, int E, int T, int top_k, i
   return cudaGetLastError();
 }
 
-cudaError_t launch_bf16_to_f16(const void* src, void* dst, size_t n, cudaStream_t s) {
+cudaError_t launch_bf16_to_f16(const void* src, void* dst, size_t rows, int K, bool gate_up, int I,
+                               cudaStream_t s) {
+  const size_t n = rows * (size_t)K;
   size_t g = (n + 255) / 256;
   if (g > 148 * 16) g = 148 * 16;
-  bf16_to_f16_kernel<<<(int)(g ? g : 1), 256, 0, s>>>(static_cast<const uint16_t*>(src), static_cast<__half*>(dst), n);
+  bf16_to_f16_kernel<<<(int)(g ? g : 1), 256, 0, s>>>(static_cast<const uint16_t*>(src), static_cast<__half*>(dst),
+                                                      rows, K, gate_up ? 1 : 0, I);
   return cudaGetLastError();
 }
 

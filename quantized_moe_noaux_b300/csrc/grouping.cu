@@ -60,16 +60,27 @@ group_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ counts
     }
   }
 
-  // CTA 0 also writes the work list (serial over experts; at most E + T*k/kTokChunk items)
-  if (e == 0 && threadIdx.x == 0) {
-    int nitems = 0;
-    for (int x = 0; x < E; ++x) {
-      const int c = counts[x];
-      for (int ch = 0; ch * kTokChunk < c; ++ch) items[nitems++] = pack_item(x, ch);
+  // CTA 0's first warp also writes the work list (at most E + T*k/kTokChunk items, plus
+  // the inline shared expert's chunks): each lane owns a contiguous run of experts, a warp
+  // scan gives every lane its first slot
+  if (items && e == 0 && warp == 0) {
+    const int per = (E + 31) / 32;
+    const int x0 = min(E, lane * per), x1 = min(E, x0 + per);
+    int mine = 0;
+    for (int x = x0; x < x1; ++x) mine += (counts[x] + kTokChunk - 1) / kTokChunk;
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
     }
-    if (shared_inline)
-      for (int ch = 0; ch * kTokChunk < T; ++ch) items[nitems++] = pack_item(E, ch);
-    meta[0] = nitems;
+    int pos = incl - mine;
+    for (int x = x0; x < x1; ++x)
+      for (int ch = 0; ch * kTokChunk < counts[x]; ++ch) items[pos++] = pack_item(x, ch);
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    const int nsh = shared_inline ? (T + kTokChunk - 1) / kTokChunk : 0;
+    for (int ch = lane; ch < nsh; ch += 32) items[total + ch] = pack_item(E, ch);
+    if (lane == 0) meta[0] = total + nsh;
   }
 }
 

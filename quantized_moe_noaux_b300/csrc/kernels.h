@@ -98,8 +98,9 @@ struct alignas(64) TensorMapBytes {
   unsigned char b[128];
 };
 struct GemmMaps {
-  TensorMapBytes codes;    // fp16 weights [rows, K], 64 x 16 box, 128-byte swizzle (kWF16 only)
-  TensorMapBytes act;      // expert-sorted fp16 activations [rows, K], 64 x 16 box, 128-byte swizzle
+  TensorMapBytes codes;    // fp16 weights [rows, K], 64 x 128 box, 128-byte swizzle (kWF16 only)
+  TensorMapBytes act[4];   // expert-sorted fp16 activations [rows, K], 64 x {32,64,128,256} boxes,
+                           // 128-byte swizzle
 };
 // Weight storage of the grouped GEMM besides MOE_W_INT4_G32 / MOE_W_NVFP4: plain fp16
 // rows (a bf16 shared expert converted once at layer creation).
@@ -124,6 +125,8 @@ struct GemmParams {
   const float* w_tscale;      // NVFP4 per-expert tensor scales of this matrix, or NULL
   const unsigned int* act_amax;   // NVFP4: amax bits of the B activations, or NULL
   int* status;
+  unsigned long long* trace;  // optional per-CTA profiling trace (64 slots per CTA), or NULL
+  int trace_base;             // first slot of this launch's 11
 };
 bool make_tmap_2d(TensorMapBytes* out, const void* base, int elem_bytes, uint64_t inner, uint64_t rows,
                   uint32_t box_inner, uint32_t box_rows, bool swizzle128);
@@ -132,7 +135,8 @@ int gemm_max_items(int T, int top_k, int E, bool routed, bool shared);
 cudaError_t gemm_kernels_init();
 cudaError_t launch_gemm_items(const int32_t* offsets, int E, int T, int top_k, int4* items, int32_t* n_items,
                               cudaStream_t s);
-cudaError_t launch_bf16_to_f16(const void* src, void* dst, size_t n, cudaStream_t s);
+cudaError_t launch_bf16_to_f16(const void* src, void* dst, size_t rows, int K, bool gate_up, int I,
+                               cudaStream_t s);
 cudaError_t launch_gather_act(const void* x, int act_dtype, bool nvfp4, int H, const int32_t* entries, int Tk,
                               int top_k, int rows, __half* dst, const unsigned int* amax_bits, cudaStream_t s);
 cudaError_t launch_quant_h(const float* h, size_t n, const unsigned int* amax_bits, __half* dst, cudaStream_t s);

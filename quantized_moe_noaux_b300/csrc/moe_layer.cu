@@ -280,20 +280,21 @@ moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt,
     if (launch_gemm_pack(L->w.gu_codes, L->w.gu_scales, H, n_store, 2 * I, I, true, L->gpack_up, s) ||
         launch_gemm_pack(L->w.d_codes, L->w.d_scales, I, n_store, H, I, false, L->gpack_down, s))
       return MOE_ERR_CUDA;
-    L->gemm_ok = make_tmap_2d(&L->maps_up.act, L->x16s, 2, H, L->gemm_rows, 64, 16, true) &&
-                 make_tmap_2d(&L->maps_down.act, L->h16s, 2, I, L->gemm_rows, 64, 16, true);
-    L->maps_up.codes = L->maps_up.act;       // unused by the packed-weight kernels
-    L->maps_down.codes = L->maps_down.act;
+    for (int b = 0; b < 4 && L->gemm_ok; ++b)
+      L->gemm_ok = make_tmap_2d(&L->maps_up.act[b], L->x16s, 2, H, L->gemm_rows, 64, 32u << b, true) &&
+                   make_tmap_2d(&L->maps_down.act[b], L->h16s, 2, I, L->gemm_rows, 64, 32u << b, true);
+    L->maps_up.codes = L->maps_up.act[0];       // unused by the packed-weight kernels
+    L->maps_down.codes = L->maps_down.act[0];
     if (L->gemm_ok && !L->shared_inline) {
       if ((st = dev_alloc(L, &L->sh16_gu, (size_t)2 * I * H * 2)) || (st = dev_alloc(L, &L->sh16_d, (size_t)H * I * 2)))
         return st;
-      if (launch_bf16_to_f16(L->ws.gu_codes, L->sh16_gu, (size_t)2 * I * H, s) ||
-          launch_bf16_to_f16(L->ws.d_codes, L->sh16_d, (size_t)H * I, s))
+      if (launch_bf16_to_f16(L->ws.gu_codes, L->sh16_gu, (size_t)2 * I, H, true, I, s) ||
+          launch_bf16_to_f16(L->ws.d_codes, L->sh16_d, (size_t)H, I, false, I, s))
         return MOE_ERR_CUDA;
       L->maps_sh_up = L->maps_up;
       L->maps_sh_down = L->maps_down;
-      L->gemm_ok = make_tmap_2d(&L->maps_sh_up.codes, L->sh16_gu, 2, H, 2 * I, 64, 16, true) &&
-                   make_tmap_2d(&L->maps_sh_down.codes, L->sh16_d, 2, I, H, 64, 16, true);
+      L->gemm_ok = make_tmap_2d(&L->maps_sh_up.codes, L->sh16_gu, 2, H, 2 * I, 64, 128, true) &&
+                   make_tmap_2d(&L->maps_sh_down.codes, L->sh16_d, 2, I, H, 64, 128, true);
     }
   }
   if (cudaMemsetAsync(L->status, 0, sizeof(int), s) || cudaMemsetAsync(L->meta, 0, 16 * 4, s))
@@ -360,12 +361,15 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
   p.entries = L->entries;
   p.weights = L->weights;
   p.status = L->status;
+  p.trace = L->trace;
+  p.trace_base = 16;
   GemmParams ps = p;   // separately stored fp16 shared expert
   ps.n_items = L->g_nitems + 1;
   ps.item_skip = L->g_nitems;
   ps.e_sub = E;
   ps.w_tscale = nullptr;
   ps.act_amax = nullptr;
+  ps.trace_base = 48;
 
   p.K = ps.K = H;
   p.rows_per_expert = ps.rows_per_expert = 2 * I;
@@ -379,6 +383,8 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
   if (nvfp4) MOE_LAUNCH(launch_quant_h(L->h32, (size_t)Tk * I, L->amax + 1, L->h16s, s));
   MOE_CK(m.mark(4));
   p.K = ps.K = I;
+  p.trace_base = 32;
+  ps.trace = nullptr;   // the shared expert's down launch is not traced
   p.rows_per_expert = ps.rows_per_expert = H;
   p.mtiles = ps.mtiles = H / 128;
   p.wpack = L->gpack_down;
@@ -425,7 +431,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
   MOE_LAUNCH(launch_select(L->logits, L->bias, T, E, c.n_group, c.topk_group, k, c.routed_scaling_factor,
                            L->ids, L->weights, L->counts, L->status, s));
   MOE_LAUNCH(launch_group(L->ids, L->counts, T, k, E, L->shared_inline, L->offsets, L->entries,
-                          L->items, L->meta, s));
+                          gemm ? nullptr : L->items, L->meta, s));
   MOE_CK(m.mark(1));
   if (gemm) return forward_gemm(L, x, T, out, s, m);
   const void* x_in = x;

@@ -6,8 +6,9 @@
 
 Each iteration is one ``moe_layer_forward`` on fresh seeded activations. ``--copies`` layer
 copies are used in turn so consecutive forwards read different weights (as in the
-benchmark). ``--trace`` records the fused decode kernel's per-CTA phase timestamps of the
-last iteration (``moe_layer_set_trace``) and saves them as a numpy array [CTAs, 16] in ns.
+benchmark). ``--trace`` records the last iteration's per-CTA trace (``moe_layer_set_trace``: the decode
+kernel's phase timestamps in ns, the grouped GEMMs' per-role wait cycles) and saves it as a
+numpy array [CTAs, 64].
 No comparison against a reference is made here: the tests do that.
 """
 
@@ -23,6 +24,10 @@ PHASES = ["start", "activation panel", "router rows", "routing published", "shar
           "shared gate/up seen", "shared down", "routing seen", "routed gate/up",
           "first routed gate/up seen", "routed down", "all down seen", "output written",
           "producer: shared issued", "producer: routing seen"]
+
+GEMM_SLOTS = ["kernel", "mma_wait_operands", "mma_wait_accumulator", "dq_wait_weights",
+              "dq_wait_stage", "act_producer_wait", "w_producer_wait", "epi_wait", "epi_busy",
+              "tiles", "dq_loop"]
 
 _PATHS = {"auto": 0, "gemv": 1, "grouped": 2, "generic": 3}
 
@@ -61,7 +66,7 @@ def main(argv=None):
     xs = [dev(make_x(spec, T, s)) for s in range(args.iters)]
     out = torch.empty((T, spec.hidden), dtype=dt, device="cuda")
     nsm = torch.cuda.get_device_properties(0).multi_processor_count
-    buf = torch.zeros((nsm, 16), dtype=torch.int64, device="cuda") if args.trace else None
+    buf = torch.zeros((nsm, 64), dtype=torch.int64, device="cuda") if args.trace else None
     for s in range(args.iters):
         L = layers[s % len(layers)]
         if buf is not None and s == args.iters - 1:
@@ -81,6 +86,23 @@ def main(argv=None):
             if v.size:
                 print(f"{i:2d} {name:26s} CTAs={v.size:3d}  min {v.min() / 1e3:8.2f}  "
                       f"median {np.median(v) / 1e3:8.2f}  max {v.max() / 1e3:8.2f} us")
+        if (t[:, 0] > 0).any() and (t[:, 20] > 0).any():
+            blk = t[:, 16:23].astype(np.float64)
+            med = np.median(blk, axis=0)
+            names = ["consumer_wait_data", "consumer_compute", "consumer_epilogue", "consumer_transition",
+                     "items", "producer_wait_slot", "items_issued"]
+            print("decode kernel, median per CTA (cycles): " +
+                  ", ".join(f"{n}={v:.0f}" for n, v in zip(names, med)))
+            t = t.copy()
+            t[:, 16:23] = 0
+        for base, label in ((16, "gate/up GEMM"), (32, "down GEMM"), (48, "shared gate/up GEMM")):
+            blk = t[:, base:base + 11].astype(np.float64)
+            used = blk[:, 0] > 0
+            if not used.any():
+                continue
+            med = np.median(blk[used], axis=0)
+            print(f"{label}: CTAs={int(used.sum())} median cycles: " +
+                  ", ".join(f"{n}={v:.0f}" for n, v in zip(GEMM_SLOTS, med)))
     print(f"ok: {args.iters} forwards of {spec.name} at T={T} (path {args.path})")
 
 

@@ -74,7 +74,12 @@ def test_grouped_matches_generic_path():
     c = out_to_host(run(layer, spec, x, moe.PATH_GROUPED))
     layer.set_path(moe.PATH_AUTO)
     assert np.linalg.norm(a - b) / np.linalg.norm(b) < 2e-3
-    assert np.linalg.norm(a - c) / np.linalg.norm(a) < 1e-6   # only atomic order differs
+    # a repeat differs only in the order of the fp32 atomic adds of the combine: the fp32
+    # sums differ by a few ulps of the summed terms, which can flip the bf16 rounding of an
+    # output by one step (at most 2^-7 of its magnitude); near a cancellation the fp32
+    # difference itself is bounded by a tiny fraction of the output's scale
+    bound = 2.0 ** -7 * np.maximum(np.abs(a), np.abs(c)) + 1e-5 * np.abs(a).max()
+    assert np.all(np.abs(a - c) <= bound)
 
 
 @pytest.mark.parametrize("T,step", [(9, 0), (64, 1), (300, 2)])
