@@ -53,11 +53,27 @@ nvfp4_quant_kernel(const void* __restrict__ src, float* __restrict__ dst, size_t
   }
 }
 
+// out = acc in the output type, 8 elements per thread step (n is a multiple of 8: H is).
 template <int DT>
 __global__ void __launch_bounds__(kThreads)
 finalize_kernel(const float* __restrict__ acc, void* __restrict__ out, size_t n) {
-  for (size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += (size_t)gridDim.x * kThreads)
-    store_act<DT>(out, i, acc[i]);
+  for (size_t i = ((size_t)blockIdx.x * kThreads + threadIdx.x) * 8; i < n; i += (size_t)gridDim.x * kThreads * 8) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(acc + i));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(acc + i) + 1);
+    if constexpr (DT == MOE_DT_F32) {
+      reinterpret_cast<float4*>(static_cast<float*>(out) + i)[0] = a;
+      reinterpret_cast<float4*>(static_cast<float*>(out) + i)[1] = b;
+    } else {
+      const __nv_bfloat162 p0 = __floats2bfloat162_rn(a.x, a.y), p1 = __floats2bfloat162_rn(a.z, a.w);
+      const __nv_bfloat162 p2 = __floats2bfloat162_rn(b.x, b.y), p3 = __floats2bfloat162_rn(b.z, b.w);
+      uint4 o;
+      o.x = *reinterpret_cast<const uint32_t*>(&p0);
+      o.y = *reinterpret_cast<const uint32_t*>(&p1);
+      o.z = *reinterpret_cast<const uint32_t*>(&p2);
+      o.w = *reinterpret_cast<const uint32_t*>(&p3);
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + i) = o;
+    }
+  }
 }
 
 int grid_for(size_t n) {
@@ -89,9 +105,9 @@ cudaError_t launch_nvfp4_quant(const void* src, int src_dtype, float* dst, size_
 cudaError_t launch_finalize(const float* out_acc, void* out, int act_dtype, size_t n,
                             cudaStream_t s) {
   if (act_dtype == MOE_DT_F32)
-    finalize_kernel<MOE_DT_F32><<<grid_for(n), kThreads, 0, s>>>(out_acc, out, n);
+    finalize_kernel<MOE_DT_F32><<<grid_for(n / 8), kThreads, 0, s>>>(out_acc, out, n);
   else
-    finalize_kernel<MOE_DT_BF16><<<grid_for(n), kThreads, 0, s>>>(out_acc, out, n);
+    finalize_kernel<MOE_DT_BF16><<<grid_for(n / 8), kThreads, 0, s>>>(out_acc, out, n);
   return cudaGetLastError();
 }
 

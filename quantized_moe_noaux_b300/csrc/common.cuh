@@ -55,6 +55,25 @@ __device__ __forceinline__ float load_act(const void* base, size_t i) {
   }
 }
 
+// 8 consecutive activation elements from element index i (a multiple of 8): one 16-byte load
+// for bf16, two for fp32.
+template <int DT>
+__device__ __forceinline__ void load8_act(const void* base, size_t i, float (&v)[8]) {
+  if constexpr (DT == MOE_DT_F32) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + i));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + i) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(base) + i));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v[2 * q] = __uint_as_float(w[q] << 16);
+      v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+    }
+  }
+}
+
 template <int DT>
 __device__ __forceinline__ void store_act(void* base, size_t i, float v) {
   if constexpr (DT == MOE_DT_F32) {

@@ -28,9 +28,11 @@
 //   C1 shared-expert down tiles              (waits until every shared gate/up tile is done)
 //   B  selected experts' gate/up tiles       (waits for the routing, in shared memory)
 //   C2 selected experts' down tiles          (waits until that expert's gate/up tiles are done)
-// The producer warp issues the shared-expert items, then waits until every CTA has written
-// its router rows and computes the selection and grouping itself (every CTA obtains the same
-// routing from the same logits; CTA 0 also writes it out), then issues the routed items.
+// After its router rows each CTA waits until every CTA has written its rows, then its
+// consumer warps select the tokens (warp t takes token t) and group the entries: every CTA
+// obtains the same routing from the same logits (CTA 0 also writes it out). The producer
+// warp issues the shared-expert items meanwhile and the routed items once the routing is
+// known.
 // Down tiles add w * y into an fp32 accumulator with atomics; after a grid-wide count every
 // CTA converts its slice to the output type. All inter-CTA waits are bounded; on time-out
 // the kernel records MOE_ERR_TIMEOUT, drains its own copies in flight and returns.
@@ -60,7 +62,7 @@ constexpr uint32_t kMbarSpin = 1u << 22;
 // Shared memory common to both modes (16-byte aligned: the reduction buffer takes float4
 // stores).
 struct alignas(16) DecCommon {
-  float red[2][8][32][4];              // cross-warp reduction (double-buffered per tile)
+  float red[2][8][32][8];              // cross-warp reduction (double-buffered per unit)
   float selb[kMaxE];                   // selection scratch (producer warp)
   float sels[kMaxE];
   int idsel[8][kMaxK];                 // per token: selected experts and weights
@@ -373,8 +375,9 @@ __device__ __forceinline__ void compute_item0(const uint2* panel, const float* s
 }
 
 // Cross-warp reduction of the tile accumulators into red (consumers, then named barrier).
+// `half` selects the second 16-row tile of a down pair.
 template <int MODE>
-__device__ __forceinline__ void stash_acc(DecCommon& C, int rb, float (&acc)[4]) {
+__device__ __forceinline__ void stash_acc(DecCommon& C, int rb, int half, float (&acc)[4]) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   if (MODE == 1) {
 #pragma unroll
@@ -383,24 +386,24 @@ __device__ __forceinline__ void stash_acc(DecCommon& C, int rb, float (&acc)[4])
       acc[1] += __shfl_xor_sync(0xffffffffu, acc[1], o);
     }
     if ((lane & 3) == 0) {
-      C.red[rb][w][lane >> 2][0] = acc[0];
-      C.red[rb][w][lane >> 2][1] = acc[1];
+      C.red[rb][w][lane >> 2][2 * half] = acc[0];
+      C.red[rb][w][lane >> 2][2 * half + 1] = acc[1];
     }
   } else {
-    *reinterpret_cast<float4*>(&C.red[rb][w][lane][0]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(&C.red[rb][w][lane][4 * half]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
   }
 }
 
 // Value of MMA row r (0..15) for column n after the reduction (rows 8..15 carry a x16 unit).
 template <int MODE>
-__device__ __forceinline__ float reduced(const DecCommon& C, int rb, int r, int n) {
+__device__ __forceinline__ float reduced(const DecCommon& C, int rb, int half, int r, int n) {
   float v = 0.f;
   if (MODE == 1) {
 #pragma unroll
-    for (int w = 0; w < 8; ++w) v += C.red[rb][w][r & 7][r >> 3];
+    for (int w = 0; w < 8; ++w) v += C.red[rb][w][r & 7][2 * half + (r >> 3)];
   } else {
     const int ln = (r & 7) * 4 + (n >> 1);
-    const int idx = (r >> 3) * 2 + (n & 1);
+    const int idx = 4 * half + (r >> 3) * 2 + (n & 1);
 #pragma unroll
     for (int w = 0; w < 8; ++w) v += C.red[rb][w][ln][idx];
   }
@@ -535,29 +538,14 @@ __device__ __forceinline__ unsigned long long global_ns() {
     if (a.trace) a.trace[(size_t)blockIdx.x * 64 + (i)] = global_ns();          \
   } while (0)
 
-// Producer warp (all lanes): wait for every CTA's router rows, select every token, group
-// the entries per expert and publish the routing in shared memory (CTA 0 also to global).
+// One consumer warp: group the selected (token, slot) entries per expert and publish the
+// routing in shared memory (CTA 0 also to global): counts, exclusive scans (entry
+// offsets, active slots), the ascending entry lists and each active expert's columns.
 template <int MODE>
-__device__ void route_in_cta(DecSmem<MODE>& S, const DecodeArgs& a, const Geo& g) {
+__device__ void group_in_cta(DecSmem<MODE>& S, const DecodeArgs& a, const Geo& g) {
   DecCommon& C = S.c;
   const int lane = threadIdx.x & 31;
   const int T = g.T, E = g.E, k = g.k;
-  bool ok = true;
-  if (lane == 0) ok = wait_geq(a.sync + 0, (uint32_t)g.G, a.spin_max);
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (!ok) {
-    if (lane == 0) {
-      atomicExch(&C.abort, 1);
-      raise_status(a.status, MOE_ERR_TIMEOUT);
-      C.n_active = 0;
-    }
-    __syncwarp();
-    return;
-  }
-  __threadfence();
-  for (int t = 0; t < T; ++t)
-    select_one(a.logits + (size_t)t * E, a.bias, E, a.n_group, a.topk_group, k, a.rsf, C.selb, C.sels, C.idsel[t],
-               C.wsel[t], a.status);
   // grouping: counts, exclusive scans (entry offsets, active slots), entry lists
   const int n = T * k;
   for (int e = lane; e < E; e += 32) C.cnt[e] = 0;
@@ -660,7 +648,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
 
   int a0, a1, c10, c11;
   seg_range(g.NTu, g.G, g.c, a0, a1);    // shared gate/up tiles
-  seg_range(g.NTd, g.G, g.c, c10, c11);  // shared down tiles
+  seg_range(g.NTd / 2, g.G, g.c, c10, c11);  // shared down tile pairs
+  c10 *= 2;
+  c11 *= 2;
 
   if (warp == 8) {
     // ------------------------------------------------------------- producer warp
@@ -673,7 +663,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       if (!ok) return;
       const int slot = it % kSlots;
       const unsigned long long t0 = clock64();
-      if (it >= kSlots && !ptx::mbar_wait(&S.empty[slot], ((it / kSlots) - 1) & 1, kMbarSpin)) ok = false;
+      if (it >= kSlots && !ptx::mbar_wait_backoff(&S.empty[slot], ((it / kSlots) - 1) & 1, kMbarSpin, 4, 128))
+        ok = false;
       p_wait += clock64() - t0;
       if (ok && *(volatile int*)&C.abort) ok = false;
       if (!ok) return;
@@ -691,15 +682,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
           issue(a.down_store + ((size_t)shared_e * g.NTd + tl) * dn_tile_bytes + (size_t)p * kItemBytes);
       DEC_TRACE(13);
     }
-    __syncwarp();
-    route_in_cta<MODE>(S, a, g);
     if (lane == 0) {
+      // the consumers publish the routing (selection and grouping) through route_bar
+      if (!ptx::mbar_wait_backoff(&S.route_bar, 0, kMbarSpin * 16, 4, 256)) {
+        ok = false;
+        atomicExch(&C.abort, 1);
+        raise_status(a.status, MOE_ERR_TIMEOUT);
+      }
       DEC_TRACE(14);
-      ptx::mbar_arrive(&S.route_bar);
-      const int na = C.n_active;
+      const int na = ok ? C.n_active : 0;
       int b0, b1, c20, c21;
       seg_range(na * g.NTu, g.G, g.c, b0, b1);
-      seg_range(na * g.NTd, g.G, g.c, c20, c21);
+      seg_range(na * (g.NTd / 2), g.G, g.c, c20, c21);   // down tile pairs
+      c20 *= 2;
+      c21 *= 2;
       for (int r = b0; r < b1; ++r) {
         const int e = C.active[r / g.NTu], tl = r % g.NTu;
         for (int p = 0; p < g.Pu; ++p)
@@ -731,25 +727,33 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     ptx::bar_sync(1, kConsumers);
     if (tid == 0) DEC_TRACE(1);
 
-    // router rows e = c, c + G, ...: each thread takes 4 consecutive columns per 1024 (all
-    // loads of a row issued together); fp32 FMA, then warp and CTA reductions
-    for (int e = g.c; e < E; e += g.G) {
-      float racc[8];
+    // router rows e = c, c + G, ... two at a time: each thread takes 4 consecutive columns
+    // per 1024 of both rows, all loads issued together; fp32 FMA, then warp and CTA
+    // reductions
+    for (int e0 = g.c; e0 < E; e0 += 2 * g.G) {
+      const int e1 = e0 + g.G;
+      const bool two = e1 < E;
+      float racc[2][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) racc[i] = 0.f;
-      float4 wv[kMaxH / 1024];
+      for (int i = 0; i < 8; ++i) racc[0][i] = racc[1][i] = 0.f;
+      float4 wv[2][kMaxH / 1024];
 #pragma unroll
-      for (int q = 0; q < kMaxH / 1024; ++q) {
-        const int col = 1024 * q + 4 * tid;
-        wv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (col < H) {
-          if constexpr (WDT == MOE_DT_F32) {
-            wv[q] = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(a.router_w) + (size_t)e * H + col));
-          } else {
-            const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(a.router_w) +
-                                                                 (size_t)e * H + col));
-            wv[q] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
-                                __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+      for (int rr = 0; rr < 2; ++rr) {
+        const int e = rr ? e1 : e0;
+#pragma unroll
+        for (int q = 0; q < kMaxH / 1024; ++q) {
+          const int col = 1024 * q + 4 * tid;
+          wv[rr][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (col < H && (rr == 0 || two)) {
+            if constexpr (WDT == MOE_DT_F32) {
+              wv[rr][q] =
+                  __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(a.router_w) + (size_t)e * H + col));
+            } else {
+              const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(a.router_w) +
+                                                                   (size_t)e * H + col));
+              wv[rr][q] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                                      __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+            }
           }
         }
       }
@@ -773,35 +777,71 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
                 xv[2] = __uint_as_float(u.y << 16);
                 xv[3] = __uint_as_float(u.y & 0xFFFF0000u);
               }
-              racc[i] = fmaf(wv[q].x, xv[0], racc[i]);
-              racc[i] = fmaf(wv[q].y, xv[1], racc[i]);
-              racc[i] = fmaf(wv[q].z, xv[2], racc[i]);
-              racc[i] = fmaf(wv[q].w, xv[3], racc[i]);
+#pragma unroll
+              for (int rr = 0; rr < 2; ++rr) {
+                racc[rr][i] = fmaf(wv[rr][q].x, xv[0], racc[rr][i]);
+                racc[rr][i] = fmaf(wv[rr][q].y, xv[1], racc[rr][i]);
+                racc[rr][i] = fmaf(wv[rr][q].z, xv[2], racc[rr][i]);
+                racc[rr][i] = fmaf(wv[rr][q].w, xv[3], racc[rr][i]);
+              }
             }
           }
         }
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float v = racc[i];
+      for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) C.red[0][warp][i][0] = v;
-      }
+        for (int i = 0; i < 8; ++i) {
+          float v = racc[rr][i];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0) C.red[0][warp][i][rr] = v;
+        }
       ptx::bar_sync(1, kConsumers);
-      if (tid < T) {
-        float v = 0.f;
+      if (tid < 2 * T) {
+        const int rr = tid / T, i = tid % T;
+        if (rr == 0 || two) {
+          float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) v += C.red[0][w][tid][0];
-        a.logits[(size_t)tid * E + e] = v;
+          for (int w = 0; w < 8; ++w) v += C.red[0][w][i][rr];
+          a.logits[(size_t)i * E + (rr ? e1 : e0)] = v;
+        }
       }
       ptx::bar_sync(1, kConsumers);
     }
+    // every CTA's router rows are needed: then warp t selects token t, warp 0 groups the
+    // entries, and the routing goes to the producer warp
     if (tid == 0) {
       __threadfence();
       ptx::red_release_add(a.sync + 0, 1u);
       DEC_TRACE(2);
+      C.flag = wait_geq(a.sync + 0, (uint32_t)g.G, a.spin_max) ? 1 : 0;
+      if (!C.flag) {
+        atomicExch(&C.abort, 1);
+        raise_status(a.status, MOE_ERR_TIMEOUT);
+        C.n_active = 0;
+      }
     }
+    ptx::bar_sync(1, kConsumers);
+    if (C.flag) {
+      __threadfence();
+      if (warp < T) {
+        float *sb, *ss;
+        if constexpr (MODE == 1) {
+          sb = C.selb;
+          ss = C.sels;
+        } else {
+          sb = reinterpret_cast<float*>(S.hpanel) + warp * 2 * kMaxE;   // h panel is free here
+          ss = sb + kMaxE;
+        }
+        select_one(a.logits + (size_t)warp * E, a.bias, E, a.n_group, a.topk_group, g.k, a.rsf, sb, ss,
+                   C.idsel[warp], C.wsel[warp], a.status);
+      }
+      ptx::bar_sync(1, kConsumers);
+      if (warp == 0) group_in_cta<MODE>(S, a, g);
+    }
+    ptx::bar_sync(1, kConsumers);
+    if (tid == 0) ptx::mbar_arrive(&S.route_bar);
 
     float acc[4];
     // profiling counters (cycles, consumer thread 0): waiting for item data, computing items,
@@ -815,7 +855,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       const int s = it % kSlots;
       slot = S.slots[s];
       if (*(volatile int*)&C.abort) return false;
-      if (!ptx::mbar_wait(&S.full[s], (it / kSlots) & 1, kMbarSpin)) {
+      if (!ptx::mbar_wait_backoff(&S.full[s], (it / kSlots) & 1, kMbarSpin, 16, 32)) {
         atomicExch(&C.abort, 1);
         raise_status(a.status, MOE_ERR_TIMEOUT);
         return false;
@@ -873,23 +913,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
 #pragma unroll 1
     for (int ph = 0; ph < 4; ++ph) {
       if (ph == 1) {
-        lo = c10;
-        hi = c11;
+        lo = c10 / 2;   // down units are pairs of 16-row tiles
+        hi = c11 / 2;
       } else if (ph == 2) {
         if (tid == 0) DEC_TRACE(6);
-        // routing known (the producer warp computed it)
-        if (!ptx::mbar_wait(&S.route_bar, 0, kMbarSpin * 16) && tid == 0) {
-          atomicExch(&C.abort, 1);
-          raise_status(a.status, MOE_ERR_TIMEOUT);
-        }
         ptx::bar_sync(1, kConsumers);
         if (tid == 0) DEC_TRACE(7);
         seg_range(C.n_active * g.NTu, g.G, g.c, lo, hi);
       } else if (ph == 3) {
-        seg_range(C.n_active * g.NTd, g.G, g.c, lo, hi);
+        seg_range(C.n_active * (g.NTd / 2), g.G, g.c, lo, hi);
       }
       const int up = (ph & 1) == 0;
-      const int ntl = up ? g.NTu : g.NTd;
+      const int ntl = up ? g.NTu : g.NTd / 2;
 #pragma unroll 1
       for (int u = lo; u < hi; ++u) {
         const int sl = ph < 2 ? -1 : u / ntl;
@@ -927,11 +962,24 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
           cur_up = up;
         }
         c_tr += clock64() - tt0;
+        unsigned long long te0;
+        if (up) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i] = 0.f;
-        run_items(up ? g.Pu : g.Pd, up != 0);
-        const unsigned long long te0 = clock64();
-        stash_acc<MODE>(C, rb, acc);
+          for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+          run_items(g.Pu, true);
+          te0 = clock64();
+          stash_acc<MODE>(C, rb, 0, acc);
+        } else {
+          // a pair of 16-row down tiles per unit: one barrier for both
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+            run_items(g.Pd, false);
+            stash_acc<MODE>(C, rb, half, acc);
+          }
+          te0 = clock64();
+        }
         ptx::bar_sync(1, kConsumers);
         if (up) {
           const int nt = (MODE == 1) ? 8 : 64;
@@ -939,18 +987,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
             const int r = (MODE == 1) ? tid : (tid >> 3), n = (MODE == 1) ? 0 : (tid & 7);
             const int pr = C.colpair[n];
             if (pr >= 0) {
-              const float gate = reduced<MODE>(C, rb, r, n), upv = reduced<MODE>(C, rb, r + 8, n);
+              const float gate = reduced<MODE>(C, rb, 0, r, n), upv = reduced<MODE>(C, rb, 0, r + 8, n);
               a.h16[(size_t)pr * g.I + tl * 8 + r] = __float2half_rn(siluf_acc(gate) * upv);
             }
           }
           ++up_n;
         } else {
-          const int nt = (MODE == 1) ? 16 : 128;
+          const int nt = (MODE == 1) ? 32 : 256;
           if (tid < nt) {
-            const int r = (MODE == 1) ? tid : (tid >> 3), n = (MODE == 1) ? 0 : (tid & 7);
+            const int half = (MODE == 1) ? (tid >> 4) : (tid >> 7);
+            const int r = (MODE == 1) ? (tid & 15) : ((tid & 127) >> 3), n = (MODE == 1) ? 0 : (tid & 7);
             const float wn = C.colw[n];
             if (n < T && wn != 0.f)
-              atomicAdd(a.out_acc + (size_t)n * H + tl * 16 + r, wn * reduced<MODE>(C, rb, r, n));
+              atomicAdd(a.out_acc + (size_t)n * H + (2 * tl + half) * 16 + r, wn * reduced<MODE>(C, rb, half, r, n));
           }
         }
         rb ^= 1;
@@ -959,20 +1008,27 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       if (up) flush_up();
       if (tid == 0) DEC_TRACE(ph == 0 ? 4 : ph == 2 ? 8 : 10);
     }
-    // ---- every CTA's down tiles are in out_acc: convert this CTA's slice of the output
+    // ---- the last CTA to finish its down tiles converts the whole output (every other CTA's
+    // atomics are ordered before its ticket by the barrier and fence below)
     ptx::bar_sync(1, kConsumers);
     if (tid == 0) {
-      ptx::red_release_add(a.sync + 4, 1u);
-      if (!wait_geq(a.sync + 4, (uint32_t)g.G, a.spin_max)) raise_status(a.status, MOE_ERR_TIMEOUT);
+      __threadfence();
+      const uint32_t ticket = atomicAdd(a.sync + 4, 1u);
+      C.flag = ticket == (uint32_t)g.G - 1;
       DEC_TRACE(11);
     }
     ptx::bar_sync(1, kConsumers);
-    {
-      const size_t n = (size_t)T * H;
-      const size_t lo = n * g.c / g.G, hi = n * (g.c + 1) / g.G;
-      for (size_t i = lo + tid; i < hi; i += kConsumers) {
-        store_act<XDT>(a.out, i, __ldcg(a.out_acc + i));
-        a.out_acc[i] = 0.f;
+    if (C.flag) {
+      __threadfence();
+      const int n4 = T * H / 4;
+#pragma unroll 4
+      for (int i = tid; i < n4; i += kConsumers) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.out_acc) + i);
+        reinterpret_cast<float4*>(a.out_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        store_act<XDT>(a.out, 4 * (size_t)i, v.x);
+        store_act<XDT>(a.out, 4 * (size_t)i + 1, v.y);
+        store_act<XDT>(a.out, 4 * (size_t)i + 2, v.z);
+        store_act<XDT>(a.out, 4 * (size_t)i + 3, v.w);
       }
     }
     if (tid == 0) {

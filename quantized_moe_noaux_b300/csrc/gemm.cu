@@ -12,15 +12,15 @@
 //
 // Persistent CTAs (one per SM) walk the tiles (item, 128-row block) in a static round-robin
 // order; warp roles:
-//   warp 14    bulk copy of the packed weights: 128 rows x 256 columns of codes and their
+//   warp 18    bulk copy of the packed weights: 128 rows x 256 columns of codes and their
 //              scales per copy (18 KB, laid out at layer creation for conflict-free reads)
-//   warps 4-11 dequantise 64 columns per K stage into an fp16 tile in the 128-byte swizzle
+//   warps 4-15 dequantise 64 columns per K stage into an fp16 tile in the 128-byte swizzle
 //              layout the MMA reads (int4 * fp16 scale rounded once to fp16; E2M1 * E4M3 is
-//              exact in fp16, the fp32 tensor scales are applied in the epilogue); two groups
-//              of 4 warps take alternate stages, a thread converts one row of its stage
-//   warp 12    TMA: the N x 64 fp16 activation tile of the same K stage (one box of 32, 64,
+//              exact in fp16, the fp32 tensor scales are applied in the epilogue); three
+//              groups of 4 warps, one per ring slot, a thread converts one row of its stage
+//   warp 16    TMA: the N x 64 fp16 activation tile of the same K stage (one box of 32, 64,
 //              128 or 256 rows)
-//   warp 13    issues tcgen05.mma kind::f16 (M=128, N, K=16) x 4 per stage into one of two
+//   warp 17    issues tcgen05.mma kind::f16 (M=128, N, K=16) x 4 per stage into one of two
 //              TMEM accumulators (256 columns each) and releases stages with tcgen05.commit
 //   warps 0-3  epilogue of the previous tile while the next one runs: tcgen05.ld, then
 //     gate/up: M rows pair 16 gate with 16 up rows per warp; h = SiLU(gate) * up is
@@ -43,12 +43,13 @@ namespace moe {
 namespace {
 
 constexpr int kEpiWarps = 4;      // warps 0-3
-constexpr int kDqWarp0 = 4;       // warps 4-11
-constexpr int kDqWarps = 8;
-constexpr int kWarpB = 12;
-constexpr int kWarpMma = 13;
-constexpr int kWarpW = 14;
-constexpr int kGThreads = 15 * 32;
+constexpr int kDqWarp0 = 4;       // warps 4-15: three groups of 4, one per A/B ring slot
+constexpr int kDqGroups = 3;
+constexpr int kDqWarps = 4 * kDqGroups;
+constexpr int kWarpB = kDqWarp0 + kDqWarps;
+constexpr int kWarpMma = kWarpB + 1;
+constexpr int kWarpW = kWarpB + 2;
+constexpr int kGThreads = (kWarpW + 1) * 32;
 constexpr int kBM = 128;          // weight rows per tile (MMA M)
 constexpr int kBN = 256;          // max tokens per tile (MMA N)
 constexpr int kBK = 64;           // K per stage: one 128-byte swizzle atom of fp16
@@ -175,7 +176,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
     for (int s = 0; s < kABStages; ++s) {
       // B producer (+ tx) and one dequant group (4 warps), or the two TMA producers (fp16
       // weights)
-      ptx::mbar_init(&S.full_ab[s], WFMT == kWF16 ? 2 : 1 + kDqWarps / 2);
+      ptx::mbar_init(&S.full_ab[s], WFMT == kWF16 ? 2 : 1 + 4);
       ptx::mbar_init(&S.empty_ab[s], 1);   // tcgen05.commit
     }
     for (int s = 0; s < kWStages; ++s) {
@@ -300,9 +301,11 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
       }
     }
   } else if (warp >= kDqWarp0) {
-    // ------------------------------------------------ dequantisers (warps 4-11)
-    // Two groups of 4 warps take alternate K stages (group 0 the even ones); a thread
+    // ------------------------------------------------ dequantisers (warps 4-15)
+    // Group j of 4 warps takes the K stages of ring slot j (kg mod 3 == j); a thread
     // converts one whole 64-column row of its stage, then fences once for the tensor core.
+    // Within a packed weight group (4 K stages) a dequant group waits for the weights
+    // before its first stage (kq <= 2) and releases them after its last (kq >= 1).
     if (WFMT != kWF16) {
       const int dq = threadIdx.x - kDqWarp0 * 32;
       const int grp = dq >> 7, r = dq & (kBM - 1);
@@ -313,9 +316,9 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
       for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
         for (int ks = 0; ks < NK; ++ks, ++kg) {
           const int kq = ks % kSub, ws = wg % kWStages;
-          if ((kq & 1) == grp) {
-            if (kq == grp && !wait_bar_t(&S.full_w[ws], (wg / kWStages) & 1, w0d)) set_abort(S, p.status);
-            const int s = kg % kABStages;
+          const int s = kg % kABStages;
+          if (s == grp) {
+            if (kq <= kSub - 2 && !wait_bar_t(&S.full_w[ws], (wg / kWStages) & 1, w0d)) set_abort(S, p.status);
             if (kg >= kABStages && !wait_bar_t(&S.empty_ab[s], ((kg / kABStages) - 1) & 1, w1d))
               set_abort(S, p.status);
             if (__any_sync(0xffffffffu, aborted(S))) {   // warp-uniform exit
@@ -351,7 +354,7 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
             __syncwarp();
             if (lane == 0) {
               ptx::mbar_arrive(&S.full_ab[s]);
-              if (kq >= kSub - 2) ptx::mbar_arrive(&S.empty_w[ws]);   // this group's last stage
+              if (kq >= 1) ptx::mbar_arrive(&S.empty_w[ws]);   // this group's last stage here
             }
           }
           if (kq == kSub - 1) ++wg;
@@ -580,8 +583,7 @@ gather_act_kernel(const void* __restrict__ x, int H, const int32_t* __restrict__
   if (!FP4 || q >= Tk) {
     for (int i = threadIdx.x * 8; i < H; i += 256 * 8) {
       float v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = load_act<XDT>(x, (size_t)tok * H + i + j);
+      load8_act<XDT>(x, (size_t)tok * H + i, v);
       uint4 o;
       o.x = h2u(__floats2half2_rn(v[0], v[1]));
       o.y = h2u(__floats2half2_rn(v[2], v[3]));
@@ -593,8 +595,16 @@ gather_act_kernel(const void* __restrict__ x, int H, const int32_t* __restrict__
     const float ts = __fdiv_rn(__uint_as_float(__ldg(amax_bits)), 2688.0f);
     for (int i = threadIdx.x * 16; i < H; i += 256 * 16) {
       float v[16], c[16], sb;
+      {
+        float v0[8], v1[8];
+        load8_act<XDT>(x, (size_t)tok * H + i, v0);
+        load8_act<XDT>(x, (size_t)tok * H + i + 8, v1);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = load_act<XDT>(x, (size_t)tok * H + i + j);
+        for (int j = 0; j < 8; ++j) {
+          v[j] = v0[j];
+          v[8 + j] = v1[j];
+        }
+      }
       nvfp4_block(v, ts, sb, c);
       uint32_t o[8];
 #pragma unroll

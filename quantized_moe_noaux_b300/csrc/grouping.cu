@@ -38,25 +38,29 @@ group_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ counts
     if (e == E - 1) offsets[E] = T * top_k;
   }
   __syncthreads();
-  int running = base_s;
+  // Each warp owns a contiguous span of the n entries: it counts the span's hits with
+  // ballots, a CTA-wide exclusive scan of the 8 counts gives its first position, and a
+  // second pass writes the hits in order (entries stay in ascending token order).
   const int n = T * top_k;
   if (counts[e] > 0) {
-    for (int c0 = 0; c0 < n; c0 += kGroupThreads) {
-      const int i = c0 + threadIdx.x;
-      const bool hit = i < n && ids[i] == e;
+    const int span = (n + kGroupThreads / 32 - 1) / (kGroupThreads / 32);
+    const int i0 = warp * span, i1 = min(n, i0 + span);
+    int mine = 0;
+    for (int c0 = i0; c0 < i1; c0 += 32) {
+      const int i = c0 + lane;
+      mine += __popc(__ballot_sync(0xffffffffu, i < i1 && __ldg(ids + i) == e));
+    }
+    __syncthreads();   // warp_sum reuse
+    if (lane == 0) warp_sum[warp] = mine;
+    __syncthreads();
+    int pos = base_s;
+    for (int w = 0; w < warp; ++w) pos += warp_sum[w];
+    for (int c0 = i0; c0 < i1; c0 += 32) {
+      const int i = c0 + lane;
+      const bool hit = i < i1 && __ldg(ids + i) == e;
       const unsigned m = __ballot_sync(0xffffffffu, hit);
-      __syncthreads();   // warp_sum reuse
-      if (lane == 0) warp_sum[warp] = __popc(m);
-      __syncthreads();
-      int before = 0, total = 0;
-#pragma unroll
-      for (int w = 0; w < kGroupThreads / 32; ++w) {
-        const int c = warp_sum[w];
-        before += (w < warp) ? c : 0;
-        total += c;
-      }
-      if (hit) entries[running + before + __popc(m & ((1u << lane) - 1u))] = i;
-      running += total;
+      if (hit) entries[pos + __popc(m & ((1u << lane) - 1u))] = i;
+      pos += __popc(m);
     }
   }
 

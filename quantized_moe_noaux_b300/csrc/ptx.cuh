@@ -50,6 +50,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return false;
 }
 
+// Bounded wait that backs off with __nanosleep(ns) after `spin` polls, so a waiting warp
+// leaves its scheduler's issue slots to the warps doing work.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, uint32_t max_iter, uint32_t spin,
+                                                  uint32_t ns) {
+  for (uint32_t i = 0; i < max_iter; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (i >= spin) __nanosleep(ns);
+  }
+  return false;
+}
+
 // ------------------------------------------------------ TMA bulk (1-D) copy
 // global -> shared, completion counted in bytes on `bar`. src, dst 16-byte aligned,
 // bytes a multiple of 16.

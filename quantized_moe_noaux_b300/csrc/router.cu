@@ -50,8 +50,9 @@ router_logits_kernel(const void* __restrict__ x, const void* __restrict__ wr,
 
 // Tiled router GEMM for larger batches: a CTA computes a 64-token x 64-expert block of
 // logits, staging 32-column slices of x and W_r in shared memory (fp32), so each router
-// row is read once per 64 tokens; 256 threads, 4 x 4 outputs each (rows ty + 16 i,
-// columns tx + 16 j), fp32 FMA in ascending column order.
+// row is read once per 64 tokens; 256 threads, a 4 x 4 block each (tokens 4 ty.., experts
+// 4 tx..) read with one 16-byte shared load per operand, fp32 FMA in ascending column
+// order.
 constexpr int kRgM = 64, kRgN = 64, kRgK = 32;
 
 template <int DT>
@@ -75,8 +76,8 @@ template <int XDT, int WDT>
 __global__ void __launch_bounds__(256)
 router_gemm_kernel(const void* __restrict__ x, const void* __restrict__ wr, float* __restrict__ logits,
                    int T, int E, int H) {
-  __shared__ float xs[kRgK][kRgM + 4];
-  __shared__ float ws[kRgK][kRgN + 4];
+  __shared__ __align__(16) float xs[kRgK][kRgM + 4];
+  __shared__ __align__(16) float ws[kRgK][kRgN + 4];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int t0 = blockIdx.y * kRgM, e0 = blockIdx.x * kRgN;
   // loader: row lr (token or expert) of the tile, 8 consecutive columns at lk
@@ -105,11 +106,9 @@ router_gemm_kernel(const void* __restrict__ x, const void* __restrict__ wr, floa
     }
 #pragma unroll
     for (int k = 0; k < kRgK; ++k) {
-      float a[4], b[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = xs[k][ty + 16 * i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = ws[k][tx + 16 * j];
+      const float4 av = *reinterpret_cast<const float4*>(&xs[k][4 * ty]);
+      const float4 bv = *reinterpret_cast<const float4*>(&ws[k][4 * tx]);
+      const float a[4] = {av.x, av.y, av.z, av.w}, b[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -119,11 +118,11 @@ router_gemm_kernel(const void* __restrict__ x, const void* __restrict__ wr, floa
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty + 16 * i;
+    const int t = t0 + 4 * ty + i;
     if (t >= T) continue;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int e = e0 + tx + 16 * j;
+      const int e = e0 + 4 * tx + j;
       if (e < E) logits[(size_t)t * E + e] = acc[i][j];
     }
   }
