@@ -182,7 +182,8 @@ moe_status moe_layer_stage_times(moe_layer* layer, float* ms, int32_t* n_forward
  * Profiling hook. With a device buffer of n_ctas x 64 uint64 (n_ctas >= the device's SM
  * count), later forwards write per-CTA records into buffer[cta * 64 + slot]:
  *  - fused decode kernel, slots 0..14, %globaltimer stamps (ns) at its phase boundaries:
- *    0 start, 1 activations staged, 2 router rows done, 4 shared gate/up done, 5 shared
+ *    0 start, 1 activations staged, 2 router rows done, 3 all CTAs' router rows seen
+ *    (routing warp), 15 selection done, 23 grouping done, 4 shared gate/up done, 5 shared
  *    gate/up of all CTAs seen, 6 shared down done, 7 routing seen, 8 routed gate/up done,
  *    9 first routed expert's gate/up seen, 10 routed down done, 11 all CTAs' down seen,
  *    12 output written, 13 producer done with shared items, 14 producer has the routing;

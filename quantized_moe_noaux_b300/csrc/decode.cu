@@ -29,7 +29,8 @@
 //   B  selected experts' gate/up tiles       (waits for the routing, in shared memory)
 //   C2 selected experts' down tiles          (waits until that expert's gate/up tiles are done)
 // After its router rows each CTA waits until every CTA has written its rows, then its
-// consumer warps select the tokens (warp t takes token t) and group the entries: every CTA
+// consumer threads select the tokens (all 256 threads per token) and group the entries:
+// every CTA
 // obtains the same routing from the same logits (CTA 0 also writes it out). The producer
 // warp issues the shared-expert items meanwhile and the routed items once the routing is
 // known.
@@ -46,7 +47,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kDecThreads = 288;      // 8 consumer warps + 1 producer warp
+constexpr int kDecThreads = 320;      // 8 consumer warps, 1 producer warp, 1 routing warp
 constexpr int kConsumers = 256;
 constexpr int kPanelK = 2048;          // columns per item
 constexpr int kCodeBytes = 16384;      // 16 rows x 2048 int4
@@ -63,7 +64,7 @@ constexpr uint32_t kMbarSpin = 1u << 22;
 // stores).
 struct alignas(16) DecCommon {
   float red[2][8][32][8];              // cross-warp reduction (double-buffered per unit)
-  float selb[kMaxE];                   // selection scratch (producer warp)
+  float selb[kMaxE];                   // selection scratch: biased and unbiased scores of one token
   float sels[kMaxE];
   int idsel[8][kMaxK];                 // per token: selected experts and weights
   float wsel[8][kMaxK];
@@ -96,6 +97,7 @@ struct DecSmem<1> {
   uint64_t full[kSlots];
   uint64_t empty[kSlots];
   uint64_t route_bar;
+  uint64_t router_bar;
   DecCommon c;
 };
 
@@ -110,6 +112,7 @@ struct DecSmem<0> {
   uint64_t full[kSlots];
   uint64_t empty[kSlots];
   uint64_t route_bar;
+  uint64_t router_bar;
   DecCommon c;
 };
 
@@ -412,88 +415,212 @@ __device__ __forceinline__ float reduced(const DecCommon& C, int rb, int half, i
 
 // ------------------------------------------------------------------ selection
 
-// Whole warp: noaux_tc selection of one token from its fp32 logits (same rule and tie order
-// as select_token of the stand-alone path): writes ids/weights of the k slots to idsel/wsel.
-// Logits are read through L2 (written by other CTAs of this grid), all loads issued first.
-__device__ __forceinline__ void select_one(const float* logits_row, const float* bias, int E, int n_group,
-                                           int topk_group, int top_k, float rsf, float* b, float* s,
-                                           int* idsel, float* wsel, int* status) {
-  const int lane = threadIdx.x & 31;
-  float lg[kMaxE / 32], bs[kMaxE / 32];
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Order key of (biased score v, expert e): larger v first, lower e on ties. The float's
+// bits are mapped to an unsigned integer with the same order (v = -0 does not occur: a
+// sigmoid in (0, 1) plus a bias never rounds to -0); the low word is ~e.
+__device__ __forceinline__ unsigned long long sel_key(float v, int e) {
+  const uint32_t u = __float_as_uint(v);
+  const uint32_t k = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+  return ((unsigned long long)k << 32) | (uint32_t)~e;
+}
+
+// Bitonic clean-up of an 8-key bitonic sequence into descending order.
+__device__ __forceinline__ void bitonic_merge8(unsigned long long (&K)[8]) {
 #pragma unroll
-  for (int i = 0; i < kMaxE / 32; ++i) {
-    const int e = lane + 32 * i;
-    lg[i] = e < E ? __ldcg(logits_row + e) : 0.f;
-    bs[i] = e < E ? __ldg(bias + e) : 0.f;
+  for (int j = 4; j > 0; j >>= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int l = i ^ j;
+      if (l > i && K[i] < K[l]) {
+        const unsigned long long t = K[i];
+        K[i] = K[l];
+        K[l] = t;
+      }
+    }
+}
+
+// One warp: noaux_tc selection of one token with the same result as the sequential picks,
+// bit for bit. Each group's score adds its two largest biased scores; the topk_group best
+// groups are kept (lower index on ties); the top_k kept experts in the order "larger biased
+// score first, lower index on ties" fill the slots; the weights' normaliser adds the picked
+// unbiased scores in slot order. Lane l holds experts l*E/32 .. (l+1)*E/32 - 1.
+// Fast path (n_group divides 32, top_k <= 8): groups are whole runs of lanes, group top-2
+// values merge over those lanes, and the top-8 keys come from a per-lane sort followed by
+// five butterfly merges of sorted 8-lists. Otherwise: group scores from shared memory and
+// top_k rounds of a warp argmax.
+__device__ __forceinline__ void select_warp(DecCommon& C, const float* logits_row, const float* bias, int E,
+                                            int n_group, int topk_group, int top_k, float rsf, int* idsel,
+                                            float* wsel) {
+  constexpr int kE = kMaxE / 32;
+  const int lane = threadIdx.x & 31;
+  const int epl = E / 32;
+  float lg[kE], bi_[kE], s[kE], b[kE];
+#pragma unroll
+  for (int j = 0; j < kE; ++j) {   // all loads first, so their latencies overlap
+    lg[j] = bi_[j] = 0.f;
+    if (j < epl) {
+      lg[j] = __ldcg(logits_row + lane * epl + j);
+      bi_[j] = __ldg(bias + lane * epl + j);
+    }
   }
 #pragma unroll
-  for (int i = 0; i < kMaxE / 32; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) {
-      const float sc = sigmoidf_acc(lg[i]);
-      s[e] = sc;
-      b[e] = sc + bs[i];
+  for (int j = 0; j < kE; ++j) {
+    s[j] = b[j] = 0.f;
+    if (j < epl) {
+      s[j] = sigmoidf_acc(lg[j]);
+      b[j] = s[j] + bi_[j];
+      C.selb[lane * epl + j] = b[j];
+      C.sels[lane * epl + j] = s[j];
     }
   }
   __syncwarp();
   const int G = E / n_group;
-  float gscore = -INFINITY;
-  if (lane < n_group) {
+  int my_e = -1;
+  float my_s = 0.f;
+  if ((32 % n_group) == 0 && top_k <= 8) {
+    // group of lane = lane / lpg; top-2 of the lane's values, then of the group's lanes
+    const int lpg = 32 / n_group;
     float m1 = -INFINITY, m2 = -INFINITY;
-    for (int i = 0; i < G; ++i) {
-      const float v = b[lane * G + i];
-      if (v > m1) {
-        m2 = m1;
-        m1 = v;
-      } else if (v > m2) {
-        m2 = v;
+#pragma unroll
+    for (int j = 0; j < kE; ++j) {
+      if (j < epl) {
+        const float v = b[j];
+        if (v > m1) {
+          m2 = m1;
+          m1 = v;
+        } else if (v > m2) {
+          m2 = v;
+        }
       }
     }
-    gscore = m1 + m2;
-  }
-  unsigned kept = 0;
-  for (int r = 0; r < topk_group; ++r) {
-    float v = gscore;
-    int gi = lane < n_group ? lane : 0x7fffffff;
-    warp_argmax(v, gi);
-    kept |= 1u << gi;
-    if (lane == gi) gscore = -INFINITY;
-  }
-  // candidates: this lane's experts of kept groups
-  float cand[kMaxE / 32];
 #pragma unroll
-  for (int i = 0; i < kMaxE / 32; ++i) {
-    const int e = lane + 32 * i;
-    cand[i] = (e < E && ((kept >> (e / G)) & 1u)) ? b[e] : -INFINITY;
-  }
-  float wsum = 0.f, my_s = 0.f;
-  int my_id = -1;
-  for (int j = 0; j < top_k; ++j) {
-    float v = -INFINITY;
-    int vi = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i)
-      if (cand[i] > v) {
-        v = cand[i];
-        vi = lane + 32 * i;
+    for (int o = 1; o < 32; o <<= 1) {
+      const float o1 = __shfl_xor_sync(0xffffffffu, m1, o), o2 = __shfl_xor_sync(0xffffffffu, m2, o);
+      if (o < lpg) {
+        const float n1 = fmaxf(m1, o1);
+        m2 = fmaxf(fminf(m1, o1), fmaxf(m2, o2));
+        m1 = n1;
       }
-    warp_argmax(v, vi);
-    if (vi < 0 || vi >= E) {   // fewer candidates than top_k: host validation forbids it
-      raise_status(status, MOE_ERR_DEVICE_CHECK);
-      vi = 0;
     }
-    const float sv = s[vi];
-    wsum += sv;
-    if (lane == j) {
-      my_id = vi;
-      my_s = sv;
-    }
+    const float gs = m1 + m2;
+    const int gid = lane / lpg;
+    int grank = 0;
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i)
-      if (lane + 32 * i == vi) cand[i] = -INFINITY;
+    for (int g2 = 0; g2 < 32; ++g2) {
+      const float w2 = __shfl_sync(0xffffffffu, gs, (g2 * lpg) & 31);
+      if (g2 < n_group) grank += (w2 > gs) || (w2 == gs && g2 < gid);
+    }
+    const bool kept = grank < topk_group;
+    unsigned long long K[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) K[j] = (j < epl && kept) ? sel_key(b[j], lane * epl + j) : 0ull;
+    // sort the lane's 8 keys (descending bitonic network)
+#pragma unroll
+    for (int k2 = 2; k2 <= 8; k2 <<= 1)
+#pragma unroll
+      for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int l = i ^ j2;
+          if (l > i) {
+            const bool desc = (i & k2) == 0 || k2 == 8;
+            if (desc ? (K[i] < K[l]) : (K[i] > K[l])) {
+              const unsigned long long t = K[i];
+              K[i] = K[l];
+              K[l] = t;
+            }
+          }
+        }
+    // top 8 of the union of two sorted lists: max(A[i], B[7-i]) is bitonic, then clean up
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      unsigned long long P[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) P[i] = __shfl_xor_sync(0xffffffffu, K[i], o);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) K[i] = K[i] > P[7 - i] ? K[i] : P[7 - i];
+      bitonic_merge8(K);
+    }
+    unsigned long long mine = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (lane == j) mine = K[j];
+    if (lane < top_k) {
+      my_e = (int)~(uint32_t)mine;
+      my_s = C.sels[my_e];
+    }
+  } else {
+    // group scores: lane gi scans group gi from a lane-dependent start (spreads the banks)
+    float gs = -INFINITY;
+    if (lane < n_group) {
+      float m1 = -INFINITY, m2 = -INFINITY;
+      const float* bg = C.selb + lane * G;
+      int i2 = lane % G;
+      for (int i = 0; i < G; ++i) {
+        const float v = bg[i2];
+        if (++i2 == G) i2 = 0;
+        if (v > m1) {
+          m2 = m1;
+          m1 = v;
+        } else if (v > m2) {
+          m2 = v;
+        }
+      }
+      gs = m1 + m2;
+    }
+    int grank = 0;
+    for (int g2 = 0; g2 < n_group; ++g2) {
+      const float w2 = __shfl_sync(0xffffffffu, gs, g2);
+      grank += (w2 > gs) || (w2 == gs && g2 < lane);
+    }
+    const unsigned kept = __ballot_sync(0xffffffffu, lane < n_group && grank < topk_group);
+    unsigned cand = 0;
+#pragma unroll
+    for (int j = 0; j < kE; ++j)
+      if (j < epl && ((kept >> ((lane * epl + j) / G)) & 1u)) cand |= 1u << j;
+    // top_k argmax rounds; lane r keeps the r-th pick
+    for (int r = 0; r < top_k; ++r) {
+      float bv = -INFINITY, bs = 0.f;
+      int bi = E;   // E: none
+#pragma unroll
+      for (int j = 0; j < kE; ++j) {
+        if ((cand >> j) & 1u) {
+          if (bi == E || b[j] > bv) {
+            bv = b[j];
+            bs = s[j];
+            bi = lane * epl + j;
+          }
+        }
+      }
+      const float local_s = bs;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (oi != E && (bi == E || ov > bv || (ov == bv && oi < bi))) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      const int win = bi < E ? bi / epl : 0;
+      const float ws = __shfl_sync(0xffffffffu, local_s, win);
+      if (lane == win && bi < E) cand &= ~(1u << (bi - lane * epl));
+      if (lane == r) {
+        my_e = bi;
+        my_s = ws;
+      }
+    }
   }
+  float wsum = 0.f;
+  for (int j = 0; j < top_k; ++j) wsum += __shfl_sync(0xffffffffu, my_s, j);
   if (lane < top_k) {
-    idsel[lane] = my_id;
+    idsel[lane] = my_e;
     wsel[lane] = my_s / wsum * rsf;
   }
   __syncwarp();
@@ -526,12 +653,6 @@ struct DecodeArgs {
 
 namespace {
 
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-
 // Phase timestamp of this CTA (profiling hook; one thread records).
 #define DEC_TRACE(i)                                                            \
   do {                                                                          \
@@ -552,12 +673,14 @@ __device__ void group_in_cta(DecSmem<MODE>& S, const DecodeArgs& a, const Geo& g
   __syncwarp();
   for (int f = lane; f < n; f += 32) atomicAdd(&C.cnt[C.idsel[f / k][f % k]], 1);
   __syncwarp();
-  const int epl = E / 32;   // lane owns experts lane*epl .. +epl-1
+  const int epl = E / 32;   // lane owns experts lane*epl .. +epl-1 (epl <= kMaxE / 32)
+  int cl[kMaxE / 32];
   int local = 0, nact = 0;
-  for (int i = 0; i < epl; ++i) {
-    const int cc = C.cnt[lane * epl + i];
-    local += cc;
-    nact += cc > 0;
+#pragma unroll
+  for (int i = 0; i < kMaxE / 32; ++i) {
+    cl[i] = i < epl ? C.cnt[lane * epl + i] : 0;
+    local += cl[i];
+    nact += cl[i] > 0;
   }
   int incl = local, inca = nact;
 #pragma unroll
@@ -570,15 +693,18 @@ __device__ void group_in_cta(DecSmem<MODE>& S, const DecodeArgs& a, const Geo& g
     }
   }
   int run = incl - local, apos = inca - nact;
-  for (int i = 0; i < epl; ++i) {
-    const int e = lane * epl + i;
-    C.soff[e] = run;
-    if (g.c == 0) a.offsets[e] = run;
-    if (C.cnt[e] > 0) {
-      C.aslot[e] = apos;
-      C.active[apos++] = e;
+#pragma unroll
+  for (int i = 0; i < kMaxE / 32; ++i) {
+    if (i < epl) {
+      const int e = lane * epl + i;
+      C.soff[e] = run;
+      if (g.c == 0) a.offsets[e] = run;
+      if (cl[i] > 0) {
+        C.aslot[e] = apos;
+        C.active[apos++] = e;
+      }
+      run += cl[i];
     }
-    run += C.cnt[e];
   }
   const int na = __shfl_sync(0xffffffffu, inca, 31);
   if (lane == 31 && g.c == 0) a.offsets[E] = run;
@@ -587,11 +713,13 @@ __device__ void group_in_cta(DecSmem<MODE>& S, const DecodeArgs& a, const Geo& g
     C.meta_w[i >> 3][i & 7] = 0.f;
   }
   __syncwarp();
+  const int* flat = &C.idsel[0][0];   // entry f = token * top_k + slot at idsel[token][slot]
   for (int f = lane; f < n; f += 32) {
     const int tok = f / k, slot = f % k;
     const int e = C.idsel[tok][slot];
     int rank = 0;
-    for (int f2 = 0; f2 < f; ++f2) rank += (C.idsel[f2 / k][f2 % k] == e);
+#pragma unroll 8
+    for (int f2 = 0; f2 < f; ++f2) rank += (flat[(f2 / k) * kMaxK + f2 % k] == e);
     const int q = C.soff[e] + rank;
     const int sl = C.aslot[e];
     C.meta_pair[sl][tok] = q;
@@ -638,6 +766,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       ptx::mbar_init(&S.empty[s], 8);
     }
     ptx::mbar_init(&S.route_bar, 1);
+    ptx::mbar_init(&S.router_bar, 1);
     ptx::fence_mbar_init();
     C.abort = 0;
     C.issued = 0;
@@ -674,16 +803,22 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       *(volatile int*)&C.issued = it;
     };
     if (lane == 0) {
+      // the router rows' weight loads go first: after two items the producer waits until this
+      // CTA's router rows are done, so the shared-expert prefetch does not delay the routing
+      int n_sh = 0;
       for (int tl = a0; tl < a1; ++tl)
-        for (int p = 0; p < g.Pu; ++p)
+        for (int p = 0; p < g.Pu; ++p) {
+          if (n_sh++ == 2) ptx::mbar_wait_backoff(&S.router_bar, 0, kMbarSpin, 4, 128);
           issue(a.up_store + ((size_t)shared_e * g.NTu + tl) * up_tile_bytes + (size_t)p * kItemBytes);
+        }
+      if (n_sh <= 2) ptx::mbar_wait_backoff(&S.router_bar, 0, kMbarSpin, 4, 128);
       for (int tl = c10; tl < c11; ++tl)
         for (int p = 0; p < g.Pd; ++p)
           issue(a.down_store + ((size_t)shared_e * g.NTd + tl) * dn_tile_bytes + (size_t)p * kItemBytes);
       DEC_TRACE(13);
     }
     if (lane == 0) {
-      // the consumers publish the routing (selection and grouping) through route_bar
+      // the routing warp publishes the routing (selection and grouping) through route_bar
       if (!ptx::mbar_wait_backoff(&S.route_bar, 0, kMbarSpin * 16, 4, 256)) {
         ok = false;
         atomicExch(&C.abort, 1);
@@ -715,6 +850,33 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
         a.trace[(size_t)blockIdx.x * 64 + 22] = (unsigned long long)it;
       }
     }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------- routing warp
+    // Waits for every CTA's router rows, selects each token's experts and groups the
+    // entries while the consumers work on the shared expert; route_bar publishes the result
+    // to the producer and the consumers.
+    int ok = 0;
+    if (lane == 0) {
+      ok = wait_geq(a.sync + 0, (uint32_t)g.G, a.spin_max) ? 1 : 0;
+      __threadfence();
+      DEC_TRACE(3);
+    }
+    __syncwarp();
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) {
+      for (int t = 0; t < g.T; ++t)
+        select_warp(C, a.logits + (size_t)t * g.E, a.bias, g.E, a.n_group, a.topk_group, g.k, a.rsf, C.idsel[t],
+                    C.wsel[t]);
+      if (lane == 0) DEC_TRACE(15);
+      group_in_cta<MODE>(S, a, g);
+      if (lane == 0) DEC_TRACE(23);
+    } else if (lane == 0) {
+      atomicExch(&C.abort, 1);
+      raise_status(a.status, MOE_ERR_TIMEOUT);
+      C.n_active = 0;
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&S.route_bar);
   } else {
     // ------------------------------------------------------------- consumers
     const int T = g.T, H = g.H, E = g.E;
@@ -809,39 +971,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       }
       ptx::bar_sync(1, kConsumers);
     }
-    // every CTA's router rows are needed: then warp t selects token t, warp 0 groups the
-    // entries, and the routing goes to the producer warp
+    // this CTA's router rows are published; the routing warp takes it from here and the
+    // consumers start on the shared expert
     if (tid == 0) {
       __threadfence();
       ptx::red_release_add(a.sync + 0, 1u);
+      ptx::mbar_arrive(&S.router_bar);
       DEC_TRACE(2);
-      C.flag = wait_geq(a.sync + 0, (uint32_t)g.G, a.spin_max) ? 1 : 0;
-      if (!C.flag) {
-        atomicExch(&C.abort, 1);
-        raise_status(a.status, MOE_ERR_TIMEOUT);
-        C.n_active = 0;
-      }
     }
-    ptx::bar_sync(1, kConsumers);
-    if (C.flag) {
-      __threadfence();
-      if (warp < T) {
-        float *sb, *ss;
-        if constexpr (MODE == 1) {
-          sb = C.selb;
-          ss = C.sels;
-        } else {
-          sb = reinterpret_cast<float*>(S.hpanel) + warp * 2 * kMaxE;   // h panel is free here
-          ss = sb + kMaxE;
-        }
-        select_one(a.logits + (size_t)warp * E, a.bias, E, a.n_group, a.topk_group, g.k, a.rsf, sb, ss,
-                   C.idsel[warp], C.wsel[warp], a.status);
-      }
-      ptx::bar_sync(1, kConsumers);
-      if (warp == 0) group_in_cta<MODE>(S, a, g);
-    }
-    ptx::bar_sync(1, kConsumers);
-    if (tid == 0) ptx::mbar_arrive(&S.route_bar);
 
     float acc[4];
     // profiling counters (cycles, consumer thread 0): waiting for item data, computing items,
@@ -909,19 +1046,28 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     // C2 routed down) so the unrolled item body exists once in the code: the consumer's
     // instruction footprint stays small. Tile results are reduced through a double-buffered
     // block, so one barrier per tile suffices.
-    int lo = a0, hi = a1, cur_sl = -2, cur_up = -1, rb = 0;
+    int lo = a0, hi = a1, cur_sl = -2, cur_up = -1, rb = 0, n_act = 0;
 #pragma unroll 1
     for (int ph = 0; ph < 4; ++ph) {
       if (ph == 1) {
         lo = c10 / 2;   // down units are pairs of 16-row tiles
         hi = c11 / 2;
       } else if (ph == 2) {
-        if (tid == 0) DEC_TRACE(6);
+        // the routed phases need the routing warp's result
+        if (tid == 0) {
+          DEC_TRACE(6);
+          C.flag = ptx::mbar_wait_backoff(&S.route_bar, 0, kMbarSpin * 16, 4, 256) ? 1 : 0;
+          if (!C.flag) {
+            atomicExch(&C.abort, 1);
+            raise_status(a.status, MOE_ERR_TIMEOUT);
+          }
+          DEC_TRACE(7);
+        }
         ptx::bar_sync(1, kConsumers);
-        if (tid == 0) DEC_TRACE(7);
-        seg_range(C.n_active * g.NTu, g.G, g.c, lo, hi);
+        n_act = C.flag ? C.n_active : 0;
+        seg_range(n_act * g.NTu, g.G, g.c, lo, hi);
       } else if (ph == 3) {
-        seg_range(C.n_active * (g.NTd / 2), g.G, g.c, lo, hi);
+        seg_range(n_act * (g.NTd / 2), g.G, g.c, lo, hi);
       }
       const int up = (ph & 1) == 0;
       const int ntl = up ? g.NTu : g.NTd / 2;

@@ -20,7 +20,7 @@ import sys
 
 import numpy as np
 
-PHASES = ["start", "activation panel", "router rows", "routing published", "shared gate/up",
+PHASES = ["start", "activation panel", "router rows", "all router rows seen", "shared gate/up",
           "shared gate/up seen", "shared down", "routing seen", "routed gate/up",
           "first routed gate/up seen", "routed down", "all down seen", "output written",
           "producer: shared issued", "producer: routing seen"]
@@ -84,6 +84,11 @@ def main(argv=None):
         for i, name in enumerate(PHASES):
             v = t[:, i][t[:, i] > 0] - t0
             if v.size:
+                print(f"{i:2d} {name:26s} CTAs={v.size:3d}  min {v.min() / 1e3:8.2f}  "
+                      f"median {np.median(v) / 1e3:8.2f}  max {v.max() / 1e3:8.2f} us")
+        for i, name in ((15, "selection done"), (23, "grouping done")):
+            v = t[:, i][t[:, i] > 0] - t0
+            if v.size and (t[:, 20] > 0).any():
                 print(f"{i:2d} {name:26s} CTAs={v.size:3d}  min {v.min() / 1e3:8.2f}  "
                       f"median {np.median(v) / 1e3:8.2f}  max {v.max() / 1e3:8.2f} us")
         if (t[:, 0] > 0).any() and (t[:, 20] > 0).any():
