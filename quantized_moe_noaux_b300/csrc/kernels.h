@@ -9,6 +9,15 @@
 namespace moe {
 
 // Router: logits[T, E] = x[T, H] W_r[E, H]^T in fp32.
+// Tensor-core router logits (bf16 activations, H % 64 == 0, E % 4 == 0): W_r as n_planes
+// (1 or 3) bf16 planes [n_planes][E][H] summing to W_r; partial: router_mma_partial_floats
+// floats of scratch. launch_router_split writes the hi/mid/lo planes of an fp32 W_r [n].
+bool router_mma_supported(int act_dtype, int H, int E);
+size_t router_mma_partial_floats(int n_sm);
+cudaError_t router_mma_init();
+cudaError_t launch_router_split(const float* w, uint16_t* planes, size_t n, cudaStream_t s);
+cudaError_t launch_router_mma(const void* x, const uint16_t* planes, int n_planes, float* logits, float* partial,
+                              int T, int E, int H, int n_sm, cudaStream_t s);
 cudaError_t launch_router_logits(const void* x, int act_dtype, const void* router_w,
                                  int router_dtype, float* logits, int T, int E, int H,
                                  cudaStream_t s);

@@ -19,6 +19,11 @@ struct moe_layer {
   float* bias = nullptr;
   ExpertWeights w{};     // routed experts (+ shared when inline)
   ExpertWeights ws{};    // separately stored shared expert
+  // tensor-core router (bf16 activations): W_r as bf16 planes summing to W_r, and the
+  // split-K scratch
+  const uint16_t* router_planes = nullptr;
+  int router_nplanes = 0;
+  float* router_part = nullptr;
   // workspace (device)
   float* logits = nullptr;
   int32_t* ids = nullptr;
@@ -233,10 +238,28 @@ moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt,
     return st;
   if (c->weight_format == MOE_W_NVFP4 && (st = dev_alloc_t(L, &L->xq, (size_t)Tm * H * 4))) return st;
 
-  // fused decode path: repack the int4 experts into MMA-fragment tiles
   int dev = 0;
   if (cudaGetDevice(&dev) || cudaDeviceGetAttribute(&L->n_sm, cudaDevAttrMultiProcessorCount, dev))
     return MOE_ERR_CUDA;
+  // tensor-core router: an fp32 W_r is split into hi/mid/lo bf16 planes once; a bf16 W_r is
+  // its own single plane
+  if (router_mma_supported(c->act_dtype, H, E)) {
+    if (router_mma_init() != cudaSuccess) return MOE_ERR_CUDA;
+    if (c->router_dtype == MOE_DT_F32) {
+      uint16_t* planes = nullptr;
+      if ((st = dev_alloc_t(L, &planes, (size_t)3 * E * H * 2))) return st;
+      if (launch_router_split(static_cast<const float*>(L->router_w), planes, (size_t)E * H, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      L->router_planes = planes;
+      L->router_nplanes = 3;
+    } else {
+      L->router_planes = static_cast<const uint16_t*>(L->router_w);
+      L->router_nplanes = 1;
+    }
+    if ((st = dev_alloc_t(L, &L->router_part, router_mma_partial_floats(L->n_sm) * 4))) return st;
+  }
+
+  // fused decode path: repack the int4 experts into MMA-fragment tiles
   L->decode_ok = c->weight_format == MOE_W_INT4_G32 && L->shared_inline &&
                  decode_supported(H, I, E, k, 1) && decode_kernels_init() == cudaSuccess;
   int occ = 0;
@@ -427,7 +450,11 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
   MOE_CK(cudaMemsetAsync(L->counts, 0, (E + 1) * sizeof(int32_t), s));
   MOE_CK(cudaMemsetAsync(L->amax, 0, 4 * sizeof(unsigned int), s));
   MOE_CK(cudaMemsetAsync(L->out_acc, 0, (size_t)T * H * sizeof(float), s));
-  MOE_LAUNCH(launch_router_logits(x, c.act_dtype, L->router_w, c.router_dtype, L->logits, T, E, H, s));
+  if (L->router_planes)
+    MOE_LAUNCH(launch_router_mma(x, L->router_planes, L->router_nplanes, L->logits, L->router_part, T, E, H,
+                                 L->n_sm, s));
+  else
+    MOE_LAUNCH(launch_router_logits(x, c.act_dtype, L->router_w, c.router_dtype, L->logits, T, E, H, s));
   MOE_LAUNCH(launch_select(L->logits, L->bias, T, E, c.n_group, c.topk_group, k, c.routed_scaling_factor,
                            L->ids, L->weights, L->counts, L->status, s));
   MOE_LAUNCH(launch_group(L->ids, L->counts, T, k, E, L->shared_inline, L->offsets, L->entries,

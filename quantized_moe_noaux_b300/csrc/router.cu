@@ -5,6 +5,7 @@
 #include <math.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 #include "route_dev.cuh"
 
 namespace moe {
@@ -128,6 +129,149 @@ router_gemm_kernel(const void* __restrict__ x, const void* __restrict__ wr, floa
   }
 }
 
+// Router logits on the tensor cores for bf16 activations (mma.sync m16n8k16, bf16
+// operands, fp32 accumulate). W_r arrives as NS bf16 planes whose sum is W_r exactly: one
+// plane for a bf16 router; hi + mid + lo for an fp32 router (split once when the layer is
+// created). Every product x * plane is then exact in fp32. The tensor core's internal
+// fp32 accumulation is not round-to-nearest, so each MMA starts from zero on one k16 step
+// and the step's sum is added to the running fp32 sum with ordinary (RN) additions. A CTA (4 warps, 32 x 32 each) computes
+// 64 tokens x 64 experts over one K split of H / S columns, staged 64 columns at a time
+// with cp.async (two buffers); with S > 1 splits the partial sums go to [S][T][E] and
+// router_split_sum_kernel adds them in split order, so the result is deterministic.
+constexpr int kRmBM = 64, kRmBN = 64, kRmBK = 64, kRmLd = kRmBK + 8;   // 144-byte smem rows
+
+template <int NS>
+struct RmSmem {
+  uint16_t x[2][kRmBM][kRmLd];
+  uint16_t w[2][NS][kRmBN][kRmLd];
+};
+
+template <int NS>
+__global__ void __launch_bounds__(128)
+router_mma_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wp, float* __restrict__ out,
+                  int T, int E, int H, int kchunk) {
+  extern __shared__ __align__(16) uint8_t rm_smem[];
+  RmSmem<NS>& S = *reinterpret_cast<RmSmem<NS>*>(rm_smem);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int wm = warp >> 1, wn = warp & 1;
+  const int t0 = blockIdx.y * kRmBM, e0 = blockIdx.x * kRmBN;
+  const int kbeg = blockIdx.z * kchunk, nk = kchunk / kRmBK;
+  // 16-byte chunk c = tid & 7 of rows tid / 8 + 16 i; rows past T or E are zero-filled
+  auto load_stage = [&](int buf, int k0) {
+    const int c = tid & 7;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = (tid >> 3) + 16 * i, t = t0 + r;
+      ptx::cp_async16(&S.x[buf][r][8 * c], x + (size_t)min(t, T - 1) * H + k0 + 8 * c, t < T ? 16u : 0u);
+    }
+#pragma unroll
+    for (int p = 0; p < NS; ++p)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = (tid >> 3) + 16 * i, e = e0 + r;
+        ptx::cp_async16(&S.w[buf][p][r][8 * c], wp + ((size_t)p * E + min(e, E - 1)) * H + k0 + 8 * c,
+                        e < E ? 16u : 0u);
+      }
+  };
+  float acc[2][4][4];
+#pragma unroll
+  for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+    for (int ni = 0; ni < 4; ++ni)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[mi][ni][q] = 0.f;
+  load_stage(0, kbeg);
+  ptx::cp_async_commit();
+  for (int ks = 0; ks < nk; ++ks) {
+    const int buf = ks & 1;
+    if (ks + 1 < nk) load_stage(buf ^ 1, kbeg + (ks + 1) * kRmBK);
+    ptx::cp_async_commit();
+    ptx::cp_async_wait<1>();
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kRmBK; kk += 16) {
+      uint32_t a[2][4];
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi)
+        ptx::ldmatrix_x4(a[mi], &S.x[buf][32 * wm + 16 * mi + (lane & 15)][kk + 8 * (lane >> 4)]);
+#pragma unroll
+      for (int nj = 0; nj < 2; ++nj) {   // two n8 blocks per ldmatrix.x4
+        uint32_t b[NS][4];
+#pragma unroll
+        for (int p = 0; p < NS; ++p)
+          ptx::ldmatrix_x4(b[p], &S.w[buf][p][32 * wn + 16 * nj + (lane & 7) + ((lane >> 4) << 3)]
+                                       [kk + 8 * ((lane >> 3) & 1)]);
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            // each k16 step starts from zero: the MMA's internal accumulation then only
+            // rounds relative to this step's own products; the step is added in fp32 (RN)
+            float th[4] = {0.f, 0.f, 0.f, 0.f};
+            ptx::mma_16816_bf16(th, a[mi], b[0][2 * h], b[0][2 * h + 1]);
+            if constexpr (NS == 3) {
+              float tl[4] = {0.f, 0.f, 0.f, 0.f};
+              ptx::mma_16816_bf16(tl, a[mi], b[1][2 * h], b[1][2 * h + 1]);
+              ptx::mma_16816_bf16(tl, a[mi], b[2][2 * h], b[2][2 * h + 1]);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) th[q] += tl[q];
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[mi][2 * nj + h][q] += th[q];
+          }
+      }
+    }
+    __syncthreads();
+  }
+  // accumulator element q of block (mi, ni): row g (+8 for q >= 2), columns 2 tq, 2 tq + 1
+  const int g = lane >> 2, tq = lane & 3;
+  float* dst = out + (size_t)blockIdx.z * T * E;
+#pragma unroll
+  for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+    for (int ni = 0; ni < 4; ++ni)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int t = t0 + 32 * wm + 16 * mi + g + 8 * hr, e = e0 + 32 * wn + 8 * ni + 2 * tq;
+        if (t < T && e < E)
+          *reinterpret_cast<float2*>(dst + (size_t)t * E + e) =
+              make_float2(acc[mi][ni][2 * hr], acc[mi][ni][2 * hr + 1]);
+      }
+}
+
+// logits = sum of the S partial blocks, added in split order.
+__global__ void router_split_sum_kernel(const float4* __restrict__ part, float4* __restrict__ logits, int n4,
+                                        int S) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += gridDim.x * blockDim.x) {
+    float4 v = part[i];
+    for (int z = 1; z < S; ++z) {
+      const float4 u = part[(size_t)z * n4 + i];
+      v.x += u.x;
+      v.y += u.y;
+      v.z += u.z;
+      v.w += u.w;
+    }
+    logits[i] = v;
+  }
+}
+
+// hi, mid, lo bf16 planes of an fp32 matrix: hi = bf16(w), mid = bf16(w - hi),
+// lo = bf16(w - hi - mid); each difference is exact (Sterbenz) and hi + mid + lo = w for
+// every normal w (24 significant bits in three 8-bit pieces).
+__global__ void router_split_kernel(const float* __restrict__ w, uint16_t* __restrict__ planes, size_t n) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const float v = w[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+    planes[i] = __bfloat16_as_ushort(hi);
+    planes[n + i] = __bfloat16_as_ushort(mid);
+    planes[2 * n + i] = __bfloat16_as_ushort(lo);
+  }
+}
+
 constexpr int kSelWarps = 4;
 constexpr int kMaxE = 1024;
 
@@ -182,6 +326,60 @@ cudaError_t launch_select(const float* logits, const float* bias, int T, int E, 
   if (E > kMaxE || n_group > 32 || top_k > 32) return cudaErrorInvalidValue;
   select_kernel<<<(T + kSelWarps - 1) / kSelWarps, kSelWarps * 32, 0, s>>>(
       logits, bias, T, E, n_group, topk_group, top_k, rsf, ids, weights, counts, status);
+  return cudaGetLastError();
+}
+
+// Split count of the tensor-core router: the smallest divisor S of H / 64 that gives at least
+// two CTAs per SM, keeping S * tiles <= 4 * n_sm (the partial buffer's capacity).
+static int router_mma_splits(int T, int E, int H, int n_sm) {
+  const long tiles = (long)((T + kRmBM - 1) / kRmBM) * ((E + kRmBN - 1) / kRmBN);
+  const int nkb = H / kRmBK;
+  int best = 1;
+  for (int d = 1; d <= nkb; ++d) {
+    if (nkb % d) continue;
+    if (d * tiles > 4L * n_sm) break;
+    best = d;
+    if (d * tiles >= 2L * n_sm) break;
+  }
+  return best;
+}
+
+size_t router_mma_partial_floats(int n_sm) { return (size_t)4 * n_sm * kRmBM * kRmBN; }
+
+bool router_mma_supported(int act_dtype, int H, int E) {
+  return act_dtype == MOE_DT_BF16 && H % kRmBK == 0 && E % 4 == 0;
+}
+
+cudaError_t router_mma_init() {
+  cudaError_t e = cudaFuncSetAttribute(router_mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sizeof(RmSmem<1>));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(router_mma_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(RmSmem<3>));
+  return e;
+}
+
+cudaError_t launch_router_split(const float* w, uint16_t* planes, size_t n, cudaStream_t s) {
+  router_split_kernel<<<592, 256, 0, s>>>(w, planes, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_mma(const void* x, const uint16_t* planes, int n_planes, float* logits, float* partial,
+                              int T, int E, int H, int n_sm, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const int S = router_mma_splits(T, E, H, n_sm);
+  const dim3 grid((E + kRmBN - 1) / kRmBN, (T + kRmBM - 1) / kRmBM, S);
+  float* out = S == 1 ? logits : partial;
+  const uint16_t* xb = static_cast<const uint16_t*>(x);
+  if (n_planes == 3)
+    router_mma_kernel<3><<<grid, 128, sizeof(RmSmem<3>), s>>>(xb, planes, out, T, E, H, H / S);
+  else
+    router_mma_kernel<1><<<grid, 128, sizeof(RmSmem<1>), s>>>(xb, planes, out, T, E, H, H / S);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || S == 1) return e;
+  const int n4 = T * E / 4;
+  router_split_sum_kernel<<<(n4 + 255) / 256, 256, 0, s>>>(reinterpret_cast<const float4*>(partial),
+                                                          reinterpret_cast<float4*>(logits), n4, S);
   return cudaGetLastError();
 }
 
