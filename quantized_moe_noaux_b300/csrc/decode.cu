@@ -880,7 +880,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
   } else {
     // ------------------------------------------------------------- consumers
     const int T = g.T, H = g.H, E = g.E;
-    if (tid == 0) DEC_TRACE(0);
+    if (tid == 0) {
+      DEC_TRACE(0);
+      if (a.trace) a.trace[(size_t)blockIdx.x * 64 + 24] = clock64();
+    }
     if constexpr (MODE == 1) {
       stage_x1<XDT>(S, a.x, H);
     } else {
@@ -1180,6 +1183,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
     if (tid == 0) {
       C.consumed = it_ok;
       DEC_TRACE(12);
+      if (a.trace) a.trace[(size_t)blockIdx.x * 64 + 25] = clock64();
       if (a.trace) {
         unsigned long long* tr = a.trace + (size_t)blockIdx.x * 64;
         tr[16] = c_wait;

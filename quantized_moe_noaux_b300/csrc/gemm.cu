@@ -576,7 +576,7 @@ __global__ void bf16_to_f16_kernel(const uint16_t* __restrict__ src, __half* __r
 template <int XDT, bool FP4>
 __global__ void __launch_bounds__(256)
 gather_act_kernel(const void* __restrict__ x, int H, const int32_t* __restrict__ entries, int Tk, int top_k,
-                  __half* __restrict__ dst, const unsigned int* __restrict__ amax_bits) {
+                  __half* __restrict__ dst, const __half* __restrict__ xq16) {
   const int q = blockIdx.x;
   const int tok = q < Tk ? __ldg(entries + q) / top_k : q - Tk;
   __half* drow = dst + (size_t)q * H;
@@ -592,26 +592,38 @@ gather_act_kernel(const void* __restrict__ x, int H, const int32_t* __restrict__
       *reinterpret_cast<uint4*>(drow + i) = o;
     }
   } else {
-    const float ts = __fdiv_rn(__uint_as_float(__ldg(amax_bits)), 2688.0f);
-    for (int i = threadIdx.x * 16; i < H; i += 256 * 16) {
-      float v[16], c[16], sb;
-      {
-        float v0[8], v1[8];
-        load8_act<XDT>(x, (size_t)tok * H + i, v0);
-        load8_act<XDT>(x, (size_t)tok * H + i + 8, v1);
+    // routed rows of an NVFP4 layer: copies of the token's quantised row
+    const uint4* srow = reinterpret_cast<const uint4*>(xq16 + (size_t)tok * H);
+    for (int i = threadIdx.x; i < H / 8; i += 256) reinterpret_cast<uint4*>(drow)[i] = __ldg(srow + i);
+  }
+}
+
+// NVFP4 activations, once per token: each 16-element block as code * block scale in fp16
+// (one thread per block; the tensor scale comes from the amax of all tokens).
+template <int XDT>
+__global__ void __launch_bounds__(256)
+quant_tokens_fp4_kernel(const void* __restrict__ x, size_t nblocks, const unsigned int* __restrict__ amax_bits,
+                        __half* __restrict__ xq16) {
+  const float ts = __fdiv_rn(__uint_as_float(__ldg(amax_bits)), 2688.0f);
+  for (size_t b = (size_t)blockIdx.x * 256 + threadIdx.x; b < nblocks; b += (size_t)gridDim.x * 256) {
+    float v[16], c[16], sb;
+    {
+      float v0[8], v1[8];
+      load8_act<XDT>(x, 16 * b, v0);
+      load8_act<XDT>(x, 16 * b + 8, v1);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          v[j] = v0[j];
-          v[8 + j] = v1[j];
-        }
+      for (int j = 0; j < 8; ++j) {
+        v[j] = v0[j];
+        v[8 + j] = v1[j];
       }
-      nvfp4_block(v, ts, sb, c);
-      uint32_t o[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) o[j] = h2u(__floats2half2_rn(c[2 * j] * sb, c[2 * j + 1] * sb));
-      *reinterpret_cast<uint4*>(drow + i) = make_uint4(o[0], o[1], o[2], o[3]);
-      *reinterpret_cast<uint4*>(drow + i + 8) = make_uint4(o[4], o[5], o[6], o[7]);
     }
+    nvfp4_block(v, ts, sb, c);
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = h2u(__floats2half2_rn(c[2 * j] * sb, c[2 * j + 1] * sb));
+    uint4* d = reinterpret_cast<uint4*>(xq16 + 16 * b);
+    d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    d[1] = make_uint4(o[4], o[5], o[6], o[7]);
   }
 }
 
@@ -728,15 +740,24 @@ cudaError_t launch_bf16_to_f16(const void* src, void* dst, size_t rows, int K, b
 }
 
 cudaError_t launch_gather_act(const void* x, int act_dtype, bool nvfp4, int H, const int32_t* entries, int Tk,
-                              int top_k, int rows, __half* dst, const unsigned int* amax_bits, cudaStream_t s) {
+                              int top_k, int rows, __half* dst, const unsigned int* amax_bits, __half* xq16,
+                              cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const bool xf = act_dtype == MOE_DT_F32;
   if (nvfp4) {
-    if (xf) gather_act_kernel<MOE_DT_F32, true><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, dst, amax_bits);
-    else gather_act_kernel<MOE_DT_BF16, true><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, dst, amax_bits);
+    const int T = rows - Tk;
+    const size_t nb = (size_t)T * H / 16;
+    size_t g = (nb + 255) / 256;
+    if (g > 148 * 16) g = 148 * 16;
+    if (nb > 0) {
+      if (xf) quant_tokens_fp4_kernel<MOE_DT_F32><<<(int)g, 256, 0, s>>>(x, nb, amax_bits, xq16);
+      else quant_tokens_fp4_kernel<MOE_DT_BF16><<<(int)g, 256, 0, s>>>(x, nb, amax_bits, xq16);
+    }
+    if (xf) gather_act_kernel<MOE_DT_F32, true><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, dst, xq16);
+    else gather_act_kernel<MOE_DT_BF16, true><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, dst, xq16);
   } else {
-    if (xf) gather_act_kernel<MOE_DT_F32, false><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, dst, amax_bits);
-    else gather_act_kernel<MOE_DT_BF16, false><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, dst, amax_bits);
+    if (xf) gather_act_kernel<MOE_DT_F32, false><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, dst, nullptr);
+    else gather_act_kernel<MOE_DT_BF16, false><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, dst, nullptr);
   }
   return cudaGetLastError();
 }

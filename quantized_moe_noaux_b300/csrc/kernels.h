@@ -146,8 +146,12 @@ cudaError_t launch_gemm_items(const int32_t* offsets, int E, int T, int top_k, i
                               cudaStream_t s);
 cudaError_t launch_bf16_to_f16(const void* src, void* dst, size_t rows, int K, bool gate_up, int I,
                                cudaStream_t s);
+// Expert-sorted fp16 activation rows: row q < Tk is token entries[q] / top_k, row Tk + t is
+// token t (shared expert). NVFP4 layers quantise each token once into xq16 [T, H] (code *
+// block scale, fp16; the tensor scale from amax_bits) and copy that row for routed rows.
 cudaError_t launch_gather_act(const void* x, int act_dtype, bool nvfp4, int H, const int32_t* entries, int Tk,
-                              int top_k, int rows, __half* dst, const unsigned int* amax_bits, cudaStream_t s);
+                              int top_k, int rows, __half* dst, const unsigned int* amax_bits, __half* xq16,
+                              cudaStream_t s);
 cudaError_t launch_quant_h(const float* h, size_t n, const unsigned int* amax_bits, __half* dst, cudaStream_t s);
 // Persistent launch over n_items x mtiles tiles (max_tiles bounds them; grid <= n_sm).
 cudaError_t launch_gemm(int wfmt, int epi, const GemmMaps& m, const GemmParams& p, int max_tiles, int n_sm,

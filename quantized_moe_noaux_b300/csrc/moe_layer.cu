@@ -368,7 +368,8 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
   const int shared_max = gemm_max_items(T, k, E, false, true);
   MOE_LAUNCH(launch_gemm_items(L->offsets, E, T, k, L->gitems, L->g_nitems, s));
   if (nvfp4) MOE_LAUNCH(launch_amax(x, c.act_dtype, (size_t)T * H, L->amax, s));
-  MOE_LAUNCH(launch_gather_act(x, c.act_dtype, nvfp4, H, L->entries, Tk, k, Tk + T, L->x16s, L->amax, s));
+  MOE_LAUNCH(launch_gather_act(x, c.act_dtype, nvfp4, H, L->entries, Tk, k, Tk + T, L->x16s, L->amax,
+                               reinterpret_cast<__half*>(L->xq), s));   // xq: [Tm, H] scratch of NVFP4 layers
   MOE_CK(m.mark(2));
   GemmParams p{};
   p.items = L->gitems;

@@ -40,6 +40,8 @@ def main(argv=None):
     ap.add_argument("--copies", type=int, default=1)
     ap.add_argument("--path", default="auto", choices=sorted(_PATHS))
     ap.add_argument("--trace", default=None, help="save decode phase timestamps here (.npy)")
+    ap.add_argument("--warm-ms", type=float, default=0.0,
+                    help="run forwards for this long first, so the traced ones see loaded clocks")
     args = ap.parse_args(argv)
 
     import torch
@@ -67,6 +69,15 @@ def main(argv=None):
     out = torch.empty((T, spec.hidden), dtype=dt, device="cuda")
     nsm = torch.cuda.get_device_properties(0).multi_processor_count
     buf = torch.zeros((nsm, 64), dtype=torch.int64, device="cuda") if args.trace else None
+    if args.warm_ms > 0:
+        import time
+        t_end = time.time() + args.warm_ms / 1e3
+        s = 0
+        while time.time() < t_end:
+            for _ in range(20):
+                layers[s % len(layers)].forward(xs[s % len(xs)], out)
+                s += 1
+            torch.cuda.synchronize()
     for s in range(args.iters):
         L = layers[s % len(layers)]
         if buf is not None and s == args.iters - 1:
@@ -91,6 +102,11 @@ def main(argv=None):
             if v.size and (t[:, 20] > 0).any():
                 print(f"{i:2d} {name:26s} CTAs={v.size:3d}  min {v.min() / 1e3:8.2f}  "
                       f"median {np.median(v) / 1e3:8.2f}  max {v.max() / 1e3:8.2f} us")
+        ok = (t[:, 25] > t[:, 24]) & (t[:, 12] > t[:, 0])
+        if ok.any():
+            mhz = (t[ok, 25] - t[ok, 24]) / (t[ok, 12] - t[ok, 0]) * 1e3
+            print(f"decode kernel SM clock (consumer thread 0, cycles / ns): median {np.median(mhz):.0f} MHz, "
+                  f"min {mhz.min():.0f}, max {mhz.max():.0f}")
         if (t[:, 0] > 0).any() and (t[:, 20] > 0).any():
             blk = t[:, 16:23].astype(np.float64)
             med = np.median(blk, axis=0)
