@@ -14,6 +14,7 @@ Prints one JSON line (rank 0). ``--impl reference`` times the fp64 CPU oracle in
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -129,6 +130,22 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                 "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
                 "samples": len(self.samples), "source": self.mode}
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from a committed ncu
+    capture (profiles/traffic.json), or None when there is none or when the kernel's source
+    file has changed since the capture (its sha256 no longer matches the recorded one)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel]
+        if rec.get("workload") != workload:
+            return None
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except (OSError, KeyError, ValueError):
+        return None
+    return float(rec["bytes_per_launch"]) if sha == rec.get("sha256") else None
 
 
 def measured_peaks():
@@ -364,7 +381,8 @@ def run_ours(args):
         achieved = dom_bytes / dom_s / 1e9
         roofline = {"bound": "hbm", "kernel": "moe_decode_kernel (router, selection, gate/up, down, combine)",
                     "achieved": achieved, "peak": peak_bw, "peak_kind": peak_kind, "unit": "GB/s",
-                    "frac": achieved / peak_bw, "traffic": None, "bytes_per_launch": dom_bytes / K}
+                    "frac": achieved / peak_bw, "traffic": recorded_traffic("moe_decode_kernel", wl.name),
+                    "bytes_per_launch": dom_bytes / K}
     else:
         # dominant kernel: the gate/up GEMM (2/3 of the FLOPs and of the weight bytes)
         dom = "gate_up_or_fused"
