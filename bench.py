@@ -17,6 +17,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import sys
 import threading
@@ -132,20 +133,32 @@ class ClockSampler:
                 "samples": len(self.samples), "source": self.mode}
 
 
+def source_fingerprint(text):
+    """sha256 of CUDA sources with /* */ and // comments, trailing blanks and empty lines
+    removed: it changes with any change to the code, not with a comment edit."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    code = [line.split("//", 1)[0].rstrip() for line in text.splitlines()]
+    return hashlib.sha256("\n".join(c for c in code if c).encode()).hexdigest()
+
+
 def recorded_traffic(kernel, workload):
     """DRAM bytes (read + write) per launch of `kernel` on `workload` from a committed ncu
-    capture (profiles/traffic.json), or None when there is none or when the kernel's source
-    file has changed since the capture (its sha256 no longer matches the recorded one)."""
+    capture (profiles/traffic.json), or None when there is none or when the code of the
+    kernel's sources (the .cu file and the headers it includes) has changed since the
+    capture (their fingerprint no longer matches the recorded one)."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)[kernel]
         if rec.get("workload") != workload:
             return None
-        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
+        text = ""
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, src)) as f:
+                text += f.read() + "\n"
+        fp = source_fingerprint(text)
     except (OSError, KeyError, ValueError):
         return None
-    return float(rec["bytes_per_launch"]) if sha == rec.get("sha256") else None
+    return float(rec["bytes_per_launch"]) if fp == rec.get("source_fingerprint") else None
 
 
 def measured_peaks():

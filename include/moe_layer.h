@@ -189,7 +189,9 @@ moe_status moe_layer_stage_times(moe_layer* layer, float* ms, int32_t* n_forward
  *    12 output written, 13 producer done with shared items, 14 producer has the routing;
  *    and in slots 16..22 clock cycles of consumer thread 0 waiting for item data,
  *    computing items, reducing tiles, switching experts, the items it consumed, the
- *    producer's cycles waiting for a free slot and the items it issued;
+ *    producer's cycles waiting for a free slot and the items it issued; slots 24 and 25:
+ *    consumer thread 0's clock64 at slots 0 and 12 (their ratio to the ns stamps is the
+ *    SM clock during the kernel);
  *  - grouped GEMMs, slots 16..26 (gate/up), 32..42 (down), 48..58 (separately stored
  *    shared expert, gate/up), clock cycles: +0 kernel, +1 MMA waiting for operands, +2 MMA
  *    waiting for an accumulator, +3 dequantiser waiting for weights, +4 dequantiser waiting

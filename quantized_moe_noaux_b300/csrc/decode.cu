@@ -28,15 +28,16 @@
 //   C1 shared-expert down tiles              (waits until every shared gate/up tile is done)
 //   B  selected experts' gate/up tiles       (waits for the routing, in shared memory)
 //   C2 selected experts' down tiles          (waits until that expert's gate/up tiles are done)
-// After its router rows each CTA waits until every CTA has written its rows, then its
-// consumer threads select the tokens (all 256 threads per token) and group the entries:
-// every CTA
-// obtains the same routing from the same logits (CTA 0 also writes it out). The producer
-// warp issues the shared-expert items meanwhile and the routed items once the routing is
-// known.
-// Down tiles add w * y into an fp32 accumulator with atomics; after a grid-wide count every
-// CTA converts its slice to the output type. All inter-CTA waits are bounded; on time-out
-// the kernel records MOE_ERR_TIMEOUT, drains its own copies in flight and returns.
+// Warps: 8 consumers, 1 producer (TMA bulk copies), 1 routing warp. Once a CTA's router
+// rows are written, its routing warp waits until every CTA has written its rows, selects
+// each token's experts (one warp per token, in turn) and groups the entries, while the
+// consumers already run the shared expert (A, C1). Every CTA obtains the same routing from
+// the same logits (CTA 0 also writes it out). The producer issues the shared-expert items
+// first and the routed items once the routing warp publishes the routing.
+// Down tiles add w * y into an fp32 accumulator with atomics; the last CTA to finish its
+// down tiles (a ticket counter) converts the whole output to the output type. All
+// inter-CTA waits are bounded; on time-out the kernel records MOE_ERR_TIMEOUT, drains its
+// own copies in flight and returns.
 #include <cstddef>
 
 #include "kernels.h"
