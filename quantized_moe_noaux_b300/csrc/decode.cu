@@ -138,6 +138,13 @@ __device__ __forceinline__ float2 half2_to_float2(uint32_t u) {
   return __half22float2(*reinterpret_cast<const __half2*>(&u));
 }
 
+// Elementwise fp16x2 product of two registers (round to nearest).
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // One word of codes -> the four fp16 A registers of an m16n8k16 MMA (see file comment).
 __device__ __forceinline__ void decode_word(uint32_t w, uint32_t (&a)[4]) {
   const uint32_t w2 = w >> 8;
@@ -307,6 +314,12 @@ __device__ __forceinline__ void compute_item1(const uint32_t* act, const float* 
   const uint8_t* scl = slot + kCodeBytes + (w * 8 + g) * 32;
   const uint32_t* xb = act + 8 * (m_base + 16 * w + 2 * g) + t;
   const uint32_t b00 = xb[0], b01 = xb[4], b10 = xb[8], b11 = xb[12];
+  // the B operand of MMA mi is the lane's x values when its group column is this lane
+  // group's (mi / 2 == g), else zero: an fp16 multiply by 1 or 0 (exact) on the FMA pipe,
+  // which leaves the ALU pipe to the int4 decode
+  uint32_t msk[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) msk[j] = j == g ? 0x3C003C00u : 0u;
   float d[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
@@ -319,9 +332,8 @@ __device__ __forceinline__ void compute_item1(const uint32_t* act, const float* 
       const int mi = 4 * cc + i;           // MMA within the k-block; active lane group mi / 2
       uint32_t a[4];
       decode_word(words[i], a);
-      const bool on = (mi >> 1) == g;
-      const uint32_t bx = on ? ((mi & 1) ? b10 : b00) : 0u;
-      const uint32_t by = on ? ((mi & 1) ? b11 : b01) : 0u;
+      const uint32_t bx = hmul2_bits((mi & 1) ? b10 : b00, msk[mi >> 1]);
+      const uint32_t by = hmul2_bits((mi & 1) ? b11 : b01, msk[mi >> 1]);
       ptx::mma_16816(d[i], a, bx, by, d[i]);
     }
   }
