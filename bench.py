@@ -54,6 +54,28 @@ def dist_info():
             int(os.environ.get("WORLD_SIZE", 1)))
 
 
+def rank_seed_base(rank, steps, warmup):
+    """First input seed of this rank: rank r draws seeds base .. base + steps + warmup - 1,
+    disjoint from every other rank's (each replica processes its own tokens)."""
+    return 1000 * rank * (steps + warmup)
+
+
+def max_over_ranks(value, world, device):
+    """The largest of the ranks' `value` (the slowest rank's time): an all_reduce MAX over
+    the default process group when world > 1."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, steps, tokens, seconds):
+    """Whole-job tokens/s: all ranks' tokens over the slowest rank's time."""
+    return world * steps * tokens / seconds
+
+
 class ClockSampler:
     """SM clock and clock-event reasons sampled on a background thread while the timed
     region runs (NVML when the Python binding is importable, else `nvidia-smi -lms`)."""
@@ -279,7 +301,7 @@ def run_ours(args):
     stream = torch.cuda.Stream()
     dt = torch.bfloat16 if spec.act_dtype == "bf16" else torch.float32
     H = spec.hidden
-    base = 1000 * rank * (K + W)          # distinct tokens per rank
+    base = rank_seed_base(rank, K, W)     # distinct tokens per rank
     X = torch.stack([x_to_device(make_x(spec, T, base + s), spec.act_dtype) for s in range(K + W)])
     OUT = torch.empty((K + W, T, H), dtype=dt, device="cuda")
 
@@ -327,12 +349,8 @@ def run_ours(args):
             torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-        ms = ev0.elapsed_time(ev1)
-        ms_t = torch.tensor([ms], device="cuda")
-        if world > 1:
-            dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-        ms = float(ms_t.item())
-        value = world * K * T / (ms / 1000.0)
+        ms = max_over_ranks(ev0.elapsed_time(ev1), world, "cuda")
+        value = job_throughput(world, K, T, ms / 1000.0)
 
         # per-stage durations over a replay of the same K steps (stage events recorded
         # inside a second graph capture)
@@ -361,11 +379,7 @@ def run_ours(args):
         t0 = time.perf_counter()
         for s in range(KE):
             layers[s % C].forward_host(xh[s], oh[s], stream)
-        e2e_s = time.perf_counter() - t0
-        e2e_t = torch.tensor([e2e_s], device="cuda")
-        if world > 1:
-            dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-        e2e_value = world * KE * T / float(e2e_t.item())
+        e2e_value = job_throughput(world, KE, T, max_over_ranks(time.perf_counter() - t0, world, "cuda"))
 
     if rank != 0:
         if world > 1:
