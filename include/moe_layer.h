@@ -210,8 +210,11 @@ moe_status moe_layer_launch_count(moe_layer* layer, int64_t* count);
  * exists for callers that cannot call cudaMalloc when they need routing (code running
  * while a stream is captured into a CUDA graph, where allocation is not capturable; hosts
  * whose framework owns the device memory budget; runtimes that forbid allocation after
- * start-up). It computes the same routing as moe_layer_forward + moe_layer_get_routing,
- * with the same kernels, from caller-owned DEVICE buffers:
+ * start-up). It computes the routing of moe_layer_forward + moe_layer_get_routing from
+ * caller-owned DEVICE buffers, with the same selection and grouping kernels; the logits
+ * come from the CUDA-core router kernels. Those add in another order than the tensor-core
+ * router that a layer uses for bf16 activations. So the selections agree except where two
+ * biased scores lie within fp32 rounding of each other. Inputs and outputs:
  *   x [T, H] (act_dtype), router_w [E, H] (router_dtype), bias [E] fp32
  *   -> ids [T, top_k] int32, weights [T, top_k] fp32, offsets [E + 1] int32,
  *      entries [T * top_k] int32 (layouts as in moe_layer_get_routing).
