@@ -80,3 +80,43 @@ def test_prefill_t2048(glm_base):
     errs, counts, rep = check("glm52_skewed", glm_base, 2048, 0, sample=[0, 777, 2047])
     assert counts.sum() == 2048 * 8
     assert counts.max() > 4 * counts[counts > 0].mean()    # the wide bias skews the load
+
+
+def test_decode_t1_bench_steps_routing(glm_base):
+    """The bench's default decode workload (seeds 10..1009, one token per step, the timed
+    steps of `bench.py` with its defaults) through the fused kernel: every step's
+    selection, weights and grouping against the oracle (near-tie rule); outputs for three
+    of the steps."""
+    spec, arrays, layer, oracle = get_layer("glm52", glm_base)
+    from oracle.moe_oracle import group_tokens, routing_weights
+    seeds = list(range(10, 1010))
+    samples = {0: None, 499: None, 999: None}          # step index -> output row
+    xs = np.concatenate([make_x(spec, 1, s) for s in seeds])
+    k = spec.top_k
+    ids = np.empty((len(seeds), k), np.int32)
+    w = np.empty((len(seeds), k), np.float32)
+    out = empty_out(1, spec.hidden, spec.act_dtype)
+    for i in range(len(seeds)):
+        layer.forward(x_to_device(xs[i:i + 1], spec.act_dtype), out)
+        r = layer.routing(1)
+        ids[i], w[i] = r["ids"][0], r["weights"][0]
+        if i in samples:
+            samples[i] = out_to_host(out)[0]
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    scores, sel = oracle.route(oracle.widen_x(xs))
+
+    class R:  # routing-only oracle result, one row per step
+        pass
+    ref = R()
+    ref.ids, ref.scores, ref.margin = sel.ids, scores, sel.margin
+    ref.weights = routing_weights(scores, sel.ids, spec.rsf)
+    ref.counts, ref.offsets, ref.entries = group_tokens(sel.ids, spec.n_experts)
+    _, goff, gent = group_tokens(ids.astype(np.int64), spec.n_experts)
+    got = {"ids": ids, "weights": w, "offsets": goff, "entries": gent}
+    rep = check_routing(ref, got, bias=arrays["bias"], n_group=spec.n_group,
+                        topk_group=spec.topk_group, top_k=k, n_experts=spec.n_experts)
+    for i, row in samples.items():
+        use = ids[i:i + 1] if i in rep["mismatch"] else None
+        o = oracle.forward(xs[i:i + 1], ids=use)
+        check_out(o.out, row[None])
