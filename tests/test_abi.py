@@ -5,6 +5,8 @@ import glob
 import os
 import re
 
+import pytest
+
 import quantized_moe_noaux_b300 as moe
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -36,3 +38,37 @@ def test_status_strings_and_null_safety():
     assert moe.lib.moe_layer_status(None) == 1
     assert moe.lib.moe_layer_set_path(None, 0) == 1
     assert moe.lib.moe_layer_create(None, None, None, None) == 1
+
+
+def _cfg(**over):
+    base = dict(hidden=6144, inter=2048, n_experts=256, top_k=8, n_group=8, topk_group=4,
+                max_tokens=64, routed_scaling_factor=2.5, weight_format=moe.W_INT4_G32,
+                shared_format=moe.W_INT4_G32, act_dtype=moe.DT_BF16, router_dtype=moe.DT_F32)
+    base.update(over)
+    return moe.Config(**base)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(hidden=0), 1), (dict(top_k=0), 1), (dict(max_tokens=0), 1),
+    (dict(routed_scaling_factor=0.0), 1), (dict(routed_scaling_factor=float("nan")), 1),
+    (dict(weight_format=7), 2), (dict(shared_format=9), 2), (dict(act_dtype=5), 2),
+    (dict(router_dtype=5), 2),
+    (dict(hidden=6000), 2),                       # H not a multiple of 256
+    (dict(inter=2000), 2),                        # I not a multiple of 64
+    (dict(n_experts=250), 2),                     # E not a multiple of n_group
+    (dict(n_group=64, n_experts=256), 2),         # more than 32 groups
+    (dict(n_experts=16, n_group=16), 2),          # one expert per group
+    (dict(topk_group=9), 2),                      # more kept groups than groups
+    (dict(top_k=33), 2),                          # top_k above the selection limit
+    (dict(n_experts=16, n_group=8, topk_group=1, top_k=3), 2),   # top_k > kept experts
+    (dict(max_tokens=16385), 2),
+])
+def test_create_rejects_bad_configs_before_touching_the_device(over, code):
+    """moe_layer_create checks the configuration first (no CUDA call, so this runs on CPU),
+    returns the documented status and leaves *out NULL."""
+    cfg = _cfg(**over)
+    w = moe.Weights()
+    out = ctypes.c_void_p(1)
+    rc = moe.lib.moe_layer_create(ctypes.byref(cfg), ctypes.byref(w), None, ctypes.byref(out))
+    assert rc == code, (over, rc)
+    assert out.value is None
