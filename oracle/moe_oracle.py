@@ -274,6 +274,16 @@ def swiglu_hidden(w_gu: np.ndarray, xr: np.ndarray) -> np.ndarray:
     return silu(gu[:, :i]) * gu[:, i:]
 
 
+def identity_glu_hidden(w_gu: np.ndarray, xr: np.ndarray) -> np.ndarray:
+    """h = gate * up, the gated unit with the SiLU bypassed. Test-only: with integer
+    activations and power-of-two scales every step of the layer is then exact in fp64 and
+    in fp32, so an implementation's expert and combine arithmetic can be compared bit for
+    bit (the layer itself always uses SiLU)."""
+    gu = np.asarray(xr, np.float64) @ np.asarray(w_gu, np.float64).T
+    i = gu.shape[1] // 2
+    return gu[:, :i] * gu[:, i:]
+
+
 def down_proj(w_d: np.ndarray, h: np.ndarray) -> np.ndarray:
     """y = W_d h."""
     return np.asarray(h, np.float64) @ np.asarray(w_d, np.float64).T
@@ -350,11 +360,15 @@ class Layer:
         return scores, sel
 
     def forward(self, x: np.ndarray, ids: np.ndarray | None = None,
-                tokens: np.ndarray | None = None) -> LayerRef:
+                tokens: np.ndarray | None = None, activation: str = "silu") -> LayerRef:
         """Whole-layer forward. ``ids`` overrides the selection (used to re-run the
         oracle on a near-tie token with the selection another implementation made);
         ``tokens`` restricts the expert FFNs and the output to those rows (the routing
-        and the NVFP4 activation scales still see every token)."""
+        and the NVFP4 activation scales still see every token); ``activation`` =
+        "identity" bypasses the SiLU (test-only exact-arithmetic cases)."""
+        if activation not in ("silu", "identity"):
+            raise ValueError(activation)
+        hidden = swiglu_hidden if activation == "silu" else identity_glu_hidden
         x64 = self.widen_x(x)
         t_count = x64.shape[0]
         scores, sel = self.route(x64)
@@ -378,7 +392,7 @@ class Layer:
             if ent.size == 0:
                 continue
             w_gu, _ = self.routed_expert(e)
-            hs[e] = (ent, swiglu_hidden(w_gu, x_in[ent // self.top_k]))
+            hs[e] = (ent, hidden(w_gu, x_in[ent // self.top_k]))
         if nvfp4 and hs:
             order = sorted(hs)
             h_q = quantize_nvfp4_activation(
@@ -400,5 +414,5 @@ class Layer:
 
         sh_gu, sh_d = self.shared_expert()
         xs = x64[rows] if self.shared_format == "bf16" else x_in[rows]
-        out[rows] += down_proj(sh_d, swiglu_hidden(sh_gu, xs))
+        out[rows] += down_proj(sh_d, hidden(sh_gu, xs))
         return LayerRef(out, use_ids, w, scores, sel.margin, counts, offsets, entries)

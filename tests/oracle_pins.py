@@ -322,6 +322,20 @@ def pin_hand_two_expert(O):
     assert np.allclose(ref.out[0], expect, rtol=1e-12, atol=1e-14), (ref.out[0][:8], expect[:8])
 
 
+def pin_identity_activation_exact(O):
+    """The hand-worked layer with the SiLU bypassed: at k = 1 the weight is exactly rsf and
+    every product is a small dyadic number, so the output is known exactly (gate 4, up 2
+    for expert 1; gate 1, up 3 for the shared expert)."""
+    layer, x = hand_layer(O, "k1")
+    ref = layer.forward(x, activation="identity")
+    assert ref.ids.tolist() == [[1]]
+    expect = np.zeros(32)
+    expect[0] = 2.5 * (4.0 * 2.0)
+    expect[7] = 2.5 * 0.875 * (4.0 * 2.0)
+    expect[1] = -2 * (1.0 * 3.0)
+    assert np.array_equal(ref.out[0], expect), (ref.out[0][:8], expect[:8])
+
+
 def pin_layer_invariants(O, spec, arrays, x):
     """Token permutation commutes with the layer; the routing weights sum to rsf;
     doubling every routed W_d scale doubles the routed part of the output."""
@@ -343,4 +357,4 @@ def pin_layer_invariants(O, spec, arrays, x):
 ALL_PINS = [pin_decode_int4, pin_decode_e4m3, pin_decode_e2m1, pin_dequant_int4_g32,
             pin_dequant_nvfp4, pin_nvfp4_rounding, pin_nvfp4_activation, pin_select_brute_force,
             pin_select_special_cases, pin_routing_weights, pin_group_tokens,
-            pin_expert_ffn_torch, pin_hand_two_expert]
+            pin_expert_ffn_torch, pin_hand_two_expert, pin_identity_activation_exact]
