@@ -27,10 +27,13 @@ neues GLM-5.2 NVFP4 Modell vor", section "Technische Details und Quantisierungsa
 10. out_t = sum_j w[t, j] y_{t, ids[t, j]} + y_{t, shared}; the shared expert has weight 1.
 
 NVFP4 layers also quantise the activations that feed the routed experts (x before the
-gate/up projection, h before the down projection) to NVFP4 with a per-call tensor scale;
-the codes are decided in fp32 (the precision the kernel decides them in), and the
-dequantised values are then used exactly. The router and a bf16 shared expert read the
-unquantised x.
+gate/up projection, h before the down projection) to NVFP4 with a per-call tensor scale
+(one scale over all tokens of x; one over all routed h rows of the call); the router and a
+bf16 shared expert read the unquantised x. The codes are decided in fp32: the format's
+tensor scale is an fp32 number by definition, and the block scale and each element's code
+are the E4M3 and E2M1 roundings of quotients by it, so those quotients are fp32
+operations (an fp64 quotient could fall on the other side of a rounding boundary); the
+dequantised values are then used exactly.
 
 Readings where the pages are silent are stated at each function. Every function here is
 pinned by ``tests/test_oracle_pins.py`` to something other than itself (brute force,
@@ -106,16 +109,29 @@ def decode_e4m3(bits: np.ndarray) -> np.ndarray:
     return sign * mag
 
 
+_E2M1_LO = decode_e2m1(np.arange(256) & 0x0F)   # value of the low nibble of every byte
+_E2M1_HI = decode_e2m1(np.arange(256) >> 4)     # and of the high nibble
+_E4M3_ALL = decode_e4m3(np.arange(256))          # value of every E4M3 byte
+
+
 def dequant_nvfp4(codes: np.ndarray, scales: np.ndarray, tensor_scale) -> np.ndarray:
     """W[n, k] = e2m1(code[n, k]) * e4m3(scale[n, k // 16]) * tensor_scale, exact in fp64
-    (NVFP4: 4-bit elements, an FP8 scale per 16 elements, one fp32 scale per tensor)."""
+    (NVFP4: 4-bit elements, an FP8 scale per 16 elements, one fp32 scale per tensor).
+    Element 2j is the low nibble of byte j; the byte tables are the decoders above applied
+    to every byte value."""
     codes = np.asarray(codes, dtype=np.uint8)
-    nib = np.stack([codes & 0x0F, codes >> 4], axis=-1).reshape(codes.shape[0], -1)
-    c = decode_e2m1(nib)
-    n, k = c.shape
-    sb = decode_e4m3(scales)
+    n, kb = codes.shape
+    k = 2 * kb
+    c = np.empty((n, k))
+    np.take(_E2M1_LO, codes, out=c[:, 0::2])
+    np.take(_E2M1_HI, codes, out=c[:, 1::2])
+    sb = _E4M3_ALL[np.asarray(scales, dtype=np.uint8)]
     assert sb.shape == (n, k // 16)
-    return (c.reshape(n, k // 16, 16) * sb[..., None]).reshape(n, k) * float(np.float32(tensor_scale))
+    c = c.reshape(n, k // 16, 16)
+    c *= sb[..., None]
+    c = c.reshape(n, k)
+    c *= float(np.float32(tensor_scale))
+    return c
 
 
 def widen_bf16(bits: np.ndarray) -> np.ndarray:
@@ -289,6 +305,31 @@ def down_proj(w_d: np.ndarray, h: np.ndarray) -> np.ndarray:
     return np.asarray(h, np.float64) @ np.asarray(w_d, np.float64).T
 
 
+# ---------------------------------------------------- NVFP4 layer activation rules
+
+
+def quantize_routed_h(hs: dict) -> dict:
+    """NVFP4 h before the routed experts' down projections (reading of the NVFP4 layer:
+    one per-call tensor scale covers every routed h row of the call, like x's covers every
+    token). ``hs`` maps expert -> (entries, h rows); the rows of all experts, in ascending
+    expert order, form one activation for quantize_nvfp4_activation."""
+    order = sorted(hs)
+    h_q = quantize_nvfp4_activation(np.concatenate([hs[e][1] for e in order]).astype(np.float32))
+    out, n0 = {}, 0
+    for e in order:
+        n1 = n0 + len(hs[e][0])
+        out[e] = (hs[e][0], h_q[n0:n1])
+        n0 = n1
+    return out
+
+
+def shared_expert_input(shared_format: str, x64: np.ndarray, x_in: np.ndarray) -> np.ndarray:
+    """Activation the shared expert reads: a bf16 shared expert (the NVFP4 layer keeps it
+    unquantised, like the router) reads the unquantised x; a shared expert stored in the
+    routed format reads the same activation as the routed experts."""
+    return x64 if shared_format == "bf16" else x_in
+
+
 # ----------------------------------------------------------------- whole layer
 
 
@@ -330,25 +371,29 @@ class Layer:
         w = self.a["router_w"]
         return widen_bf16(w) if self.router_dtype == "bf16" else np.asarray(w, np.float64)
 
-    def _expert(self, prefix: str, idx: int, fmt: str):
-        a = self.a
+    def _matrix(self, prefix: str, idx: int, fmt: str, which: str) -> np.ndarray:
+        """One dequantised expert matrix: which = "gu" (W_gu [2I, H]) or "d" (W_d [H, I])."""
+        a, p = self.a, prefix + which
         if fmt == "int4_g32":
-            return (dequant_int4_g32(a[prefix + "gu_codes"][idx], a[prefix + "gu_scales"][idx]),
-                    dequant_int4_g32(a[prefix + "d_codes"][idx], a[prefix + "d_scales"][idx]))
+            return dequant_int4_g32(a[p + "_codes"][idx], a[p + "_scales"][idx])
         if fmt == "nvfp4":
-            return (dequant_nvfp4(a[prefix + "gu_codes"][idx], a[prefix + "gu_scales"][idx],
-                                  a[prefix + "gu_tscale"][idx]),
-                    dequant_nvfp4(a[prefix + "d_codes"][idx], a[prefix + "d_scales"][idx],
-                                  a[prefix + "d_tscale"][idx]))
+            return dequant_nvfp4(a[p + "_codes"][idx], a[p + "_scales"][idx], a[p + "_tscale"][idx])
         if fmt == "bf16":
-            return widen_bf16(a[prefix + "gu_bf16"][idx]), widen_bf16(a[prefix + "d_bf16"][idx])
+            return widen_bf16(a[p + "_bf16"][idx])
         raise ValueError(fmt)
 
+    def routed_gu(self, e: int) -> np.ndarray:
+        return self._matrix("", e, self.weight_format, "gu")
+
+    def routed_d(self, e: int) -> np.ndarray:
+        return self._matrix("", e, self.weight_format, "d")
+
     def routed_expert(self, e: int):
-        return self._expert("", e, self.weight_format)
+        return self.routed_gu(e), self.routed_d(e)
 
     def shared_expert(self):
-        return self._expert("sh_", 0, self.shared_format)
+        return (self._matrix("sh_", 0, self.shared_format, "gu"),
+                self._matrix("sh_", 0, self.shared_format, "d"))
 
     def widen_x(self, x: np.ndarray) -> np.ndarray:
         return widen_bf16(x) if self.act_dtype == "bf16" else np.asarray(x, np.float64)
@@ -391,28 +436,19 @@ class Layer:
                 ent = ent[want[ent // self.top_k]]
             if ent.size == 0:
                 continue
-            w_gu, _ = self.routed_expert(e)
-            hs[e] = (ent, hidden(w_gu, x_in[ent // self.top_k]))
+            hs[e] = (ent, hidden(self.routed_gu(e), x_in[ent // self.top_k]))
         if nvfp4 and hs:
-            order = sorted(hs)
-            h_q = quantize_nvfp4_activation(
-                np.concatenate([hs[e][1] for e in order]).astype(np.float32))
-            n0 = 0
-            for e in order:
-                n1 = n0 + len(hs[e][0])
-                hs[e] = (hs[e][0], h_q[n0:n1])
-                n0 = n1
+            hs = quantize_routed_h(hs)
         for e, (ent, h) in hs.items():
             keep = want[ent // self.top_k]
             if not keep.any():
                 continue
-            _, w_d = self.routed_expert(e)
-            y = down_proj(w_d, h[keep])
+            y = down_proj(self.routed_d(e), h[keep])
             for r, yy in zip(ent[keep], y):
                 t, j = divmod(int(r), self.top_k)
                 out[t] += w[t, j] * yy
 
         sh_gu, sh_d = self.shared_expert()
-        xs = x64[rows] if self.shared_format == "bf16" else x_in[rows]
+        xs = shared_expert_input(self.shared_format, x64, x_in)[rows]
         out[rows] += down_proj(sh_d, hidden(sh_gu, xs))
         return LayerRef(out, use_ids, w, scores, sel.margin, counts, offsets, entries)

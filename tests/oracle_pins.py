@@ -77,6 +77,59 @@ def hand_layer(O, case: str):
     return layer, x
 
 
+_E2M1_CODE = {0.0: 0, 0.5: 1, 1.0: 2, 1.5: 3, 2.0: 4, 3.0: 5, 4.0: 6, 6.0: 7}
+
+
+def _bf16_bits(v: float) -> int:
+    """bf16 bit pattern of a value that bf16 holds exactly (the top half of its fp32 bits)."""
+    b = int(np.array([v], np.float32).view(np.uint32)[0])
+    assert b & 0xFFFF == 0, v
+    return b >> 16
+
+
+def hand_nvfp4_layer(O):
+    """Build the hand-worked NVFP4 layer of tests/golden/hand_nvfp4_layer.json."""
+    with open(os.path.join(GOLDEN, "hand_nvfp4_layer.json")) as f:
+        g = json.load(f)
+    H, I, E = g["hidden"], g["inter"], g["n_experts"]
+    x = np.zeros((1, H), np.uint16)
+    for k, v in g["x_nonzero"].items():
+        x[0, int(k)] = _bf16_bits(v)
+    wr = np.zeros((E, H), np.uint16)
+    for e, row in g["router_w"].items():
+        for h, v in row.items():
+            wr[int(e), int(h)] = _bf16_bits(v)
+
+    def nvfp4(rows, K, spec):
+        nib = np.zeros((rows, K), np.uint8)
+        for r, cols in spec.items():
+            for c, v in cols.items():
+                nib[int(r), int(c)] = _E2M1_CODE[abs(v)] | (8 if v < 0 else 0)
+        packed = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+        return packed, np.full((rows, K // 16), 0x38, np.uint8), np.float32(1.0)
+
+    def bf16(rows, K, spec):
+        w = np.zeros((rows, K), np.uint16)
+        for r, cols in spec.items():
+            for c, v in cols.items():
+                w[int(r), int(c)] = _bf16_bits(v)
+        return w
+
+    ex = [(nvfp4(2 * I, H, s["gu"]), nvfp4(H, I, s["d"])) for s in g["experts"]]
+    arrays = {
+        "router_w": wr, "bias": np.zeros(E, np.float32),
+        "gu_codes": np.stack([e[0][0] for e in ex]), "gu_scales": np.stack([e[0][1] for e in ex]),
+        "gu_tscale": np.array([e[0][2] for e in ex], np.float32),
+        "d_codes": np.stack([e[1][0] for e in ex]), "d_scales": np.stack([e[1][1] for e in ex]),
+        "d_tscale": np.array([e[1][2] for e in ex], np.float32),
+        "sh_gu_bf16": bf16(2 * I, H, g["shared"]["gu"])[None], "sh_d_bf16": bf16(H, I, g["shared"]["d"])[None],
+    }
+    layer = O.Layer(arrays, hidden=H, inter=I, n_experts=E, top_k=g["top_k"], n_group=1, topk_group=1,
+                    rsf=g["rsf"], weight_format="nvfp4", act_dtype="bf16", router_dtype="bf16",
+                    shared_format="bf16")
+    return layer, x
+
+
 def brute_force_select(b: np.ndarray, n_group: int, topk_group: int, top_k: int):
     """Exhaustive noaux_tc selection for one token with distinct scores: the best group
     subset by summed group score, then the best expert subset by summed score."""
@@ -336,6 +389,37 @@ def pin_identity_activation_exact(O):
     assert np.array_equal(ref.out[0], expect), (ref.out[0][:8], expect[:8])
 
 
+def pin_hand_nvfp4_layer(O):
+    """The hand-worked NVFP4 layer: one h tensor scale over every routed h row of the call,
+    and the bf16 shared expert fed the unquantised x (closed form in the fixture)."""
+    layer, x = hand_nvfp4_layer(O)
+    ref = layer.forward(x, activation="identity")
+    assert sorted(ref.ids[0].tolist()) == [0, 1]
+    ts_x = float(np.float32(6.0) / np.float32(2688.0))
+    r = 448.0 * ts_x
+    ts_h = float(np.float32(np.float32(8.0 * r * r) / np.float32(2688.0)))
+    h0_q, h1_q = 6.0 * 448.0 * ts_h, 6.0 * 256.0 * ts_h
+    s0, s1 = sigmoid_scalar(0.25), sigmoid_scalar(-1.0)
+    w0, w1 = s0 / (s0 + s1) * 2.5, s1 / (s0 + s1) * 2.5
+    expect = np.zeros(32)
+    expect[0] = w0 * h0_q + w1 * 0.5 * h1_q
+    expect[3] = w0 * -0.5 * h0_q
+    expect[5] = w1 * 2.0 * h1_q
+    expect[7] = 0.30078125 * 2.0
+    assert np.allclose(ref.out[0], expect, rtol=1e-12, atol=1e-15), (ref.out[0][:8], expect[:8])
+
+
+def pin_widen_bf16(O):
+    """Every bf16 bit pattern widens to the value torch's bfloat16 -> float64 gives."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):
+        got = O.widen_bf16(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+
+
 def pin_layer_invariants(O, spec, arrays, x):
     """Token permutation commutes with the layer; the routing weights sum to rsf;
     doubling every routed W_d scale doubles the routed part of the output."""
@@ -357,4 +441,5 @@ def pin_layer_invariants(O, spec, arrays, x):
 ALL_PINS = [pin_decode_int4, pin_decode_e4m3, pin_decode_e2m1, pin_dequant_int4_g32,
             pin_dequant_nvfp4, pin_nvfp4_rounding, pin_nvfp4_activation, pin_select_brute_force,
             pin_select_special_cases, pin_routing_weights, pin_group_tokens,
-            pin_expert_ffn_torch, pin_hand_two_expert, pin_identity_activation_exact]
+            pin_expert_ffn_torch, pin_hand_two_expert, pin_identity_activation_exact,
+            pin_hand_nvfp4_layer, pin_widen_bf16]

@@ -125,6 +125,20 @@ def _act_scale_no6(a):
     return _orig["quantize_nvfp4_activation"](a32 * np.float32(6.0)) / 6.0 * 1.0001
 
 
+def _h_scale_per_expert(hs):
+    # each routed expert's h rows quantised with a tensor scale of their own
+    return {e: (ent, _orig["quantize_nvfp4_activation"](np.asarray(h, np.float32))) for e, (ent, h) in hs.items()}
+
+
+def _shared_reads_quantised_x(shared_format, x64, x_in):
+    return x_in
+
+
+def _widen_bf16_truncating(bits):
+    # drops the lowest mantissa bit of every pattern
+    return _orig["widen_bf16"](np.asarray(bits, np.uint16) & np.uint16(0xFFFE))
+
+
 MUTANTS = {
     "decode_int4/nibbles_swapped": ("decode_int4", _nibbles_swapped),
     "decode_int4/unsigned": ("decode_int4", _unsigned_int4),
@@ -143,6 +157,9 @@ MUTANTS = {
     "weights/unnormalised": ("routing_weights", _weights_unnormalised),
     "group/descending": ("group_tokens", _group_descending),
     "nvfp4_act/scale": ("quantize_nvfp4_activation", _act_scale_no6),
+    "nvfp4_layer/h_scale_per_expert": ("quantize_routed_h", _h_scale_per_expert),
+    "nvfp4_layer/shared_reads_quantised_x": ("shared_expert_input", _shared_reads_quantised_x),
+    "widen_bf16/truncating": ("widen_bf16", _widen_bf16_truncating),
 }
 
 
