@@ -206,6 +206,20 @@ moe_status moe_layer_set_trace(moe_layer* layer, void* buffer, int32_t n_ctas);
 moe_status moe_layer_launch_count(moe_layer* layer, int64_t* count);
 
 /*
+ * Failure-handling hook. Every device-side wait on work of other CTAs (the fused decode
+ * kernel's router-row and gate/up completion counters; the grouped GEMM's pipeline waits)
+ * gives up after `ns` nanoseconds (default 2e9), sets MOE_ERR_TIMEOUT in the layer's status
+ * word, lets the copies and tensor-core operations it issued land, frees its tensor memory
+ * and returns; the forward's output is then undefined. ns = 0 makes every such wait that is
+ * not already satisfied give up at once, which exercises that path without a GPU fault.
+ * ns < 0 is MOE_ERR_INVALID_ARG. Later forwards start from a clean state.
+ */
+moe_status moe_layer_set_wait_limit(moe_layer* layer, int64_t ns);
+
+/* Clear the sticky device status word (enqueued on `stream`). */
+moe_status moe_layer_reset_status(moe_layer* layer, void* stream);
+
+/*
  * Routing without any allocation. The pages have no counterpart to this entry point: it
  * exists for callers that cannot call cudaMalloc when they need routing (code running
  * while a stream is captured into a CUDA graph, where allocation is not capturable; hosts

@@ -66,6 +66,8 @@ SYMBOLS = {
     "moe_layer_stage_times": (_I, [_P, _P, _P]),
     "moe_layer_launch_count": (_I, [_P, _P]),
     "moe_layer_set_trace": (_I, [_P, _P, _I]),
+    "moe_layer_set_wait_limit": (_I, [_P, ctypes.c_int64]),
+    "moe_layer_reset_status": (_I, [_P, _P]),
     "moe_route_noalloc": (_I, [_P, _I, _I, _I, _P, _I, _P, _I, _I, _I, _I, ctypes.c_float,
                                _P, _P, _P, _P, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -227,6 +229,14 @@ class MoeLayer:
 
     def status(self) -> int:
         return _get_lib().moe_layer_status(self._h)
+
+    def set_wait_limit(self, ns: int):
+        """Time limit (ns) of the kernels' waits on other CTAs (failure-handling hook)."""
+        _check("moe_layer_set_wait_limit", _get_lib().moe_layer_set_wait_limit(self._h, int(ns)))
+
+    def reset_status(self, stream=None):
+        """Clear the sticky device status word."""
+        _check("moe_layer_reset_status", _get_lib().moe_layer_reset_status(self._h, _stream(stream)))
 
     def close(self):
         if getattr(self, "_h", None) is not None and self._h.value:

@@ -1,43 +1,46 @@
-// Fused decode-path kernel of the MoE layer (T <= 8 tokens per call), plus the weight repack
-// it reads.
+// Fused decode-path kernel of the MoE layer (T <= 8 tokens per call) on the tcgen05 tensor
+// cores, with the dequantised weights staged in tensor memory.
 //
 // One persistent cooperative grid (one CTA per SM) runs the whole layer forward of a decode
 // step: router logits, noaux_tc selection and batch-union grouping, the SwiGLU gate/up
-// projection of the shared and the selected experts, and the down projection fused with the
+// projection of the shared and the selected experts, and the down projection with the
 // weighted combine ("Show HN: Menjalankan GLM 5.2 di komputer lambat", section "Fitur utama
 // yang diimplementasikan": DeepSeek-V3-style router with noaux_tc, routed_scaling_factor and
 // a shared expert; packed int4 with dequant-on-use; batch-union MoE). Every selected expert's
 // weights are streamed from HBM exactly once.
 //
-// Weights are repacked at layer creation into 16-row tiles in the register-fragment order of
-// the m16n8k16 fp16 MMA. One 32-bit word holds the 8 int4 codes a lane needs for one MMA;
-// a shift and four LOP3s turn it into the four fp16 A registers: (code + 8) is placed in the
-// mantissa of 1024.0 (rows 0-7: value 1032 + c) or at mantissa bit 4 (rows 8-15: value
-// 1152 + 16c). The MMA accumulates in fp32; the per-row bias (1032 or 1152 times the group's
-// activation sum) is removed and the fp16 group scale applied once per 32-element group.
-// Column layout of the MMA's B operand:
-//   MODE 1 (one token): column n of MMA m holds the token's values of group (m/2) mod 8, so the
-//     8 groups of a 256-column k-block land in 8 accumulator columns; the operand is built in
-//     registers from a compact fp16 copy of the activation (the other columns are zero);
-//   MODE 0 (2..8 tokens): column n holds token n, from a fragment-ordered activation panel.
+// Weights are read from the packed store of the grouped GEMM: per (expert, 128-row tile,
+// 256-column group) one 18 KB item (codes, then fp16 scales). Gate/up tiles pair 16 gate rows
+// with the matching 16 up rows in each 32-row quarter.
 //
-// Work per CTA, in order, each item a 16-row x 2048-column panel (18 KB) brought in by the
-// producer warp with TMA bulk copies into a ring of slots:
-//   consumers: activations staged; router rows e = cta, cta + grid (unrolled vector loads)
-//   A  shared-expert gate/up tiles           (no dependency)
-//   C1 shared-expert down tiles              (waits until every shared gate/up tile is done)
-//   B  selected experts' gate/up tiles       (waits for the routing, in shared memory)
-//   C2 selected experts' down tiles          (waits until that expert's gate/up tiles are done)
-// Warps: 8 consumers, 1 producer (TMA bulk copies), 1 routing warp. Once a CTA's router
-// rows are written, its routing warp waits until every CTA has written its rows, selects
-// each token's experts (one warp per token, in turn) and groups the entries, while the
-// consumers already run the shared expert (A, C1). Every CTA obtains the same routing from
-// the same logits (CTA 0 also writes it out). The producer issues the shared-expert items
-// first and the routed items once the routing warp publishes the routing.
-// Down tiles add w * y into an fp32 accumulator with atomics; the last CTA to finish its
-// down tiles (a ticket counter) converts the whole output to the output type. All
-// inter-CTA waits are bounded; on time-out the kernel records MOE_ERR_TIMEOUT, drains its
-// own copies in flight and returns.
+// A unit of work is (expert, 128-row tile, K split); each CTA walks its share of four
+// segments in order: shared gate/up, routed gate/up (after the routing is known), shared
+// down, routed down. Warp roles:
+//   warp 12     producer: one TMA bulk copy per item into a ring of shared-memory slots;
+// (segment order: shared gate/up, routed gate/up, shared down, routed down)
+//   warps 4-11  decoders: every item is split over the 8 warps (row quarter = warp mod 4,
+//               column half = the warp's half of the group); a thread turns its row's 128
+//               int4 codes into fp16 (code times the fp16 group scale, rounded once) and
+//               stores them to tensor memory (a ring of three 128-column A slots);
+//   warp 13     lane 0 issues tcgen05.mma kind::f16 (M=128 weight rows with A read from
+//               tensor memory, N=16 columns: the tokens, K=16) into one of two accumulators;
+//   warp 15     stages the h rows each down unit multiplies into one of two shared-memory
+//               panels, once all gate/up tiles of that expert are done;
+//   warps 0-11  router rows at the start;
+//   warps 0-3   then the epilogue of each unit: the accumulator
+//               rows go to a K-split partial buffer; the last split of a gate/up tile to
+//               arrive computes h = SiLU(gate) * up (fp16); the last unit of a 128-row block
+//               of the output to arrive computes out = sum_j w_j y_j + y_shared in a fixed
+//               order (the combine is deterministic);
+//   warps 0-3   routing, between the router rows and the first epilogue: once every CTA's
+//               router rows are written, block-parallel selection of each token's experts
+//               and grouping of the entries (every CTA gets the same result);
+//   warp 14     spare.
+// The activations (B operand) live in shared memory as [K/8][T][8] fp16 panels: an 8 x 16 B
+// core matrix starting at a chunk holds the T tokens of that chunk in its first T rows (the
+// other rows read the next chunk; those accumulator columns are ignored).
+// All waits are bounded; on time-out the kernel records MOE_ERR_TIMEOUT, stops issuing work,
+// lets its copies and MMAs in flight land, frees its tensor memory and returns.
 #include <cstddef>
 
 #include "kernels.h"
@@ -48,128 +51,183 @@ namespace moe {
 
 namespace {
 
-constexpr int kDecThreads = 320;      // 8 consumer warps, 1 producer warp, 1 routing warp
-constexpr int kConsumers = 256;
-constexpr int kPanelK = 2048;          // columns per item
-constexpr int kCodeBytes = 16384;      // 16 rows x 2048 int4
-constexpr int kScaleBytes = 2048;      // 16 rows x 64 groups fp16
-constexpr int kItemBytes = kCodeBytes + kScaleBytes;
-constexpr int kMaxH = 6144;
-constexpr int kMaxI = 2048;
+constexpr int kEpiWarps = 4;           // warps 0-3
+constexpr int kDecWarp0 = 4;           // warps 4-11
+constexpr int kWarpProd = 12;
+constexpr int kWarpMma = 13;
+constexpr int kWarpRoute = 14;
+constexpr int kWarpStage = 15;
+constexpr int kWorkWarps = 12;         // warps 0-11 share the router rows
+constexpr int kDecThreads = 16 * 32;
+constexpr int kTileM = 128;            // weight rows per unit (MMA M)
+constexpr int kGroupK = 256;           // K columns per item
+constexpr int kItemCodes = 16384;      // 128 rows x 256 int4
+constexpr int kItemBytes = 18432;      // + 128 rows x 8 fp16 scales
+constexpr int kASlots = 3;             // tensor-memory A slots of 128 columns
+constexpr int kDCol0 = kASlots * 128;  // two 16-column accumulators after the A slots
+constexpr int kN = 16;                 // MMA N (tokens; T <= 8 columns used)
+constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxT = 8;
+constexpr int kMaxH = 8192;
+constexpr int kMaxI = 4096;
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 16;
 constexpr int kMaxActive = 64;         // T * top_k <= 64 on this path
-constexpr uint32_t kMbarSpin = 1u << 22;
+constexpr int kMaxSlots = 12;          // shared-memory ring slots
+constexpr int kMaxKsu = 8;             // K splits of a gate/up tile
+constexpr int kMaxKsd = 4;             // K splits of a down tile
+constexpr int kPanelPad = 512;         // bytes after a panel that the last core matrices may touch
+constexpr int kSmemLimit = 227 * 1024;
 
-// Shared memory common to both modes (16-byte aligned: the reduction buffer takes float4
-// stores).
-struct alignas(16) DecCommon {
-  float red[2][8][32][8];              // cross-warp reduction (double-buffered per unit)
+// Fixed part of the shared memory (the ring and the panels follow at runtime offsets).
+struct alignas(16) DecFixed {
   float selb[kMaxE];                   // selection scratch: biased and unbiased scores of one token
   float sels[kMaxE];
-  int idsel[8][kMaxK];                 // per token: selected experts and weights
-  float wsel[8][kMaxK];
+  int idsel[kMaxT][kMaxK];             // per token: selected experts and weights (slot order)
+  float wsel[kMaxT][kMaxK];
   int cnt[kMaxE];
   int soff[kMaxE];
   int aslot[kMaxE];
-  int active[kMaxE];
-  int meta_pair[kMaxActive][8];        // per active expert: h row of token n (-1: not routed)
-  float meta_w[kMaxActive][8];         // per active expert: combine weight of token n
-  int colpair[8];
-  float colw[8];
+  int active[kMaxE];                   // active expert a (routed units use slot 1 + a)
+  int meta_j[kMaxActive][kMaxT];       // per active expert and token: selection slot (-1 none)
+  float red[kWorkWarps][2][kMaxT];     // router-row reduction
+  // one-token mode (CUDA-core dot products): unit results handed to the epilogue, the half
+  // sums of a unit, and per 32-column group the sums of the activation values that meet
+  // the 1032 + c and the 1152 + 16 c decoded forms (x, and the two h panels)
+  float gscore[32];                    // block selection: group scores, kept flags, picks
+  int gkept[32];
+  int pick[kMaxK];
+  float dsm[2][2][kTileM];             // [accumulator buffer][column half][row]
+  float xsum[kMaxH / 32][2];
+  float hsum[2][kMaxI / 32][2];
+  uint64_t full[kMaxSlots];
+  uint64_t empty[kMaxSlots];
+  uint64_t afull[kASlots];
+  uint64_t aempty[kASlots];
+  uint64_t dfull[2];
+  uint64_t dempty[2];
+  uint64_t hfree[2];
+  uint64_t hready[2];
+  uint64_t route_bar;
+  uint64_t router_bar;
+
+  uint64_t fin_bar;
+  uint32_t tmem_base;
   int n_active;
-  int flag;
   int abort;
   int issued;
   int consumed;
+  int flag;      // epilogue: this unit arrived last
+  int ep_stop;   // epilogue: uniform stop decision
+  int ep_nact;   // epilogue: active experts, read once by thread 0
 };
 
-template <int MODE>
-struct DecSmem;
-
-template <>
-struct DecSmem<1> {
-  static constexpr int kSlots = 8;
-  uint8_t slots[kSlots][kItemBytes];
-  uint32_t xs[kMaxH / 2];              // compact fp16 pairs of the token's activation
-  uint32_t hs[kMaxI / 2];              // compact fp16 pairs of the current h row
-  float xsums[kMaxH / 32];             // per 32-element group: sum of the fp16 values
-  float hsums[kMaxI / 32];
-  uint64_t full[kSlots];
-  uint64_t empty[kSlots];
-  uint64_t route_bar;
-  uint64_t router_bar;
-  DecCommon c;
+struct DecodeArgs {
+  const void* x;
+  int T;
+  const void* router_w;
+  const float* bias;
+  int H, I, E, top_k, n_group, topk_group;
+  float rsf;
+  const uint8_t* pack_up;      // [E+1][I/64 tiles][H/256 groups][18432]
+  const uint8_t* pack_dn;      // [E+1][H/128 tiles][I/256 groups][18432]
+  float* logits;               // [T, E]
+  int32_t* ids;
+  float* weights;
+  int32_t* offsets;
+  int32_t* entries;
+  __half* h16;                 // [(1 + active) * T][I]: h of slot s, token t at row s * T + t
+  float* gu_part;              // gate/up K-split partials [slot][tile][split][T][128]
+  float* y_part;               // down K-split outputs [T][top_k + 1][split][H]
+  void* out;
+  uint32_t* sync;              // [0] CTAs done with router rows, [2] CTAs exited; up_done, up_cnt, dn_cnt
+  int* status;
+  unsigned long long wait_ns;  // time limit of the waits on other CTAs
+  unsigned long long* trace;   // optional [grid][64] phase timestamps (ns), or NULL
+  int ns;                      // ring slots
+  int off_ring, off_x, off_h0, off_h1;   // shared-memory offsets
+  int ksu, ksd;                // K splits of gate/up and down units
 };
 
-template <>
-struct DecSmem<0> {
-  static constexpr int kSlots = 3;
-  uint8_t slots[kSlots][kItemBytes];
-  uint2 xpanel[kMaxH / 16 * 32];       // B fragments of x: 8 bytes per lane per MMA
-  uint2 hpanel[kMaxI / 16 * 32];       // B fragments of h
-  float xsums[kMaxH / 32 * 8];         // per group and column: sum of the fp16 values
-  float hsums[kMaxI / 32 * 8];
-  uint64_t full[kSlots];
-  uint64_t empty[kSlots];
-  uint64_t route_bar;
-  uint64_t router_bar;
-  DecCommon c;
-};
-
-static_assert(offsetof(DecSmem<1>, c) % 16 == 0 && offsetof(DecSmem<0>, c) % 16 == 0,
-              "vector stores into the common block need 16-byte alignment");
-static_assert(offsetof(DecSmem<1>, xs) % 16 == 0 && offsetof(DecSmem<1>, hs) % 16 == 0,
-              "vector accesses into the staged activations need 16-byte alignment");
-static_assert(offsetof(DecSmem<0>, xsums) % 8 == 0 && offsetof(DecSmem<1>, xsums) % 8 == 0 &&
-                  offsetof(DecSmem<0>, hsums) % 8 == 0 && offsetof(DecSmem<1>, hsums) % 8 == 0,
-              "float2 reads of the group sums need 8-byte alignment");
-static_assert(sizeof(DecSmem<1>) <= 227 * 1024, "decode kernel shared memory over the per-CTA limit");
-static_assert(sizeof(DecSmem<0>) <= 227 * 1024, "decode kernel shared memory over the per-CTA limit");
+// Sync-word layout: [0] CTAs done with router rows, [2] CTAs exited, [3] set when a CTA
+// aborted, [4] selection published; then per-slot gate/up tiles done, per (slot, tile)
+// K-split arrivals, per 128-row block down arrivals, and the published selection.
+constexpr int kSyncUpDone = 8;                          // [1 + kMaxActive] tiles done per slot
+constexpr int kSyncUpCnt = kSyncUpDone + 1 + kMaxActive;   // [(1 + kMaxActive) * NTu] split arrivals
+__host__ __device__ inline int sync_dn_cnt(int ntu) { return kSyncUpCnt + (1 + kMaxActive) * ntu; }
+// published selection: [kMaxT * kMaxK] expert ids, then as many weights (fp32 bits)
+__host__ __device__ inline int sync_route(int ntu) { return sync_dn_cnt(ntu) + kMaxH / kTileM; }
 
 // ------------------------------------------------------------------ helpers
 
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
 }
 
-__device__ __forceinline__ float2 half2_to_float2(uint32_t u) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&u));
-}
-
-// Elementwise fp16x2 product of two registers (round to nearest).
-__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-// One word of codes -> the four fp16 A registers of an m16n8k16 MMA (see file comment).
-__device__ __forceinline__ void decode_word(uint32_t w, uint32_t (&a)[4]) {
+// One word of packed codes (column 8j + 2i in bits 4i..4i+3, 8j + 2i + 1 in bits 16+4i..)
+// -> four fp16x2 (columns 8j..8j+7 in order) of code * scale. (nibble ^ 8) placed in the
+// mantissa of 1024 is 1032 + code; placed at mantissa bit 4 it is 1152 + 16 code. Both are
+// turned into the code exactly (a subtraction, or x 1/16 - 72 in one fused step); the
+// product with the scale is rounded once.
+__device__ __forceinline__ void dq_word(uint32_t w, __half2 s2, uint32_t* o) {
+  const __half2 k1032 = __float2half2_rn(1032.f);
+  const __half2 k16 = __float2half2_rn(0.0625f);
+  const __half2 km72 = __float2half2_rn(-72.f);
   const uint32_t w2 = w >> 8;
-  a[0] = (w & 0x000F000Fu) ^ 0x64086408u;
-  a[1] = (w & 0x00F000F0u) ^ 0x64806480u;
-  a[2] = (w2 & 0x000F000Fu) ^ 0x64086408u;
-  a[3] = (w2 & 0x00F000F0u) ^ 0x64806480u;
+  const uint32_t p0 = (w & 0x000F000Fu) ^ 0x64086408u;
+  const uint32_t p1 = (w & 0x00F000F0u) ^ 0x64806480u;
+  const uint32_t p2 = (w2 & 0x000F000Fu) ^ 0x64086408u;
+  const uint32_t p3 = (w2 & 0x00F000F0u) ^ 0x64806480u;
+  o[0] = h2u(__hmul2(__hsub2(u2h(p0), k1032), s2));
+  o[1] = h2u(__hmul2(__hfma2(u2h(p1), k16, km72), s2));
+  o[2] = h2u(__hmul2(__hsub2(u2h(p2), k1032), s2));
+  o[3] = h2u(__hmul2(__hfma2(u2h(p3), k16, km72), s2));
 }
 
-// Bounded wait for *p >= target (one thread). Returns false on time-out.
-__device__ __forceinline__ bool wait_geq(const uint32_t* p, uint32_t target, uint32_t spin_max) {
-  for (uint32_t i = 0; i < spin_max; ++i) {
-    if (ptx::ld_acquire(p) >= target) return true;
-    __nanosleep(64);
+// acc + (fp16 half of a) * (fp16 half of x) with one fp32 rounding (the product is exact).
+__device__ __forceinline__ float fma_f16f32(uint32_t a, uint32_t x, float acc, bool hi) {
+  const unsigned short ah = hi ? (unsigned short)(a >> 16) : (unsigned short)(a & 0xFFFFu);
+  const unsigned short xh = hi ? (unsigned short)(x >> 16) : (unsigned short)(x & 0xFFFFu);
+  asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc) : "h"(ah), "h"(xh));
+  return acc;
+}
+
+// Time limit of the waits inside a CTA (mbarrier phases) and of the final drains.
+constexpr unsigned long long kLocalWaitNs = 2000000000ull;
+
+// Wait for an mbarrier phase; false when the CTA's abort flag is set or after limit_ns.
+// (try_wait itself may suspend the thread for a while, so the bound is a time, not a count.)
+__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity, const int* abort_flag,
+                                         unsigned long long limit_ns) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (abort_flag && *(volatile const int*)abort_flag) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
-  return false;
 }
 
-struct Geo {
-  int T, H, I, E, k;
-  int NTu, Pu, NTd, Pd;   // tiles and panels per tile: up (gate/up) and down
-  int G, c;
-};
+// Wait for *p >= target, written by other CTAs (each calling thread polls with acquire
+// loads); false when the abort flag is set or after limit_ns.
+__device__ __forceinline__ bool geq_wait(const uint32_t* p, uint32_t target, const int* abort_flag,
+                                         unsigned long long limit_ns) {
+  if (ptx::ld_acquire(p) >= target) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    __nanosleep(128);
+    if (ptx::ld_acquire(p) >= target) return true;
+    if (*(volatile const int*)abort_flag) return false;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
 
-// Item ranges of this CTA (balanced contiguous split of each segment over the grid).
+// Balanced contiguous split of n units over G CTAs.
 __device__ __forceinline__ void seg_range(int n, int G, int c, int& b, int& e) {
   b = (int)(((long)n * c) / G);
   e = (int)(((long)n * (c + 1)) / G);
@@ -193,478 +251,72 @@ __device__ __forceinline__ void load_act8(const void* x, size_t idx, float (&v)[
   }
 }
 
-// Sum of the fp16 values held by 4 half2 words.
-__device__ __forceinline__ float sum4h2(const uint32_t (&p)[4]) {
-  float s = 0.f;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float2 f = half2_to_float2(p[q]);
-    s += f.x + f.y;
-  }
-  return s;
-}
-
-// ------------------------------------------------------------- activation staging
-
-// MODE 1: compact fp16 pairs of token 0 and the per-group sums (thread per 32-element group).
-template <int XDT>
-__device__ void stage_x1(DecSmem<1>& S, const void* x, int H) {
-  for (int j = threadIdx.x; j < H / 32; j += kConsumers) {
-    float s = 0.f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float v[8];
-      load_act8<XDT>(x, (size_t)32 * j + 8 * q, v);
-      uint32_t p[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) p[i] = pack_half2(v[2 * i], v[2 * i + 1]);
-      s += sum4h2(p);
-      *reinterpret_cast<uint4*>(&S.xs[16 * j + 4 * q]) = make_uint4(p[0], p[1], p[2], p[3]);
-    }
-    S.xsums[j] = s;
-  }
-}
-
-// MODE 0: fragment panel (column n = token n, zero for n >= T) and per-(group, token) sums.
-// Element pair (k, k+1), k = 16 m + r, goes to lane (token, (r mod 8) / 2), half r / 8.
-template <int XDT>
-__device__ void stage_x0(DecSmem<0>& S, const void* x, int T, int H) {
-  const int ng = H / 32;
-  for (int idx = threadIdx.x; idx < ng * 8; idx += kConsumers) {
-    const int j = idx >> 3, tok = idx & 7;
-    float s = 0.f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {   // 8 elements 32 j + 8 q ..: MMA m = 2 j + q / 2, half q & 1
-      uint32_t p[4] = {0u, 0u, 0u, 0u};
-      if (tok < T) {
-        float v[8];
-        load_act8<XDT>(x, (size_t)tok * H + 32 * j + 8 * q, v);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) p[i] = pack_half2(v[2 * i], v[2 * i + 1]);
-        s += sum4h2(p);
-      }
-      const int m = 2 * j + (q >> 1);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t* e = reinterpret_cast<uint32_t*>(&S.xpanel[m * 32 + tok * 4 + i]);
-        e[q & 1] = p[i];
-      }
-    }
-    S.xsums[idx] = s;   // [group j][column tok]
-  }
-}
-
-// h rows of the current expert (rows S.c.colpair, written by other CTAs: read through L2).
-__device__ void stage_h1(DecSmem<1>& S, const __half* h16, int I) {
-  const int row = S.c.colpair[0];
-  for (int i = threadIdx.x; i < I / 8; i += kConsumers) {
-    uint4 u = make_uint4(0u, 0u, 0u, 0u);
-    if (row >= 0) u = __ldcg(reinterpret_cast<const uint4*>(h16 + (size_t)row * I) + i);
-    *reinterpret_cast<uint4*>(&S.hs[4 * i]) = u;
-  }
-  ptx::bar_sync(1, kConsumers);
-  for (int j = threadIdx.x; j < I / 32; j += kConsumers) {
-    float s = 0.f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 u = *reinterpret_cast<const uint4*>(&S.hs[16 * j + 4 * q]);
-      const uint32_t p[4] = {u.x, u.y, u.z, u.w};
-      s += sum4h2(p);
-    }
-    S.hsums[j] = s;
-  }
-}
-
-__device__ void stage_h0(DecSmem<0>& S, const __half* h16, int I) {
-  const int ng = I / 32;
-  for (int idx = threadIdx.x; idx < ng * 8; idx += kConsumers) {
-    const int j = idx >> 3, col = idx & 7;
-    const int row = S.c.colpair[col];
-    float s = 0.f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t p[4] = {0u, 0u, 0u, 0u};
-      if (row >= 0) {
-        const uint4 u = __ldcg(reinterpret_cast<const uint4*>(h16 + (size_t)row * I + 32 * j + 8 * q));
-        p[0] = u.x; p[1] = u.y; p[2] = u.z; p[3] = u.w;
-        s += sum4h2(p);
-      }
-      const int m = 2 * j + (q >> 1);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t* e = reinterpret_cast<uint32_t*>(&S.hpanel[m * 32 + col * 4 + i]);
-        e[q & 1] = p[i];
-      }
-    }
-    S.hsums[idx] = s;
-  }
-}
-
-// ------------------------------------------------------- consumer: compute
-
-// One item (16 rows x 2048 columns): warp `w` handles k-block w (256 columns = 16 MMAs).
-// m_base = global MMA index of the panel start (p * 128). kb = global k-block index.
-// MODE 1: `act` = compact fp16 pairs; lane group g holds the operand of MMAs 2g, 2g+1 only.
-// Four independent accumulator chains keep the MMA pipe busy.
-__device__ __forceinline__ void compute_item1(const uint32_t* act, const float* sums, const uint8_t* slot,
-                                              int m_base, int kb, float (&acc)[4]) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const uint8_t* codes = slot + ((size_t)(4 * w) * 32 + lane) * 16;
-  const uint8_t* scl = slot + kCodeBytes + (w * 8 + g) * 32;
-  const uint32_t* xb = act + 8 * (m_base + 16 * w + 2 * g) + t;
-  const uint32_t b00 = xb[0], b01 = xb[4], b10 = xb[8], b11 = xb[12];
-  // the B operand of MMA mi is the lane's x values when its group column is this lane
-  // group's (mi / 2 == g), else zero: an fp16 multiply by 1 or 0 (exact) on the FMA pipe,
-  // which leaves the ALU pipe to the int4 decode
-  uint32_t msk[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) msk[j] = j == g ? 0x3C003C00u : 0u;
-  float d[4][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
-#pragma unroll
-  for (int cc = 0; cc < 4; ++cc) {
-    const uint4 q = *reinterpret_cast<const uint4*>(codes + cc * 32 * 16);
-    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int mi = 4 * cc + i;           // MMA within the k-block; active lane group mi / 2
-      uint32_t a[4];
-      decode_word(words[i], a);
-      const uint32_t bx = hmul2_bits((mi & 1) ? b10 : b00, msk[mi >> 1]);
-      const uint32_t by = hmul2_bits((mi & 1) ? b11 : b01, msk[mi >> 1]);
-      ptx::mma_16816(d[i], a, bx, by, d[i]);
-    }
-  }
-  float dd[4];
-#pragma unroll
-  for (int r = 0; r < 4; ++r) dd[r] = (d[0][r] + d[1][r]) + (d[2][r] + d[3][r]);
-  const uint2 sraw = *reinterpret_cast<const uint2*>(scl + t * 8);
-  const float2 sg = half2_to_float2(sraw.x);   // s[g][j0], s[g][j0+1]
-  const float2 su = half2_to_float2(sraw.y);   // s[g+8][j0], s[g+8][j0+1]
-  const float2 X = *reinterpret_cast<const float2*>(sums + 8 * kb + 2 * t);
-  acc[0] = fmaf(sg.x, fmaf(-1032.f, X.x, dd[0]), acc[0]);
-  acc[0] = fmaf(sg.y, fmaf(-1032.f, X.y, dd[1]), acc[0]);
-  acc[1] = fmaf(su.x, fmaf(-1152.f, X.x, dd[2]), acc[1]);
-  acc[1] = fmaf(su.y, fmaf(-1152.f, X.y, dd[3]), acc[1]);
-}
-
-// MODE 0: B fragments from the panel; each group's two MMAs form an independent chain.
-__device__ __forceinline__ void compute_item0(const uint2* panel, const float* sums, const uint8_t* slot,
-                                              int m_base, int kb, float (&acc)[4]) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int gq = lane >> 2, t = lane & 3;
-  const uint8_t* codes = slot + ((size_t)(4 * w) * 32 + lane) * 16;
-  const uint8_t* scl = slot + kCodeBytes + (w * 8 + gq) * 32;
-  const uint2* bp = panel + (size_t)(m_base + 16 * w) * 32 + lane;
-  const uint4 s0 = *reinterpret_cast<const uint4*>(scl);
-  const uint4 s1 = *reinterpret_cast<const uint4*>(scl + 16);
-  const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-  for (int cc = 0; cc < 4; ++cc) {
-    const uint4 q = *reinterpret_cast<const uint4*>(codes + cc * 32 * 16);
-    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int gi = 0; gi < 2; ++gi) {
-      const int jl = 2 * cc + gi;   // group within the k-block
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        uint32_t a[4];
-        decode_word(words[2 * gi + i], a);
-        const uint2 b = bp[(4 * cc + 2 * gi + i) * 32];
-        ptx::mma_16816(d, a, b.x, b.y, d);
-      }
-      // scale words per (k-block, row g): [t'][s[g][2t'], s[g][2t'+1], s[g+8][2t'], s[g+8][2t'+1]]
-      const float2 sgp = half2_to_float2(sw[2 * (jl >> 1)]);
-      const float2 sup = half2_to_float2(sw[2 * (jl >> 1) + 1]);
-      const float sgate = (jl & 1) ? sgp.y : sgp.x;
-      const float sup1 = (jl & 1) ? sup.y : sup.x;
-      const float2 X = *reinterpret_cast<const float2*>(sums + (8 * kb + jl) * 8 + 2 * t);
-      acc[0] = fmaf(sgate, fmaf(-1032.f, X.x, d[0]), acc[0]);
-      acc[1] = fmaf(sgate, fmaf(-1032.f, X.y, d[1]), acc[1]);
-      acc[2] = fmaf(sup1, fmaf(-1152.f, X.x, d[2]), acc[2]);
-      acc[3] = fmaf(sup1, fmaf(-1152.f, X.y, d[3]), acc[3]);
-    }
-  }
-}
-
-// Cross-warp reduction of the tile accumulators into red (consumers, then named barrier).
-// `half` selects the second 16-row tile of a down pair.
-template <int MODE>
-__device__ __forceinline__ void stash_acc(DecCommon& C, int rb, int half, float (&acc)[4]) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  if (MODE == 1) {
-#pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-      acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
-      acc[1] += __shfl_xor_sync(0xffffffffu, acc[1], o);
-    }
-    if ((lane & 3) == 0) {
-      C.red[rb][w][lane >> 2][2 * half] = acc[0];
-      C.red[rb][w][lane >> 2][2 * half + 1] = acc[1];
-    }
-  } else {
-    *reinterpret_cast<float4*>(&C.red[rb][w][lane][4 * half]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  }
-}
-
-// Value of MMA row r (0..15) for column n after the reduction (rows 8..15 carry a x16 unit).
-template <int MODE>
-__device__ __forceinline__ float reduced(const DecCommon& C, int rb, int half, int r, int n) {
-  float v = 0.f;
-  if (MODE == 1) {
-#pragma unroll
-    for (int w = 0; w < 8; ++w) v += C.red[rb][w][r & 7][2 * half + (r >> 3)];
-  } else {
-    const int ln = (r & 7) * 4 + (n >> 1);
-    const int idx = 4 * half + (r >> 3) * 2 + (n & 1);
-#pragma unroll
-    for (int w = 0; w < 8; ++w) v += C.red[rb][w][ln][idx];
-  }
-  return (r >= 8) ? v * 0.0625f : v;
-}
-
 // ------------------------------------------------------------------ selection
 
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Order key of (biased score v, expert e): larger v first, lower e on ties. The float's
-// bits are mapped to an unsigned integer with the same order (v = -0 does not occur: a
-// sigmoid in (0, 1) plus a bias never rounds to -0); the low word is ~e.
-__device__ __forceinline__ unsigned long long sel_key(float v, int e) {
-  const uint32_t u = __float_as_uint(v);
-  const uint32_t k = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
-  return ((unsigned long long)k << 32) | (uint32_t)~e;
-}
-
-// Bitonic clean-up of an 8-key bitonic sequence into descending order.
-__device__ __forceinline__ void bitonic_merge8(unsigned long long (&K)[8]) {
-#pragma unroll
-  for (int j = 4; j > 0; j >>= 1)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int l = i ^ j;
-      if (l > i && K[i] < K[l]) {
-        const unsigned long long t = K[i];
-        K[i] = K[l];
-        K[l] = t;
-      }
-    }
-}
-
-// One warp: noaux_tc selection of one token with the same result as the sequential picks,
-// bit for bit. Each group's score adds its two largest biased scores; the topk_group best
-// groups are kept (lower index on ties); the top_k kept experts in the order "larger biased
-// score first, lower index on ties" fill the slots; the weights' normaliser adds the picked
-// unbiased scores in slot order. Lane l holds experts l*E/32 .. (l+1)*E/32 - 1.
-// Fast path (n_group divides 32, top_k <= 8): groups are whole runs of lanes, group top-2
-// values merge over those lanes, and the top-8 keys come from a per-lane sort followed by
-// five butterfly merges of sorted 8-lists. Otherwise: group scores from shared memory and
-// top_k rounds of a warp argmax.
-__device__ __forceinline__ void select_warp(DecCommon& C, const float* logits_row, const float* bias, int E,
-                                            int n_group, int topk_group, int top_k, float rsf, int* idsel,
-                                            float* wsel) {
-  constexpr int kE = kMaxE / 32;
-  const int lane = threadIdx.x & 31;
-  const int epl = E / 32;
-  float lg[kE], bi_[kE], s[kE], b[kE];
-#pragma unroll
-  for (int j = 0; j < kE; ++j) {   // all loads first, so their latencies overlap
-    lg[j] = bi_[j] = 0.f;
-    if (j < epl) {
-      lg[j] = __ldcg(logits_row + lane * epl + j);
-      bi_[j] = __ldg(bias + lane * epl + j);
-    }
+// noaux_tc selection of one token by the four epilogue warps (128 threads, named barrier 2),
+// with the same result as the sequential picks, bit for bit: s = sigmoid(logit), b = s +
+// bias; a group's score adds its two largest b (a thread scans each group); the
+// topk_group best groups are kept (lower index on ties); an expert of a kept group takes
+// slot r when exactly r kept experts rank above it (larger b first, lower index on ties);
+// the normaliser adds the picked unbiased scores in slot order.
+__device__ void select_block(DecFixed& C, const float* logits_row, const float* bias, int E, int n_group,
+                             int topk_group, int top_k, float rsf, int* idsel, float* wsel) {
+  const int tid = threadIdx.x;
+  for (int e = tid; e < E; e += 128) {
+    const float sc = sigmoidf_acc(__ldcg(logits_row + e));
+    C.sels[e] = sc;
+    C.selb[e] = sc + __ldg(bias + e);
   }
-#pragma unroll
-  for (int j = 0; j < kE; ++j) {
-    s[j] = b[j] = 0.f;
-    if (j < epl) {
-      s[j] = sigmoidf_acc(lg[j]);
-      b[j] = s[j] + bi_[j];
-      C.selb[lane * epl + j] = b[j];
-      C.sels[lane * epl + j] = s[j];
-    }
-  }
-  __syncwarp();
+  ptx::bar_sync(2, 128);
   const int G = E / n_group;
-  int my_e = -1;
-  float my_s = 0.f;
-  if ((32 % n_group) == 0 && top_k <= 8) {
-    // group of lane = lane / lpg; top-2 of the lane's values, then of the group's lanes
-    const int lpg = 32 / n_group;
+  if (tid < n_group) {
     float m1 = -INFINITY, m2 = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kE; ++j) {
-      if (j < epl) {
-        const float v = b[j];
-        if (v > m1) {
-          m2 = m1;
-          m1 = v;
-        } else if (v > m2) {
-          m2 = v;
-        }
+    for (int i = 0; i < G; ++i) {
+      const float v = C.selb[tid * G + i];
+      if (v > m1) {
+        m2 = m1;
+        m1 = v;
+      } else if (v > m2) {
+        m2 = v;
       }
     }
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float o1 = __shfl_xor_sync(0xffffffffu, m1, o), o2 = __shfl_xor_sync(0xffffffffu, m2, o);
-      if (o < lpg) {
-        const float n1 = fmaxf(m1, o1);
-        m2 = fmaxf(fminf(m1, o1), fmaxf(m2, o2));
-        m1 = n1;
-      }
-    }
-    const float gs = m1 + m2;
-    const int gid = lane / lpg;
-    int grank = 0;
-#pragma unroll
-    for (int g2 = 0; g2 < 32; ++g2) {
-      const float w2 = __shfl_sync(0xffffffffu, gs, (g2 * lpg) & 31);
-      if (g2 < n_group) grank += (w2 > gs) || (w2 == gs && g2 < gid);
-    }
-    const bool kept = grank < topk_group;
-    unsigned long long K[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) K[j] = (j < epl && kept) ? sel_key(b[j], lane * epl + j) : 0ull;
-    // sort the lane's 8 keys (descending bitonic network)
-#pragma unroll
-    for (int k2 = 2; k2 <= 8; k2 <<= 1)
-#pragma unroll
-      for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int l = i ^ j2;
-          if (l > i) {
-            const bool desc = (i & k2) == 0 || k2 == 8;
-            if (desc ? (K[i] < K[l]) : (K[i] > K[l])) {
-              const unsigned long long t = K[i];
-              K[i] = K[l];
-              K[l] = t;
-            }
-          }
-        }
-    // top 8 of the union of two sorted lists: max(A[i], B[7-i]) is bitonic, then clean up
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      unsigned long long P[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) P[i] = __shfl_xor_sync(0xffffffffu, K[i], o);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) K[i] = K[i] > P[7 - i] ? K[i] : P[7 - i];
-      bitonic_merge8(K);
-    }
-    unsigned long long mine = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (lane == j) mine = K[j];
-    if (lane < top_k) {
-      my_e = (int)~(uint32_t)mine;
-      my_s = C.sels[my_e];
-    }
-  } else {
-    // group scores: lane gi scans group gi from a lane-dependent start (spreads the banks)
-    float gs = -INFINITY;
-    if (lane < n_group) {
-      float m1 = -INFINITY, m2 = -INFINITY;
-      const float* bg = C.selb + lane * G;
-      int i2 = lane % G;
-      for (int i = 0; i < G; ++i) {
-        const float v = bg[i2];
-        if (++i2 == G) i2 = 0;
-        if (v > m1) {
-          m2 = m1;
-          m1 = v;
-        } else if (v > m2) {
-          m2 = v;
-        }
-      }
-      gs = m1 + m2;
-    }
-    int grank = 0;
+    C.gscore[tid] = m1 + m2;
+  }
+  ptx::bar_sync(2, 128);
+  if (tid < n_group) {
+    const float gs = C.gscore[tid];
+    int rank = 0;
     for (int g2 = 0; g2 < n_group; ++g2) {
-      const float w2 = __shfl_sync(0xffffffffu, gs, g2);
-      grank += (w2 > gs) || (w2 == gs && g2 < lane);
+      const float o = C.gscore[g2];
+      rank += (o > gs) || (o == gs && g2 < tid);
     }
-    const unsigned kept = __ballot_sync(0xffffffffu, lane < n_group && grank < topk_group);
-    unsigned cand = 0;
-#pragma unroll
-    for (int j = 0; j < kE; ++j)
-      if (j < epl && ((kept >> ((lane * epl + j) / G)) & 1u)) cand |= 1u << j;
-    // top_k argmax rounds; lane r keeps the r-th pick
-    for (int r = 0; r < top_k; ++r) {
-      float bv = -INFINITY, bs = 0.f;
-      int bi = E;   // E: none
-#pragma unroll
-      for (int j = 0; j < kE; ++j) {
-        if ((cand >> j) & 1u) {
-          if (bi == E || b[j] > bv) {
-            bv = b[j];
-            bs = s[j];
-            bi = lane * epl + j;
-          }
-        }
-      }
-      const float local_s = bs;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (oi != E && (bi == E || ov > bv || (ov == bv && oi < bi))) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      const int win = bi < E ? bi / epl : 0;
-      const float ws = __shfl_sync(0xffffffffu, local_s, win);
-      if (lane == win && bi < E) cand &= ~(1u << (bi - lane * epl));
-      if (lane == r) {
-        my_e = bi;
-        my_s = ws;
+    C.gkept[tid] = rank < topk_group;
+  }
+  ptx::bar_sync(2, 128);
+  for (int e = tid; e < E; e += 128) {
+    if (!C.gkept[e / G]) continue;
+    const float v = C.selb[e];
+    int rank = 0;
+    for (int g2 = 0; g2 < n_group; ++g2) {
+      if (!C.gkept[g2]) continue;
+      for (int e2 = g2 * G; e2 < (g2 + 1) * G; ++e2) {
+        const float o = C.selb[e2];
+        rank += (o > v) || (o == v && e2 < e);
       }
     }
+    if (rank < top_k) C.pick[rank] = e;
   }
-  float wsum = 0.f;
-  for (int j = 0; j < top_k; ++j) wsum += __shfl_sync(0xffffffffu, my_s, j);
-  if (lane < top_k) {
-    idsel[lane] = my_e;
-    wsel[lane] = my_s / wsum * rsf;
+  ptx::bar_sync(2, 128);
+  if (tid == 0) {
+    float wsum = 0.f;
+    for (int j = 0; j < top_k; ++j) wsum += C.sels[C.pick[j]];
+    for (int j = 0; j < top_k; ++j) {
+      idsel[j] = C.pick[j];
+      wsel[j] = C.sels[C.pick[j]] / wsum * rsf;
+    }
   }
-  __syncwarp();
+  ptx::bar_sync(2, 128);
 }
-
-}  // namespace
-
-struct DecodeArgs {
-  const void* x;
-  int T;
-  const void* router_w;
-  const float* bias;
-  int H, I, E, top_k, n_group, topk_group;
-  float rsf;
-  const uint8_t* up_store;     // [E+1][I/8 tiles][H/2048 panels][18432]
-  const uint8_t* down_store;   // [E+1][H/16 tiles][I/2048 panels][18432]
-  float* logits;               // [T, E]
-  int32_t* ids;
-  float* weights;
-  int32_t* offsets;
-  int32_t* entries;
-  __half* h16;                 // [T*k + T, I]
-  float* out_acc;              // [T, H], zero between calls
-  void* out;
-  uint32_t* sync;              // see the kernel
-  int* status;
-  uint32_t spin_max;
-  unsigned long long* trace;   // optional [grid][64] phase timestamps (ns, slots 0..15), or NULL
-};
-
-namespace {
 
 // Phase timestamp of this CTA (profiling hook; one thread records).
 #define DEC_TRACE(i)                                                            \
@@ -672,15 +324,13 @@ namespace {
     if (a.trace) a.trace[(size_t)blockIdx.x * 64 + (i)] = global_ns();          \
   } while (0)
 
-// One consumer warp: group the selected (token, slot) entries per expert and publish the
-// routing in shared memory (CTA 0 also to global): counts, exclusive scans (entry
-// offsets, active slots), the ascending entry lists and each active expert's columns.
-template <int MODE>
-__device__ void group_in_cta(DecSmem<MODE>& S, const DecodeArgs& a, const Geo& g) {
-  DecCommon& C = S.c;
+// One warp: group the selected (token, slot) entries per expert and publish the routing in
+// shared memory (CTA 0 also to global): counts, exclusive scans (entry offsets, active
+// slots), each active expert's selection slot per token, and the ascending entry lists.
+__device__ void group_in_cta(DecFixed& C, const DecodeArgs& a) {
   const int lane = threadIdx.x & 31;
-  const int T = g.T, E = g.E, k = g.k;
-  // grouping: counts, exclusive scans (entry offsets, active slots), entry lists
+  const int T = a.T, E = a.E, k = a.top_k;
+  const bool cta0 = blockIdx.x == 0;
   const int n = T * k;
   for (int e = lane; e < E; e += 32) C.cnt[e] = 0;
   __syncwarp();
@@ -711,7 +361,7 @@ __device__ void group_in_cta(DecSmem<MODE>& S, const DecodeArgs& a, const Geo& g
     if (i < epl) {
       const int e = lane * epl + i;
       C.soff[e] = run;
-      if (g.c == 0) a.offsets[e] = run;
+      if (cta0) a.offsets[e] = run;
       if (cl[i] > 0) {
         C.aslot[e] = apos;
         C.active[apos++] = e;
@@ -720,25 +370,18 @@ __device__ void group_in_cta(DecSmem<MODE>& S, const DecodeArgs& a, const Geo& g
     }
   }
   const int na = __shfl_sync(0xffffffffu, inca, 31);
-  if (lane == 31 && g.c == 0) a.offsets[E] = run;
-  for (int i = lane; i < na * 8; i += 32) {
-    C.meta_pair[i >> 3][i & 7] = -1;
-    C.meta_w[i >> 3][i & 7] = 0.f;
-  }
+  if (lane == 31 && cta0) a.offsets[E] = run;
+  for (int i = lane; i < na * kMaxT; i += 32) C.meta_j[i / kMaxT][i % kMaxT] = -1;
   __syncwarp();
   const int* flat = &C.idsel[0][0];   // entry f = token * top_k + slot at idsel[token][slot]
   for (int f = lane; f < n; f += 32) {
     const int tok = f / k, slot = f % k;
     const int e = C.idsel[tok][slot];
-    int rank = 0;
-#pragma unroll 8
-    for (int f2 = 0; f2 < f; ++f2) rank += (flat[(f2 / k) * kMaxK + f2 % k] == e);
-    const int q = C.soff[e] + rank;
-    const int sl = C.aslot[e];
-    C.meta_pair[sl][tok] = q;
-    C.meta_w[sl][tok] = C.wsel[tok][slot];
-    if (g.c == 0) {
-      a.entries[q] = f;
+    C.meta_j[C.aslot[e]][tok] = slot;
+    if (cta0) {
+      int rank = 0;
+      for (int f2 = 0; f2 < f; ++f2) rank += (flat[(f2 / k) * kMaxK + f2 % k] == e);
+      a.entries[C.soff[e] + rank] = f;
       a.ids[f] = e;
       a.weights[f] = C.wsel[tok][slot];
     }
@@ -747,200 +390,167 @@ __device__ void group_in_cta(DecSmem<MODE>& S, const DecodeArgs& a, const Geo& g
   __syncwarp();
 }
 
-template <int MODE, int XDT, int WDT>
+// A unit of work: expert slot (0 = shared, 1 + a = active expert a), expert index in the
+// packed store, 128-row tile, K split and its item range.
+struct Unit {
+  int down, slot, e, tile, split, g0, ng;
+};
+
+struct Geo {
+  int NTu, NGu, NTd, NGd, ksu, ksd;
+  int G, c;
+  int a0, a1, c10, c11;   // this CTA's shared gate/up and shared down unit ranges
+};
+
+// Unit v of segment ph (0 shared gate/up, 1 shared down, 2 routed gate/up, 3 routed down).
+__device__ __forceinline__ Unit make_unit(const Geo& g, const DecFixed& C, int ph, int v, int E) {
+  Unit u;
+  u.down = ph & 1;
+  const int nt = u.down ? g.NTd : g.NTu, ks = u.down ? g.ksd : g.ksu, ngr = u.down ? g.NGd : g.NGu;
+  const int per = nt * ks;
+  const int sl = ph < 2 ? 0 : 1 + v / per;
+  const int w = v % per;
+  u.slot = sl;
+  u.e = sl == 0 ? E : C.active[sl - 1];
+  u.tile = w / ks;
+  u.split = w % ks;
+  u.ng = ngr / ks;
+  u.g0 = u.split * u.ng;
+  return u;
+}
+
+// Execution order of the segments: shared gate/up, routed gate/up (once the routing is
+// known), shared down, routed down. The shared down units come after the routed gate/up
+// ones so that no CTA idles on the shared expert's h while the routing is already known;
+// by the time they run, that h is complete.
+__device__ __forceinline__ int seg_at(int step) { return step == 0 ? 0 : step == 1 ? 2 : step == 2 ? 1 : 3; }
+
+__device__ __forceinline__ void seg_of(const Geo& g, int ph, int nact, int& lo, int& hi) {
+  if (ph == 0) {
+    lo = g.a0;
+    hi = g.a1;
+  } else if (ph == 1) {
+    lo = g.c10;
+    hi = g.c11;
+  } else if (ph == 2) {
+    seg_range(nact * g.NTu * g.ksu, g.G, g.c, lo, hi);
+  } else {
+    seg_range(nact * g.NTd * g.ksd, g.G, g.c, lo, hi);
+  }
+}
+
+template <int XDT, int WDT, bool CC>
 __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  DecSmem<MODE>& S = *reinterpret_cast<DecSmem<MODE>*>(smem_raw);
-  DecCommon& C = S.c;
-  constexpr int kSlots = DecSmem<MODE>::kSlots;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  DecFixed& C = *reinterpret_cast<DecFixed*>(smem_raw);
+  uint8_t* const ring = smem_raw + a.off_ring;
+  uint8_t* const xpanel = smem_raw + a.off_x;
+  uint8_t* const hpanel[2] = {smem_raw + a.off_h0, smem_raw + a.off_h1};
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = a.T, H = a.H, I = a.I, E = a.E, k = a.top_k;
+  const int ns = a.ns;
   Geo g;
-  g.T = a.T;
-  g.H = a.H;
-  g.I = a.I;
-  g.E = a.E;
-  g.k = a.top_k;
-  g.NTu = a.I / 8;
-  g.Pu = a.H / kPanelK;
-  g.NTd = a.H / 16;
-  g.Pd = a.I / kPanelK;
+  g.NTu = I / 64;
+  g.NGu = H / kGroupK;
+  g.NTd = H / kTileM;
+  g.NGd = I / kGroupK;
+  g.ksu = a.ksu;
+  g.ksd = a.ksd;
   g.G = gridDim.x;
   g.c = blockIdx.x;
-  // sync words: [0] CTAs done with router rows, [2] CTAs exited, [4] CTAs done with down
-  // tiles; [8..8+E] gate/up tiles done per expert
-  uint32_t* up_done = a.sync + 8;
-  const int shared_e = a.E;
-  const size_t up_tile_bytes = (size_t)g.Pu * kItemBytes;
-  const size_t dn_tile_bytes = (size_t)g.Pd * kItemBytes;
+  seg_range(g.NTu * g.ksu, g.G, g.c, g.a0, g.a1);
+  seg_range(g.NTd * g.ksd, g.G, g.c, g.c10, g.c11);
+  uint32_t* const up_done = a.sync + kSyncUpDone;
+  uint32_t* const up_cnt = a.sync + kSyncUpCnt;
+  uint32_t* const dn_cnt = a.sync + sync_dn_cnt(g.NTu);
 
   if (tid == 0) {
-    for (int s = 0; s < kSlots; ++s) {
-      ptx::mbar_init(&S.full[s], 1);
-      ptx::mbar_init(&S.empty[s], 8);
+    for (int s = 0; s < ns; ++s) {
+      ptx::mbar_init(&C.full[s], 1);
+      ptx::mbar_init(&C.empty[s], 8);
     }
-    ptx::mbar_init(&S.route_bar, 1);
-    ptx::mbar_init(&S.router_bar, 1);
+    for (int s = 0; s < kASlots; ++s) {
+      ptx::mbar_init(&C.afull[s], 8);
+      ptx::mbar_init(&C.aempty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      // one-token mode: the 8 decoder warps arrive themselves; tensor mode: one commit
+      ptx::mbar_init(&C.dfull[b], CC ? 8 : 1);
+      ptx::mbar_init(&C.dempty[b], kEpiWarps);
+      ptx::mbar_init(&C.hfree[b], CC ? 8 : 1);
+      ptx::mbar_init(&C.hready[b], 1);
+    }
+    ptx::mbar_init(&C.route_bar, 1);
+    ptx::mbar_init(&C.router_bar, 1);
+
+    ptx::mbar_init(&C.fin_bar, 1);
     ptx::fence_mbar_init();
     C.abort = 0;
     C.issued = 0;
     C.consumed = 0;
     C.n_active = 0;
   }
+  if (!CC && warp == kWarpMma) {
+    ptx::tmem_alloc(&C.tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
   __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = CC ? 0u : C.tmem_base;
 
-  int a0, a1, c10, c11;
-  seg_range(g.NTu, g.G, g.c, a0, a1);    // shared gate/up tiles
-  seg_range(g.NTd / 2, g.G, g.c, c10, c11);  // shared down tile pairs
-  c10 *= 2;
-  c11 *= 2;
-
-  if (warp == 8) {
-    // ------------------------------------------------------------- producer warp
-    const uint64_t pol = ptx::policy_evict_first();
-    int it = 0;
-    bool ok = true;
-    unsigned long long p_wait = 0;   // cycles waiting for a free slot (profiling)
-    // Brings item `it` into slot it % kSlots once the consumers released its previous use.
-    auto issue = [&](const uint8_t* src) {
-      if (!ok) return;
-      const int slot = it % kSlots;
-      const unsigned long long t0 = clock64();
-      if (it >= kSlots && !ptx::mbar_wait_backoff(&S.empty[slot], ((it / kSlots) - 1) & 1, kMbarSpin, 4, 128))
-        ok = false;
-      p_wait += clock64() - t0;
-      if (ok && *(volatile int*)&C.abort) ok = false;
-      if (!ok) return;
-      ptx::mbar_arrive_expect_tx(&S.full[slot], kItemBytes);
-      ptx::bulk_g2s(S.slots[slot], src, kItemBytes, &S.full[slot], pol);
-      ++it;
-      *(volatile int*)&C.issued = it;
-    };
-    if (lane == 0) {
-      // the router rows' weight loads go first: after two items the producer waits until this
-      // CTA's router rows are done, so the shared-expert prefetch does not delay the routing
-      int n_sh = 0;
-      for (int tl = a0; tl < a1; ++tl)
-        for (int p = 0; p < g.Pu; ++p) {
-          if (n_sh++ == 2) ptx::mbar_wait_backoff(&S.router_bar, 0, kMbarSpin, 4, 128);
-          issue(a.up_store + ((size_t)shared_e * g.NTu + tl) * up_tile_bytes + (size_t)p * kItemBytes);
-        }
-      if (n_sh <= 2) ptx::mbar_wait_backoff(&S.router_bar, 0, kMbarSpin, 4, 128);
-      for (int tl = c10; tl < c11; ++tl)
-        for (int p = 0; p < g.Pd; ++p)
-          issue(a.down_store + ((size_t)shared_e * g.NTd + tl) * dn_tile_bytes + (size_t)p * kItemBytes);
-      DEC_TRACE(13);
+  auto abort_now = [&]() {
+    atomicExch(&C.abort, 1);
+    atomicExch(a.sync + 3, 1u);   // the last CTA out then resets every counter
+    raise_status(a.status, MOE_ERR_TIMEOUT);
+  };
+  auto aborted = [&]() { return *(volatile int*)&C.abort != 0; };
+  // The routing, once the routing warp published it (bounded wait; 0 active on time-out).
+  auto wait_route = [&]() -> int {
+    if (!bar_wait(&C.route_bar, 0, &C.abort, kLocalWaitNs)) {
+      abort_now();
+      return 0;
     }
-    if (lane == 0) {
-      // the routing warp publishes the routing (selection and grouping) through route_bar
-      if (!ptx::mbar_wait_backoff(&S.route_bar, 0, kMbarSpin * 16, 4, 256)) {
-        ok = false;
-        atomicExch(&C.abort, 1);
-        raise_status(a.status, MOE_ERR_TIMEOUT);
-      }
-      DEC_TRACE(14);
-      const int na = ok ? C.n_active : 0;
-      int b0, b1, c20, c21;
-      seg_range(na * g.NTu, g.G, g.c, b0, b1);
-      seg_range(na * (g.NTd / 2), g.G, g.c, c20, c21);   // down tile pairs
-      c20 *= 2;
-      c21 *= 2;
-      for (int r = b0; r < b1; ++r) {
-        const int e = C.active[r / g.NTu], tl = r % g.NTu;
-        for (int p = 0; p < g.Pu; ++p)
-          issue(a.up_store + ((size_t)e * g.NTu + tl) * up_tile_bytes + (size_t)p * kItemBytes);
-      }
-      for (int u = c20; u < c21; ++u) {
-        const int e = C.active[u / g.NTd], tl = u % g.NTd;
-        for (int p = 0; p < g.Pd; ++p)
-          issue(a.down_store + ((size_t)e * g.NTd + tl) * dn_tile_bytes + (size_t)p * kItemBytes);
-      }
-      if (!ok) {
-        atomicExch(&C.abort, 1);
-        raise_status(a.status, MOE_ERR_TIMEOUT);
-      }
-      if (a.trace) {
-        a.trace[(size_t)blockIdx.x * 64 + 21] = p_wait;
-        a.trace[(size_t)blockIdx.x * 64 + 22] = (unsigned long long)it;
-      }
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------- routing warp
-    // Waits for every CTA's router rows, selects each token's experts and groups the
-    // entries while the consumers work on the shared expert; route_bar publishes the result
-    // to the producer and the consumers.
-    int ok = 0;
-    if (lane == 0) {
-      ok = wait_geq(a.sync + 0, (uint32_t)g.G, a.spin_max) ? 1 : 0;
-      __threadfence();
-      DEC_TRACE(3);
-    }
-    __syncwarp();
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) {
-      for (int t = 0; t < g.T; ++t)
-        select_warp(C, a.logits + (size_t)t * g.E, a.bias, g.E, a.n_group, a.topk_group, g.k, a.rsf, C.idsel[t],
-                    C.wsel[t]);
-      if (lane == 0) DEC_TRACE(15);
-      group_in_cta<MODE>(S, a, g);
-      if (lane == 0) DEC_TRACE(23);
-    } else if (lane == 0) {
-      atomicExch(&C.abort, 1);
-      raise_status(a.status, MOE_ERR_TIMEOUT);
-      C.n_active = 0;
-    }
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(&S.route_bar);
-  } else {
-    // ------------------------------------------------------------- consumers
-    const int T = g.T, H = g.H, E = g.E;
-    if (tid == 0) {
-      DEC_TRACE(0);
-      if (a.trace) a.trace[(size_t)blockIdx.x * 64 + 24] = clock64();
-    }
-    if constexpr (MODE == 1) {
-      stage_x1<XDT>(S, a.x, H);
-    } else {
-      stage_x0<XDT>(S, a.x, T, H);
-    }
-    ptx::bar_sync(1, kConsumers);
-    if (tid == 0) DEC_TRACE(1);
-
-    // router rows e = c, c + G, ... two at a time: each thread takes 4 consecutive columns
-    // per 1024 of both rows, all loads issued together; fp32 FMA, then warp and CTA
-    // reductions
+    return C.n_active;
+  };
+  // Router rows e = c, c + G, ..., two at a time over warps 0-11: a thread takes 4
+  // consecutive columns per 1536 of both rows (fp32 FMA), then warp and CTA reductions.
+  // Afterwards this CTA's rows are published to the routing warps of every CTA.
+  auto router_rows = [&]() {
+    constexpr int kRowVec = (kMaxH + 1535) / 1536;
     for (int e0 = g.c; e0 < E; e0 += 2 * g.G) {
       const int e1 = e0 + g.G;
       const bool two = e1 < E;
-      float racc[2][8];
+      float racc[2][kMaxT];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) racc[0][i] = racc[1][i] = 0.f;
-      float4 wv[2][kMaxH / 1024];
+      for (int i = 0; i < kMaxT; ++i) racc[0][i] = racc[1][i] = 0.f;
+      float4 wv[2][kRowVec];
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         const int e = rr ? e1 : e0;
 #pragma unroll
-        for (int q = 0; q < kMaxH / 1024; ++q) {
-          const int col = 1024 * q + 4 * tid;
-          wv[rr][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int qq = 0; qq < kRowVec; ++qq) {
+          const int col = 1536 * qq + 4 * tid;
+          wv[rr][qq] = make_float4(0.f, 0.f, 0.f, 0.f);
           if (col < H && (rr == 0 || two)) {
             if constexpr (WDT == MOE_DT_F32) {
-              wv[rr][q] =
+              wv[rr][qq] =
                   __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(a.router_w) + (size_t)e * H + col));
             } else {
-              const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(a.router_w) +
-                                                                   (size_t)e * H + col));
-              wv[rr][q] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
-                                      __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+              const uint2 uu = __ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(a.router_w) +
+                                                                    (size_t)e * H + col));
+              wv[rr][qq] = make_float4(__uint_as_float(uu.x << 16), __uint_as_float(uu.x & 0xFFFF0000u),
+                                       __uint_as_float(uu.y << 16), __uint_as_float(uu.y & 0xFFFF0000u));
             }
           }
         }
       }
 #pragma unroll
-      for (int q = 0; q < kMaxH / 1024; ++q) {
-        const int col = 1024 * q + 4 * tid;
+      for (int qq = 0; qq < kRowVec; ++qq) {
+        const int col = 1536 * qq + 4 * tid;
         if (col < H) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
+          for (int i = 0; i < kMaxT; ++i) {
             if (i < T) {
               float xv[4];
               if constexpr (XDT == MOE_DT_F32) {
@@ -948,19 +558,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
                     __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + (size_t)i * H + col));
                 xv[0] = f.x; xv[1] = f.y; xv[2] = f.z; xv[3] = f.w;
               } else {
-                const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(a.x) +
-                                                                     (size_t)i * H + col));
-                xv[0] = __uint_as_float(u.x << 16);
-                xv[1] = __uint_as_float(u.x & 0xFFFF0000u);
-                xv[2] = __uint_as_float(u.y << 16);
-                xv[3] = __uint_as_float(u.y & 0xFFFF0000u);
+                const uint2 uu = __ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(a.x) +
+                                                                      (size_t)i * H + col));
+                xv[0] = __uint_as_float(uu.x << 16);
+                xv[1] = __uint_as_float(uu.x & 0xFFFF0000u);
+                xv[2] = __uint_as_float(uu.y << 16);
+                xv[3] = __uint_as_float(uu.y & 0xFFFF0000u);
               }
 #pragma unroll
               for (int rr = 0; rr < 2; ++rr) {
-                racc[rr][i] = fmaf(wv[rr][q].x, xv[0], racc[rr][i]);
-                racc[rr][i] = fmaf(wv[rr][q].y, xv[1], racc[rr][i]);
-                racc[rr][i] = fmaf(wv[rr][q].z, xv[2], racc[rr][i]);
-                racc[rr][i] = fmaf(wv[rr][q].w, xv[3], racc[rr][i]);
+                racc[rr][i] = fmaf(wv[rr][qq].x, xv[0], racc[rr][i]);
+                racc[rr][i] = fmaf(wv[rr][qq].y, xv[1], racc[rr][i]);
+                racc[rr][i] = fmaf(wv[rr][qq].z, xv[2], racc[rr][i]);
+                racc[rr][i] = fmaf(wv[rr][qq].w, xv[3], racc[rr][i]);
               }
             }
           }
@@ -969,377 +579,794 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kMaxT; ++i) {
           float v = racc[rr][i];
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-          if (lane == 0) C.red[0][warp][i][rr] = v;
+          if (lane == 0) C.red[warp][rr][i] = v;
         }
-      ptx::bar_sync(1, kConsumers);
+      ptx::bar_sync(1, kWorkWarps * 32);
       if (tid < 2 * T) {
         const int rr = tid / T, i = tid % T;
         if (rr == 0 || two) {
           float v = 0.f;
 #pragma unroll
-          for (int w = 0; w < 8; ++w) v += C.red[0][w][i][rr];
+          for (int w = 0; w < kWorkWarps; ++w) v += C.red[w][rr][i];
           a.logits[(size_t)i * E + (rr ? e1 : e0)] = v;
         }
       }
-      ptx::bar_sync(1, kConsumers);
+      ptx::bar_sync(1, kWorkWarps * 32);
     }
-    // this CTA's router rows are published; the routing warp takes it from here and the
-    // consumers start on the shared expert
     if (tid == 0) {
       __threadfence();
       ptx::red_release_add(a.sync + 0, 1u);
-      ptx::mbar_arrive(&S.router_bar);
+      ptx::mbar_arrive(&C.router_bar);
       DEC_TRACE(2);
     }
+  };
 
-    float acc[4];
-    // profiling counters (cycles, consumer thread 0): waiting for item data, computing items,
-    // tile reduction and epilogue, expert transitions
-    unsigned long long c_wait = 0, c_comp = 0, c_epi = 0, c_tr = 0;
-    int it = 0;          // items consumed
-    int it_ok = 0;       // items whose copy this CTA saw complete (contiguous prefix)
-    // Wait for item `it`; on time-out or abort the item is skipped and not released, so
-    // its slot is never re-armed while a copy may still be in flight.
-    auto wait_item = [&](const uint8_t*& slot) -> bool {
-      const int s = it % kSlots;
-      slot = S.slots[s];
-      if (*(volatile int*)&C.abort) return false;
-      if (!ptx::mbar_wait_backoff(&S.full[s], (it / kSlots) & 1, kMbarSpin, 16, 32)) {
-        atomicExch(&C.abort, 1);
-        raise_status(a.status, MOE_ERR_TIMEOUT);
-        return false;
-      }
-      return true;
-    };
-    auto run_items = [&](int np, bool up) {
-      for (int p = 0; p < np; ++p) {
-        const uint8_t* slot;
+  if (warp == kWarpProd) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol = ptx::policy_evict_first();
+      int it = 0;
+      bool ok = true;
+      unsigned long long c_wait = 0;   // profiling: cycles waiting for a free slot
+      auto issue = [&](const uint8_t* src) {
+        if (!ok) return;
+        const int s = it % ns;
         const unsigned long long t0 = clock64();
-        const bool have = wait_item(slot);
-        const unsigned long long t1 = clock64();
-        c_wait += t1 - t0;
-        if (have) {
-          if constexpr (MODE == 1) {
-            compute_item1(up ? S.xs : S.hs, up ? S.xsums : S.hsums, slot, p * 128, p * 8 + warp, acc);
-          } else {
-            compute_item0(up ? S.xpanel : S.hpanel, up ? S.xsums : S.hsums, slot, p * 128, p * 8 + warp, acc);
-          }
-        }
-        __syncwarp();
-        c_comp += clock64() - t1;
-        if (have) {
-          if (lane == 0) ptx::mbar_arrive(&S.empty[it % kSlots]);
-          if (it_ok == it) ++it_ok;
-        }
+        // the first two items go out at once; the rest wait until this CTA's router rows are
+        // written, so the weight stream does not delay the routing
+        if (it == 2 && !bar_wait(&C.router_bar, 0, &C.abort, kLocalWaitNs)) ok = false;
+        if (ok && it >= ns && !bar_wait(&C.empty[s], ((it / ns) - 1) & 1, &C.abort, kLocalWaitNs)) ok = false;
+        c_wait += clock64() - t0;
+        if (ok && aborted()) ok = false;
+        if (!ok) return;
+        ptx::mbar_arrive_expect_tx(&C.full[s], kItemBytes);
+        ptx::bulk_g2s(ring + (size_t)s * kItemBytes, src, kItemBytes, &C.full[s], pol);
         ++it;
-      }
-    };
-
-    // gate/up tiles are counted per expert and published with one release-add per run
-    int up_e = -1, up_n = 0;
-    auto flush_up = [&]() {
-      if (up_n > 0 && tid == 0) ptx::red_release_add(up_done + up_e, (uint32_t)up_n);
-      up_n = 0;
-    };
-
-    // one thread waits until every gate/up tile of expert e is done; uniform continuation
-    auto wait_up = [&](int e) {
-      if (tid == 0) {
-        const bool ok = !*(volatile int*)&C.abort && wait_geq(up_done + e, (uint32_t)g.NTu, a.spin_max);
-        if (!ok) {
-          atomicExch(&C.abort, 1);
-          raise_status(a.status, MOE_ERR_TIMEOUT);
+        *(volatile int*)&C.issued = it;
+      };
+      int nact = 0;
+      for (int step = 0; step < 4 && ok; ++step) {
+        const int ph = seg_at(step);
+        if (ph == 2) nact = wait_route();
+        int lo, hi;
+        seg_of(g, ph, nact, lo, hi);
+        for (int v = lo; v < hi && ok; ++v) {
+          const Unit u = make_unit(g, C, ph, v, E);
+          const uint8_t* base = u.down ? a.pack_dn + ((size_t)u.e * g.NTd + u.tile) * g.NGd * kItemBytes
+                                       : a.pack_up + ((size_t)u.e * g.NTu + u.tile) * g.NGu * kItemBytes;
+          for (int q = 0; q < u.ng; ++q) issue(base + (size_t)(u.g0 + q) * kItemBytes);
         }
       }
-      ptx::bar_sync(1, kConsumers);
-    };
-
-    // One loop over the four phases (A shared gate/up, C1 shared down, B routed gate/up,
-    // C2 routed down) so the unrolled item body exists once in the code: the consumer's
-    // instruction footprint stays small. Tile results are reduced through a double-buffered
-    // block, so one barrier per tile suffices.
-    int lo = a0, hi = a1, cur_sl = -2, cur_up = -1, rb = 0, n_act = 0;
-#pragma unroll 1
-    for (int ph = 0; ph < 4; ++ph) {
-      if (ph == 1) {
-        lo = c10 / 2;   // down units are pairs of 16-row tiles
-        hi = c11 / 2;
-      } else if (ph == 2) {
-        // the routed phases need the routing warp's result
-        if (tid == 0) {
-          DEC_TRACE(6);
-          C.flag = ptx::mbar_wait_backoff(&S.route_bar, 0, kMbarSpin * 16, 4, 256) ? 1 : 0;
-          if (!C.flag) {
-            atomicExch(&C.abort, 1);
-            raise_status(a.status, MOE_ERR_TIMEOUT);
-          }
-          DEC_TRACE(7);
-        }
-        ptx::bar_sync(1, kConsumers);
-        n_act = C.flag ? C.n_active : 0;
-        seg_range(n_act * g.NTu, g.G, g.c, lo, hi);
-      } else if (ph == 3) {
-        seg_range(n_act * (g.NTd / 2), g.G, g.c, lo, hi);
+      if (!ok) abort_now();
+      DEC_TRACE(13);
+      if (a.trace) {
+        a.trace[(size_t)blockIdx.x * 64 + 27] = c_wait;
+        a.trace[(size_t)blockIdx.x * 64 + 28] = (unsigned long long)it;
       }
-      const int up = (ph & 1) == 0;
-      const int ntl = up ? g.NTu : g.NTd / 2;
-#pragma unroll 1
-      for (int u = lo; u < hi; ++u) {
-        const int sl = ph < 2 ? -1 : u / ntl;
-        const int tl = ph < 2 ? u : u % ntl;
-        const int e = sl < 0 ? shared_e : C.active[sl];
-        const unsigned long long tt0 = clock64();
-        if (sl != cur_sl || up != cur_up) {
-          // new expert or new direction: publish finished gate/up tiles, load the columns'
-          // h rows and weights, and for down tiles wait for that expert's h and stage it
-          flush_up();
-          up_e = e;
-          ptx::bar_sync(1, kConsumers);
-          if (tid < 8) {
-            if (sl < 0) {
-              C.colpair[tid] = tid < T ? T * g.k + tid : -1;
-              C.colw[tid] = tid < T ? 1.f : 0.f;
-            } else {
-              C.colpair[tid] = C.meta_pair[sl][tid];
-              C.colw[tid] = C.meta_w[sl][tid];
-            }
-          }
-          ptx::bar_sync(1, kConsumers);
-          if (!up) {
-            wait_up(e);
-            if (tid == 0 && ph == 1) DEC_TRACE(5);
-            if (tid == 0 && ph == 3) DEC_TRACE(9);
-            if constexpr (MODE == 1) {
-              stage_h1(S, a.h16, g.I);
-            } else {
-              stage_h0(S, a.h16, g.I);
-            }
-            ptx::bar_sync(1, kConsumers);
-          }
-          cur_sl = sl;
-          cur_up = up;
-        }
-        c_tr += clock64() - tt0;
-        unsigned long long te0;
-        if (up) {
+    }
+  } else if (warp == kWarpRoute) {
+    // spare warp (the routing runs on the epilogue warps)
+  } else if (warp >= kDecWarp0 && warp < kDecWarp0 + 8) {
+    // ------------------------------------------------------------- decoders
+    const int dt = tid - kDecWarp0 * 32;       // 0..255
+    const int hf = (warp - kDecWarp0) >> 2;    // column half of every item: groups 4 hf .. 4 hf + 3
+    const int q = warp & 3, r = 32 * q + lane;  // TMEM lane quarter and weight row
+    // activation panel: [H/8][T][8] fp16 (the tensor core reads it)
+    {
+      const int n = (H / 8) * T;
+      for (int idx = dt; idx < n; idx += 256) {
+        const int c = idx % T, chunk = idx / T;
+        float v[8];
+        load_act8<XDT>(a.x, (size_t)c * H + 8 * chunk, v);
+        uint4 o;
+        o.x = h2u(__floats2half2_rn(v[0], v[1]));
+        o.y = h2u(__floats2half2_rn(v[2], v[3]));
+        o.z = h2u(__floats2half2_rn(v[4], v[5]));
+        o.w = h2u(__floats2half2_rn(v[6], v[7]));
+        *reinterpret_cast<uint4*>(xpanel + (size_t)idx * 16) = o;
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::bar_sync(3, 256);
+      if constexpr (CC) {
+        // per 32-column group: sums of the x values at the 1032 + c and 1152 + 16 c positions
+        const uint32_t* xp = reinterpret_cast<const uint32_t*>(xpanel);
+        for (int j = dt; j < H / 32; j += 256) {
+          float s1 = 0.f, s16 = 0.f;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) acc[i] = 0.f;
-          run_items(g.Pu, true);
-          te0 = clock64();
-          stash_acc<MODE>(C, rb, 0, acc);
-        } else {
-          // a pair of 16-row down tiles per unit: one barrier for both
-#pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] = 0.f;
-            run_items(g.Pd, false);
-            stash_acc<MODE>(C, rb, half, acc);
+          for (int w = 0; w < 4; ++w) {
+            const float2 p0 = __half22float2(u2h(xp[16 * j + 4 * w]));
+            const float2 p1 = __half22float2(u2h(xp[16 * j + 4 * w + 1]));
+            const float2 p2 = __half22float2(u2h(xp[16 * j + 4 * w + 2]));
+            const float2 p3 = __half22float2(u2h(xp[16 * j + 4 * w + 3]));
+            s1 += (p0.x + p0.y) + (p2.x + p2.y);
+            s16 += (p1.x + p1.y) + (p3.x + p3.y);
           }
-          te0 = clock64();
+          C.xsum[j][0] = s1;
+          C.xsum[j][1] = s16;
         }
-        ptx::bar_sync(1, kConsumers);
-        if (up) {
-          const int nt = (MODE == 1) ? 8 : 64;
-          if (tid < nt) {
-            const int r = (MODE == 1) ? tid : (tid >> 3), n = (MODE == 1) ? 0 : (tid & 7);
-            const int pr = C.colpair[n];
-            if (pr >= 0) {
-              const float gate = reduced<MODE>(C, rb, 0, r, n), upv = reduced<MODE>(C, rb, 0, r + 8, n);
-              a.h16[(size_t)pr * g.I + tl * 8 + r] = __float2half_rn(siluf_acc(gate) * upv);
+        ptx::bar_sync(3, 256);
+      }
+    }
+    router_rows();
+    int it_ok = 0;   // items consumed (for the drain count)
+    if constexpr (CC) {
+      // ---- one token: every thread computes its row's dot product over its half of each
+      // item (groups 4 hf .. 4 hf + 3) with exact products; unit results go to the
+      // epilogue through shared memory
+      int it = 0, uc = 0, sw = -1, sslot = -1, nact = 0;
+      bool ok = true;
+      unsigned long long c_full = 0, c_busy = 0, c_hand = 0, c_route = 0, c_hready = 0;
+      const unsigned long long c_loop0 = clock64();
+      unsigned long long c_ph[4] = {0, 0, 0, 0};
+      int rs = 0;           // ring slot of item `it`
+      uint32_t rpar = 0;    // its phase parity
+      for (int step = 0; step < 4 && ok; ++step) {
+        const int ph = seg_at(step);
+        c_ph[step] = clock64();
+        if (ph == 2) {
+          const unsigned long long tr0 = clock64();
+          if (lane == 0) nact = wait_route();
+          nact = __shfl_sync(0xffffffffu, nact, 0);
+          c_route += clock64() - tr0;
+        }
+        int lo, hi;
+        seg_of(g, ph, nact, lo, hi);
+        for (int v = lo; v < hi && ok; ++v, ++uc) {
+          const Unit u = make_unit(g, C, ph, v, E);
+          const uint32_t* act;
+          const float(*asum)[2];
+          if (u.down) {
+            if (u.slot != sslot || sw < 0) {
+              // the previous panel is free once every decoder is done with it
+              if (sw >= 0) {
+                // this warp is done with the previous panel
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&C.hfree[sw & 1]);
+              }
+              ++sw;
+              sslot = u.slot;
+              const unsigned long long th0 = clock64();
+              if (!bar_wait(&C.hready[sw & 1], (sw >> 1) & 1, &C.abort, kLocalWaitNs)) ok = false;
+              c_hready += clock64() - th0;
+              if (__any_sync(0xffffffffu, !ok)) {
+                ok = false;
+                abort_now();
+                break;
+              }
             }
+            act = reinterpret_cast<const uint32_t*>(hpanel[sw & 1]);
+            asum = C.hsum[sw & 1];
+          } else {
+            act = reinterpret_cast<const uint32_t*>(xpanel);
+            asum = C.xsum;
           }
-          ++up_n;
-        } else {
-          const int nt = (MODE == 1) ? 32 : 256;
-          if (tid < nt) {
-            const int half = (MODE == 1) ? (tid >> 4) : (tid >> 7);
-            const int r = (MODE == 1) ? (tid & 15) : ((tid & 127) >> 3), n = (MODE == 1) ? 0 : (tid & 7);
-            const float wn = C.colw[n];
-            if (n < T && wn != 0.f)
-              atomicAdd(a.out_acc + (size_t)n * H + (2 * tl + half) * 16 + r, wn * reduced<MODE>(C, rb, half, r, n));
+          float y = 0.f;
+          for (int qi = 0; qi < u.ng; ++qi, ++it) {
+            const int s = rs;
+            const uint32_t par = rpar;
+            if (++rs == ns) {
+              rs = 0;
+              rpar ^= 1u;
+            }
+            const unsigned long long t0 = clock64();
+            if (!bar_wait(&C.full[s], par, &C.abort, kLocalWaitNs)) ok = false;
+            const unsigned long long t1 = clock64();
+            c_full += t1 - t0;
+            if (__any_sync(0xffffffffu, !ok)) {
+              ok = false;
+              abort_now();
+              break;
+            }
+            const uint8_t* sl = ring + (size_t)s * kItemBytes;
+            const int gbase = (u.g0 + qi) * 8;   // 32-column group index of the item's first group
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const int gi = 4 * hf + h;
+              const uint4 cw = *reinterpret_cast<const uint4*>(sl + ((size_t)gi * kTileM + r) * 16);
+              const float sc =
+                  __half2float(*reinterpret_cast<const __half*>(sl + kItemCodes + ((size_t)gi * kTileM + r) * 2));
+              const uint32_t* xg = act + 16 * (gbase + gi);
+              const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+              float a1 = 0.f, a1b = 0.f, a16 = 0.f, a16b = 0.f;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint4 xv = *reinterpret_cast<const uint4*>(xg + 4 * j);
+                const uint32_t w2 = w[j] >> 8;
+                const uint32_t p0 = (w[j] & 0x000F000Fu) ^ 0x64086408u;
+                const uint32_t p1 = (w[j] & 0x00F000F0u) ^ 0x64806480u;
+                const uint32_t p2 = (w2 & 0x000F000Fu) ^ 0x64086408u;
+                const uint32_t p3 = (w2 & 0x00F000F0u) ^ 0x64806480u;
+                a1 = fma_f16f32(p0, xv.x, a1, false);
+                a1b = fma_f16f32(p0, xv.x, a1b, true);
+                a16 = fma_f16f32(p1, xv.y, a16, false);
+                a16b = fma_f16f32(p1, xv.y, a16b, true);
+                a1 = fma_f16f32(p2, xv.z, a1, false);
+                a1b = fma_f16f32(p2, xv.z, a1b, true);
+                a16 = fma_f16f32(p3, xv.w, a16, false);
+                a16b = fma_f16f32(p3, xv.w, a16b, true);
+              }
+              const float c1 = fmaf(-1032.f, asum[gbase + gi][0], a1 + a1b);
+              const float c16 = fmaf(-1152.f, asum[gbase + gi][1], a16 + a16b);
+              y = fmaf(sc, fmaf(c16, 0.0625f, c1), y);
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&C.empty[s]);
+            c_busy += clock64() - t1;
+            ++it_ok;
           }
+          if (!ok) break;
+          // unit result: each column half goes to accumulator buffer uc % 2 (once the
+          // epilogue released it two units ago); the epilogue adds the halves
+          const unsigned long long th = clock64();
+          const int db = uc & 1;
+          if (uc >= 2 && !bar_wait(&C.dempty[db], ((uc >> 1) - 1) & 1, &C.abort, kLocalWaitNs)) abort_now();
+          C.dsm[db][hf][r] = y;
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&C.dfull[db]);
+          c_hand += clock64() - th;
+          ok = !aborted();
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         }
-        rb ^= 1;
-        c_epi += clock64() - te0;
       }
-      if (up) flush_up();
-      if (tid == 0) DEC_TRACE(ph == 0 ? 4 : ph == 2 ? 8 : 10);
-    }
-    // ---- the last CTA to finish its down tiles converts the whole output (every other CTA's
-    // atomics are ordered before its ticket by the barrier and fence below)
-    ptx::bar_sync(1, kConsumers);
-    if (tid == 0) {
-      __threadfence();
-      const uint32_t ticket = atomicAdd(a.sync + 4, 1u);
-      C.flag = ticket == (uint32_t)g.G - 1;
-      DEC_TRACE(11);
-    }
-    ptx::bar_sync(1, kConsumers);
-    if (C.flag) {
-      __threadfence();
-      const int n4 = T * H / 4;
-#pragma unroll 4
-      for (int i = tid; i < n4; i += kConsumers) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.out_acc) + i);
-        reinterpret_cast<float4*>(a.out_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        store_act<XDT>(a.out, 4 * (size_t)i, v.x);
-        store_act<XDT>(a.out, 4 * (size_t)i + 1, v.y);
-        store_act<XDT>(a.out, 4 * (size_t)i + 2, v.z);
-        store_act<XDT>(a.out, 4 * (size_t)i + 3, v.w);
+      if (a.trace && tid == kDecWarp0 * 32) {
+        unsigned long long* tr = a.trace + (size_t)blockIdx.x * 64;
+        tr[16] = c_full;
+        tr[17] = c_hand;
+        tr[18] = c_busy;
+        tr[19] = (unsigned long long)it_ok;
+        tr[35] = c_route;
+        tr[36] = c_hready;
+        tr[37] = clock64() - c_loop0;
+        for (int i = 0; i < 4; ++i) tr[38 + i] = c_ph[i] ? c_ph[i] - c_loop0 : 0;
       }
+      if (tid == kDecWarp0 * 32) C.consumed = it_ok;
+    } else {
+    const int ipu_up = g.NGu / g.ksu, ipu_dn = g.NGd / g.ksd;
+    int n_items = (g.a1 - g.a0) * ipu_up + (g.c11 - g.c10) * ipu_dn;   // shared items; routed ones later
+    bool routed_known = false;
+    unsigned long long c_full = 0, c_aempty = 0, c_busy = 0;   // profiling (cycles)
+    for (int i = 0;; ++i) {
+      if (i >= n_items) {
+        if (routed_known) break;
+        int nact = 0;
+        if (lane == 0) nact = wait_route();
+        nact = __shfl_sync(0xffffffffu, nact, 0);
+        int lo, hi;
+        seg_of(g, 2, nact, lo, hi);
+        n_items += (hi - lo) * ipu_up;
+        seg_of(g, 3, nact, lo, hi);
+        n_items += (hi - lo) * ipu_dn;
+        routed_known = true;
+        if (i >= n_items) break;
+      }
+      const int s = i % ns, as = i % kASlots;
+      bool ok = !aborted();
+      const unsigned long long t0 = clock64();
+      if (ok && !bar_wait(&C.full[s], (i / ns) & 1, &C.abort, kLocalWaitNs)) ok = false;
+      const unsigned long long t1 = clock64();
+      if (ok && i >= kASlots && !bar_wait(&C.aempty[as], ((i / kASlots) - 1) & 1, &C.abort, kLocalWaitNs))
+        ok = false;
+      const unsigned long long t2 = clock64();
+      c_full += t1 - t0;
+      c_aempty += t2 - t1;
+      if (__any_sync(0xffffffffu, !ok)) {
+        abort_now();
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint8_t* sl = ring + (size_t)s * kItemBytes;
+      const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * as);
+#pragma unroll 1
+      for (int gp = 2 * hf; gp < 2 * hf + 2; ++gp) {
+        uint32_t o[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int gi = 2 * gp + h;    // 32-column group within the item
+          const uint4 cw = *reinterpret_cast<const uint4*>(sl + ((size_t)gi * kTileM + r) * 16);
+          const __half sc = *reinterpret_cast<const __half*>(sl + kItemCodes + ((size_t)gi * kTileM + r) * 2);
+          const __half2 s2 = __half2half2(sc);
+          dq_word(cw.x, s2, &o[16 * h + 0]);
+          dq_word(cw.y, s2, &o[16 * h + 4]);
+          dq_word(cw.z, s2, &o[16 * h + 8]);
+          dq_word(cw.w, s2, &o[16 * h + 12]);
+        }
+        ptx::tmem_st32(tbase + (uint32_t)(32 * gp), o);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(&C.empty[s]);
+        ptx::mbar_arrive(&C.afull[as]);
+      }
+      c_busy += clock64() - t2;
+      ++it_ok;
     }
-    if (tid == 0) {
-      C.consumed = it_ok;
-      DEC_TRACE(12);
-      if (a.trace) a.trace[(size_t)blockIdx.x * 64 + 25] = clock64();
+    if (a.trace && tid == kDecWarp0 * 32) {
+      unsigned long long* tr = a.trace + (size_t)blockIdx.x * 64;
+      tr[16] = c_full;
+      tr[17] = c_aempty;
+      tr[18] = c_busy;
+      tr[19] = (unsigned long long)it_ok;
+    }
+    // consumed item count (the drain below needs it)
+    if (tid == kDecWarp0 * 32) C.consumed = it_ok;
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------- MMA issuer
+    if (!CC && lane == 0) {
+      constexpr uint32_t idesc = ptx::f16_idesc(kTileM, kN, false);
+      const uint32_t lbo = 16u * (uint32_t)T, sbo = 128u;
+      const uint64_t dstep = (uint64_t)(2 * T);   // one K step (16 columns = 32 T bytes) in descriptor units
+      int it = 0, uc = 0;
+      int hsw = -1, hslot = -1;   // down-unit switch index and slot whose h panel is in use
+      bool ok = true;
+      int nact = 0;
+      unsigned long long c_afull = 0, c_dempty = 0, c_stage = 0, c_issue = 0;   // profiling (cycles)
+      const unsigned long long c_start = clock64();
+      for (int step = 0; step < 4 && ok; ++step) {
+        const int ph = seg_at(step);
+        if (ph == 2) nact = wait_route();
+        int lo, hi;
+        seg_of(g, ph, nact, lo, hi);
+        for (int v = lo; v < hi && ok; ++v, ++uc) {
+          const Unit u = make_unit(g, C, ph, v, E);
+          uint32_t panel;
+          if (u.down) {
+            if (u.slot != hslot || hsw < 0) {
+              // a new expert: release the previous panel once its MMAs complete, then wait
+              // for the stager to fill panel (switch index) % 2 with this expert's h rows
+              const unsigned long long ts0 = clock64();
+              if (hsw >= 0) ptx::tc_commit(&C.hfree[hsw & 1]);
+              ++hsw;
+              hslot = u.slot;
+              if (!bar_wait(&C.hready[hsw & 1], (hsw >> 1) & 1, &C.abort, kLocalWaitNs)) {
+                ok = false;
+                break;
+              }
+              c_stage += clock64() - ts0;
+            }
+            panel = ptx::smem_u32(hpanel[hsw & 1]);
+          } else {
+            panel = ptx::smem_u32(xpanel);
+          }
+          const int db = uc & 1;
+          const unsigned long long tw = clock64();
+          if (uc >= 2 && !bar_wait(&C.dempty[db], ((uc >> 1) - 1) & 1, &C.abort, kLocalWaitNs)) {
+            ok = false;
+            break;
+          }
+          c_dempty += clock64() - tw;
+          ptx::tc_fence_after();
+          const uint32_t d = tmem + (uint32_t)(kDCol0 + kN * db);
+          for (int qi = 0; qi < u.ng; ++qi, ++it) {
+            const int as = it % kASlots;
+            const unsigned long long ta = clock64();
+            if (!bar_wait(&C.afull[as], (it / kASlots) & 1, &C.abort, kLocalWaitNs)) {
+              ok = false;
+              break;
+            }
+            c_afull += clock64() - ta;
+            ptx::tc_fence_after();
+            const uint32_t a0 = tmem + (uint32_t)(128 * as);
+            const uint64_t bd0 = ptx::kmajor_desc(panel + (uint32_t)(u.g0 + qi) * 16u * 32u * (uint32_t)T, lbo, sbo);
+            const uint32_t acc0 = qi != 0 ? 1u : 0u;
+            const unsigned long long ti = clock64();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+              ptx::tc_mma_f16_tmem_a(d, a0 + 8u * jj, bd0 + dstep * (uint64_t)jj, idesc, jj ? 1u : acc0);
+            ptx::tc_commit(&C.aempty[as]);
+            c_issue += clock64() - ti;
+          }
+          if (ok) ptx::tc_commit(&C.dfull[db]);
+        }
+      }
+      if (!ok) abort_now();
+      DEC_TRACE(14);
       if (a.trace) {
         unsigned long long* tr = a.trace + (size_t)blockIdx.x * 64;
-        tr[16] = c_wait;
-        tr[17] = c_comp;
-        tr[18] = c_epi;
-        tr[19] = c_tr;
-        tr[20] = (unsigned long long)it;
+        tr[20] = c_afull;
+        tr[21] = c_dempty;
+        tr[22] = c_stage;
+        tr[23] = (unsigned long long)uc;
+        tr[33] = c_issue;
+        tr[34] = clock64() - c_start;
+      }
+    }
+  } else if (warp == kWarpStage) {
+    // ------------------------------------------------------------- h stager
+    // Walks this CTA's down units in order; for each new expert, waits until every MMA that
+    // read the panel it will overwrite has completed and until all the expert's gate/up
+    // tiles (from every CTA) are done, copies the expert's h rows into the panel
+    // ([I/8][T][8] fp16) and signals the MMA issuer.
+    int hsw = -1, hslot = -1;
+    bool ok = true;
+    unsigned long long c_wait = 0;
+    for (int ph = 1; ph < 4 && ok; ph += 2) {
+      int nact = 0;
+      if (ph == 3) {
+        if (lane == 0) nact = wait_route();
+        nact = __shfl_sync(0xffffffffu, nact, 0);
+      }
+      int lo, hi;
+      seg_of(g, ph, nact, lo, hi);
+      for (int v = lo; v < hi && ok; ++v) {
+        const Unit u = make_unit(g, C, ph, v, E);
+        if (u.slot == hslot && hsw >= 0) continue;
+        ++hsw;
+        hslot = u.slot;
+        const int b = hsw & 1;
+        const unsigned long long t0 = clock64();
+        bool good = true;
+        if (hsw >= 2 && !bar_wait(&C.hfree[b], ((hsw - 2) >> 1) & 1, &C.abort, kLocalWaitNs)) good = false;
+        if (good && !geq_wait(up_done + u.slot, (uint32_t)g.NTu, &C.abort, a.wait_ns)) good = false;
+        c_wait += clock64() - t0;
+        if (__any_sync(0xffffffffu, !good)) {
+          if (lane == 0) abort_now();
+          ok = false;
+          break;
+        }
+        const int n = (I / 8) * T;
+        for (int idx = lane; idx < n; idx += 32) {
+          const int c = idx % T, chunk = idx / T;
+          const uint4 hv = __ldcg(reinterpret_cast<const uint4*>(a.h16 + ((size_t)u.slot * T + c) * I) + chunk);
+          *reinterpret_cast<uint4*>(hpanel[b] + (size_t)idx * 16) = hv;
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if constexpr (CC) {
+          // per 32-column group: sums of the h values at the 1032 + c and 1152 + 16 c positions
+          const uint32_t* hp = reinterpret_cast<const uint32_t*>(hpanel[b]);
+          for (int j = lane; j < I / 32; j += 32) {
+            float s1 = 0.f, s16 = 0.f;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const float2 p0 = __half22float2(u2h(hp[16 * j + 4 * w]));
+              const float2 p1 = __half22float2(u2h(hp[16 * j + 4 * w + 1]));
+              const float2 p2 = __half22float2(u2h(hp[16 * j + 4 * w + 2]));
+              const float2 p3 = __half22float2(u2h(hp[16 * j + 4 * w + 3]));
+              s1 += (p0.x + p0.y) + (p2.x + p2.y);
+              s16 += (p1.x + p1.y) + (p3.x + p3.y);
+            }
+            C.hsum[b][j][0] = s1;
+            C.hsum[b][j][1] = s16;
+          }
+          __syncwarp();
+        }
+        if (lane == 0) ptx::mbar_arrive(&C.hready[b]);
+      }
+    }
+    if (a.trace && lane == 0) a.trace[(size_t)blockIdx.x * 64 + 32] = c_wait;
+  } else {
+    // ------------------------------------------------------------- epilogue warps 0-3
+    const int q = warp, r = tid;   // TMEM lane quarter q, accumulator row r
+    if (tid == 0) {
+      DEC_TRACE(0);
+      if (a.trace) a.trace[(size_t)blockIdx.x * 64 + 29] = clock64();
+    }
+    unsigned long long c_dfull = 0, c_epi = 0, c_last = 0;   // profiling (cycles)
+    router_rows();
+    // routing: once every CTA's router rows are written, select each token's experts
+    // (block-parallel), group the entries (warp 0) and publish the result to this CTA
+    {
+      if (tid == 0) {
+        C.ep_stop = geq_wait(a.sync + 0, (uint32_t)g.G, &C.abort, a.wait_ns) ? 0 : 1;
+        __threadfence();
+        DEC_TRACE(3);
+      }
+      ptx::bar_sync(2, kEpiWarps * 32);
+      if (!C.ep_stop) {
+        for (int t = 0; t < T; ++t)
+          select_block(C, a.logits + (size_t)t * E, a.bias, E, a.n_group, a.topk_group, k, a.rsf, C.idsel[t],
+                       C.wsel[t]);
+        if (tid == 0) DEC_TRACE(7);
+        if (warp == 0) group_in_cta(C, a);
+      } else if (tid == 0) {
+        abort_now();
+        C.n_active = 0;
+      }
+      ptx::bar_sync(2, kEpiWarps * 32);
+      if (tid == 0) {
+        ptx::mbar_arrive(&C.route_bar);
+        DEC_TRACE(15);
+      }
+    }
+    // unit epilogues; every stop decision and the routing are taken by thread 0 and
+    // shared, so the four warps pass the same named barriers
+    const int ksu = g.ksu, ksd = g.ksd;
+    int uc = 0, nact = 0;
+    bool have_route = false, ok = true;
+    auto ep_route = [&]() -> int {
+      if (tid == 0) C.ep_nact = wait_route();
+      ptx::bar_sync(2, kEpiWarps * 32);
+      return C.ep_nact;
+    };
+    for (int step = 0; step < 4 && ok; ++step) {
+      const int ph = seg_at(step);
+      if (tid == 0 && step >= 1) DEC_TRACE(3 + step);   // 4: shared gate/up, 5: routed gate/up, 6: shared down done
+      if (ph == 2 && !have_route) {
+        nact = ep_route();
+        have_route = true;
+      }
+      int lo, hi;
+      seg_of(g, ph, nact, lo, hi);
+      for (int v = lo; v < hi && ok; ++v, ++uc) {
+        const Unit u = make_unit(g, C, ph, v, E);
+        const int db = uc & 1;
+        const unsigned long long tw = clock64();
+        if (!bar_wait(&C.dfull[db], (uc >> 1) & 1, &C.abort, kLocalWaitNs)) abort_now();
+        const unsigned long long tb = clock64();
+        c_dfull += tb - tw;
+        ptx::bar_sync(2, kEpiWarps * 32);
+        if (tid == 0) C.ep_stop = aborted() ? 1 : 0;
+        ptx::bar_sync(2, kEpiWarps * 32);
+        if (C.ep_stop) {
+          ok = false;
+          break;
+        }
+        float dv[16];
+        if constexpr (CC) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) dv[c] = 0.f;
+          dv[0] = C.dsm[db][0][r] + C.dsm[db][1][r];
+        } else {
+          ptx::tc_fence_after();
+          ptx::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kDCol0 + kN * db), dv);
+          ptx::tc_fence_before();
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&C.dempty[db]);
+        if (!u.down) {
+          // gate/up: K-split partial of this tile, then the last split computes h
+          float* part = a.gu_part + ((((size_t)u.slot * g.NTu + u.tile) * ksu + u.split) * T) * kTileM;
+#pragma unroll
+          for (int c = 0; c < kMaxT; ++c)
+            if (c < T) part[(size_t)c * kTileM + r] = dv[c];
+          __threadfence();
+          ptx::bar_sync(2, kEpiWarps * 32);
+          if (tid == 0) {
+            const uint32_t old = atomicAdd(up_cnt + u.slot * g.NTu + u.tile, 1u);
+            C.flag = old == (uint32_t)(ksu - 1);
+            if (C.flag) up_cnt[u.slot * g.NTu + u.tile] = 0;
+          }
+          ptx::bar_sync(2, kEpiWarps * 32);
+          if (C.flag) {
+            const unsigned long long tl = clock64();
+            __threadfence();
+            if (lane < 16) {
+              const float* p0 = a.gu_part + (((size_t)u.slot * g.NTu + u.tile) * ksu * T) * kTileM;
+#pragma unroll 1
+              for (int c = 0; c < T; ++c) {
+                // all splits' loads first, then the sums in split order
+                float gv[kMaxKsu], uv[kMaxKsu];
+#pragma unroll
+                for (int sp = 0; sp < kMaxKsu; ++sp) {
+                  gv[sp] = uv[sp] = 0.f;
+                  if (sp < ksu) {
+                    gv[sp] = __ldcg(p0 + ((size_t)sp * T + c) * kTileM + 32 * q + lane);
+                    uv[sp] = __ldcg(p0 + ((size_t)sp * T + c) * kTileM + 32 * q + 16 + lane);
+                  }
+                }
+                float gs = 0.f, us = 0.f;
+#pragma unroll
+                for (int sp = 0; sp < kMaxKsu; ++sp)
+                  if (sp < ksu) {
+                    gs += gv[sp];
+                    us += uv[sp];
+                  }
+                a.h16[((size_t)u.slot * T + c) * I + 64 * u.tile + 16 * q + lane] = __float2half_rn(siluf_acc(gs) * us);
+              }
+            }
+            __threadfence();
+            ptx::bar_sync(2, kEpiWarps * 32);
+            if (tid == 0) ptx::red_release_add(up_done + u.slot, 1u);
+            c_last += clock64() - tl;
+          }
+        } else {
+          // down: this split's y rows of the unit's tokens, then the last unit of the
+          // 128-row block to arrive combines the block's outputs
+          if (!have_route) {
+            nact = ep_route();
+            have_route = true;
+          }
+          const int row = kTileM * u.tile + r;
+#pragma unroll
+          for (int c = 0; c < kMaxT; ++c) {
+            if (c < T) {
+              const int j = u.slot == 0 ? k : C.meta_j[u.slot - 1][c];
+              if (j >= 0) a.y_part[(((size_t)c * (k + 1) + j) * ksd + u.split) * H + row] = dv[c];
+            }
+          }
+          __threadfence();
+          ptx::bar_sync(2, kEpiWarps * 32);
+          if (tid == 0) {
+            const uint32_t target = (uint32_t)((nact + 1) * ksd);
+            const uint32_t old = atomicAdd(dn_cnt + u.tile, 1u);
+            C.flag = old == target - 1;
+            if (C.flag) dn_cnt[u.tile] = 0;
+          }
+          ptx::bar_sync(2, kEpiWarps * 32);
+          if (C.flag) {
+            const unsigned long long tl = clock64();
+            __threadfence();
+            for (int c = 0; c < T; ++c) {
+              const float* yp = a.y_part + (size_t)c * (k + 1) * ksd * H + row;
+              // per selection slot: all its splits' loads first, then the sum in split order;
+              // slots in order, the shared expert last
+              float acc = 0.f, ysh = 0.f;
+              for (int j = 0; j <= k; ++j) {
+                float yv[kMaxKsd];
+#pragma unroll
+                for (int sp = 0; sp < kMaxKsd; ++sp)
+                  yv[sp] = sp < ksd ? __ldcg(yp + ((size_t)j * ksd + sp) * H) : 0.f;
+                float ys = 0.f;
+#pragma unroll
+                for (int sp = 0; sp < kMaxKsd; ++sp)
+                  if (sp < ksd) ys += yv[sp];
+                if (j < k)
+                  acc = fmaf(C.wsel[c][j], ys, acc);
+                else
+                  ysh = ys;
+              }
+              store_act<XDT>(a.out, (size_t)c * H + row, acc + ysh);
+            }
+            c_last += clock64() - tl;
+          }
+        }
+        c_epi += clock64() - tb;
+      }
+    }
+    if (tid == 0) {
+      DEC_TRACE(12);
+      if (a.trace) {
+        unsigned long long* tr = a.trace + (size_t)blockIdx.x * 64;
+        tr[24] = c_dfull;
+        tr[25] = c_epi;
+        tr[26] = c_last;
+        tr[30] = clock64();
+        tr[31] = (unsigned long long)uc;
       }
     }
   }
+
+  // ---------------------------------------------------------------------- teardown
+  ptx::tc_fence_before();
   __syncthreads();
   if (tid == 0) {
-    // drain copies this CTA issued but did not see complete (only after an abort): the last
-    // issued item of each slot is the only one that can still be in flight
+    // after an abort, wait for the copies that may still be in flight (the last ns issued)
     const int issued = C.issued;
-    for (int i = max(C.consumed, issued - kSlots); i < issued; ++i)
-      ptx::mbar_wait(&S.full[i % kSlots], (i / kSlots) & 1, kMbarSpin);
+    if (issued != C.consumed)
+      for (int i = max(0, issued - ns); i < issued; ++i) bar_wait(&C.full[i % ns], (i / ns) & 1, nullptr, kLocalWaitNs);
+  }
+  if (!CC && warp == kWarpMma) {
+    if (aborted() && lane == 0) {
+      ptx::tc_commit(&C.fin_bar);
+      bar_wait(&C.fin_bar, 0, nullptr, kLocalWaitNs);
+    }
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+  if (tid == 0) {
     __threadfence();
     const uint32_t old = atomicAdd(a.sync + 2, 1u);
     if (old == (uint32_t)g.G - 1) {
-      // last CTA out: reset the counters for the next call
+      // last CTA out: reset the per-call counters for the next call (after a time-out
+      // also the K-split and row-block counters that the aborted units left behind)
       a.sync[0] = 0;
       a.sync[4] = 0;
-      for (int i = 0; i <= g.E; ++i) up_done[i] = 0;
+      for (int i = 0; i <= kMaxActive; ++i) up_done[i] = 0;
+      if (__ldcg(a.sync + 3)) {
+        for (int i = 0; i < (1 + kMaxActive) * g.NTu; ++i) up_cnt[i] = 0;
+        for (int i = 0; i < g.NTd; ++i) dn_cnt[i] = 0;
+        a.sync[3] = 0;
+      }
       __threadfence();
       a.sync[2] = 0;
     }
   }
 }
 
-// ------------------------------------------------------------------ repack
-
-// Row-major int4-g32 matrix (codes [R][K/2], fp16 scales [R][K/32]) -> 16-row tiles of
-// 2048-column panels in MMA fragment order. `up` selects the gate/up row pairing
-// (MMA rows 0-7 = gate rows 8i.., rows 8-15 = up rows R/2 + 8i..).
-// Per panel: codes [32 chunks of 64 columns][32 lanes][4 words] (word q of lane (g, t) in
-// chunk c: the 8 nibbles (g, 2t) (g+8, 2t) (g, 2t+8) (g+8, 2t+8) (g, 2t+1) (g+8, 2t+1)
-// (g, 2t+9) (g+8, 2t+9) of MMA 4c+q, low nibble first), then scales [8 k-blocks][8 g][4 t]
-// x {s[g][j], s[g][j+1], s[g+8][j], s[g+8][j+1]} with j = 8 * kblock + 2t.
-__global__ void repack_kernel(const uint8_t* __restrict__ codes, const __half* __restrict__ scales,
-                              int R, int K, int up, uint8_t* __restrict__ dst) {
-  const int ntile = R / 16, np = K / kPanelK;
-  const size_t words_per_panel = kCodeBytes / 4;
-  const size_t total_words = (size_t)ntile * np * words_per_panel;
-  const size_t total_scl = (size_t)ntile * np * (kScaleBytes / 8);   // 8-byte scale quads
-  auto row_of = [&](int tile, int m) -> int {
-    if (!up) return tile * 16 + m;
-    const int half = R / 2;
-    return (m < 8) ? tile * 8 + m : half + tile * 8 + (m - 8);
-  };
-  auto nib = [&](int row, int kk) -> uint32_t {
-    const uint8_t b = codes[(size_t)row * (K / 2) + (kk >> 1)];
-    return (kk & 1) ? (b >> 4) : (b & 15u);
-  };
-  for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total_words + total_scl;
-       idx += (size_t)gridDim.x * blockDim.x) {
-    if (idx < total_words) {
-      const size_t tp = idx / words_per_panel;          // tile * np + panel
-      const int wi = (int)(idx % words_per_panel);      // word within the panel
-      const int tile = (int)(tp / np), p = (int)(tp % np);
-      const int q = wi & 3, lane = (wi >> 2) & 31, c = wi >> 7;
-      const int gq = lane >> 2, t = lane & 3;
-      const int k0 = p * kPanelK + 64 * c + 16 * q;
-      const int rA = row_of(tile, gq), rB = row_of(tile, gq + 8);
-      const uint32_t w = nib(rA, k0 + 2 * t) | (nib(rB, k0 + 2 * t) << 4) | (nib(rA, k0 + 2 * t + 8) << 8) |
-                         (nib(rB, k0 + 2 * t + 8) << 12) | (nib(rA, k0 + 2 * t + 1) << 16) |
-                         (nib(rB, k0 + 2 * t + 1) << 20) | (nib(rA, k0 + 2 * t + 9) << 24) |
-                         (nib(rB, k0 + 2 * t + 9) << 28);
-      reinterpret_cast<uint32_t*>(dst + tp * kItemBytes)[wi] = w;
-    } else {
-      const size_t si = idx - total_words;
-      const size_t tp = si / (kScaleBytes / 8);
-      const int qi = (int)(si % (kScaleBytes / 8));     // (kb, g, t) quad
-      const int tile = (int)(tp / np), p = (int)(tp % np);
-      const int t = qi & 3, gq = (qi >> 2) & 7, kb = qi >> 5;
-      const int grp = (p * kPanelK) / 32 + 8 * kb + 2 * t;
-      const int rA = row_of(tile, gq), rB = row_of(tile, gq + 8);
-      __half* o = reinterpret_cast<__half*>(dst + tp * kItemBytes + kCodeBytes) + (size_t)qi * 4;
-      o[0] = scales[(size_t)rA * (K / 32) + grp];
-      o[1] = scales[(size_t)rA * (K / 32) + grp + 1];
-      o[2] = scales[(size_t)rB * (K / 32) + grp];
-      o[3] = scales[(size_t)rB * (K / 32) + grp + 1];
-    }
-  }
-}
-
-template <int MODE, int XDT, int WDT>
-cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t s) {
+template <int XDT, int WDT, bool CC>
+cudaError_t launch_decode_t(const DecodeArgs& a, int grid, size_t smem, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kDecThreads);
-  cfg.dynamicSmemBytes = sizeof(DecSmem<MODE>);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, moe_decode_kernel<MODE, XDT, WDT>, a);
+  return cudaLaunchKernelEx(&cfg, moe_decode_kernel<XDT, WDT, CC>, a);
 }
 
-template <int MODE, int XDT, int WDT>
+template <int XDT, int WDT>
 cudaError_t init_one() {
-  return cudaFuncSetAttribute(moe_decode_kernel<MODE, XDT, WDT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)sizeof(DecSmem<MODE>));
+  cudaError_t e = cudaFuncSetAttribute(moe_decode_kernel<XDT, WDT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemLimit);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(moe_decode_kernel<XDT, WDT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemLimit);
+  return e;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Shared-memory layout for T tokens: fixed block, ring, activation panel, h panels.
+// Returns the dynamic shared-memory bytes (0 if the ring would have fewer than 2 slots).
+size_t decode_layout(int T, int H, int I, DecodeArgs* a) {
+  const size_t fixed = align_up(sizeof(DecFixed), 1024);
+  const size_t xb = align_up((size_t)H * T * 2 + kPanelPad, 128);
+  const size_t hb = align_up((size_t)I * T * 2 + kPanelPad, 128);
+  const size_t rest = fixed + xb + 2 * hb;
+  if (rest + 2 * (size_t)kItemBytes > (size_t)kSmemLimit) return 0;
+  int ns = (int)(((size_t)kSmemLimit - rest) / kItemBytes);
+  if (ns > kMaxSlots) ns = kMaxSlots;
+  if (a) {
+    a->ns = ns;
+    a->off_ring = (int)fixed;
+    a->off_x = (int)(fixed + (size_t)ns * kItemBytes);
+    a->off_h0 = a->off_x + (int)xb;
+    a->off_h1 = a->off_h0 + (int)hb;
+  }
+  return fixed + (size_t)ns * kItemBytes + xb + 2 * hb;
+}
+
+int pick_split(int n, const int* cands, int nc) {
+  for (int i = 0; i < nc; ++i)
+    if (n % cands[i] == 0) return cands[i];
+  return 1;
+}
+
+// K splits: gate/up units of about 6 items and down units of about 4 at the GLM shape.
+// Smaller units balance the CTAs' shares better but cost more per-unit epilogue work
+// (partials, fences, counters); at these sizes that work dominates.
+int ksu_for(int H) {
+  const int c[] = {4, 3, 2};
+  return pick_split(H / kGroupK, c, 3);
+}
+
+int ksd_for(int I) {
+  const int c[] = {2};
+  return pick_split(I / kGroupK, c, 1);
 }
 
 }  // namespace
 
-size_t decode_tile_bytes(int R, int K) { return (size_t)(R / 16) * (K / kPanelK) * kItemBytes; }
-
 bool decode_supported(int H, int I, int E, int top_k, int T) {
-  return H % kPanelK == 0 && I % kPanelK == 0 && H <= kMaxH && I <= kMaxI && E <= kMaxE && E % 32 == 0 &&
-         T >= 1 && T <= 8 && T * top_k <= kMaxActive && top_k <= kMaxK;
+  return H % kGroupK == 0 && I % kGroupK == 0 && H <= kMaxH && I <= kMaxI && E <= kMaxE && E % 32 == 0 &&
+         T >= 1 && T <= kMaxT && T * top_k <= kMaxActive && top_k <= kMaxK && decode_layout(T, H, I, nullptr) > 0;
 }
 
-size_t decode_smem_bytes() {
-  return sizeof(DecSmem<0>) > sizeof(DecSmem<1>) ? sizeof(DecSmem<0>) : sizeof(DecSmem<1>);
+size_t decode_sync_words(int I) { return (size_t)sync_route(I / 64) + 2 * kMaxT * kMaxK + 8; }
+
+size_t decode_gu_part_floats(int T, int H, int I, int E, int top_k) {
+  const int act = T * top_k < E ? T * top_k : E;
+  return (size_t)(1 + act) * (I / 64) * ksu_for(H) * T * kTileM;
+}
+
+size_t decode_y_part_floats(int T, int H, int I, int top_k) { return (size_t)T * (top_k + 1) * ksd_for(I) * H; }
+
+size_t decode_h16_elems(int T, int I, int E, int top_k) {
+  const int act = T * top_k < E ? T * top_k : E;
+  return (size_t)(1 + act) * T * I;
 }
 
 cudaError_t decode_occupancy(int* blocks_per_sm) {
-  int b0 = 0, b1 = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, moe_decode_kernel<0, MOE_DT_BF16, MOE_DT_F32>,
-                                                                kDecThreads, sizeof(DecSmem<0>));
-  if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, moe_decode_kernel<1, MOE_DT_BF16, MOE_DT_F32>, kDecThreads,
-                                                      sizeof(DecSmem<1>));
-  *blocks_per_sm = b0 < b1 ? b0 : b1;
-  return e;
-}
-
-cudaError_t launch_repack(const uint8_t* codes, const void* scales, int R, int K, bool up, uint8_t* dst,
-                          cudaStream_t s) {
-  repack_kernel<<<148 * 8, 256, 0, s>>>(codes, static_cast<const __half*>(scales), R, K, up ? 1 : 0, dst);
-  return cudaGetLastError();
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, moe_decode_kernel<MOE_DT_BF16, MOE_DT_F32, false>,
+                                                       kDecThreads, kSmemLimit);
 }
 
 cudaError_t decode_kernels_init() {
   cudaError_t e = cudaSuccess;
-  const cudaError_t r[] = {init_one<0, MOE_DT_F32, MOE_DT_F32>(), init_one<0, MOE_DT_BF16, MOE_DT_F32>(),
-                           init_one<0, MOE_DT_F32, MOE_DT_BF16>(), init_one<0, MOE_DT_BF16, MOE_DT_BF16>(),
-                           init_one<1, MOE_DT_F32, MOE_DT_F32>(), init_one<1, MOE_DT_BF16, MOE_DT_F32>(),
-                           init_one<1, MOE_DT_F32, MOE_DT_BF16>(), init_one<1, MOE_DT_BF16, MOE_DT_BF16>()};
+  const cudaError_t r[] = {init_one<MOE_DT_F32, MOE_DT_F32>(), init_one<MOE_DT_BF16, MOE_DT_F32>(),
+                           init_one<MOE_DT_F32, MOE_DT_BF16>(), init_one<MOE_DT_BF16, MOE_DT_BF16>()};
   for (cudaError_t x : r)
     if (x != cudaSuccess) e = x;
   return e;
@@ -1359,27 +1386,37 @@ cudaError_t launch_decode_fused(const DecodeLaunch& d, int act_dtype, int router
   a.n_group = d.n_group;
   a.topk_group = d.topk_group;
   a.rsf = d.rsf;
-  a.up_store = d.up_store;
-  a.down_store = d.down_store;
+  a.pack_up = d.pack_up;
+  a.pack_dn = d.pack_dn;
   a.logits = d.logits;
   a.ids = d.ids;
   a.weights = d.weights;
   a.offsets = d.offsets;
   a.entries = d.entries;
-  a.h16 = static_cast<__half*>(d.h16);
-  a.out_acc = d.out_acc;
+  a.h16 = d.h16;
+  a.gu_part = d.gu_part;
+  a.y_part = d.y_part;
   a.out = d.out;
   a.sync = d.sync;
   a.status = d.status;
-  a.spin_max = d.spin_max;
+  a.wait_ns = d.wait_ns;
   a.trace = d.trace;
+  a.ksu = ksu_for(d.H);
+  a.ksd = ksd_for(d.I);
+  const size_t smem = decode_layout(d.T, d.H, d.I, &a);
+  if (smem == 0) return cudaErrorInvalidValue;
   const bool xf = act_dtype == MOE_DT_F32, wf = router_dtype == MOE_DT_F32;
-  if (a.T == 1) {
-    if (xf) return wf ? launch_decode_t<1, MOE_DT_F32, MOE_DT_F32>(a, grid, s) : launch_decode_t<1, MOE_DT_F32, MOE_DT_BF16>(a, grid, s);
-    return wf ? launch_decode_t<1, MOE_DT_BF16, MOE_DT_F32>(a, grid, s) : launch_decode_t<1, MOE_DT_BF16, MOE_DT_BF16>(a, grid, s);
+  // one token: CUDA-core dot products (exact products, fp32 sums); 2..8 tokens: tensor cores
+  if (d.T == 1) {
+    if (xf) return wf ? launch_decode_t<MOE_DT_F32, MOE_DT_F32, true>(a, grid, smem, s)
+                      : launch_decode_t<MOE_DT_F32, MOE_DT_BF16, true>(a, grid, smem, s);
+    return wf ? launch_decode_t<MOE_DT_BF16, MOE_DT_F32, true>(a, grid, smem, s)
+              : launch_decode_t<MOE_DT_BF16, MOE_DT_BF16, true>(a, grid, smem, s);
   }
-  if (xf) return wf ? launch_decode_t<0, MOE_DT_F32, MOE_DT_F32>(a, grid, s) : launch_decode_t<0, MOE_DT_F32, MOE_DT_BF16>(a, grid, s);
-  return wf ? launch_decode_t<0, MOE_DT_BF16, MOE_DT_F32>(a, grid, s) : launch_decode_t<0, MOE_DT_BF16, MOE_DT_BF16>(a, grid, s);
+  if (xf) return wf ? launch_decode_t<MOE_DT_F32, MOE_DT_F32, false>(a, grid, smem, s)
+                    : launch_decode_t<MOE_DT_F32, MOE_DT_BF16, false>(a, grid, smem, s);
+  return wf ? launch_decode_t<MOE_DT_BF16, MOE_DT_F32, false>(a, grid, smem, s)
+            : launch_decode_t<MOE_DT_BF16, MOE_DT_BF16, false>(a, grid, smem, s);
 }
 
 }  // namespace moe

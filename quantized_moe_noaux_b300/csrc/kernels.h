@@ -67,14 +67,17 @@ cudaError_t launch_nvfp4_quant(const void* src, int src_dtype, float* dst, size_
                                const unsigned int* amax_bits, cudaStream_t s);
 
 // ------------------------------------------------------------- fused decode path
-size_t decode_tile_bytes(int R, int K);
+// One cooperative kernel per decode step (T <= 8) reading the grouped GEMM's packed int4
+// store (shared expert at index E). Scratch per layer (sized for min(max_tokens, 8)
+// tokens): sync words (zero at creation, left zero by every call), h rows, gate/up K-split
+// partials and down outputs.
 bool decode_supported(int H, int I, int E, int top_k, int T);
-size_t decode_smem_bytes();
+size_t decode_sync_words(int I);
+size_t decode_gu_part_floats(int T, int H, int I, int E, int top_k);
+size_t decode_y_part_floats(int T, int H, int I, int top_k);
+size_t decode_h16_elems(int T, int I, int E, int top_k);
 cudaError_t decode_occupancy(int* blocks_per_sm);
 cudaError_t decode_kernels_init();
-// Repack a row-major int4-g32 matrix [R][K] into decode tiles (up = gate/up row pairing).
-cudaError_t launch_repack(const uint8_t* codes, const void* scales, int R, int K, bool up, uint8_t* dst,
-                          cudaStream_t s);
 
 struct DecodeLaunch {
   const void* x;
@@ -83,19 +86,20 @@ struct DecodeLaunch {
   const float* bias;
   int H, I, E, top_k, n_group, topk_group;
   float rsf;
-  const uint8_t* up_store;
-  const uint8_t* down_store;
+  const uint8_t* pack_up;      // grouped-GEMM packed gate/up store
+  const uint8_t* pack_dn;      // grouped-GEMM packed down store
   float* logits;
   int32_t* ids;
   float* weights;
   int32_t* offsets;
   int32_t* entries;
-  void* h16;
-  float* out_acc;
+  __half* h16;
+  float* gu_part;
+  float* y_part;
   void* out;
   uint32_t* sync;
   int* status;
-  uint32_t spin_max;
+  unsigned long long wait_ns;  // time limit of the waits on other CTAs
   unsigned long long* trace;   // optional per-CTA phase timestamps, or NULL
 };
 cudaError_t launch_decode_fused(const DecodeLaunch& d, int act_dtype, int router_dtype, int grid,

@@ -40,14 +40,15 @@ struct moe_layer {
   int* status = nullptr;
   void* x_stage = nullptr;
   void* out_stage = nullptr;
-  // fused decode path (int4-g32 layers with an int4 shared expert)
+  // fused decode path (int4-g32 layers with an int4 shared expert; reads the grouped
+  // GEMM's packed store)
   bool decode_ok = false;
+  int decode_tmax = 0;          // largest T the decode scratch is sized for
   int n_sm = 0;
-  uint8_t* up_store = nullptr;
-  uint8_t* down_store = nullptr;
   uint32_t* dsync = nullptr;
-  void* h16 = nullptr;
-  float* dec_acc = nullptr;
+  __half* dec_h16 = nullptr;
+  float* dec_gu_part = nullptr;
+  float* dec_y_part = nullptr;
   // grouped tcgen05 GEMM path
   bool gemm_ok = false;
   int gemm_rows = 0;            // rows of the expert-sorted activation matrices
@@ -69,6 +70,7 @@ struct moe_layer {
   int timing_used = 0;
   int64_t launches = 0;
   unsigned long long* trace = nullptr;   // decode-kernel phase timestamps (profiling)
+  unsigned long long wait_ns = 2000000000ull;   // limit of the kernels' waits on other CTAs
 };
 
 static constexpr int kStageEvents = 7;
@@ -259,31 +261,6 @@ moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt,
     if ((st = dev_alloc_t(L, &L->router_part, router_mma_partial_floats(L->n_sm) * 4))) return st;
   }
 
-  // fused decode path: repack the int4 experts into MMA-fragment tiles
-  L->decode_ok = c->weight_format == MOE_W_INT4_G32 && L->shared_inline &&
-                 decode_supported(H, I, E, k, 1) && decode_kernels_init() == cudaSuccess;
-  int occ = 0;
-  if (L->decode_ok && (decode_occupancy(&occ) != cudaSuccess || occ < 1)) L->decode_ok = false;
-  if (L->decode_ok) {
-    const size_t ub = decode_tile_bytes(2 * I, H), db = decode_tile_bytes(H, I);
-    const int Td = Tm < 8 ? Tm : 8;
-    const size_t nsync = (size_t)8 + E + 1;
-    if ((st = dev_alloc_t(L, &L->up_store, (size_t)(E + 1) * ub)) ||
-        (st = dev_alloc_t(L, &L->down_store, (size_t)(E + 1) * db)) ||
-        (st = dev_alloc_t(L, &L->dsync, nsync * 4)) ||
-        (st = dev_alloc(L, &L->h16, (size_t)Td * (k + 1) * I * 2)) ||
-        (st = dev_alloc_t(L, &L->dec_acc, (size_t)Td * H * 4)))
-      return st;
-    const size_t gcb = (size_t)2 * I * (H / 2), gsb = (size_t)2 * I * (H / 32) * 2;
-    const size_t dcb = (size_t)H * (I / 2), dsb = (size_t)H * (I / 32) * 2;
-    for (int e = 0; e <= E; ++e) {
-      if (launch_repack(L->w.gu_codes + e * gcb, L->w.gu_scales + e * gsb, 2 * I, H, true, L->up_store + e * ub, s) ||
-          launch_repack(L->w.d_codes + e * dcb, L->w.d_scales + e * dsb, H, I, false, L->down_store + e * db, s))
-        return MOE_ERR_CUDA;
-    }
-    if (cudaMemsetAsync(L->dsync, 0, nsync * 4, s) || cudaMemsetAsync(L->dec_acc, 0, (size_t)Td * H * 4, s))
-      return MOE_ERR_CUDA;
-  }
   // grouped GEMM path: expert-sorted activation buffers and the TMA descriptors; a
   // separately stored (bf16) shared expert gets an fp16 copy for the same kernel
   L->gemm_ok = gemm_supported(H, I) && gemm_kernels_init() == cudaSuccess &&
@@ -318,6 +295,27 @@ moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt,
       L->maps_sh_down = L->maps_down;
       L->gemm_ok = make_tmap_2d(&L->maps_sh_up.codes, L->sh16_gu, 2, H, 2 * I, 64, 128, true) &&
                    make_tmap_2d(&L->maps_sh_down.codes, L->sh16_d, 2, I, H, 64, 128, true);
+    }
+  }
+  // fused decode path: reads the grouped GEMM's packed store; scratch for min(max_tokens, 8)
+  // tokens
+  {
+    const int Td = Tm < 8 ? Tm : 8;
+    L->decode_ok = L->gemm_ok && c->weight_format == MOE_W_INT4_G32 && L->shared_inline &&
+                   decode_supported(H, I, E, k, 1) && decode_kernels_init() == cudaSuccess;
+    int occ = 0;
+    if (L->decode_ok && (decode_occupancy(&occ) != cudaSuccess || occ < 1)) L->decode_ok = false;
+    if (L->decode_ok) {
+      int td = Td;
+      while (td > 1 && !decode_supported(H, I, E, k, td)) --td;
+      L->decode_tmax = td;
+      const size_t nsync = decode_sync_words(I);
+      if ((st = dev_alloc_t(L, &L->dsync, nsync * 4)) ||
+          (st = dev_alloc_t(L, &L->dec_h16, decode_h16_elems(td, I, E, k) * 2)) ||
+          (st = dev_alloc_t(L, &L->dec_gu_part, decode_gu_part_floats(td, H, I, E, k) * 4)) ||
+          (st = dev_alloc_t(L, &L->dec_y_part, decode_y_part_floats(td, H, I, k) * 4)))
+        return st;
+      if (cudaMemsetAsync(L->dsync, 0, nsync * 4, s)) return MOE_ERR_CUDA;
     }
   }
   if (cudaMemsetAsync(L->status, 0, sizeof(int), s) || cudaMemsetAsync(L->meta, 0, 16 * 4, s))
@@ -429,7 +427,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
   StageMarks m;
   m.s = s;
   if (L->timing_used < L->timing_cap) m.ev = &L->events[(size_t)kStageEvents * L->timing_used++];
-  const bool decode = L->decode_ok && T <= 8 && (long)T * k <= 64 &&
+  const bool decode = L->decode_ok && T <= L->decode_tmax && (long)T * k <= 64 &&
                      (L->path == MOE_PATH_AUTO || L->path == MOE_PATH_GEMV);
   if (L->path == MOE_PATH_GEMV && !decode) return MOE_ERR_UNSUPPORTED;
   if (L->path == MOE_PATH_GROUPED && !L->gemm_ok) return MOE_ERR_UNSUPPORTED;
@@ -440,9 +438,9 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
     MOE_CK(m.mark(1));
     MOE_CK(m.mark(2));
     DecodeLaunch d{x, T, L->router_w, L->bias, H, I, E, k, c.n_group, c.topk_group,
-                   c.routed_scaling_factor, L->up_store, L->down_store, L->logits, L->ids,
-                   L->weights, L->offsets, L->entries, L->h16, L->dec_acc,
-                   out, L->dsync, L->status, 1u << 22, L->trace};
+                   c.routed_scaling_factor, L->gpack_up, L->gpack_down, L->logits, L->ids,
+                   L->weights, L->offsets, L->entries, L->dec_h16, L->dec_gu_part, L->dec_y_part,
+                   out, L->dsync, L->status, L->wait_ns, L->trace};
     MOE_LAUNCH(launch_decode_fused(d, c.act_dtype, c.router_dtype, L->n_sm, s));
     for (int i = 3; i < kStageEvents; ++i) MOE_CK(m.mark(i));
     return MOE_OK;
@@ -651,6 +649,20 @@ moe_status moe_layer_launch_count(moe_layer* L, int64_t* count) {
   if (!L || !count) return MOE_ERR_INVALID_ARG;
   *count = L->launches;
   return MOE_OK;
+}
+
+moe_status moe_layer_set_wait_limit(moe_layer* L, int64_t ns) {
+  if (!L || ns < 0) return MOE_ERR_INVALID_ARG;
+  L->wait_ns = (unsigned long long)ns;
+  return MOE_OK;
+}
+
+moe_status moe_layer_reset_status(moe_layer* L, void* stream) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(L->device);
+  return cudaMemsetAsync(L->status, 0, sizeof(int), static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
 }
 
 void moe_layer_destroy(moe_layer* L) {

@@ -20,10 +20,14 @@ import sys
 
 import numpy as np
 
-PHASES = ["start", "activation panel", "router rows", "all router rows seen", "shared gate/up",
-          "shared gate/up seen", "shared down", "routing seen", "routed gate/up",
-          "first routed gate/up seen", "routed down", "all down seen", "output written",
-          "producer: shared issued", "producer: routing seen"]
+PHASES = ["start", "-", "router rows written", "all router rows seen",
+          "epilogue: shared gate/up done", "epilogue: routed gate/up done", "epilogue: shared down done",
+          "selection done", "-", "-", "-", "-",
+          "epilogue: all units done", "producer: all issued", "mma: all issued", "routing done"]
+DECODE_SLOTS = ["dec wait data (cycles)", "dec wait A slot", "dec busy", "dec items (wg0)",
+                "mma wait A", "mma wait accumulator", "mma h staging", "units",
+                "epi wait accumulator", "epi busy", "epi last-arriver work", "prod wait slot",
+                "prod items issued"]
 
 GEMM_SLOTS = ["kernel", "mma_wait_operands", "mma_wait_accumulator", "dq_wait_weights",
               "dq_wait_stage", "act_producer_wait", "w_producer_wait", "epi_wait", "epi_busy",
@@ -92,30 +96,31 @@ def main(argv=None):
         t = buf.cpu().numpy()
         np.save(args.trace, t)
         t0 = t[:, 0][t[:, 0] > 0].min() if (t[:, 0] > 0).any() else 0
-        for i, name in enumerate(PHASES):
-            v = t[:, i][t[:, i] > 0] - t0
-            if v.size:
-                print(f"{i:2d} {name:26s} CTAs={v.size:3d}  min {v.min() / 1e3:8.2f}  "
-                      f"median {np.median(v) / 1e3:8.2f}  max {v.max() / 1e3:8.2f} us")
-        for i, name in ((15, "selection done"), (23, "grouping done")):
-            v = t[:, i][t[:, i] > 0] - t0
-            if v.size and (t[:, 20] > 0).any():
-                print(f"{i:2d} {name:26s} CTAs={v.size:3d}  min {v.min() / 1e3:8.2f}  "
-                      f"median {np.median(v) / 1e3:8.2f}  max {v.max() / 1e3:8.2f} us")
-        ok = (t[:, 25] > t[:, 24]) & (t[:, 12] > t[:, 0])
-        if ok.any():
-            mhz = (t[ok, 25] - t[ok, 24]) / (t[ok, 12] - t[ok, 0]) * 1e3
-            print(f"decode kernel SM clock (consumer thread 0, cycles / ns): median {np.median(mhz):.0f} MHz, "
-                  f"min {mhz.min():.0f}, max {mhz.max():.0f}")
-        if (t[:, 0] > 0).any() and (t[:, 20] > 0).any():
-            blk = t[:, 16:23].astype(np.float64)
+        decode = (t[:, 29] > 0).any()
+        if decode:
+            for i, name in enumerate(PHASES):
+                v = t[:, i][t[:, i] > 0] - t0
+                if v.size:
+                    print(f"{i:2d} {name:28s} CTAs={v.size:3d}  min {v.min() / 1e3:8.2f}  "
+                          f"median {np.median(v) / 1e3:8.2f}  max {v.max() / 1e3:8.2f} us")
+            print("CTA 0 stamps (us): " + ", ".join(f"{i}:{(t[0, i] - t0) / 1e3:.2f}" for i in (0, 2, 3, 6, 7, 15)
+                                                      if t[0, i] > 0))
+            ok = (t[:, 30] > t[:, 29]) & (t[:, 12] > t[:, 0])
+            if ok.any():
+                mhz = (t[ok, 30] - t[ok, 29]) / (t[ok, 12] - t[ok, 0]) * 1e3
+                print(f"decode kernel SM clock (epilogue thread 0, cycles / ns): median {np.median(mhz):.0f} MHz")
+            blk = t[:, 16:29].astype(np.float64)
             med = np.median(blk, axis=0)
-            names = ["consumer_wait_data", "consumer_compute", "consumer_epilogue", "consumer_transition",
-                     "items", "producer_wait_slot", "items_issued"]
-            print("decode kernel, median per CTA (cycles): " +
-                  ", ".join(f"{n}={v:.0f}" for n, v in zip(names, med)))
+            mx = blk.max(axis=0)
+            for n, v, m in zip(DECODE_SLOTS, med, mx):
+                print(f"   {n:28s} median {v:12.0f}  max {m:12.0f}")
+            for i, n in ((32, "stager wait"), (33, "mma issue blocks"), (34, "mma loop total"),
+                         (35, "dec wait routing"), (36, "dec wait h ready"), (37, "dec loop total"),
+                         (38, "dec phase 0 start"), (39, "dec phase 1 start"), (40, "dec phase 2 start"),
+                         (41, "dec phase 3 start")):
+                print(f"   {n:28s} median {np.median(t[:, i]):12.0f}  max {t[:, i].max():12.0f}")
             t = t.copy()
-            t[:, 16:23] = 0
+            t[:, 16:48] = 0
         for base, label in ((16, "gate/up GEMM"), (32, "down GEMM"), (48, "shared gate/up GEMM")):
             blk = t[:, base:base + 11].astype(np.float64)
             used = blk[:, 0] > 0

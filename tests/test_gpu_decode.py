@@ -75,3 +75,32 @@ def test_decode_path_refuses_large_t(small):
     with pytest.raises(moe.MoeError):
         layer.forward(x_to_device(x, spec.act_dtype), empty_out(9, spec.hidden, spec.act_dtype))
     layer.set_path(moe.PATH_AUTO)
+
+
+def test_decode_wait_timeout_and_recovery(small):
+    """With a wait limit of 0 the fused kernel's waits on other CTAs give up at once: the
+    forward ends (no hang) and the status word reports MOE_ERR_TIMEOUT. With the limit
+    restored and the status cleared, the next two forwards are correct again (the aborted
+    call left no stale counters behind)."""
+    import quantized_moe_noaux_b300 as moe
+    spec, arrays, layer, oracle = small
+    layer.set_path(moe.PATH_GEMV)
+    x = make_x(spec, 1, 21)
+    out = empty_out(1, spec.hidden, spec.act_dtype)
+    layer.set_wait_limit(0)
+    layer.forward(x_to_device(x, spec.act_dtype), out)
+    torch.cuda.synchronize()
+    assert layer.status() == 5            # MOE_ERR_TIMEOUT
+    layer.set_wait_limit(2_000_000_000)
+    layer.reset_status()
+    for T, step in [(1, 22), (3, 23)]:
+        x = make_x(spec, T, step)
+        out, _ = run(spec, layer, x, moe.PATH_GEMV)
+        got = layer.routing(T)
+        ref = oracle.forward(x)
+        rep = check_routing(ref, got, bias=arrays["bias"], n_group=spec.n_group,
+                            topk_group=spec.topk_group, top_k=spec.top_k, n_experts=spec.n_experts)
+        if rep["mismatch"]:
+            ref = oracle.forward(x, ids=got["ids"])
+        check_out(ref.out, out_to_host(out))
+    layer.set_path(moe.PATH_AUTO)
