@@ -215,17 +215,44 @@ def expert_bytes(spec):
 # ----------------------------------------------------------------- CPU oracle
 
 
-def oracle_tokens_per_s(spec, arrays, T, budget_s, step0=0, max_tokens=8):
+def host_cpu():
+    """(logical cores, CPU model name) of this host."""
+    model = None
+    try:
+        import subprocess
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return os.cpu_count() or 1, model
+
+
+def oracle_tokens_per_s(spec, arrays, T, budget_s, step0=0, max_tokens=8, threads=None):
     """Time the fp64 oracle on successive steps of the workload until ``budget_s``
     seconds have passed (at least one step). Each step routes all T tokens and runs the
     expert FFNs and the combine for the first min(T, max_tokens) of them (the oracle's
     ``tokens=`` restriction), so a step of a large batch stays a bounded sample (NVFP4
     layers, whose h tensor scale depends on every routed token, run the first
     min(T, max_tokens) tokens as a batch of their own instead). Returns
-    (tokens/s over the sampled tokens, steps, threads, seconds, sampled tokens per step)."""
+    (tokens/s over the sampled tokens, steps, threads, seconds, sampled tokens per step).
+    ``threads`` caps the BLAS thread pool (None: all of the host's cores)."""
     from oracle.moe_oracle import Layer
+    try:
+        from threadpoolctl import threadpool_limits
+    except ImportError:
+        threadpool_limits = None
+    cores = os.cpu_count() or 1
+    use = cores if threads is None else min(threads, cores)
+    if threadpool_limits is not None:
+        with threadpool_limits(limits=use):
+            return _oracle_loop(Layer.from_spec(spec, arrays), spec, T, budget_s, step0, max_tokens, use)
+    return _oracle_loop(Layer.from_spec(spec, arrays), spec, T, budget_s, step0, max_tokens, 1)
+
+
+def _oracle_loop(layer, spec, T, budget_s, step0, max_tokens, threads):
     from synth import make_x
-    layer = Layer.from_spec(spec, arrays)
     n = min(T, max_tokens)
     toks = np.arange(n)
     t0 = time.perf_counter()
@@ -241,11 +268,6 @@ def oracle_tokens_per_s(spec, arrays, T, budget_s, step0=0, max_tokens=8):
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    try:
-        from threadpoolctl import threadpool_info
-        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
-    except Exception:
-        threads = 1
     return steps * n / dt, steps, threads, dt, n
 
 
@@ -264,8 +286,10 @@ def run_reference(args):
     if args.warmup:
         oracle_tokens_per_s(spec, arrays, T, 0.0, step0=10_000)
     value, steps, threads, dt, n = oracle_tokens_per_s(spec, arrays, T, budget)
-    sample = (f"fp64 numpy oracle, {steps} steps of the workload (T={T} routed, expert FFNs and "
-              f"combine for {n} tokens per step), {dt:.1f} s time-bounded")
+    cores, model = host_cpu()
+    sample = (f"fp64 numpy oracle on {threads} of {cores} host threads ({model}), {steps} steps of the "
+              f"workload (T={T} routed, expert FFNs and combine for {n} tokens per step), {dt:.1f} s "
+              f"time-bounded")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * dt / steps, "higher_is_better": True, "scaling": "weak",
@@ -402,14 +426,15 @@ def run_ours(args):
     peak_tf, tf_kind = measured_tflops()
     step_s = ms / K / 1000.0
     if fused:
-        dom = "gate_up_or_fused"
+        # one kernel per step: its time per launch is the graph-timed step (the launch
+        # overhead included, so this is a lower bound of the kernel's own rate)
         dom_bytes = unit_all + K * router_b
-        dom_s = stage_ms[dom] / 1000.0
-        achieved = dom_bytes / dom_s / 1e9
+        achieved = dom_bytes / (ms / 1000.0) / 1e9
         roofline = {"bound": "hbm", "kernel": "moe_decode_kernel (router, selection, gate/up, down, combine)",
                     "achieved": achieved, "peak": peak_bw, "peak_kind": peak_kind, "unit": "GB/s",
                     "frac": achieved / peak_bw, "traffic": recorded_traffic("moe_decode_kernel", wl.name),
-                    "bytes_per_launch": dom_bytes / K}
+                    "bytes_per_launch": dom_bytes / K,
+                    "time_per_launch_ms": ms / K, "time_source": "CUDA-graph replay time per step"}
     else:
         # dominant kernel: the gate/up GEMM (2/3 of the FLOPs and of the weight bytes)
         dom = "gate_up_or_fused"
@@ -451,10 +476,14 @@ def run_ours(args):
                     "d2h_bytes_per_step": T * H * (2 if spec.act_dtype == "bf16" else 4),
                     "steps": KE}}
     if world == 1 and not args.no_cpu_baseline:
-        v, steps, threads, dt_cpu, n = oracle_tokens_per_s(spec, arrays, T, args.cpu_budget)
+        cores, model = host_cpu()
+        v, steps, threads, dt_cpu, n = oracle_tokens_per_s(spec, arrays, T, args.cpu_budget / 2)
+        v1, steps1, _, dt1, _ = oracle_tokens_per_s(spec, arrays, T, args.cpu_budget / 2, threads=1)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
-                                "sample": f"{steps} steps of the workload, T={T} routed, {n} tokens "
-                                          f"through the experts per step ({dt_cpu:.1f} s), fp64 numpy"}
+                                "model": model, "value_1_thread": v1,
+                                "sample": f"{steps} steps of the workload on {threads} threads ({dt_cpu:.1f} s) "
+                                          f"and {steps1} on 1 thread ({dt1:.1f} s), T={T} routed, {n} tokens "
+                                          f"through the experts per step, fp64 numpy"}
     print(json.dumps(line), flush=True)
     for L in layers:
         L.close()
