@@ -1,7 +1,9 @@
 """GPU parity on the GLM-5.2-shaped layer (H=6144, I=2048, E=256 + 1 shared, k=8,
 n_group=8, topk_group=4, int4 with fp16 scales per 32): decode at T=1, T=4 and T=32
 (unbiased router) and prefill at T=2048 (bias N(0, 0.5)). Routing is checked for every
-token; outputs for every token at T <= 4 and for sampled tokens above."""
+token; outputs for every token up to T=32, and at T=2048 for 320 tokens that include every
+256-row chunk boundary of the most loaded expert and every token of the experts that
+received a single token."""
 
 import numpy as np
 import pytest
@@ -73,11 +75,42 @@ def test_decode_t4(glm_base):
 
 
 def test_decode_t32(glm_base):
-    check("glm52_unbiased", glm_base, 32, 0, sample=[0, 13, 31])
+    check("glm52_unbiased", glm_base, 32, 0)
+
+
+def prefill_sample(routing, top_k, T, n=320, seed=0):
+    """Tokens whose outputs are compared at T=2048: the first and last token of every
+    256-row chunk of the most loaded expert's entry list (the grouped GEMM's tile
+    boundaries), every token of the experts that got one token, then seeded random tokens
+    up to n."""
+    off, ent = routing["offsets"], routing["entries"]
+    counts = np.diff(off)
+    e_max = int(np.argmax(counts))
+    toks = ent[off[e_max]:off[e_max + 1]] // top_k
+    pick = set()
+    for c0 in range(0, len(toks), 256):
+        pick.add(int(toks[c0]))
+        pick.add(int(toks[min(c0 + 255, len(toks) - 1)]))
+    for e in np.nonzero(counts == 1)[0]:
+        pick.add(int(ent[off[e]] // top_k))
+    rng = np.random.default_rng(seed)
+    for t in rng.permutation(T):
+        if len(pick) >= n:
+            break
+        pick.add(int(t))
+    return np.array(sorted(pick)), e_max, int(counts[e_max])
 
 
 def test_prefill_t2048(glm_base):
-    errs, counts, rep = check("glm52_skewed", glm_base, 2048, 0, sample=[0, 777, 2047])
+    spec, arrays, layer, oracle = get_layer("glm52_skewed", glm_base)
+    # routing first, to choose the compared tokens from the GPU's own entry lists
+    x = make_x(spec, 2048, 0)
+    out = empty_out(2048, spec.hidden, spec.act_dtype)
+    layer.forward(x_to_device(x, spec.act_dtype), out)
+    torch.cuda.synchronize()
+    sample, e_max, n_max = prefill_sample(layer.routing(2048), spec.top_k, 2048)
+    assert n_max > 3 * 256                                  # the heavy expert spans several chunks
+    errs, counts, rep = check("glm52_skewed", glm_base, 2048, 0, sample=sample)
     assert counts.sum() == 2048 * 8
     assert counts.max() > 4 * counts[counts > 0].mean()    # the wide bias skews the load
 
@@ -85,38 +118,38 @@ def test_prefill_t2048(glm_base):
 def test_decode_t1_bench_steps_routing(glm_base):
     """The bench's default decode workload (seeds 10..1009, one token per step, the timed
     steps of `bench.py` with its defaults) through the fused kernel: every step's
-    selection, weights and grouping against the oracle (near-tie rule); outputs for three
-    of the steps."""
+    selection, weights and the kernel's own grouping (offsets and entries) against the
+    oracle (near-tie rule); outputs for three of the steps."""
     spec, arrays, layer, oracle = get_layer("glm52", glm_base)
     from oracle.moe_oracle import group_tokens, routing_weights
     seeds = list(range(10, 1010))
     samples = {0: None, 499: None, 999: None}          # step index -> output row
     xs = np.concatenate([make_x(spec, 1, s) for s in seeds])
     k = spec.top_k
-    ids = np.empty((len(seeds), k), np.int32)
-    w = np.empty((len(seeds), k), np.float32)
     out = empty_out(1, spec.hidden, spec.act_dtype)
+    got_steps = []
     for i in range(len(seeds)):
         layer.forward(x_to_device(xs[i:i + 1], spec.act_dtype), out)
-        r = layer.routing(1)
-        ids[i], w[i] = r["ids"][0], r["weights"][0]
+        got_steps.append(layer.routing(1))
         if i in samples:
             samples[i] = out_to_host(out)[0]
     torch.cuda.synchronize()
     assert layer.status() == 0
     scores, sel = oracle.route(oracle.widen_x(xs))
 
-    class R:  # routing-only oracle result, one row per step
+    class R:  # routing-only oracle result of one step
         pass
-    ref = R()
-    ref.ids, ref.scores, ref.margin = sel.ids, scores, sel.margin
-    ref.weights = routing_weights(scores, sel.ids, spec.rsf)
-    ref.counts, ref.offsets, ref.entries = group_tokens(sel.ids, spec.n_experts)
-    _, goff, gent = group_tokens(ids.astype(np.int64), spec.n_experts)
-    got = {"ids": ids, "weights": w, "offsets": goff, "entries": gent}
-    rep = check_routing(ref, got, bias=arrays["bias"], n_group=spec.n_group,
-                        topk_group=spec.topk_group, top_k=k, n_experts=spec.n_experts)
+    mismatch = set()
+    for i, got in enumerate(got_steps):
+        ref = R()
+        ref.ids, ref.scores, ref.margin = sel.ids[i:i + 1], scores[i:i + 1], sel.margin[i:i + 1]
+        ref.weights = routing_weights(ref.scores, ref.ids, spec.rsf)
+        ref.counts, ref.offsets, ref.entries = group_tokens(ref.ids, spec.n_experts)
+        rep = check_routing(ref, got, bias=arrays["bias"], n_group=spec.n_group,
+                            topk_group=spec.topk_group, top_k=k, n_experts=spec.n_experts)
+        if rep["mismatch"]:
+            mismatch.add(i)
     for i, row in samples.items():
-        use = ids[i:i + 1] if i in rep["mismatch"] else None
+        use = got_steps[i]["ids"] if i in mismatch else None
         o = oracle.forward(xs[i:i + 1], ids=use)
         check_out(o.out, row[None])
