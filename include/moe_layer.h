@@ -234,14 +234,23 @@ moe_status moe_layer_reset_status(moe_layer* layer, void* stream);
  *      entries [T * top_k] int32 (layouts as in moe_layer_get_routing).
  * The kernels' scratch (logits, histogram, work list, status word) lives in one
  * file-scope __device__ array of about 1.04 MiB that every device loading the library
- * holds until the process exits. Limits: T * E <= 262144 and
- * T * top_k / 4 + min(T * top_k, E) + 1 <= 8192; larger problems return
- * MOE_ERR_UNSUPPORTED before any work is enqueued. Other checks as moe_layer_create.
+ * holds until the process exits. Checks, all made before any work is enqueued:
+ *   MOE_ERR_INVALID_ARG: T < 0, H <= 0, E, n_group, topk_group or top_k <= 0, an unknown
+ *     act_dtype or router_dtype, routed_scaling_factor not > 0, a NULL pointer (T > 0),
+ *     x or router_w not 16-byte aligned, bias, ids, weights, offsets or entries not
+ *     4-byte aligned;
+ *   MOE_ERR_UNSUPPORTED: E > 1024, n_group > 32 or not dividing E, fewer than 2 experts
+ *     per group, topk_group > n_group, top_k > topk_group * E / n_group or > 32, and the
+ *     scratch limits T * E <= 262144 and T * top_k / 4 + min(T * top_k, E) + 1 <= 8192.
+ * T = 0 returns MOE_OK and does nothing. Scores that are not finite (a NaN or infinite
+ * logit) give an unspecified selection: the selection kernel's check word stays in the
+ * scratch array and is not reported by this entry point.
  * The first call on a device looks up the array's device address (once per device, with
- * that device current); make that first call before any stream capture. Every call shares
- * the one array: calls whose work overlaps on the GPU (different streams, or concurrent
- * host threads) race on it and must be serialised by the caller. Asynchronous on
- * `stream`; no host synchronisation.
+ * that device current) and caches it for the life of the process; make that first call
+ * before any stream capture, and make no call after cudaDeviceReset on that device (the
+ * cached address would be stale). Every call shares the one array: calls whose work
+ * overlaps on the GPU (different streams, or concurrent host threads) race on it and must
+ * be serialised by the caller. Asynchronous on `stream`; no host synchronisation.
  */
 moe_status moe_route_noalloc(const void* x, int32_t act_dtype, int32_t T, int32_t H,
                              const void* router_w, int32_t router_dtype, const float* bias,

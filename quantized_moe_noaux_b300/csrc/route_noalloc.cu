@@ -79,6 +79,11 @@ extern "C" moe_status moe_route_noalloc(const void* x, int32_t act_dtype, int32_
     return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   if (!x || !router_w || !bias || !ids || !weights || !offsets || !entries) return MOE_ERR_INVALID_ARG;
+  // the tiled router reads x and W_r 16 bytes at a time; the other buffers hold 4-byte elements
+  auto misaligned = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; };
+  if (misaligned(x, 16) || misaligned(router_w, 16) || misaligned(bias, 4) || misaligned(ids, 4) ||
+      misaligned(weights, 4) || misaligned(offsets, 4) || misaligned(entries, 4))
+    return MOE_ERR_INVALID_ARG;
 
   unsigned char* base = nullptr;
   if (scratch_on_current_device(&base) != cudaSuccess) return MOE_ERR_CUDA;

@@ -37,11 +37,13 @@ def test_noalloc_routing_matches_layer_entry_point():
     lib = moe.lib
     spec = LAYERS["tiny"]
     arrays = make_layer(spec)
-    layer = moe.MoeLayer.from_spec(spec, arrays, max_tokens=64)
+    layer = moe.MoeLayer.from_spec(spec, arrays, max_tokens=8175)
     wr = torch.from_numpy(np.array(arrays["router_w"])).cuda()
     bias = torch.from_numpy(np.array(arrays["bias"])).cuda()
     stream = torch.cuda.current_stream().cuda_stream
-    for T, step in [(37, 11), (64, 12)]:          # two calls in a row
+    # two calls in a row with the row router, one with the tiled router (T >= 128), and the
+    # largest T whose grouping work list fits the scratch (T + E + 1 = 8192 items at k = 4)
+    for T, step in [(37, 11), (64, 12), (256, 13), (8175, 14)]:
         x = make_x(spec, T, step)
         xd = x_to_device(x, spec.act_dtype)
         out = empty_out(T, spec.hidden, spec.act_dtype)
@@ -65,3 +67,62 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
                                    spec.n_experts, spec.n_group, spec.topk_group, spec.top_k,
                                    spec.rsf, 1 << 20, 1 << 20, 1 << 20, 1 << 20, None)
     assert rc == 2   # MOE_ERR_UNSUPPORTED
+
+
+def test_noalloc_bf16_activations_match_within_near_ties():
+    """bf16 activations with an fp32 router: the layer computes the logits on the tensor
+    cores, this entry point on the CUDA cores, so their sums are rounded differently. Every
+    token whose selection margin (fp64) exceeds the near-tie bound gets the same experts
+    and weights within 1e-5; the grouping is the same wherever the selections agree."""
+    import quantized_moe_noaux_b300 as moe
+    from oracle.moe_oracle import Layer
+    from tests.parity import NEAR_TIE
+    lib = moe.lib
+    spec = LAYERS["small"]
+    arrays = make_layer(spec)
+    layer = moe.MoeLayer.from_spec(spec, arrays, max_tokens=256)
+    oracle = Layer.from_spec(spec, arrays)
+    wr = torch.from_numpy(np.array(arrays["router_w"])).cuda()
+    bias = torch.from_numpy(np.array(arrays["bias"])).cuda()
+    stream = torch.cuda.current_stream().cuda_stream
+    for T, step in [(64, 21), (256, 22)]:
+        x = make_x(spec, T, step)
+        xd = x_to_device(x, spec.act_dtype)
+        out = empty_out(T, spec.hidden, spec.act_dtype)
+        layer.forward(xd, out)
+        ref = layer.routing(T)
+        rc, ids, w, off, ent = _noalloc(lib, spec, xd, wr, bias, T, stream)
+        assert rc == 0, moe.STATUS.get(rc, rc)
+        torch.cuda.synchronize()
+        ids, w = ids.cpu().numpy(), w.cpu().numpy()
+        _, sel = oracle.route(oracle.widen_x(x))
+        same = np.array([sorted(ids[t]) == sorted(ref["ids"][t]) for t in range(T)])
+        assert np.all(same | (sel.margin <= NEAR_TIE))
+        for t in np.nonzero(same)[0]:
+            ra = dict(zip(ref["ids"][t].tolist(), ref["weights"][t].tolist()))
+            for e, wv in zip(ids[t].tolist(), w[t].tolist()):
+                assert abs(wv - ra[e]) <= 1e-5 * abs(ra[e])
+        if same.all():
+            assert np.array_equal(off.cpu().numpy(), ref["offsets"])
+            assert np.array_equal(ent.cpu().numpy(), ref["entries"])
+    layer.close()
+
+
+def test_noalloc_rejects_misaligned_activations():
+    """x must be 16-byte aligned (the tiled router reads it 16 bytes at a time): an offset
+    view is refused before anything is enqueued."""
+    import quantized_moe_noaux_b300 as moe
+    spec = LAYERS["tiny"]
+    arrays = make_layer(spec)
+    wr = torch.from_numpy(np.array(arrays["router_w"])).cuda()
+    bias = torch.from_numpy(np.array(arrays["bias"])).cuda()
+    x = torch.zeros((257, spec.hidden), dtype=torch.float32, device="cuda").view(-1)[1:1 + 256 * spec.hidden]
+    stream = torch.cuda.current_stream().cuda_stream
+    k, E, T = spec.top_k, spec.n_experts, 256
+    outs = [torch.empty(n, dtype=dt, device="cuda") for n, dt in
+            ((T * k, torch.int32), (T * k, torch.float32), (E + 1, torch.int32), (T * k, torch.int32))]
+    rc = moe.lib.moe_route_noalloc(x.data_ptr(), 0, T, spec.hidden, wr.data_ptr(), 0, bias.data_ptr(), E,
+                                   spec.n_group, spec.topk_group, k, spec.rsf, *[o.data_ptr() for o in outs],
+                                   stream)
+    assert rc == 1   # MOE_ERR_INVALID_ARG
+    torch.cuda.synchronize()
