@@ -220,6 +220,24 @@ moe_status moe_layer_set_wait_limit(moe_layer* layer, int64_t ns);
 moe_status moe_layer_reset_status(moe_layer* layer, void* stream);
 
 /*
+ * Inspection of the NVFP4 activation quantiser ("NVIDIA stellt neues GLM-5.2 NVFP4 Modell
+ * vor", section "Technische Details und Quantisierungsansatz": E2M1 elements, one E4M3 scale
+ * per 16 elements, an fp32 tensor scale). After a forward of T tokens that ran the grouped
+ * path of an NVFP4 layer whose shared expert is stored separately (the layers that use the
+ * block-scaled FP4 tensor cores), copies to HOST buffers, synchronously on `stream`:
+ *   codes  [T * top_k, hidden / 2] uint8: the expert-sorted routed rows (row q is token
+ *          entries[q] / top_k of moe_layer_get_routing), element 2j in the low nibble of
+ *          byte j;
+ *   scales [T * top_k, hidden / 16] uint8: the E4M3 scale of each 16-element block;
+ *   amax   one float: the amax of |x| over the call; the tensor scale is amax / 2688.
+ * The caller owns the buffers. Other layers return MOE_ERR_UNSUPPORTED; T outside
+ * [0, max_tokens] or a NULL pointer is MOE_ERR_INVALID_ARG. T must be the last forward's T
+ * (the contents are otherwise unspecified).
+ */
+moe_status moe_layer_get_nvfp4_act(moe_layer* layer, int32_t T, uint8_t* codes, uint8_t* scales,
+                                   float* amax, void* stream);
+
+/*
  * Routing without any allocation. The pages have no counterpart to this entry point: it
  * exists for callers that cannot call cudaMalloc when they need routing (code running
  * while a stream is captured into a CUDA graph, where allocation is not capturable; hosts

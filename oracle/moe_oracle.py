@@ -164,21 +164,24 @@ def _rne_code(mag: np.ndarray, table: np.ndarray) -> np.ndarray:
     return np.where(mag >= table[-1], len(table) - 1, j + up).astype(np.int64)
 
 
-def quantize_nvfp4_activation(a: np.ndarray) -> np.ndarray:
-    """Quantise a [M, K] activation to NVFP4 and return the dequantised values (fp64).
+def nvfp4_activation_parts(a: np.ndarray):
+    """NVFP4 quantisation of a [M, K] activation, as its three parts: the E2M1 element
+    values [M, K/16, 16] (signed, fp64), the E4M3 block scales [M, K/16] (fp64) and the fp32
+    tensor scale.
 
     Reading of the NVFP4 scheme for activations (the pages give only "FP8 scales per 16
     elements"): one dynamic fp32 tensor scale per call, ts = amax(|a|) / (6 * 448); per
     16-element block, scale = E4M3_rne_satfinite((amax16 / 6) / ts); element code =
     E2M1_rne_satfinite(a / (scale * ts)). Every quotient and product that decides a code
-    is an fp32 operation, in this order, on the fp32 value of ``a``.
+    is an fp32 operation, in this order, on the fp32 value of ``a``. ts = 0 gives zero
+    scales and codes.
     """
     a32 = np.asarray(a, dtype=np.float32)
     m, k = a32.shape
     amax = np.float32(np.max(np.abs(a32))) if a32.size else np.float32(0)
     ts = np.float32(amax / np.float32(2688.0))
     if ts == 0:
-        return np.zeros((m, k))
+        return np.zeros((m, k // 16, 16)), np.zeros((m, k // 16)), ts
     blocks = a32.reshape(m, k // 16, 16)
     bamax = np.max(np.abs(blocks), axis=2)
     ratio = ((bamax / np.float32(6.0)).astype(np.float32) / ts).astype(np.float32)
@@ -187,8 +190,15 @@ def quantize_nvfp4_activation(a: np.ndarray) -> np.ndarray:
     q = np.zeros(blocks.shape, np.float32)
     np.divide(blocks, denom[..., None], out=q, where=denom[..., None] != 0)
     mag = _E2M1_MAGS[_rne_code(np.abs(q), _E2M1_MAGS)]
-    code_val = np.sign(q) * mag
-    return (code_val * sb[..., None].astype(np.float64) * float(ts)).reshape(m, k)
+    return np.sign(q) * mag, sb, ts
+
+
+def quantize_nvfp4_activation(a: np.ndarray) -> np.ndarray:
+    """Quantise a [M, K] activation to NVFP4 (nvfp4_activation_parts) and return the
+    dequantised values code * block scale * tensor scale (fp64)."""
+    m, k = np.shape(a)
+    code_val, sb, ts = nvfp4_activation_parts(a)
+    return (code_val * sb[..., None] * float(ts)).reshape(m, k)
 
 
 # ----------------------------------------------------------------------- router

@@ -68,6 +68,7 @@ SYMBOLS = {
     "moe_layer_set_trace": (_I, [_P, _P, _I]),
     "moe_layer_set_wait_limit": (_I, [_P, ctypes.c_int64]),
     "moe_layer_reset_status": (_I, [_P, _P]),
+    "moe_layer_get_nvfp4_act": (_I, [_P, _I, _P, _P, _P, _P]),
     "moe_route_noalloc": (_I, [_P, _I, _I, _I, _P, _I, _P, _I, _I, _I, _I, ctypes.c_float,
                                _P, _P, _P, _P, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -237,6 +238,16 @@ class MoeLayer:
     def reset_status(self, stream=None):
         """Clear the sticky device status word."""
         _check("moe_layer_reset_status", _get_lib().moe_layer_reset_status(self._h, _stream(stream)))
+
+    def nvfp4_act(self, T: int, stream=None) -> dict:
+        """NVFP4 codes and E4M3 scales of the last forward's sorted routed x rows, and the
+        amax of |x| (layers on the block-scaled FP4 path)."""
+        rows, H = T * self.top_k, self.hidden
+        r = {"codes": np.empty((rows, H // 2), np.uint8), "scales": np.empty((rows, H // 16), np.uint8),
+             "amax": np.empty(1, np.float32)}
+        _check("moe_layer_get_nvfp4_act", _get_lib().moe_layer_get_nvfp4_act(
+            self._h, T, _ptr(r["codes"]), _ptr(r["scales"]), _ptr(r["amax"]), _stream(stream)))
+        return r
 
     def close(self):
         if getattr(self, "_h", None) is not None and self._h.value:

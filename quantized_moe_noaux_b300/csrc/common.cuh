@@ -93,22 +93,32 @@ __device__ __forceinline__ float siluf_acc(float z) { return z / (1.0f + expf(-z
 // E4M3_rne_satfinite((amax16 / 6) / ts), element code c[i] = E2M1_rne_satfinite(v[i] /
 // (sb * ts)), each quotient and product a correctly rounded fp32 operation in that order.
 // The dequantised element is c[i] * sb * ts. ts = 0 gives sb = 0 and all-zero codes.
-__device__ __forceinline__ void nvfp4_block(const float (&v)[16], float ts, float& sb, float (&c)[16]) {
+// nvfp4_block_bits gives the storage: the E4M3 byte of sb and the E2M1 nibble of each c[i].
+__device__ __forceinline__ void nvfp4_block_bits(const float (&v)[16], float ts, uint32_t& sbyte,
+                                                 uint32_t (&nib)[16]) {
   float bmax = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
-  sb = 0.f;
+  sbyte = 0u;
   if (ts != 0.f) {
     const float ratio = __fdiv_rn(__fdiv_rn(bmax, 6.0f), ts);
-    sb = e4m3_to_float(__nv_cvt_float_to_fp8(ratio, __NV_SATFINITE, __NV_E4M3));
+    sbyte = __nv_cvt_float_to_fp8(ratio, __NV_SATFINITE, __NV_E4M3);
   }
-  const float denom = __fmul_rn(sb, ts);
+  const float denom = __fmul_rn(e4m3_to_float(sbyte), ts);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    c[i] = 0.f;
+    nib[i] = 0u;
     if (denom != 0.f)
-      c[i] = e2m1_to_float(__nv_cvt_float_to_fp4(__fdiv_rn(v[i], denom), __NV_E2M1, cudaRoundNearest));
+      nib[i] = __nv_cvt_float_to_fp4(__fdiv_rn(v[i], denom), __NV_E2M1, cudaRoundNearest) & 15u;
   }
+}
+
+__device__ __forceinline__ void nvfp4_block(const float (&v)[16], float ts, float& sb, float (&c)[16]) {
+  uint32_t sbyte, nib[16];
+  nvfp4_block_bits(v, ts, sbyte, nib);
+  sb = e4m3_to_float(sbyte);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) c[i] = e2m1_to_float(nib[i]);
 }
 
 // ------------------------------------------------------------ weight formats

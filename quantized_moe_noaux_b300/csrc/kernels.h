@@ -138,16 +138,21 @@ struct GemmParams {
   const float* w_tscale;      // NVFP4 per-expert tensor scales of this matrix, or NULL
   const unsigned int* act_amax;   // NVFP4: amax bits of the B activations, or NULL
   int* status;
+  unsigned long long wait_ns; // time limit of every wait on another warp's or unit's work
   unsigned long long* trace;  // optional per-CTA profiling trace (64 slots per CTA), or NULL
   int trace_base;             // first slot of this launch's 11
+  // block-scaled FP4 kernel only
+  const uint8_t* wsf;         // weight scales in MMA order (fp4_pack_kernel)
+  const uint8_t* asf;         // activation E4M3 scales [rows, K / 16] of the sorted rows
 };
 bool make_tmap_2d(TensorMapBytes* out, const void* base, int elem_bytes, uint64_t inner, uint64_t rows,
                   uint32_t box_inner, uint32_t box_rows, bool swizzle128);
 bool gemm_supported(int H, int I);
-int gemm_max_items(int T, int top_k, int E, bool routed, bool shared);
+// Items of at most `chunk` rows (16..256): the fp16 kernels take 256, the FP4 kernel kFp4MaxN.
+int gemm_max_items(int T, int top_k, int E, bool routed, bool shared, int chunk);
 cudaError_t gemm_kernels_init();
-cudaError_t launch_gemm_items(const int32_t* offsets, int E, int T, int top_k, int4* items, int32_t* n_items,
-                              cudaStream_t s);
+cudaError_t launch_gemm_items(const int32_t* offsets, int E, int T, int top_k, int chunk, int4* items,
+                              int32_t* n_items, cudaStream_t s);
 cudaError_t launch_bf16_to_f16(const void* src, void* dst, size_t rows, int K, bool gate_up, int I,
                                cudaStream_t s);
 // Expert-sorted fp16 activation rows: row q < Tk is token entries[q] / top_k, row Tk + t is
@@ -157,12 +162,36 @@ cudaError_t launch_gather_act(const void* x, int act_dtype, bool nvfp4, int H, c
                               int top_k, int rows, __half* dst, const unsigned int* amax_bits, __half* xq16,
                               cudaStream_t s);
 cudaError_t launch_quant_h(const float* h, size_t n, const unsigned int* amax_bits, __half* dst, cudaStream_t s);
+// fp16 x rows Tk .. Tk + T - 1 of the sorted activation matrix (the shared expert's rows).
+cudaError_t launch_gather_shared_rows(const void* x, int act_dtype, int H, int Tk, int T, __half* dst,
+                                      cudaStream_t s);
 // Persistent launch over n_items x mtiles tiles (max_tiles bounds them; grid <= n_sm).
 cudaError_t launch_gemm(int wfmt, int epi, const GemmMaps& m, const GemmParams& p, int max_tiles, int n_sm,
                         cudaStream_t s);
 size_t gemm_pack_bytes(int rows_per_expert, int K, int n_exp);
 cudaError_t launch_gemm_pack(const uint8_t* codes, const void* scales, int K, int n_exp, int rows_per_expert,
                              int I, bool gate_up, uint8_t* dst, cudaStream_t s);
+
+// ------------------------------------ block-scaled FP4 grouped GEMM (NVFP4 layers)
+// Routed experts of NVFP4 layers with a separately stored shared expert: E2M1 weights and
+// activations straight into tcgen05.mma kind::mxf4nvf4 (gemm_fp4.cu).
+constexpr int kFp4MaxN = 128;       // token rows per tile (item chunk)
+struct Fp4Maps {
+  TensorMapBytes w;        // weight codes [n_exp * rows, K/2] uint8, 128 x 128 box, 128-byte swizzle
+  TensorMapBytes act[3];   // sorted activation codes [rows, K/2] uint8, 128 x {32, 64, 128} boxes
+};
+bool fp4_gemm_supported(int H, int I);
+cudaError_t fp4_gemm_init();
+size_t fp4_scale_bytes(int rows, int K, int n_exp);   // bytes of the MMA-ordered weight scales
+cudaError_t launch_fp4_pack(const uint8_t* codes, const uint8_t* scales, int K, int n_exp, int rows, int I,
+                            bool gate_up, uint8_t* dcodes, uint8_t* dsf, cudaStream_t s);
+// NVFP4 codes [Tk, H/2] and E4M3 scales [Tk, H/16] of the sorted routed rows (row q = token
+// entries[q] / top_k), tensor scale amax / 2688 from amax_bits.
+cudaError_t launch_quant_gather_fp4(const void* x, int act_dtype, int H, const int32_t* entries, int Tk, int top_k,
+                                    const unsigned int* amax_bits, uint8_t* codes, uint8_t* sf, cudaStream_t s);
+cudaError_t launch_quant_h_fp4(const float* h, size_t n, const unsigned int* amax_bits, uint8_t* codes, uint8_t* sf,
+                               cudaStream_t s);
+cudaError_t launch_gemm_fp4(int epi, const Fp4Maps& m, const GemmParams& p, int max_tiles, int n_sm, cudaStream_t s);
 
 // out[T, H] (act dtype) = out_acc
 cudaError_t launch_finalize(const float* out_acc, void* out, int act_dtype, size_t n,

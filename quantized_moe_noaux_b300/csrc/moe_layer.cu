@@ -63,6 +63,20 @@ struct moe_layer {
   void* sh16_gu = nullptr;      // separately stored shared expert as fp16 [2I, H], [H, I]
   void* sh16_d = nullptr;
   GemmMaps maps_sh_up{}, maps_sh_down{};
+  int gemm_chunk = 256;         // token rows per grouped-GEMM item
+  // block-scaled FP4 path of NVFP4 layers (routed experts; the bf16 shared expert keeps the
+  // fp16 kernel): weight stores in tile order with MMA-ordered scales, and the sorted
+  // NVFP4 activations of the two GEMMs
+  bool fp4_ok = false;
+  uint8_t* f4_up_codes = nullptr;
+  uint8_t* f4_up_sf = nullptr;
+  uint8_t* f4_dn_codes = nullptr;
+  uint8_t* f4_dn_sf = nullptr;
+  uint8_t* xc = nullptr;        // [T*k, H/2] codes, [T*k, H/16] scales of the sorted x rows
+  uint8_t* xsf = nullptr;
+  uint8_t* hc = nullptr;        // [T*k, I/2] codes, [T*k, I/16] scales of the routed h rows
+  uint8_t* hsf = nullptr;
+  Fp4Maps f4_up{}, f4_dn{};
   std::vector<void*> allocs;
   // measurement
   std::vector<cudaEvent_t> events;   // kStageEvents per recorded forward
@@ -268,18 +282,43 @@ moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt,
   if (L->gemm_ok) {
     const int fmt = c->weight_format;
     L->gemm_rows = Tm * k + Tm;
+    // NVFP4 routed experts with a separate shared expert run on the block-scaled FP4 kernel
+    L->fp4_ok = fmt == MOE_W_NVFP4 && !L->shared_inline && fp4_gemm_supported(H, I) &&
+                fp4_gemm_init() == cudaSuccess;
+    L->gemm_chunk = L->fp4_ok ? kFp4MaxN : 256;
     if ((st = dev_alloc(L, reinterpret_cast<void**>(&L->x16s), (size_t)L->gemm_rows * H * 2)) ||
         (st = dev_alloc(L, reinterpret_cast<void**>(&L->h16s), (size_t)L->gemm_rows * I * 2)) ||
-        (st = dev_alloc_t(L, &L->gitems, (size_t)gemm_max_items(Tm, k, E, true, true) * sizeof(int4))) ||
+        (st = dev_alloc_t(L, &L->gitems,
+                          (size_t)gemm_max_items(Tm, k, E, true, true, L->gemm_chunk) * sizeof(int4))) ||
         (st = dev_alloc_t(L, &L->g_nitems, 4 * sizeof(int32_t))))
       return st;
     if (fmt == MOE_W_NVFP4 && (st = dev_alloc_t(L, &L->h32, (size_t)Tm * k * I * 4))) return st;
-    if ((st = dev_alloc_t(L, &L->gpack_up, gemm_pack_bytes(2 * I, H, n_store))) ||
-        (st = dev_alloc_t(L, &L->gpack_down, gemm_pack_bytes(H, I, n_store))))
-      return st;
-    if (launch_gemm_pack(L->w.gu_codes, L->w.gu_scales, H, n_store, 2 * I, I, true, L->gpack_up, s) ||
-        launch_gemm_pack(L->w.d_codes, L->w.d_scales, I, n_store, H, I, false, L->gpack_down, s))
-      return MOE_ERR_CUDA;
+    if (L->fp4_ok) {
+      const size_t rk = (size_t)Tm * k;
+      if ((st = dev_alloc_t(L, &L->f4_up_codes, (size_t)E * 2 * I * (H / 2))) ||
+          (st = dev_alloc_t(L, &L->f4_up_sf, fp4_scale_bytes(2 * I, H, E))) ||
+          (st = dev_alloc_t(L, &L->f4_dn_codes, (size_t)E * H * (I / 2))) ||
+          (st = dev_alloc_t(L, &L->f4_dn_sf, fp4_scale_bytes(H, I, E))) ||
+          (st = dev_alloc_t(L, &L->xc, rk * (H / 2))) || (st = dev_alloc_t(L, &L->xsf, rk * (H / 16))) ||
+          (st = dev_alloc_t(L, &L->hc, rk * (I / 2))) || (st = dev_alloc_t(L, &L->hsf, rk * (I / 16))))
+        return st;
+      if (launch_fp4_pack(L->w.gu_codes, L->w.gu_scales, H, E, 2 * I, I, true, L->f4_up_codes, L->f4_up_sf, s) ||
+          launch_fp4_pack(L->w.d_codes, L->w.d_scales, I, E, H, I, false, L->f4_dn_codes, L->f4_dn_sf, s))
+        return MOE_ERR_CUDA;
+      bool ok = make_tmap_2d(&L->f4_up.w, L->f4_up_codes, 1, H / 2, (uint64_t)E * 2 * I, 128, 128, true) &&
+                make_tmap_2d(&L->f4_dn.w, L->f4_dn_codes, 1, I / 2, (uint64_t)E * H, 128, 128, true);
+      for (int b = 0; b < 3 && ok; ++b)
+        ok = make_tmap_2d(&L->f4_up.act[b], L->xc, 1, H / 2, rk, 128, 32u << b, true) &&
+             make_tmap_2d(&L->f4_dn.act[b], L->hc, 1, I / 2, rk, 128, 32u << b, true);
+      if (!ok) return MOE_ERR_CUDA;
+    } else {
+      if ((st = dev_alloc_t(L, &L->gpack_up, gemm_pack_bytes(2 * I, H, n_store))) ||
+          (st = dev_alloc_t(L, &L->gpack_down, gemm_pack_bytes(H, I, n_store))))
+        return st;
+      if (launch_gemm_pack(L->w.gu_codes, L->w.gu_scales, H, n_store, 2 * I, I, true, L->gpack_up, s) ||
+          launch_gemm_pack(L->w.d_codes, L->w.d_scales, I, n_store, H, I, false, L->gpack_down, s))
+        return MOE_ERR_CUDA;
+    }
     for (int b = 0; b < 4 && L->gemm_ok; ++b)
       L->gemm_ok = make_tmap_2d(&L->maps_up.act[b], L->x16s, 2, H, L->gemm_rows, 64, 32u << b, true) &&
                    make_tmap_2d(&L->maps_down.act[b], L->h16s, 2, I, L->gemm_rows, 64, 32u << b, true);
@@ -362,12 +401,20 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
   // inline shared expert: one launch covers routed and shared items (n_items[2]);
   // otherwise the routed items (n_items[0]) and the fp16 shared expert (n_items[1], after
   // the routed ones) are separate launches
-  const int routed_max = gemm_max_items(T, k, E, true, inl);
-  const int shared_max = gemm_max_items(T, k, E, false, true);
-  MOE_LAUNCH(launch_gemm_items(L->offsets, E, T, k, L->gitems, L->g_nitems, s));
+  const bool f4 = L->fp4_ok;
+  const int chunk = L->gemm_chunk;
+  const int routed_max = gemm_max_items(T, k, E, true, inl, chunk);
+  const int shared_max = gemm_max_items(T, k, E, false, true, chunk);
+  MOE_LAUNCH(launch_gemm_items(L->offsets, E, T, k, chunk, L->gitems, L->g_nitems, s));
   if (nvfp4) MOE_LAUNCH(launch_amax(x, c.act_dtype, (size_t)T * H, L->amax, s));
-  MOE_LAUNCH(launch_gather_act(x, c.act_dtype, nvfp4, H, L->entries, Tk, k, Tk + T, L->x16s, L->amax,
-                               reinterpret_cast<__half*>(L->xq), s));   // xq: [Tm, H] scratch of NVFP4 layers
+  if (f4) {
+    // routed rows as NVFP4 codes + scales; the bf16 shared expert reads fp16 x
+    MOE_LAUNCH(launch_quant_gather_fp4(x, c.act_dtype, H, L->entries, Tk, k, L->amax, L->xc, L->xsf, s));
+    MOE_LAUNCH(launch_gather_shared_rows(x, c.act_dtype, H, Tk, T, L->x16s, s));
+  } else {
+    MOE_LAUNCH(launch_gather_act(x, c.act_dtype, nvfp4, H, L->entries, Tk, k, Tk + T, L->x16s, L->amax,
+                                 reinterpret_cast<__half*>(L->xq), s));   // xq: [Tm, H] scratch of NVFP4 layers
+  }
   MOE_CK(m.mark(2));
   GemmParams p{};
   p.items = L->gitems;
@@ -383,6 +430,7 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
   p.entries = L->entries;
   p.weights = L->weights;
   p.status = L->status;
+  p.wait_ns = L->wait_ns;
   p.trace = L->trace;
   p.trace_base = 16;
   GemmParams ps = p;   // separately stored fp16 shared expert
@@ -399,10 +447,17 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
   p.wpack = L->gpack_up;
   p.w_tscale = L->w.gu_tscale;
   p.act_amax = L->amax;
-  MOE_LAUNCH(launch_gemm(c.weight_format, 0, L->maps_up, p, routed_max * p.mtiles, L->n_sm, s));
+  if (f4) {
+    p.wsf = L->f4_up_sf;
+    p.asf = L->xsf;
+    MOE_LAUNCH(launch_gemm_fp4(0, L->f4_up, p, routed_max * p.mtiles, L->n_sm, s));
+  } else {
+    MOE_LAUNCH(launch_gemm(c.weight_format, 0, L->maps_up, p, routed_max * p.mtiles, L->n_sm, s));
+  }
   if (!inl) MOE_LAUNCH(launch_gemm(kWF16, 0, L->maps_sh_up, ps, shared_max * ps.mtiles, L->n_sm, s));
   MOE_CK(m.mark(3));
-  if (nvfp4) MOE_LAUNCH(launch_quant_h(L->h32, (size_t)Tk * I, L->amax + 1, L->h16s, s));
+  if (f4) MOE_LAUNCH(launch_quant_h_fp4(L->h32, (size_t)Tk * I, L->amax + 1, L->hc, L->hsf, s));
+  else if (nvfp4) MOE_LAUNCH(launch_quant_h(L->h32, (size_t)Tk * I, L->amax + 1, L->h16s, s));
   MOE_CK(m.mark(4));
   p.K = ps.K = I;
   p.trace_base = 32;
@@ -412,7 +467,13 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
   p.wpack = L->gpack_down;
   p.w_tscale = L->w.d_tscale;
   p.act_amax = L->amax + 1;
-  MOE_LAUNCH(launch_gemm(c.weight_format, 1, L->maps_down, p, routed_max * p.mtiles, L->n_sm, s));
+  if (f4) {
+    p.wsf = L->f4_dn_sf;
+    p.asf = L->hsf;
+    MOE_LAUNCH(launch_gemm_fp4(1, L->f4_dn, p, routed_max * p.mtiles, L->n_sm, s));
+  } else {
+    MOE_LAUNCH(launch_gemm(c.weight_format, 1, L->maps_down, p, routed_max * p.mtiles, L->n_sm, s));
+  }
   if (!inl) MOE_LAUNCH(launch_gemm(kWF16, 1, L->maps_sh_down, ps, shared_max * ps.mtiles, L->n_sm, s));
   MOE_CK(m.mark(5));
   MOE_LAUNCH(launch_finalize(L->out_acc, out, c.act_dtype, (size_t)T * H, s));
@@ -655,6 +716,20 @@ moe_status moe_layer_set_wait_limit(moe_layer* L, int64_t ns) {
   if (!L || ns < 0) return MOE_ERR_INVALID_ARG;
   L->wait_ns = (unsigned long long)ns;
   return MOE_OK;
+}
+
+moe_status moe_layer_get_nvfp4_act(moe_layer* L, int32_t T, uint8_t* codes, uint8_t* scales, float* amax,
+                                   void* stream) {
+  if (!L || T < 0 || T > L->cfg.max_tokens || !codes || !scales || !amax) return MOE_ERR_INVALID_ARG;
+  if (!L->fp4_ok) return MOE_ERR_UNSUPPORTED;
+  DeviceGuard g(L->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t rows = (size_t)T * L->cfg.top_k, H = (size_t)L->cfg.hidden;
+  if (cudaMemcpyAsync(codes, L->xc, rows * (H / 2), cudaMemcpyDeviceToHost, s) ||
+      cudaMemcpyAsync(scales, L->xsf, rows * (H / 16), cudaMemcpyDeviceToHost, s) ||
+      cudaMemcpyAsync(amax, L->amax, sizeof(float), cudaMemcpyDeviceToHost, s))
+    return MOE_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status moe_layer_reset_status(moe_layer* L, void* stream) {

@@ -170,6 +170,51 @@ __device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tm
       : "memory");
 }
 
+// D[tmem] (+)= (A . SFA) (B . SFB)^T, kind::mxf4nvf4 with one E4M3 scale per 16 K elements
+// (scale_vec::4X; M = 128, K = 64): A and B packed E2M1 (two per byte) in shared memory,
+// fp32 accumulator. The four scale bytes of A row m sit in TMEM lane m % 32 (the same in all
+// four lane quarters), column sfa_tmem + m / 32, byte j for K elements 16j..16j+15; B's
+// alike with its row n in place of m.
+__device__ __forceinline__ void tc_mma_fp4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copy 32 rows x 16 bytes of shared memory (the no-swizzle K-major layout, rows 16 bytes
+// apart) into TMEM columns taddr..taddr+3 of lanes r, 32 + r, 64 + r and 96 + r (row r in
+// every lane quarter). Ordered with this thread's later tcgen05.mma.
+__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Instruction descriptor of kind::mxf4nvf4: A and B E2M1, UE4M3 scales (scale ids 0), fp32
+// accumulator, both K-major, M x N tile, dense K = 64.
+__host__ __device__ constexpr uint32_t fp4_idesc(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Nanoseconds of the global timer.
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait on an mbarrier phase for at most `limit_ns` nanoseconds; false on time-out.
+__device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // Shared-memory matrix descriptor of a K-major operand without swizzle: 8-row x 16-byte
 // core matrices, `lbo` bytes between core matrices adjacent in K, `sbo` bytes between
 // core matrices adjacent in M/N (both multiples of 16), descriptor version 1.

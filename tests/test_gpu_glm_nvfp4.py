@@ -15,6 +15,7 @@ from oracle.moe_oracle import Layer
 from synth import LAYERS, make_layer, make_x
 from tests.gpu_util import empty_out, out_to_host, x_to_device
 from tests.parity import check_out, check_routing
+from tests.test_gpu_nvfp4_act import check_act
 
 
 @pytest.fixture(scope="module")
@@ -46,6 +47,8 @@ def run(spec, arrays, layer, oracle, T, step, sample=None):
 def test_nvfp4_glm_t256_all_tokens(nvfp4_layer):
     spec, arrays, layer, oracle = nvfp4_layer
     run(spec, arrays, layer, oracle, 256, 0)
+    # the NVFP4 codes and scales the FP4 tensor cores read, byte for byte
+    check_act(spec, layer, make_x(spec, 256, 0), 256)
 
 
 def test_nvfp4_glm_t4096_sampled(nvfp4_layer):

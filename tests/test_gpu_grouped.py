@@ -85,3 +85,28 @@ def test_grouped_matches_generic_path():
 @pytest.mark.parametrize("T,step", [(9, 0), (64, 1), (300, 2)])
 def test_grouped_nvfp4_parity(T, step):
     check_layer("small_nvfp4", T, step)
+
+
+@pytest.mark.parametrize("name", ["small", "small_nvfp4"])
+def test_grouped_wait_timeout_and_recovery(name):
+    """A wait limit of 0 ns makes the grouped GEMMs' waits on their copies and MMAs give up:
+    the call reports MOE_ERR_TIMEOUT and leaves the context usable; with the limit restored
+    and the status cleared, the next forward is correct again (fp16 kernel for the int4
+    layer, block-scaled FP4 kernel for the NVFP4 layer)."""
+    import quantized_moe_noaux_b300 as moe
+    spec, _, layer, _ = get(name)
+    x = make_x(spec, 64, 21)
+    layer.set_path(moe.PATH_GROUPED)
+    layer.set_wait_limit(0)
+    try:
+        out = empty_out(64, spec.hidden, spec.act_dtype)
+        layer.forward(x_to_device(x, spec.act_dtype), out)
+        torch.cuda.synchronize()
+        assert layer.status() == 5   # MOE_ERR_TIMEOUT
+    finally:
+        layer.set_wait_limit(2_000_000_000)
+        layer.reset_status()
+        torch.cuda.synchronize()
+        layer.set_path(moe.PATH_AUTO)
+    assert layer.status() == 0
+    check_layer(name, 64, 21)
