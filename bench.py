@@ -43,6 +43,7 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle time")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--fp4-peak", action="store_true", help="measure the dense NVFP4 tensor peak and exit")
     return p.parse_args()
 
 
@@ -200,6 +201,49 @@ def measured_tflops():
         return d["bf16_tflops"], "measured burst bf16 (kind::f16 runs fp16 at the same rate)"
     except Exception:
         return 1800.0, "fallback"
+
+
+def measured_fp4_tflops():
+    """Dense NVFP4 (E2M1, E4M3 scales per 16) tensor peak: the figure `bench.py --fp4-peak`
+    measured with cuBLASLt and recorded in profiles/fp4_peak.json, else the measured bf16
+    burst peak times the nominal dense fp4/bf16 ratio (13.5 / 2.25)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "fp4_peak.json")) as f:
+            d = json.load(f)
+        return float(d["fp4_tflops"]), "measured burst nvfp4 (torch._scaled_mm, cuBLASLt)"
+    except Exception:
+        tf, _ = measured_tflops()
+        return tf * 13.5 / 2.25, "measured bf16 burst x nominal fp4/bf16 ratio 6"
+
+
+def fp4_peak():
+    """Time a dense NVFP4 GEMM (8192^3, bf16 output) through torch._scaled_mm: best of 10
+    after warm-up, CUDA events. Prints one JSON line."""
+    import torch
+    n = 8192
+    g = torch.Generator(device="cuda").manual_seed(0)
+    a = torch.randint(0, 256, (n, n // 2), dtype=torch.uint8, device="cuda", generator=g)
+    b = torch.randint(0, 256, (n, n // 2), dtype=torch.uint8, device="cuda", generator=g)
+    a, b = a.view(torch.float4_e2m1fn_x2), b.view(torch.float4_e2m1fn_x2)
+    sa = torch.full((n * n // 16,), 1.0, device="cuda").to(torch.float8_e4m3fn)
+    sb = torch.full((n * n // 16,), 1.0, device="cuda").to(torch.float8_e4m3fn)
+    f = lambda: torch._scaled_mm(a, b.t(), sa, sb, out_dtype=torch.bfloat16)
+    for _ in range(3):
+        f()
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        f()
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1000.0
+        best = t if best is None else min(best, t)
+    print(json.dumps({"fp4_tflops": 2.0 * n ** 3 / best / 1e12, "shape": [n, n, n],
+                      "how": "torch._scaled_mm float4_e2m1fn_x2 x float4_e2m1fn_x2, e4m3 scales per 16, "
+                             "bf16 out, best of 10, CUDA events", "torch": torch.__version__,
+                      "gpu": torch.cuda.get_device_name()}), flush=True)
 
 
 def expert_bytes(spec):
@@ -436,32 +480,40 @@ def run_ours(args):
                     "bytes_per_launch": dom_bytes / K,
                     "time_per_launch_ms": ms / K, "time_source": "CUDA-graph replay time per step"}
     else:
-        # dominant kernel: the gate/up GEMM (2/3 of the FLOPs and of the weight bytes)
-        dom = "gate_up_or_fused"
-        dom_s = stage_ms[dom] / 1000.0
-        rows = T * spec.top_k + T
-        flops = K * 2.0 * rows * 2 * spec.inter * spec.hidden
-        intensity = flops / unit_gu
-        if intensity > peak_tf * 1e12 / (peak_bw * 1e9):
-            achieved = flops / dom_s / 1e12
-            roofline = {"bound": "tensor", "kernel": "moe_gemm_kernel gate/up (tcgen05 kind::f16)",
-                        "achieved": achieved, "peak": peak_tf, "peak_kind": tf_kind, "unit": "TFLOP/s",
-                        "frac": achieved / peak_tf, "traffic": None, "flops_per_step": flops / K,
-                        "weight_bytes_per_step": unit_gu / K}
+        # dominant kernel: the routed gate/up GEMM (2/3 of the routed FLOPs and weight bytes;
+        # a shared expert in the routed format runs in the same launch, a bf16 one in the
+        # next stage)
+        dom_s = stage_ms["gate_up_or_fused"] / 1000.0
+        if spec.weight_format == "nvfp4" and spec.shared_format == "bf16":
+            kernel = "moe_gemm_fp4_kernel gate/up (tcgen05 kind::mxf4nvf4)"
+            rows, dom_bytes = T * spec.top_k, n_units * gu_b
+            peak_t, t_kind = measured_fp4_tflops()
         else:
-            achieved = unit_gu / dom_s / 1e9
-            roofline = {"bound": "hbm", "kernel": "moe_gemm_kernel gate/up (tcgen05 kind::f16)",
-                        "achieved": achieved, "peak": peak_bw, "peak_kind": peak_kind, "unit": "GB/s",
-                        "frac": achieved / peak_bw, "traffic": None, "bytes_per_launch": unit_gu / K,
-                        "flops_per_step": flops / K}
-        all_flops = K * 2.0 * rows * 3 * spec.inter * spec.hidden
+            kernel = "moe_gemm_kernel gate/up (tcgen05 kind::f16)"
+            rows, dom_bytes = T * spec.top_k + T, unit_gu
+            peak_t, t_kind = peak_tf, tf_kind
+        flops = K * 2.0 * rows * 2 * spec.inter * spec.hidden
+        ach_t, ach_b = flops / dom_s / 1e12, dom_bytes / dom_s / 1e9
+        tensor = flops / dom_bytes > peak_t * 1e12 / (peak_bw * 1e9)
+        roofline = {"bound": "tensor" if tensor else "hbm", "kernel": kernel,
+                    "achieved": ach_t if tensor else ach_b, "peak": peak_t if tensor else peak_bw,
+                    "peak_kind": t_kind if tensor else peak_kind, "unit": "TFLOP/s" if tensor else "GB/s",
+                    "frac": ach_t / peak_t if tensor else ach_b / peak_bw, "traffic": None,
+                    "frac_hbm": ach_b / peak_bw, "frac_tensor": ach_t / peak_t,
+                    "achieved_gbs": ach_b, "achieved_tflops": ach_t, "hbm_peak": peak_bw,
+                    "tensor_peak": peak_t, "tensor_peak_kind": t_kind,
+                    "bytes_per_launch": dom_bytes / K, "flops_per_launch": flops / K,
+                    "time_per_launch_ms": dom_s * 1000.0 / K,
+                    "time_source": "stage events around the launch, CUDA-graph replay"}
+        all_flops = K * 2.0 * (T * spec.top_k + T) * 3 * spec.inter * spec.hidden
         roofline["layer_tflops"] = all_flops / (ms / 1000.0) / 1e12
     roofline["step_expert_bytes"] = unit_all / K
     roofline["step_expert_gbs"] = unit_all / K / step_s / 1e9
     roofline["frac_of_8tbs_nominal"] = unit_all / K / step_s / 8e12
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded, random-init weights)",
+            "vs_baseline": None, "dtype": "nvfp4" if spec.weight_format == "nvfp4" else "f16",
+            "data": "synthetic (seeded, random-init weights)",
             "config": {"workload": wl.name, "tokens_per_step": T, "layer": spec.name,
                        "layer_copies": C, "l2": f"inputs larger than L2: {C} layer copies "
                        "rotated per step, each step streams its experts from HBM",
@@ -493,6 +545,9 @@ def run_ours(args):
 
 def main():
     args = parse()
+    if args.fp4_peak:
+        fp4_peak()
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -162,18 +162,21 @@ moe_status moe_layer_set_path(moe_layer* layer, int32_t path);
 moe_status moe_layer_status(moe_layer* layer);
 
 /*
- * Stage timing (for measurement): with enable = N > 0 the layer creates N x 7 CUDA
- * events and each of the next N forwards records 7 events on its stream at the stage
- * boundaries: start | routing (router logits, selection, grouping) | activation quantise
- * (NVFP4) | gate/up + SwiGLU | h quantise (NVFP4) | down + combine | output conversion |.
+ * Stage timing (for measurement): with enable = N > 0 the layer creates N x 8 CUDA
+ * events and each of the next N forwards records 8 events on its stream at the stage
+ * boundaries: start | routing (router logits, selection, grouping) | activation staging
+ * (NVFP4 quantise, expert-sorted rows) | routed gate/up + SwiGLU (with a shared expert
+ * stored in the routed format: it too; the fused decode kernel: the whole layer) |
+ * separately stored shared expert's gate/up | h quantise (NVFP4) | down + combine |
+ * output conversion |.
  * Events recorded while the stream is being captured become graph nodes and are timed
  * on replay. enable = 0 releases the events.
  */
 moe_status moe_layer_enable_timing(moe_layer* layer, int32_t enable);
 
 /*
- * Synchronise the device, then write into ms[0..5] the summed durations (milliseconds)
- * of the 6 stages over the forwards recorded since timing was enabled (or last read),
+ * Synchronise the device, then write into ms[0..6] the summed durations (milliseconds)
+ * of the 7 stages over the forwards recorded since timing was enabled (or last read),
  * and their number into *n_forwards; resets the record count. An empty stage reads 0.
  */
 moe_status moe_layer_stage_times(moe_layer* layer, float* ms, int32_t* n_forwards);

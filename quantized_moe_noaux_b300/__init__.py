@@ -76,7 +76,7 @@ SYMBOLS = {
 
 # Stage slots of moe_layer_stage_times. The fused decode kernel (routing + gate/up + down +
 # combine in one launch) is recorded in the third slot.
-STAGES = ("routing", "act_quant", "gate_up_or_fused", "h_quant", "down_combine", "output")
+STAGES = ("routing", "act_quant", "gate_up_or_fused", "shared_gate_up", "h_quant", "down_combine", "output")
 
 
 def _load():
@@ -213,7 +213,7 @@ class MoeLayer:
 
     def stage_times(self) -> tuple[dict, int]:
         """Summed stage durations (ms) over the recorded forwards, and their count."""
-        ms = (ctypes.c_float * 6)()
+        ms = (ctypes.c_float * len(STAGES))()
         n = ctypes.c_int32()
         _check("moe_layer_stage_times", _get_lib().moe_layer_stage_times(self._h, ms, ctypes.byref(n)))
         return dict(zip(STAGES, list(ms))), n.value

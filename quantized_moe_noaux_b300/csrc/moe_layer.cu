@@ -87,7 +87,7 @@ struct moe_layer {
   unsigned long long wait_ns = 2000000000ull;   // limit of the kernels' waits on other CTAs
 };
 
-static constexpr int kStageEvents = 7;
+static constexpr int kStageEvents = 8;
 
 namespace {
 
@@ -454,11 +454,12 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
   } else {
     MOE_LAUNCH(launch_gemm(c.weight_format, 0, L->maps_up, p, routed_max * p.mtiles, L->n_sm, s));
   }
-  if (!inl) MOE_LAUNCH(launch_gemm(kWF16, 0, L->maps_sh_up, ps, shared_max * ps.mtiles, L->n_sm, s));
   MOE_CK(m.mark(3));
+  if (!inl) MOE_LAUNCH(launch_gemm(kWF16, 0, L->maps_sh_up, ps, shared_max * ps.mtiles, L->n_sm, s));
+  MOE_CK(m.mark(4));
   if (f4) MOE_LAUNCH(launch_quant_h_fp4(L->h32, (size_t)Tk * I, L->amax + 1, L->hc, L->hsf, s));
   else if (nvfp4) MOE_LAUNCH(launch_quant_h(L->h32, (size_t)Tk * I, L->amax + 1, L->h16s, s));
-  MOE_CK(m.mark(4));
+  MOE_CK(m.mark(5));
   p.K = ps.K = I;
   p.trace_base = 32;
   ps.trace = nullptr;   // the shared expert's down launch is not traced
@@ -475,9 +476,9 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
     MOE_LAUNCH(launch_gemm(c.weight_format, 1, L->maps_down, p, routed_max * p.mtiles, L->n_sm, s));
   }
   if (!inl) MOE_LAUNCH(launch_gemm(kWF16, 1, L->maps_sh_down, ps, shared_max * ps.mtiles, L->n_sm, s));
-  MOE_CK(m.mark(5));
-  MOE_LAUNCH(launch_finalize(L->out_acc, out, c.act_dtype, (size_t)T * H, s));
   MOE_CK(m.mark(6));
+  MOE_LAUNCH(launch_finalize(L->out_acc, out, c.act_dtype, (size_t)T * H, s));
+  MOE_CK(m.mark(7));
   return MOE_OK;
 }
 
@@ -565,15 +566,16 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
     }
   }
   MOE_LAUNCH(launch_expert_up(a, s));
-  if (!L->shared_inline) MOE_LAUNCH(launch_expert_up(sh, s));
   MOE_CK(m.mark(3));
-  if (nvfp4) MOE_LAUNCH(launch_nvfp4_quant(L->h, MOE_DT_F32, L->h, (size_t)T * k * I, L->amax + 1, s));
+  if (!L->shared_inline) MOE_LAUNCH(launch_expert_up(sh, s));
   MOE_CK(m.mark(4));
+  if (nvfp4) MOE_LAUNCH(launch_nvfp4_quant(L->h, MOE_DT_F32, L->h, (size_t)T * k * I, L->amax + 1, s));
+  MOE_CK(m.mark(5));
   MOE_LAUNCH(launch_expert_down(a, s));
   if (!L->shared_inline) MOE_LAUNCH(launch_expert_down(sh, s));
-  MOE_CK(m.mark(5));
-  MOE_LAUNCH(launch_finalize(L->out_acc, out, c.act_dtype, (size_t)T * H, s));
   MOE_CK(m.mark(6));
+  MOE_LAUNCH(launch_finalize(L->out_acc, out, c.act_dtype, (size_t)T * H, s));
+  MOE_CK(m.mark(7));
   return MOE_OK;
 }
 
