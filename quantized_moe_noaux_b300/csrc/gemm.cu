@@ -22,11 +22,11 @@
 //              128 or 256 rows)
 //   warp 17    issues tcgen05.mma kind::f16 (M=128, N, K=16) x 4 per stage into one of two
 //              TMEM accumulators (256 columns each) and releases stages with tcgen05.commit
-//   warps 0-3  epilogue of the previous tile while the next one runs: tcgen05.ld, then
+//   warps 0-3  epilogue of the previous tile while the next one runs (gemm_tile_epilogue):
 //     gate/up: M rows pair 16 gate with 16 up rows per warp; h = SiLU(gate) * up is
 //              written to the expert-sorted h matrix (fp16, or fp32 for NVFP4 layers
 //              whose h is quantised next);
-//     down:    out_acc[token] += w[token, slot] * y (fp32 atomics; the weighted combine).
+//     down:    the expert-sorted output rows y (fp32), combined per token afterwards.
 // A separately stored bf16 shared expert (the NVFP4 layers keep it unquantised) is
 // converted to fp16 once at layer creation (exact for its range, gate/up rows stored in tile
 // order) and runs through the same kernel with each stage's 128-row weight tile loaded by
@@ -514,9 +514,12 @@ __global__ void bf16_to_f16_kernel(const uint16_t* __restrict__ src, __half* __r
 template <int XDT, bool FP4>
 __global__ void __launch_bounds__(256)
 gather_act_kernel(const void* __restrict__ x, int H, const int32_t* __restrict__ entries, int Tk, int top_k,
-                  int first_row, __half* __restrict__ dst, const __half* __restrict__ xq16) {
+                  int first_row, __half* __restrict__ dst, const __half* __restrict__ xq16,
+                  int32_t* __restrict__ inv) {
   const int q = first_row + (int)blockIdx.x;
-  const int tok = q < Tk ? __ldg(entries + q) / top_k : q - Tk;
+  const int ent = q < Tk ? __ldg(entries + q) : 0;
+  const int tok = q < Tk ? ent / top_k : q - Tk;
+  if (q < Tk && threadIdx.x == 0) inv[ent] = q;   // sorted row of each (token, slot)
   __half* drow = dst + (size_t)q * H;
   if (!FP4 || q >= Tk) {
     for (int i = threadIdx.x * 8; i < H; i += 256 * 8) {
@@ -680,7 +683,7 @@ cudaError_t launch_bf16_to_f16(const void* src, void* dst, size_t rows, int K, b
 
 cudaError_t launch_gather_act(const void* x, int act_dtype, bool nvfp4, int H, const int32_t* entries, int Tk,
                               int top_k, int rows, __half* dst, const unsigned int* amax_bits, __half* xq16,
-                              cudaStream_t s) {
+                              int32_t* inv, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const bool xf = act_dtype == MOE_DT_F32;
   if (nvfp4) {
@@ -692,11 +695,11 @@ cudaError_t launch_gather_act(const void* x, int act_dtype, bool nvfp4, int H, c
       if (xf) quant_tokens_fp4_kernel<MOE_DT_F32><<<(int)g, 256, 0, s>>>(x, nb, amax_bits, xq16);
       else quant_tokens_fp4_kernel<MOE_DT_BF16><<<(int)g, 256, 0, s>>>(x, nb, amax_bits, xq16);
     }
-    if (xf) gather_act_kernel<MOE_DT_F32, true><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, 0, dst, xq16);
-    else gather_act_kernel<MOE_DT_BF16, true><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, 0, dst, xq16);
+    if (xf) gather_act_kernel<MOE_DT_F32, true><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, 0, dst, xq16, inv);
+    else gather_act_kernel<MOE_DT_BF16, true><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, 0, dst, xq16, inv);
   } else {
-    if (xf) gather_act_kernel<MOE_DT_F32, false><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, 0, dst, nullptr);
-    else gather_act_kernel<MOE_DT_BF16, false><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, 0, dst, nullptr);
+    if (xf) gather_act_kernel<MOE_DT_F32, false><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, 0, dst, nullptr, inv);
+    else gather_act_kernel<MOE_DT_BF16, false><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, 0, dst, nullptr, inv);
   }
   return cudaGetLastError();
 }
@@ -705,9 +708,58 @@ cudaError_t launch_gather_shared_rows(const void* x, int act_dtype, int H, int T
                                       cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   if (act_dtype == MOE_DT_F32)
-    gather_act_kernel<MOE_DT_F32, false><<<T, 256, 0, s>>>(x, H, nullptr, Tk, 1, Tk, dst, nullptr);
+    gather_act_kernel<MOE_DT_F32, false><<<T, 256, 0, s>>>(x, H, nullptr, Tk, 1, Tk, dst, nullptr, nullptr);
   else
-    gather_act_kernel<MOE_DT_BF16, false><<<T, 256, 0, s>>>(x, H, nullptr, Tk, 1, Tk, dst, nullptr);
+    gather_act_kernel<MOE_DT_BF16, false><<<T, 256, 0, s>>>(x, H, nullptr, Tk, 1, Tk, dst, nullptr, nullptr);
+  return cudaGetLastError();
+}
+
+namespace {
+
+// Weighted combine of the grouped path ("routed_scaling_factor"-scaled routing weights times
+// each selected expert's output, plus the shared expert): out[t] = sum over slots j in
+// ascending order of w[t, j] * y[inv[t k + j]], then + y[T k + t], in fp32, converted once to
+// the activation dtype. A fixed order, so repeated calls give identical outputs.
+template <int DT>
+__global__ void __launch_bounds__(256)
+combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv, const float* __restrict__ w, int T,
+               int top_k, int H, void* __restrict__ out) {
+  const int t = blockIdx.x;
+  const int Tk = T * top_k;
+  for (int h = threadIdx.x * 4; h < H; h += 256 * 4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < top_k; ++j) {
+      const float wj = __ldg(w + (size_t)t * top_k + j);
+      const float4 v = __ldg(reinterpret_cast<const float4*>(y + (size_t)__ldg(inv + (size_t)t * top_k + j) * H + h));
+      acc.x += wj * v.x;
+      acc.y += wj * v.y;
+      acc.z += wj * v.z;
+      acc.w += wj * v.w;
+    }
+    const float4 sh = __ldg(reinterpret_cast<const float4*>(y + (size_t)(Tk + t) * H + h));
+    acc.x += sh.x;
+    acc.y += sh.y;
+    acc.z += sh.z;
+    acc.w += sh.w;
+    if constexpr (DT == MOE_DT_F32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(out) + (size_t)t * H + h) = acc;
+    } else {
+      const __nv_bfloat162 p0 = __floats2bfloat162_rn(acc.x, acc.y), p1 = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 o;
+      o.x = *reinterpret_cast<const uint32_t*>(&p0);
+      o.y = *reinterpret_cast<const uint32_t*>(&p1);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + (size_t)t * H + h) = o;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float* y, const int32_t* inv, const float* weights, int T, int top_k, int H,
+                           void* out, int act_dtype, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  if (act_dtype == MOE_DT_F32) combine_kernel<MOE_DT_F32><<<T, 256, 0, s>>>(y, inv, weights, T, top_k, H, out);
+  else combine_kernel<MOE_DT_BF16><<<T, 256, 0, s>>>(y, inv, weights, T, top_k, H, out);
   return cudaGetLastError();
 }
 

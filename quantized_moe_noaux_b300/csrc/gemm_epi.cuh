@@ -7,9 +7,10 @@
 //     h = SiLU(gate) * up for every token column c < n ("SwiGLU" of the expert FFN), written
 //     as fp16, or as fp32 together with the amax of the routed rows when h is quantised to
 //     NVFP4 next.
-//   down: out_acc[token] += w[token, slot] * y (fp32 atomics; the weighted combine). Column
-//     c < n is sorted row row0 + c: a routed entry (token * top_k + slot) below T * top_k,
-//     else shared-expert token row0 + c - T * top_k with weight 1.
+//   down: y row row0 + c of the expert-sorted output (a routed entry below T * top_k, else
+//     shared-expert token row0 + c - T * top_k) for every token column c < n; plain
+//     coalesced stores (a warp writes 128 consecutive bytes of one row per column), the
+//     weighted combine of the rows follows in one ordered pass (combine_kernel).
 // sc_out multiplies the accumulator first (the fp32 tensor scales of NVFP4 operands, else 1).
 #pragma once
 
@@ -51,28 +52,10 @@ __device__ __forceinline__ void gemm_tile_epilogue(uint32_t lane_addr, int N, in
         }
       }
     } else {
-      // lane j fetches the token and weight of column c0 + j; shuffles hand them round
-      int tok = 0;
-      float wt = 0.f;
-      const int c = c0 + lane;
-      if (c < n) {
-        const int q = row0 + c;
-        if (q < Tk) {
-          const int ent = __ldg(p.entries + q);
-          tok = ent / p.top_k;
-          wt = __ldg(p.weights + ent);
-        } else {
-          tok = q - Tk;
-          wt = 1.f;
-        }
-      }
-      const int hrow = 128 * mt + 32 * warp + lane;
+      float* yrow = p.y + (size_t)(row0 + c0) * p.H + 128 * mt + 32 * warp + lane;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int tj = __shfl_sync(0xffffffffu, tok, j);
-        const float wj = __shfl_sync(0xffffffffu, wt, j);
-        if (c0 + j < n) atomicAdd(p.out_acc + (size_t)tj * p.H + hrow, wj * (v[j] * sc_out));
-      }
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < n) yrow[(size_t)j * p.H] = v[j] * sc_out;
     }
   }
   if (EPI == 0 && H32) {

@@ -5,21 +5,27 @@
 // kind::mxf4nvf4 multiplies E2M1 codes block-scaled by their E4M3 scales and accumulates in
 // fp32; the two fp32 tensor scales multiply the accumulator in the epilogue.
 //
-// A tile is D = W[128 rows, K] . X[n <= 128 tokens, K]^T of one expert (weight rows on the
+// A tile is D = W[128 rows, K] . X[n <= 160 tokens, K]^T of one expert (weight rows on the
 // MMA's M side, the expert's tokens on N, as in the fp16 kernel), K walked in stages of 256
 // elements: one 128-byte row of packed codes per weight row and per token, four MMAs of
 // K = 64 each. Persistent CTAs walk the tiles (item, 128-row block) round-robin; warp roles:
-//   warp 4    TMA of the stage's 128 x 128-byte weight codes (128-byte swizzle) and one bulk
-//             copy of its 2 KB of weight scales, already in the MMA's scale order
-//   warp 5    TMA of the stage's n x 128-byte activation codes (boxes of 32, 64 or 128 rows)
-//   warp 6    activation scales: the 16 scale bytes per token of the stage, from the
-//             row-major scale matrix (four stages per load round), into the MMA's order
-//   warp 7    copies both scale blocks shared -> TMEM (tcgen05.cp, in issue order with the
-//             MMAs that read them), issues the four MMAs, releases the stage by commit
-//   warps 0-3 epilogue of the previous tile from the other TMEM accumulator
-//             (gemm_tile_epilogue: SwiGLU h rows, or the weighted combine)
-// TMEM: two 128-column accumulators and, per pipeline stage, 16 columns of weight scales and
-// 16 of activation scales (the stage's smem slot and TMEM slot are released together).
+//   warp 8     TMA of the stage's 128 x 128-byte weight codes (128-byte swizzle) and one bulk
+//              copy of its 2 KB of weight scales (laid out per MMA as 32 x 16 bytes)
+//   warp 9     TMA of the stage's n x 128-byte activation codes (boxes of 32, 64, 128 or 160
+//              rows)
+//   warps 4-7  scales into TMEM: warp 4 + q writes lanes 32q..32q+31 of the stage's scale
+//              slot with tcgen05.st, the same values in every lane quarter (the block-scaled
+//              MMA reads the scales of row 32 j + l from lane l, column j): the weight scales
+//              from shared memory, the activation scales (16 bytes per token and stage) from
+//              the row-major scale matrix, loaded four stages per round
+//   warp 10    issues the four MMAs of a stage once its operands and scales are in place and
+//              releases both rings' stages by commit (4 MMAs and 2 commits per stage: the
+//              single issuing thread is the kernel's narrowest resource)
+//   warps 0-3  epilogue of the previous tile from the other TMEM accumulator
+//              (gemm_tile_epilogue: SwiGLU h rows, or the weighted combine)
+// Rings: weights 6 stages, activations 4; the activation stage's TMEM scale slot is freed
+// with it (by the commit of the MMAs that read it). TMEM: two 160-column accumulators and
+// four 48-column scale slots (16 weight-scale + 4 x 8 activation-scale columns).
 // Every wait has a time limit (GemmParams::wait_ns); a time-out sets MOE_ERR_TIMEOUT, the
 // CTA stops issuing work, lets copies and MMAs in flight land, frees its TMEM and exits.
 #include <cuda.h>
@@ -32,31 +38,35 @@ namespace moe {
 
 namespace {
 
-constexpr int kF4WarpW = 4;
-constexpr int kF4WarpB = 5;
-constexpr int kF4WarpSF = 6;
-constexpr int kF4WarpMma = 7;
-constexpr int kF4Threads = 8 * 32;
+constexpr int kF4WarpSc = 4;              // warps 4-7: scales into TMEM
+constexpr int kF4WarpW = 8;
+constexpr int kF4WarpB = 9;
+constexpr int kF4WarpMma = 10;
+constexpr int kF4Threads = 11 * 32;
 constexpr int kF4BM = 128;
 constexpr int kF4BN = kFp4MaxN;
 constexpr int kF4BK = 256;                // K elements per stage (128 bytes of codes per row)
-constexpr int kF4Stages = 5;
+constexpr int kF4WStages = 6;             // weight ring
+constexpr int kF4BStages = 4;             // activation ring = TMEM scale slots
 constexpr int kF4A = kF4BM * 128;         // 16 KB of weight codes
-constexpr int kF4B = kF4BN * 128;         // 16 KB of activation codes
-constexpr int kF4SF = 4 * 512;            // 4 MMAs x (32 rows x 16 bytes) of scales
-constexpr int kF4AccCols = 128;
-constexpr int kF4SfCols = 32;             // per stage: 4 x 4 weight-scale + 4 x 4 activation-scale
+constexpr int kF4B = kF4BN * 128;         // 20 KB of activation codes
+constexpr int kF4SFA = 4 * 512;           // 4 MMAs x (32 rows x 16 bytes) of weight scales
+constexpr int kF4AccCols = 160;
+constexpr int kF4SlotCols = 48;           // 4 MMAs x 4 weight-scale + 4 MMAs x 8 activation-scale
+constexpr int kF4NB = kF4BN / 32;         // activation-scale columns used per MMA (5)
 constexpr uint32_t kF4TmemCols = 512;
-static_assert(kF4BN == 128, "one 512-byte scale block covers 128 token rows");
-static_assert(2 * kF4AccCols + kF4Stages * kF4SfCols <= (int)kF4TmemCols, "TMEM budget");
+static_assert(kF4BN % 32 == 0 && kF4NB <= 8, "activation scale columns per MMA");
+static_assert(2 * kF4AccCols + kF4BStages * kF4SlotCols <= (int)kF4TmemCols, "TMEM budget");
 
 struct F4Smem {
-  uint8_t a[kF4Stages][kF4A];
-  uint8_t b[kF4Stages][kF4B];
-  uint8_t sfa[kF4Stages][kF4SF];
-  uint8_t sfb[kF4Stages][kF4SF];
-  uint64_t full[kF4Stages];
-  uint64_t empty[kF4Stages];
+  uint8_t a[kF4WStages][kF4A];
+  uint8_t b[kF4BStages][kF4B];
+  uint8_t sfa[kF4WStages][kF4SFA];
+  uint64_t full_w[kF4WStages];
+  uint64_t empty_w[kF4WStages];
+  uint64_t full_b[kF4BStages];
+  uint64_t empty_b[kF4BStages];
+  uint64_t sf_full[kF4BStages];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t mma_done;
@@ -78,7 +88,7 @@ template <int EPI>
 __global__ void __launch_bounds__(kF4Threads, 1)
 moe_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b32,
                     const __grid_constant__ CUtensorMap tm_b64, const __grid_constant__ CUtensorMap tm_b128,
-                    const GemmParams p) {
+                    const __grid_constant__ CUtensorMap tm_b160, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   F4Smem& S = *reinterpret_cast<F4Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int MT = p.mtiles;
@@ -91,9 +101,14 @@ moe_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
   const unsigned long long lim = p.wait_ns;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kF4Stages; ++s) {
-      ptx::mbar_init(&S.full[s], 3);    // weight copy (+ tx), activation copy (+ tx), scale stager
-      ptx::mbar_init(&S.empty[s], 1);   // tcgen05.commit
+    for (int s = 0; s < kF4WStages; ++s) {
+      ptx::mbar_init(&S.full_w[s], 1);    // weight copies (+ tx)
+      ptx::mbar_init(&S.empty_w[s], 1);   // tcgen05.commit
+    }
+    for (int s = 0; s < kF4BStages; ++s) {
+      ptx::mbar_init(&S.full_b[s], 1);    // activation copy (+ tx)
+      ptx::mbar_init(&S.empty_b[s], 1);   // tcgen05.commit
+      ptx::mbar_init(&S.sf_full[s], 4);   // the four scale warps
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&S.tmem_full[b], 1);
@@ -122,17 +137,17 @@ moe_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
         const int4 it = __ldg(p.items + skip + t / MT);
         const int e = it.x - p.e_sub, mt = t % MT;
         const int wrow = e * p.rows_per_expert + kF4BM * mt;
-        const uint8_t* sf = p.wsf + ((size_t)e * MT + mt) * (size_t)NK * kF4SF;
+        const uint8_t* sf = p.wsf + ((size_t)e * MT + mt) * (size_t)NK * kF4SFA;
         for (int ks = 0; ks < NK; ++ks, ++kg) {
-          const int s = kg % kF4Stages;
-          if (kg >= kF4Stages && !ptx::mbar_wait_ns(&S.empty[s], ((kg / kF4Stages) - 1) & 1, lim)) {
+          const int s = kg % kF4WStages;
+          if (kg >= kF4WStages && !ptx::mbar_wait_ns(&S.empty_w[s], ((kg / kF4WStages) - 1) & 1, lim)) {
             f4_abort(S, p.status);
             stop = true;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&S.full[s], kF4A + kF4SF);
-          ptx::tma_load_2d(S.a[s], &tm_w, ks * 128, wrow, &S.full[s]);
-          ptx::bulk_g2s(S.sfa[s], sf + (size_t)ks * kF4SF, kF4SF, &S.full[s], ptx::policy_evict_first());
+          ptx::mbar_arrive_expect_tx(&S.full_w[s], kF4A + kF4SFA);
+          ptx::tma_load_2d(S.a[s], &tm_w, ks * 128, wrow, &S.full_w[s]);
+          ptx::bulk_g2s(S.sfa[s], sf + (size_t)ks * kF4SFA, kF4SFA, &S.full_w[s], ptx::policy_evict_first());
         }
       }
     }
@@ -142,32 +157,33 @@ moe_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
       ptx::prefetch_tmap(&tm_b32);
       ptx::prefetch_tmap(&tm_b64);
       ptx::prefetch_tmap(&tm_b128);
+      ptx::prefetch_tmap(&tm_b160);
       int kg = 0;
       bool stop = false;
       for (int t = blockIdx.x; t < ntiles && !stop && !f4_aborted(S); t += gridDim.x) {
         const int4 it = __ldg(p.items + skip + t / MT);
         const int row0 = it.y, n = it.z;
         // the shortest box that covers the tile; rows past it are not read by the MMA's N
-        const CUtensorMap* tm = n <= 32 ? &tm_b32 : n <= 64 ? &tm_b64 : &tm_b128;
-        const uint32_t box_bytes = (n <= 32 ? 32u : n <= 64 ? 64u : 128u) * 128u;
+        const CUtensorMap* tm = n <= 32 ? &tm_b32 : n <= 64 ? &tm_b64 : n <= 128 ? &tm_b128 : &tm_b160;
+        const uint32_t box_bytes = (n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : 160u) * 128u;
         for (int ks = 0; ks < NK; ++ks, ++kg) {
-          const int s = kg % kF4Stages;
-          if (kg >= kF4Stages && !ptx::mbar_wait_ns(&S.empty[s], ((kg / kF4Stages) - 1) & 1, lim)) {
+          const int s = kg % kF4BStages;
+          if (kg >= kF4BStages && !ptx::mbar_wait_ns(&S.empty_b[s], ((kg / kF4BStages) - 1) & 1, lim)) {
             f4_abort(S, p.status);
             stop = true;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&S.full[s], box_bytes);
-          ptx::tma_load_2d(S.b[s], tm, ks * 128, row0, &S.full[s]);
+          ptx::mbar_arrive_expect_tx(&S.full_b[s], box_bytes);
+          ptx::tma_load_2d(S.b[s], tm, ks * 128, row0, &S.full_b[s]);
         }
       }
     }
-  } else if (warp == kF4WarpSF) {
-    // --------------------------------------------------- activation scale stager
-    // Lane l owns token rows l, 32 + l, 64 + l, 96 + l of the tile; a round loads their 16
-    // scale bytes for up to four stages, then fills each stage's block: MMA kk's 512 bytes
-    // hold, at 16 r + 4 q, the four scale bytes (K blocks 16 ks + 4 kk ..) of token row
-    // 32 q + r. Rows at or past n get zero scales.
+  } else if (warp >= kF4WarpSc && warp < kF4WarpSc + 4) {
+    // ------------------------------------------------------- scales into TMEM
+    // Lane l holds, per MMA kk of the stage, the four scale bytes (K blocks 16 ks + 4 kk ..)
+    // of weight rows 32 j + l (j < 4; column 4 kk + j of the slot) and of token rows
+    // 32 c + l (c < 5; column 16 + 8 kk + c). Token rows at or past n get zero scales.
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(2 * kF4AccCols);
     const int sf_row = p.K / 16;
     int kg = 0;
     bool stop = false;
@@ -176,37 +192,50 @@ moe_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
       const int4 it = __ldg(p.items + skip + t / MT);
       const int row0 = it.y, n = it.z;
       for (int ks0 = 0; ks0 < NK && !stop; ks0 += 4) {
-        uint4 v[4][4];
+        uint4 v[4][kF4NB];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int r = lane + 32 * q;
-            v[j][q] = make_uint4(0u, 0u, 0u, 0u);
+          for (int c = 0; c < kF4NB; ++c) {
+            const int r = lane + 32 * c;
+            v[j][c] = make_uint4(0u, 0u, 0u, 0u);
             if (ks0 + j < NK && r < n)
-              v[j][q] = __ldg(reinterpret_cast<const uint4*>(p.asf + (size_t)(row0 + r) * sf_row) + ks0 + j);
+              v[j][c] = __ldg(reinterpret_cast<const uint4*>(p.asf + (size_t)(row0 + r) * sf_row) + ks0 + j);
           }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           if (ks0 + j >= NK) break;
-          const int s = kg % kF4Stages;
-          const bool ok = kg < kF4Stages || ptx::mbar_wait_ns(&S.empty[s], ((kg / kF4Stages) - 1) & 1, lim);
+          const int sw = kg % kF4WStages, sb = kg % kF4BStages;
+          // the weight scales have landed; the slot's previous MMAs have completed
+          const bool ok = ptx::mbar_wait_ns(&S.full_w[sw], (kg / kF4WStages) & 1, lim) &&
+                          (kg < kF4BStages || ptx::mbar_wait_ns(&S.empty_b[sb], ((kg / kF4BStages) - 1) & 1, lim));
           if (!__all_sync(0xffffffffu, ok)) {
             if (lane == 0) f4_abort(S, p.status);
             stop = true;
             break;
           }
-          uint32_t* dst = reinterpret_cast<uint32_t*>(S.sfb[s]) + lane * 4;
+          uint32_t lo[16], hi[32];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            dst[q] = v[j][q].x;
-            dst[128 + q] = v[j][q].y;
-            dst[256 + q] = v[j][q].z;
-            dst[384 + q] = v[j][q].w;
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint4 a = *reinterpret_cast<const uint4*>(S.sfa[sw] + kk * 512 + lane * 16);
+            lo[4 * kk] = a.x;
+            lo[4 * kk + 1] = a.y;
+            lo[4 * kk + 2] = a.z;
+            lo[4 * kk + 3] = a.w;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              uint32_t w = 0u;
+              if (c < kF4NB) w = kk == 0 ? v[j][c].x : kk == 1 ? v[j][c].y : kk == 2 ? v[j][c].z : v[j][c].w;
+              hi[8 * kk + c] = w;
+            }
           }
-          ptx::fence_proxy_async_smem();
+          const uint32_t col = lane_base + (uint32_t)(sb * kF4SlotCols);
+          ptx::tmem_st16(col, lo);
+          ptx::tmem_st32(col + 16, hi);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&S.full[s]);
+          if (lane == 0) ptx::mbar_arrive(&S.sf_full[sb]);
           ++kg;
         }
       }
@@ -228,32 +257,29 @@ moe_gemm_fp4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
         ptx::tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * kF4AccCols);
         for (int ks = 0; ks < NK; ++ks, ++kg) {
-          const int s = kg % kF4Stages;
-          if (!ptx::mbar_wait_ns(&S.full[s], (kg / kF4Stages) & 1, lim)) {
+          const int sw = kg % kF4WStages, sb = kg % kF4BStages;
+          if (!ptx::mbar_wait_ns(&S.full_w[sw], (kg / kF4WStages) & 1, lim) ||
+              !ptx::mbar_wait_ns(&S.full_b[sb], (kg / kF4BStages) & 1, lim) ||
+              !ptx::mbar_wait_ns(&S.sf_full[sb], (kg / kF4BStages) & 1, lim)) {
             f4_abort(S, p.status);
             stop = true;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sf = tmem + (uint32_t)(2 * kF4AccCols + s * kF4SfCols);
-          const uint32_t a0 = ptx::smem_u32(S.a[s]), b0 = ptx::smem_u32(S.b[s]);
-          const uint32_t sa = ptx::smem_u32(S.sfa[s]), sb = ptx::smem_u32(S.sfb[s]);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            ptx::tc_cp_32x128b_x4(sf + 4 * kk, ptx::kmajor_desc(sa + 512 * kk, 128, 128));
-            ptx::tc_cp_32x128b_x4(sf + 16 + 4 * kk, ptx::kmajor_desc(sb + 512 * kk, 128, 128));
-          }
+          const uint32_t sf = tmem + (uint32_t)(2 * kF4AccCols + sb * kF4SlotCols);
+          const uint32_t a0 = ptx::smem_u32(S.a[sw]), b0 = ptx::smem_u32(S.b[sb]);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             ptx::tc_mma_fp4(d, ptx::sw128_desc(a0 + 32 * kk), ptx::sw128_desc(b0 + 32 * kk), idesc, sf + 4 * kk,
-                            sf + 16 + 4 * kk, (ks | kk) != 0 ? 1u : 0u);
-          ptx::tc_commit(&S.empty[s]);
+                            sf + 16 + 8 * kk, (ks | kk) != 0 ? 1u : 0u);
+          ptx::tc_commit(&S.empty_w[sw]);
+          ptx::tc_commit(&S.empty_b[sb]);
         }
         if (stop) break;
         ptx::tc_commit(&S.tmem_full[buf]);
       }
     }
-  } else {
+  } else if (warp < 4) {
     // ------------------------------------------------------ epilogue (warps 0-3)
     int tc = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tc) {
@@ -358,30 +384,48 @@ __device__ __forceinline__ void fp4_block_store(const float (&v)[16], float ts, 
   *sbyte = (uint8_t)sb;
 }
 
-// Activation rows of the FP4 gate/up GEMM: sorted row q (< T * top_k) is token
-// entries[q] / top_k quantised to NVFP4 with the per-call tensor scale ts = amax / 2688:
-// codes [q][H/2], scales [q][H/16]. One CTA per sorted row.
+// NVFP4 activation of each token, once per call: x [T, H] quantised with the per-call
+// tensor scale ts = amax / 2688 into codes [T][H/2] and scales [T][H/16]. One thread per
+// 16-element block.
 template <int XDT>
 __global__ void __launch_bounds__(256)
-quant_gather_fp4_kernel(const void* __restrict__ x, int H, const int32_t* __restrict__ entries, int top_k,
-                        const unsigned int* __restrict__ amax_bits, uint8_t* __restrict__ codes,
-                        uint8_t* __restrict__ sf) {
-  const int q = blockIdx.x;
-  const int tok = __ldg(entries + q) / top_k;
+quant_tokens_fp4_kernel(const void* __restrict__ x, size_t nblocks, const unsigned int* __restrict__ amax_bits,
+                        uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
   const float ts = __fdiv_rn(__uint_as_float(__ldg(amax_bits)), 2688.0f);
-  for (int b = threadIdx.x; b < H / 16; b += 256) {
+  for (size_t b = (size_t)blockIdx.x * 256 + threadIdx.x; b < nblocks; b += (size_t)gridDim.x * 256) {
     float v[16];
     {
       float v0[8], v1[8];
-      load8_act<XDT>(x, (size_t)tok * H + 16 * b, v0);
-      load8_act<XDT>(x, (size_t)tok * H + 16 * b + 8, v1);
+      load8_act<XDT>(x, 16 * b, v0);
+      load8_act<XDT>(x, 16 * b + 8, v1);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         v[j] = v0[j];
         v[8 + j] = v1[j];
       }
     }
-    fp4_block_store(v, ts, codes + (size_t)q * (H / 2) + 8 * b, sf + (size_t)q * (H / 16) + b);
+    fp4_block_store(v, ts, codes + 8 * b, sf + b);
+  }
+}
+
+// Activation rows of the FP4 gate/up GEMM: sorted row q (< T * top_k) is a copy of token
+// entries[q] / top_k's codes [q][H/2] and scales [q][H/16]. One CTA per sorted row.
+__global__ void __launch_bounds__(256)
+gather_fp4_rows_kernel(const uint8_t* __restrict__ tok_codes, const uint8_t* __restrict__ tok_sf, int H,
+                       const int32_t* __restrict__ entries, int top_k, uint8_t* __restrict__ codes,
+                       uint8_t* __restrict__ sf, int32_t* __restrict__ inv) {
+  const int q = blockIdx.x;
+  const int ent = __ldg(entries + q);
+  const int tok = ent / top_k;
+  if (threadIdx.x == 0) inv[ent] = q;   // sorted row of each (token, slot)
+  const int nc = H / 32, ns = H / 256;   // 16-byte words of codes and of scales per row
+  const uint4* sc = reinterpret_cast<const uint4*>(tok_codes + (size_t)tok * (H / 2));
+  const uint4* ss = reinterpret_cast<const uint4*>(tok_sf + (size_t)tok * (H / 16));
+  uint4* dc = reinterpret_cast<uint4*>(codes + (size_t)q * (H / 2));
+  uint4* ds = reinterpret_cast<uint4*>(sf + (size_t)q * (H / 16));
+  for (int i = threadIdx.x; i < nc + ns; i += 256) {
+    if (i < nc) dc[i] = __ldg(sc + i);
+    else ds[i - nc] = __ldg(ss + (i - nc));
   }
 }
 
@@ -406,18 +450,19 @@ quant_h_fp4_kernel(const float* __restrict__ h, size_t nblocks, const unsigned i
   }
 }
 
-template <int EPI>
-cudaError_t launch_fp4_t(const Fp4Maps& m, const GemmParams& p, int grid, cudaStream_t s) {
-  moe_gemm_fp4_kernel<EPI><<<grid, kF4Threads, kF4SmemBytes, s>>>(
-      *reinterpret_cast<const CUtensorMap*>(&m.w), *reinterpret_cast<const CUtensorMap*>(&m.act[0]),
-      *reinterpret_cast<const CUtensorMap*>(&m.act[1]), *reinterpret_cast<const CUtensorMap*>(&m.act[2]), p);
-  return cudaGetLastError();
-}
-
 size_t grid_for(size_t n) {
   size_t g = (n + 255) / 256;
   if (g > 148 * 16) g = 148 * 16;
   return g ? g : 1;
+}
+
+template <int EPI>
+cudaError_t launch_fp4_t(const Fp4Maps& m, const GemmParams& p, int grid, cudaStream_t s) {
+  moe_gemm_fp4_kernel<EPI><<<grid, kF4Threads, kF4SmemBytes, s>>>(
+      *reinterpret_cast<const CUtensorMap*>(&m.w), *reinterpret_cast<const CUtensorMap*>(&m.act[0]),
+      *reinterpret_cast<const CUtensorMap*>(&m.act[1]), *reinterpret_cast<const CUtensorMap*>(&m.act[2]),
+      *reinterpret_cast<const CUtensorMap*>(&m.act[3]), p);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -440,13 +485,16 @@ cudaError_t launch_fp4_pack(const uint8_t* codes, const uint8_t* scales, int K, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_gather_fp4(const void* x, int act_dtype, int H, const int32_t* entries, int Tk, int top_k,
-                                    const unsigned int* amax_bits, uint8_t* codes, uint8_t* sf, cudaStream_t s) {
-  if (Tk <= 0) return cudaSuccess;
+cudaError_t launch_quant_gather_fp4(const void* x, int act_dtype, int H, int T, const int32_t* entries, int top_k,
+                                    const unsigned int* amax_bits, uint8_t* tok_codes, uint8_t* tok_sf,
+                                    uint8_t* codes, uint8_t* sf, int32_t* inv, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const size_t nb = (size_t)T * H / 16;
   if (act_dtype == MOE_DT_F32)
-    quant_gather_fp4_kernel<MOE_DT_F32><<<Tk, 256, 0, s>>>(x, H, entries, top_k, amax_bits, codes, sf);
+    quant_tokens_fp4_kernel<MOE_DT_F32><<<(int)grid_for(nb), 256, 0, s>>>(x, nb, amax_bits, tok_codes, tok_sf);
   else
-    quant_gather_fp4_kernel<MOE_DT_BF16><<<Tk, 256, 0, s>>>(x, H, entries, top_k, amax_bits, codes, sf);
+    quant_tokens_fp4_kernel<MOE_DT_BF16><<<(int)grid_for(nb), 256, 0, s>>>(x, nb, amax_bits, tok_codes, tok_sf);
+  gather_fp4_rows_kernel<<<T * top_k, 256, 0, s>>>(tok_codes, tok_sf, H, entries, top_k, codes, sf, inv);
   return cudaGetLastError();
 }
 

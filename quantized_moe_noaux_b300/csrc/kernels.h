@@ -132,7 +132,7 @@ struct GemmParams {
   __half* h16;                // gate/up output [rows, I] (fp16)
   float* h32;                 // gate/up output [rows, I] (fp32, NVFP4 layers)
   unsigned int* h_amax;       // NVFP4: amax bits of the routed h
-  float* out_acc;             // down output [T, H] (fp32 accumulator)
+  float* y;                   // down output: expert-sorted rows [rows, H] fp32 (combined later)
   const int32_t* entries;     // [T * top_k] token * top_k + slot, grouped by expert
   const float* weights;       // [T * top_k]
   const float* w_tscale;      // NVFP4 per-expert tensor scales of this matrix, or NULL
@@ -160,7 +160,12 @@ cudaError_t launch_bf16_to_f16(const void* src, void* dst, size_t rows, int K, b
 // block scale, fp16; the tensor scale from amax_bits) and copy that row for routed rows.
 cudaError_t launch_gather_act(const void* x, int act_dtype, bool nvfp4, int H, const int32_t* entries, int Tk,
                               int top_k, int rows, __half* dst, const unsigned int* amax_bits, __half* xq16,
-                              cudaStream_t s);
+                              int32_t* inv, cudaStream_t s);
+// out[t] = sum_j w[t, j] y[inv[t k + j]] + y[T k + t] (slots in ascending order, fp32), in the
+// activation dtype: the combine of the grouped path. inv[t k + j] = sorted row of entry t k + j
+// (written by the gather kernels).
+cudaError_t launch_combine(const float* y, const int32_t* inv, const float* weights, int T, int top_k, int H,
+                           void* out, int act_dtype, cudaStream_t s);
 cudaError_t launch_quant_h(const float* h, size_t n, const unsigned int* amax_bits, __half* dst, cudaStream_t s);
 // fp16 x rows Tk .. Tk + T - 1 of the sorted activation matrix (the shared expert's rows).
 cudaError_t launch_gather_shared_rows(const void* x, int act_dtype, int H, int Tk, int T, __half* dst,
@@ -175,20 +180,22 @@ cudaError_t launch_gemm_pack(const uint8_t* codes, const void* scales, int K, in
 // ------------------------------------ block-scaled FP4 grouped GEMM (NVFP4 layers)
 // Routed experts of NVFP4 layers with a separately stored shared expert: E2M1 weights and
 // activations straight into tcgen05.mma kind::mxf4nvf4 (gemm_fp4.cu).
-constexpr int kFp4MaxN = 128;       // token rows per tile (item chunk)
+constexpr int kFp4MaxN = 160;       // token rows per tile (item chunk)
 struct Fp4Maps {
   TensorMapBytes w;        // weight codes [n_exp * rows, K/2] uint8, 128 x 128 box, 128-byte swizzle
-  TensorMapBytes act[3];   // sorted activation codes [rows, K/2] uint8, 128 x {32, 64, 128} boxes
+  TensorMapBytes act[4];   // sorted activation codes [rows, K/2] uint8, 128 x {32, 64, 128, 160} boxes
 };
 bool fp4_gemm_supported(int H, int I);
 cudaError_t fp4_gemm_init();
 size_t fp4_scale_bytes(int rows, int K, int n_exp);   // bytes of the MMA-ordered weight scales
 cudaError_t launch_fp4_pack(const uint8_t* codes, const uint8_t* scales, int K, int n_exp, int rows, int I,
                             bool gate_up, uint8_t* dcodes, uint8_t* dsf, cudaStream_t s);
-// NVFP4 codes [Tk, H/2] and E4M3 scales [Tk, H/16] of the sorted routed rows (row q = token
-// entries[q] / top_k), tensor scale amax / 2688 from amax_bits.
-cudaError_t launch_quant_gather_fp4(const void* x, int act_dtype, int H, const int32_t* entries, int Tk, int top_k,
-                                    const unsigned int* amax_bits, uint8_t* codes, uint8_t* sf, cudaStream_t s);
+// NVFP4 codes [T*k, H/2] and E4M3 scales [T*k, H/16] of the sorted routed rows (row q =
+// token entries[q] / top_k), tensor scale amax / 2688 from amax_bits; each token is
+// quantised once into tok_codes [T, H/2] / tok_sf [T, H/16], then copied to its rows.
+cudaError_t launch_quant_gather_fp4(const void* x, int act_dtype, int H, int T, const int32_t* entries, int top_k,
+                                    const unsigned int* amax_bits, uint8_t* tok_codes, uint8_t* tok_sf,
+                                    uint8_t* codes, uint8_t* sf, int32_t* inv, cudaStream_t s);
 cudaError_t launch_quant_h_fp4(const float* h, size_t n, const unsigned int* amax_bits, uint8_t* codes, uint8_t* sf,
                                cudaStream_t s);
 cudaError_t launch_gemm_fp4(int epi, const Fp4Maps& m, const GemmParams& p, int max_tiles, int n_sm, cudaStream_t s);

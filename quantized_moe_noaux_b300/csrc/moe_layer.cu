@@ -54,6 +54,8 @@ struct moe_layer {
   int gemm_rows = 0;            // rows of the expert-sorted activation matrices
   __half* x16s = nullptr;       // [gemm_rows, H] expert-sorted activations (fp16)
   __half* h16s = nullptr;       // [gemm_rows, I] expert-sorted h (fp16)
+  float* ys = nullptr;          // [gemm_rows, H] expert-sorted down outputs (fp32)
+  int32_t* inv = nullptr;       // [T*k] sorted row of each (token, slot)
   float* h32 = nullptr;         // [T*k, I] routed h before NVFP4 quantisation
   int4* gitems = nullptr;
   int32_t* g_nitems = nullptr;
@@ -76,6 +78,8 @@ struct moe_layer {
   uint8_t* xsf = nullptr;
   uint8_t* hc = nullptr;        // [T*k, I/2] codes, [T*k, I/16] scales of the routed h rows
   uint8_t* hsf = nullptr;
+  uint8_t* xtc = nullptr;       // [T, H/2] codes, [T, H/16] scales of each token's x
+  uint8_t* xts = nullptr;
   Fp4Maps f4_up{}, f4_dn{};
   std::vector<void*> allocs;
   // measurement
@@ -288,6 +292,8 @@ moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt,
     L->gemm_chunk = L->fp4_ok ? kFp4MaxN : 256;
     if ((st = dev_alloc(L, reinterpret_cast<void**>(&L->x16s), (size_t)L->gemm_rows * H * 2)) ||
         (st = dev_alloc(L, reinterpret_cast<void**>(&L->h16s), (size_t)L->gemm_rows * I * 2)) ||
+        (st = dev_alloc_t(L, &L->ys, (size_t)L->gemm_rows * H * 4)) ||
+        (st = dev_alloc_t(L, &L->inv, (size_t)Tm * k * 4)) ||
         (st = dev_alloc_t(L, &L->gitems,
                           (size_t)gemm_max_items(Tm, k, E, true, true, L->gemm_chunk) * sizeof(int4))) ||
         (st = dev_alloc_t(L, &L->g_nitems, 4 * sizeof(int32_t))))
@@ -300,16 +306,19 @@ moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt,
           (st = dev_alloc_t(L, &L->f4_dn_codes, (size_t)E * H * (I / 2))) ||
           (st = dev_alloc_t(L, &L->f4_dn_sf, fp4_scale_bytes(H, I, E))) ||
           (st = dev_alloc_t(L, &L->xc, rk * (H / 2))) || (st = dev_alloc_t(L, &L->xsf, rk * (H / 16))) ||
-          (st = dev_alloc_t(L, &L->hc, rk * (I / 2))) || (st = dev_alloc_t(L, &L->hsf, rk * (I / 16))))
+          (st = dev_alloc_t(L, &L->hc, rk * (I / 2))) || (st = dev_alloc_t(L, &L->hsf, rk * (I / 16))) ||
+          (st = dev_alloc_t(L, &L->xtc, (size_t)Tm * (H / 2))) || (st = dev_alloc_t(L, &L->xts, (size_t)Tm * (H / 16))))
         return st;
       if (launch_fp4_pack(L->w.gu_codes, L->w.gu_scales, H, E, 2 * I, I, true, L->f4_up_codes, L->f4_up_sf, s) ||
           launch_fp4_pack(L->w.d_codes, L->w.d_scales, I, E, H, I, false, L->f4_dn_codes, L->f4_dn_sf, s))
         return MOE_ERR_CUDA;
       bool ok = make_tmap_2d(&L->f4_up.w, L->f4_up_codes, 1, H / 2, (uint64_t)E * 2 * I, 128, 128, true) &&
                 make_tmap_2d(&L->f4_dn.w, L->f4_dn_codes, 1, I / 2, (uint64_t)E * H, 128, 128, true);
-      for (int b = 0; b < 3 && ok; ++b)
-        ok = make_tmap_2d(&L->f4_up.act[b], L->xc, 1, H / 2, rk, 128, 32u << b, true) &&
-             make_tmap_2d(&L->f4_dn.act[b], L->hc, 1, I / 2, rk, 128, 32u << b, true);
+      for (int b = 0; b < 4 && ok; ++b) {
+        const uint32_t box = b < 3 ? 32u << b : (uint32_t)kFp4MaxN;
+        ok = make_tmap_2d(&L->f4_up.act[b], L->xc, 1, H / 2, rk, 128, box, true) &&
+             make_tmap_2d(&L->f4_dn.act[b], L->hc, 1, I / 2, rk, 128, box, true);
+      }
       if (!ok) return MOE_ERR_CUDA;
     } else {
       if ((st = dev_alloc_t(L, &L->gpack_up, gemm_pack_bytes(2 * I, H, n_store))) ||
@@ -409,11 +418,12 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
   if (nvfp4) MOE_LAUNCH(launch_amax(x, c.act_dtype, (size_t)T * H, L->amax, s));
   if (f4) {
     // routed rows as NVFP4 codes + scales; the bf16 shared expert reads fp16 x
-    MOE_LAUNCH(launch_quant_gather_fp4(x, c.act_dtype, H, L->entries, Tk, k, L->amax, L->xc, L->xsf, s));
+    MOE_LAUNCH(launch_quant_gather_fp4(x, c.act_dtype, H, T, L->entries, k, L->amax, L->xtc, L->xts, L->xc, L->xsf,
+                                       L->inv, s));
     MOE_LAUNCH(launch_gather_shared_rows(x, c.act_dtype, H, Tk, T, L->x16s, s));
   } else {
     MOE_LAUNCH(launch_gather_act(x, c.act_dtype, nvfp4, H, L->entries, Tk, k, Tk + T, L->x16s, L->amax,
-                                 reinterpret_cast<__half*>(L->xq), s));   // xq: [Tm, H] scratch of NVFP4 layers
+                                 reinterpret_cast<__half*>(L->xq), L->inv, s));   // xq: [Tm, H] NVFP4 scratch
   }
   MOE_CK(m.mark(2));
   GemmParams p{};
@@ -426,7 +436,7 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
   p.h16 = L->h16s;
   p.h32 = L->h32;
   p.h_amax = L->amax + 1;
-  p.out_acc = L->out_acc;
+  p.y = L->ys;
   p.entries = L->entries;
   p.weights = L->weights;
   p.status = L->status;
@@ -477,7 +487,7 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
   }
   if (!inl) MOE_LAUNCH(launch_gemm(kWF16, 1, L->maps_sh_down, ps, shared_max * ps.mtiles, L->n_sm, s));
   MOE_CK(m.mark(6));
-  MOE_LAUNCH(launch_finalize(L->out_acc, out, c.act_dtype, (size_t)T * H, s));
+  MOE_LAUNCH(launch_combine(L->ys, L->inv, L->weights, T, k, H, out, c.act_dtype, s));
   MOE_CK(m.mark(7));
   return MOE_OK;
 }
@@ -510,7 +520,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
   MOE_CK(m.mark(0));
   MOE_CK(cudaMemsetAsync(L->counts, 0, (E + 1) * sizeof(int32_t), s));
   MOE_CK(cudaMemsetAsync(L->amax, 0, 4 * sizeof(unsigned int), s));
-  MOE_CK(cudaMemsetAsync(L->out_acc, 0, (size_t)T * H * sizeof(float), s));
+  if (!gemm) MOE_CK(cudaMemsetAsync(L->out_acc, 0, (size_t)T * H * sizeof(float), s));
   if (L->router_planes)
     MOE_LAUNCH(launch_router_mma(x, L->router_planes, L->router_nplanes, L->logits, L->router_part, T, E, H,
                                  L->n_sm, s));
