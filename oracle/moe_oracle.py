@@ -263,26 +263,77 @@ def select_experts(scores: np.ndarray, bias: np.ndarray, n_group: int, topk_grou
 
 
 def routing_weights(scores: np.ndarray, ids: np.ndarray, rsf: float) -> np.ndarray:
-    """w[t, j] = s[t, ids[t, j]] / sum_j s[t, ids[t, j]] * routed_scaling_factor."""
-    sel = np.take_along_axis(np.asarray(scores, np.float64), ids, axis=1)
+    """w[t, j] = s[t, ids[t, j]] / sum_j s[t, ids[t, j]] * routed_scaling_factor, the sum
+    over the routed slots; a slot dropped by the adaptive top-p (id -1) has weight 0."""
+    ids = np.asarray(ids)
+    routed = ids >= 0
+    sel = np.where(routed, np.take_along_axis(np.asarray(scores, np.float64), np.where(routed, ids, 0), axis=1),
+                   0.0)
     return sel / sel.sum(axis=1, keepdims=True) * float(np.float32(rsf))
 
 
 def group_tokens(ids: np.ndarray, n_experts: int):
     """Batch-union grouping: counts[E], offsets[E+1] (exclusive scan) and the entry list
-    [T*k] holding token*top_k + slot, grouped by expert, ascending token in each group."""
+    holding token*top_k + slot of every routed slot (id >= 0), grouped by expert, ascending
+    token in each group."""
     t_count, k = ids.shape
-    counts = np.bincount(ids.ravel(), minlength=n_experts)[:n_experts]
+    flat = np.asarray(ids).ravel()
+    counts = np.bincount(flat[flat >= 0], minlength=n_experts)[:n_experts]
     offsets = np.zeros(n_experts + 1, np.int64)
     offsets[1:] = np.cumsum(counts)
-    lst = np.empty(t_count * k, np.int64)
+    lst = np.empty(int(offsets[-1]), np.int64)
     cursor = offsets[:-1].copy()
     for t in range(t_count):
         for j in range(k):
             e = ids[t, j]
+            if e < 0:
+                continue
             lst[cursor[e]] = t * k + j
             cursor[e] += 1
     return counts, offsets, lst
+
+
+# ------------------------------------------------------- adaptive expert top-p
+
+
+@dataclass
+class TopP:
+    keep: np.ndarray     # [T, top_k] bool: the slot stays routed
+    margin: np.ndarray   # [T] distance of the decision from its threshold (relative), inf if none
+
+
+def expert_top_p(scores: np.ndarray, ids: np.ndarray, p: float) -> TopP:
+    """Adaptive expert top-p (the "--topp" option of "Show HN: Menjalankan GLM 5.2 di komputer
+    lambat", section "Mengunduh model dan menjalankannya": fewer experts per token, less
+    expert data read; section "Benchmark komunitas" for its effect). The pages do not state
+    the rule. Reading: order the top_k experts the selection chose by their unbiased score s,
+    largest first (equal scores: lower expert index first), and keep the shortest prefix
+    whose summed s reaches p times the summed s of all top_k: an expert stays when the mass
+    ranked before it is below p times the total, so the first always stays. p <= 0 or p >= 1
+    keeps every slot. margin[t]: the smallest |mass before rank r - p * total| over r >= 1,
+    and the score gap across the cut, each divided by the total."""
+    s = np.asarray(scores, np.float64)
+    ids = np.asarray(ids, np.int64)
+    t_count, k = ids.shape
+    keep = np.ones((t_count, k), bool)
+    margin = np.full(t_count, np.inf)
+    if not 0.0 < p < 1.0:
+        return TopP(keep, margin)
+    for t in range(t_count):
+        sel = s[t, ids[t]]
+        order = np.lexsort((ids[t], -sel))          # s descending, then lower id
+        ranked = sel[order]
+        total = ranked.sum()
+        before = np.concatenate([[0.0], np.cumsum(ranked)[:-1]])
+        kept = before < p * total
+        keep[t, order] = kept
+        if k > 1:
+            m = np.min(np.abs(before[1:] - p * total))
+            n_kept = int(kept.sum())
+            if n_kept < k:
+                m = min(m, ranked[n_kept - 1] - ranked[n_kept])
+            margin[t] = m / total
+    return TopP(keep, margin)
 
 
 # ------------------------------------------------------------------- expert FFN
@@ -361,11 +412,12 @@ class Layer:
     """Weights of one layer as the oracle sees them (dequantised lazily, per expert)."""
 
     def __init__(self, arrays: dict, *, hidden, inter, n_experts, top_k, n_group, topk_group,
-                 rsf, weight_format, act_dtype, router_dtype, shared_format):
+                 rsf, weight_format, act_dtype, router_dtype, shared_format, expert_top_p=0.0):
         self.a = arrays
         self.H, self.I, self.E = hidden, inter, n_experts
         self.top_k, self.n_group, self.topk_group = top_k, n_group, topk_group
         self.rsf = rsf
+        self.expert_top_p = expert_top_p
         self.weight_format, self.act_dtype = weight_format, act_dtype
         self.router_dtype, self.shared_format = router_dtype, shared_format
 
@@ -374,7 +426,8 @@ class Layer:
         return cls(arrays, hidden=spec.hidden, inter=spec.inter, n_experts=spec.n_experts,
                    top_k=spec.top_k, n_group=spec.n_group, topk_group=spec.topk_group,
                    rsf=spec.rsf, weight_format=spec.weight_format, act_dtype=spec.act_dtype,
-                   router_dtype=spec.router_dtype, shared_format=spec.shared_format)
+                   router_dtype=spec.router_dtype, shared_format=spec.shared_format,
+                   expert_top_p=getattr(spec, "expert_top_p", 0.0))
 
     # -- weights
     def router_w(self) -> np.ndarray:
@@ -427,7 +480,14 @@ class Layer:
         x64 = self.widen_x(x)
         t_count = x64.shape[0]
         scores, sel = self.route(x64)
-        use_ids = sel.ids if ids is None else np.asarray(ids, np.int64)
+        margin = sel.margin
+        if ids is None:
+            # adaptive expert top-p: dropped slots get id -1 (no-op unless 0 < p < 1)
+            tp = expert_top_p(scores, sel.ids, self.expert_top_p)
+            use_ids = np.where(tp.keep, sel.ids, -1)
+            margin = np.minimum(margin, tp.margin)
+        else:
+            use_ids = np.asarray(ids, np.int64)
         w = routing_weights(scores, use_ids, self.rsf)
         counts, offsets, entries = group_tokens(use_ids, self.E)
         rows = np.arange(t_count) if tokens is None else np.asarray(tokens, np.int64)
@@ -461,4 +521,4 @@ class Layer:
         sh_gu, sh_d = self.shared_expert()
         xs = shared_expert_input(self.shared_format, x64, x_in)[rows]
         out[rows] += down_proj(sh_d, hidden(sh_gu, xs))
-        return LayerRef(out, use_ids, w, scores, sel.margin, counts, offsets, entries)
+        return LayerRef(out, use_ids, w, scores, margin, counts, offsets, entries)

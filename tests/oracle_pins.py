@@ -331,6 +331,56 @@ def pin_group_tokens(O):
     assert sorted(lst.tolist()) == list(range(T * k))
 
 
+def _top_p_case(O, c, E=8):
+    k = len(c["ids"])
+    scores = np.full((1, E), 0.01)
+    ids = np.asarray([c["ids"]], np.int64)
+    scores[0, ids[0]] = c["scores_of_slots"]
+    tp = O.expert_top_p(scores, ids, c["p"])
+    routed = np.where(tp.keep, ids, -1)
+    w = O.routing_weights(scores, routed, 2.5)
+    return tp, routed, w, k
+
+
+def pin_expert_top_p_hand(O):
+    """Hand-worked adaptive top-p cases (tests/golden/hand_expert_top_p.json)."""
+    with open(os.path.join(GOLDEN, "hand_expert_top_p.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        tp, routed, w, k = _top_p_case(O, c)
+        assert tp.keep[0].tolist() == c["keep"], (c["p"], tp.keep[0].tolist())
+        assert np.allclose(w[0], c["weights"], rtol=1e-15, atol=0), (c["p"], w[0])
+
+
+def pin_expert_top_p_invariants(O):
+    """On random scores: the kept mass reaches p * total and dropping the smallest kept
+    score would fall below it (shortest prefix); kept scores are the largest ones; the
+    weights are 0 on dropped slots, sum to rsf and stay proportional to s; grouping skips
+    dropped slots."""
+    rng = np.random.default_rng(11)
+    E, k = 32, 8
+    for p in (0.3, 0.7, 0.9):
+        s = O.sigmoid(rng.standard_normal((40, E)))
+        ids = np.stack([rng.choice(E, k, replace=False) for _ in range(40)])
+        tp = O.expert_top_p(s, ids, p)
+        routed = np.where(tp.keep, ids, -1)
+        w = O.routing_weights(s, routed, 2.5)
+        for t in range(40):
+            sel = s[t, ids[t]]
+            kept = sel[tp.keep[t]]
+            assert kept.sum() >= p * sel.sum() - 1e-15
+            assert kept.sum() - kept.min() < p * sel.sum()
+            if (~tp.keep[t]).any():
+                assert kept.min() >= sel[~tp.keep[t]].max()
+            assert np.all(w[t][~tp.keep[t]] == 0)
+            assert abs(w[t].sum() - 2.5) < 1e-13
+            ratio = w[t][tp.keep[t]] / kept
+            assert np.allclose(ratio, ratio[0], rtol=1e-13)
+        counts, offsets, lst = O.group_tokens(routed, E)
+        assert offsets[-1] == tp.keep.sum() == lst.size
+        assert np.all(routed.ravel()[lst] >= 0)
+
+
 # ------------------------------------------------------------------- expert FFN
 
 
@@ -442,4 +492,5 @@ ALL_PINS = [pin_decode_int4, pin_decode_e4m3, pin_decode_e2m1, pin_dequant_int4_
             pin_dequant_nvfp4, pin_nvfp4_rounding, pin_nvfp4_activation, pin_select_brute_force,
             pin_select_special_cases, pin_routing_weights, pin_group_tokens,
             pin_expert_ffn_torch, pin_hand_two_expert, pin_identity_activation_exact,
-            pin_hand_nvfp4_layer, pin_widen_bf16]
+            pin_hand_nvfp4_layer, pin_widen_bf16, pin_expert_top_p_hand,
+            pin_expert_top_p_invariants]

@@ -139,6 +139,33 @@ def _widen_bf16_truncating(bits):
     return _orig["widen_bf16"](np.asarray(bits, np.uint16) & np.uint16(0xFFFE))
 
 
+def _top_p_variant(scores, ids, p, le=False, slot_order=False, ties_high=False):
+    s = np.asarray(scores, np.float64)
+    ids = np.asarray(ids, np.int64)
+    keep = np.ones(ids.shape, bool)
+    if not 0.0 < p < 1.0:
+        return O.TopP(keep, np.full(ids.shape[0], np.inf))
+    for t in range(ids.shape[0]):
+        sel = s[t, ids[t]]
+        if slot_order:
+            order = np.arange(ids.shape[1])
+        else:
+            order = np.lexsort((-ids[t] if ties_high else ids[t], -sel))
+        before = np.concatenate([[0.0], np.cumsum(sel[order])[:-1]])
+        keep[t, order] = before <= p * sel.sum() if le else before < p * sel.sum()
+    return O.TopP(keep, np.full(ids.shape[0], np.inf))
+
+
+def _weights_dropped_unmasked(scores, ids, rsf):
+    # forgets that -1 marks a dropped slot (indexes the last expert instead)
+    sel = np.take_along_axis(np.asarray(scores, np.float64), np.asarray(ids), axis=1)
+    return sel / sel.sum(axis=1, keepdims=True) * rsf
+
+
+def _group_dropped_counted(ids, n_experts):
+    return _orig["group_tokens"](np.asarray(ids) % n_experts, n_experts)
+
+
 MUTANTS = {
     "decode_int4/nibbles_swapped": ("decode_int4", _nibbles_swapped),
     "decode_int4/unsigned": ("decode_int4", _unsigned_int4),
@@ -160,6 +187,11 @@ MUTANTS = {
     "nvfp4_layer/h_scale_per_expert": ("quantize_routed_h", _h_scale_per_expert),
     "nvfp4_layer/shared_reads_quantised_x": ("shared_expert_input", _shared_reads_quantised_x),
     "widen_bf16/truncating": ("widen_bf16", _widen_bf16_truncating),
+    "top_p/boundary_inclusive": ("expert_top_p", lambda s, i, p: _top_p_variant(s, i, p, le=True)),
+    "top_p/slot_order": ("expert_top_p", lambda s, i, p: _top_p_variant(s, i, p, slot_order=True)),
+    "top_p/ties_high": ("expert_top_p", lambda s, i, p: _top_p_variant(s, i, p, ties_high=True)),
+    "weights/dropped_unmasked": ("routing_weights", _weights_dropped_unmasked),
+    "group/dropped_counted": ("group_tokens", _group_dropped_counted),
 }
 
 
