@@ -74,7 +74,21 @@ typedef struct {
   int32_t shared_format;       /* shared expert: MOE_W_INT4_G32 | MOE_W_NVFP4 | MOE_W_BF16 */
   int32_t act_dtype;           /* x and out: MOE_DT_F32 | MOE_DT_BF16 */
   int32_t router_dtype;        /* W_r: MOE_DT_F32 | MOE_DT_BF16 */
+  float expert_top_p;          /* adaptive expert top-p; 0 (or >= 1) = off, see below */
 } moe_config;
+
+/*
+ * Adaptive expert top-p (the "--topp" option of "Show HN: Menjalankan GLM 5.2 di komputer
+ * lambat", section "Mengunduh model dan menjalankannya": fewer experts per token, less
+ * expert data read). With 0 < expert_top_p < 1, each token's top_k selected experts are
+ * ordered by their unbiased score s (largest first, equal scores lower id first) and the
+ * shortest prefix whose summed s reaches expert_top_p times the summed s of all top_k is
+ * kept (an expert stays while the mass ranked before it is below that). The kept weights
+ * are renormalised to routed_scaling_factor; a dropped slot reads id -1 and weight 0 in
+ * moe_layer_get_routing and has no entry in the grouping (offsets[E] = the kept count).
+ * Decisions within fp32 rounding of the threshold may differ from an fp64 evaluation.
+ * A NaN value is MOE_ERR_INVALID_ARG.
+ */
 
 /*
  * Layer weights, read once by moe_layer_create (host or device memory, contiguous,

@@ -40,7 +40,8 @@ class Config(ctypes.Structure):
                 ("n_group", ctypes.c_int32), ("topk_group", ctypes.c_int32),
                 ("max_tokens", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
                 ("weight_format", ctypes.c_int32), ("shared_format", ctypes.c_int32),
-                ("act_dtype", ctypes.c_int32), ("router_dtype", ctypes.c_int32)]
+                ("act_dtype", ctypes.c_int32), ("router_dtype", ctypes.c_int32),
+                ("expert_top_p", ctypes.c_float)]
 
 
 class Weights(ctypes.Structure):
@@ -148,10 +149,10 @@ class MoeLayer:
     def __init__(self, arrays: dict, *, hidden: int, inter: int, n_experts: int, top_k: int,
                  n_group: int, topk_group: int, rsf: float, weight_format: str,
                  shared_format: str, act_dtype: str, router_dtype: str, max_tokens: int,
-                 stream=None):
+                 expert_top_p: float = 0.0, stream=None):
         self.cfg = Config(hidden, inter, n_experts, top_k, n_group, topk_group, max_tokens,
                           rsf, _FMT[weight_format], _FMT[shared_format], _DT[act_dtype],
-                          _DT[router_dtype])
+                          _DT[router_dtype], expert_top_p)
         self.hidden, self.top_k, self.n_experts, self.max_tokens = hidden, top_k, n_experts, max_tokens
         self.act_dtype = act_dtype
         a = arrays
@@ -174,7 +175,8 @@ class MoeLayer:
                    top_k=spec.top_k, n_group=spec.n_group, topk_group=spec.topk_group,
                    rsf=spec.rsf, weight_format=spec.weight_format,
                    shared_format=spec.shared_format, act_dtype=spec.act_dtype,
-                   router_dtype=spec.router_dtype, max_tokens=max_tokens, stream=stream)
+                   router_dtype=spec.router_dtype, max_tokens=max_tokens,
+                   expert_top_p=getattr(spec, "expert_top_p", 0.0), stream=stream)
 
     @property
     def handle(self) -> int:

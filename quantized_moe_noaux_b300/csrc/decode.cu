@@ -129,6 +129,7 @@ struct DecodeArgs {
   const float* bias;
   int H, I, E, top_k, n_group, topk_group;
   float rsf;
+  float top_p;                 // adaptive expert top-p (0 < top_p < 1), else every slot kept
   const uint8_t* pack_up;      // [E+1][I/64 tiles][H/256 groups][18432]
   const uint8_t* pack_dn;      // [E+1][H/128 tiles][I/256 groups][18432]
   float* logits;               // [T, E]
@@ -258,9 +259,12 @@ __device__ __forceinline__ void load_act8(const void* x, size_t idx, float (&v)[
 // bias; a group's score adds its two largest b (a thread scans each group); the
 // topk_group best groups are kept (lower index on ties); an expert of a kept group takes
 // slot r when exactly r kept experts rank above it (larger b first, lower index on ties);
-// the normaliser adds the picked unbiased scores in slot order.
+// the normaliser adds the picked unbiased scores in slot order. Adaptive top-p as in
+// select_token (route_dev.cuh), sums in the same order: a slot stays while the s of the
+// slots ranked above it (larger s, lower id on ties) sum below top_p times the total;
+// dropped slots get id -1 and weight 0, the kept weights are renormalised.
 __device__ void select_block(DecFixed& C, const float* logits_row, const float* bias, int E, int n_group,
-                             int topk_group, int top_k, float rsf, int* idsel, float* wsel) {
+                             int topk_group, int top_k, float rsf, float top_p, int* idsel, float* wsel) {
   const int tid = threadIdx.x;
   for (int e = tid; e < E; e += 128) {
     const float sc = sigmoidf_acc(__ldcg(logits_row + e));
@@ -310,9 +314,30 @@ __device__ void select_block(DecFixed& C, const float* logits_row, const float* 
   if (tid == 0) {
     float wsum = 0.f;
     for (int j = 0; j < top_k; ++j) wsum += C.sels[C.pick[j]];
+    float norm = wsum;
+    unsigned keep = (1u << top_k) - 1u;
+    if (top_p > 0.f && top_p < 1.f) {
+      keep = 0u;
+      for (int j = 0; j < top_k; ++j) {
+        const float sj = C.sels[C.pick[j]];
+        int rank = 0;
+        float before = 0.f;
+        for (int i = 0; i < top_k; ++i) {
+          const float si = C.sels[C.pick[i]];
+          const bool above = si > sj || (si == sj && C.pick[i] < C.pick[j]);
+          rank += above;
+          if (above) before += si;
+        }
+        if (rank == 0 || before < top_p * wsum) keep |= 1u << j;
+      }
+      norm = 0.f;
+      for (int i = 0; i < top_k; ++i)
+        if ((keep >> i) & 1u) norm += C.sels[C.pick[i]];
+    }
     for (int j = 0; j < top_k; ++j) {
-      idsel[j] = C.pick[j];
-      wsel[j] = C.sels[C.pick[j]] / wsum * rsf;
+      const bool kj = (keep >> j) & 1u;
+      idsel[j] = kj ? C.pick[j] : -1;
+      wsel[j] = kj ? C.sels[C.pick[j]] / norm * rsf : 0.f;
     }
   }
   ptx::bar_sync(2, 128);
@@ -334,7 +359,10 @@ __device__ void group_in_cta(DecFixed& C, const DecodeArgs& a) {
   const int n = T * k;
   for (int e = lane; e < E; e += 32) C.cnt[e] = 0;
   __syncwarp();
-  for (int f = lane; f < n; f += 32) atomicAdd(&C.cnt[C.idsel[f / k][f % k]], 1);
+  for (int f = lane; f < n; f += 32) {
+    const int e = C.idsel[f / k][f % k];
+    if (e >= 0) atomicAdd(&C.cnt[e], 1);   // -1: dropped by the adaptive top-p
+  }
   __syncwarp();
   const int epl = E / 32;   // lane owns experts lane*epl .. +epl-1 (epl <= kMaxE / 32)
   int cl[kMaxE / 32];
@@ -377,11 +405,13 @@ __device__ void group_in_cta(DecFixed& C, const DecodeArgs& a) {
   for (int f = lane; f < n; f += 32) {
     const int tok = f / k, slot = f % k;
     const int e = C.idsel[tok][slot];
-    C.meta_j[C.aslot[e]][tok] = slot;
+    if (e >= 0) C.meta_j[C.aslot[e]][tok] = slot;
     if (cta0) {
-      int rank = 0;
-      for (int f2 = 0; f2 < f; ++f2) rank += (flat[(f2 / k) * kMaxK + f2 % k] == e);
-      a.entries[C.soff[e] + rank] = f;
+      if (e >= 0) {
+        int rank = 0;
+        for (int f2 = 0; f2 < f; ++f2) rank += (flat[(f2 / k) * kMaxK + f2 % k] == e);
+        a.entries[C.soff[e] + rank] = f;
+      }
       a.ids[f] = e;
       a.weights[f] = C.wsel[tok][slot];
     }
@@ -1061,8 +1091,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
       ptx::bar_sync(2, kEpiWarps * 32);
       if (!C.ep_stop) {
         for (int t = 0; t < T; ++t)
-          select_block(C, a.logits + (size_t)t * E, a.bias, E, a.n_group, a.topk_group, k, a.rsf, C.idsel[t],
-                       C.wsel[t]);
+          select_block(C, a.logits + (size_t)t * E, a.bias, E, a.n_group, a.topk_group, k, a.rsf, a.top_p,
+                       C.idsel[t], C.wsel[t]);
         if (tid == 0) DEC_TRACE(7);
         if (warp == 0) group_in_cta(C, a);
       } else if (tid == 0) {
@@ -1199,6 +1229,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
               // slots in order, the shared expert last
               float acc = 0.f, ysh = 0.f;
               for (int j = 0; j <= k; ++j) {
+                if (j < k && C.idsel[c][j] < 0) continue;   // slot dropped by the adaptive top-p
                 float yv[kMaxKsd];
 #pragma unroll
                 for (int sp = 0; sp < kMaxKsd; ++sp)
@@ -1386,6 +1417,7 @@ cudaError_t launch_decode_fused(const DecodeLaunch& d, int act_dtype, int router
   a.n_group = d.n_group;
   a.topk_group = d.topk_group;
   a.rsf = d.rsf;
+  a.top_p = d.top_p;
   a.pack_up = d.pack_up;
   a.pack_dn = d.pack_dn;
   a.logits = d.logits;

@@ -515,8 +515,9 @@ template <int XDT, bool FP4>
 __global__ void __launch_bounds__(256)
 gather_act_kernel(const void* __restrict__ x, int H, const int32_t* __restrict__ entries, int Tk, int top_k,
                   int first_row, __half* __restrict__ dst, const __half* __restrict__ xq16,
-                  int32_t* __restrict__ inv) {
+                  int32_t* __restrict__ inv, const int32_t* __restrict__ n_routed) {
   const int q = first_row + (int)blockIdx.x;
+  if (q < Tk && q >= __ldg(n_routed)) return;   // past the routed rows (adaptive top-p)
   const int ent = q < Tk ? __ldg(entries + q) : 0;
   const int tok = q < Tk ? ent / top_k : q - Tk;
   if (q < Tk && threadIdx.x == 0) inv[ent] = q;   // sorted row of each (token, slot)
@@ -683,7 +684,7 @@ cudaError_t launch_bf16_to_f16(const void* src, void* dst, size_t rows, int K, b
 
 cudaError_t launch_gather_act(const void* x, int act_dtype, bool nvfp4, int H, const int32_t* entries, int Tk,
                               int top_k, int rows, __half* dst, const unsigned int* amax_bits, __half* xq16,
-                              int32_t* inv, cudaStream_t s) {
+                              int32_t* inv, const int32_t* n_routed, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const bool xf = act_dtype == MOE_DT_F32;
   if (nvfp4) {
@@ -695,11 +696,17 @@ cudaError_t launch_gather_act(const void* x, int act_dtype, bool nvfp4, int H, c
       if (xf) quant_tokens_fp4_kernel<MOE_DT_F32><<<(int)g, 256, 0, s>>>(x, nb, amax_bits, xq16);
       else quant_tokens_fp4_kernel<MOE_DT_BF16><<<(int)g, 256, 0, s>>>(x, nb, amax_bits, xq16);
     }
-    if (xf) gather_act_kernel<MOE_DT_F32, true><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, 0, dst, xq16, inv);
-    else gather_act_kernel<MOE_DT_BF16, true><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, 0, dst, xq16, inv);
+    if (xf)
+      gather_act_kernel<MOE_DT_F32, true><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, 0, dst, xq16, inv, n_routed);
+    else
+      gather_act_kernel<MOE_DT_BF16, true><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, 0, dst, xq16, inv, n_routed);
   } else {
-    if (xf) gather_act_kernel<MOE_DT_F32, false><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, 0, dst, nullptr, inv);
-    else gather_act_kernel<MOE_DT_BF16, false><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, 0, dst, nullptr, inv);
+    if (xf)
+      gather_act_kernel<MOE_DT_F32, false><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, 0, dst, nullptr, inv,
+                                                                n_routed);
+    else
+      gather_act_kernel<MOE_DT_BF16, false><<<rows, 256, 0, s>>>(x, H, entries, Tk, top_k, 0, dst, nullptr, inv,
+                                                                 n_routed);
   }
   return cudaGetLastError();
 }
@@ -708,27 +715,29 @@ cudaError_t launch_gather_shared_rows(const void* x, int act_dtype, int H, int T
                                       cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   if (act_dtype == MOE_DT_F32)
-    gather_act_kernel<MOE_DT_F32, false><<<T, 256, 0, s>>>(x, H, nullptr, Tk, 1, Tk, dst, nullptr, nullptr);
+    gather_act_kernel<MOE_DT_F32, false><<<T, 256, 0, s>>>(x, H, nullptr, Tk, 1, Tk, dst, nullptr, nullptr, nullptr);
   else
-    gather_act_kernel<MOE_DT_BF16, false><<<T, 256, 0, s>>>(x, H, nullptr, Tk, 1, Tk, dst, nullptr, nullptr);
+    gather_act_kernel<MOE_DT_BF16, false><<<T, 256, 0, s>>>(x, H, nullptr, Tk, 1, Tk, dst, nullptr, nullptr, nullptr);
   return cudaGetLastError();
 }
 
 namespace {
 
 // Weighted combine of the grouped path ("routed_scaling_factor"-scaled routing weights times
-// each selected expert's output, plus the shared expert): out[t] = sum over slots j in
+// each selected expert's output, plus the shared expert): out[t] = sum over routed slots j in
 // ascending order of w[t, j] * y[inv[t k + j]], then + y[T k + t], in fp32, converted once to
-// the activation dtype. A fixed order, so repeated calls give identical outputs.
+// the activation dtype. A fixed order, so repeated calls give identical outputs. Slots the
+// adaptive top-p dropped (id -1) are skipped.
 template <int DT>
 __global__ void __launch_bounds__(256)
-combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv, const float* __restrict__ w, int T,
-               int top_k, int H, void* __restrict__ out) {
+combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv, const int32_t* __restrict__ ids,
+               const float* __restrict__ w, int T, int top_k, int H, void* __restrict__ out) {
   const int t = blockIdx.x;
   const int Tk = T * top_k;
   for (int h = threadIdx.x * 4; h < H; h += 256 * 4) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < top_k; ++j) {
+      if (__ldg(ids + (size_t)t * top_k + j) < 0) continue;
       const float wj = __ldg(w + (size_t)t * top_k + j);
       const float4 v = __ldg(reinterpret_cast<const float4*>(y + (size_t)__ldg(inv + (size_t)t * top_k + j) * H + h));
       acc.x += wj * v.x;
@@ -755,11 +764,13 @@ combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv, con
 
 }  // namespace
 
-cudaError_t launch_combine(const float* y, const int32_t* inv, const float* weights, int T, int top_k, int H,
-                           void* out, int act_dtype, cudaStream_t s) {
+cudaError_t launch_combine(const float* y, const int32_t* inv, const int32_t* ids, const float* weights, int T,
+                           int top_k, int H, void* out, int act_dtype, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  if (act_dtype == MOE_DT_F32) combine_kernel<MOE_DT_F32><<<T, 256, 0, s>>>(y, inv, weights, T, top_k, H, out);
-  else combine_kernel<MOE_DT_BF16><<<T, 256, 0, s>>>(y, inv, weights, T, top_k, H, out);
+  if (act_dtype == MOE_DT_F32)
+    combine_kernel<MOE_DT_F32><<<T, 256, 0, s>>>(y, inv, ids, weights, T, top_k, H, out);
+  else
+    combine_kernel<MOE_DT_BF16><<<T, 256, 0, s>>>(y, inv, ids, weights, T, top_k, H, out);
   return cudaGetLastError();
 }
 

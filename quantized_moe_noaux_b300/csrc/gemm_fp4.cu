@@ -413,8 +413,9 @@ quant_tokens_fp4_kernel(const void* __restrict__ x, size_t nblocks, const unsign
 __global__ void __launch_bounds__(256)
 gather_fp4_rows_kernel(const uint8_t* __restrict__ tok_codes, const uint8_t* __restrict__ tok_sf, int H,
                        const int32_t* __restrict__ entries, int top_k, uint8_t* __restrict__ codes,
-                       uint8_t* __restrict__ sf, int32_t* __restrict__ inv) {
+                       uint8_t* __restrict__ sf, int32_t* __restrict__ inv, const int32_t* __restrict__ n_routed) {
   const int q = blockIdx.x;
+  if (q >= __ldg(n_routed)) return;   // past the routed rows (adaptive top-p)
   const int ent = __ldg(entries + q);
   const int tok = ent / top_k;
   if (threadIdx.x == 0) inv[ent] = q;   // sorted row of each (token, slot)
@@ -487,14 +488,15 @@ cudaError_t launch_fp4_pack(const uint8_t* codes, const uint8_t* scales, int K, 
 
 cudaError_t launch_quant_gather_fp4(const void* x, int act_dtype, int H, int T, const int32_t* entries, int top_k,
                                     const unsigned int* amax_bits, uint8_t* tok_codes, uint8_t* tok_sf,
-                                    uint8_t* codes, uint8_t* sf, int32_t* inv, cudaStream_t s) {
+                                    uint8_t* codes, uint8_t* sf, int32_t* inv, const int32_t* n_routed,
+                                    cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const size_t nb = (size_t)T * H / 16;
   if (act_dtype == MOE_DT_F32)
     quant_tokens_fp4_kernel<MOE_DT_F32><<<(int)grid_for(nb), 256, 0, s>>>(x, nb, amax_bits, tok_codes, tok_sf);
   else
     quant_tokens_fp4_kernel<MOE_DT_BF16><<<(int)grid_for(nb), 256, 0, s>>>(x, nb, amax_bits, tok_codes, tok_sf);
-  gather_fp4_rows_kernel<<<T * top_k, 256, 0, s>>>(tok_codes, tok_sf, H, entries, top_k, codes, sf, inv);
+  gather_fp4_rows_kernel<<<T * top_k, 256, 0, s>>>(tok_codes, tok_sf, H, entries, top_k, codes, sf, inv, n_routed);
   return cudaGetLastError();
 }
 

@@ -35,7 +35,7 @@ group_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ counts
     for (int w = 0; w < kGroupThreads / 32; ++w) b += warp_sum[w];
     base_s = b;
     offsets[e] = b;
-    if (e == E - 1) offsets[E] = T * top_k;
+    if (e == E - 1) offsets[E] = b + counts[e];   // routed entries (slots with id -1 have none)
   }
   __syncthreads();
   // Each warp owns a contiguous span of the n entries: it counts the span's hits with

@@ -22,13 +22,15 @@ cudaError_t launch_router_logits(const void* x, int act_dtype, const void* route
                                  int router_dtype, float* logits, int T, int E, int H,
                                  cudaStream_t s);
 
-// Selection: sigmoid, bias, group top-2 sums, top-k-group, top-k, renormalise x rsf.
-// Also histograms the chosen experts into counts[E] (zeroed by the caller).
+// Selection: sigmoid, bias, group top-2 sums, top-k-group, top-k, adaptive top-p (0 < top_p
+// < 1; dropped slots id -1), renormalise x rsf. Also histograms the routed experts into
+// counts[E] (zeroed by the caller).
 cudaError_t launch_select(const float* logits, const float* bias, int T, int E, int n_group,
-                          int topk_group, int top_k, float rsf, int32_t* ids, float* weights,
+                          int topk_group, int top_k, float rsf, float top_p, int32_t* ids, float* weights,
                           int32_t* counts, int* status, cudaStream_t s);
 
-// Grouping: offsets[E+1], entries[T*k] (ascending token per expert) and the work list
+// Grouping: offsets[E+1] (offsets[E] = routed entries), entries (ascending token per
+// expert; slots with id -1 have none) and the work list
 // (expert, token-chunk) of every active expert, plus the inline shared expert when
 // shared_inline != 0. meta[0] = number of work items.
 cudaError_t launch_group(const int32_t* ids, const int32_t* counts, int T, int top_k, int E,
@@ -86,6 +88,7 @@ struct DecodeLaunch {
   const float* bias;
   int H, I, E, top_k, n_group, topk_group;
   float rsf;
+  float top_p;                 // adaptive expert top-p (0 < top_p < 1), else off
   const uint8_t* pack_up;      // grouped-GEMM packed gate/up store
   const uint8_t* pack_dn;      // grouped-GEMM packed down store
   float* logits;
@@ -160,12 +163,12 @@ cudaError_t launch_bf16_to_f16(const void* src, void* dst, size_t rows, int K, b
 // block scale, fp16; the tensor scale from amax_bits) and copy that row for routed rows.
 cudaError_t launch_gather_act(const void* x, int act_dtype, bool nvfp4, int H, const int32_t* entries, int Tk,
                               int top_k, int rows, __half* dst, const unsigned int* amax_bits, __half* xq16,
-                              int32_t* inv, cudaStream_t s);
-// out[t] = sum_j w[t, j] y[inv[t k + j]] + y[T k + t] (slots in ascending order, fp32), in the
-// activation dtype: the combine of the grouped path. inv[t k + j] = sorted row of entry t k + j
-// (written by the gather kernels).
-cudaError_t launch_combine(const float* y, const int32_t* inv, const float* weights, int T, int top_k, int H,
-                           void* out, int act_dtype, cudaStream_t s);
+                              int32_t* inv, const int32_t* n_routed, cudaStream_t s);
+// out[t] = sum_j w[t, j] y[inv[t k + j]] + y[T k + t] (routed slots in ascending order, fp32),
+// in the activation dtype: the combine of the grouped path. inv[t k + j] = sorted row of
+// entry t k + j (written by the gather kernels); slots with ids < 0 are skipped.
+cudaError_t launch_combine(const float* y, const int32_t* inv, const int32_t* ids, const float* weights, int T,
+                           int top_k, int H, void* out, int act_dtype, cudaStream_t s);
 cudaError_t launch_quant_h(const float* h, size_t n, const unsigned int* amax_bits, __half* dst, cudaStream_t s);
 // fp16 x rows Tk .. Tk + T - 1 of the sorted activation matrix (the shared expert's rows).
 cudaError_t launch_gather_shared_rows(const void* x, int act_dtype, int H, int Tk, int T, __half* dst,
@@ -195,7 +198,8 @@ cudaError_t launch_fp4_pack(const uint8_t* codes, const uint8_t* scales, int K, 
 // quantised once into tok_codes [T, H/2] / tok_sf [T, H/16], then copied to its rows.
 cudaError_t launch_quant_gather_fp4(const void* x, int act_dtype, int H, int T, const int32_t* entries, int top_k,
                                     const unsigned int* amax_bits, uint8_t* tok_codes, uint8_t* tok_sf,
-                                    uint8_t* codes, uint8_t* sf, int32_t* inv, cudaStream_t s);
+                                    uint8_t* codes, uint8_t* sf, int32_t* inv, const int32_t* n_routed,
+                                    cudaStream_t s);
 cudaError_t launch_quant_h_fp4(const float* h, size_t n, const unsigned int* amax_bits, uint8_t* codes, uint8_t* sf,
                                cudaStream_t s);
 cudaError_t launch_gemm_fp4(int epi, const Fp4Maps& m, const GemmParams& p, int max_tiles, int n_sm, cudaStream_t s);

@@ -120,6 +120,7 @@ moe_status validate_config(const moe_config* c) {
       c->topk_group <= 0 || c->max_tokens <= 0)
     return MOE_ERR_INVALID_ARG;
   if (!(c->routed_scaling_factor > 0.f)) return MOE_ERR_INVALID_ARG;
+  if (c->expert_top_p != c->expert_top_p) return MOE_ERR_INVALID_ARG;   // NaN
   if (c->weight_format != MOE_W_INT4_G32 && c->weight_format != MOE_W_NVFP4) return MOE_ERR_UNSUPPORTED;
   if (c->shared_format != MOE_W_INT4_G32 && c->shared_format != MOE_W_NVFP4 &&
       c->shared_format != MOE_W_BF16)
@@ -419,11 +420,11 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
   if (f4) {
     // routed rows as NVFP4 codes + scales; the bf16 shared expert reads fp16 x
     MOE_LAUNCH(launch_quant_gather_fp4(x, c.act_dtype, H, T, L->entries, k, L->amax, L->xtc, L->xts, L->xc, L->xsf,
-                                       L->inv, s));
+                                       L->inv, L->offsets + E, s));
     MOE_LAUNCH(launch_gather_shared_rows(x, c.act_dtype, H, Tk, T, L->x16s, s));
   } else {
     MOE_LAUNCH(launch_gather_act(x, c.act_dtype, nvfp4, H, L->entries, Tk, k, Tk + T, L->x16s, L->amax,
-                                 reinterpret_cast<__half*>(L->xq), L->inv, s));   // xq: [Tm, H] NVFP4 scratch
+                                 reinterpret_cast<__half*>(L->xq), L->inv, L->offsets + E, s));   // xq: NVFP4 scratch
   }
   MOE_CK(m.mark(2));
   GemmParams p{};
@@ -487,7 +488,7 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
   }
   if (!inl) MOE_LAUNCH(launch_gemm(kWF16, 1, L->maps_sh_down, ps, shared_max * ps.mtiles, L->n_sm, s));
   MOE_CK(m.mark(6));
-  MOE_LAUNCH(launch_combine(L->ys, L->inv, L->weights, T, k, H, out, c.act_dtype, s));
+  MOE_LAUNCH(launch_combine(L->ys, L->inv, L->ids, L->weights, T, k, H, out, c.act_dtype, s));
   MOE_CK(m.mark(7));
   return MOE_OK;
 }
@@ -510,7 +511,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
     MOE_CK(m.mark(1));
     MOE_CK(m.mark(2));
     DecodeLaunch d{x, T, L->router_w, L->bias, H, I, E, k, c.n_group, c.topk_group,
-                   c.routed_scaling_factor, L->gpack_up, L->gpack_down, L->logits, L->ids,
+                   c.routed_scaling_factor, c.expert_top_p, L->gpack_up, L->gpack_down, L->logits, L->ids,
                    L->weights, L->offsets, L->entries, L->dec_h16, L->dec_gu_part, L->dec_y_part,
                    out, L->dsync, L->status, L->wait_ns, L->trace};
     MOE_LAUNCH(launch_decode_fused(d, c.act_dtype, c.router_dtype, L->n_sm, s));
@@ -527,6 +528,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
   else
     MOE_LAUNCH(launch_router_logits(x, c.act_dtype, L->router_w, c.router_dtype, L->logits, T, E, H, s));
   MOE_LAUNCH(launch_select(L->logits, L->bias, T, E, c.n_group, c.topk_group, k, c.routed_scaling_factor,
+                           c.expert_top_p,
                            L->ids, L->weights, L->counts, L->status, s));
   MOE_LAUNCH(launch_group(L->ids, L->counts, T, k, E, L->shared_inline, L->offsets, L->entries,
                           gemm ? nullptr : L->items, L->meta, s));

@@ -5,6 +5,9 @@
 //   keep the topk_group best groups (ties -> lower group index)
 //   top_k largest b among kept experts (ties -> lower expert index), slot order descending
 //   w[j] = s[id_j] / sum_j s[id_j] * rsf
+//   adaptive top-p (0 < top_p < 1): order the top_k by s (larger first, lower id on ties);
+//   a slot stays while the s ranked before it sums below top_p * sum s (the first always);
+//   dropped slots get id -1, weight 0, and the kept weights are renormalised to rsf
 // (DeepSeek-V3-style sigmoid router with noaux_tc and routed_scaling_factor, "Show HN:
 // Menjalankan GLM 5.2 di komputer lambat", section "Fitur utama yang diimplementasikan".)
 #pragma once
@@ -33,8 +36,8 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 // Logits are read through L2 (they may have been written by other CTAs of this grid).
 __device__ __forceinline__ int select_token(const float* logits_row, const float* bias, int E,
                                             int n_group, int topk_group, int top_k, float rsf,
-                                            float* b, float* s, int32_t* ids, float* weights,
-                                            int* status) {
+                                            float top_p, float* b, float* s, int32_t* ids,
+                                            float* weights, int* status) {
   const int lane = threadIdx.x & 31;
   for (int e = lane; e < E; e += 32) {
     const float sc = sigmoidf_acc(__ldcg(logits_row + e));
@@ -93,9 +96,33 @@ __device__ __forceinline__ int select_token(const float* logits_row, const float
     if (lane == 0) b[vi] = -INFINITY;
     __syncwarp();
   }
+  float norm = wsum;
+  if (top_p > 0.f && top_p < 1.f) {
+    // rank by s and the mass ranked before this slot, both added in slot order
+    int rank = 0;
+    float before = 0.f;
+    for (int i = 0; i < top_k; ++i) {
+      const float si = __shfl_sync(0xffffffffu, my_s, i);
+      const int ii = __shfl_sync(0xffffffffu, my_id, i);
+      const bool above = si > my_s || (si == my_s && ii < my_id);
+      rank += above;
+      if (above) before += si;
+    }
+    const bool keep = rank == 0 || before < top_p * wsum;
+    norm = 0.f;
+    for (int i = 0; i < top_k; ++i) {
+      const int ki = __shfl_sync(0xffffffffu, (int)keep, i);
+      const float si = __shfl_sync(0xffffffffu, my_s, i);
+      if (ki) norm += si;
+    }
+    if (lane < top_k && !keep) {
+      my_id = -1;
+      my_s = 0.f;
+    }
+  }
   if (lane < top_k) {
     ids[lane] = my_id;
-    weights[lane] = my_s / wsum * rsf;
+    weights[lane] = my_s / norm * rsf;
   }
   return my_id;
 }

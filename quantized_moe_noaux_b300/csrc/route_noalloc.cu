@@ -99,7 +99,7 @@ extern "C" moe_status moe_route_noalloc(const void* x, int32_t act_dtype, int32_
       cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (moe::launch_router_logits(x, act_dtype, router_w, router_dtype, logits, T, E, H, s) != cudaSuccess ||
-      moe::launch_select(logits, bias, T, E, n_group, topk_group, top_k, routed_scaling_factor, ids,
+      moe::launch_select(logits, bias, T, E, n_group, topk_group, top_k, routed_scaling_factor, 0.f, ids,
                          weights, counts, status, s) != cudaSuccess ||
       moe::launch_group(ids, counts, T, top_k, E, 0, offsets, entries, items, meta, s) != cudaSuccess)
     return MOE_ERR_CUDA;

@@ -278,17 +278,17 @@ constexpr int kMaxE = 1024;
 // One warp per token.
 __global__ void __launch_bounds__(kSelWarps * 32)
 select_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
-              int n_group, int topk_group, int top_k, float rsf, int32_t* __restrict__ ids,
+              int n_group, int topk_group, int top_k, float rsf, float top_p, int32_t* __restrict__ ids,
               float* __restrict__ weights, int32_t* __restrict__ counts, int* status) {
   __shared__ float sb[kSelWarps][kMaxE];   // biased scores; -inf once taken or excluded
   __shared__ float ss[kSelWarps][kMaxE];   // unbiased sigmoid scores
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kSelWarps + warp;
   if (t >= T) return;
-  const int id = select_token(logits + (size_t)t * E, bias, E, n_group, topk_group, top_k, rsf,
+  const int id = select_token(logits + (size_t)t * E, bias, E, n_group, topk_group, top_k, rsf, top_p,
                               sb[warp], ss[warp], ids + (size_t)t * top_k,
                               weights + (size_t)t * top_k, status);
-  if (lane < top_k) atomicAdd(&counts[id], 1);
+  if (lane < top_k && id >= 0) atomicAdd(&counts[id], 1);
 }
 
 }  // namespace
@@ -321,11 +321,11 @@ cudaError_t launch_router_logits(const void* x, int act_dtype, const void* route
 }
 
 cudaError_t launch_select(const float* logits, const float* bias, int T, int E, int n_group,
-                          int topk_group, int top_k, float rsf, int32_t* ids, float* weights,
+                          int topk_group, int top_k, float rsf, float top_p, int32_t* ids, float* weights,
                           int32_t* counts, int* status, cudaStream_t s) {
   if (E > kMaxE || n_group > 32 || top_k > 32) return cudaErrorInvalidValue;
   select_kernel<<<(T + kSelWarps - 1) / kSelWarps, kSelWarps * 32, 0, s>>>(
-      logits, bias, T, E, n_group, topk_group, top_k, rsf, ids, weights, counts, status);
+      logits, bias, T, E, n_group, topk_group, top_k, rsf, top_p, ids, weights, counts, status);
   return cudaGetLastError();
 }
 

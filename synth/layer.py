@@ -67,6 +67,7 @@ class LayerSpec:
     bias_std: float
     seed: int = 0
     weight_std: float = 0.02
+    expert_top_p: float = 0.0  # adaptive expert top-p (0 = off)
 
     @property
     def experts_per_group(self) -> int:
@@ -113,11 +114,17 @@ LAYERS = {
     # NVFP4 routed experts; router and shared expert stay bf16
     "glm52_nvfp4": replace(_GLM, name="glm52_h6144_e256_nvfp4", weight_format="nvfp4",
                            router_dtype="bf16", shared_format="bf16"),
+    # adaptive expert top-p 0.7 (the pages' --topp 0.7) on the same weights
+    "small_topp": replace(_SMALL, expert_top_p=0.7),
+    "small_nvfp4_topp": replace(_SMALL, name="small_h2048_e32_nvfp4", weight_format="nvfp4",
+                                router_dtype="bf16", shared_format="bf16", expert_top_p=0.7),
+    "glm52_topp": replace(_GLM, expert_top_p=0.7),
 }
 
 WORKLOADS = {
     "tiny_t4": Workload("tiny_t4", LAYERS["tiny"], tokens=4),
     "glm52_decode_t1": Workload("glm52_decode_t1", LAYERS["glm52"], tokens=1, steps=1000),
+    "glm52_decode_t1_topp07": Workload("glm52_decode_t1_topp07", LAYERS["glm52_topp"], tokens=1, steps=1000),
     "glm52_decode_t4": Workload("glm52_decode_t4", LAYERS["glm52_unbiased"], tokens=4),
     "glm52_decode_t32": Workload("glm52_decode_t32", LAYERS["glm52_unbiased"], tokens=32),
     "glm52_prefill_t2048": Workload("glm52_prefill_t2048", LAYERS["glm52_skewed"], tokens=2048),
