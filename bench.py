@@ -527,6 +527,13 @@ def run_ours(args):
                     "h2d_bytes_per_step": T * H * (2 if spec.act_dtype == "bf16" else 4),
                     "d2h_bytes_per_step": T * H * (2 if spec.act_dtype == "bf16" else 4),
                     "steps": KE}}
+    if wl.name.startswith("glm52_mtp_verify"):
+        # MTP draft-verify: expert loads of one verify forward, per position and per token
+        # generated at the pages' 2.2-2.8 tokens per forward (a decode step loads top_k + 1)
+        loads = float(np.mean(uniq)) + 1.0
+        line["mtp"] = {"draft": T - 1, "expert_loads_per_forward": loads, "per_position": loads / T,
+                       "per_generated_token": {"2.2": loads / 2.2, "2.8": loads / 2.8},
+                       "decode_loads_per_token": spec.top_k + 1}
     if world == 1 and not args.no_cpu_baseline:
         cores, model = host_cpu()
         v, steps, threads, dt_cpu, n = oracle_tokens_per_s(spec, arrays, T, args.cpu_budget / 2)

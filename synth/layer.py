@@ -125,6 +125,11 @@ WORKLOADS = {
     "tiny_t4": Workload("tiny_t4", LAYERS["tiny"], tokens=4),
     "glm52_decode_t1": Workload("glm52_decode_t1", LAYERS["glm52"], tokens=1, steps=1000),
     "glm52_decode_t1_topp07": Workload("glm52_decode_t1_topp07", LAYERS["glm52_topp"], tokens=1, steps=1000),
+    # MTP draft-verify: one forward over the accepted position and DRAFT draft positions of a
+    # sequence (DRAFT = 2 and 4), batch-union over their experts; positions drawn
+    # independently (the pages give no statistics of how their routing overlaps)
+    "glm52_mtp_verify_t3": Workload("glm52_mtp_verify_t3", LAYERS["glm52"], tokens=3, steps=1000),
+    "glm52_mtp_verify_t5": Workload("glm52_mtp_verify_t5", LAYERS["glm52"], tokens=5, steps=1000),
     "glm52_decode_t4": Workload("glm52_decode_t4", LAYERS["glm52_unbiased"], tokens=4),
     "glm52_decode_t32": Workload("glm52_decode_t32", LAYERS["glm52_unbiased"], tokens=32),
     "glm52_prefill_t2048": Workload("glm52_prefill_t2048", LAYERS["glm52_skewed"], tokens=2048),

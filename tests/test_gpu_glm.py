@@ -78,6 +78,20 @@ def test_decode_t32(glm_base):
     check("glm52_unbiased", glm_base, 32, 0)
 
 
+@pytest.mark.parametrize("T", [3, 5])
+def test_mtp_verify_batch(glm_base, T):
+    """MTP draft-verify forward (the accepted position and T - 1 draft positions in one
+    batch-union call) through the fused decode kernel: every position's routing and output;
+    the experts read once for all positions are the union of the positions' selections."""
+    import quantized_moe_noaux_b300 as moe
+    check("glm52", glm_base, T, 40 + T, path=moe.PATH_GEMV)
+    spec, _, layer, _ = get_layer("glm52", glm_base)
+    layer.set_path(moe.PATH_AUTO)
+    got = layer.routing(T)
+    union = set(got["ids"].ravel().tolist())
+    assert int(np.count_nonzero(np.diff(got["offsets"]))) == len(union)
+
+
 def prefill_sample(routing, top_k, T, n=320, seed=0):
     """Tokens whose outputs are compared at T=2048: the first and last token of every
     256-row chunk of the most loaded expert's entry list (the grouped GEMM's tile
