@@ -134,6 +134,44 @@ def dequant_nvfp4(codes: np.ndarray, scales: np.ndarray, tensor_scale) -> np.nda
     return c
 
 
+def decode_int_row(codes: np.ndarray, bits: int) -> np.ndarray:
+    """Packed two's-complement integers of the per-row formats -> int64 [N, K]: int8 one
+    per byte; int4 two per byte (element 2j in the low nibble of byte j); int2 four per byte
+    (element 4j + i in bits 2i..2i+1 of byte j)."""
+    c = np.asarray(codes, np.uint8).astype(np.int64)
+    per = 8 // bits
+    fields = np.stack([(c >> (bits * i)) & ((1 << bits) - 1) for i in range(per)], axis=-1)
+    v = fields.reshape(c.shape[:-1] + (c.shape[-1] * per,))
+    return np.where(v >= 1 << (bits - 1), v - (1 << bits), v)
+
+
+def dequant_int_row(codes: np.ndarray, scales: np.ndarray, bits: int) -> np.ndarray:
+    """Per-row symmetric integer weights (the "int8, packed int4, packed int2, scale per-row"
+    formats of "Show HN: Menjalankan GLM 5.2 di komputer lambat", section "Fitur utama yang
+    diimplementasikan"): w[n, k] = code[n, k] * scale[n], one fp32 scale per row."""
+    return decode_int_row(codes, bits) * np.asarray(scales, np.float64).reshape(-1, 1)
+
+
+def quantize_q8_0_activation(a: np.ndarray) -> np.ndarray:
+    """Q8_0-style int8 activations (the integer-dot kernels' activations of "Show HN:
+    Menjalankan GLM 5.2 di komputer lambat", section "Fitur utama yang diimplementasikan").
+    The pages name the style only; reading: per 32 consecutive elements of a row, d =
+    fp16_rne(amax / 127) and q = clamp(rint_even(a / d), -127, 127) (d = 0 gives q = 0),
+    both quotients fp32 operations on the fp32 value of a; returns q * d (fp64)."""
+    a32 = np.asarray(a, np.float32)
+    m, k = a32.shape
+    blocks = a32.reshape(m, k // 32, 32)
+    amax = np.max(np.abs(blocks), axis=2)
+    d = (amax / np.float32(127.0)).astype(np.float32).astype(np.float16).astype(np.float32)
+    q = np.zeros(blocks.shape, np.float32)
+    np.divide(blocks, d[..., None], out=q, where=d[..., None] != 0)
+    q = np.clip(np.rint(q), -127, 127)
+    return (q.astype(np.float64) * d[..., None].astype(np.float64)).reshape(m, k)
+
+
+ROW_FORMAT_BITS = {"int8_row": 8, "int4_row": 4, "int2_row": 2}
+
+
 def widen_bf16(bits: np.ndarray) -> np.ndarray:
     """bf16 bit patterns -> fp64 (exact)."""
     u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
@@ -412,12 +450,16 @@ class Layer:
     """Weights of one layer as the oracle sees them (dequantised lazily, per expert)."""
 
     def __init__(self, arrays: dict, *, hidden, inter, n_experts, top_k, n_group, topk_group,
-                 rsf, weight_format, act_dtype, router_dtype, shared_format, expert_top_p=0.0):
+                 rsf, weight_format, act_dtype, router_dtype, shared_format, expert_top_p=0.0,
+                 act_quant="none"):
         self.a = arrays
         self.H, self.I, self.E = hidden, inter, n_experts
         self.top_k, self.n_group, self.topk_group = top_k, n_group, topk_group
         self.rsf = rsf
         self.expert_top_p = expert_top_p
+        if act_quant not in ("none", "q8_0") or (act_quant == "q8_0" and shared_format != weight_format):
+            raise ValueError(act_quant)
+        self.act_quant = act_quant
         self.weight_format, self.act_dtype = weight_format, act_dtype
         self.router_dtype, self.shared_format = router_dtype, shared_format
 
@@ -427,7 +469,8 @@ class Layer:
                    top_k=spec.top_k, n_group=spec.n_group, topk_group=spec.topk_group,
                    rsf=spec.rsf, weight_format=spec.weight_format, act_dtype=spec.act_dtype,
                    router_dtype=spec.router_dtype, shared_format=spec.shared_format,
-                   expert_top_p=getattr(spec, "expert_top_p", 0.0))
+                   expert_top_p=getattr(spec, "expert_top_p", 0.0),
+                   act_quant=getattr(spec, "act_quant", "none"))
 
     # -- weights
     def router_w(self) -> np.ndarray:
@@ -443,6 +486,8 @@ class Layer:
             return dequant_nvfp4(a[p + "_codes"][idx], a[p + "_scales"][idx], a[p + "_tscale"][idx])
         if fmt == "bf16":
             return widen_bf16(a[p + "_bf16"][idx])
+        if fmt in ROW_FORMAT_BITS:
+            return dequant_int_row(a[p + "_codes"][idx], a[p + "_scales"][idx], ROW_FORMAT_BITS[fmt])
         raise ValueError(fmt)
 
     def routed_gu(self, e: int) -> np.ndarray:
@@ -496,7 +541,14 @@ class Layer:
         out = np.zeros((t_count, self.H))
 
         nvfp4 = self.weight_format == "nvfp4"
+        q8 = self.act_quant == "q8_0"
         x_in = quantize_nvfp4_activation(x64.astype(np.float32)) if nvfp4 else x64
+        if q8:      # int8 activations into every expert matmul (x here, h below)
+            x_in = quantize_q8_0_activation(x64)
+            hidden_in = hidden
+
+            def hidden(w_gu, xr):
+                return quantize_q8_0_activation(hidden_in(w_gu, xr))
 
         # routed experts, batch-union: each expert's weights applied to all its tokens
         hs = {}      # e -> (entries, h rows)

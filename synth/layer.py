@@ -68,6 +68,7 @@ class LayerSpec:
     seed: int = 0
     weight_std: float = 0.02
     expert_top_p: float = 0.0  # adaptive expert top-p (0 = off)
+    act_quant: str = "none"    # "none" | "q8_0" (int8 activations into the expert matmuls)
 
     @property
     def experts_per_group(self) -> int:
@@ -119,6 +120,25 @@ LAYERS = {
     "small_nvfp4_topp": replace(_SMALL, name="small_h2048_e32_nvfp4", weight_format="nvfp4",
                                 router_dtype="bf16", shared_format="bf16", expert_top_p=0.7),
     "glm52_topp": replace(_GLM, expert_top_p=0.7),
+    # the pages' per-row formats (scale per row; int8, packed int4, packed int2), and int4
+    # per row with Q8_0-style int8 activations
+    "small_int8_row": replace(_SMALL, name="small_h2048_e32_int8row", weight_format="int8_row",
+                              shared_format="int8_row"),
+    "small_int4_row": replace(_SMALL, name="small_h2048_e32_int4row", weight_format="int4_row",
+                              shared_format="int4_row"),
+    "small_int2_row": replace(_SMALL, name="small_h2048_e32_int2row", weight_format="int2_row",
+                              shared_format="int2_row"),
+    "small_int4_row_q8": replace(_SMALL, name="small_h2048_e32_int4row", weight_format="int4_row",
+                                 shared_format="int4_row", act_quant="q8_0"),
+    # GLM expert shapes with 64 routed experts, one per weight format (per-format GEMV
+    # comparison at T = 1)
+    "glm52_e64_int4_g32": replace(_GLM, name="glm52_h6144_e64_int4g32", n_experts=64),
+    "glm52_e64_int8_row": replace(_GLM, name="glm52_h6144_e64_int8row", n_experts=64,
+                                  weight_format="int8_row", shared_format="int8_row"),
+    "glm52_e64_int4_row": replace(_GLM, name="glm52_h6144_e64_int4row", n_experts=64,
+                                  weight_format="int4_row", shared_format="int4_row"),
+    "glm52_e64_int2_row": replace(_GLM, name="glm52_h6144_e64_int2row", n_experts=64,
+                                  weight_format="int2_row", shared_format="int2_row"),
 }
 
 WORKLOADS = {
@@ -130,6 +150,11 @@ WORKLOADS = {
     # independently (the pages give no statistics of how their routing overlaps)
     "glm52_mtp_verify_t3": Workload("glm52_mtp_verify_t3", LAYERS["glm52"], tokens=3, steps=1000),
     "glm52_mtp_verify_t5": Workload("glm52_mtp_verify_t5", LAYERS["glm52"], tokens=5, steps=1000),
+    # per-format GEMV comparison, T = 1 (E = 64 stand-in of the GLM layer)
+    "glm52_e64_int4_g32_t1": Workload("glm52_e64_int4_g32_t1", LAYERS["glm52_e64_int4_g32"], tokens=1, steps=200),
+    "glm52_e64_int8_row_t1": Workload("glm52_e64_int8_row_t1", LAYERS["glm52_e64_int8_row"], tokens=1, steps=200),
+    "glm52_e64_int4_row_t1": Workload("glm52_e64_int4_row_t1", LAYERS["glm52_e64_int4_row"], tokens=1, steps=200),
+    "glm52_e64_int2_row_t1": Workload("glm52_e64_int2_row_t1", LAYERS["glm52_e64_int2_row"], tokens=1, steps=200),
     "glm52_decode_t4": Workload("glm52_decode_t4", LAYERS["glm52_unbiased"], tokens=4),
     "glm52_decode_t32": Workload("glm52_decode_t32", LAYERS["glm52_unbiased"], tokens=32),
     "glm52_prefill_t2048": Workload("glm52_prefill_t2048", LAYERS["glm52_skewed"], tokens=2048),
@@ -177,6 +202,34 @@ def quantize_int4_g32(w: np.ndarray):
     u = (q.view(np.uint8) & np.uint8(0x0F)).reshape(n, k // 2, 2)
     codes = (u[..., 0] | (u[..., 1] << np.uint8(4))).astype(np.uint8)
     return codes, scale
+
+
+def quantize_int_row(w: np.ndarray, bits: int):
+    """Symmetric per-row integers (int8, packed int4, packed int2 with one scale per row).
+
+    qmax = 2^(bits-1) - 1; scale = float32(absmax(row)) / qmax in fp32; code =
+    clamp(rint_even(w / scale), -qmax - 1, qmax) (a zero row stores zero codes). Packing:
+    int8 one per byte; int4 element 2j in the low nibble of byte j; int2 element 4j + i in
+    bits 2i..2i+1 of byte j (two's complement fields).
+    Returns (codes uint8 [N, K * bits / 8], scales float32 [N, 1]).
+    """
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    n, k = w.shape
+    per = 8 // bits
+    assert k % per == 0
+    qmax = (1 << (bits - 1)) - 1
+    scale = (np.max(np.abs(w), axis=1) / np.float32(qmax)).astype(np.float32)
+    q = np.zeros_like(w)
+    np.divide(w, scale[:, None], out=q, where=scale[:, None] != 0)
+    q = np.clip(np.rint(q), -qmax - 1, qmax).astype(np.int64)
+    u = (q & ((1 << bits) - 1)).reshape(n, k // per, per)
+    codes = np.zeros((n, k // per), np.int64)
+    for i in range(per):
+        codes |= u[..., i] << (bits * i)
+    return codes.astype(np.uint8), scale.reshape(n, 1)
+
+
+_ROW_BITS = {"int8_row": 8, "int4_row": 4, "int2_row": 2}
 
 
 def _grid_e4m3() -> np.ndarray:
@@ -260,6 +313,10 @@ def _draw_expert(args):
                 "d_codes": dc, "d_scales": ds, "d_tscale": dt}
     if fmt == "bf16":
         return {"gu_bf16": f32_to_bf16_bits(w_gu), "d_bf16": f32_to_bf16_bits(w_d)}
+    if fmt in _ROW_BITS:
+        gc, gs = quantize_int_row(w_gu, _ROW_BITS[fmt])
+        dc, ds = quantize_int_row(w_d, _ROW_BITS[fmt])
+        return {"gu_codes": gc, "gu_scales": gs, "d_codes": dc, "d_scales": ds}
     raise ValueError(f"unknown weight format {fmt!r}")
 
 
@@ -279,6 +336,12 @@ def _alloc_expert_arrays(n: int, hidden: int, inter: int, fmt: str, prefix: str)
     if fmt == "bf16":
         return {f"{prefix}gu_bf16": np.empty((n, 2 * inter, hidden), np.uint16),
                 f"{prefix}d_bf16": np.empty((n, hidden, inter), np.uint16)}
+    if fmt in _ROW_BITS:
+        per = 8 // _ROW_BITS[fmt]
+        return {f"{prefix}gu_codes": np.empty((n, 2 * inter, hidden // per), np.uint8),
+                f"{prefix}gu_scales": np.empty((n, 2 * inter, 1), np.float32),
+                f"{prefix}d_codes": np.empty((n, hidden, inter // per), np.uint8),
+                f"{prefix}d_scales": np.empty((n, hidden, 1), np.float32)}
     raise ValueError(fmt)
 
 

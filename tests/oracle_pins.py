@@ -381,6 +381,50 @@ def pin_expert_top_p_invariants(O):
         assert np.all(routed.ravel()[lst] >= 0)
 
 
+def pin_int_row_formats(O):
+    """Per-row integer formats, hand-decoded bytes: int8 one per byte, int4 element 2j in
+    the low nibble, int2 element 4j + i in bits 2i..2i+1, all two's complement; the row
+    scale multiplies every element of its row."""
+    assert O.decode_int_row(np.array([[0x00, 0x7F, 0x80, 0xFF]], np.uint8), 8).tolist() == [[0, 127, -128, -1]]
+    assert O.decode_int_row(np.array([[0x8F, 0x71]], np.uint8), 4).tolist() == [[-1, -8, 1, 7]]
+    assert O.decode_int_row(np.array([[0xE4, 0x1B]], np.uint8), 2).tolist() == [[0, 1, -2, -1, -1, -2, 1, 0]]
+    w = O.dequant_int_row(np.array([[0xE4], [0x1B]], np.uint8), np.array([[0.5], [4.0]], np.float32), 2)
+    assert w.tolist() == [[0.0, 0.5, -1.0, -0.5], [-4.0, -8.0, 4.0, 0.0]]
+
+
+def pin_int_row_roundtrip(O):
+    """The generator's per-row quantiser decoded by the oracle stays within half a step
+    (|w - code * scale| <= scale / 2; the largest |w| of a row maps to qmax exactly)."""
+    from synth.layer import quantize_int_row
+    rng = np.random.default_rng(13)
+    w = rng.normal(0, 0.05, (16, 128)).astype(np.float32)
+    for bits in (8, 4, 2):
+        codes, scale = quantize_int_row(w, bits)
+        deq = O.dequant_int_row(codes, scale, bits)
+        assert np.all(np.abs(deq - w) <= scale.astype(np.float64) / 2 * (1 + 1e-6))
+        qmax = (1 << (bits - 1)) - 1
+        assert np.all(np.abs(O.decode_int_row(codes, bits)).max(axis=1) == qmax)
+
+
+def pin_q8_0_activation(O):
+    """Q8_0 activations, hand-worked: exact multiples of the block step come back exactly;
+    halfway quotients round to even; the block step is the fp16 value of amax / 127
+    (amax 1 gives d = 516 / 65536, so 1 -> 127 d = 0.99993896484375 and 0.5 -> 64 d =
+    0.50390625); an all-zero block stays zero; blocks are 32 wide."""
+    n = np.arange(-16, 16, dtype=np.float64)
+    n[0] = -127.0
+    a = (n / 16.0)[None, :]
+    assert np.array_equal(O.quantize_q8_0_activation(a), a)
+    b = np.zeros((1, 32))
+    b[0, :4] = [127.0, 2.5, 3.5, -0.5]
+    assert O.quantize_q8_0_activation(b)[0, :4].tolist() == [127.0, 2.0, 4.0, 0.0]
+    c = np.zeros((1, 64))
+    c[0, :2] = [1.0, 0.5]
+    got = O.quantize_q8_0_activation(c)
+    assert got[0, 0] == 0.99993896484375 and got[0, 1] == 0.50390625
+    assert not got[0, 2:].any()
+
+
 # ------------------------------------------------------------------- expert FFN
 
 
@@ -493,4 +537,5 @@ ALL_PINS = [pin_decode_int4, pin_decode_e4m3, pin_decode_e2m1, pin_dequant_int4_
             pin_select_special_cases, pin_routing_weights, pin_group_tokens,
             pin_expert_ffn_torch, pin_hand_two_expert, pin_identity_activation_exact,
             pin_hand_nvfp4_layer, pin_widen_bf16, pin_expert_top_p_hand,
-            pin_expert_top_p_invariants]
+            pin_expert_top_p_invariants, pin_int_row_formats, pin_int_row_roundtrip,
+            pin_q8_0_activation]

@@ -166,6 +166,38 @@ def _group_dropped_counted(ids, n_experts):
     return _orig["group_tokens"](np.asarray(ids) % n_experts, n_experts)
 
 
+def _int_row_fields_reversed(codes, bits):
+    v = _orig["decode_int_row"](codes, bits)
+    per = 8 // bits
+    return v.reshape(v.shape[:-1] + (-1, per))[..., ::-1].reshape(v.shape)
+
+
+def _int_row_unsigned(codes, bits):
+    v = _orig["decode_int_row"](codes, bits)
+    return np.where(v < 0, v + (1 << bits), v)
+
+
+def _q8_0_no_fp16_step(a):
+    a32 = np.asarray(a, np.float32)
+    m, k = a32.shape
+    blk = a32.reshape(m, k // 32, 32)
+    d = (np.max(np.abs(blk), axis=2) / np.float32(127.0)).astype(np.float32)
+    q = np.zeros(blk.shape, np.float32)
+    np.divide(blk, d[..., None], out=q, where=d[..., None] != 0)
+    return (np.clip(np.rint(q), -127, 127) * d[..., None]).astype(np.float64).reshape(m, k)
+
+
+def _q8_0_round_half_up(a):
+    a32 = np.asarray(a, np.float32)
+    m, k = a32.shape
+    blk = a32.reshape(m, k // 32, 32)
+    d = (np.max(np.abs(blk), axis=2) / np.float32(127.0)).astype(np.float16).astype(np.float32)
+    q = np.zeros(blk.shape, np.float32)
+    np.divide(blk, d[..., None], out=q, where=d[..., None] != 0)
+    q = np.sign(q) * np.floor(np.abs(q) + 0.5)
+    return (np.clip(q, -127, 127) * d[..., None]).astype(np.float64).reshape(m, k)
+
+
 MUTANTS = {
     "decode_int4/nibbles_swapped": ("decode_int4", _nibbles_swapped),
     "decode_int4/unsigned": ("decode_int4", _unsigned_int4),
@@ -192,6 +224,10 @@ MUTANTS = {
     "top_p/ties_high": ("expert_top_p", lambda s, i, p: _top_p_variant(s, i, p, ties_high=True)),
     "weights/dropped_unmasked": ("routing_weights", _weights_dropped_unmasked),
     "group/dropped_counted": ("group_tokens", _group_dropped_counted),
+    "int_row/fields_reversed": ("decode_int_row", _int_row_fields_reversed),
+    "int_row/unsigned": ("decode_int_row", _int_row_unsigned),
+    "q8_0/no_fp16_step": ("quantize_q8_0_activation", _q8_0_no_fp16_step),
+    "q8_0/round_half_up": ("quantize_q8_0_activation", _q8_0_round_half_up),
 }
 
 
