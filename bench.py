@@ -44,6 +44,8 @@ def parse():
     p.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle time")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--fp4-peak", action="store_true", help="measure the dense NVFP4 tensor peak and exit")
+    p.add_argument("--path", default="auto", choices=["auto", "gemv", "grouped", "generic"],
+                   help="force the expert path (per-format GEMV comparisons)")
     return p.parse_args()
 
 
@@ -251,8 +253,11 @@ def expert_bytes(spec):
     H, I = spec.hidden, spec.inter
     if spec.weight_format == "int4_g32":
         per = lambda n, k: n * (k // 2 + k // 32 * 2)
-    else:
+    elif spec.weight_format == "nvfp4":
         per = lambda n, k: n * (k // 2 + k // 16) + 4
+    else:   # per-row int8 / int4 / int2 with an fp32 scale per row
+        bits = {"int8_row": 8, "int4_row": 4, "int2_row": 2}[spec.weight_format]
+        per = lambda n, k: n * (k * bits // 8 + 4)
     return per(2 * I, H), per(H, I)
 
 
@@ -366,6 +371,10 @@ def run_ours(args):
     K, W, C = args.steps, args.warmup, max(1, args.copies)
     arrays = make_layer(spec)
     layers = [moe.MoeLayer.from_spec(spec, arrays, max_tokens=T) for _ in range(C)]
+    path = {"auto": moe.PATH_AUTO, "gemv": moe.PATH_GEMV, "grouped": moe.PATH_GROUPED,
+            "generic": moe.PATH_GENERIC}[args.path]
+    for L in layers:
+        L.set_path(path)
     stream = torch.cuda.Stream()
     dt = torch.bfloat16 if spec.act_dtype == "bf16" else torch.float32
     H = spec.hidden
@@ -466,6 +475,9 @@ def run_ours(args):
         unit_gu = n_units * gu_b
         unit_all = n_units * (gu_b + d_b)
     fused = launches == K                              # decode path: one kernel per step
+    generic = args.path == "generic" or spec.weight_format.endswith("_row") or \
+        getattr(spec, "act_quant", "none") != "none"
+    dtype = "f32" if generic else "nvfp4" if spec.weight_format == "nvfp4" else "f16"
     peak_bw, peak_kind = measured_peaks()
     peak_tf, tf_kind = measured_tflops()
     step_s = ms / K / 1000.0
@@ -484,7 +496,11 @@ def run_ours(args):
         # a shared expert in the routed format runs in the same launch, a bf16 one in the
         # next stage)
         dom_s = stage_ms["gate_up_or_fused"] / 1000.0
-        if spec.weight_format == "nvfp4" and spec.shared_format == "bf16":
+        if generic:
+            kernel = "expert_up_kernel gate/up (CUDA cores, fp32)"
+            rows, dom_bytes = T * spec.top_k + T, unit_gu
+            peak_t, t_kind = 148 * 128 * 2 * 2.032e9 / 1e12, "fp32 FMA: 148 SMs x 128 lanes x 2 x 2.032 GHz"
+        elif spec.weight_format == "nvfp4" and spec.shared_format == "bf16":
             kernel = "moe_gemm_fp4_kernel gate/up (tcgen05 kind::mxf4nvf4)"
             rows, dom_bytes = T * spec.top_k, n_units * gu_b
             peak_t, t_kind = measured_fp4_tflops()
@@ -512,12 +528,13 @@ def run_ours(args):
     roofline["frac_of_8tbs_nominal"] = unit_all / K / step_s / 8e12
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "nvfp4" if spec.weight_format == "nvfp4" else "f16",
+            "vs_baseline": None, "dtype": dtype,
             "data": "synthetic (seeded, random-init weights)",
             "config": {"workload": wl.name, "tokens_per_step": T, "layer": spec.name,
                        "layer_copies": C, "l2": f"inputs larger than L2: {C} layer copies "
                        "rotated per step, each step streams its experts from HBM",
-                       "unique_experts_mean": float(np.mean(uniq)),
+                       "unique_experts_mean": float(np.mean(uniq)), "path": args.path,
+                       "weight_format": spec.weight_format, "act_quant": getattr(spec, "act_quant", "none"),
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline,
             "stage_ms_per_step": {k: v / max(nfw, 1) for k, v in stage_ms.items()},

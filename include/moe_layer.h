@@ -48,7 +48,12 @@ typedef enum {
 } moe_status;
 
 /* storage formats */
-enum { MOE_W_INT4_G32 = 0, MOE_W_NVFP4 = 1, MOE_W_BF16 = 2 };
+enum { MOE_W_INT4_G32 = 0, MOE_W_NVFP4 = 1, MOE_W_BF16 = 2, MOE_W_INT8_ROW = 3, MOE_W_INT4_ROW = 4,
+       MOE_W_INT2_ROW = 5 };
+/* Activations into the expert matmuls: as given, or Q8_0-style int8 (per 32 elements of a
+ * row, step d = fp16(amax / 127), code = clamp(rint(v / d), -127, 127); x before gate/up and
+ * h before down, routed and shared experts). */
+enum { MOE_ACT_NONE = 0, MOE_ACT_Q8_0 = 1 };
 /* activation / router element types */
 enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 };
 /*
@@ -70,12 +75,23 @@ typedef struct {
   int32_t topk_group;          /* groups kept per token */
   int32_t max_tokens;          /* largest T forward will be called with */
   float routed_scaling_factor; /* rsf */
-  int32_t weight_format;       /* routed experts: MOE_W_INT4_G32 | MOE_W_NVFP4 */
-  int32_t shared_format;       /* shared expert: MOE_W_INT4_G32 | MOE_W_NVFP4 | MOE_W_BF16 */
+  int32_t weight_format;       /* routed experts: MOE_W_INT4_G32 | MOE_W_NVFP4 | MOE_W_INT*_ROW */
+  int32_t shared_format;       /* shared expert: the routed format, or MOE_W_BF16 */
   int32_t act_dtype;           /* x and out: MOE_DT_F32 | MOE_DT_BF16 */
   int32_t router_dtype;        /* W_r: MOE_DT_F32 | MOE_DT_BF16 */
   float expert_top_p;          /* adaptive expert top-p; 0 (or >= 1) = off, see below */
+  int32_t act_quant;           /* MOE_ACT_NONE | MOE_ACT_Q8_0 (per-row integer or int4_g32
+                                  layers whose shared expert is in the routed format) */
 } moe_config;
+
+/*
+ * Per-row integer formats ("Show HN: Menjalankan GLM 5.2 di komputer lambat", section "Fitur
+ * utama yang diimplementasikan": int8, packed int4, packed int2, scale per-row): codes
+ * [rows, K * bits / 8] two's complement (int8 one per byte; int4 element 2j in the low
+ * nibble of byte j; int2 element 4j + i in bits 2i..2i+1 of byte j) and one fp32 scale per
+ * row ([rows, 1]); w = code * scale. They and MOE_ACT_Q8_0 run on the CUDA-core batch-union
+ * kernels (MOE_PATH_GENERIC; AUTO picks it, GEMV and GROUPED are MOE_ERR_UNSUPPORTED).
+ */
 
 /*
  * Adaptive expert top-p (the "--topp" option of "Show HN: Menjalankan GLM 5.2 di komputer

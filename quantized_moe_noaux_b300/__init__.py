@@ -18,11 +18,13 @@ __all__ = ["MoeLayer", "MoeError", "lib", "LIB_PATH", "SYMBOLS", "STAGES", "W_IN
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
 
-W_INT4_G32, W_NVFP4, W_BF16 = 0, 1, 2
+W_INT4_G32, W_NVFP4, W_BF16, W_INT8_ROW, W_INT4_ROW, W_INT2_ROW = 0, 1, 2, 3, 4, 5
 DT_F32, DT_BF16 = 0, 1
 PATH_AUTO, PATH_GEMV, PATH_GROUPED, PATH_GENERIC = 0, 1, 2, 3
 
-_FMT = {"int4_g32": W_INT4_G32, "nvfp4": W_NVFP4, "bf16": W_BF16}
+_FMT = {"int4_g32": W_INT4_G32, "nvfp4": W_NVFP4, "bf16": W_BF16, "int8_row": W_INT8_ROW,
+        "int4_row": W_INT4_ROW, "int2_row": W_INT2_ROW}
+_ACT = {"none": 0, "q8_0": 1}
 _DT = {"f32": DT_F32, "bf16": DT_BF16}
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_OOM",
           4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_DEVICE_CHECK"}
@@ -41,7 +43,7 @@ class Config(ctypes.Structure):
                 ("max_tokens", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
                 ("weight_format", ctypes.c_int32), ("shared_format", ctypes.c_int32),
                 ("act_dtype", ctypes.c_int32), ("router_dtype", ctypes.c_int32),
-                ("expert_top_p", ctypes.c_float)]
+                ("expert_top_p", ctypes.c_float), ("act_quant", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
@@ -149,10 +151,10 @@ class MoeLayer:
     def __init__(self, arrays: dict, *, hidden: int, inter: int, n_experts: int, top_k: int,
                  n_group: int, topk_group: int, rsf: float, weight_format: str,
                  shared_format: str, act_dtype: str, router_dtype: str, max_tokens: int,
-                 expert_top_p: float = 0.0, stream=None):
+                 expert_top_p: float = 0.0, act_quant: str = "none", stream=None):
         self.cfg = Config(hidden, inter, n_experts, top_k, n_group, topk_group, max_tokens,
                           rsf, _FMT[weight_format], _FMT[shared_format], _DT[act_dtype],
-                          _DT[router_dtype], expert_top_p)
+                          _DT[router_dtype], expert_top_p, _ACT[act_quant])
         self.hidden, self.top_k, self.n_experts, self.max_tokens = hidden, top_k, n_experts, max_tokens
         self.act_dtype = act_dtype
         a = arrays
@@ -176,7 +178,8 @@ class MoeLayer:
                    rsf=spec.rsf, weight_format=spec.weight_format,
                    shared_format=spec.shared_format, act_dtype=spec.act_dtype,
                    router_dtype=spec.router_dtype, max_tokens=max_tokens,
-                   expert_top_p=getattr(spec, "expert_top_p", 0.0), stream=stream)
+                   expert_top_p=getattr(spec, "expert_top_p", 0.0),
+                   act_quant=getattr(spec, "act_quant", "none"), stream=stream)
 
     @property
     def handle(self) -> int:

@@ -53,6 +53,30 @@ nvfp4_quant_kernel(const void* __restrict__ src, float* __restrict__ dst, size_t
   }
 }
 
+// Q8_0-style int8 activations (the integer-dot kernels' activations of "Show HN: Menjalankan
+// GLM 5.2 di komputer lambat", section "Fitur utama yang diimplementasikan"): one thread per
+// 32-element block; step d = fp16_rn(amax / 127), code = clamp(rint(v / d), -127, 127) (d = 0
+// gives 0), both quotients correctly rounded fp32 operations; writes code * d (exact in fp32).
+template <int DT>
+__global__ void __launch_bounds__(kThreads)
+q8_0_quant_kernel(const void* __restrict__ src, float* dst, size_t nblocks) {
+  for (size_t b = (size_t)blockIdx.x * kThreads + threadIdx.x; b < nblocks;
+       b += (size_t)gridDim.x * kThreads) {
+    float v[32], amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      v[i] = load_act<DT>(src, b * 32 + i);
+      amax = fmaxf(amax, fabsf(v[i]));
+    }
+    const float d = __half2float(__float2half_rn(__fdiv_rn(amax, 127.0f)));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float q = d != 0.f ? fminf(fmaxf(rintf(__fdiv_rn(v[i], d)), -127.f), 127.f) : 0.f;
+      dst[b * 32 + i] = q * d;
+    }
+  }
+}
+
 // out = acc in the output type, 8 elements per thread step (n is a multiple of 8: H is).
 template <int DT>
 __global__ void __launch_bounds__(kThreads)
@@ -89,6 +113,16 @@ cudaError_t launch_amax(const void* src, int src_dtype, size_t n, unsigned int* 
     amax_kernel<MOE_DT_F32><<<grid_for(n), kThreads, 0, s>>>(src, n, amax_bits);
   else
     amax_kernel<MOE_DT_BF16><<<grid_for(n), kThreads, 0, s>>>(src, n, amax_bits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_q8_0_quant(const void* src, int src_dtype, float* dst, size_t n, cudaStream_t s) {
+  const size_t nb = n / 32;
+  if (nb == 0) return cudaSuccess;
+  if (src_dtype == MOE_DT_F32)
+    q8_0_quant_kernel<MOE_DT_F32><<<grid_for(nb), kThreads, 0, s>>>(src, dst, nb);
+  else
+    q8_0_quant_kernel<MOE_DT_BF16><<<grid_for(nb), kThreads, 0, s>>>(src, dst, nb);
   return cudaGetLastError();
 }
 

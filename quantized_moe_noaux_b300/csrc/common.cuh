@@ -176,12 +176,47 @@ struct WFmt<MOE_W_BF16> {
   }
 };
 
+// Per-row integer formats (one fp32 scale per row): int8 16, int4 32, int2 64 elements per
+// 16-byte chunk, two's complement fields from the low bits up.
+template <int BITS>
+struct WFmtRow {
+  static constexpr int EPC = 128 / BITS;
+  __device__ __forceinline__ static void decode(uint4 d, const uint8_t* srow, int, float, float (&w)[EPC]) {
+    const float s = __ldg(reinterpret_cast<const float*>(srow));
+    const uint32_t words[4] = {d.x, d.y, d.z, d.w};
+    constexpr int per = 32 / BITS;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int i = 0; i < per; ++i) {
+        const int v = (int)(words[q] << (32 - BITS * (i + 1))) >> (32 - BITS);   // sign-extended field
+        w[q * per + i] = (float)v * s;
+      }
+  }
+};
+template <>
+struct WFmt<MOE_W_INT8_ROW> : WFmtRow<8> {};
+template <>
+struct WFmt<MOE_W_INT4_ROW> : WFmtRow<4> {};
+template <>
+struct WFmt<MOE_W_INT2_ROW> : WFmtRow<2> {};
+
+__host__ __device__ inline bool is_row_format(int fmt) {
+  return fmt == MOE_W_INT8_ROW || fmt == MOE_W_INT4_ROW || fmt == MOE_W_INT2_ROW;
+}
+
 // Bytes of one stored weight row of K input elements (codes) and of its scales.
 __host__ __device__ inline size_t row_code_bytes(int fmt, int K) {
-  return fmt == MOE_W_BF16 ? (size_t)K * 2 : (size_t)K / 2;
+  return fmt == MOE_W_BF16       ? (size_t)K * 2
+         : fmt == MOE_W_INT8_ROW ? (size_t)K
+         : fmt == MOE_W_INT2_ROW ? (size_t)K / 4
+                                 : (size_t)K / 2;
 }
 __host__ __device__ inline size_t row_scale_bytes(int fmt, int K) {
-  return fmt == MOE_W_INT4_G32 ? (size_t)K / 32 * 2 : fmt == MOE_W_NVFP4 ? (size_t)K / 16 : 0;
+  return fmt == MOE_W_INT4_G32 ? (size_t)K / 32 * 2
+         : fmt == MOE_W_NVFP4  ? (size_t)K / 16
+         : is_row_format(fmt)  ? 4
+                               : 0;
 }
 
 // ----------------------------------------------------------- work decomposition

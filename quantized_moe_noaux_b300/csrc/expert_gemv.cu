@@ -200,9 +200,18 @@ cudaError_t expert_kernels_init() {
       allow_smem(expert_up_kernel<MOE_W_NVFP4, MOE_DT_BF16>),
       allow_smem(expert_up_kernel<MOE_W_BF16, MOE_DT_F32>),
       allow_smem(expert_up_kernel<MOE_W_BF16, MOE_DT_BF16>),
+      allow_smem(expert_up_kernel<MOE_W_INT8_ROW, MOE_DT_F32>),
+      allow_smem(expert_up_kernel<MOE_W_INT8_ROW, MOE_DT_BF16>),
+      allow_smem(expert_up_kernel<MOE_W_INT4_ROW, MOE_DT_F32>),
+      allow_smem(expert_up_kernel<MOE_W_INT4_ROW, MOE_DT_BF16>),
+      allow_smem(expert_up_kernel<MOE_W_INT2_ROW, MOE_DT_F32>),
+      allow_smem(expert_up_kernel<MOE_W_INT2_ROW, MOE_DT_BF16>),
       allow_smem(expert_down_kernel<MOE_W_INT4_G32>),
       allow_smem(expert_down_kernel<MOE_W_NVFP4>),
-      allow_smem(expert_down_kernel<MOE_W_BF16>)};
+      allow_smem(expert_down_kernel<MOE_W_BF16>),
+      allow_smem(expert_down_kernel<MOE_W_INT8_ROW>),
+      allow_smem(expert_down_kernel<MOE_W_INT4_ROW>),
+      allow_smem(expert_down_kernel<MOE_W_INT2_ROW>)};
   for (cudaError_t x : r)
     if (x != cudaSuccess) e = x;
   return e;
@@ -222,6 +231,15 @@ cudaError_t launch_expert_up(const ExpertGemvArgs& a, cudaStream_t s) {
     case MOE_W_BF16:
       return xf ? launch_with_smem(expert_up_kernel<MOE_W_BF16, MOE_DT_F32>, grid, smem, s, a)
                 : launch_with_smem(expert_up_kernel<MOE_W_BF16, MOE_DT_BF16>, grid, smem, s, a);
+    case MOE_W_INT8_ROW:
+      return xf ? launch_with_smem(expert_up_kernel<MOE_W_INT8_ROW, MOE_DT_F32>, grid, smem, s, a)
+                : launch_with_smem(expert_up_kernel<MOE_W_INT8_ROW, MOE_DT_BF16>, grid, smem, s, a);
+    case MOE_W_INT4_ROW:
+      return xf ? launch_with_smem(expert_up_kernel<MOE_W_INT4_ROW, MOE_DT_F32>, grid, smem, s, a)
+                : launch_with_smem(expert_up_kernel<MOE_W_INT4_ROW, MOE_DT_BF16>, grid, smem, s, a);
+    case MOE_W_INT2_ROW:
+      return xf ? launch_with_smem(expert_up_kernel<MOE_W_INT2_ROW, MOE_DT_F32>, grid, smem, s, a)
+                : launch_with_smem(expert_up_kernel<MOE_W_INT2_ROW, MOE_DT_BF16>, grid, smem, s, a);
   }
   return cudaErrorInvalidValue;
 }
@@ -233,6 +251,9 @@ cudaError_t launch_expert_down(const ExpertGemvArgs& a, cudaStream_t s) {
     case MOE_W_INT4_G32: return launch_with_smem(expert_down_kernel<MOE_W_INT4_G32>, grid, smem, s, a);
     case MOE_W_NVFP4: return launch_with_smem(expert_down_kernel<MOE_W_NVFP4>, grid, smem, s, a);
     case MOE_W_BF16: return launch_with_smem(expert_down_kernel<MOE_W_BF16>, grid, smem, s, a);
+    case MOE_W_INT8_ROW: return launch_with_smem(expert_down_kernel<MOE_W_INT8_ROW>, grid, smem, s, a);
+    case MOE_W_INT4_ROW: return launch_with_smem(expert_down_kernel<MOE_W_INT4_ROW>, grid, smem, s, a);
+    case MOE_W_INT2_ROW: return launch_with_smem(expert_down_kernel<MOE_W_INT2_ROW>, grid, smem, s, a);
   }
   return cudaErrorInvalidValue;
 }

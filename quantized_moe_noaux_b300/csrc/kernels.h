@@ -67,6 +67,9 @@ cudaError_t launch_amax(const void* src, int src_dtype, size_t n, unsigned int* 
                         cudaStream_t s);
 cudaError_t launch_nvfp4_quant(const void* src, int src_dtype, float* dst, size_t n,
                                const unsigned int* amax_bits, cudaStream_t s);
+// Q8_0-style int8 activations, dequantised to fp32: per 32 elements d = fp16(amax / 127),
+// dst = clamp(rint(v / d), -127, 127) * d (dst may alias an fp32 src).
+cudaError_t launch_q8_0_quant(const void* src, int src_dtype, float* dst, size_t n, cudaStream_t s);
 
 // ------------------------------------------------------------- fused decode path
 // One cooperative kernel per decode step (T <= 8) reading the grouped GEMM's packed int4
@@ -120,7 +123,7 @@ struct GemmMaps {
 };
 // Weight storage of the grouped GEMM besides MOE_W_INT4_G32 / MOE_W_NVFP4: plain fp16
 // rows (a bf16 shared expert converted once at layer creation).
-constexpr int kWF16 = 3;
+constexpr int kWF16 = 16;
 
 struct GemmParams {
   const int4* items;          // (expert, first sorted row, rows, 0)

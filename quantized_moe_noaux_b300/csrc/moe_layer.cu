@@ -121,9 +121,11 @@ moe_status validate_config(const moe_config* c) {
     return MOE_ERR_INVALID_ARG;
   if (!(c->routed_scaling_factor > 0.f)) return MOE_ERR_INVALID_ARG;
   if (c->expert_top_p != c->expert_top_p) return MOE_ERR_INVALID_ARG;   // NaN
-  if (c->weight_format != MOE_W_INT4_G32 && c->weight_format != MOE_W_NVFP4) return MOE_ERR_UNSUPPORTED;
-  if (c->shared_format != MOE_W_INT4_G32 && c->shared_format != MOE_W_NVFP4 &&
-      c->shared_format != MOE_W_BF16)
+  if (c->weight_format != MOE_W_INT4_G32 && c->weight_format != MOE_W_NVFP4 && !is_row_format(c->weight_format))
+    return MOE_ERR_UNSUPPORTED;
+  if (c->shared_format != c->weight_format && c->shared_format != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
+  if (c->act_quant != MOE_ACT_NONE && c->act_quant != MOE_ACT_Q8_0) return MOE_ERR_UNSUPPORTED;
+  if (c->act_quant == MOE_ACT_Q8_0 && (c->weight_format == MOE_W_NVFP4 || c->shared_format != c->weight_format))
     return MOE_ERR_UNSUPPORTED;
   if (c->act_dtype != MOE_DT_F32 && c->act_dtype != MOE_DT_BF16) return MOE_ERR_UNSUPPORTED;
   if (c->router_dtype != MOE_DT_F32 && c->router_dtype != MOE_DT_BF16) return MOE_ERR_UNSUPPORTED;
@@ -257,7 +259,9 @@ moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt,
       (st = dev_alloc(L, &L->x_stage, (size_t)Tm * H * ab)) ||
       (st = dev_alloc(L, &L->out_stage, (size_t)Tm * H * ab)))
     return st;
-  if (c->weight_format == MOE_W_NVFP4 && (st = dev_alloc_t(L, &L->xq, (size_t)Tm * H * 4))) return st;
+  if ((c->weight_format == MOE_W_NVFP4 || c->act_quant == MOE_ACT_Q8_0) &&
+      (st = dev_alloc_t(L, &L->xq, (size_t)Tm * H * 4)))
+    return st;
 
   int dev = 0;
   if (cudaGetDevice(&dev) || cudaDeviceGetAttribute(&L->n_sm, cudaDevAttrMultiProcessorCount, dev))
@@ -282,8 +286,9 @@ moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt,
 
   // grouped GEMM path: expert-sorted activation buffers and the TMA descriptors; a
   // separately stored (bf16) shared expert gets an fp16 copy for the same kernel
-  L->gemm_ok = gemm_supported(H, I) && gemm_kernels_init() == cudaSuccess &&
-               (L->shared_inline || c->shared_format == MOE_W_BF16);
+  // (per-row formats and Q8_0 activations run on the CUDA-core kernels only)
+  L->gemm_ok = gemm_supported(H, I) && !is_row_format(c->weight_format) && c->act_quant == MOE_ACT_NONE &&
+               gemm_kernels_init() == cudaSuccess && (L->shared_inline || c->shared_format == MOE_W_BF16);
   if (L->gemm_ok) {
     const int fmt = c->weight_format;
     L->gemm_rows = Tm * k + Tm;
@@ -536,9 +541,14 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
   if (gemm) return forward_gemm(L, x, T, out, s, m);
   const void* x_in = x;
   int x_dt = c.act_dtype;
+  const bool q8 = c.act_quant == MOE_ACT_Q8_0;
   if (nvfp4) {
     MOE_LAUNCH(launch_amax(x, c.act_dtype, (size_t)T * H, L->amax, s));
     MOE_LAUNCH(launch_nvfp4_quant(x, c.act_dtype, L->xq, (size_t)T * H, L->amax, s));
+    x_in = L->xq;
+    x_dt = MOE_DT_F32;
+  } else if (q8) {
+    MOE_LAUNCH(launch_q8_0_quant(x, c.act_dtype, L->xq, (size_t)T * H, s));
     x_in = L->xq;
     x_dt = MOE_DT_F32;
   }
@@ -582,6 +592,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
   if (!L->shared_inline) MOE_LAUNCH(launch_expert_up(sh, s));
   MOE_CK(m.mark(4));
   if (nvfp4) MOE_LAUNCH(launch_nvfp4_quant(L->h, MOE_DT_F32, L->h, (size_t)T * k * I, L->amax + 1, s));
+  if (q8) MOE_LAUNCH(launch_q8_0_quant(L->h, MOE_DT_F32, L->h, (size_t)T * (k + 1) * I, s));   // routed + shared h
   MOE_CK(m.mark(5));
   MOE_LAUNCH(launch_expert_down(a, s));
   if (!L->shared_inline) MOE_LAUNCH(launch_expert_down(sh, s));

@@ -62,6 +62,11 @@ def _cfg(**over):
     (dict(top_k=33), 2),                          # top_k above the selection limit
     (dict(n_experts=16, n_group=8, topk_group=1, top_k=3), 2),   # top_k > kept experts
     (dict(max_tokens=16385), 2),
+    (dict(expert_top_p=float("nan")), 1),          # adaptive top-p NaN
+    (dict(weight_format=moe.W_INT8_ROW), 2),       # shared expert neither the routed format nor bf16
+    (dict(act_quant=2), 2),                        # unknown activation quantisation
+    (dict(act_quant=1, weight_format=moe.W_NVFP4, shared_format=moe.W_NVFP4), 2),   # Q8_0 + NVFP4
+    (dict(act_quant=1, weight_format=moe.W_INT4_ROW, shared_format=moe.W_BF16), 2),  # Q8_0, bf16 shared
 ])
 def test_create_rejects_bad_configs_before_touching_the_device(over, code):
     """moe_layer_create checks the configuration first (no CUDA call, so this runs on CPU),
