@@ -567,10 +567,109 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def link_h2d_gbs(torch):
+    """Pinned host -> device copy bandwidth (1 GiB, best of 5, CUDA events): the host link's
+    measured peak, the denominator of the expert cache's link fraction."""
+    n = 1 << 30
+    src = torch.empty(n, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(n, dtype=torch.uint8, device="cuda")
+    best = None
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1000.0
+        best = t if best is None else min(best, t)
+    return n / best / 1e9
+
+
+def run_hostcache(args):
+    """Decode through a stack of GLM-shaped int4 layers whose routed experts live in host
+    memory, each with an HBM cache of a few expert slots (the pages' engine: experts streamed
+    from slower storage into a per-layer LRU cache, router-driven prefetch of the next layer,
+    a pinned hot set learned from usage). Token t's input to layer l is drawn correlated with
+    its input to layer l - 1 (x_l = rho x_(l-1) + sqrt(1 - rho^2) z), so predicting layer l's
+    experts from layer l - 1's input is informative but not exact. Three passes over the same
+    tokens: LRU only, LRU + prefetch, LRU + prefetch + the hot set pinned after the first
+    pass. Host-synchronous per layer (the host reads the routing back), timed by wall clock."""
+    import torch
+
+    import quantized_moe_noaux_b300 as moe
+    from synth import WORKLOADS, make_layer
+
+    wl = WORKLOADS[args.workload]
+    spec = wl.layer
+    n_layers, slots, rho, n_tok = 4, 32, 0.9, min(args.steps, wl.steps)
+    arrays = make_layer(spec)
+    layers = [moe.MoeLayer.from_spec(spec, arrays, max_tokens=1, cache_slots=slots) for _ in range(n_layers)]
+    rng = np.random.default_rng(77)
+    xs = np.empty((n_tok, n_layers, spec.hidden), np.float32)
+    for t in range(n_tok):
+        xs[t, 0] = rng.standard_normal(spec.hidden, dtype=np.float32)
+        for l in range(1, n_layers):
+            xs[t, l] = rho * xs[t, l - 1] + np.float32(np.sqrt(1 - rho * rho)) * rng.standard_normal(
+                spec.hidden, dtype=np.float32)
+    xb = torch.from_numpy(xs).to(torch.bfloat16).cuda()
+    out = torch.empty((1, spec.hidden), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    link = link_h2d_gbs(torch)
+
+    def one_pass(prefetch):
+        for L in layers:
+            L.reset_status()
+        before = [L.cache_stats() for L in layers]
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for t in range(n_tok):
+            for l in range(n_layers):
+                if prefetch and l + 1 < n_layers:
+                    layers[l + 1].prefetch(xb[t, l:l + 1], stream)   # next layer's experts from this input
+                layers[l].forward(xb[t, l:l + 1], out, stream)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        after = [L.cache_stats() for L in layers]
+        d = {k: sum(a[k] - b[k] for a, b in zip(after, before)) for k in moe.MoeLayer.CACHE_STATS}
+        routed = d["hits"] + d["misses"]
+        return {"tokens_per_s": n_tok / dt, "ms_per_token": dt * 1000 / n_tok,
+                "expert_hit_rate": d["hits"] / max(routed, 1),
+                "prefetched": d["prefetched"], "prefetch_hits": d["prefetch_hits"],
+                "h2d_gb_per_token": d["bytes_h2d"] / n_tok / 1e9, "link_gbs": d["bytes_h2d"] / dt / 1e9,
+                "link_frac": d["bytes_h2d"] / dt / 1e9 / link, "evictions": d["evictions"]}
+
+    one_pass(False)                     # warm-up pass: fills the caches and the usage counts
+    lru = one_pass(False)
+    pre = one_pass(True)
+    for L in layers:
+        L.cache_pin_hot(slots - 8)      # keep min(E, T * k) = 8 slots free for the rest
+    pin = one_pass(True)
+    for L in layers:
+        assert L.status() == 0
+        L.close()
+    line = {"metric": METRIC, "value": pin["tokens_per_s"], "unit": UNIT, "n_gpus": 1, "steps": n_tok,
+            "warmup": n_tok, "ms_per_step": pin["ms_per_token"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded, random-init weights)",
+            "config": {"workload": wl.name, "layer": spec.name, "layers": n_layers, "tokens_per_step": 1,
+                       "cache_slots_per_layer": slots, "experts_per_layer": spec.n_experts,
+                       "input_correlation_between_layers": rho,
+                       "host_store_gb_per_layer": (2 * spec.inter * spec.hidden + spec.hidden * spec.inter) * 9 / 16
+                       * spec.n_experts / 1e9},
+            "roofline": {"bound": "host link", "achieved": pin["link_gbs"], "peak": link,
+                         "peak_kind": "measured pinned host->device copy (1 GiB)", "unit": "GB/s",
+                         "frac": pin["link_frac"], "traffic": None},
+            "modes": {"lru": lru, "lru_prefetch": pre, "lru_prefetch_pinned": pin},
+            "gpu_launches": None}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.fp4_peak:
         fp4_peak()
+        return
+    if args.workload == "glm52_hostcache_t1":
+        run_hostcache(args)
         return
     if args.impl == "reference":
         run_reference(args)

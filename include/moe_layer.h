@@ -253,6 +253,47 @@ moe_status moe_layer_set_wait_limit(moe_layer* layer, int64_t ns);
 moe_status moe_layer_reset_status(moe_layer* layer, void* stream);
 
 /*
+ * Host-resident experts with an HBM cache ("Cara kerja eksekusi MoE berbasis streaming disk"
+ * in "Show HN: Menjalankan GLM 5.2 di komputer lambat": a per-layer LRU cache of experts over
+ * slower storage, an optional pinned hot store learned from usage counts; "Yönlendirici
+ * İleriye Dönük Ön-Getirme" in "Show HN: GLM 5.2 Modelini Yavaş Bilgisayarımda
+ * Çalıştırmak": the router predicts the next layer's experts so their loads start early).
+ *
+ * moe_layer_create_cached: like moe_layer_create, but the routed experts stay in pinned host
+ * memory (the library's copy, in the tensor-core path's packed layout) and HBM holds `slots`
+ * of them; the shared expert stays in HBM. Requires int4_g32 routed and shared experts, no
+ * act_quant, H and I multiples of 256, and min(E, max_tokens * top_k) <= slots <= E
+ * (MOE_ERR_INVALID_ARG otherwise for slots, MOE_ERR_UNSUPPORTED for the rest). Forwards on
+ * the layer run the grouped tensor-core path (GEMV and GENERIC are MOE_ERR_UNSUPPORTED): the
+ * routing runs on `stream`, the host reads the routed experts back (a synchronisation of
+ * `stream`; such forwards cannot be captured into a CUDA graph), the missing ones are copied
+ * into slots on the layer's copy stream (least recently used, unpinned experts that the call
+ * does not need are evicted), and the expert kernels wait for those copies. Use one stream
+ * for a cached layer's forwards and prefetches.
+ *
+ * moe_layer_prefetch: predict the experts of x [T, H] (device, act_dtype) with this layer's
+ * router on the copy stream (after the work already on `stream`) and start loading the
+ * missing ones, without waiting for the copies. For a stack of layers: prefetch layer l + 1
+ * with layer l's input before running layer l. Uses a routing workspace of its own.
+ *
+ * moe_layer_cache_pin_hot: pin the n experts most often routed so far (ties: lower id),
+ * loading them if needed; pinned experts are never evicted; a new call replaces the pins.
+ * MOE_ERR_INVALID_ARG if fewer than min(E, max_tokens * top_k) slots would stay unpinned.
+ *
+ * moe_layer_cache_stats: stats[0..5] = expert hits, misses, experts loaded by prefetch,
+ * prefetched experts later used, bytes copied host -> device, evictions.
+ * moe_layer_cache_query: slot_of[e] (-1 if not in HBM) and pinned[e] (0/1) for the E routed
+ * experts, into host arrays.
+ * All four return MOE_ERR_UNSUPPORTED on a layer created without a cache.
+ */
+moe_status moe_layer_create_cached(const moe_config* cfg, const moe_weights* w, int32_t slots,
+                                   void* stream, moe_layer** out);
+moe_status moe_layer_prefetch(moe_layer* layer, const void* x, int32_t T, void* stream);
+moe_status moe_layer_cache_pin_hot(moe_layer* layer, int32_t n);
+moe_status moe_layer_cache_stats(moe_layer* layer, int64_t* stats);
+moe_status moe_layer_cache_query(moe_layer* layer, int32_t* slot_of, int32_t* pinned);
+
+/*
  * Inspection of the NVFP4 activation quantiser ("NVIDIA stellt neues GLM-5.2 NVFP4 Modell
  * vor", section "Technische Details und Quantisierungsansatz": E2M1 elements, one E4M3 scale
  * per 16 elements, an fp32 tensor scale). After a forward of T tokens that ran the grouped

@@ -72,6 +72,12 @@ SYMBOLS = {
     "moe_layer_set_wait_limit": (_I, [_P, ctypes.c_int64]),
     "moe_layer_reset_status": (_I, [_P, _P]),
     "moe_layer_get_nvfp4_act": (_I, [_P, _I, _P, _P, _P, _P]),
+    "moe_layer_create_cached": (_I, [ctypes.POINTER(Config), ctypes.POINTER(Weights), _I, _P,
+                                     ctypes.POINTER(_P)]),
+    "moe_layer_prefetch": (_I, [_P, _P, _I, _P]),
+    "moe_layer_cache_pin_hot": (_I, [_P, _I]),
+    "moe_layer_cache_stats": (_I, [_P, _P]),
+    "moe_layer_cache_query": (_I, [_P, _P, _P]),
     "moe_route_noalloc": (_I, [_P, _I, _I, _I, _P, _I, _P, _I, _I, _I, _I, ctypes.c_float,
                                _P, _P, _P, _P, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -151,7 +157,8 @@ class MoeLayer:
     def __init__(self, arrays: dict, *, hidden: int, inter: int, n_experts: int, top_k: int,
                  n_group: int, topk_group: int, rsf: float, weight_format: str,
                  shared_format: str, act_dtype: str, router_dtype: str, max_tokens: int,
-                 expert_top_p: float = 0.0, act_quant: str = "none", stream=None):
+                 expert_top_p: float = 0.0, act_quant: str = "none", cache_slots: int = 0,
+                 stream=None):
         self.cfg = Config(hidden, inter, n_experts, top_k, n_group, topk_group, max_tokens,
                           rsf, _FMT[weight_format], _FMT[shared_format], _DT[act_dtype],
                           _DT[router_dtype], expert_top_p, _ACT[act_quant])
@@ -166,12 +173,17 @@ class MoeLayer:
                     _ptr(a.get("sh_gu_scales")), _ptr(a.get("sh_gu_tscale")), _ptr(sh_d),
                     _ptr(a.get("sh_d_scales")), _ptr(a.get("sh_d_tscale")))
         handle = _P()
-        _check("moe_layer_create", _get_lib().moe_layer_create(ctypes.byref(self.cfg), ctypes.byref(w),
-                                                         _stream(stream), ctypes.byref(handle)))
+        if cache_slots:
+            # routed experts stay in host memory; HBM caches `cache_slots` of them
+            _check("moe_layer_create_cached", _get_lib().moe_layer_create_cached(
+                ctypes.byref(self.cfg), ctypes.byref(w), int(cache_slots), _stream(stream), ctypes.byref(handle)))
+        else:
+            _check("moe_layer_create", _get_lib().moe_layer_create(ctypes.byref(self.cfg), ctypes.byref(w),
+                                                             _stream(stream), ctypes.byref(handle)))
         self._h = handle
 
     @classmethod
-    def from_spec(cls, spec, arrays: dict, max_tokens: int, stream=None) -> "MoeLayer":
+    def from_spec(cls, spec, arrays: dict, max_tokens: int, stream=None, cache_slots: int = 0) -> "MoeLayer":
         """Build from any object with the ``synth.LayerSpec`` attribute names."""
         return cls(arrays, hidden=spec.hidden, inter=spec.inter, n_experts=spec.n_experts,
                    top_k=spec.top_k, n_group=spec.n_group, topk_group=spec.topk_group,
@@ -179,7 +191,7 @@ class MoeLayer:
                    shared_format=spec.shared_format, act_dtype=spec.act_dtype,
                    router_dtype=spec.router_dtype, max_tokens=max_tokens,
                    expert_top_p=getattr(spec, "expert_top_p", 0.0),
-                   act_quant=getattr(spec, "act_quant", "none"), stream=stream)
+                   act_quant=getattr(spec, "act_quant", "none"), cache_slots=cache_slots, stream=stream)
 
     @property
     def handle(self) -> int:
@@ -253,6 +265,29 @@ class MoeLayer:
         _check("moe_layer_get_nvfp4_act", _get_lib().moe_layer_get_nvfp4_act(
             self._h, T, _ptr(r["codes"]), _ptr(r["scales"]), _ptr(r["amax"]), _stream(stream)))
         return r
+
+    # ---------------------------------------------------------- HBM expert cache
+    CACHE_STATS = ("hits", "misses", "prefetched", "prefetch_hits", "bytes_h2d", "evictions")
+
+    def prefetch(self, x, stream=None):
+        """Start loading the experts this layer's router predicts for x (device tensor)."""
+        _check("moe_layer_prefetch", _get_lib().moe_layer_prefetch(self._h, _ptr(x), int(x.shape[0]),
+                                                                   _stream(stream)))
+
+    def cache_pin_hot(self, n: int):
+        _check("moe_layer_cache_pin_hot", _get_lib().moe_layer_cache_pin_hot(self._h, int(n)))
+
+    def cache_stats(self) -> dict:
+        st = (ctypes.c_int64 * 6)()
+        _check("moe_layer_cache_stats", _get_lib().moe_layer_cache_stats(self._h, st))
+        return dict(zip(self.CACHE_STATS, list(st)))
+
+    def cache_query(self) -> tuple[np.ndarray, np.ndarray]:
+        """(slot of each routed expert or -1, pinned flags)."""
+        slot = np.empty(self.n_experts, np.int32)
+        pinned = np.empty(self.n_experts, np.int32)
+        _check("moe_layer_cache_query", _get_lib().moe_layer_cache_query(self._h, _ptr(slot), _ptr(pinned)))
+        return slot, pinned
 
     def close(self):
         if getattr(self, "_h", None) is not None and self._h.value:

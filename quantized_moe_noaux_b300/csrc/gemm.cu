@@ -210,8 +210,10 @@ moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
             ptx::tma_load_2d(S.a[s], &tm_w, ks * kBK, (e - p.e_sub) * p.rows_per_expert + kBM * mt, &S.full_ab[s]);
           }
         } else {
-          const uint8_t* src =
-              p.wpack + ((size_t)(e - p.e_sub) * MT + mt) * (size_t)(NK / kSub) * kGroupBytes;
+          // expert -> packed-store index: through the HBM cache's slot table when the
+          // experts live in host memory
+          const int widx = p.slot_of ? __ldg(p.slot_of + e) : e - p.e_sub;
+          const uint8_t* src = p.wpack + ((size_t)widx * MT + mt) * (size_t)(NK / kSub) * kGroupBytes;
           for (int g = 0; g < NK / kSub; ++g, ++wg) {
             const int s = wg % kWStages;
             if (wg >= kWStages && !wait_bar_t(&S.empty_w[s], ((wg / kWStages) - 1) & 1, w0, p.wait_ns)) {

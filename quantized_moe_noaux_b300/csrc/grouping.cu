@@ -88,7 +88,17 @@ group_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ counts
   }
 }
 
+__global__ void set_slots_kernel(const SlotTable t, int n, int32_t* __restrict__ dst) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = t.slot[i];
+}
+
 }  // namespace
+
+cudaError_t launch_set_slots(const SlotTable& t, int n, int32_t* dst, cudaStream_t s) {
+  if (n <= 0 || n > kMaxSlotTable) return cudaErrorInvalidValue;
+  set_slots_kernel<<<1, 256, 0, s>>>(t, n, dst);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_group(const int32_t* ids, const int32_t* counts, int T, int top_k, int E,
                          int shared_inline, int32_t* offsets, int32_t* entries, int32_t* items,

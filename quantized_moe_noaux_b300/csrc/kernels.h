@@ -147,6 +147,7 @@ struct GemmParams {
   unsigned long long wait_ns; // time limit of every wait on another warp's or unit's work
   unsigned long long* trace;  // optional per-CTA profiling trace (64 slots per CTA), or NULL
   int trace_base;             // first slot of this launch's 11
+  const int32_t* slot_of;     // packed-store slot of each expert (HBM expert cache), or NULL
   // block-scaled FP4 kernel only
   const uint8_t* wsf;         // weight scales in MMA order (fp4_pack_kernel)
   const uint8_t* asf;         // activation E4M3 scales [rows, K / 16] of the sorted rows
@@ -206,6 +207,15 @@ cudaError_t launch_quant_gather_fp4(const void* x, int act_dtype, int H, int T, 
 cudaError_t launch_quant_h_fp4(const float* h, size_t n, const unsigned int* amax_bits, uint8_t* codes, uint8_t* sf,
                                cudaStream_t s);
 cudaError_t launch_gemm_fp4(int epi, const Fp4Maps& m, const GemmParams& p, int max_tiles, int n_sm, cudaStream_t s);
+
+// ------------------------------------------------------------- HBM expert cache
+// Slot table of the cache (expert -> slot of the packed store), written by a kernel that
+// takes it by value, so the host's table may change as soon as the launch is enqueued.
+constexpr int kMaxSlotTable = 1025;   // E <= 1024 routed experts + the shared expert
+struct SlotTable {
+  int32_t slot[kMaxSlotTable];
+};
+cudaError_t launch_set_slots(const SlotTable& t, int n, int32_t* dst, cudaStream_t s);
 
 // out[T, H] (act dtype) = out_acc
 cudaError_t launch_finalize(const float* out_acc, void* out, int act_dtype, size_t n,

@@ -5,6 +5,7 @@
 #include <new>
 #include <vector>
 
+#include "expert_cache.h"
 #include "kernels.h"
 
 using namespace moe;
@@ -82,6 +83,22 @@ struct moe_layer {
   uint8_t* xts = nullptr;
   Fp4Maps f4_up{}, f4_dn{};
   std::vector<void*> allocs;
+  // HBM cache of host-resident experts (moe_layer_create_cached): the routed experts' packed
+  // gate/up and down stores in pinned host memory, the HBM slots in gpack_up / gpack_down
+  // (slot `slots` holds the shared expert), the device slot table, the read-back counts
+  ExpertCache* cache = nullptr;
+  std::vector<void*> host_allocs;
+  uint8_t* host_up = nullptr;
+  uint8_t* host_dn = nullptr;
+  int32_t* d_slot = nullptr;
+  int32_t* h_counts = nullptr;
+  // routing workspace of moe_layer_prefetch (its own, so it may run beside a forward)
+  float* logits_p = nullptr;
+  int32_t* ids_p = nullptr;
+  float* weights_p = nullptr;
+  int32_t* counts_p = nullptr;
+  int32_t* h_counts_p = nullptr;
+  cudaEvent_t ev_x = nullptr;
   // measurement
   std::vector<cudaEvent_t> events;   // kStageEvents per recorded forward
   int timing_cap = 0;
@@ -161,8 +178,25 @@ moe_status dev_alloc_t(moe_layer* L, T** p, size_t bytes) {
 }
 
 void free_all(moe_layer* L) {
+  delete L->cache;   // waits for its copies
+  L->cache = nullptr;
+  if (L->ev_x) cudaEventDestroy(L->ev_x);
+  L->ev_x = nullptr;
   for (void* p : L->allocs) cudaFree(p);
   L->allocs.clear();
+  for (void* p : L->host_allocs) cudaFreeHost(p);
+  L->host_allocs.clear();
+}
+
+moe_status host_alloc(moe_layer* L, void** p, size_t bytes) {
+  *p = nullptr;
+  if (cudaHostAlloc(p, bytes, cudaHostAllocDefault) != cudaSuccess) {
+    cudaGetLastError();
+    *p = nullptr;
+    return MOE_ERR_OOM;
+  }
+  L->host_allocs.push_back(*p);
+  return MOE_OK;
 }
 
 // Upload one expert matrix family (codes, scales, tensor scales) of n experts into slots
@@ -203,7 +237,67 @@ moe_status alloc_family(moe_layer* L, ExpertWeights& w, int fmt, int n, int H, i
   return MOE_OK;
 }
 
-moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt, cudaStream_t s) {
+// Store of a cached layer: each routed expert is uploaded row-major into a one-expert
+// staging area, packed there into the grouped GEMM's layout and copied to pinned host
+// memory; the shared expert is packed straight into its HBM slot (slot `slots`). Then the
+// cache, the slot table, the read-back buffers and the prefetch workspace.
+moe_status create_cache_store(moe_layer* L, const moe_config* c, const moe_weights* wt, int slots, cudaStream_t s) {
+  moe_status st;
+  const int H = c->hidden, I = c->inter, E = c->n_experts, k = c->top_k, Tm = c->max_tokens;
+  const int fmt = c->weight_format;
+  const size_t up_b = gemm_pack_bytes(2 * I, H, 1), dn_b = gemm_pack_bytes(H, I, 1);
+  const size_t gcb = (size_t)2 * I * row_code_bytes(fmt, H), gsb = (size_t)2 * I * row_scale_bytes(fmt, H);
+  const size_t dcb = (size_t)H * row_code_bytes(fmt, I), dsb = (size_t)H * row_scale_bytes(fmt, I);
+  ExpertWeights stage{};
+  uint8_t *pk_up, *pk_dn;
+  void *hu, *hd;
+  if ((st = alloc_family(L, stage, fmt, 1, H, I)) || (st = dev_alloc_t(L, &pk_up, up_b)) ||
+      (st = dev_alloc_t(L, &pk_dn, dn_b)) || (st = dev_alloc_t(L, &L->gpack_up, (size_t)(slots + 1) * up_b)) ||
+      (st = dev_alloc_t(L, &L->gpack_down, (size_t)(slots + 1) * dn_b)) ||
+      (st = host_alloc(L, &hu, (size_t)E * up_b)) || (st = host_alloc(L, &hd, (size_t)E * dn_b)))
+    return st;
+  L->host_up = static_cast<uint8_t*>(hu);
+  L->host_dn = static_cast<uint8_t*>(hd);
+  uint8_t* sgc = const_cast<uint8_t*>(stage.gu_codes);
+  uint8_t* sgs = const_cast<uint8_t*>(stage.gu_scales);
+  uint8_t* sdc = const_cast<uint8_t*>(stage.d_codes);
+  uint8_t* sds = const_cast<uint8_t*>(stage.d_scales);
+  for (int e = 0; e <= E; ++e) {
+    const bool sh = e == E;
+    const uint8_t* gc = sh ? static_cast<const uint8_t*>(wt->sh_gu) : wt->gu_codes + (size_t)e * gcb;
+    const uint8_t* gs = sh ? static_cast<const uint8_t*>(wt->sh_gu_scales)
+                           : static_cast<const uint8_t*>(wt->gu_scales) + (size_t)e * gsb;
+    const uint8_t* dc = sh ? static_cast<const uint8_t*>(wt->sh_d) : wt->d_codes + (size_t)e * dcb;
+    const uint8_t* ds = sh ? static_cast<const uint8_t*>(wt->sh_d_scales)
+                           : static_cast<const uint8_t*>(wt->d_scales) + (size_t)e * dsb;
+    if ((st = upload_family(gc, gs, nullptr, fmt, 2 * I, H, 0, 1, sgc, sgs, nullptr, s)) ||
+        (st = upload_family(dc, ds, nullptr, fmt, H, I, 0, 1, sdc, sds, nullptr, s)))
+      return st;
+    uint8_t* du = sh ? L->gpack_up + (size_t)slots * up_b : pk_up;
+    uint8_t* dd = sh ? L->gpack_down + (size_t)slots * dn_b : pk_dn;
+    if (launch_gemm_pack(sgc, sgs, H, 1, 2 * I, I, true, du, s) || launch_gemm_pack(sdc, sds, I, 1, H, I, false, dd, s))
+      return MOE_ERR_CUDA;
+    if (!sh && (cudaMemcpyAsync(L->host_up + (size_t)e * up_b, pk_up, up_b, cudaMemcpyDeviceToHost, s) ||
+                cudaMemcpyAsync(L->host_dn + (size_t)e * dn_b, pk_dn, dn_b, cudaMemcpyDeviceToHost, s)))
+      return MOE_ERR_CUDA;
+  }
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  void *hc, *hcp;
+  if ((st = dev_alloc_t(L, &L->d_slot, (size_t)(E + 1) * 4)) || (st = host_alloc(L, &hc, (size_t)(E + 1) * 4)) ||
+      (st = host_alloc(L, &hcp, (size_t)(E + 1) * 4)) || (st = dev_alloc_t(L, &L->logits_p, (size_t)Tm * E * 4)) ||
+      (st = dev_alloc_t(L, &L->ids_p, (size_t)Tm * k * 4)) || (st = dev_alloc_t(L, &L->weights_p, (size_t)Tm * k * 4)) ||
+      (st = dev_alloc_t(L, &L->counts_p, (size_t)(E + 1) * 4)))
+    return st;
+  L->h_counts = static_cast<int32_t*>(hc);
+  L->h_counts_p = static_cast<int32_t*>(hcp);
+  if (cudaEventCreateWithFlags(&L->ev_x, cudaEventDisableTiming) != cudaSuccess) return MOE_ERR_CUDA;
+  L->cache = new (std::nothrow) ExpertCache();
+  if (!L->cache) return MOE_ERR_OOM;
+  return L->cache->init(E, slots, up_b, dn_b, L->host_up, L->host_dn, L->gpack_up, L->gpack_down);
+}
+
+moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt, cudaStream_t s,
+                       int cache_slots = 0) {
   moe_status st;
   const int H = c->hidden, I = c->inter, E = c->n_experts, k = c->top_k, Tm = c->max_tokens;
   if (!wt->router_w || !wt->bias || !wt->gu_codes || !wt->d_codes || !wt->sh_gu || !wt->sh_d)
@@ -219,9 +313,15 @@ moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt,
       cudaMemcpyAsync(L->bias, wt->bias, E * sizeof(float), cudaMemcpyDefault, s))
     return MOE_ERR_CUDA;
 
-  if ((st = alloc_family(L, L->w, c->weight_format, n_store, H, I))) return st;
+  if (cache_slots > 0) {
+    if ((st = create_cache_store(L, c, wt, cache_slots, s))) return st;
+  } else if ((st = alloc_family(L, L->w, c->weight_format, n_store, H, I))) {
+    return st;
+  }
   ExpertWeights& w = L->w;
-  if ((st = upload_family(wt->gu_codes, wt->gu_scales, wt->gu_tscale, c->weight_format, 2 * I, H, 0, E,
+  if (cache_slots > 0) {
+    // routed and shared experts live in the cache store only
+  } else if ((st = upload_family(wt->gu_codes, wt->gu_scales, wt->gu_tscale, c->weight_format, 2 * I, H, 0, E,
                           const_cast<uint8_t*>(w.gu_codes), const_cast<uint8_t*>(w.gu_scales),
                           const_cast<float*>(w.gu_tscale), s)) ||
       (st = upload_family(wt->d_codes, wt->d_scales, wt->d_tscale, c->weight_format, H, I, 0, E,
@@ -230,17 +330,20 @@ moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt,
     return st;
   ExpertWeights* sw = &L->w;
   int slot = E;
-  if (!L->shared_inline) {
+  if (cache_slots > 0) {
+    // shared expert packed into its HBM slot by create_cache_store
+  } else if (!L->shared_inline) {
     if ((st = alloc_family(L, L->ws, c->shared_format, 1, H, I))) return st;
     sw = &L->ws;
     slot = 0;
   }
-  if ((st = upload_family(wt->sh_gu, wt->sh_gu_scales, wt->sh_gu_tscale, c->shared_format, 2 * I, H, slot,
-                          1, const_cast<uint8_t*>(sw->gu_codes), const_cast<uint8_t*>(sw->gu_scales),
-                          const_cast<float*>(sw->gu_tscale), s)) ||
-      (st = upload_family(wt->sh_d, wt->sh_d_scales, wt->sh_d_tscale, c->shared_format, H, I, slot, 1,
-                          const_cast<uint8_t*>(sw->d_codes), const_cast<uint8_t*>(sw->d_scales),
-                          const_cast<float*>(sw->d_tscale), s)))
+  if (cache_slots == 0 &&
+      ((st = upload_family(wt->sh_gu, wt->sh_gu_scales, wt->sh_gu_tscale, c->shared_format, 2 * I, H, slot,
+                           1, const_cast<uint8_t*>(sw->gu_codes), const_cast<uint8_t*>(sw->gu_scales),
+                           const_cast<float*>(sw->gu_tscale), s)) ||
+       (st = upload_family(wt->sh_d, wt->sh_d_scales, wt->sh_d_tscale, c->shared_format, H, I, slot, 1,
+                           const_cast<uint8_t*>(sw->d_codes), const_cast<uint8_t*>(sw->d_scales),
+                           const_cast<float*>(sw->d_tscale), s))))
     return st;
 
   const size_t ab = act_bytes(c->act_dtype);
@@ -326,7 +429,7 @@ moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt,
              make_tmap_2d(&L->f4_dn.act[b], L->hc, 1, I / 2, rk, 128, box, true);
       }
       if (!ok) return MOE_ERR_CUDA;
-    } else {
+    } else if (cache_slots == 0) {
       if ((st = dev_alloc_t(L, &L->gpack_up, gemm_pack_bytes(2 * I, H, n_store))) ||
           (st = dev_alloc_t(L, &L->gpack_down, gemm_pack_bytes(H, I, n_store))))
         return st;
@@ -355,7 +458,7 @@ moe_status create_impl(moe_layer* L, const moe_config* c, const moe_weights* wt,
   // tokens
   {
     const int Td = Tm < 8 ? Tm : 8;
-    L->decode_ok = L->gemm_ok && c->weight_format == MOE_W_INT4_G32 && L->shared_inline &&
+    L->decode_ok = L->gemm_ok && !L->cache && c->weight_format == MOE_W_INT4_G32 && L->shared_inline &&
                    decode_supported(H, I, E, k, 1) && decode_kernels_init() == cudaSuccess;
     int occ = 0;
     if (L->decode_ok && (decode_occupancy(&occ) != cudaSuccess || occ < 1)) L->decode_ok = false;
@@ -421,6 +524,18 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
   const int routed_max = gemm_max_items(T, k, E, true, inl, chunk);
   const int shared_max = gemm_max_items(T, k, E, false, true, chunk);
   MOE_LAUNCH(launch_gemm_items(L->offsets, E, T, k, chunk, L->gitems, L->g_nitems, s));
+  if (L->cache) {
+    // host-resident experts: read the routed experts back, load the missing ones into HBM
+    // slots (copy stream), then publish the slot table on this stream
+    MOE_CK(cudaMemcpyAsync(L->h_counts, L->counts, (size_t)E * 4, cudaMemcpyDeviceToHost, s));
+    MOE_CK(cudaStreamSynchronize(s));
+    moe_status cs = L->cache->ensure(L->h_counts, false);
+    if (cs || (cs = L->cache->wait_copies(s))) return cs;
+    SlotTable t;
+    for (int e = 0; e < E; ++e) t.slot[e] = L->cache->slot_of(e);
+    t.slot[E] = L->cache->slots();
+    MOE_LAUNCH(launch_set_slots(t, E + 1, L->d_slot, s));
+  }
   if (nvfp4) MOE_LAUNCH(launch_amax(x, c.act_dtype, (size_t)T * H, L->amax, s));
   if (f4) {
     // routed rows as NVFP4 codes + scales; the bf16 shared expert reads fp16 x
@@ -447,6 +562,7 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
   p.weights = L->weights;
   p.status = L->status;
   p.wait_ns = L->wait_ns;
+  p.slot_of = L->cache ? L->d_slot : nullptr;
   p.trace = L->trace;
   p.trace_base = 16;
   GemmParams ps = p;   // separately stored fp16 shared expert
@@ -492,6 +608,10 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
     MOE_LAUNCH(launch_gemm(c.weight_format, 1, L->maps_down, p, routed_max * p.mtiles, L->n_sm, s));
   }
   if (!inl) MOE_LAUNCH(launch_gemm(kWF16, 1, L->maps_sh_down, ps, shared_max * ps.mtiles, L->n_sm, s));
+  if (L->cache) {
+    moe_status cs = L->cache->note_compute(s);   // the slots' last readers
+    if (cs) return cs;
+  }
   MOE_CK(m.mark(6));
   MOE_LAUNCH(launch_combine(L->ys, L->inv, L->ids, L->weights, T, k, H, out, c.act_dtype, s));
   MOE_CK(m.mark(7));
@@ -505,6 +625,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
   StageMarks m;
   m.s = s;
   if (L->timing_used < L->timing_cap) m.ev = &L->events[(size_t)kStageEvents * L->timing_used++];
+  if (L->cache && (L->path == MOE_PATH_GEMV || L->path == MOE_PATH_GENERIC)) return MOE_ERR_UNSUPPORTED;
   const bool decode = L->decode_ok && T <= L->decode_tmax && (long)T * k <= 64 &&
                      (L->path == MOE_PATH_AUTO || L->path == MOE_PATH_GEMV);
   if (L->path == MOE_PATH_GEMV && !decode) return MOE_ERR_UNSUPPORTED;
@@ -755,6 +876,86 @@ moe_status moe_layer_get_nvfp4_act(moe_layer* L, int32_t T, uint8_t* codes, uint
       cudaMemcpyAsync(amax, L->amax, sizeof(float), cudaMemcpyDeviceToHost, s))
     return MOE_ERR_CUDA;
   return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_layer_create_cached(const moe_config* cfg, const moe_weights* w, int32_t slots, void* stream,
+                                   moe_layer** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || !w) return MOE_ERR_INVALID_ARG;
+  moe_status st = validate_config(cfg);
+  if (st) return st;
+  const int need = (long)cfg->max_tokens * cfg->top_k < cfg->n_experts ? cfg->max_tokens * cfg->top_k : cfg->n_experts;
+  if (slots < need || slots > cfg->n_experts) return MOE_ERR_INVALID_ARG;
+  if (cfg->weight_format != MOE_W_INT4_G32 || cfg->shared_format != MOE_W_INT4_G32 ||
+      cfg->act_quant != MOE_ACT_NONE || !gemm_supported(cfg->hidden, cfg->inter) || cfg->n_experts + 1 > kMaxSlotTable)
+    return MOE_ERR_UNSUPPORTED;
+  moe_layer* L = new (std::nothrow) moe_layer();
+  if (!L) return MOE_ERR_OOM;
+  L->cfg = *cfg;
+  if (cudaGetDevice(&L->device) != cudaSuccess) {
+    delete L;
+    return MOE_ERR_CUDA;
+  }
+  st = create_impl(L, cfg, w, static_cast<cudaStream_t>(stream), slots);
+  if (!st && !L->gemm_ok) st = MOE_ERR_UNSUPPORTED;
+  if (st) {
+    cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    cudaGetLastError();
+    free_all(L);
+    delete L;
+    return st;
+  }
+  L->path = MOE_PATH_GROUPED;
+  *out = L;
+  return MOE_OK;
+}
+
+moe_status moe_layer_prefetch(moe_layer* L, const void* x, int32_t T, void* stream) {
+  if (!L || T < 0 || T > L->cfg.max_tokens || (T > 0 && !x)) return MOE_ERR_INVALID_ARG;
+  if (!L->cache) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  DeviceGuard g(L->device);
+  const moe_config& c = L->cfg;
+  const int E = c.n_experts, H = c.hidden;
+  cudaStream_t cs = L->cache->copy_stream();
+  // predict on the copy stream, after x is ready on the caller's stream
+  if (cudaEventRecord(L->ev_x, static_cast<cudaStream_t>(stream)) || cudaStreamWaitEvent(cs, L->ev_x, 0) ||
+      cudaMemsetAsync(L->counts_p, 0, (size_t)(E + 1) * 4, cs) ||
+      launch_router_logits(x, c.act_dtype, L->router_w, c.router_dtype, L->logits_p, T, E, H, cs) ||
+      launch_select(L->logits_p, L->bias, T, E, c.n_group, c.topk_group, c.top_k, c.routed_scaling_factor,
+                    c.expert_top_p, L->ids_p, L->weights_p, L->counts_p, L->status, cs) ||
+      cudaMemcpyAsync(L->h_counts_p, L->counts_p, (size_t)E * 4, cudaMemcpyDeviceToHost, cs) ||
+      cudaStreamSynchronize(cs))
+    return MOE_ERR_CUDA;
+  L->launches += 2;
+  return L->cache->ensure(L->h_counts_p, true);
+}
+
+moe_status moe_layer_cache_pin_hot(moe_layer* L, int32_t n) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  if (!L->cache) return MOE_ERR_UNSUPPORTED;
+  DeviceGuard g(L->device);
+  const moe_config& c = L->cfg;
+  const int need = (long)c.max_tokens * c.top_k < c.n_experts ? c.max_tokens * c.top_k : c.n_experts;
+  return L->cache->pin_hot(n, need);
+}
+
+moe_status moe_layer_cache_stats(moe_layer* L, int64_t* stats) {
+  if (!L || !stats) return MOE_ERR_INVALID_ARG;
+  if (!L->cache) return MOE_ERR_UNSUPPORTED;
+  for (int i = 0; i < ExpertCache::kNumStats; ++i) stats[i] = L->cache->stats()[i];
+  return MOE_OK;
+}
+
+moe_status moe_layer_cache_query(moe_layer* L, int32_t* slot_of, int32_t* pinned) {
+  if (!L || !slot_of || !pinned) return MOE_ERR_INVALID_ARG;
+  if (!L->cache) return MOE_ERR_UNSUPPORTED;
+  for (int e = 0; e < L->cfg.n_experts; ++e) {
+    slot_of[e] = L->cache->slot_of(e);
+    pinned[e] = L->cache->pinned(e) ? 1 : 0;
+  }
+  return MOE_OK;
 }
 
 moe_status moe_layer_reset_status(moe_layer* L, void* stream) {

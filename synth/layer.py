@@ -150,6 +150,8 @@ WORKLOADS = {
     # independently (the pages give no statistics of how their routing overlaps)
     "glm52_mtp_verify_t3": Workload("glm52_mtp_verify_t3", LAYERS["glm52"], tokens=3, steps=1000),
     "glm52_mtp_verify_t5": Workload("glm52_mtp_verify_t5", LAYERS["glm52"], tokens=5, steps=1000),
+    # host-resident experts with an HBM cache per layer: decode through a stack of layers
+    "glm52_hostcache_t1": Workload("glm52_hostcache_t1", LAYERS["glm52"], tokens=1, steps=48),
     # per-format GEMV comparison, T = 1 (E = 64 stand-in of the GLM layer)
     "glm52_e64_int4_g32_t1": Workload("glm52_e64_int4_g32_t1", LAYERS["glm52_e64_int4_g32"], tokens=1, steps=200),
     "glm52_e64_int8_row_t1": Workload("glm52_e64_int8_row_t1", LAYERS["glm52_e64_int8_row"], tokens=1, steps=200),

@@ -77,3 +77,19 @@ def test_create_rejects_bad_configs_before_touching_the_device(over, code):
     rc = moe.lib.moe_layer_create(ctypes.byref(cfg), ctypes.byref(w), None, ctypes.byref(out))
     assert rc == code, (over, rc)
     assert out.value is None
+
+
+@pytest.mark.parametrize("over,slots,code", [
+    (dict(), 63, 1),                                             # fewer slots than one forward needs (64 * 8 > 256 -> 256)
+    (dict(max_tokens=4), 31, 1),                                 # min(E, 4 * 8) = 32
+    (dict(max_tokens=4), 257, 1),                                # more slots than experts
+    (dict(max_tokens=4, weight_format=moe.W_NVFP4, shared_format=moe.W_NVFP4), 64, 2),   # int4_g32 only
+    (dict(max_tokens=4, act_quant=1), 64, 2),
+])
+def test_create_cached_rejects_before_touching_the_device(over, slots, code):
+    cfg = _cfg(**over)
+    w = moe.Weights()
+    out = ctypes.c_void_p(1)
+    rc = moe.lib.moe_layer_create_cached(ctypes.byref(cfg), ctypes.byref(w), slots, None, ctypes.byref(out))
+    assert rc == code, (over, slots, rc)
+    assert out.value is None
