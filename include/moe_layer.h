@@ -249,6 +249,14 @@ moe_status moe_layer_launch_count(moe_layer* layer, int64_t* count);
  */
 moe_status moe_layer_set_wait_limit(moe_layer* layer, int64_t ns);
 
+/*
+ * Test-only: identity = 1 makes every path compute h = gate * up instead of SiLU(gate) * up
+ * for later forwards (0 restores SiLU). It exists so that inputs chosen for exact
+ * arithmetic (small integers, power-of-two scales) give outputs that an exact evaluation of
+ * the same formula reproduces bit for bit. Anything but 0 or 1 is MOE_ERR_INVALID_ARG.
+ */
+moe_status moe_layer_set_test_activation(moe_layer* layer, int32_t identity);
+
 /* Clear the sticky device status word (enqueued on `stream`). */
 moe_status moe_layer_reset_status(moe_layer* layer, void* stream);
 

@@ -71,6 +71,7 @@ SYMBOLS = {
     "moe_layer_set_trace": (_I, [_P, _P, _I]),
     "moe_layer_set_wait_limit": (_I, [_P, ctypes.c_int64]),
     "moe_layer_reset_status": (_I, [_P, _P]),
+    "moe_layer_set_test_activation": (_I, [_P, _I]),
     "moe_layer_get_nvfp4_act": (_I, [_P, _I, _P, _P, _P, _P]),
     "moe_layer_create_cached": (_I, [ctypes.POINTER(Config), ctypes.POINTER(Weights), _I, _P,
                                      ctypes.POINTER(_P)]),
@@ -251,6 +252,10 @@ class MoeLayer:
     def set_wait_limit(self, ns: int):
         """Time limit (ns) of the kernels' waits on other CTAs (failure-handling hook)."""
         _check("moe_layer_set_wait_limit", _get_lib().moe_layer_set_wait_limit(self._h, int(ns)))
+
+    def set_test_activation(self, identity: bool):
+        """Test-only: h = gate * up instead of SiLU(gate) * up (exact-arithmetic cases)."""
+        _check("moe_layer_set_test_activation", _get_lib().moe_layer_set_test_activation(self._h, int(identity)))
 
     def reset_status(self, stream=None):
         """Clear the sticky device status word."""

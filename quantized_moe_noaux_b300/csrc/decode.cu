@@ -130,6 +130,7 @@ struct DecodeArgs {
   int H, I, E, top_k, n_group, topk_group;
   float rsf;
   float top_p;                 // adaptive expert top-p (0 < top_p < 1), else every slot kept
+  int identity_act;            // test-only: h = gate * up (no SiLU)
   const uint8_t* pack_up;      // [E+1][I/64 tiles][H/256 groups][18432]
   const uint8_t* pack_dn;      // [E+1][H/128 tiles][I/256 groups][18432]
   float* logits;               // [T, E]
@@ -1188,7 +1189,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(DecodeArgs a
                     gs += gv[sp];
                     us += uv[sp];
                   }
-                a.h16[((size_t)u.slot * T + c) * I + 64 * u.tile + 16 * q + lane] = __float2half_rn(siluf_acc(gs) * us);
+                a.h16[((size_t)u.slot * T + c) * I + 64 * u.tile + 16 * q + lane] =
+                    __float2half_rn((a.identity_act ? gs : siluf_acc(gs)) * us);
               }
             }
             __threadfence();
@@ -1418,6 +1420,7 @@ cudaError_t launch_decode_fused(const DecodeLaunch& d, int act_dtype, int router
   a.topk_group = d.topk_group;
   a.rsf = d.rsf;
   a.top_p = d.top_p;
+  a.identity_act = d.identity_act;
   a.pack_up = d.pack_up;
   a.pack_dn = d.pack_dn;
   a.logits = d.logits;

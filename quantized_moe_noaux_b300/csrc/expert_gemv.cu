@@ -120,7 +120,7 @@ expert_up_kernel(ExpertGemvArgs a) {
     }
     if (lane == 0) {
       for (int i = 0; i < c.ntok; ++i) {
-        const float hv = siluf_acc(ag[i]) * au[i];
+        const float hv = (a.identity_act ? ag[i] : siluf_acc(ag[i])) * au[i];
         a.h[(size_t)c.pair[i] * I + r] = hv;
         if (a.h_amax && c.routed) atomicMax(a.h_amax, __float_as_uint(fabsf(hv)));
       }

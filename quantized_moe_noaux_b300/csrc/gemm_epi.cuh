@@ -41,7 +41,7 @@ __device__ __forceinline__ void gemm_tile_epilogue(uint32_t lane_addr, int N, in
         const float u = (upl ? v[16 + j] : recv) * sc_out;
         const int c = c0 + j + (upl ? 16 : 0);
         if (c < n) {
-          const float hv = siluf_acc(g) * u;
+          const float hv = (p.identity_act ? g : siluf_acc(g)) * u;
           const size_t idx = (size_t)(row0 + c) * p.I + hcol;
           if (H32) {
             p.h32[idx] = hv;

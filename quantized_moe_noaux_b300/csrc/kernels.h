@@ -53,6 +53,7 @@ struct ExpertGemvArgs {
   const float* weights;     // [T, k]
   float* out_acc;           // [T, H] fp32
   int max_items;
+  int identity_act;         // test-only: h = gate * up (no SiLU)
 };
 
 // Largest dynamic shared memory a generic expert CTA may use (x or h rows of a token chunk).
@@ -92,6 +93,7 @@ struct DecodeLaunch {
   int H, I, E, top_k, n_group, topk_group;
   float rsf;
   float top_p;                 // adaptive expert top-p (0 < top_p < 1), else off
+  int identity_act;            // test-only: h = gate * up (no SiLU)
   const uint8_t* pack_up;      // grouped-GEMM packed gate/up store
   const uint8_t* pack_dn;      // grouped-GEMM packed down store
   float* logits;
@@ -148,6 +150,7 @@ struct GemmParams {
   unsigned long long* trace;  // optional per-CTA profiling trace (64 slots per CTA), or NULL
   int trace_base;             // first slot of this launch's 11
   const int32_t* slot_of;     // packed-store slot of each expert (HBM expert cache), or NULL
+  int identity_act;           // test-only: h = gate * up (no SiLU)
   // block-scaled FP4 kernel only
   const uint8_t* wsf;         // weight scales in MMA order (fp4_pack_kernel)
   const uint8_t* asf;         // activation E4M3 scales [rows, K / 16] of the sorted rows

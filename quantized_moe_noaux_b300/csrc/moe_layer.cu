@@ -106,6 +106,7 @@ struct moe_layer {
   int64_t launches = 0;
   unsigned long long* trace = nullptr;   // decode-kernel phase timestamps (profiling)
   unsigned long long wait_ns = 2000000000ull;   // limit of the kernels' waits on other CTAs
+  int identity_act = 0;                          // test-only: h = gate * up (no SiLU)
 };
 
 static constexpr int kStageEvents = 8;
@@ -563,6 +564,7 @@ moe_status forward_gemm(moe_layer* L, const void* x, int T, void* out, cudaStrea
   p.status = L->status;
   p.wait_ns = L->wait_ns;
   p.slot_of = L->cache ? L->d_slot : nullptr;
+  p.identity_act = L->identity_act;
   p.trace = L->trace;
   p.trace_base = 16;
   GemmParams ps = p;   // separately stored fp16 shared expert
@@ -637,7 +639,8 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
     MOE_CK(m.mark(1));
     MOE_CK(m.mark(2));
     DecodeLaunch d{x, T, L->router_w, L->bias, H, I, E, k, c.n_group, c.topk_group,
-                   c.routed_scaling_factor, c.expert_top_p, L->gpack_up, L->gpack_down, L->logits, L->ids,
+                   c.routed_scaling_factor, c.expert_top_p, L->identity_act, L->gpack_up, L->gpack_down,
+                   L->logits, L->ids,
                    L->weights, L->offsets, L->entries, L->dec_h16, L->dec_gu_part, L->dec_y_part,
                    out, L->dsync, L->status, L->wait_ns, L->trace};
     MOE_LAUNCH(launch_decode_fused(d, c.act_dtype, c.router_dtype, L->n_sm, s));
@@ -694,6 +697,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
   a.weights = L->weights;
   a.out_acc = L->out_acc;
   a.max_items = max_items_for(c, T);
+  a.identity_act = L->identity_act;
   ExpertGemvArgs sh = a;
   if (!L->shared_inline) {
     sh.w = L->ws;
@@ -955,6 +959,12 @@ moe_status moe_layer_cache_query(moe_layer* L, int32_t* slot_of, int32_t* pinned
     slot_of[e] = L->cache->slot_of(e);
     pinned[e] = L->cache->pinned(e) ? 1 : 0;
   }
+  return MOE_OK;
+}
+
+moe_status moe_layer_set_test_activation(moe_layer* L, int32_t identity) {
+  if (!L || (identity != 0 && identity != 1)) return MOE_ERR_INVALID_ARG;
+  L->identity_act = identity;
   return MOE_OK;
 }
 
