@@ -514,7 +514,8 @@ def run_ours(args):
         roofline = {"bound": "tensor" if tensor else "hbm", "kernel": kernel,
                     "achieved": ach_t if tensor else ach_b, "peak": peak_t if tensor else peak_bw,
                     "peak_kind": t_kind if tensor else peak_kind, "unit": "TFLOP/s" if tensor else "GB/s",
-                    "frac": ach_t / peak_t if tensor else ach_b / peak_bw, "traffic": None,
+                    "frac": ach_t / peak_t if tensor else ach_b / peak_bw,
+                    "traffic": recorded_traffic("moe_gemm_fp4_kernel", wl.name) if "fp4" in kernel else None,
                     "frac_hbm": ach_b / peak_bw, "frac_tensor": ach_t / peak_t,
                     "achieved_gbs": ach_b, "achieved_tflops": ach_t, "hbm_peak": peak_bw,
                     "tensor_peak": peak_t, "tensor_peak_kind": t_kind,

@@ -130,6 +130,9 @@ LAYERS = {
                               shared_format="int2_row"),
     "small_int4_row_q8": replace(_SMALL, name="small_h2048_e32_int4row", weight_format="int4_row",
                                  shared_format="int4_row", act_quant="q8_0"),
+    # GLM-shaped NVFP4 with 64 routed experts: a 1.4 GB profiling stand-in of the NVFP4 layer
+    "glm52_e64_nvfp4": replace(_GLM, name="glm52_h6144_e64_nvfp4", n_experts=64, weight_format="nvfp4",
+                               router_dtype="bf16", shared_format="bf16"),
     # GLM expert shapes with 64 routed experts, one per weight format (per-format GEMV
     # comparison at T = 1)
     "glm52_e64_int4_g32": replace(_GLM, name="glm52_h6144_e64_int4g32", n_experts=64),
