@@ -250,6 +250,28 @@ moe_status moe_layer_launch_count(moe_layer* layer, int64_t* count);
 moe_status moe_layer_set_wait_limit(moe_layer* layer, int64_t ns);
 
 /*
+ * Debug checks (a sanitizer substitute): with on = 1 every later forward checks its routing
+ * on the device after the grouping: ids in [-1, E), offsets starting at 0, never decreasing
+ * and ending at the number of routed slots (at most T * top_k), each entry of expert e's
+ * range naming a slot whose id is e, tokens strictly ascending in each range. A violation
+ * sets MOE_ERR_DEVICE_CHECK in the status word (moe_layer_status); nothing traps.
+ * moe_check_routing runs the same checks on caller DEVICE arrays ids [T * top_k], offsets
+ * [n_experts + 1], entries [T * top_k] and raises MOE_ERR_DEVICE_CHECK in the caller's
+ * device int *status (enqueued on `stream`); the checks read only inside those arrays.
+ */
+moe_status moe_layer_set_debug_checks(moe_layer* layer, int32_t on);
+moe_status moe_check_routing(const int32_t* ids, const int32_t* offsets, const int32_t* entries,
+                             int32_t T, int32_t top_k, int32_t n_experts, int32_t* status,
+                             void* stream);
+
+/*
+ * Test hook: after this call the nth device or host allocation made by the library fails
+ * with MOE_ERR_OOM (nth = 0 switches it off; counting restarts at each call). Creation
+ * then returns MOE_ERR_OOM and releases everything it had allocated.
+ */
+moe_status moe_test_fail_allocation(int32_t nth);
+
+/*
  * Test-only: identity = 1 makes every path compute h = gate * up instead of SiLU(gate) * up
  * for later forwards (0 restores SiLU). It exists so that inputs chosen for exact
  * arithmetic (small integers, power-of-two scales) give outputs that an exact evaluation of

@@ -72,6 +72,9 @@ SYMBOLS = {
     "moe_layer_set_wait_limit": (_I, [_P, ctypes.c_int64]),
     "moe_layer_reset_status": (_I, [_P, _P]),
     "moe_layer_set_test_activation": (_I, [_P, _I]),
+    "moe_layer_set_debug_checks": (_I, [_P, _I]),
+    "moe_check_routing": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    "moe_test_fail_allocation": (_I, [_I]),
     "moe_layer_get_nvfp4_act": (_I, [_P, _I, _P, _P, _P, _P]),
     "moe_layer_create_cached": (_I, [ctypes.POINTER(Config), ctypes.POINTER(Weights), _I, _P,
                                      ctypes.POINTER(_P)]),
@@ -252,6 +255,10 @@ class MoeLayer:
     def set_wait_limit(self, ns: int):
         """Time limit (ns) of the kernels' waits on other CTAs (failure-handling hook)."""
         _check("moe_layer_set_wait_limit", _get_lib().moe_layer_set_wait_limit(self._h, int(ns)))
+
+    def set_debug_checks(self, on: bool):
+        """Check each forward's routing on the device (MOE_ERR_DEVICE_CHECK on a violation)."""
+        _check("moe_layer_set_debug_checks", _get_lib().moe_layer_set_debug_checks(self._h, int(on)))
 
     def set_test_activation(self, identity: bool):
         """Test-only: h = gate * up instead of SiLU(gate) * up (exact-arithmetic cases)."""

@@ -88,11 +88,66 @@ group_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ counts
   }
 }
 
+// Debug checks of a call's routing (one CTA): every id in [-1, E); offsets start at 0, never
+// decrease and end at the number of routed slots (ids >= 0), at most T * k; each entry of
+// expert e's range names a slot whose id is e, tokens strictly ascending within the range.
+// A violation sets MOE_ERR_DEVICE_CHECK; reads stay inside the arrays whatever their values.
+__global__ void __launch_bounds__(1024)
+check_routing_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ offsets,
+                     const int32_t* __restrict__ entries, int T, int top_k, int E, int* status) {
+  __shared__ int bad, routed;
+  if (threadIdx.x == 0) {
+    bad = 0;
+    routed = 0;
+  }
+  __syncthreads();
+  const int n = T * top_k;
+  int mine = 0;
+  for (int f = threadIdx.x; f < n; f += blockDim.x) {
+    const int id = ids[f];
+    if (id < -1 || id >= E) bad = 1;
+    mine += id >= 0;
+  }
+  atomicAdd(&routed, mine);
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (offsets[e + 1] < offsets[e]) bad = 1;
+  __syncthreads();
+  const int total = offsets[E];
+  if (threadIdx.x == 0 && (offsets[0] != 0 || total != routed || total > n)) bad = 1;
+  __syncthreads();
+  if (!bad) {
+    for (int q = threadIdx.x; q < total; q += blockDim.x) {
+      int lo = 0, hi = E - 1;   // expert whose range holds q: last e with offsets[e] <= q
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (offsets[mid] <= q) lo = mid;
+        else hi = mid - 1;
+      }
+      const int ent = entries[q];
+      if (ent < 0 || ent >= n || ids[ent] != lo) {
+        bad = 1;
+      } else if (q > offsets[lo]) {
+        const int prev = entries[q - 1];
+        if (prev < 0 || prev >= n || prev / top_k >= ent / top_k) bad = 1;
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && bad) raise_status(status, MOE_ERR_DEVICE_CHECK);
+}
+
 __global__ void set_slots_kernel(const SlotTable t, int n, int32_t* __restrict__ dst) {
   for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = t.slot[i];
 }
 
 }  // namespace
+
+cudaError_t launch_check_routing(const int32_t* ids, const int32_t* offsets, const int32_t* entries, int T,
+                                 int top_k, int E, int* status, cudaStream_t s) {
+  if (T <= 0 || top_k <= 0 || E <= 0) return cudaErrorInvalidValue;
+  check_routing_kernel<<<1, 1024, 0, s>>>(ids, offsets, entries, T, top_k, E, status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_set_slots(const SlotTable& t, int n, int32_t* dst, cudaStream_t s) {
   if (n <= 0 || n > kMaxSlotTable) return cudaErrorInvalidValue;

@@ -220,6 +220,12 @@ struct SlotTable {
 };
 cudaError_t launch_set_slots(const SlotTable& t, int n, int32_t* dst, cudaStream_t s);
 
+// Debug checks of a routing (ids [T*k], offsets [E+1], entries): sets MOE_ERR_DEVICE_CHECK in
+// *status on a violation (ids outside [-1, E), offsets not monotone or not ending at the
+// routed count, an entry naming another expert's slot or tokens out of order).
+cudaError_t launch_check_routing(const int32_t* ids, const int32_t* offsets, const int32_t* entries, int T,
+                                 int top_k, int E, int* status, cudaStream_t s);
+
 // out[T, H] (act dtype) = out_acc
 cudaError_t launch_finalize(const float* out_acc, void* out, int act_dtype, size_t n,
                             cudaStream_t s);

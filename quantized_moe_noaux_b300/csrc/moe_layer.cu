@@ -1,5 +1,6 @@
 // C ABI of the MoE layer (include/moe_layer.h): layer creation (weight upload and
 // workspace sizing), the forward pipeline, routing read-back and status reporting.
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -107,11 +108,21 @@ struct moe_layer {
   unsigned long long* trace = nullptr;   // decode-kernel phase timestamps (profiling)
   unsigned long long wait_ns = 2000000000ull;   // limit of the kernels' waits on other CTAs
   int identity_act = 0;                          // test-only: h = gate * up (no SiLU)
+  int debug_checks = 0;                          // check each call's routing on the device
 };
 
 static constexpr int kStageEvents = 8;
 
 namespace {
+
+// Test hook: the n-th allocation from now fails (0 = off).
+std::atomic<int> g_fail_alloc_at{0};
+std::atomic<int> g_alloc_count{0};
+
+bool forced_alloc_failure() {
+  const int at = g_fail_alloc_at.load();
+  return at > 0 && g_alloc_count.fetch_add(1) + 1 == at;
+}
 
 size_t act_bytes(int dt) { return dt == MOE_DT_F32 ? 4 : 2; }
 
@@ -161,6 +172,7 @@ moe_status validate_config(const moe_config* c) {
 moe_status dev_alloc(moe_layer* L, void** p, size_t bytes) {
   *p = nullptr;
   if (bytes == 0) return MOE_OK;
+  if (forced_alloc_failure()) return MOE_ERR_OOM;
   if (cudaMalloc(p, bytes) != cudaSuccess) {
     cudaGetLastError();
     *p = nullptr;
@@ -191,6 +203,7 @@ void free_all(moe_layer* L) {
 
 moe_status host_alloc(moe_layer* L, void** p, size_t bytes) {
   *p = nullptr;
+  if (forced_alloc_failure()) return MOE_ERR_OOM;
   if (cudaHostAlloc(p, bytes, cudaHostAllocDefault) != cudaSuccess) {
     cudaGetLastError();
     *p = nullptr;
@@ -644,6 +657,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
                    L->weights, L->offsets, L->entries, L->dec_h16, L->dec_gu_part, L->dec_y_part,
                    out, L->dsync, L->status, L->wait_ns, L->trace};
     MOE_LAUNCH(launch_decode_fused(d, c.act_dtype, c.router_dtype, L->n_sm, s));
+    if (L->debug_checks) MOE_LAUNCH(launch_check_routing(L->ids, L->offsets, L->entries, T, k, E, L->status, s));
     for (int i = 3; i < kStageEvents; ++i) MOE_CK(m.mark(i));
     return MOE_OK;
   }
@@ -661,6 +675,7 @@ moe_status forward_impl(moe_layer* L, const void* x, int T, void* out, cudaStrea
                            L->ids, L->weights, L->counts, L->status, s));
   MOE_LAUNCH(launch_group(L->ids, L->counts, T, k, E, L->shared_inline, L->offsets, L->entries,
                           gemm ? nullptr : L->items, L->meta, s));
+  if (L->debug_checks) MOE_LAUNCH(launch_check_routing(L->ids, L->offsets, L->entries, T, k, E, L->status, s));
   MOE_CK(m.mark(1));
   if (gemm) return forward_gemm(L, x, T, out, s, m);
   const void* x_in = x;
@@ -959,6 +974,29 @@ moe_status moe_layer_cache_query(moe_layer* L, int32_t* slot_of, int32_t* pinned
     slot_of[e] = L->cache->slot_of(e);
     pinned[e] = L->cache->pinned(e) ? 1 : 0;
   }
+  return MOE_OK;
+}
+
+moe_status moe_layer_set_debug_checks(moe_layer* L, int32_t on) {
+  if (!L || (on != 0 && on != 1)) return MOE_ERR_INVALID_ARG;
+  L->debug_checks = on;
+  return MOE_OK;
+}
+
+moe_status moe_check_routing(const int32_t* ids, const int32_t* offsets, const int32_t* entries, int32_t T,
+                             int32_t top_k, int32_t n_experts, int32_t* status, void* stream) {
+  if (!ids || !offsets || !entries || !status || T <= 0 || top_k <= 0 || n_experts <= 0)
+    return MOE_ERR_INVALID_ARG;
+  return launch_check_routing(ids, offsets, entries, T, top_k, n_experts, status,
+                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+moe_status moe_test_fail_allocation(int32_t nth) {
+  if (nth < 0) return MOE_ERR_INVALID_ARG;
+  g_alloc_count.store(0);
+  g_fail_alloc_at.store(nth);
   return MOE_OK;
 }
 

@@ -93,3 +93,14 @@ def test_create_cached_rejects_before_touching_the_device(over, slots, code):
     rc = moe.lib.moe_layer_create_cached(ctypes.byref(cfg), ctypes.byref(w), slots, None, ctypes.byref(out))
     assert rc == code, (over, slots, rc)
     assert out.value is None
+
+
+def test_debug_and_test_hooks_reject_bad_arguments():
+    """Host-side argument checks of the debug and test hooks (no device work)."""
+    assert moe.lib.moe_test_fail_allocation(-1) == 1
+    assert moe.lib.moe_test_fail_allocation(0) == 0
+    assert moe.lib.moe_check_routing(None, None, None, 4, 2, 8, None, None) == 1
+    assert moe.lib.moe_layer_set_debug_checks(None, 1) == 1
+    assert moe.lib.moe_layer_set_test_activation(None, 1) == 1
+    assert moe.lib.moe_layer_prefetch(None, None, 1, None) == 1
+    assert moe.lib.moe_layer_cache_stats(None, None) == 1
