@@ -302,9 +302,10 @@ moe_status moe_layer_reset_status(moe_layer* layer, void* stream);
  * for a cached layer's forwards and prefetches.
  *
  * moe_layer_prefetch: predict the experts of x [T, H] (device, act_dtype) with this layer's
- * router on the copy stream (after the work already on `stream`) and start loading the
- * missing ones, without waiting for the copies. For a stack of layers: prefetch layer l + 1
- * with layer l's input before running layer l. Uses a routing workspace of its own.
+ * router on a routing stream of the layer's own (after the work already on `stream`; the
+ * host waits for this routing only) and start loading the missing ones on the copy stream,
+ * without waiting for the copies. For a stack of layers: prefetch layer l + 1 with layer l's
+ * input before running layer l. Uses a routing workspace of its own.
  *
  * moe_layer_cache_pin_hot: pin the n experts most often routed so far (ties: lower id),
  * loading them if needed; pinned experts are never evicted; a new call replaces the pins.

@@ -100,6 +100,7 @@ struct moe_layer {
   int32_t* counts_p = nullptr;
   int32_t* h_counts_p = nullptr;
   cudaEvent_t ev_x = nullptr;
+  cudaStream_t route_stream = nullptr;   // prefetch routing (not behind the copies)
   // measurement
   std::vector<cudaEvent_t> events;   // kStageEvents per recorded forward
   int timing_cap = 0;
@@ -195,6 +196,11 @@ void free_all(moe_layer* L) {
   L->cache = nullptr;
   if (L->ev_x) cudaEventDestroy(L->ev_x);
   L->ev_x = nullptr;
+  if (L->route_stream) {
+    cudaStreamSynchronize(L->route_stream);
+    cudaStreamDestroy(L->route_stream);
+  }
+  L->route_stream = nullptr;
   for (void* p : L->allocs) cudaFree(p);
   L->allocs.clear();
   for (void* p : L->host_allocs) cudaFreeHost(p);
@@ -304,7 +310,9 @@ moe_status create_cache_store(moe_layer* L, const moe_config* c, const moe_weigh
     return st;
   L->h_counts = static_cast<int32_t*>(hc);
   L->h_counts_p = static_cast<int32_t*>(hcp);
-  if (cudaEventCreateWithFlags(&L->ev_x, cudaEventDisableTiming) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaEventCreateWithFlags(&L->ev_x, cudaEventDisableTiming) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&L->route_stream, cudaStreamNonBlocking) != cudaSuccess)
+    return MOE_ERR_CUDA;
   L->cache = new (std::nothrow) ExpertCache();
   if (!L->cache) return MOE_ERR_OOM;
   return L->cache->init(E, slots, up_b, dn_b, L->host_up, L->host_dn, L->gpack_up, L->gpack_down);
@@ -937,8 +945,9 @@ moe_status moe_layer_prefetch(moe_layer* L, const void* x, int32_t T, void* stre
   DeviceGuard g(L->device);
   const moe_config& c = L->cfg;
   const int E = c.n_experts, H = c.hidden;
-  cudaStream_t cs = L->cache->copy_stream();
-  // predict on the copy stream, after x is ready on the caller's stream
+  cudaStream_t cs = L->route_stream;
+  // predict on the layer's routing stream (not behind the copies in flight), after x is
+  // ready on the caller's stream; the loads then go out on the copy stream
   if (cudaEventRecord(L->ev_x, static_cast<cudaStream_t>(stream)) || cudaStreamWaitEvent(cs, L->ev_x, 0) ||
       cudaMemsetAsync(L->counts_p, 0, (size_t)(E + 1) * 4, cs) ||
       launch_router_logits(x, c.act_dtype, L->router_w, c.router_dtype, L->logits_p, T, E, H, cs) ||
