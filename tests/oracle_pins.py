@@ -425,6 +425,39 @@ def pin_q8_0_activation(O):
     assert not got[0, 2:].any()
 
 
+def pin_q8_0_layer_composition(O):
+    """Q8_0 in the whole layer, recomposed token by token from the pinned parts: x quantised
+    before every expert's gate/up (routed and shared), each expert's h quantised before its
+    down projection, the weighted combine, the shared expert added with weight 1."""
+    from dataclasses import replace
+
+    from synth import LAYERS, make_layer, make_x
+    spec = replace(LAYERS["tiny"], name="tiny_int4row_q8", weight_format="int4_row",
+                   shared_format="int4_row", act_quant="q8_0")
+    layer = O.Layer.from_spec(spec, make_layer(spec))
+    x = make_x(spec, 5, 0)
+    ref = layer.forward(x)
+    I = spec.inter
+    xq = O.quantize_q8_0_activation(x)
+    got = np.zeros_like(ref.out)
+
+    def ffn(w_gu, w_d, xt):
+        gu = w_gu @ xt
+        h = O.silu(gu[:I]) * gu[I:]
+        return w_d @ O.quantize_q8_0_activation(h[None, :])[0]
+
+    sh_gu, sh_d = layer.shared_expert()
+    for t in range(x.shape[0]):
+        for j in range(spec.top_k):
+            e = int(ref.ids[t, j])
+            got[t] += ref.weights[t, j] * ffn(layer.routed_gu(e), layer.routed_d(e), xq[t])
+        got[t] += ffn(sh_gu, sh_d, xq[t])
+    assert np.allclose(got, ref.out, rtol=1e-12, atol=1e-14)
+    # and the quantisation matters here (the unquantised layer differs)
+    plain = O.Layer.from_spec(replace(spec, act_quant="none"), make_layer(spec)).forward(x).out
+    assert not np.allclose(plain, ref.out, rtol=1e-6, atol=0)
+
+
 # ------------------------------------------------------------------- expert FFN
 
 
@@ -538,4 +571,4 @@ ALL_PINS = [pin_decode_int4, pin_decode_e4m3, pin_decode_e2m1, pin_dequant_int4_
             pin_expert_ffn_torch, pin_hand_two_expert, pin_identity_activation_exact,
             pin_hand_nvfp4_layer, pin_widen_bf16, pin_expert_top_p_hand,
             pin_expert_top_p_invariants, pin_int_row_formats, pin_int_row_roundtrip,
-            pin_q8_0_activation]
+            pin_q8_0_activation, pin_q8_0_layer_composition]

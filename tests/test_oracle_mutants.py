@@ -198,6 +198,15 @@ def _q8_0_round_half_up(a):
     return (np.clip(q, -127, 127) * d[..., None]).astype(np.float64).reshape(m, k)
 
 
+def _q8_0_h_unquantised(a):
+    # a wiring mistake of the layer: its h step (the `hidden` wrapper inside Layer.forward)
+    # skips the quantisation; every other caller gets the real quantiser
+    import sys
+    if sys._getframe(1).f_code.co_name == "hidden":
+        return np.asarray(a, np.float64)
+    return _orig["quantize_q8_0_activation"](a)
+
+
 MUTANTS = {
     "decode_int4/nibbles_swapped": ("decode_int4", _nibbles_swapped),
     "decode_int4/unsigned": ("decode_int4", _unsigned_int4),
@@ -228,6 +237,7 @@ MUTANTS = {
     "int_row/unsigned": ("decode_int_row", _int_row_unsigned),
     "q8_0/no_fp16_step": ("quantize_q8_0_activation", _q8_0_no_fp16_step),
     "q8_0/round_half_up": ("quantize_q8_0_activation", _q8_0_round_half_up),
+    "q8_0_layer/h_unquantised": ("quantize_q8_0_activation", _q8_0_h_unquantised),
 }
 
 
