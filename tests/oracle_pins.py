@@ -458,6 +458,28 @@ def pin_q8_0_layer_composition(O):
     assert not np.allclose(plain, ref.out, rtol=1e-6, atol=0)
 
 
+def pin_top_p_layer_composition(O):
+    """The adaptive top-p inside the layer: the routed ids are the selection cut by
+    expert_top_p (dropped slots -1, some dropped here), the weights are renormalised over the
+    kept slots, and the output equals the forward re-run on those ids."""
+    from dataclasses import replace
+
+    from synth import LAYERS, make_layer, make_x
+    spec = replace(LAYERS["tiny"], expert_top_p=0.6)
+    arrays = make_layer(spec)
+    layer = O.Layer.from_spec(spec, arrays)
+    x = make_x(spec, 12, 1)
+    ref = layer.forward(x)
+    scores, sel = layer.route(layer.widen_x(x))
+    keep = O.expert_top_p(scores, sel.ids, 0.6).keep
+    assert (~keep).any()
+    assert np.array_equal(ref.ids, np.where(keep, sel.ids, -1))
+    assert np.allclose(ref.weights.sum(axis=1), spec.rsf, atol=1e-12)
+    assert np.all(ref.weights[~keep] == 0)
+    full = O.Layer.from_spec(replace(spec, expert_top_p=0.0), arrays)
+    assert np.allclose(full.forward(x, ids=ref.ids).out, ref.out, rtol=1e-13, atol=1e-15)
+
+
 # ------------------------------------------------------------------- expert FFN
 
 
@@ -571,4 +593,4 @@ ALL_PINS = [pin_decode_int4, pin_decode_e4m3, pin_decode_e2m1, pin_dequant_int4_
             pin_expert_ffn_torch, pin_hand_two_expert, pin_identity_activation_exact,
             pin_hand_nvfp4_layer, pin_widen_bf16, pin_expert_top_p_hand,
             pin_expert_top_p_invariants, pin_int_row_formats, pin_int_row_roundtrip,
-            pin_q8_0_activation, pin_q8_0_layer_composition]
+            pin_q8_0_activation, pin_q8_0_layer_composition, pin_top_p_layer_composition]

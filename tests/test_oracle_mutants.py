@@ -268,5 +268,12 @@ def test_shared_weighted_by_rsf_is_caught(monkeypatch):
     assert _some_pin_fails()
 
 
+def test_layer_ignoring_top_p_is_caught(monkeypatch):
+    # a wiring mistake of the layer: the selection is used without the adaptive top-p cut
+    monkeypatch.setattr(O, "expert_top_p",
+                        lambda s, i, p: O.TopP(np.ones(np.shape(i), bool), np.full(np.shape(i)[0], np.inf)))
+    assert _some_pin_fails()
+
+
 def test_unmutated_oracle_passes_every_pin():
     assert not _some_pin_fails()
