@@ -214,18 +214,19 @@ moe_status moe_layer_stage_times(moe_layer* layer, float* ms, int32_t* n_forward
 /*
  * Profiling hook. With a device buffer of n_ctas x 64 uint64 (n_ctas >= the device's SM
  * count), later forwards write per-CTA records into buffer[cta * 64 + slot]:
- *  - fused decode kernel, slots 0..14, %globaltimer stamps (ns) at its phase boundaries:
- *    0 start, 1 activations staged, 2 router rows done, 3 all CTAs' router rows seen
- *    (routing warp), 15 selection done, 23 grouping done, 4 shared gate/up done, 5 shared
- *    gate/up of all CTAs seen, 6 shared down done, 7 routing seen, 8 routed gate/up done,
- *    9 first routed expert's gate/up seen, 10 routed down done, 11 all CTAs' down seen,
- *    12 output written, 13 producer done with shared items, 14 producer has the routing;
- *    and in slots 16..22 clock cycles of consumer thread 0 waiting for item data,
- *    computing items, reducing tiles, switching experts, the items it consumed, the
- *    producer's cycles waiting for a free slot and the items it issued; slots 24 and 25:
- *    consumer thread 0's clock64 at slots 0 and 12 (their ratio to the ns stamps is the
- *    SM clock during the kernel);
- *  - grouped GEMMs, slots 16..26 (gate/up), 32..42 (down), 48..58 (separately stored
+ *  - fused decode kernel: %globaltimer stamps (ns) at its phase boundaries in slots 0 start,
+ *    2 this CTA's router rows written, 3 every CTA's router rows seen, 7 selection done,
+ *    15 routing published, 4 / 5 / 6 epilogue done with the shared gate/up / routed gate/up /
+ *    shared down units, 12 all units done, 13 producer done issuing, 14 MMA warp done
+ *    (tensor mode); clock-cycle counters in slots 16..28 (decoders: waiting for item data,
+ *    for an accumulator or hand-off slot, busy, items; MMA warp (tensor mode): waiting for A,
+ *    for an accumulator, h staging, units; epilogue: waiting, busy, last-arriver work;
+ *    producer: waiting for a slot, items issued), 29 / 30 the epilogue thread's clock64 at
+ *    slots 0 and 12 (their ratio to the ns stamps is the SM clock), 31 units, 32 h stager
+ *    waiting, 33 / 34 MMA issue / loop cycles, 35 / 36 / 37 decoders waiting for the routing,
+ *    for an expert's h, loop total;
+ *  - grouped fp16/int4 GEMMs (the FP4 kernel writes none), slots 16..26 (gate/up), 32..42
+ *    (down), 48..58 (separately stored
  *    shared expert, gate/up), clock cycles: +0 kernel, +1 MMA waiting for operands, +2 MMA
  *    waiting for an accumulator, +3 dequantiser waiting for weights, +4 dequantiser waiting
  *    for a free stage, +5 activation producer waiting, +6 weight producer waiting, +7
