@@ -18,12 +18,18 @@ neues GLM-5.2 NVFP4 Modell vor", section "Technische Details und Quantisierungsa
 5. keep the topk_group best groups; experts of other groups are excluded (-inf);
 6. ids = the top_k largest b among kept experts; ties go to the lower index, for
    groups and for experts;
-7. w = s[ids] / sum(s[ids]) * routed_scaling_factor (unbiased s);
+7. w = s[ids] / sum(s[ids]) * routed_scaling_factor (unbiased s); with the adaptive
+   expert top-p (the "--topp" option of the first page, section "Mengunduh model dan
+   menjalankannya") the slots outside the shortest score-ordered prefix reaching p of the
+   mass are dropped (id -1, weight 0) and the sum runs over the kept slots;
 8. batch-union grouping: per expert, the (token, slot) entries that chose it, in
    ascending token order; entry = token * top_k + slot;
 9. per (token, expert): gu = W_gu x_t; h = SiLU(gu[:I]) * gu[I:]; y = W_d h, with the
-   weights dequantised exactly (int4 code * fp16 scale, or E2M1 code * E4M3 block scale
-   * fp32 tensor scale);
+   weights dequantised exactly (int4 code * fp16 scale, E2M1 code * E4M3 block scale
+   * fp32 tensor scale, or an int8 / int4 / int2 code * its row's fp32 scale: the per-row
+   formats of "Fitur utama yang diimplementasikan"); with Q8_0-style activations (same
+   section) x and every h are rounded to int8 codes with an fp16 step per 32 elements
+   before their matmul;
 10. out_t = sum_j w[t, j] y_{t, ids[t, j]} + y_{t, shared}; the shared expert has weight 1.
 
 NVFP4 layers also quantise the activations that feed the routed experts (x before the
