@@ -47,16 +47,19 @@ int ExpertCache::choose_slot(const std::vector<char>& needed) const {
 }
 
 moe_status ExpertCache::load(int e, int slot, bool& fenced) {
-  const int old = owner_[slot];
-  if (old >= 0) {
-    slot_of_[old] = -1;
-    prefetched_[old] = 0;
-    ++stats_[kEvictions];
-  }
   // kernels enqueued before this point may still read the slot: the copy waits for them
   if (!fenced && computed_valid_) {
     if (cudaStreamWaitEvent(copy_, computed_, 0) != cudaSuccess) return MOE_ERR_CUDA;
     fenced = true;
+  }
+  // the slot stops holding its expert before the first byte is overwritten, so a failed
+  // copy leaves it free rather than claimed by an expert whose bytes are gone
+  const int old = owner_[slot];
+  if (old >= 0) {
+    slot_of_[old] = -1;
+    owner_[slot] = -1;
+    prefetched_[old] = 0;
+    ++stats_[kEvictions];
   }
   if (cudaMemcpyAsync(dev_up_ + (size_t)slot * up_bytes_, host_up_ + (size_t)e * up_bytes_, up_bytes_,
                       cudaMemcpyHostToDevice, copy_) != cudaSuccess ||

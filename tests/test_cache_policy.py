@@ -222,6 +222,32 @@ def test_runtime_failures_are_reported(lib):
     lib.ch_fail_call(0)
 
 
+def test_state_after_a_failed_load(lib):
+    """A load whose fence fails changes nothing; one whose copy fails leaves the victim's
+    slot free (its expert no longer resident, counted once as evicted), and the next
+    request takes that free slot."""
+    c = Cache(lib, E=8, slots=2)
+    assert c.ensure({0})[0] == OK and c.ensure({1})[0] == OK
+    assert c.note_compute()[0] == OK
+    lib.ch_fail_call(1)                              # the fence
+    st, ops = c.ensure({2})
+    assert st == ERR_CUDA and COPY not in kinds(ops)
+    assert list(c.owners()) == [0, 1] and c.stats()["evictions"] == 0
+    lib.ch_fail_call(2)                              # the gate/up copy into slot 0 (expert 0, LRU)
+    assert c.ensure({2})[0] == ERR_CUDA
+    assert list(c.owners()) == [-1, 1] and c.stats()["evictions"] == 1
+    st, ops = c.ensure({3})                          # the free slot, not the LRU expert 1
+    assert st == OK and copies_of(c, ops) == [(3, 0)]
+    assert list(c.owners()) == [3, 1] and c.stats()["evictions"] == 1
+    lib.ch_fail_call(3)                              # the down copy into slot 1 (expert 1)
+    assert c.ensure({4})[0] == ERR_CUDA
+    assert list(c.owners()) == [3, -1] and c.stats()["evictions"] == 2
+    st, ops = c.ensure({1})
+    assert st == OK and copies_of(c, ops) == [(1, 1)]
+    assert list(c.owners()) == [3, 1]
+    c.check_contents()
+
+
 # ---------------------------------------------------------------------------------------
 # randomised sequences against the definitions
 
