@@ -66,12 +66,27 @@ enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 };
  */
 enum { MOE_PATH_AUTO = 0, MOE_PATH_GEMV = 1, MOE_PATH_GROUPED = 2, MOE_PATH_GENERIC = 3 };
 
+/*
+ * Limits checked by moe_layer_create (outside them: MOE_ERR_UNSUPPORTED; a size <= 0 or an
+ * rsf not > 0: MOE_ERR_INVALID_ARG):
+ *   hidden      multiple of 256, at most 14336 (the CUDA-core kernels stage 4 tokens of x
+ *               in fp32 in shared memory)
+ *   inter       multiple of 64
+ *   n_experts   at most 1024, a multiple of n_group; n_group at most 32, and at least 2
+ *               experts per group
+ *   topk_group  at most n_group
+ *   top_k       at most 32 and at most topk_group * n_experts / n_group (the fused decode
+ *               path takes top_k <= 16 with T * top_k <= 64; other layers skip it)
+ *   max_tokens  at most 16384, and the work list of the CUDA-core kernels fits 16 bits:
+ *               floor(max_tokens * top_k / 4) + min(max_tokens * top_k, n_experts)
+ *               + ceil(max_tokens / 4) + 1 <= 65535
+ */
 typedef struct {
-  int32_t hidden;              /* H: multiple of 256 */
-  int32_t inter;               /* I: per-expert intermediate size, multiple of 64 */
+  int32_t hidden;              /* H */
+  int32_t inter;               /* I: per-expert intermediate size */
   int32_t n_experts;           /* E routed experts (the shared expert is extra) */
-  int32_t top_k;               /* experts per token, 1..16 */
-  int32_t n_group;             /* groups of E/n_group experts (>= 2 experts each) */
+  int32_t top_k;               /* experts per token */
+  int32_t n_group;             /* groups of E/n_group experts */
   int32_t topk_group;          /* groups kept per token */
   int32_t max_tokens;          /* largest T forward will be called with */
   float routed_scaling_factor; /* rsf */

@@ -79,6 +79,34 @@ def test_create_rejects_bad_configs_before_touching_the_device(over, code):
     assert out.value is None
 
 
+# the limits documented with moe_config, each just inside and just outside
+_SMALL = dict(inter=64, n_experts=8, n_group=4, topk_group=2, top_k=4)
+
+
+@pytest.mark.parametrize("over,accepted", [
+    (dict(hidden=14336, **_SMALL), True), (dict(hidden=14592, **_SMALL), False),
+    (dict(n_experts=1024, n_group=32), True), (dict(n_experts=1056, n_group=32), False),
+    (dict(n_experts=64, n_group=32, topk_group=32, top_k=32), True),
+    (dict(n_experts=66, n_group=33, topk_group=32, top_k=8), False),
+    (dict(n_experts=64, n_group=8, topk_group=4, top_k=32), True),    # 4 groups of 8 hold 32
+    (dict(n_experts=64, n_group=8, topk_group=3, top_k=25), False),   # 3 groups of 8 hold 24
+    (dict(max_tokens=16384), True), (dict(max_tokens=16385, top_k=1), False),
+    # work list: 8191 * 32 / 4 + 256 + 2048 + 1 = 67,833 > 65535; 7,400 tokens: 61,307
+    (dict(n_experts=256, n_group=8, topk_group=8, top_k=32, max_tokens=8191), False),
+    (dict(n_experts=256, n_group=8, topk_group=8, top_k=32, max_tokens=7400), True),
+])
+def test_create_limits_at_their_boundaries(over, accepted):
+    """A configuration inside every documented limit passes validation (creation then stops
+    at the NULL weights, or at the missing device: MOE_ERR_INVALID_ARG or MOE_ERR_CUDA); one
+    step outside a limit is MOE_ERR_UNSUPPORTED."""
+    cfg = _cfg(**over)
+    w = moe.Weights()
+    out = ctypes.c_void_p(1)
+    rc = moe.lib.moe_layer_create(ctypes.byref(cfg), ctypes.byref(w), None, ctypes.byref(out))
+    assert (rc in (1, 4)) if accepted else (rc == 2), (over, rc)
+    assert out.value is None
+
+
 @pytest.mark.parametrize("over,slots,code", [
     (dict(), 63, 1),                                             # fewer slots than one forward needs (64 * 8 > 256 -> 256)
     (dict(max_tokens=4), 31, 1),                                 # min(E, 4 * 8) = 32
