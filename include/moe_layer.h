@@ -170,10 +170,14 @@ moe_status moe_layer_create(const moe_config* cfg, const moe_weights* w, void* s
  * out[T, H] = layer(x[T, H]); x and out are device pointers in act_dtype, row-major,
  * 16-byte aligned, not overlapping. 0 <= T <= max_tokens (T = 0 is a no-op).
  * Asynchronous on `stream`: no host synchronisation, no allocation, capturable in a
- * CUDA graph. Not thread-safe per layer (the workspace is shared by calls).
+ * CUDA graph (a layer made by moe_layer_create_cached is the exception: see there). Not
+ * thread-safe per layer (the workspace is shared by calls).
  * Routing results stay on the device; moe_layer_get_routing copies them out.
- * Errors: MOE_ERR_INVALID_ARG synchronously; device-side check failures are reported by
- * moe_layer_status.
+ * Errors, returned before or while enqueueing: MOE_ERR_INVALID_ARG (NULL layer, x or out,
+ * a pointer not 16-byte aligned, x == out, T out of range); MOE_ERR_UNSUPPORTED when the
+ * path forced by moe_layer_set_path does not apply to this layer or T; MOE_ERR_CUDA when a
+ * launch or copy fails to enqueue; for a cached layer also the cache's errors. Device-side
+ * failures (check violations, wait time-outs) are reported by moe_layer_status.
  */
 moe_status moe_layer_forward(moe_layer* layer, const void* x, int32_t T, void* out, void* stream);
 
