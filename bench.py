@@ -41,7 +41,9 @@ def parse():
     p.add_argument("--workload", default="glm52_decode_t1")
     p.add_argument("--copies", type=int, default=4)
     p.add_argument("--e2e-steps", type=int, default=200)
-    p.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle time")
+    p.add_argument("--cpu-budget", type=float, default=None,
+                   help="seconds of oracle time (cpu_baseline: 20 by default; --impl reference: "
+                        "scaled with --steps and --warmup by default)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--fp4-peak", action="store_true", help="measure the dense NVFP4 tensor peak and exit")
     p.add_argument("--path", default="auto", choices=["auto", "gemv", "grouped", "generic"],
@@ -55,6 +57,14 @@ def parse():
 def dist_info():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
             int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def workload_config(wl, world):
+    """The keys that name the workload, the same on both arms' lines."""
+    spec = wl.layer
+    return {"workload": wl.name, "tokens_per_step": wl.tokens, "layer": spec.name,
+            "weight_format": spec.weight_format, "act_quant": getattr(spec, "act_quant", "none"),
+            "parallelism": f"replicas x{world}"}
 
 
 def rank_seed_base(rank, steps, warmup):
@@ -331,7 +341,8 @@ def run_reference(args):
     wl = WORKLOADS[args.workload]
     spec, T = wl.layer, wl.tokens
     arrays = make_layer(spec)
-    budget = min(150.0, max(10.0, 0.15 * (args.steps + args.warmup)))
+    budget = (args.cpu_budget if args.cpu_budget is not None
+              else min(150.0, max(10.0, 0.15 * (args.steps + args.warmup))))
     if args.warmup:
         oracle_tokens_per_s(spec, arrays, T, 0.0, step0=10_000)
     value, steps, threads, dt, n = oracle_tokens_per_s(spec, arrays, T, budget)
@@ -343,7 +354,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * dt / steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": wl.name, "tokens_per_step": T},
+            "config": workload_config(wl, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -531,12 +542,10 @@ def run_ours(args):
             "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": dtype,
             "data": "synthetic (seeded, random-init weights)",
-            "config": {"workload": wl.name, "tokens_per_step": T, "layer": spec.name,
+            "config": {**workload_config(wl, world),
                        "layer_copies": C, "l2": f"inputs larger than L2: {C} layer copies "
                        "rotated per step, each step streams its experts from HBM",
-                       "unique_experts_mean": float(np.mean(uniq)), "path": args.path,
-                       "weight_format": spec.weight_format, "act_quant": getattr(spec, "act_quant", "none"),
-                       "parallelism": f"replicas x{world}"},
+                       "unique_experts_mean": float(np.mean(uniq)), "path": args.path},
             "roofline": roofline,
             "stage_ms_per_step": {k: v / max(nfw, 1) for k, v in stage_ms.items()},
             "gpu_launches": launches,
@@ -554,8 +563,9 @@ def run_ours(args):
                        "decode_loads_per_token": spec.top_k + 1}
     if world == 1 and not args.no_cpu_baseline:
         cores, model = host_cpu()
-        v, steps, threads, dt_cpu, n = oracle_tokens_per_s(spec, arrays, T, args.cpu_budget / 2)
-        v1, steps1, _, dt1, _ = oracle_tokens_per_s(spec, arrays, T, args.cpu_budget / 2, threads=1)
+        cpu_budget = 20.0 if args.cpu_budget is None else args.cpu_budget
+        v, steps, threads, dt_cpu, n = oracle_tokens_per_s(spec, arrays, T, cpu_budget / 2)
+        v1, steps1, _, dt1, _ = oracle_tokens_per_s(spec, arrays, T, cpu_budget / 2, threads=1)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
                                 "model": model, "value_1_thread": v1,
                                 "sample": f"{steps} steps of the workload on {threads} threads ({dt_cpu:.1f} s) "
@@ -651,8 +661,7 @@ def run_hostcache(args):
     line = {"metric": METRIC, "value": pin["tokens_per_s"], "unit": UNIT, "n_gpus": 1, "steps": n_tok,
             "warmup": n_tok, "ms_per_step": pin["ms_per_token"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded, random-init weights)",
-            "config": {"workload": wl.name, "layer": spec.name, "layers": n_layers, "tokens_per_step": 1,
-                       "cache_slots_per_layer": slots, "experts_per_layer": spec.n_experts,
+            "config": {**workload_config(wl, 1), "layers": n_layers, "cache_slots_per_layer": slots, "experts_per_layer": spec.n_experts,
                        "input_correlation_between_layers": rho,
                        "host_store_gb_per_layer": (2 * spec.inter * spec.hidden + spec.hidden * spec.inter) * 9 / 16
                        * spec.n_experts / 1e9},
@@ -669,11 +678,10 @@ def main():
     if args.fp4_peak:
         fp4_peak()
         return
-    if args.workload == "glm52_hostcache_t1":
-        run_hostcache(args)
-        return
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "glm52_hostcache_t1":
+        run_hostcache(args)
     else:
         run_ours(args)
 
