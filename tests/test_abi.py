@@ -132,3 +132,60 @@ def test_debug_and_test_hooks_reject_bad_arguments():
     assert moe.lib.moe_layer_set_test_activation(None, 1) == 1
     assert moe.lib.moe_layer_prefetch(None, None, 1, None) == 1
     assert moe.lib.moe_layer_cache_stats(None, None) == 1
+
+
+# moe_route_noalloc checks every argument before its first CUDA call, so its refusals can
+# be exercised with stand-in addresses that are never dereferenced. Where a GPU is visible
+# the tests are skipped: stand-in addresses must never be able to reach a kernel launch.
+_A = 1 << 20                     # a 16-byte-aligned stand-in address
+_NOALLOC = dict(x=_A, act=1, T=4, H=256, rw=_A, rdt=0, bias=_A, E=16, n_group=4, topk_group=2,
+                top_k=4, rsf=2.5, ids=_A, w=_A, off=_A, ent=_A)
+
+
+def _gpu_visible():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+@pytest.mark.skipif(_gpu_visible(), reason="stand-in addresses: CPU only")
+@pytest.mark.parametrize("over,code", [
+    (dict(T=-1), 1), (dict(H=0), 1), (dict(E=0), 1), (dict(n_group=0), 1),
+    (dict(topk_group=0), 1), (dict(top_k=0), 1), (dict(act=5), 1), (dict(rdt=5), 1),
+    (dict(rsf=0.0), 1), (dict(rsf=float("nan")), 1),
+    (dict(E=1056, n_group=32), 2),                  # more than 1024 experts
+    (dict(E=18), 2),                                # n_group does not divide E
+    (dict(E=66, n_group=33), 2),                    # more than 32 groups
+    (dict(E=8, n_group=8, topk_group=2), 2),        # one expert per group
+    (dict(topk_group=5), 2),                        # more kept groups than groups
+    (dict(topk_group=2, top_k=9), 2),               # 2 kept groups of 4 hold 8
+    (dict(E=256, n_group=8, topk_group=8, top_k=33), 2),
+    (dict(T=257, E=1024, n_group=32), 2),           # T * E = 263168 logits > 262144
+    (dict(T=256, E=1024, n_group=32), 4),           # 262144: accepted (then no device)
+    # work list: T * k / 4 + min(T * k, E) + 1 = 8193 > 8192 at T = 2032, k = 16, E = 64
+    (dict(T=2032, E=64, n_group=4, topk_group=4, top_k=16), 2),
+    (dict(T=2028, E=64, n_group=4, topk_group=4, top_k=16), 4),   # 8177: accepted
+    (dict(x=0), 1), (dict(rw=0), 1), (dict(bias=0), 1), (dict(ids=0), 1), (dict(w=0), 1),
+    (dict(off=0), 1), (dict(ent=0), 1),
+    (dict(x=_A + 4), 1), (dict(rw=_A + 8), 1),      # x, W_r: 16-byte alignment
+    (dict(bias=_A + 2), 1), (dict(ids=_A + 2), 1), (dict(w=_A + 1), 1), (dict(off=_A + 2), 1),
+    (dict(ent=_A + 3), 1),                          # the rest: 4-byte alignment
+])
+def test_route_noalloc_refusals(over, code):
+    """Each refusal with its documented status; a case just inside a scratch limit passes
+    every check and stops at the first CUDA call (no device here: MOE_ERR_CUDA)."""
+    a = {**_NOALLOC, **over}
+    rc = moe.lib.moe_route_noalloc(a["x"], a["act"], a["T"], a["H"], a["rw"], a["rdt"], a["bias"], a["E"],
+                                   a["n_group"], a["topk_group"], a["top_k"], a["rsf"], a["ids"], a["w"],
+                                   a["off"], a["ent"], None)
+    assert rc == code, (over, rc)
+
+
+def test_route_noalloc_zero_tokens_is_a_no_op():
+    """T = 0 returns MOE_OK with NULL buffers, before any CUDA call."""
+    a = {**_NOALLOC, "T": 0}
+    rc = moe.lib.moe_route_noalloc(None, a["act"], 0, a["H"], None, a["rdt"], None, a["E"], a["n_group"],
+                                   a["topk_group"], a["top_k"], a["rsf"], None, None, None, None, None)
+    assert rc == 0
