@@ -513,6 +513,14 @@ def pin_hand_two_expert(O):
     expect[7] = w1 * 0.875 * h_e1
     expect[1] = -2 * h_sh
     assert np.allclose(ref.out[0], expect, rtol=1e-12, atol=1e-14), (ref.out[0][:8], expect[:8])
+    # k = 2 with a bias: both experts are chosen all the same, and noaux_tc's bias only
+    # selects, so the weights (per expert) and the output are those of the unbiased case
+    layer, x = hand_layer(O, "k2_bias")
+    ref_b = layer.forward(x)
+    assert sorted(ref_b.ids[0].tolist()) == [0, 1]
+    w_of = dict(zip(ref_b.ids[0].tolist(), ref_b.weights[0].tolist()))
+    assert np.allclose([w_of[0], w_of[1]], [w0, w1], rtol=1e-14, atol=0), (w_of, w0, w1)
+    assert np.allclose(ref_b.out[0], expect, rtol=1e-12, atol=1e-14), (ref_b.out[0][:8], expect[:8])
     # k = 1 with a bias that flips the choice to expert 1; its weight is exactly rsf
     layer, x = hand_layer(O, "k1")
     ref = layer.forward(x)

@@ -207,6 +207,81 @@ def _q8_0_h_unquantised(a):
     return _orig["quantize_q8_0_activation"](a)
 
 
+def _select_variant(kind):
+    """noaux_tc selection with one step changed: the group score summed over the whole
+    group, no group mask, or groups ranked by the unbiased scores."""
+    def select(scores, bias, n_group, topk_group, top_k):
+        s = np.asarray(scores, np.float64)
+        T, E = s.shape
+        G = E // n_group
+        b = s + np.asarray(bias)[None]
+        ids = np.empty((T, top_k), np.int64)
+        for t in range(T):
+            grp = (s[t] if kind == "groups_unbiased" else b[t]).reshape(n_group, G)
+            gs = grp.sum(1) if kind == "group_sum_all" else np.sort(grp, 1)[:, -2:].sum(1)
+            kept = np.argsort(-gs, kind="stable")[:topk_group]
+            m = b[t].copy() if kind == "no_group_mask" else np.full(E, -np.inf)
+            if kind != "no_group_mask":
+                for g in kept:
+                    m[g * G:(g + 1) * G] = b[t, g * G:(g + 1) * G]
+            ids[t] = np.argsort(-m, kind="stable")[:top_k]
+        return O.Selection(ids, np.full(T, np.inf), np.full(T, np.inf))
+    return select
+
+
+def _softmax(z):
+    z = np.asarray(z, np.float64)
+    e = np.exp(z - z.max(axis=-1, keepdims=True))
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def _weights_slot_rolled(scores, ids, rsf):
+    return np.roll(_orig["routing_weights"](scores, ids, rsf), 1, axis=1)
+
+
+def _silu_without_x(z):
+    return 1.0 / (1.0 + np.exp(-np.asarray(z, np.float64)))
+
+
+def _widen_as_fp16(bits):
+    return np.asarray(bits).astype(np.uint16).view(np.float16).astype(np.float64)
+
+
+def _e4m3_no_subnormal(bits):
+    # exponent field 0 read as a normal number (implicit leading 1)
+    b = np.asarray(bits).astype(np.int64)
+    exp, man = (b >> 3) & 15, b & 7
+    sgn = np.where(b & 128, -1.0, 1.0)
+    return np.where(exp == 0, sgn * (1 + man / 8.0) * 2.0 ** -6, _orig["decode_e4m3"](bits))
+
+
+def _e2m1_sign_ignored(n):
+    return np.abs(_orig["decode_e2m1"](n))
+
+
+def _q8_0_block16(a):
+    # blocks of 16 elements instead of 32
+    a = np.asarray(a, np.float64)
+    out = np.empty_like(a).reshape(-1, 16)
+    for i, blk in enumerate(a.reshape(-1, 16)):
+        out[i] = _orig["quantize_q8_0_activation"](np.concatenate([blk, np.zeros(16)])[None])[0, :16]
+    return out.reshape(a.shape)
+
+
+def _int_row_scale_ignored(codes, scales, bits):
+    return O.decode_int_row(codes, bits).astype(np.float64)
+
+
+def _group_slot_major(ids, n_experts):
+    counts, offsets, lst = _orig["group_tokens"](ids, n_experts)
+    lst = lst.copy()
+    k = np.shape(ids)[1]
+    for e in range(n_experts):
+        seg = lst[offsets[e]:offsets[e + 1]]
+        lst[offsets[e]:offsets[e + 1]] = sorted(seg, key=lambda r: (r % k, r // k))
+    return counts, offsets, lst
+
+
 MUTANTS = {
     "decode_int4/nibbles_swapped": ("decode_int4", _nibbles_swapped),
     "decode_int4/unsigned": ("decode_int4", _unsigned_int4),
@@ -238,6 +313,18 @@ MUTANTS = {
     "q8_0/no_fp16_step": ("quantize_q8_0_activation", _q8_0_no_fp16_step),
     "q8_0/round_half_up": ("quantize_q8_0_activation", _q8_0_round_half_up),
     "q8_0_layer/h_unquantised": ("quantize_q8_0_activation", _q8_0_h_unquantised),
+    "select/group_sum_all": ("select_experts", _select_variant("group_sum_all")),
+    "select/no_group_mask": ("select_experts", _select_variant("no_group_mask")),
+    "select/groups_by_unbiased_scores": ("select_experts", _select_variant("groups_unbiased")),
+    "sigmoid/softmax": ("sigmoid", _softmax),
+    "weights/slot_rolled": ("routing_weights", _weights_slot_rolled),
+    "silu/without_x": ("silu", _silu_without_x),
+    "widen_bf16/as_fp16": ("widen_bf16", _widen_as_fp16),
+    "decode_e4m3/no_subnormal": ("decode_e4m3", _e4m3_no_subnormal),
+    "decode_e2m1/sign_ignored": ("decode_e2m1", _e2m1_sign_ignored),
+    "q8_0/block16": ("quantize_q8_0_activation", _q8_0_block16),
+    "dequant_int_row/scale_ignored": ("dequant_int_row", _int_row_scale_ignored),
+    "group/slot_major": ("group_tokens", _group_slot_major),
 }
 
 
@@ -272,6 +359,19 @@ def test_layer_ignoring_top_p_is_caught(monkeypatch):
     # a wiring mistake of the layer: the selection is used without the adaptive top-p cut
     monkeypatch.setattr(O, "expert_top_p",
                         lambda s, i, p: O.TopP(np.ones(np.shape(i), bool), np.full(np.shape(i)[0], np.inf)))
+    assert _some_pin_fails()
+
+
+def test_layer_weights_from_biased_scores_is_caught(monkeypatch):
+    # a wiring mistake of the layer: the combine weights (and the top-p cut) use the biased
+    # scores b = s + bias, which noaux_tc uses for the selection only
+    orig = O.Layer.route
+
+    def route(self, x64):
+        scores, sel = orig(self, x64)
+        return scores + np.asarray(self.a["bias"], np.float64)[None], sel
+
+    monkeypatch.setattr(O.Layer, "route", route)
     assert _some_pin_fails()
 
 
