@@ -245,6 +245,15 @@ def pin_nvfp4_activation(O):
     a[1, :16] = [3, 1.5, 0.5, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0]  # block scale 0.5
     deq = O.quantize_nvfp4_activation(a)
     assert np.allclose(deq, a, rtol=1e-6, atol=0), (deq, a)
+    # exact ties of the element rounding: with amax 6 the block scale is 448 and the fp32
+    # product scale * tensor scale is exactly 1, so each element's quotient is the element
+    # itself; 0.25, 1.25, 2.5 and 5.0 lie halfway between E2M1 neighbours and round to the
+    # even one (0, 1, 2, 4; signs kept), as round-to-nearest-even does
+    a = np.zeros((1, 16), np.float32)
+    a[0, :9] = [6.0, 0.25, 1.25, 2.5, 5.0, -0.25, -1.25, -2.5, -5.0]
+    vals, sb, ts = O.nvfp4_activation_parts(a)
+    assert sb[0, 0] == 448.0 and np.float32(np.float32(sb[0, 0]) * ts) == np.float32(1.0)
+    assert vals[0, 0, :9].tolist() == [6.0, 0.0, 1.0, 2.0, 4.0, 0.0, -1.0, -2.0, -4.0], vals[0, 0]
     # error bound on random data: half an E2M1 step at the code's magnitude, relative
     # to the block's scale; at most a quarter of the block scale near zero
     x = rng.standard_normal((8, 64)).astype(np.float32)

@@ -282,6 +282,84 @@ def _group_slot_major(ids, n_experts):
     return counts, offsets, lst
 
 
+def _code_ties_away(mag, table):
+    # nearest table entry, halfway cases away from zero instead of to the even entry
+    mag = np.asarray(mag, np.float64)
+    j = np.clip(np.searchsorted(table, mag, side="right") - 1, 0, len(table) - 2)
+    up = (table[j + 1] - mag) <= (mag - table[j])
+    return np.where(mag >= table[-1], len(table) - 1, j + up).astype(np.int64)
+
+
+def _code_truncated(mag, table):
+    mag = np.asarray(mag, np.float64)
+    return np.clip(np.searchsorted(table, mag, side="right") - 1, 0, len(table) - 1).astype(np.int64)
+
+
+def _nvfp4_parts_variant(kind):
+    """NVFP4 activation quantiser with one step changed: E2M1 ties away from zero, E4M3
+    block scales truncated, a tensor scale per row, block amax over 32 elements, or a
+    tensor scale amax / 448."""
+    def parts(a):
+        a32 = np.asarray(a, np.float32)
+        m, k = a32.shape
+        if kind == "ts_per_row":
+            amax = np.max(np.abs(a32), axis=1, keepdims=True).astype(np.float32)
+        else:
+            amax = np.float32(np.max(np.abs(a32)))
+        den = np.float32(448.0 if kind == "ts_no6" else 2688.0)
+        ts = (amax / den).astype(np.float32)
+        if np.all(ts == 0):
+            return np.zeros((m, k // 16, 16)), np.zeros((m, k // 16)), np.float32(0)
+        blocks = a32.reshape(m, k // 16, 16)
+        if kind == "amax32":
+            bamax = np.repeat(np.max(np.abs(a32.reshape(m, k // 32, 32)), axis=2), 2, axis=1)
+        else:
+            bamax = np.max(np.abs(blocks), axis=2)
+        ratio = ((bamax / np.float32(6.0)).astype(np.float32) / ts).astype(np.float32)
+        scode = _code_truncated if kind == "e4m3_truncated" else O._rne_code
+        sb = O._E4M3_MAGS[scode(ratio, O._E4M3_MAGS)]
+        denom = (sb.astype(np.float32) * ts).astype(np.float32)
+        q = np.zeros(blocks.shape, np.float32)
+        np.divide(blocks, denom[..., None], out=q, where=denom[..., None] != 0)
+        ecode = _code_ties_away if kind == "e2m1_ties_away" else O._rne_code
+        vals = np.sign(q) * O._E2M1_MAGS[ecode(np.abs(q), O._E2M1_MAGS)]
+        if kind == "ts_per_row":
+            return vals, sb * ts, np.float32(1.0)
+        return vals, sb, np.float32(ts)
+    return parts
+
+
+def _nvfp4_tensor_scale_ignored(codes, scales, tensor_scale):
+    return _orig["dequant_nvfp4"](codes, scales, 1.0)
+
+
+def _nvfp4_scale_per_32(codes, scales, tensor_scale):
+    sc = np.asarray(scales, np.uint8)
+    return _orig["dequant_nvfp4"](codes, np.repeat(sc[:, 0::2], 2, axis=1)[:, :sc.shape[1]], tensor_scale)
+
+
+def _e4m3_no_nan(bits):
+    # S.1111.111 read as +-480 instead of NaN
+    b = np.asarray(bits).astype(np.int64) & 0xFF
+    return np.where((b & 0x7F) == 0x7F, np.where(b & 0x80, -480.0, 480.0), _orig["decode_e4m3"](bits))
+
+
+def _int4_scale_per_16(codes, scales):
+    c = O.decode_int4(codes).astype(np.float64)
+    sc = np.asarray(scales, np.float64)
+    return c * sc[:, np.minimum(np.arange(c.shape[1]) // 16, sc.shape[1] - 1)]
+
+
+def _q8_0_divide_by_128(a):
+    a32 = np.asarray(a, np.float32)
+    m, k = a32.shape
+    blocks = a32.reshape(m, k // 32, 32)
+    d = (np.max(np.abs(blocks), axis=2) / np.float32(128.0)).astype(np.float16).astype(np.float32)
+    q = np.zeros(blocks.shape, np.float32)
+    np.divide(blocks, d[..., None], out=q, where=d[..., None] != 0)
+    return (np.clip(np.rint(q), -127, 127).astype(np.float64) * d[..., None]).reshape(m, k)
+
+
 MUTANTS = {
     "decode_int4/nibbles_swapped": ("decode_int4", _nibbles_swapped),
     "decode_int4/unsigned": ("decode_int4", _unsigned_int4),
@@ -325,6 +403,16 @@ MUTANTS = {
     "q8_0/block16": ("quantize_q8_0_activation", _q8_0_block16),
     "dequant_int_row/scale_ignored": ("dequant_int_row", _int_row_scale_ignored),
     "group/slot_major": ("group_tokens", _group_slot_major),
+    "nvfp4_act/e2m1_ties_away": ("nvfp4_activation_parts", _nvfp4_parts_variant("e2m1_ties_away")),
+    "nvfp4_act/e4m3_scale_truncated": ("nvfp4_activation_parts", _nvfp4_parts_variant("e4m3_truncated")),
+    "nvfp4_act/tensor_scale_per_row": ("nvfp4_activation_parts", _nvfp4_parts_variant("ts_per_row")),
+    "nvfp4_act/block_amax_per_32": ("nvfp4_activation_parts", _nvfp4_parts_variant("amax32")),
+    "nvfp4_act/tensor_scale_without_6": ("nvfp4_activation_parts", _nvfp4_parts_variant("ts_no6")),
+    "dequant_nvfp4/tensor_scale_ignored": ("dequant_nvfp4", _nvfp4_tensor_scale_ignored),
+    "dequant_nvfp4/scale_per_32": ("dequant_nvfp4", _nvfp4_scale_per_32),
+    "decode_e4m3/no_nan": ("decode_e4m3", _e4m3_no_nan),
+    "dequant_int4_g32/scale_per_16": ("dequant_int4_g32", _int4_scale_per_16),
+    "q8_0/divide_by_128": ("quantize_q8_0_activation", _q8_0_divide_by_128),
 }
 
 
