@@ -283,6 +283,68 @@ def pin_select_brute_force(O):
             assert sorted(sel.ids[0].tolist()) == want, (E, ng, tg, k)
 
 
+def pin_router_logits(O):
+    """l = x W_r^T in fp64: small integers give the exact integer dot products (pins the
+    operand order and indexing, H != E), and a single product that needs 25 significant bits,
+    (1 + 2^-12)^2 = 1 + 2^-11 + 2^-24, comes out exactly (an fp32 evaluation rounds it)."""
+    rng = np.random.default_rng(21)
+    x = rng.integers(-4, 5, (3, 5))
+    w = rng.integers(-4, 5, (4, 5))
+    got = O.router_logits(x.astype(np.float32), w.astype(np.float32))
+    want = [[sum(int(x[t, h]) * int(w[e, h]) for h in range(5)) for e in range(4)] for t in range(3)]
+    assert got.tolist() == want
+    v = np.float32(1 + 2.0 ** -12)
+    assert O.router_logits(np.array([[v]]), np.array([[v]]))[0, 0] == 1 + 2.0 ** -11 + 2.0 ** -24
+
+
+def pin_selection_margins(O):
+    """The selection's margins, which the parity checks use to tell near-ties from
+    mismatches: group margin = score of the last kept group - score of the first dropped
+    group; expert margin = k-th - (k+1)-th biased score among the kept groups' experts; inf
+    where nothing is dropped at that level."""
+    # hand-worked: groups (0.9, 0.1) (0.8, 0.3) (0.5, 0.45) (0.2, 0.1) score 1.0, 1.1, 0.95,
+    # 0.3; groups 1 and 0 kept (margin 1.0 - 0.95); experts 0.9, 0.8 chosen over 0.3
+    b = np.array([[0.9, 0.1, 0.8, 0.3, 0.5, 0.45, 0.2, 0.1]])
+    sel = O.select_experts(b, np.zeros(8), 4, 2, 2)
+    assert sorted(sel.ids[0].tolist()) == [0, 2]
+    assert abs(sel.group_margin[0] - 0.05) < 1e-15 and abs(sel.expert_margin[0] - 0.5) < 1e-15
+    # every group kept: no group margin; the 2nd and 3rd largest of all eight are 0.8, 0.5
+    all_groups = O.select_experts(b, np.zeros(8), 4, 4, 2)
+    assert np.isinf(all_groups.group_margin[0]) and abs(all_groups.expert_margin[0] - 0.3) < 1e-15
+    all_experts = O.select_experts(b, np.zeros(8), 4, 2, 4)
+    assert np.isinf(all_experts.expert_margin[0])
+    # brute force on random rows
+    rng = np.random.default_rng(22)
+    s = rng.uniform(0, 1, (200, 12))
+    bias = rng.normal(0, 0.2, 12)
+    sel = O.select_experts(s, bias, 4, 2, 3)
+    bb = s + bias[None]
+    for t in range(200):
+        gsc = sorted((sum(sorted(bb[t, 3 * g:3 * g + 3].tolist())[-2:]), g) for g in range(4))[::-1]
+        kept = [g for _, g in gsc[:2]]
+        cand = sorted((bb[t, e] for g in kept for e in range(3 * g, 3 * g + 3)), reverse=True)
+        assert abs(sel.group_margin[t] - (gsc[1][0] - gsc[2][0])) < 1e-12
+        assert abs(sel.expert_margin[t] - (cand[2] - cand[3])) < 1e-12
+        assert sel.margin[t] == min(sel.group_margin[t], sel.expert_margin[t])
+
+
+def pin_top_p_margin(O):
+    """The adaptive top-p's margin: the distance of the nearest mass-before-rank from the
+    threshold p * total, or the score gap across the cut when smaller, over the total; inf
+    when nothing can be cut (p outside (0, 1), or one expert)."""
+    ids = np.array([[0, 1, 2]])
+    # s 0.5, 0.35, 0.15, p 0.7: masses before ranks 1, 2 are 0.5 and 0.85 -> nearest 0.15
+    r = O.expert_top_p(np.array([[0.5, 0.35, 0.15]]), ids, 0.7)
+    assert r.keep[0].tolist() == [True, True, False] and abs(r.margin[0] - 0.15) < 1e-12
+    # s 0.5, 0.26, 0.24, p 0.6: masses 0.5, 0.76 (0.1 away) but the cut separates 0.26 from
+    # 0.24 -> 0.02
+    r = O.expert_top_p(np.array([[0.5, 0.26, 0.24]]), ids, 0.6)
+    assert r.keep[0].tolist() == [True, True, False] and abs(r.margin[0] - 0.02) < 1e-12
+    for p in (0.0, 1.0):
+        assert np.isinf(O.expert_top_p(np.array([[0.5, 0.26, 0.24]]), ids, p).margin[0])
+    assert np.isinf(O.expert_top_p(np.array([[0.5, 0.26, 0.24]]), ids[:, :1], 0.5).margin[0])
+
+
 def pin_select_special_cases(O):
     rng = np.random.default_rng(5)
     # one group: plain top-k of b, as torch.topk finds it (distinct values)
@@ -610,4 +672,5 @@ ALL_PINS = [pin_decode_int4, pin_decode_e4m3, pin_decode_e2m1, pin_dequant_int4_
             pin_expert_ffn_torch, pin_hand_two_expert, pin_identity_activation_exact,
             pin_hand_nvfp4_layer, pin_widen_bf16, pin_expert_top_p_hand,
             pin_expert_top_p_invariants, pin_int_row_formats, pin_int_row_roundtrip,
-            pin_q8_0_activation, pin_q8_0_layer_composition, pin_top_p_layer_composition]
+            pin_q8_0_activation, pin_q8_0_layer_composition, pin_top_p_layer_composition,
+            pin_router_logits, pin_selection_margins, pin_top_p_margin]

@@ -360,6 +360,66 @@ def _q8_0_divide_by_128(a):
     return (np.clip(np.rint(q), -127, 127).astype(np.float64) * d[..., None]).reshape(m, k)
 
 
+def _top_p_rule_variant(kind):
+    """Adaptive top-p with one step changed: the threshold taken from the mass of all E
+    experts, the expert that crosses the threshold dropped, or the experts ranked by id."""
+    def top_p(scores, ids, p):
+        ref = _orig["expert_top_p"](scores, ids, p)
+        if not 0.0 < p < 1.0:
+            return ref
+        s = np.asarray(scores, np.float64)
+        ids = np.asarray(ids, np.int64)
+        keep = np.ones(ids.shape, bool)
+        for t in range(ids.shape[0]):
+            sel = s[t, ids[t]]
+            order = np.argsort(ids[t]) if kind == "order_by_id" else np.lexsort((ids[t], -sel))
+            ranked = sel[order]
+            total = s[t].sum() if kind == "mass_of_all_E" else ranked.sum()
+            upto = np.cumsum(ranked)
+            before = np.concatenate([[0.0], upto[:-1]])
+            kept = upto < p * total if kind == "crossing_dropped" else before < p * total
+            kept[0] = True
+            keep[t, order] = kept
+        return O.TopP(keep, ref.margin)
+    return top_p
+
+
+def _top_p_margin_zero(scores, ids, p):
+    r = _orig["expert_top_p"](scores, ids, p)
+    return O.TopP(r.keep, np.where(np.isfinite(r.margin), 0.0, r.margin))
+
+
+def _select_margins(value):
+    def select(scores, bias, n_group, topk_group, top_k):
+        r = _orig["select_experts"](scores, bias, n_group, topk_group, top_k)
+        return O.Selection(r.ids, np.full_like(r.group_margin, value), np.full_like(r.expert_margin, value))
+    return select
+
+
+def _router_fp32(x, router_w):
+    return (np.asarray(x, np.float32) @ np.asarray(router_w, np.float32).T).astype(np.float64)
+
+
+def _sigmoid_fp32(z):
+    z = np.asarray(z, np.float32)
+    return (np.float32(1) / (np.float32(1) + np.exp(-z))).astype(np.float64)
+
+
+def _silu_fp32(z):
+    z = np.asarray(z, np.float32)
+    return (z / (np.float32(1) + np.exp(-z))).astype(np.float64)
+
+
+def _group_token_only(ids, n_experts):
+    counts, offsets, lst = _orig["group_tokens"](ids, n_experts)
+    return counts, offsets, lst // np.shape(ids)[1]
+
+
+def _identity_glu_up_only(w_gu, xr):
+    gu = np.asarray(xr, np.float64) @ np.asarray(w_gu, np.float64).T
+    return gu[:, gu.shape[1] // 2:]
+
+
 MUTANTS = {
     "decode_int4/nibbles_swapped": ("decode_int4", _nibbles_swapped),
     "decode_int4/unsigned": ("decode_int4", _unsigned_int4),
@@ -413,6 +473,17 @@ MUTANTS = {
     "decode_e4m3/no_nan": ("decode_e4m3", _e4m3_no_nan),
     "dequant_int4_g32/scale_per_16": ("dequant_int4_g32", _int4_scale_per_16),
     "q8_0/divide_by_128": ("quantize_q8_0_activation", _q8_0_divide_by_128),
+    "top_p/mass_of_all_experts": ("expert_top_p", _top_p_rule_variant("mass_of_all_E")),
+    "top_p/crossing_expert_dropped": ("expert_top_p", _top_p_rule_variant("crossing_dropped")),
+    "top_p/ranked_by_id": ("expert_top_p", _top_p_rule_variant("order_by_id")),
+    "top_p/margin_zero": ("expert_top_p", _top_p_margin_zero),
+    "select/margins_zero": ("select_experts", _select_margins(0.0)),
+    "select/margins_inf": ("select_experts", _select_margins(np.inf)),
+    "router/fp32": ("router_logits", _router_fp32),
+    "sigmoid/fp32": ("sigmoid", _sigmoid_fp32),
+    "silu/fp32": ("silu", _silu_fp32),
+    "group/token_only": ("group_tokens", _group_token_only),
+    "identity_glu/up_only": ("identity_glu_hidden", _identity_glu_up_only),
 }
 
 
