@@ -529,6 +529,46 @@ def pin_q8_0_layer_composition(O):
     assert not np.allclose(plain, ref.out, rtol=1e-6, atol=0)
 
 
+def pin_nvfp4_layer_composition(O):
+    """NVFP4 in the whole layer, recomposed token by token from the pinned parts: x quantised
+    once for the call (one tensor scale over every token), each routed expert's gate/up on
+    those rows, all routed h rows of the call quantised together (one h tensor scale), the
+    down projection, the weighted combine, and the bf16 shared expert on the unquantised x.
+    Token 1 is rescaled to three times token 0's amax, so a tensor scale per token would move
+    token 0's block scales through E4M3 rounding: checked to change the output."""
+    from dataclasses import replace
+
+    from synth import LAYERS, make_layer, make_x
+    spec = replace(LAYERS["tiny"], name="tiny_nvfp4_f32", weight_format="nvfp4", shared_format="bf16")
+    layer = O.Layer.from_spec(spec, make_layer(spec))
+    x = make_x(spec, 4, 0)
+    a0, a1 = np.abs(x[0]).max(), np.abs(x[1]).max()
+    x[1] = (x[1] * np.float32(3.0 * a0 / a1)).astype(np.float32)
+    ref = layer.forward(x)
+    I = spec.inter
+
+    def compose(xq):
+        hs = {}
+        for e in range(spec.n_experts):
+            ent = ref.entries[ref.offsets[e]:ref.offsets[e + 1]]
+            if ent.size:
+                gu = xq[ent // spec.top_k] @ layer.routed_gu(e).T
+                hs[e] = (ent, O.silu(gu[:, :I]) * gu[:, I:])
+        out = np.zeros_like(ref.out)
+        for e, (ent, h) in O.quantize_routed_h(hs).items():
+            for r, y in zip(ent, h @ layer.routed_d(e).T):
+                t, j = divmod(int(r), spec.top_k)
+                out[t] += ref.weights[t, j] * y
+        sh_gu, sh_d = layer.shared_expert()
+        gu = x.astype(np.float64) @ sh_gu.T
+        return out + (O.silu(gu[:, :I]) * gu[:, I:]) @ sh_d.T
+
+    got = compose(O.quantize_nvfp4_activation(x))
+    assert np.allclose(got, ref.out, rtol=1e-12, atol=1e-14)
+    per_token = compose(np.vstack([O.quantize_nvfp4_activation(x[t:t + 1]) for t in range(4)]))
+    assert not np.allclose(per_token[0], ref.out[0], rtol=1e-6, atol=0)
+
+
 def pin_top_p_layer_composition(O):
     """The adaptive top-p inside the layer: the routed ids are the selection cut by
     expert_top_p (dropped slots -1, some dropped here), the weights are renormalised over the
@@ -673,4 +713,5 @@ ALL_PINS = [pin_decode_int4, pin_decode_e4m3, pin_decode_e2m1, pin_dequant_int4_
             pin_hand_nvfp4_layer, pin_widen_bf16, pin_expert_top_p_hand,
             pin_expert_top_p_invariants, pin_int_row_formats, pin_int_row_roundtrip,
             pin_q8_0_activation, pin_q8_0_layer_composition, pin_top_p_layer_composition,
-            pin_router_logits, pin_selection_margins, pin_top_p_margin]
+            pin_router_logits, pin_selection_margins, pin_top_p_margin,
+            pin_nvfp4_layer_composition]

@@ -420,6 +420,37 @@ def _identity_glu_up_only(w_gu, xr):
     return gu[:, gu.shape[1] // 2:]
 
 
+def _called_from_layer_forward():
+    import sys
+    return sys._getframe(2).f_code.co_name == "forward"
+
+
+def _nvfp4_x_unquantised_in_layer(a):
+    # wiring mistake: Layer.forward feeds the routed experts the unquantised x
+    if _called_from_layer_forward():
+        return np.asarray(a, np.float64)
+    return _orig["quantize_nvfp4_activation"](a)
+
+
+def _nvfp4_x_per_token_in_layer(a):
+    # wiring mistake: Layer.forward quantises each token with a tensor scale of its own
+    if _called_from_layer_forward():
+        a = np.asarray(a)
+        return np.vstack([_orig["quantize_nvfp4_activation"](a[t:t + 1]) for t in range(a.shape[0])])
+    return _orig["quantize_nvfp4_activation"](a)
+
+
+def _nvfp4_h_unquantised(hs):
+    return hs
+
+
+def _q8_0_x_unquantised_in_layer(a):
+    # wiring mistake: Layer.forward skips the Q8_0 step of x (its h step still runs)
+    if _called_from_layer_forward():
+        return np.asarray(a, np.float64)
+    return _orig["quantize_q8_0_activation"](a)
+
+
 MUTANTS = {
     "decode_int4/nibbles_swapped": ("decode_int4", _nibbles_swapped),
     "decode_int4/unsigned": ("decode_int4", _unsigned_int4),
@@ -484,6 +515,10 @@ MUTANTS = {
     "silu/fp32": ("silu", _silu_fp32),
     "group/token_only": ("group_tokens", _group_token_only),
     "identity_glu/up_only": ("identity_glu_hidden", _identity_glu_up_only),
+    "nvfp4_layer/x_unquantised": ("quantize_nvfp4_activation", _nvfp4_x_unquantised_in_layer),
+    "nvfp4_layer/x_tensor_scale_per_token": ("quantize_nvfp4_activation", _nvfp4_x_per_token_in_layer),
+    "nvfp4_layer/h_unquantised": ("quantize_routed_h", _nvfp4_h_unquantised),
+    "q8_0_layer/x_unquantised": ("quantize_q8_0_activation", _q8_0_x_unquantised_in_layer),
 }
 
 
