@@ -23,23 +23,36 @@ MAX_REL = 1e-2
 
 
 def valid_selection(b: np.ndarray, ids, n_group: int, topk_group: int, tol: float) -> bool:
-    """Is ``ids`` a noaux_tc top-k of the biased scores ``b`` up to ``tol``?"""
+    """Is ``ids`` a noaux_tc top-k of the biased scores ``b`` up to ``tol``? There must be a
+    set of topk_group groups, each within tol of the topk_group-th best group score and
+    holding every group that beats the best dropped group by more than tol, such that the
+    chosen experts (distinct) lie in those groups and no other expert of them exceeds the
+    smallest chosen score by more than tol. (A selection made exactly on scores within
+    tol / 4 of ``b`` always passes: group scores move by at most twice that.)"""
     E = b.size
     G = E // n_group
-    grp = b.reshape(n_group, G)
-    gs = np.sort(grp, axis=1)[:, -2:].sum(1)
-    cutoff = np.sort(gs)[::-1][topk_group - 1]
-    groups = {int(e) // G for e in ids}
-    if len(groups) > topk_group or any(gs[g] < cutoff - tol for g in groups):
+    gs = np.sort(b.reshape(n_group, G), axis=1)[:, -2:].sum(1)
+    desc = np.sort(gs)[::-1]
+    cutoff = desc[topk_group - 1]
+    chosen = [int(e) for e in ids]
+    if len(set(chosen)) != len(chosen):
         return False
-    cand = np.concatenate([b[g * G:(g + 1) * G] for g in sorted(groups)]) if groups else b
-    kth = np.sort(cand)[::-1][len(ids) - 1]
-    chosen = set(int(e) for e in ids)
-    if len(chosen) != len(ids):
+    chosen_set = set(chosen)
+    low = min(b[e] for e in chosen)
+
+    def below_chosen(g):
+        return all(b[e] <= low + tol for e in range(g * G, (g + 1) * G) if e not in chosen_set)
+
+    groups = {e // G for e in chosen}
+    if any(gs[g] < cutoff - tol for g in groups):
         return False
-    return min(b[e] for e in chosen) >= kth - tol and all(
-        b[e] <= min(b[c] for c in chosen) + tol for g in groups
-        for e in range(g * G, (g + 1) * G) if e not in chosen)
+    forced = ({g for g in range(n_group) if gs[g] > desc[topk_group] + tol}
+              if topk_group < n_group else set(range(n_group)))
+    kept = groups | forced
+    if len(kept) > topk_group or not all(below_chosen(g) for g in kept):
+        return False
+    spare = [g for g in range(n_group) if g not in kept and gs[g] >= cutoff - tol and below_chosen(g)]
+    return len(spare) >= topk_group - len(kept)
 
 
 def check_routing(ref, got: dict, *, bias, n_group: int, topk_group: int, top_k: int,
