@@ -189,3 +189,47 @@ def test_route_noalloc_zero_tokens_is_a_no_op():
     rc = moe.lib.moe_route_noalloc(None, a["act"], 0, a["H"], None, a["rdt"], None, a["E"], a["n_group"],
                                    a["topk_group"], a["top_k"], a["rsf"], None, None, None, None, None)
     assert rc == 0
+
+
+def test_struct_layouts_and_enums_match_the_header(tmp_path):
+    """The ctypes structs and constants of the binding against the C compiler's view of
+    include/moe_layer.h: size and offset of every field of moe_config and moe_weights, and
+    the value of every enum constant the binding mirrors."""
+    import json
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not found")
+    consts = {"MOE_OK": 0, "MOE_ERR_INVALID_ARG": 1, "MOE_ERR_UNSUPPORTED": 2, "MOE_ERR_OOM": 3,
+              "MOE_ERR_CUDA": 4, "MOE_ERR_TIMEOUT": 5, "MOE_ERR_DEVICE_CHECK": 6,
+              "MOE_W_INT4_G32": moe.W_INT4_G32, "MOE_W_NVFP4": moe.W_NVFP4, "MOE_W_BF16": moe.W_BF16,
+              "MOE_W_INT8_ROW": moe.W_INT8_ROW, "MOE_W_INT4_ROW": moe.W_INT4_ROW,
+              "MOE_W_INT2_ROW": moe.W_INT2_ROW, "MOE_ACT_NONE": 0, "MOE_ACT_Q8_0": 1,
+              "MOE_DT_F32": moe.DT_F32, "MOE_DT_BF16": moe.DT_BF16, "MOE_PATH_AUTO": moe.PATH_AUTO,
+              "MOE_PATH_GEMV": moe.PATH_GEMV, "MOE_PATH_GROUPED": moe.PATH_GROUPED,
+              "MOE_PATH_GENERIC": moe.PATH_GENERIC}
+    assert {v: k for k, v in moe.STATUS.items()} == {k: v for k, v in consts.items() if k.startswith("MOE_OK")
+                                                     or k.startswith("MOE_ERR")}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "moe_layer.h"', "int main(void) {",
+             'printf("{");']
+    for struct, cls in (("moe_config", moe.Config), ("moe_weights", moe.Weights)):
+        lines.append(f'printf("\\"{struct}\\": %zu, ", sizeof({struct}));')
+        for name, _ in cls._fields_:
+            lines.append(f'printf("\\"{struct}.{name}\\": %zu, ", offsetof({struct}, {name}));')
+    for name in consts:
+        lines.append(f'printf("\\"{name}\\": %d, ", (int){name});')
+    lines += ['printf("\\"end\\": 0}\\n");', "return 0; }"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                        "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    c = json.loads(subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout)
+    for struct, cls in (("moe_config", moe.Config), ("moe_weights", moe.Weights)):
+        assert c[struct] == ctypes.sizeof(cls), struct
+        for name, _ in cls._fields_:
+            assert c[f"{struct}.{name}"] == getattr(cls, name).offset, (struct, name)
+    for name, value in consts.items():
+        assert c[name] == value, name
