@@ -233,3 +233,24 @@ def test_struct_layouts_and_enums_match_the_header(tmp_path):
             assert c[f"{struct}.{name}"] == getattr(cls, name).offset, (struct, name)
     for name, value in consts.items():
         assert c[name] == value, name
+
+
+def test_plain_c_consumer(tmp_path):
+    """tests/c_abi/host_only.c, a C program that includes the header and links libmoe.so,
+    builds with a C compiler and runs its host-only checks (status names, NULL handles,
+    argument checks)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not found")
+    libdir = os.path.dirname(moe.LIB_PATH)
+    if not os.path.exists(moe.LIB_PATH):
+        pytest.fail("libmoe.so not built")
+    exe = tmp_path / "host_only"
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        os.path.join(ROOT, "tests", "c_abi", "host_only.c"), "-L", libdir, "-lmoe",
+                        "-Wl,-rpath," + libdir, "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert run.returncode == 0 and run.stdout.strip() == "ok", (run.returncode, run.stderr)
