@@ -184,14 +184,20 @@ moe_status moe_layer_forward(moe_layer* layer, const void* x, int32_t T, void* o
 /*
  * Same computation with HOST buffers: copies x_host (T*H elements of act_dtype) to the
  * device, runs the forward and copies the result into out_host, then synchronises
- * `stream`. Uses the layer's own device staging buffers (allocated at create).
+ * `stream`. Uses the layer's own device staging buffers (allocated at create); the caller
+ * keeps ownership of both host buffers, which may be pageable or pinned.
+ * Errors: MOE_ERR_INVALID_ARG (NULL layer, T out of range, NULL x_host or out_host with
+ * T > 0); the errors of moe_layer_forward; MOE_ERR_CUDA when a copy or the synchronisation
+ * fails (a device-side failure of this forward surfaces here or in moe_layer_status).
  */
 moe_status moe_layer_forward_host(moe_layer* layer, const void* x_host, int32_t T,
                                   void* out_host, void* stream);
 
 /*
  * Copy the routing of the last forward (called with the same T) to host memory and
- * synchronise `stream`. Any output pointer may be NULL to skip it.
+ * synchronise `stream`. Any output pointer may be NULL to skip it; the buffers are the
+ * caller's. Errors: MOE_ERR_INVALID_ARG (NULL layer, T outside [0, max_tokens]),
+ * MOE_ERR_CUDA (a copy or the synchronisation failed).
  *   ids     [T, top_k] int32 selected experts (slot order: descending biased score)
  *   weights [T, top_k] fp32 combine weights
  *   offsets [E + 1]    int32 exclusive scan of per-expert counts
@@ -201,12 +207,14 @@ moe_status moe_layer_get_routing(moe_layer* layer, int32_t T, int32_t* ids, floa
                                  int32_t* offsets, int32_t* entries, void* stream);
 
 /* Force the expert path (MOE_PATH_*) for later forwards; AUTO picks by T and shape. A
- * forced path that does not apply to a forward makes it return MOE_ERR_UNSUPPORTED. */
+ * forced path that does not apply to a forward makes it return MOE_ERR_UNSUPPORTED.
+ * Errors: MOE_ERR_INVALID_ARG (NULL layer, a value outside MOE_PATH_*). */
 moe_status moe_layer_set_path(moe_layer* layer, int32_t path);
 
 /*
  * Synchronise the device and report the sticky device-side status word (MOE_OK,
- * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK) plus any pending CUDA error.
+ * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK) plus any pending CUDA error (MOE_ERR_CUDA).
+ * MOE_ERR_INVALID_ARG for a NULL layer. The word stays set until moe_layer_reset_status.
  */
 moe_status moe_layer_status(moe_layer* layer);
 
@@ -219,14 +227,17 @@ moe_status moe_layer_status(moe_layer* layer);
  * separately stored shared expert's gate/up | h quantise (NVFP4) | down + combine |
  * output conversion |.
  * Events recorded while the stream is being captured become graph nodes and are timed
- * on replay. enable = 0 releases the events.
+ * on replay. enable = 0 releases the events. Errors: MOE_ERR_INVALID_ARG (NULL layer,
+ * enable < 0), MOE_ERR_CUDA (an event could not be created; none are kept then).
  */
 moe_status moe_layer_enable_timing(moe_layer* layer, int32_t enable);
 
 /*
  * Synchronise the device, then write into ms[0..6] the summed durations (milliseconds)
  * of the 7 stages over the forwards recorded since timing was enabled (or last read),
- * and their number into *n_forwards; resets the record count. An empty stage reads 0.
+ * and their number into *n_forwards (which may be NULL); resets the record count. An empty
+ * stage reads 0. ms is the caller's, 7 floats. Errors: MOE_ERR_INVALID_ARG (NULL layer or
+ * ms), MOE_ERR_CUDA (the synchronisation or an event query failed).
  */
 moe_status moe_layer_stage_times(moe_layer* layer, float* ms, int32_t* n_forwards);
 
@@ -250,12 +261,15 @@ moe_status moe_layer_stage_times(moe_layer* layer, float* ms, int32_t* n_forward
  *    waiting for an accumulator, +3 dequantiser waiting for weights, +4 dequantiser waiting
  *    for a free stage, +5 activation producer waiting, +6 weight producer waiting, +7
  *    epilogue waiting, +8 epilogue busy, +9 tiles, +10 dequantiser loop.
- * buffer = NULL switches it off (the default).
+ * buffer = NULL switches it off (the default). The buffer stays the caller's and must stay
+ * valid while traced forwards run. Errors: MOE_ERR_INVALID_ARG (NULL layer, n_ctas < 0, or
+ * a buffer with n_ctas below the SM count).
  */
 moe_status moe_layer_set_trace(moe_layer* layer, void* buffer, int32_t n_ctas);
 
 /* Cumulative number of kernel launches this layer has issued (host-side count; a forward
- * captured into a CUDA graph counts once at capture). */
+ * captured into a CUDA graph counts once at capture). MOE_ERR_INVALID_ARG for a NULL layer
+ * or count. */
 moe_status moe_layer_launch_count(moe_layer* layer, int64_t* count);
 
 /*
