@@ -36,7 +36,7 @@ GEMM_SLOTS = ["kernel", "mma_wait_operands", "mma_wait_accumulator", "dq_wait_we
 _PATHS = {"auto": 0, "gemv": 1, "grouped": 2, "generic": 3}
 
 
-def main(argv=None):
+def parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--layer", default="glm52")
     ap.add_argument("--tokens", type=int, default=1)
@@ -46,7 +46,11 @@ def main(argv=None):
     ap.add_argument("--trace", default=None, help="save decode phase timestamps here (.npy)")
     ap.add_argument("--warm-ms", type=float, default=0.0,
                     help="run forwards for this long first, so the traced ones see loaded clocks")
-    args = ap.parse_args(argv)
+    return ap
+
+
+def main(argv=None):
+    args = parser().parse_args(argv)
 
     import torch
 
