@@ -140,6 +140,49 @@ def _ptr(a) -> int | None:
     raise TypeError(type(a))
 
 
+_torch = None
+
+
+def _torch_module():
+    global _torch
+    if _torch is None:
+        import torch
+        _torch = torch
+    return _torch
+
+
+def _act_ptr(a, hidden: int, act_dtype: str, device: bool, name: str) -> int:
+    """Address of an activation buffer, after checking that it is a contiguous [T, hidden]
+    array in act_dtype (bf16: torch.bfloat16, or 16-bit integer bit patterns; f32: float32),
+    in device memory for forward and prefetch and in host memory for forward_host. The
+    library cannot see a buffer's size or memory kind, and a wrong one would make its
+    kernels read or write outside the buffer or dereference a host address, so the binding
+    refuses it before the call."""
+    if isinstance(a, np.ndarray):
+        if device:
+            raise TypeError(f"{name}: a numpy array is host memory; pass a CUDA tensor (or use forward_host)")
+        dt = a.dtype
+        ok = dt == np.float32 if act_dtype == "f32" else (dt == np.uint16 or dt == np.int16)
+        contiguous = a.flags.c_contiguous
+    else:
+        is_cuda = getattr(a, "is_cuda", None)
+        if is_cuda is None:
+            raise TypeError(f"{name}: {type(a)} is neither a numpy array nor a torch tensor")
+        if is_cuda != device:
+            raise TypeError(f"{name}: expected a {'CUDA' if device else 'host (CPU)'} tensor")
+        t, dt = _torch_module(), a.dtype
+        ok = dt is t.float32 if act_dtype == "f32" else (dt is t.bfloat16 or dt is t.int16)
+        contiguous = a.is_contiguous()
+    shape = a.shape
+    if len(shape) != 2 or shape[1] != hidden:
+        raise ValueError(f"{name}: expected shape [T, {hidden}], got {tuple(shape)}")
+    if not ok:
+        raise TypeError(f"{name}: element type {dt} does not match the layer's {act_dtype} activations")
+    if not contiguous:
+        raise ValueError(f"{name}: must be contiguous")
+    return a.ctypes.data if isinstance(a, np.ndarray) else a.data_ptr()
+
+
 def _stream(stream) -> int | None:
     if stream is None:
         import torch
@@ -203,16 +246,22 @@ class MoeLayer:
 
     def forward(self, x, out, stream=None):
         """out[T, H] = layer(x[T, H]) on device tensors, asynchronous on ``stream``."""
-        T = int(x.shape[0])
-        _check("moe_layer_forward", _get_lib().moe_layer_forward(self._h, _ptr(x), T, _ptr(out),
-                                                           _stream(stream)))
+        px = _act_ptr(x, self.hidden, self.act_dtype, True, "x")
+        po = _act_ptr(out, self.hidden, self.act_dtype, True, "out")
+        T = x.shape[0]
+        if out.shape[0] != T:
+            raise ValueError(f"out has {out.shape[0]} rows for {T} tokens")
+        _check("moe_layer_forward", _get_lib().moe_layer_forward(self._h, px, T, po, _stream(stream)))
         return out
 
     def forward_host(self, x_host, out_host, stream=None):
         """Same with host buffers (copies in, forward, copies out, synchronises)."""
-        T = int(x_host.shape[0])
-        _check("moe_layer_forward_host", _get_lib().moe_layer_forward_host(
-            self._h, _ptr(x_host), T, _ptr(out_host), _stream(stream)))
+        px = _act_ptr(x_host, self.hidden, self.act_dtype, False, "x_host")
+        po = _act_ptr(out_host, self.hidden, self.act_dtype, False, "out_host")
+        T = x_host.shape[0]
+        if out_host.shape[0] != T:
+            raise ValueError(f"out_host has {out_host.shape[0]} rows for {T} tokens")
+        _check("moe_layer_forward_host", _get_lib().moe_layer_forward_host(self._h, px, T, po, _stream(stream)))
         return out_host
 
     def routing(self, T: int, stream=None) -> dict:
@@ -240,8 +289,9 @@ class MoeLayer:
         return dict(zip(STAGES, list(ms))), n.value
 
     def set_trace(self, buffer, n_ctas: int):
-        """Profiling hook: per-CTA phase timestamps of the fused decode kernel into a
-        device buffer of n_ctas x 16 int64 (None switches it off)."""
+        """Profiling hook: per-CTA phase records of the fused decode kernel and the grouped
+        GEMMs into a device buffer of n_ctas x 64 int64, n_ctas at least the SM count (None
+        switches it off); the slots are listed with moe_layer_set_trace in the header."""
         _check("moe_layer_set_trace", _get_lib().moe_layer_set_trace(self._h, _ptr(buffer), n_ctas))
 
     def launch_count(self) -> int:
@@ -283,8 +333,8 @@ class MoeLayer:
 
     def prefetch(self, x, stream=None):
         """Start loading the experts this layer's router predicts for x (device tensor)."""
-        _check("moe_layer_prefetch", _get_lib().moe_layer_prefetch(self._h, _ptr(x), int(x.shape[0]),
-                                                                   _stream(stream)))
+        px = _act_ptr(x, self.hidden, self.act_dtype, True, "x")
+        _check("moe_layer_prefetch", _get_lib().moe_layer_prefetch(self._h, px, x.shape[0], _stream(stream)))
 
     def cache_pin_hot(self, n: int):
         _check("moe_layer_cache_pin_hot", _get_lib().moe_layer_cache_pin_hot(self._h, int(n)))

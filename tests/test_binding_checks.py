@@ -1,0 +1,63 @@
+"""The binding refuses activation buffers of the wrong shape, element type or memory kind
+before calling the library (which cannot see them, and whose kernels would read or write
+outside such a buffer or dereference a host address). A buffer that passes reaches the
+library: with a NULL layer handle that call returns MOE_ERR_INVALID_ARG (CPU only; stream 0
+is the legacy default stream, so no CUDA context is needed)."""
+
+import numpy as np
+import pytest
+import torch
+
+import quantized_moe_noaux_b300 as moe
+
+
+def layer(act_dtype, hidden=256):
+    L = object.__new__(moe.MoeLayer)      # no library object: the handle stays NULL
+    L.hidden, L.act_dtype, L.top_k, L.n_experts = hidden, act_dtype, 4, 16
+    L._h = moe._P()
+    return L
+
+
+def reaches_library(call):
+    with pytest.raises(moe.MoeError) as ei:
+        call()
+    return ei.value.code == 1
+
+
+def test_forward_host_accepts_host_buffers_of_the_layer_type():
+    L = layer("f32")
+    assert reaches_library(lambda: L.forward_host(np.zeros((3, 256), np.float32), np.zeros((3, 256), np.float32), 0))
+    assert reaches_library(lambda: L.forward_host(torch.zeros(3, 256), torch.zeros(3, 256), 0))
+    B = layer("bf16")
+    assert reaches_library(lambda: B.forward_host(np.zeros((2, 256), np.uint16), np.zeros((2, 256), np.uint16), 0))
+    assert reaches_library(lambda: B.forward_host(torch.zeros(2, 256, dtype=torch.bfloat16),
+                                                  torch.zeros(2, 256, dtype=torch.bfloat16), 0))
+
+
+@pytest.mark.parametrize("x,out,exc", [
+    (np.zeros((3, 128), np.float32), np.zeros((3, 128), np.float32), ValueError),     # wrong H
+    (np.zeros(256, np.float32), np.zeros(256, np.float32), ValueError),               # not 2-D
+    (np.zeros((3, 256), np.float64), np.zeros((3, 256), np.float64), TypeError),      # wrong type
+    (np.zeros((3, 256), np.float32), np.zeros((2, 256), np.float32), ValueError),     # row count
+    ([[0.0] * 256], np.zeros((1, 256), np.float32), TypeError),                       # not an array
+])
+def test_forward_host_refusals(x, out, exc):
+    with pytest.raises(exc):
+        layer("f32").forward_host(x, out)
+
+
+def test_bf16_layer_refuses_other_16_and_32_bit_types():
+    B = layer("bf16")
+    with pytest.raises(TypeError):
+        B.forward_host(np.zeros((2, 256), np.float32), np.zeros((2, 256), np.float32))
+    with pytest.raises(TypeError):
+        B.forward_host(torch.zeros(2, 256, dtype=torch.float16), torch.zeros(2, 256, dtype=torch.float16))
+
+
+def test_device_entry_points_refuse_host_memory():
+    L = layer("f32")
+    for bad in (np.zeros((3, 256), np.float32), torch.zeros(3, 256)):
+        with pytest.raises(TypeError):
+            L.forward(bad, bad)
+        with pytest.raises(TypeError):
+            L.prefetch(bad)
