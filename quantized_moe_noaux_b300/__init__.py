@@ -291,7 +291,13 @@ class MoeLayer:
     def set_trace(self, buffer, n_ctas: int):
         """Profiling hook: per-CTA phase records of the fused decode kernel and the grouped
         GEMMs into a device buffer of n_ctas x 64 int64, n_ctas at least the SM count (None
-        switches it off); the slots are listed with moe_layer_set_trace in the header."""
+        switches it off); the slots are listed with moe_layer_set_trace in the header. The
+        kernels write into the buffer, so it must be a CUDA tensor of at least that size."""
+        if buffer is not None:
+            if not getattr(buffer, "is_cuda", False):
+                raise TypeError("the trace buffer must be a CUDA tensor")
+            if buffer.numel() * buffer.element_size() < int(n_ctas) * 64 * 8:
+                raise ValueError(f"the trace buffer holds fewer than {n_ctas} x 64 int64")
         _check("moe_layer_set_trace", _get_lib().moe_layer_set_trace(self._h, _ptr(buffer), n_ctas))
 
     def launch_count(self) -> int:

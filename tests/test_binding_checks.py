@@ -61,3 +61,12 @@ def test_device_entry_points_refuse_host_memory():
             L.forward(bad, bad)
         with pytest.raises(TypeError):
             L.prefetch(bad)
+
+
+def test_trace_buffer_must_be_a_large_enough_device_tensor():
+    L = layer("f32")
+    with pytest.raises(TypeError):
+        L.set_trace(torch.zeros((148, 64), dtype=torch.int64), 148)      # host memory
+    with pytest.raises(TypeError):
+        L.set_trace(np.zeros((148, 64), np.int64), 148)
+    assert reaches_library(lambda: L.set_trace(None, 148))              # switching off
