@@ -183,6 +183,38 @@ def _act_ptr(a, hidden: int, act_dtype: str, device: bool, name: str) -> int:
     return a.ctypes.data if isinstance(a, np.ndarray) else a.data_ptr()
 
 
+def _row_bytes(fmt: str, k: int) -> tuple[int, int]:
+    """(code bytes, scale bytes) of one weight row of k inputs in a storage format."""
+    return {"int4_g32": (k // 2, (k // 32) * 2), "nvfp4": (k // 2, k // 16), "int8_row": (k, 4),
+            "int4_row": (k // 2, 4), "int2_row": (k // 4, 4), "bf16": (2 * k, 0)}[fmt]
+
+
+def weight_bytes(hidden: int, inter: int, n_experts: int, weight_format: str, shared_format: str,
+                 router_dtype: str) -> dict:
+    """Byte size of every weight array of a layer, as laid out in include/moe_layer.h."""
+    H, I, E = hidden, inter, n_experts
+    gc, gs = _row_bytes(weight_format, H)
+    dc, ds = _row_bytes(weight_format, I)
+    want = {"router_w": E * H * (4 if router_dtype == "f32" else 2), "bias": 4 * E,
+            "gu_codes": E * 2 * I * gc, "gu_scales": E * 2 * I * gs, "d_codes": E * H * dc,
+            "d_scales": E * H * ds}
+    if weight_format == "nvfp4":
+        want.update(gu_tscale=4 * E, d_tscale=4 * E)
+    sgc, sgs = _row_bytes(shared_format, H)
+    sdc, sds = _row_bytes(shared_format, I)
+    if shared_format == "bf16":
+        want.update(sh_gu_bf16=2 * I * sgc, sh_d_bf16=H * sdc)
+    else:
+        want.update(sh_gu_codes=2 * I * sgc, sh_gu_scales=2 * I * sgs, sh_d_codes=H * sdc, sh_d_scales=H * sds)
+        if shared_format == "nvfp4":
+            want.update(sh_gu_tscale=4, sh_d_tscale=4)
+    return want
+
+
+def _nbytes(a) -> int:
+    return a.nbytes if isinstance(a, np.ndarray) else a.numel() * a.element_size()
+
+
 def _stream(stream) -> int | None:
     if stream is None:
         import torch
@@ -212,6 +244,12 @@ class MoeLayer:
         self.hidden, self.top_k, self.n_experts, self.max_tokens = hidden, top_k, n_experts, max_tokens
         self.act_dtype = act_dtype
         a = arrays
+        # the library copies each array with the size its layout implies: a shorter array
+        # would be read past its end (a missing one is the library's MOE_ERR_INVALID_ARG)
+        for name, nb in weight_bytes(hidden, inter, n_experts, weight_format, shared_format,
+                                     router_dtype).items():
+            if a.get(name) is not None and _nbytes(a[name]) != nb:
+                raise ValueError(f"weight array {name}: {_nbytes(a[name])} bytes, the layout needs {nb}")
         sh_gu = a.get("sh_gu_bf16") if shared_format == "bf16" else a.get("sh_gu_codes")
         sh_d = a.get("sh_d_bf16") if shared_format == "bf16" else a.get("sh_d_codes")
         w = Weights(_ptr(a["router_w"]), _ptr(a["bias"]), _ptr(a["gu_codes"]),

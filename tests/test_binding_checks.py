@@ -70,3 +70,39 @@ def test_trace_buffer_must_be_a_large_enough_device_tensor():
     with pytest.raises(TypeError):
         L.set_trace(np.zeros((148, 64), np.int64), 148)
     assert reaches_library(lambda: L.set_trace(None, 148))              # switching off
+
+
+def test_weight_sizes_follow_the_header_layout_for_every_generated_layer():
+    """weight_bytes (the header's layout table) against the arrays the generator allocates
+    for every layer spec: its per-expert allocation (no data drawn) times E for the routed
+    experts, once for the shared expert, and its router arrays."""
+    from synth import LAYERS
+    from synth.layer import _alloc_expert_arrays, make_router
+    for name, s in LAYERS.items():
+        want = moe.weight_bytes(s.hidden, s.inter, s.n_experts, s.weight_format, s.shared_format,
+                                s.router_dtype)
+        got = {k: moe._nbytes(a) * s.n_experts
+               for k, a in _alloc_expert_arrays(1, s.hidden, s.inter, s.weight_format, "").items()}
+        got.update({k: moe._nbytes(a)
+                    for k, a in _alloc_expert_arrays(1, s.hidden, s.inter, s.shared_format, "sh_").items()})
+        router_w, bias = make_router(s)
+        got.update(router_w=router_w.nbytes, bias=bias.nbytes)
+        assert got == want, (name, {k: (got.get(k), want.get(k)) for k in set(got) | set(want)
+                                    if got.get(k) != want.get(k)})
+
+
+def test_weight_arrays_of_the_wrong_size_are_refused_before_creation():
+    from synth import LAYERS
+    from synth.layer import make_layer
+    spec = LAYERS["tiny"]
+    arrays = make_layer(spec)
+    short = dict(arrays, gu_scales=arrays["gu_scales"][:, :, :4].copy())      # scales per 64
+    with pytest.raises(ValueError):
+        moe.MoeLayer.from_spec(spec, short, max_tokens=4, stream=0)
+    wide = dict(arrays, router_w=np.zeros((spec.n_experts, 2 * spec.hidden), np.float32))
+    with pytest.raises(ValueError):
+        moe.MoeLayer.from_spec(spec, wide, max_tokens=4, stream=0)
+    # the right sizes reach the library (no device here: MOE_ERR_CUDA)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.MoeLayer.from_spec(spec, arrays, max_tokens=4, stream=0)
+    assert ei.value.code == 4
