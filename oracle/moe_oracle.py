@@ -1,8 +1,8 @@
 """fp64 CPU oracle of the quantised routed-MoE layer forward.
 
-TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline
-leg of ``bench.py`` may import this module; the library's own path never does, and it
-shares no code with the CUDA sources.
+TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s
+CPU-baseline leg and ``--impl reference`` arm may import this module; the library's own
+path never does, and it shares no code with the CUDA sources.
 
 What it computes, step by step, in the pages' order (DeepSeek-V3-style router with
 noaux_tc, routed_scaling_factor and an always-on shared expert: "Show HN: Menjalankan
