@@ -106,3 +106,13 @@ def test_weight_arrays_of_the_wrong_size_are_refused_before_creation():
     with pytest.raises(moe.MoeError) as ei:
         moe.MoeLayer.from_spec(spec, arrays, max_tokens=4, stream=0)
     assert ei.value.code == 4
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without libmoe.so every use of the library raises; there is no fallback path."""
+    monkeypatch.setattr(moe, "LIB_PATH", str(tmp_path / "libmoe.so"))
+    monkeypatch.setattr(moe, "_lib", None)
+    with pytest.raises(ImportError, match="no fallback"):
+        moe.lib
+    with pytest.raises(ImportError):
+        layer("f32").forward_host(np.zeros((1, 256), np.float32), np.zeros((1, 256), np.float32), 0)
