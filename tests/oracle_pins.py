@@ -232,6 +232,11 @@ def pin_nvfp4_rounding(O):
     got = O._rne_code(vals, O._E2M1_MAGS)
     want = [7 if v >= 6 else _brute_round(v, table) for v in vals]
     assert got.tolist() == want
+    # every representable E2M1 magnitude comes back to its own code, and every code decodes
+    # to the magnitude with its sign
+    assert O._rne_code(np.array(table, np.float64), O._E2M1_MAGS).tolist() == list(range(8))
+    assert O.decode_e2m1(np.arange(8)).tolist() == table
+    assert O.decode_e2m1(np.arange(8, 16)).tolist() == [-v for v in table]
 
 
 def pin_nvfp4_activation(O):
