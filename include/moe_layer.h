@@ -335,6 +335,18 @@ moe_status moe_layer_reset_status(moe_layer* layer, void* stream);
  * does not need are evicted), and the expert kernels wait for those copies. Use one stream
  * for a cached layer's forwards and prefetches.
  *
+ * moe_cache_slots_for_memory: the largest number of expert slots (at most n_experts) whose
+ * HBM store, the shared expert's slot included, fits in budget_bytes for a layer that
+ * moe_layer_create_cached accepts with this configuration: the sizing step of the expert
+ * cache that "Fitur utama yang diimplementasikan" of "Show HN: Menjalankan GLM 5.2 di
+ * komputer lambat" describes (the cache sized at start-up from the memory available). The
+ * budget is the caller's share of free device memory for this layer's experts (for
+ * instance cudaMemGetInfo's free bytes less the layers' workspaces, divided among the
+ * layers of a stack). Host arithmetic only, no CUDA call. Errors: MOE_ERR_INVALID_ARG (a
+ * NULL pointer, or a configuration moe_layer_create refuses as such), MOE_ERR_UNSUPPORTED
+ * (a configuration moe_layer_create_cached does not take), MOE_ERR_OOM (the budget holds
+ * fewer than min(n_experts, max_tokens * top_k) + 1 slots); *slots is 0 on any error.
+ *
  * moe_layer_prefetch: predict the experts of x [T, H] (device, act_dtype) with this layer's
  * router on a routing stream of the layer's own (after the work already on `stream`; the
  * host waits for this routing only) and start loading the missing ones on the copy stream,
@@ -353,6 +365,7 @@ moe_status moe_layer_reset_status(moe_layer* layer, void* stream);
  */
 moe_status moe_layer_create_cached(const moe_config* cfg, const moe_weights* w, int32_t slots,
                                    void* stream, moe_layer** out);
+moe_status moe_cache_slots_for_memory(const moe_config* cfg, uint64_t budget_bytes, int32_t* slots);
 moe_status moe_layer_prefetch(moe_layer* layer, const void* x, int32_t T, void* stream);
 moe_status moe_layer_cache_pin_hot(moe_layer* layer, int32_t n);
 moe_status moe_layer_cache_stats(moe_layer* layer, int64_t* stats);

@@ -78,6 +78,7 @@ SYMBOLS = {
     "moe_layer_get_nvfp4_act": (_I, [_P, _I, _P, _P, _P, _P]),
     "moe_layer_create_cached": (_I, [ctypes.POINTER(Config), ctypes.POINTER(Weights), _I, _P,
                                      ctypes.POINTER(_P)]),
+    "moe_cache_slots_for_memory": (_I, [ctypes.POINTER(Config), ctypes.c_uint64, ctypes.POINTER(_I)]),
     "moe_layer_prefetch": (_I, [_P, _P, _I, _P]),
     "moe_layer_cache_pin_hot": (_I, [_P, _I]),
     "moe_layer_cache_stats": (_I, [_P, _P]),
@@ -222,6 +223,23 @@ def _stream(stream) -> int | None:
     if hasattr(stream, "cuda_stream"):
         return stream.cuda_stream
     return int(stream)
+
+
+def config_from_spec(spec, max_tokens: int) -> Config:
+    """The moe_config of any object with the ``synth.LayerSpec`` attribute names."""
+    return Config(spec.hidden, spec.inter, spec.n_experts, spec.top_k, spec.n_group, spec.topk_group,
+                  max_tokens, spec.rsf, _FMT[spec.weight_format], _FMT[spec.shared_format],
+                  _DT[spec.act_dtype], _DT[spec.router_dtype], getattr(spec, "expert_top_p", 0.0),
+                  _ACT[getattr(spec, "act_quant", "none")])
+
+
+def cache_slots_for_memory(spec, max_tokens: int, budget_bytes: int) -> int:
+    """moe_cache_slots_for_memory: the expert slots of a cached layer that fit the budget."""
+    slots = ctypes.c_int32()
+    cfg = config_from_spec(spec, max_tokens)
+    _check("moe_cache_slots_for_memory", _get_lib().moe_cache_slots_for_memory(
+        ctypes.byref(cfg), int(budget_bytes), ctypes.byref(slots)))
+    return slots.value
 
 
 class MoeLayer:

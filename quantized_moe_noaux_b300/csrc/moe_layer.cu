@@ -905,6 +905,32 @@ moe_status moe_layer_get_nvfp4_act(moe_layer* L, int32_t T, uint8_t* codes, uint
   return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// Layers with host-resident experts: int4-g32 routed and shared experts without Q8_0, on
+// the grouped tensor-core path, with a slot table that holds every expert.
+static moe_status cached_layer_support(const moe_config* c) {
+  if (c->weight_format != MOE_W_INT4_G32 || c->shared_format != MOE_W_INT4_G32 || c->act_quant != MOE_ACT_NONE ||
+      !gemm_supported(c->hidden, c->inter) || c->n_experts + 1 > kMaxSlotTable)
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+static int cached_min_slots(const moe_config* c) {
+  return (long)c->max_tokens * c->top_k < c->n_experts ? c->max_tokens * c->top_k : c->n_experts;
+}
+
+moe_status moe_cache_slots_for_memory(const moe_config* cfg, uint64_t budget_bytes, int32_t* slots) {
+  if (!slots) return MOE_ERR_INVALID_ARG;
+  *slots = 0;
+  if (!cfg) return MOE_ERR_INVALID_ARG;
+  moe_status st = validate_config(cfg);
+  if (st || (st = cached_layer_support(cfg))) return st;
+  const uint64_t per = gemm_pack_bytes(2 * cfg->inter, cfg->hidden, 1) + gemm_pack_bytes(cfg->hidden, cfg->inter, 1);
+  const uint64_t fit = budget_bytes / per;   // routed slots + the shared expert's slot
+  if (fit < (uint64_t)cached_min_slots(cfg) + 1) return MOE_ERR_OOM;
+  *slots = fit - 1 > (uint64_t)cfg->n_experts ? cfg->n_experts : (int32_t)(fit - 1);
+  return MOE_OK;
+}
+
 moe_status moe_layer_create_cached(const moe_config* cfg, const moe_weights* w, int32_t slots, void* stream,
                                    moe_layer** out) {
   if (!out) return MOE_ERR_INVALID_ARG;
@@ -912,11 +938,8 @@ moe_status moe_layer_create_cached(const moe_config* cfg, const moe_weights* w, 
   if (!cfg || !w) return MOE_ERR_INVALID_ARG;
   moe_status st = validate_config(cfg);
   if (st) return st;
-  const int need = (long)cfg->max_tokens * cfg->top_k < cfg->n_experts ? cfg->max_tokens * cfg->top_k : cfg->n_experts;
-  if (slots < need || slots > cfg->n_experts) return MOE_ERR_INVALID_ARG;
-  if (cfg->weight_format != MOE_W_INT4_G32 || cfg->shared_format != MOE_W_INT4_G32 ||
-      cfg->act_quant != MOE_ACT_NONE || !gemm_supported(cfg->hidden, cfg->inter) || cfg->n_experts + 1 > kMaxSlotTable)
-    return MOE_ERR_UNSUPPORTED;
+  if (slots < cached_min_slots(cfg) || slots > cfg->n_experts) return MOE_ERR_INVALID_ARG;
+  if ((st = cached_layer_support(cfg))) return st;
   moe_layer* L = new (std::nothrow) moe_layer();
   if (!L) return MOE_ERR_OOM;
   L->cfg = *cfg;
